@@ -1,0 +1,390 @@
+"""Pins of the CPU oracle to things other than itself (CPU only).
+
+Each test fixes some part of the oracle against what the pages print, a closed
+form, a library routine on a special case, finite differences, brute force
+with an independent implementation, or an invariant of softmax attention.
+"""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from synth import MaskProgram, make_alibi_slopes, make_doc_ids
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def P(*nodes):
+    return MaskProgram(tuple(nodes))
+
+
+CAUSAL = P(("causal",))
+DOC_CAUSAL = P(("causal",), ("same_doc",), ("and",))
+
+
+def _golden_tile_counts():
+    rows = []
+    with open(os.path.join(GOLDEN, "tile_counts_64k.txt")) as f:
+        for line in f:
+            line = line.split("#")[0].strip()
+            if not line:
+                continue
+            name, S, block, tiles = line.split()[:4]
+            rows.append((name, int(S), int(block), int(tiles)))
+    return rows
+
+
+def _golden_program(name, S):
+    if name == "causal":
+        return oracle.Program(CAUSAL)
+    if name == "causal_window1024":
+        return oracle.Program(P(("causal",), ("window", 1024), ("and",)))
+    if name == "causal_chunks1024":
+        return oracle.Program(DOC_CAUSAL, doc_row=(np.arange(S) // 1024).astype(np.int32))
+    raise KeyError(name)
+
+
+# ---------------------------------------------------------------- tile classes
+
+@pytest.mark.parametrize("row", _golden_tile_counts(), ids=lambda r: r[0])
+def test_page_tile_counts(row):
+    """Brute-force classifier reproduces the page's counts for a 64K sequence."""
+    name, S, block, tiles = row
+    cls = oracle.classify_tiles(_golden_program(name, S), S, S, block)
+    assert int((cls > 0).sum()) == tiles
+
+
+def test_page_ratios_consistent():
+    """57x (dense causal vs chunks) and about 2x (window vs chunks), Record #12."""
+    g = {r[0]: r[3] for r in _golden_tile_counts()}
+    assert round(g["causal"] / g["causal_chunks1024"]) == 57
+    assert abs(g["causal_window1024"] / g["causal_chunks1024"] - 2.0) < 0.05
+
+
+def _window_closed_form(n, W, B=128):
+    """Tile d = I - J of causal & (i - j < W) is non-empty iff 0 <= d <= (W + B - 2) // B,
+    full iff 1 <= d <= (W - B) // B (derived from i - j spanning [B d - B + 1, B d + B - 1])."""
+    dne = min((W + B - 2) // B, n - 1)
+    dfull = min((W - B) // B, n - 1) if W >= B else 0
+    nonempty = sum(n - d for d in range(0, dne + 1))
+    full = sum(n - d for d in range(1, dfull + 1))
+    return nonempty, full
+
+
+@pytest.mark.parametrize("W", [1, 64, 127, 128, 129, 255, 256, 640, 1024, 1792, 5000])
+def test_window_classes_closed_form(W):
+    S = 8192
+    cls = oracle.classify_tiles(oracle.Program(P(("causal",), ("window", W), ("and",))), S, S)
+    nonempty, full = _window_closed_form(S // 128, W)
+    assert int((cls > 0).sum()) == nonempty
+    assert int((cls == 2).sum()) == full
+
+
+def test_causal_classes_closed_form():
+    """Causal: the diagonal tiles are PARTIAL, the strictly lower ones FULL."""
+    S = 4096
+    n = S // 128
+    cls = oracle.classify_tiles(oracle.Program(CAUSAL), S, S)
+    expect = np.tril(np.full((n, n), 2, dtype=np.int8), -1) + np.eye(n, dtype=np.int8)
+    np.testing.assert_array_equal(cls, expect)
+
+
+def test_window_sinks_32k_sparsity():
+    """Tutorial Pattern 2: 32k context, 1k window + 4 sinks is about 97% block-sparse."""
+    S = 32768
+    prog = oracle.Program(P(("causal",), ("window", 1024), ("sink", 4), ("or",), ("and",)))
+    cls = oracle.classify_tiles(prog, S, S)
+    n = S // 128
+    nonempty = int((cls > 0).sum())
+    # closed form: the window band plus the first tile column below it
+    band, _ = _window_closed_form(n, 1024)
+    assert nonempty == band + (n - 9)
+    assert 0.95 < 1 - nonempty / (n * n) < 0.98
+
+
+def _random_program(rng, depth=3):
+    atoms = [("causal",), ("same_doc",), ("window", int(rng.integers(0, 400))),
+             ("sink", int(rng.integers(0, 200))), ("prefix",), ("true",)]
+    if depth == 0 or rng.random() < 0.3:
+        return [atoms[int(rng.integers(len(atoms)))]]
+    a = _random_program(rng, depth - 1)
+    b = _random_program(rng, depth - 1)
+    return a + b + [("and",) if rng.random() < 0.6 else ("or",)]
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_mask_and_classes_match_numpy_twin(seed):
+    """C element-wise evaluation vs numpy broadcasting on random and/or programs,
+    with ragged lengths and small blocks."""
+    rng = np.random.default_rng(seed)
+    nodes = _random_program(rng)
+    if len(nodes) > 16:
+        nodes = nodes[:1]
+    prog = MaskProgram(tuple(nodes))
+    prog.validate()
+    q_len, kv_len = int(rng.integers(1, 300)), int(rng.integers(1, 300))
+    docs = make_doc_ids(("geometric", 40.0), max(q_len, kv_len), seed)[0]
+    prefix = int(rng.integers(0, 150))
+    cp = oracle.Program(prog, doc_row=docs, prefix_len=prefix)
+    M_c = oracle.mask_dense(cp, q_len, kv_len)
+    M_np = oracle.np_mask(prog, q_len, kv_len, doc_row=docs, prefix_len=prefix)
+    np.testing.assert_array_equal(M_c, M_np)
+    for block in (16, 32, 64, 128):
+        np.testing.assert_array_equal(oracle.classify_tiles(cp, q_len, kv_len, block),
+                                      oracle.np_classify(M_np, block))
+
+
+def test_tile_lists_shape_and_order():
+    S = 1000  # ragged: 8 tiles, the last one 104 rows
+    docs = make_doc_ids(("geometric", 100.0), S, 7)[0]
+    cls = oracle.classify_tiles(oracle.Program(DOC_CAUSAL, doc_row=docs), S, S)
+    L = oracle.tile_lists(cls)
+    n = cls.shape[0]
+    for I in range(n):
+        p = L["kv_indices"][I, :L["kv_num_blocks"][I]]
+        f = L["full_kv_indices"][I, :L["full_kv_num_blocks"][I]]
+        assert list(p) == sorted(p) and list(f) == sorted(f)
+        assert set(p).isdisjoint(f)
+        assert set(p) | set(f) == set(np.nonzero(cls[I])[0])
+        assert not L["kv_indices"][I, L["kv_num_blocks"][I]:].any()
+    assert L["q_num_blocks"].sum() == L["kv_num_blocks"].sum()
+    assert L["full_q_num_blocks"].sum() == L["full_kv_num_blocks"].sum()
+
+
+# ---------------------------------------------------------------- forward
+
+def _qkv(S, D, seed, kv_len=None):
+    g = torch.Generator().manual_seed(seed)
+    kv_len = S if kv_len is None else kv_len
+    f = lambda n: torch.randn(n, D, generator=g).to(torch.bfloat16).double().numpy()
+    return f(S), f(kv_len), f(kv_len), f(S)
+
+
+def test_forward_matches_sdpa_causal():
+    """Causal mask without score_mod is textbook causal attention (torch SDPA, fp64)."""
+    S, D = 300, 64
+    q, k, v, _ = _qkv(S, D, 1)
+    out, lse = oracle.forward_head(q, k, v, oracle.Program(CAUSAL), ("none",), 0, 1 / np.sqrt(D))
+    tq, tk, tv = (torch.from_numpy(a)[None, None] for a in (q, k, v))
+    ref = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, is_causal=True)[0, 0].numpy()
+    np.testing.assert_allclose(out, ref, atol=1e-12, rtol=0)
+    s = (q @ k.T) / np.sqrt(D)
+    ref_lse = torch.logsumexp(torch.from_numpy(np.where(np.tril(np.ones((S, S), bool)), s, -np.inf)), 1)
+    np.testing.assert_allclose(lse, ref_lse.numpy(), atol=1e-12, rtol=0)
+
+
+def test_forward_matches_sdpa_doc_mask_and_alibi():
+    """Document mask + ALiBi as an additive bias is SDPA with a float mask."""
+    S, D, H = 257, 64, 4
+    q, k, v, _ = _qkv(S, D, 2)
+    docs = make_doc_ids(("geometric", 50.0), S, 3)[0]
+    slopes = make_alibi_slopes(H)
+    h = 2
+    prog = oracle.Program(DOC_CAUSAL, doc_row=docs)
+    out, lse = oracle.forward_head(q, k, v, prog, ("alibi", slopes), h, 1 / np.sqrt(D))
+    i = np.arange(S)[:, None]
+    j = np.arange(S)[None, :]
+    visible = (i >= j) & (docs[:, None] == docs[None, :])
+    bias = np.where(visible, -float(slopes[h]) * (i - j), -np.inf)
+    tq, tk, tv = (torch.from_numpy(a)[None, None] for a in (q, k, v))
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        tq, tk, tv, attn_mask=torch.from_numpy(bias)[None, None])[0, 0].numpy()
+    np.testing.assert_allclose(out, ref, atol=1e-12, rtol=0)
+
+
+def test_forward_q_zero_closed_form():
+    """q = 0: every visible logit is 0, so out_i is the mean of visible v_j and LSE_i = ln |V_i|."""
+    S, D = 333, 64
+    _, k, v, _ = _qkv(S, D, 4)
+    q = np.zeros((S, D))
+    docs = make_doc_ids(("geometric", 60.0), S, 5)[0]
+    prog = oracle.Program(P(("causal",), ("same_doc",), ("and",), ("window", 100), ("and",)), doc_row=docs)
+    out, lse = oracle.forward_head(q, k, v, prog, ("none",), 0, 0.125)
+    for i in range(S):
+        js = [j for j in range(max(0, i - 99), i + 1) if docs[j] == docs[i]]
+        np.testing.assert_allclose(out[i], v[js].mean(axis=0), atol=1e-12)
+        assert abs(lse[i] - np.log(len(js))) < 1e-12
+
+
+def test_forward_q_zero_alibi_geometric_weights():
+    """q = 0 with ALiBi: weights proportional to exp(-slope (i - j)), a geometric series."""
+    S, D = 200, 64
+    _, k, v, _ = _qkv(S, D, 6)
+    q = np.zeros((S, D))
+    slope = 0.25
+    out, lse = oracle.forward_head(q, k, v, oracle.Program(CAUSAL), ("alibi", [slope]), 0, 0.125)
+    for i in (0, 1, 17, 199):
+        r = np.exp(-slope)
+        w = r ** (i - np.arange(i + 1))           # j = 0..i
+        total = (1 - r ** (i + 1)) / (1 - r)       # geometric sum
+        np.testing.assert_allclose(out[i], (w[:, None] * v[:i + 1]).sum(0) / total, atol=1e-12)
+        assert abs(lse[i] - np.log(total)) < 1e-12
+
+
+def test_forward_v_ones_rows_sum_to_one():
+    S, D = 260, 128
+    q, k, _, _ = _qkv(S, D, 7)
+    v = np.ones((S, D))
+    out, _ = oracle.forward_head(q, k, v, oracle.Program(CAUSAL), ("softcap", 30.0), 0, 0.3)
+    np.testing.assert_allclose(out, 1.0, atol=1e-13)
+
+
+def test_forward_diagonal_window_one():
+    """causal & (i - j < 1) leaves only the diagonal: out_i = v_i, LSE_i = s_ii."""
+    S, D = 150, 64
+    q, k, v, _ = _qkv(S, D, 8)
+    prog = oracle.Program(P(("causal",), ("window", 1), ("and",)))
+    out, lse = oracle.forward_head(q, k, v, prog, ("none",), 0, 0.125)
+    np.testing.assert_allclose(out, v, atol=1e-14)
+    np.testing.assert_allclose(lse, 0.125 * (q * k).sum(1), atol=1e-12)
+
+
+def test_forward_fully_masked_rows():
+    """Rows that see nothing: out = 0, LSE = -inf (window 0 masks everything;
+    same_doc & sink(n) masks the rows of every document that starts after n)."""
+    S, D = 200, 64
+    q, k, v, do = _qkv(S, D, 9)
+    out, lse = oracle.forward_head(q, k, v, oracle.Program(P(("causal",), ("window", 0), ("and",))),
+                                   ("none",), 0, 0.125)
+    assert np.all(out == 0) and np.all(np.isneginf(lse))
+    docs = np.repeat(np.arange(4), 50).astype(np.int32)
+    prog = oracle.Program(P(("same_doc",), ("sink", 10), ("and",)), doc_row=docs)
+    out, lse = oracle.forward_head(q, k, v, prog, ("none",), 0, 0.125)
+    assert np.all(np.isfinite(lse[:50])) and np.all(np.isneginf(lse[50:]))
+    assert np.all(out[50:] == 0)
+    dq, dk, dv, _, _ = oracle.backward_head(q, k, v, do, prog, ("none",), 0, 0.125)
+    assert np.all(dq[50:] == 0) and np.all(dk[10:] == 0) and np.all(dv[10:] == 0)
+
+
+def test_softcap_small_logits_close_to_plain():
+    """c tanh(s / c) = s - s^3 / (3 c^2) + ...: tiny logits barely change."""
+    S, D = 128, 64
+    q, k, v, _ = _qkv(S, D, 10)
+    scale = 1e-3
+    prog = oracle.Program(CAUSAL)
+    o1, l1 = oracle.forward_head(q, k, v, prog, ("softcap", 30.0), 0, scale)
+    o0, l0 = oracle.forward_head(q, k, v, prog, ("none",), 0, scale)
+    smax = np.abs(scale * q @ k.T).max()
+    bound = smax ** 3 / (3 * 30.0 ** 2) * 2
+    assert np.abs(l1 - l0).max() <= bound
+    assert np.abs(o1 - o0).max() <= 4 * bound * np.abs(v).max()
+
+
+def test_softcap_saturates():
+    """Huge logits are capped to [-c, c], so LSE_i <= c + ln |V_i|."""
+    S, D = 128, 64
+    q, k, v, _ = _qkv(S, D, 11)
+    _, lse = oracle.forward_head(q, k, v, oracle.Program(CAUSAL), ("softcap", 30.0), 0, 1e4)
+    assert np.all(lse <= 30.0 + np.log(np.arange(1, S + 1)) + 1e-12)
+
+
+@pytest.mark.parametrize("score", ["none", "softcap", "alibi"])
+def test_forward_matches_numpy_twin(score):
+    S, D = 203, 64
+    q, k, v, _ = _qkv(S, D, 12, kv_len=190)
+    docs = make_doc_ids(("geometric", 30.0), S, 13)[0]
+    mask = P(("causal",), ("same_doc",), ("and",), ("window", 70), ("sink", 3), ("or",), ("and",))
+    sc = {"none": ("none",), "softcap": ("softcap", 5.0), "alibi": ("alibi", [0.125])}[score]
+    prog = oracle.Program(mask, doc_row=docs)
+    out, lse = oracle.forward_head(q, k, v, prog, sc, 0, 0.2)
+    M = oracle.np_mask(mask, S, 190, doc_row=docs)
+    ref, ref_lse, _ = oracle.np_forward(q, k, v, M, sc if score != "alibi" else ("alibi",), 0.125, 0.2)
+    np.testing.assert_allclose(out, ref, atol=1e-12)
+    np.testing.assert_array_equal(np.isneginf(lse), np.isneginf(ref_lse))
+    f = np.isfinite(lse)
+    np.testing.assert_allclose(lse[f], ref_lse[f], atol=1e-12)
+
+
+def test_forward_row_subset_matches_full():
+    S, D = 300, 64
+    q, k, v, _ = _qkv(S, D, 14)
+    prog = oracle.Program(CAUSAL)
+    out, lse = oracle.forward_head(q, k, v, prog, ("none",), 0, 0.125)
+    rows = [0, 5, 299, 128]
+    o2, l2 = oracle.forward_head(q, k, v, prog, ("none",), 0, 0.125, rows=rows)
+    np.testing.assert_array_equal(o2, out[rows])
+    np.testing.assert_array_equal(l2, lse[rows])
+
+
+# ---------------------------------------------------------------- backward
+
+def test_backward_matches_sdpa_autograd():
+    """Causal, no score_mod: gradients of torch SDPA (fp64 autograd)."""
+    S, D = 200, 64
+    q, k, v, do = _qkv(S, D, 15)
+    dq, dk, dv, _, _ = oracle.backward_head(q, k, v, do, oracle.Program(CAUSAL), ("none",), 0, 1 / np.sqrt(D))
+    tq, tk, tv = (torch.from_numpy(a)[None, None].requires_grad_() for a in (q, k, v))
+    o = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, is_causal=True)
+    o.backward(torch.from_numpy(do)[None, None])
+    np.testing.assert_allclose(dq, tq.grad[0, 0].numpy(), atol=1e-11)
+    np.testing.assert_allclose(dk, tk.grad[0, 0].numpy(), atol=1e-11)
+    np.testing.assert_allclose(dv, tv.grad[0, 0].numpy(), atol=1e-11)
+
+
+@pytest.mark.parametrize("score", ["none", "softcap", "alibi"])
+def test_backward_finite_differences(score):
+    """Central differences of L = sum(out * dO) through the oracle forward."""
+    S, D = 40, 16
+    q, k, v, do = _qkv(S, D, 16)
+    docs = make_doc_ids(("geometric", 12.0), S, 17)[0]
+    mask = P(("causal",), ("same_doc",), ("and",), ("sink", 2), ("or",))
+    prog = oracle.Program(mask, doc_row=docs)
+    sc = {"none": ("none",), "softcap": ("softcap", 1.5), "alibi": ("alibi", [0.3])}[score]
+    scale = 0.7
+    dq, dk, dv, _, _ = oracle.backward_head(q, k, v, do, prog, sc, 0, scale)
+
+    def loss(qq, kk, vv):
+        o, _ = oracle.forward_head(qq, kk, vv, prog, sc, 0, scale)
+        return float((o * do).sum())
+
+    eps = 1e-6
+    rng = np.random.default_rng(0)
+    for name, g, arr in (("q", dq, q), ("k", dk, k), ("v", dv, v)):
+        for _ in range(12):
+            r, c = int(rng.integers(S)), int(rng.integers(D))
+            args = {"q": q, "k": k, "v": v}
+            plus = {n: a.copy() for n, a in args.items()}
+            minus = {n: a.copy() for n, a in args.items()}
+            plus[name][r, c] += eps
+            minus[name][r, c] -= eps
+            num = (loss(plus["q"], plus["k"], plus["v"]) - loss(minus["q"], minus["k"], minus["v"])) / (2 * eps)
+            assert abs(num - g[r, c]) < 1e-7 * max(1.0, abs(num)), (name, r, c, num, g[r, c])
+
+
+@pytest.mark.parametrize("score", ["none", "softcap", "alibi"])
+def test_backward_matches_numpy_twin(score):
+    S, D = 150, 32
+    q, k, v, do = _qkv(S, D, 18, kv_len=170)
+    docs = make_doc_ids(("geometric", 30.0), 170, 19)[0]
+    mask = P(("causal",), ("same_doc",), ("and",), ("window", 50), ("and",))
+    sc = {"none": ("none",), "softcap": ("softcap", 4.0), "alibi": ("alibi", [0.0625])}[score]
+    prog = oracle.Program(mask, doc_row=docs)
+    dq, dk, dv, _, _ = oracle.backward_head(q, k, v, do, prog, sc, 0, 0.3)
+    M = oracle.np_mask(mask, S, 170, doc_row=docs)
+    ref = oracle.np_backward(q, k, v, do, M, sc if score != "alibi" else ("alibi",), 0.0625, 0.3)
+    for a, b in zip((dq, dk, dv), ref):
+        np.testing.assert_allclose(a, b, atol=1e-11)
+
+
+def test_backward_diagonal_only():
+    """Only the diagonal visible: P = 1, so dv = dO and dq = dk = 0."""
+    S, D = 100, 64
+    q, k, v, do = _qkv(S, D, 20)
+    prog = oracle.Program(P(("causal",), ("window", 1), ("and",)))
+    dq, dk, dv, _, _ = oracle.backward_head(q, k, v, do, prog, ("none",), 0, 0.125)
+    np.testing.assert_allclose(dv, do, atol=1e-14)
+    assert np.abs(dq).max() < 1e-14 and np.abs(dk).max() < 1e-14
+
+
+def test_backward_subsets_match_full():
+    S, D = 180, 64
+    q, k, v, do = _qkv(S, D, 21)
+    prog = oracle.Program(CAUSAL)
+    dq, dk, dv, _, _ = oracle.backward_head(q, k, v, do, prog, ("softcap", 3.0), 0, 0.2)
+    rows, cols = [3, 179, 64], [0, 100, 177]
+    dq2, dk2, dv2, _, _ = oracle.backward_head(q, k, v, do, prog, ("softcap", 3.0), 0, 0.2, rows=rows, cols=cols)
+    np.testing.assert_array_equal(dq2, dq[rows])
+    np.testing.assert_array_equal(dk2, dk[cols])
+    np.testing.assert_array_equal(dv2, dv[cols])
