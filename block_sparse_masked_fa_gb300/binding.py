@@ -1,0 +1,282 @@
+"""ctypes binding of the C ABI in include/fa.h (argument marshalling only).
+
+Names mirror the C entry points: fa_block_mask_bytes, fa_create_block_mask,
+fa_forward, fa_backward_workspace_bytes, fa_backward, fa_get_status,
+fa_block_mask_summary, fa_status_string.  Tensors are torch CUDA tensors; the
+binding passes their device pointers and the current CUDA stream.  Every step
+of the computation runs in the library's kernels; importing this module fails
+loudly when the library has not been built.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libfa_gb300.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(
+        f"{LIB_PATH} is missing: build the CUDA library first "
+        "(python -c 'import __graft_entry__ as g; g.build()')")
+
+_lib = ctypes.CDLL(LIB_PATH)
+
+MAX_NODES = 16
+MASK_OPS = {"true": 0, "causal": 1, "same_doc": 2, "window": 3, "sink": 4, "prefix": 5, "and": 6, "or": 7}
+SCORE_OPS = {"none": 0, "softcap": 1, "alibi": 2}
+STATUS = {0: "FA_OK", 1: "FA_ERR_INVALID_ARG", 2: "FA_ERR_UNSUPPORTED", 3: "FA_ERR_SHAPE",
+          4: "FA_ERR_ALIGNMENT", 5: "FA_ERR_CUDA", 6: "FA_ERR_TIMEOUT", 7: "FA_ERR_DEVICE_CHECK",
+          8: "FA_ERR_WORKSPACE"}
+
+
+class FaError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        super().__init__(f"{where}: {STATUS.get(code, code)} ({_lib.fa_status_string(code).decode()})")
+        self.code = code
+
+
+class MaskNode(ctypes.Structure):
+    _fields_ = [("op", ctypes.c_int32), ("param", ctypes.c_void_p)]
+
+
+class MaskSpec(ctypes.Structure):
+    _fields_ = [("n", ctypes.c_int32), ("doc_len", ctypes.c_int64), ("node", MaskNode * MAX_NODES)]
+
+
+class ScoreSpec(ctypes.Structure):
+    _fields_ = [("op", ctypes.c_int32), ("param", ctypes.c_void_p)]
+
+
+class BlockMaskStruct(ctypes.Structure):
+    _fields_ = [("Bm", ctypes.c_int32), ("Hm", ctypes.c_int32), ("block", ctypes.c_int32),
+                ("nq", ctypes.c_int32), ("nkv", ctypes.c_int32),
+                ("q_len", ctypes.c_int64), ("kv_len", ctypes.c_int64)] + \
+               [(name, ctypes.c_void_p) for name in (
+                   "kv_num_blocks", "kv_indices", "full_kv_num_blocks", "full_kv_indices",
+                   "q_num_blocks", "q_indices", "full_q_num_blocks", "full_q_indices",
+                   "row_order", "col_order", "tile_class", "tile_summary", "status")] + \
+               [("spec", MaskSpec)]
+
+
+_c = ctypes
+_lib.fa_block_mask_bytes.argtypes = [_c.c_int32, _c.c_int32, _c.c_int64, _c.c_int64, _c.c_int32,
+                                     _c.POINTER(_c.c_size_t)]
+_lib.fa_create_block_mask.argtypes = [_c.POINTER(MaskSpec), _c.c_int32, _c.c_int32, _c.c_int64, _c.c_int64,
+                                      _c.c_int32, _c.c_void_p, _c.c_size_t, _c.POINTER(BlockMaskStruct),
+                                      _c.c_void_p]
+_lib.fa_forward.argtypes = [_c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_int32, _c.c_int32, _c.c_int64,
+                            _c.c_int64, _c.c_int32, _c.POINTER(BlockMaskStruct), _c.POINTER(ScoreSpec),
+                            _c.c_float, _c.c_void_p, _c.c_void_p, _c.c_void_p]
+_lib.fa_backward_workspace_bytes.argtypes = [_c.c_int32, _c.c_int32, _c.c_int64, _c.c_int32,
+                                             _c.POINTER(_c.c_size_t)]
+_lib.fa_backward.argtypes = [_c.c_void_p] * 6 + [_c.c_int32, _c.c_int32, _c.c_int64, _c.c_int64, _c.c_int32,
+                                                 _c.POINTER(BlockMaskStruct), _c.POINTER(ScoreSpec), _c.c_float,
+                                                 _c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_void_p,
+                                                 _c.c_size_t, _c.c_void_p]
+_lib.fa_get_status.argtypes = [_c.POINTER(BlockMaskStruct), _c.c_int32, _c.c_void_p]
+_lib.fa_block_mask_summary.argtypes = [_c.POINTER(BlockMaskStruct), _c.POINTER(_c.c_int64 * 3), _c.c_void_p]
+_lib.fa_status_string.argtypes = [_c.c_int]
+_lib.fa_status_string.restype = _c.c_char_p
+for _f in (_lib.fa_block_mask_bytes, _lib.fa_create_block_mask, _lib.fa_forward, _lib.fa_backward_workspace_bytes,
+           _lib.fa_backward, _lib.fa_get_status, _lib.fa_block_mask_summary):
+    _f.restype = _c.c_int
+_lib.fa_version.restype = _c.c_int32
+
+EXPORTED = ("fa_block_mask_bytes", "fa_create_block_mask", "fa_forward", "fa_backward_workspace_bytes",
+            "fa_backward", "fa_get_status", "fa_block_mask_summary", "fa_status_string", "fa_version")
+
+
+def _check(code: int, where: str):
+    if code != 0:
+        raise FaError(code, where)
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _dev_int32(x, device) -> torch.Tensor:
+    if isinstance(x, torch.Tensor):
+        if x.dtype != torch.int32 or not x.is_cuda:
+            raise TypeError("mask parameters must be int32 CUDA tensors")
+        return x.contiguous()
+    return torch.as_tensor(x, dtype=torch.int32, device=device).reshape(-1)
+
+
+def make_mask_spec(nodes: Sequence[tuple], device=None):
+    """Device-side mask spec from a postfix node list.
+
+    Nodes: ("causal",), ("true",), ("same_doc", doc_ids [Bm, doc_len] int32),
+    ("window", W), ("sink", n), ("prefix", prefix_len [Bm]), ("and",), ("or",).
+    Scalars given as Python ints are copied into fresh device int32 tensors;
+    pass an int32 CUDA tensor to change a parameter later without a new spec.
+    Returns (MaskSpec, keepalive list of tensors).
+    """
+    device = device or torch.device("cuda", torch.cuda.current_device())
+    if not 1 <= len(nodes) <= MAX_NODES:
+        raise ValueError("a mask program has 1..16 nodes")
+    spec = MaskSpec()
+    spec.n = len(nodes)
+    keep = []
+    doc_len = 0
+    for k, node in enumerate(nodes):
+        kind = node[0]
+        spec.node[k].op = MASK_OPS[kind]
+        spec.node[k].param = None
+        if kind in ("same_doc", "window", "sink", "prefix"):
+            t = _dev_int32(node[1], device)
+            keep.append(t)
+            spec.node[k].param = t.data_ptr()
+            if kind == "same_doc":
+                doc_len = int(t.shape[-1])
+    spec.doc_len = doc_len
+    return spec, keep
+
+
+def make_score_spec(kind: str = "none", param=None, device=None):
+    """("none"), ("softcap", c), ("alibi", slopes[H]); param becomes a device fp32 tensor."""
+    device = device or torch.device("cuda", torch.cuda.current_device())
+    s = ScoreSpec()
+    s.op = SCORE_OPS[kind]
+    s.param = None
+    keep = []
+    if kind != "none":
+        t = param if isinstance(param, torch.Tensor) else torch.as_tensor(param, dtype=torch.float32)
+        t = t.to(device=device, dtype=torch.float32).reshape(-1).contiguous()
+        keep.append(t)
+        s.param = t.data_ptr()
+    return s, keep
+
+
+class BlockMask:
+    """A built block mask: the caller-owned device buffer plus the C descriptor."""
+
+    def __init__(self, struct: BlockMaskStruct, buffer: torch.Tensor, keep: list):
+        self.struct = struct
+        self.buffer = buffer
+        self._keep = keep
+
+    def _view(self, field: str, shape, dtype=torch.int32) -> torch.Tensor:
+        off = getattr(self.struct, field) - self.buffer.data_ptr()
+        n = 1
+        for s in shape:
+            n *= s
+        nbytes = n * torch.empty(0, dtype=dtype).element_size()
+        return self.buffer[off:off + nbytes].view(dtype).view(*shape)
+
+    def lists(self) -> dict:
+        s = self.struct
+        r, c = (s.Bm, s.Hm, s.nq), (s.Bm, s.Hm, s.nkv)
+        return {
+            "kv_num_blocks": self._view("kv_num_blocks", r),
+            "kv_indices": self._view("kv_indices", r + (s.nkv,)),
+            "full_kv_num_blocks": self._view("full_kv_num_blocks", r),
+            "full_kv_indices": self._view("full_kv_indices", r + (s.nkv,)),
+            "q_num_blocks": self._view("q_num_blocks", c),
+            "q_indices": self._view("q_indices", c + (s.nq,)),
+            "full_q_num_blocks": self._view("full_q_num_blocks", c),
+            "full_q_indices": self._view("full_q_indices", c + (s.nq,)),
+        }
+
+    def tile_class(self) -> torch.Tensor:
+        s = self.struct
+        return self._view("tile_class", (s.Bm, s.Hm, s.nq, s.nkv), torch.uint8)
+
+    def row_order(self) -> torch.Tensor:
+        s = self.struct
+        return self._view("row_order", (s.Bm * s.Hm * s.nq,))
+
+
+def fa_block_mask_bytes(Bm: int, Hm: int, q_len: int, kv_len: int, block: int = 128) -> int:
+    n = ctypes.c_size_t()
+    _check(_lib.fa_block_mask_bytes(Bm, Hm, q_len, kv_len, block, ctypes.byref(n)), "fa_block_mask_bytes")
+    return n.value
+
+
+def fa_create_block_mask(nodes: Sequence[tuple], Bm: int, Hm: int, q_len: int, kv_len: int, block: int = 128,
+                         buffer: Optional[torch.Tensor] = None, stream=None) -> BlockMask:
+    """Builds the block mask of a postfix mask program (see make_mask_spec)."""
+    spec, keep = nodes if isinstance(nodes, tuple) and isinstance(nodes[0], MaskSpec) else make_mask_spec(nodes)
+    nbytes = fa_block_mask_bytes(Bm, Hm, q_len, kv_len, block)
+    if buffer is None:
+        buffer = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    st = BlockMaskStruct()
+    _check(_lib.fa_create_block_mask(ctypes.byref(spec), Bm, Hm, q_len, kv_len, block, buffer.data_ptr(),
+                                     buffer.numel(), ctypes.byref(st), _stream(stream)), "fa_create_block_mask")
+    return BlockMask(st, buffer, keep + [spec])
+
+
+def _score(score):
+    if score is None:
+        return make_score_spec("none")
+    if isinstance(score, tuple) and isinstance(score[0], ScoreSpec):
+        return score
+    if isinstance(score, str):
+        return make_score_spec(score)
+    return make_score_spec(score[0], score[1] if len(score) > 1 else None)
+
+
+def fa_forward(q, k, v, block_mask: BlockMask, score=None, scale: float = 0.0, out=None, lse=None, stream=None):
+    """out [B,H,q_len,D] bf16 and lse [B,H,q_len] fp32."""
+    B, H, q_len, D = q.shape
+    kv_len = k.shape[2]
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty(B, H, q_len, dtype=torch.float32, device=q.device)
+    sspec, keep = _score(score)
+    _check(_lib.fa_forward(_ptr(q), _ptr(k), _ptr(v), B, H, q_len, kv_len, D, ctypes.byref(block_mask.struct),
+                           ctypes.byref(sspec), float(scale), _ptr(out), _ptr(lse), _stream(stream)), "fa_forward")
+    return out, lse
+
+
+def fa_backward_workspace_bytes(B: int, H: int, q_len: int, D: int) -> int:
+    n = ctypes.c_size_t()
+    _check(_lib.fa_backward_workspace_bytes(B, H, q_len, D, ctypes.byref(n)), "fa_backward_workspace_bytes")
+    return n.value
+
+
+def fa_backward(q, k, v, out, lse, dout, block_mask: BlockMask, score=None, scale: float = 0.0,
+                dq=None, dk=None, dv=None, workspace=None, stream=None):
+    """dq, dk, dv (bf16, shaped like q, k, v)."""
+    B, H, q_len, D = q.shape
+    kv_len = k.shape[2]
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    if workspace is None:
+        workspace = torch.empty(fa_backward_workspace_bytes(B, H, q_len, D), dtype=torch.uint8, device=q.device)
+    sspec, keep = _score(score)
+    _check(_lib.fa_backward(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout), B, H, q_len, kv_len, D,
+                            ctypes.byref(block_mask.struct), ctypes.byref(sspec), float(scale), _ptr(dq), _ptr(dk),
+                            _ptr(dv), _ptr(workspace), workspace.numel(), _stream(stream)), "fa_backward")
+    return dq, dk, dv
+
+
+def fa_get_status(block_mask: BlockMask, clear: bool = True, stream=None) -> int:
+    return _lib.fa_get_status(ctypes.byref(block_mask.struct), 1 if clear else 0, _stream(stream))
+
+
+def fa_block_mask_summary(block_mask: BlockMask, stream=None):
+    counts = (ctypes.c_int64 * 3)()
+    _check(_lib.fa_block_mask_summary(ctypes.byref(block_mask.struct), ctypes.byref(counts), _stream(stream)),
+           "fa_block_mask_summary")
+    return tuple(int(c) for c in counts)
+
+
+def fa_status_string(code: int) -> str:
+    return _lib.fa_status_string(code).decode()
+
+
+def fa_version() -> int:
+    return int(_lib.fa_version())

@@ -1,0 +1,377 @@
+// api.cu -- the C ABI declared in include/fa.h: host-side validation, the
+// block-mask buffer layout, tensor-map encoding and kernel launches.
+// Everything here runs on the host; it never synchronises a stream except in
+// fa_get_status and fa_block_mask_summary.
+#include <cmath>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include <cudaTypedefs.h>
+
+#include "internal.h"
+
+namespace fa {
+namespace {
+
+constexpr size_t kAlign = 256;
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+// Byte offsets of the block-mask arrays inside the caller's buffer.
+struct Layout {
+  enum {
+    KV_NUM, KV_IDX, FULL_NUM, FULL_IDX, Q_NUM, Q_IDX, FULL_Q_NUM, FULL_Q_IDX, ROW_ORDER, COL_ORDER, TILE_CLASS,
+    SUMMARY, STATUS, N
+  };
+  size_t off[N];
+  size_t total;
+  int64_t nq, nkv;
+};
+
+fa_status make_layout(int32_t Bm, int32_t Hm, int64_t q_len, int64_t kv_len, int32_t block, Layout* L) {
+  if (Bm < 1 || Hm < 1 || q_len < 1 || kv_len < 1) return FA_ERR_SHAPE;
+  if (block < 16 || block > 128 || (block & (block - 1)) != 0) return FA_ERR_UNSUPPORTED;
+  if (q_len > (int64_t)INT32_MAX - 256 || kv_len > (int64_t)INT32_MAX - 256) return FA_ERR_SHAPE;
+  const int64_t nq = (q_len + block - 1) / block, nkv = (kv_len + block - 1) / block;
+  const int64_t rows = (int64_t)Bm * Hm * nq, cols = (int64_t)Bm * Hm * nkv;
+  const int64_t tiles = rows * nkv;
+  if (tiles > (int64_t)INT32_MAX || rows > (int64_t)INT32_MAX / 2 || cols > (int64_t)INT32_MAX / 2)
+    return FA_ERR_SHAPE;
+  const size_t sizes[Layout::N] = {
+      (size_t)rows * 4,  (size_t)tiles * 4, (size_t)rows * 4, (size_t)tiles * 4,
+      (size_t)cols * 4,  (size_t)tiles * 4, (size_t)cols * 4, (size_t)tiles * 4,
+      (size_t)rows * 4,  (size_t)cols * 4,  (size_t)tiles,
+      (size_t)Bm * 2 * (size_t)(nq > nkv ? nq : nkv) * 2 * 4,
+      4};
+  size_t at = 0;
+  for (int k = 0; k < Layout::N; ++k) {
+    L->off[k] = at;
+    at += align_up(sizes[k]);
+  }
+  L->total = at;
+  L->nq = nq;
+  L->nkv = nkv;
+  return FA_OK;
+}
+
+// Checks a mask program and fills its device copy.
+fa_status check_mask(const fa_mask_spec* spec, int64_t q_len, int64_t kv_len, DevMask* dm) {
+  if (spec == nullptr) return FA_ERR_INVALID_ARG;
+  if (spec->n < 1 || spec->n > FA_MAX_MASK_NODES) return FA_ERR_INVALID_ARG;
+  std::memset(dm, 0, sizeof(*dm));
+  dm->n = spec->n;
+  int depth = 0;
+  const int32_t* doc = nullptr;
+  for (int k = 0; k < spec->n; ++k) {
+    const int op = spec->node[k].op;
+    const int32_t* prm = spec->node[k].param;
+    switch (op) {
+      case FA_M_TRUE:
+      case FA_M_CAUSAL:
+        depth += 1;
+        break;
+      case FA_M_WINDOW:
+      case FA_M_SINK:
+      case FA_M_PREFIX:
+        if (prm == nullptr || !aligned4(prm)) return FA_ERR_INVALID_ARG;
+        depth += 1;
+        break;
+      case FA_M_SAME_DOC:
+        if (prm == nullptr || !aligned4(prm)) return FA_ERR_INVALID_ARG;
+        if (doc != nullptr && doc != prm) return FA_ERR_INVALID_ARG;  // one doc array per program
+        doc = prm;
+        depth += 1;
+        break;
+      case FA_M_AND:
+      case FA_M_OR:
+        if (depth < 2) return FA_ERR_INVALID_ARG;
+        depth -= 1;
+        break;
+      default:
+        return FA_ERR_INVALID_ARG;
+    }
+    if (depth > FA_MAX_MASK_STACK) return FA_ERR_INVALID_ARG;
+    dm->op[k] = op;
+    dm->param[k] = prm;
+  }
+  if (depth != 1) return FA_ERR_INVALID_ARG;
+  if (doc != nullptr) {
+    const int64_t need = q_len > kv_len ? q_len : kv_len;
+    if (spec->doc_len < need) return FA_ERR_SHAPE;
+    dm->has_doc = 1;
+    dm->doc = doc;
+    dm->doc_len = spec->doc_len;
+    dm->doc_vec_ok = aligned16(doc) && (spec->doc_len % 4 == 0);
+  }
+  return FA_OK;
+}
+
+// ---- driver entry point for tensor-map encoding (the library does not link libcuda)
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+void load_encode() {
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+          cudaSuccess &&
+      q == cudaDriverEntryPointSuccess)
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+}
+
+fa_status cuda_status(cudaError_t e) { return e == cudaSuccess ? FA_OK : FA_ERR_CUDA; }
+
+// Shared shape checks of fa_forward / fa_backward.
+fa_status check_attn(int32_t B, int32_t H, int64_t q_len, int64_t kv_len, int32_t D, const fa_block_mask* bm,
+                     const fa_score_spec* score, float* scale) {
+  if (bm == nullptr) return FA_ERR_INVALID_ARG;
+  if (B < 1 || H < 1 || q_len < 1 || kv_len < 1) return FA_ERR_SHAPE;
+  if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
+  if (bm->block != 128) return FA_ERR_UNSUPPORTED;
+  if (bm->q_len != q_len || bm->kv_len != kv_len) return FA_ERR_SHAPE;
+  if (!(bm->Bm == 1 || bm->Bm == B) || !(bm->Hm == 1 || bm->Hm == H)) return FA_ERR_SHAPE;
+  if ((int64_t)B * H * ((q_len + 127) / 128) > (int64_t)INT32_MAX) return FA_ERR_SHAPE;
+  if ((int64_t)B * H * ((kv_len + 127) / 128) > (int64_t)INT32_MAX) return FA_ERR_SHAPE;
+  if (bm->status == nullptr || bm->row_order == nullptr) return FA_ERR_INVALID_ARG;
+  if (score != nullptr) {
+    if (score->op < FA_S_NONE || score->op > FA_S_ALIBI) return FA_ERR_INVALID_ARG;
+    if (score->op != FA_S_NONE && (score->param == nullptr || !aligned4(score->param))) return FA_ERR_INVALID_ARG;
+  }
+  if (!(*scale >= 0.f) || std::isinf(*scale)) return FA_ERR_INVALID_ARG;
+  if (*scale == 0.f) *scale = 1.0f / std::sqrt((float)D);
+  return FA_OK;
+}
+
+AttnArgs attn_args(int32_t B, int32_t H, int64_t q_len, int64_t kv_len, int32_t D, const fa_block_mask* bm,
+                   const fa_score_spec* score, float scale, DevMask dm) {
+  AttnArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.B = B;
+  a.H = H;
+  a.Bm = bm->Bm;
+  a.Hm = bm->Hm;
+  a.nq = bm->nq;
+  a.nkv = bm->nkv;
+  a.D = D;
+  a.q_len = (int32_t)q_len;
+  a.kv_len = (int32_t)kv_len;
+  a.kv_num = bm->kv_num_blocks;
+  a.kv_idx = bm->kv_indices;
+  a.full_num = bm->full_kv_num_blocks;
+  a.full_idx = bm->full_kv_indices;
+  a.q_num = bm->q_num_blocks;
+  a.q_idx = bm->q_indices;
+  a.full_q_num = bm->full_q_num_blocks;
+  a.full_q_idx = bm->full_q_indices;
+  a.row_order = bm->row_order;
+  a.col_order = bm->col_order;
+  a.scale = scale;
+  a.score_op = score ? score->op : FA_S_NONE;
+  a.score_param = score ? score->param : nullptr;
+  a.status = bm->status;
+  a.mask = dm;
+  return a;
+}
+
+}  // namespace
+
+bool encode_tmap_3d(CUtensorMap* map, CUtensorMapDataType dtype, int elem_bytes, const void* base, uint64_t d0,
+                    uint64_t d1, uint64_t d2, uint32_t box0, uint32_t box1, CUtensorMapSwizzle swizzle) {
+  std::call_once(g_encode_once, load_encode);
+  if (g_encode == nullptr) return false;
+  const cuuint64_t dims[3] = {d0, d1, d2};
+  const cuuint64_t strides[2] = {d0 * elem_bytes, d0 * d1 * elem_bytes};
+  const cuuint32_t box[3] = {box0, box1, 1};
+  const cuuint32_t es[3] = {1, 1, 1};
+  return g_encode(map, dtype, 3, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace fa
+
+using namespace fa;
+
+extern "C" {
+
+int32_t fa_version(void) { return 100; }
+
+const char* fa_status_string(fa_status s) {
+  switch (s) {
+    case FA_OK: return "ok";
+    case FA_ERR_INVALID_ARG: return "invalid argument";
+    case FA_ERR_UNSUPPORTED: return "unsupported configuration";
+    case FA_ERR_SHAPE: return "bad or inconsistent shape";
+    case FA_ERR_ALIGNMENT: return "pointer not 16-byte aligned";
+    case FA_ERR_CUDA: return "CUDA call failed";
+    case FA_ERR_TIMEOUT: return "device wait timed out";
+    case FA_ERR_DEVICE_CHECK: return "device range check failed";
+    case FA_ERR_WORKSPACE: return "buffer too small";
+  }
+  return "unknown status";
+}
+
+fa_status fa_block_mask_bytes(int32_t Bm, int32_t Hm, int64_t q_len, int64_t kv_len, int32_t block, size_t* bytes) {
+  if (bytes == nullptr) return FA_ERR_INVALID_ARG;
+  Layout L;
+  const fa_status st = make_layout(Bm, Hm, q_len, kv_len, block, &L);
+  if (st != FA_OK) return st;
+  *bytes = L.total;
+  return FA_OK;
+}
+
+fa_status fa_create_block_mask(const fa_mask_spec* spec, int32_t Bm, int32_t Hm, int64_t q_len, int64_t kv_len,
+                               int32_t block, void* buffer, size_t buffer_bytes, fa_block_mask* bm,
+                               cudaStream_t stream) {
+  if (bm == nullptr || buffer == nullptr) return FA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(buffer) & (kAlign - 1)) != 0) return FA_ERR_ALIGNMENT;
+  Layout L;
+  fa_status st = make_layout(Bm, Hm, q_len, kv_len, block, &L);
+  if (st != FA_OK) return st;
+  if (buffer_bytes < L.total) return FA_ERR_WORKSPACE;
+  DevMask dm;
+  st = check_mask(spec, q_len, kv_len, &dm);
+  if (st != FA_OK) return st;
+
+  uint8_t* base = static_cast<uint8_t*>(buffer);
+  auto i32 = [&](int k) { return reinterpret_cast<int32_t*>(base + L.off[k]); };
+  std::memset(bm, 0, sizeof(*bm));
+  bm->Bm = Bm;
+  bm->Hm = Hm;
+  bm->block = block;
+  bm->nq = (int32_t)L.nq;
+  bm->nkv = (int32_t)L.nkv;
+  bm->q_len = q_len;
+  bm->kv_len = kv_len;
+  bm->kv_num_blocks = i32(Layout::KV_NUM);
+  bm->kv_indices = i32(Layout::KV_IDX);
+  bm->full_kv_num_blocks = i32(Layout::FULL_NUM);
+  bm->full_kv_indices = i32(Layout::FULL_IDX);
+  bm->q_num_blocks = i32(Layout::Q_NUM);
+  bm->q_indices = i32(Layout::Q_IDX);
+  bm->full_q_num_blocks = i32(Layout::FULL_Q_NUM);
+  bm->full_q_indices = i32(Layout::FULL_Q_IDX);
+  bm->row_order = i32(Layout::ROW_ORDER);
+  bm->col_order = i32(Layout::COL_ORDER);
+  bm->tile_class = base + L.off[Layout::TILE_CLASS];
+  bm->tile_summary = i32(Layout::SUMMARY);
+  bm->status = reinterpret_cast<uint32_t*>(base + L.off[Layout::STATUS]);
+  bm->spec = *spec;
+
+  cudaError_t e = cudaMemsetAsync(bm->status, 0, 4, stream);
+  if (e != cudaSuccess) return FA_ERR_CUDA;
+  BuildArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.mask = dm;
+  a.Bm = Bm;
+  a.Hm = Hm;
+  a.block = block;
+  a.nq = bm->nq;
+  a.nkv = bm->nkv;
+  a.q_len = q_len;
+  a.kv_len = kv_len;
+  a.kv_num = bm->kv_num_blocks;
+  a.kv_idx = bm->kv_indices;
+  a.full_num = bm->full_kv_num_blocks;
+  a.full_idx = bm->full_kv_indices;
+  a.q_num = bm->q_num_blocks;
+  a.q_idx = bm->q_indices;
+  a.full_q_num = bm->full_q_num_blocks;
+  a.full_q_idx = bm->full_q_indices;
+  a.row_order = bm->row_order;
+  a.col_order = bm->col_order;
+  a.tile_class = bm->tile_class;
+  a.summary = bm->tile_summary;
+  a.status = bm->status;
+  return cuda_status(launch_build(a, stream));
+}
+
+fa_status fa_forward(const void* q, const void* k, const void* v, int32_t B, int32_t H, int64_t q_len,
+                     int64_t kv_len, int32_t D, const fa_block_mask* bm, const fa_score_spec* score, float scale,
+                     void* out, float* lse, cudaStream_t stream) {
+  if (!q || !k || !v || !out || !lse) return FA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned4(lse)) return FA_ERR_ALIGNMENT;
+  fa_status st = check_attn(B, H, q_len, kv_len, D, bm, score, &scale);
+  if (st != FA_OK) return st;
+  DevMask dm;
+  st = check_mask(&bm->spec, q_len, kv_len, &dm);
+  if (st != FA_OK) return st;
+  const AttnArgs a = attn_args(B, H, q_len, kv_len, D, bm, score, scale, dm);
+  FwdTensors t{q, k, v, out, lse};
+  bool enc_failed = false;
+  const cudaError_t e = launch_forward(a, t, stream, &enc_failed);
+  if (enc_failed) return FA_ERR_CUDA;
+  return cuda_status(e);
+}
+
+fa_status fa_backward_workspace_bytes(int32_t B, int32_t H, int64_t q_len, int32_t D, size_t* bytes) {
+  if (bytes == nullptr) return FA_ERR_INVALID_ARG;
+  if (B < 1 || H < 1 || q_len < 1) return FA_ERR_SHAPE;
+  if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
+  const size_t rows = (size_t)B * H * (size_t)q_len;
+  *bytes = align_up(rows * D * 4) + align_up(rows * 4);
+  return FA_OK;
+}
+
+fa_status fa_backward(const void* q, const void* k, const void* v, const void* out, const float* lse,
+                      const void* dout, int32_t B, int32_t H, int64_t q_len, int64_t kv_len, int32_t D,
+                      const fa_block_mask* bm, const fa_score_spec* score, float scale, void* dq, void* dk,
+                      void* dv, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  if (!q || !k || !v || !out || !lse || !dout || !dq || !dk || !dv || !workspace) return FA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(dout) || !aligned16(dq) ||
+      !aligned16(dk) || !aligned16(dv) || !aligned16(workspace) || !aligned4(lse))
+    return FA_ERR_ALIGNMENT;
+  fa_status st = check_attn(B, H, q_len, kv_len, D, bm, score, &scale);
+  if (st != FA_OK) return st;
+  size_t need = 0;
+  st = fa_backward_workspace_bytes(B, H, q_len, D, &need);
+  if (st != FA_OK) return st;
+  if (workspace_bytes < need) return FA_ERR_WORKSPACE;
+  DevMask dm;
+  st = check_mask(&bm->spec, q_len, kv_len, &dm);
+  if (st != FA_OK) return st;
+  const AttnArgs a = attn_args(B, H, q_len, kv_len, D, bm, score, scale, dm);
+  const size_t rows = (size_t)B * H * (size_t)q_len;
+  BwdTensors t;
+  t.q = q;
+  t.k = k;
+  t.v = v;
+  t.out = out;
+  t.dout = dout;
+  t.lse = lse;
+  t.dq = dq;
+  t.dk = dk;
+  t.dv = dv;
+  t.dq_acc = static_cast<float*>(workspace);
+  t.delta = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + align_up(rows * D * 4));
+  bool enc_failed = false;
+  const cudaError_t e = launch_backward(a, t, stream, &enc_failed);
+  if (enc_failed) return FA_ERR_CUDA;
+  return cuda_status(e);
+}
+
+fa_status fa_get_status(const fa_block_mask* bm, int32_t clear, cudaStream_t stream) {
+  if (bm == nullptr || bm->status == nullptr) return FA_ERR_INVALID_ARG;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return FA_ERR_CUDA;
+  uint32_t word = 0;
+  if (cudaMemcpy(&word, bm->status, 4, cudaMemcpyDeviceToHost) != cudaSuccess) return FA_ERR_CUDA;
+  if (clear && word != 0 && cudaMemset(bm->status, 0, 4) != cudaSuccess) return FA_ERR_CUDA;
+  if (word & kStatusTimeout) return FA_ERR_TIMEOUT;
+  if (word & kStatusCheck) return FA_ERR_DEVICE_CHECK;
+  return FA_OK;
+}
+
+fa_status fa_block_mask_summary(const fa_block_mask* bm, int64_t counts[3], cudaStream_t stream) {
+  if (bm == nullptr || counts == nullptr || bm->tile_class == nullptr) return FA_ERR_INVALID_ARG;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return FA_ERR_CUDA;
+  const size_t tiles = (size_t)bm->Bm * bm->Hm * (size_t)bm->nq * (size_t)bm->nkv;
+  std::vector<uint8_t> cls(tiles);
+  if (cudaMemcpy(cls.data(), bm->tile_class, tiles, cudaMemcpyDeviceToHost) != cudaSuccess) return FA_ERR_CUDA;
+  counts[0] = counts[1] = counts[2] = 0;
+  for (uint8_t c : cls) counts[c < 3 ? c : 0] += 1;
+  return FA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,80 @@
+// common.cuh -- definitions shared by the block-mask builder and the attention
+// kernels: the device copy of a mask program and its evaluation.
+//
+// A mask program (tutorial "FlexAttention in PyTorch", sections "The two
+// hooks" and Patterns 1-3) is evaluated 32 key columns at a time: for one
+// query row i and columns j0 .. j0+31 every atom yields a 32-bit word whose bit
+// c says whether (i, j0 + c) is visible, and AND / OR combine the words.  The
+// operand stack is a fixed set of eight registers shifted on push and pop, so
+// the evaluation never touches local memory.
+#pragma once
+#include <climits>
+#include <cstdint>
+
+#include "fa.h"
+
+namespace fa {
+
+constexpr uint32_t kStatusTimeout = 1u;  // a bounded wait gave up
+constexpr uint32_t kStatusCheck = 2u;    // a device range check failed
+
+// Device copy of a mask program: node kinds by value, parameters as device
+// pointers.  `doc` is the (single) SAME_DOC array, row-major [Bm][doc_len].
+struct DevMask {
+  int32_t n;
+  int32_t has_doc;
+  int32_t doc_vec_ok;  // doc rows are 16-byte aligned (base and doc_len % 4 == 0)
+  int64_t doc_len;
+  const int32_t* doc;
+  int32_t op[FA_MAX_MASK_NODES];
+  const int32_t* param[FA_MAX_MASK_NODES];
+};
+
+// Scalar parameter of node k for batch row bm: W, n_sink or prefix_len[bm].
+__device__ __forceinline__ int32_t node_arg(const DevMask& m, int k, int bm) {
+  const int op = m.op[k];
+  if (op == FA_M_WINDOW || op == FA_M_SINK) return __ldg(m.param[k]);
+  if (op == FA_M_PREFIX) return __ldg(m.param[k] + bm);
+  return 0;
+}
+
+// Bits [0, n) set, n clamped to [0, 32].
+__device__ __forceinline__ uint32_t low_bits(int64_t n) {
+  return n <= 0 ? 0u : (n >= 32 ? 0xffffffffu : ((1u << (uint32_t)n) - 1u));
+}
+
+// Visibility word of query row i over key columns j0 .. j0+31.
+//  arg[k]    resolved scalar parameter of node k (see node_arg)
+//  eq_doc()  word of (doc[j0 + c] == doc[i]) for c = 0..31
+template <class EqDoc>
+__device__ __forceinline__ uint32_t mask_word(const DevMask& m, const int32_t* arg, int64_t i, int64_t j0,
+                                              EqDoc eq_doc) {
+  uint32_t s0 = 0, s1 = 0, s2 = 0, s3 = 0, s4 = 0, s5 = 0, s6 = 0, s7 = 0;
+#pragma unroll
+  for (int k = 0; k < FA_MAX_MASK_NODES; ++k) {
+    if (k < m.n) {
+      const int op = m.op[k];
+      if (op == FA_M_AND || op == FA_M_OR) {
+        s0 = (op == FA_M_AND) ? (s1 & s0) : (s1 | s0);
+        s1 = s2; s2 = s3; s3 = s4; s4 = s5; s5 = s6; s6 = s7; s7 = 0;
+      } else {
+        uint32_t w;
+        if (op == FA_M_CAUSAL) {
+          w = low_bits(i - j0 + 1);                      // j <= i
+        } else if (op == FA_M_WINDOW) {
+          w = ~low_bits(i - (int64_t)arg[k] + 1 - j0);   // j >= i - W + 1
+        } else if (op == FA_M_SINK || op == FA_M_PREFIX) {
+          w = low_bits((int64_t)arg[k] - j0);            // j < n
+        } else if (op == FA_M_SAME_DOC) {
+          w = eq_doc();
+        } else {
+          w = 0xffffffffu;                               // FA_M_TRUE
+        }
+        s7 = s6; s6 = s5; s5 = s4; s4 = s3; s3 = s2; s2 = s1; s1 = s0; s0 = w;
+      }
+    }
+  }
+  return s0;
+}
+
+}  // namespace fa

@@ -1,0 +1,61 @@
+// internal.h -- launch interfaces between the C ABI (api.cu) and the kernels.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+
+namespace fa {
+
+struct BuildArgs {
+  DevMask mask;
+  int32_t Bm, Hm, block, nq, nkv;
+  int64_t q_len, kv_len;
+  int32_t *kv_num, *kv_idx, *full_num, *full_idx;
+  int32_t *q_num, *q_idx, *full_q_num, *full_q_idx;
+  int32_t *row_order, *col_order;
+  uint8_t* tile_class;
+  int32_t* summary;  // [Bm][2][max(nq, nkv)][2]: doc-id min / max per query and key tile
+  uint32_t* status;
+};
+
+cudaError_t launch_build(const BuildArgs& a, cudaStream_t stream);
+
+// Work description shared by the forward and backward kernels.
+struct AttnArgs {
+  int32_t B, H, Bm, Hm, nq, nkv, D;
+  int32_t q_len, kv_len;
+  const int32_t *kv_num, *kv_idx, *full_num, *full_idx;        // per query-tile row
+  const int32_t *q_num, *q_idx, *full_q_num, *full_q_idx;      // per key-tile column
+  const int32_t *row_order, *col_order;
+  float scale;
+  int32_t score_op;
+  const float* score_param;
+  uint32_t* status;
+  DevMask mask;
+};
+
+struct FwdTensors {
+  const void *q, *k, *v;
+  void* out;
+  float* lse;
+};
+
+struct BwdTensors {
+  const void *q, *k, *v, *out, *dout;
+  const float* lse;
+  void *dq, *dk, *dv;
+  float* dq_acc;  // fp32 [B, H, q_len, D]
+  float* delta;   // fp32 [B, H, q_len]
+};
+
+// Returns a CUDA error, or cudaErrorUnknown with *enc_failed set when a
+// tensor map could not be encoded.
+cudaError_t launch_forward(const AttnArgs& a, const FwdTensors& t, cudaStream_t stream, bool* enc_failed);
+cudaError_t launch_backward(const AttnArgs& a, const BwdTensors& t, cudaStream_t stream, bool* enc_failed);
+
+// Tensor-map encoding through the driver entry point (no libcuda link).
+bool encode_tmap_3d(CUtensorMap* map, CUtensorMapDataType dtype, int elem_bytes, const void* base, uint64_t d0,
+                    uint64_t d1, uint64_t d2, uint32_t box0, uint32_t box1, CUtensorMapSwizzle swizzle);
+
+}  // namespace fa

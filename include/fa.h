@@ -1,0 +1,229 @@
+/*
+ * fa.h -- C ABI of block_sparse_masked_fa_gb300: exact softmax attention whose
+ * mask is summarised at tile level, for one NVIDIA GB300 (sm_103a).
+ *
+ * The method (speedrun notes "FlexAttention", Context paragraph and the
+ * tile-summary paragraph after the mask_mod code block; tutorial "FlexAttention
+ * in PyTorch: Custom and Sparse Attention Without Writing Kernels", section
+ * "The two hooks: score_mod and mask_mod"): a boolean mask_mod decides which
+ * (query, key) pairs are visible; a builder summarises it over BLOCK x BLOCK
+ * tiles into, per query-tile row, the count and column indices of the tiles
+ * that are not fully masked; the attention kernels loop over those lists only,
+ * skip the mask on fully visible tiles, apply it element by element on partial
+ * ones, and let an optional score_mod edit every surviving logit.
+ *
+ * Conventions for every call:
+ *  - Tensors are device pointers into caller-owned memory; the library never
+ *    allocates, frees or keeps a pointer after a call returns (the block mask
+ *    descriptor keeps pointers into the caller's block-mask buffer).
+ *  - q, out, dq, dO are bf16 [B, H, q_len, D]; k, v, dk, dv are bf16
+ *    [B, H, kv_len, D]; lse is fp32 [B, H, q_len]; all contiguous, row-major,
+ *    16-byte aligned.
+ *  - Every call is asynchronous on `stream` (no host synchronisation) except
+ *    fa_get_status and fa_block_mask_summary, which synchronise the stream.
+ *  - Errors that the host can see (null pointers, bad shapes, unsupported
+ *    head dims, misalignment, buffers too small) are returned before any GPU
+ *    work is queued.  Errors that only the device sees (a bounded wait that
+ *    gave up) set bits in the block mask's device status word; read them with
+ *    fa_get_status.  Nothing traps.  No C++ exception crosses this boundary.
+ */
+#ifndef BLOCK_SPARSE_MASKED_FA_GB300_FA_H
+#define BLOCK_SPARSE_MASKED_FA_GB300_FA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FA_OK = 0,
+  FA_ERR_INVALID_ARG = 1,  /* null pointer, unknown enum value, malformed mask program */
+  FA_ERR_UNSUPPORTED = 2,  /* well-formed but not implemented (head dim, block size)   */
+  FA_ERR_SHAPE = 3,        /* sizes out of range or inconsistent with the block mask    */
+  FA_ERR_ALIGNMENT = 4,    /* a pointer is not 16-byte aligned                          */
+  FA_ERR_CUDA = 5,         /* a CUDA runtime or driver call failed                      */
+  FA_ERR_TIMEOUT = 6,      /* device: a bounded wait inside a kernel gave up            */
+  FA_ERR_DEVICE_CHECK = 7, /* device: a range check inside a kernel failed              */
+  FA_ERR_WORKSPACE = 8     /* a caller-provided buffer is smaller than required         */
+} fa_status;
+
+/* ------------------------------------------------------------------------
+ * Mask programs (mask_mod as a fixed, parameterised set).
+ *
+ * A program is up to FA_MAX_MASK_NODES nodes in postfix order; atoms push one
+ * predicate of (b, q_idx, kv_idx), FA_M_AND / FA_M_OR pop two and push one
+ * (tutorial, Pattern 3: compose with and_masks / or_masks).  The stack never
+ * holds more than FA_MAX_MASK_STACK values.  Parameters live in DEVICE memory
+ * so that they can change between calls without rebuilding anything (speedrun
+ * notes, Record #13: the window is read from a tensor):
+ *
+ *   FA_M_TRUE      every pair visible                       param: NULL
+ *   FA_M_CAUSAL    q_idx >= kv_idx                          param: NULL
+ *                  (speedrun notes, mask_mod code; tutorial, "The two hooks")
+ *   FA_M_SAME_DOC  doc[b][q_idx] == doc[b][kv_idx]          param: int32 doc ids
+ *                  [Bm][doc_len], e.g. the inclusive cumsum of end-of-text flags
+ *                  (speedrun notes, mask_mod code; tutorial, Pattern 1).  Every
+ *                  SAME_DOC node of one program must use the same array.
+ *   FA_M_WINDOW    q_idx - kv_idx < W                       param: int32 W (1 value)
+ *                  (speedrun notes, mask_mod code; tutorial, Pattern 2).  No
+ *                  lower bound: combine with FA_M_CAUSAL for a causal window.
+ *   FA_M_SINK      kv_idx < n_sink                          param: int32 n_sink (1 value)
+ *                  (tutorial, Pattern 2)
+ *   FA_M_PREFIX    kv_idx < prefix_len[b]                   param: int32 [Bm]
+ *                  (prefix-LM, named in the tutorial's introduction; the usual
+ *                  form is FA_M_CAUSAL OR FA_M_PREFIX)
+ * ---------------------------------------------------------------------- */
+#define FA_MAX_MASK_NODES 16
+#define FA_MAX_MASK_STACK 8
+
+typedef enum {
+  FA_M_TRUE = 0,
+  FA_M_CAUSAL = 1,
+  FA_M_SAME_DOC = 2,
+  FA_M_WINDOW = 3,
+  FA_M_SINK = 4,
+  FA_M_PREFIX = 5,
+  FA_M_AND = 6,
+  FA_M_OR = 7
+} fa_mask_op;
+
+typedef struct {
+  int32_t op;           /* fa_mask_op                      */
+  const int32_t* param; /* device pointer, see the table   */
+} fa_mask_node;
+
+typedef struct {
+  int32_t n;         /* number of nodes, 1..FA_MAX_MASK_NODES                    */
+  int64_t doc_len;   /* row length (elements) of the SAME_DOC array; must be
+                        >= max(q_len, kv_len) when SAME_DOC is used, else 0     */
+  fa_mask_node node[FA_MAX_MASK_NODES];
+} fa_mask_spec;
+
+/* ------------------------------------------------------------------------
+ * Score mods (score_mod as a fixed set; tutorial, Pattern 3).  The score that
+ * a score_mod sees is the scaled logit x = scale * (q . k).
+ *   FA_S_NONE     s = x                                 param: NULL
+ *   FA_S_SOFTCAP  s = c * tanh(x / c)                   param: device fp32 c (1 value), c > 0
+ *   FA_S_ALIBI    s = x - slope[h] * (q_idx - kv_idx)   param: device fp32 slopes [H]
+ * ---------------------------------------------------------------------- */
+typedef enum { FA_S_NONE = 0, FA_S_SOFTCAP = 1, FA_S_ALIBI = 2 } fa_score_op;
+
+typedef struct {
+  int32_t op;          /* fa_score_op */
+  const float* param;  /* device pointer, see the table */
+} fa_score_spec;
+
+/* ------------------------------------------------------------------------
+ * Block mask (the tile summary of a mask program).
+ *
+ * Tile (I, J) covers query rows [I*block, (I+1)*block) and key rows
+ * [J*block, (J+1)*block), cut at q_len / kv_len.  Its class is EMPTY when no
+ * in-range pair is visible, FULL when every one is, PARTIAL otherwise
+ * (tutorial, "The two hooks": empty / partially masked / full blocks).
+ *
+ *   kv_num_blocks      int32 [Bm][Hm][nq]        PARTIAL tiles of each query-tile row
+ *   kv_indices         int32 [Bm][Hm][nq][nkv]   their J, ascending, zero padded
+ *   full_kv_num_blocks int32 [Bm][Hm][nq]        FULL tiles of each row
+ *   full_kv_indices    int32 [Bm][Hm][nq][nkv]   their J, ascending, zero padded
+ *   q_num_blocks, q_indices, full_q_num_blocks, full_q_indices:
+ *                      the same per key-tile column ([..][nkv], [..][nkv][nq]),
+ *                      used by the backward.
+ *   row_order, col_order: rows / columns sorted by descending tile count (the
+ *                      order the attention kernels take their work in).
+ *   tile_class         uint8 [Bm][Hm][nq][nkv]: 0 EMPTY, 1 PARTIAL, 2 FULL.
+ *   status             device status word (bit 0: a wait timed out).
+ *
+ * The union kv_num_blocks + full_kv_num_blocks is the count of "tiles that are
+ * not fully masked" of the speedrun notes' tile-summary paragraph.  Bm is 1 or
+ * B and Hm is 1 or H: a size of 1 is broadcast over that dimension (tutorial,
+ * B=None / H=None).  All pointers point into one caller-owned device buffer of
+ * fa_block_mask_bytes() bytes; `spec` is a copy of the mask program, which the
+ * attention kernels evaluate on PARTIAL tiles.  Rebuild the block mask when
+ * any mask parameter changes; the kernels need no rebuild.
+ * ---------------------------------------------------------------------- */
+typedef struct {
+  int32_t Bm, Hm, block, nq, nkv;
+  int64_t q_len, kv_len;
+  int32_t* kv_num_blocks;
+  int32_t* kv_indices;
+  int32_t* full_kv_num_blocks;
+  int32_t* full_kv_indices;
+  int32_t* q_num_blocks;
+  int32_t* q_indices;
+  int32_t* full_q_num_blocks;
+  int32_t* full_q_indices;
+  int32_t* row_order;
+  int32_t* col_order;
+  uint8_t* tile_class;
+  int32_t* tile_summary;
+  uint32_t* status;
+  fa_mask_spec spec;
+} fa_block_mask;
+
+/* Bytes of device memory a block mask of this shape needs.
+ * block: a power of two in [16, 128].  Returns FA_ERR_SHAPE for non-positive
+ * sizes or more than 2^31 tiles. */
+fa_status fa_block_mask_bytes(int32_t Bm, int32_t Hm, int64_t q_len, int64_t kv_len, int32_t block,
+                              size_t* bytes);
+
+/* Builds the block mask of `spec` (speedrun notes, tile-summary paragraph:
+ * create_block_mask evaluates mask_mod over the index grid and stores per
+ * query-tile row the count and the column indices of the non-empty tiles).
+ * buffer: device memory of at least fa_block_mask_bytes() bytes, 256-byte
+ * aligned, owned by the caller and used until the block mask is dropped.
+ * bm: host struct, filled with pointers into `buffer` and a copy of `spec`.
+ * Queues 4-5 kernels on `stream`; clears the status word. */
+fa_status fa_create_block_mask(const fa_mask_spec* spec, int32_t Bm, int32_t Hm, int64_t q_len, int64_t kv_len,
+                               int32_t block, void* buffer, size_t buffer_bytes, fa_block_mask* bm,
+                               cudaStream_t stream);
+
+/* Forward: out and LSE (speedrun notes, Context: the two matmuls and the
+ * softmax fused in one tiled kernel that never writes the score matrix; the
+ * kernel visits only the listed tiles).
+ *   out_i = sum_{j visible} softmax_j(s_i) v_j,  LSE_i = ln sum_{j visible} exp(s_ij)
+ * with s_ij = score_mod(scale * q_i . k_j).  A row with no visible key gets
+ * out = 0 and LSE = -inf.  scale: > 0, or 0 for 1/sqrt(D).
+ * D: 64 or 128.  bm: built with block = 128 for this q_len / kv_len, Bm in
+ * {1, B}, Hm in {1, H}. */
+fa_status fa_forward(const void* q, const void* k, const void* v, int32_t B, int32_t H, int64_t q_len,
+                     int64_t kv_len, int32_t D, const fa_block_mask* bm, const fa_score_spec* score, float scale,
+                     void* out, float* lse, cudaStream_t stream);
+
+/* Device workspace fa_backward needs: an fp32 dq accumulator and the per-row
+ * sum(dO * out). */
+fa_status fa_backward_workspace_bytes(int32_t B, int32_t H, int64_t q_len, int32_t D, size_t* bytes);
+
+/* Backward: dq, dk, dv of L = sum(out * dO) (tutorial, Pattern 3: the
+ * score mods are differentiable and the backward is fused).  out and lse are
+ * the forward's results for the same inputs.  dk and dv are written once per
+ * key tile (no atomics); dq is accumulated in fp32 in `workspace` and then
+ * converted.  Same shape rules as fa_forward. */
+fa_status fa_backward(const void* q, const void* k, const void* v, const void* out, const float* lse,
+                      const void* dout, int32_t B, int32_t H, int64_t q_len, int64_t kv_len, int32_t D,
+                      const fa_block_mask* bm, const fa_score_spec* score, float scale, void* dq, void* dk,
+                      void* dv, void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* Synchronises `stream`, reads the block mask's device status word and
+ * returns FA_OK, FA_ERR_TIMEOUT or FA_ERR_DEVICE_CHECK.  clear != 0 resets the
+ * word to 0. */
+fa_status fa_get_status(const fa_block_mask* bm, int32_t clear, cudaStream_t stream);
+
+/* Synchronises `stream` and counts EMPTY, PARTIAL and FULL tiles over the
+ * whole [Bm][Hm][nq][nkv] grid into counts[0..2] (host memory) -- the numbers
+ * behind the tutorial's sparsity map (sharp edge 6). */
+fa_status fa_block_mask_summary(const fa_block_mask* bm, int64_t counts[3], cudaStream_t stream);
+
+/* Static description of a status code. */
+const char* fa_status_string(fa_status status);
+
+/* Library ABI version (major * 100 + minor). */
+int32_t fa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* BLOCK_SPARSE_MASKED_FA_GB300_FA_H */

@@ -1,0 +1,183 @@
+"""C-ABI checks that need no GPU: the library loads, exports every function
+declared in include/fa.h, computes buffer sizes, and rejects bad arguments on
+the host before queuing any GPU work.
+
+Every call here fails host validation, so no fake pointer ever reaches CUDA.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fa.h")
+
+fa = pytest.importorskip("block_sparse_masked_fa_gb300")
+from block_sparse_masked_fa_gb300 import binding as B  # noqa: E402
+
+OK, INVALID, UNSUPPORTED, SHAPE, ALIGN, CUDA, TIMEOUT, CHECK, WORKSPACE = range(9)
+FAKE = 0x7F0000000000  # 256-byte aligned, never dereferenced: every call below fails validation first
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    return sorted(set(re.findall(r"^\s*(?:fa_status|const char\s*\*|int32_t)\s+(fa_\w+)\s*\(", src, re.M)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("fa_create_block_mask", "fa_forward", "fa_backward", "fa_block_mask_bytes",
+              "fa_backward_workspace_bytes", "fa_get_status", "fa_block_mask_summary", "fa_status_string"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol():
+    lib = ctypes.CDLL(B.LIB_PATH)
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    assert set(declared_functions()) == set(B.EXPORTED)
+
+
+def test_version_and_status_strings():
+    assert fa.fa_version() == 100
+    for code in range(9):
+        assert fa.fa_status_string(code) and fa.fa_status_string(code) != "unknown status"
+    assert fa.fa_status_string(99) == "unknown status"
+
+
+def _align(x):
+    return (x + 255) // 256 * 256
+
+
+@pytest.mark.parametrize("Bm,Hm,q,kv,block", [(1, 1, 65536, 65536, 128), (2, 3, 1000, 777, 64), (1, 1, 1, 1, 16)])
+def test_block_mask_bytes_layout(Bm, Hm, q, kv, block):
+    nq, nkv = -(-q // block), -(-kv // block)
+    rows, cols, tiles = Bm * Hm * nq, Bm * Hm * nkv, Bm * Hm * nq * nkv
+    sizes = [rows * 4, tiles * 4, rows * 4, tiles * 4, cols * 4, tiles * 4, cols * 4, tiles * 4, rows * 4, cols * 4,
+             tiles, Bm * 2 * max(nq, nkv) * 2 * 4, 4]
+    assert fa.fa_block_mask_bytes(Bm, Hm, q, kv, block) == sum(_align(s) for s in sizes)
+
+
+def _bytes_status(*args):
+    n = ctypes.c_size_t()
+    return B._lib.fa_block_mask_bytes(*args, ctypes.byref(n))
+
+
+def test_block_mask_bytes_rejects():
+    assert _bytes_status(1, 1, 512, 512, 24) == UNSUPPORTED
+    assert _bytes_status(1, 1, 512, 512, 256) == UNSUPPORTED
+    assert _bytes_status(1, 1, 512, 512, 8) == UNSUPPORTED
+    assert _bytes_status(0, 1, 512, 512, 128) == SHAPE
+    assert _bytes_status(1, 1, 0, 512, 128) == SHAPE
+    assert _bytes_status(1, 1, 1 << 40, 512, 128) == SHAPE
+    assert B._lib.fa_block_mask_bytes(1, 1, 512, 512, 128, None) == INVALID
+
+
+def _spec(nodes, doc_len=0):
+    s = B.MaskSpec()
+    s.n = len(nodes)
+    s.doc_len = doc_len
+    for k, (op, param) in enumerate(nodes):
+        s.node[k].op = op
+        s.node[k].param = param
+    return s
+
+
+def _create(spec, q=512, kv=512, block=128, buf=FAKE, nbytes=1 << 30, bm=True):
+    st = B.BlockMaskStruct()
+    return B._lib.fa_create_block_mask(ctypes.byref(spec) if spec is not None else None, 1, 1, q, kv, block, buf,
+                                       nbytes, ctypes.byref(st) if bm else None, None)
+
+
+M = B.MASK_OPS
+
+
+def test_create_block_mask_rejects():
+    causal = _spec([(M["causal"], None)])
+    assert _create(None) == INVALID
+    assert _create(causal, bm=False) == INVALID
+    assert _create(causal, buf=FAKE + 16) == ALIGN
+    assert _create(causal, nbytes=100) == WORKSPACE
+    assert _create(causal, block=48) == UNSUPPORTED
+    assert _create(_spec([])) == INVALID
+    assert _create(_spec([(99, None)])) == INVALID
+    assert _create(_spec([(M["causal"], None), (M["and"], None)])) == INVALID           # AND with one operand
+    assert _create(_spec([(M["causal"], None), (M["causal"], None)])) == INVALID        # two values left
+    assert _create(_spec([(M["window"], None)])) == INVALID                             # window needs its W
+    assert _create(_spec([(M["window"], FAKE + 2)])) == INVALID                         # misaligned parameter
+    assert _create(_spec([(M["same_doc"], FAKE)], doc_len=100)) == SHAPE                # doc ids too short
+    two_docs = [(M["same_doc"], FAKE), (M["same_doc"], FAKE + 4096), (M["and"], None)]
+    assert _create(_spec(two_docs, doc_len=512)) == INVALID                             # one doc array only
+    deep = [(M["causal"], None)] * 9 + [(M["and"], None)] * 7
+    assert _create(_spec(deep)) == INVALID                                              # stack deeper than 8
+    too_many = B.MaskSpec()
+    too_many.n = 17
+    assert _create(too_many) == INVALID
+
+
+def _bm(block=128, q=1024, kv=1024, Bm=1, Hm=1):
+    st = B.BlockMaskStruct()
+    st.Bm, st.Hm, st.block, st.q_len, st.kv_len = Bm, Hm, block, q, kv
+    st.nq, st.nkv = -(-q // block), -(-kv // block)
+    st.status = FAKE
+    st.row_order = FAKE
+    st.spec.n = 1
+    st.spec.node[0].op = M["causal"]
+    return st
+
+
+def _fwd(q=FAKE, D=64, B_=1, H=1, S=1024, bm=None, score=None, scale=0.0, lse=FAKE):
+    bm = _bm() if bm is None else bm
+    sc = B.ScoreSpec() if score is None else score
+    return B._lib.fa_forward(q, FAKE, FAKE, B_, H, S, S, D, ctypes.byref(bm), ctypes.byref(sc), scale, FAKE, lse,
+                             None)
+
+
+def test_forward_rejects():
+    assert _fwd(q=None) == INVALID
+    assert _fwd(q=FAKE + 8) == ALIGN
+    assert _fwd(lse=FAKE + 2) == ALIGN
+    assert _fwd(D=96) == UNSUPPORTED
+    assert _fwd(D=256) == UNSUPPORTED
+    assert _fwd(bm=_bm(block=64)) == UNSUPPORTED
+    assert _fwd(S=2048) == SHAPE                      # block mask built for another length
+    assert _fwd(B_=2, bm=_bm(Bm=3)) == SHAPE         # Bm must be 1 or B
+    assert _fwd(H=4, bm=_bm(Hm=2)) == SHAPE          # Hm must be 1 or H
+    assert _fwd(B_=0) == SHAPE
+    assert _fwd(scale=-1.0) == INVALID
+    assert _fwd(scale=float("nan")) == INVALID
+    bad_score = B.ScoreSpec()
+    bad_score.op = 7
+    assert _fwd(score=bad_score) == INVALID
+    cap_without_param = B.ScoreSpec()
+    cap_without_param.op = B.SCORE_OPS["softcap"]
+    assert _fwd(score=cap_without_param) == INVALID
+    broken = _bm()
+    broken.spec.n = 0
+    assert _fwd(bm=broken) == INVALID
+
+
+def test_backward_workspace_and_rejects():
+    assert fa.fa_backward_workspace_bytes(2, 3, 1000, 128) == _align(2 * 3 * 1000 * 128 * 4) + _align(2 * 3 * 1000 * 4)
+    n = ctypes.c_size_t()
+    assert B._lib.fa_backward_workspace_bytes(1, 1, 100, 80, ctypes.byref(n)) == UNSUPPORTED
+    bm = _bm()
+    sc = B.ScoreSpec()
+    args = [FAKE] * 6 + [1, 1, 1024, 1024, 64, ctypes.byref(bm), ctypes.byref(sc), 0.0] + [FAKE] * 4
+    assert B._lib.fa_backward(*args, 16, None) == WORKSPACE        # workspace too small
+    bad = list(args)
+    bad[3] = FAKE + 4
+    assert B._lib.fa_backward(*bad, 1 << 30, None) == ALIGN
+    bad = list(args)
+    bad[0] = None
+    assert B._lib.fa_backward(*bad, 1 << 30, None) == INVALID
+    bad = list(args)
+    bad[10] = 32
+    assert B._lib.fa_backward(*bad, 1 << 30, None) == UNSUPPORTED
+
+
+def test_status_calls_reject_null():
+    assert B._lib.fa_get_status(None, 0, None) == INVALID
+    counts = (ctypes.c_int64 * 3)()
+    assert B._lib.fa_block_mask_summary(None, ctypes.byref(counts), None) == INVALID
