@@ -1,0 +1,393 @@
+"""Throughput of the tile-sparse masked attention hot path on one GB300.
+
+A step is one pass of the whole path over one batch of synthetic input:
+fa_create_block_mask + fa_forward + fa_backward, on the packed 64K-token
+workload (B=1, H=6, S=65536, D=128, causal & same document & 1024 window,
+log-normal document lengths).  The metric is attention TFLOP/s counted over
+visible tiles only: forward 4*128*128*D per visible tile per (b, h), backward
+2.5x that (five tile GEMMs against two).
+
+Prints ONE JSON line (rank 0).  --impl reference times the CPU oracle on a
+bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from synth import WORKLOADS, make_doc_ids, make_qkv  # noqa: E402
+
+PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}
+METRIC = "attention TFLOP/s over visible tiles (fwd+bwd)"
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return json.load(f), "measured"
+    return PEAKS_FALLBACK, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[3:7]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def workload_tensors(w, seed=None):
+    seed = w.seed if seed is None else seed
+    q, k, v, do = make_qkv(w.B, w.H, w.S, w.D, seed)
+    docs = make_doc_ids(w.docs, w.S, w.doc_seed or seed) if w.docs is not None else None
+    return q, k, v, do, docs
+
+
+def visible_tiles(fa, bm, B, H):
+    """Sum over (b, h) of non-empty tiles, from the block mask's counts."""
+    L = bm.lists()
+    per_row = (L["kv_num_blocks"].long() + L["full_kv_num_blocks"].long()).sum().item()
+    rep = (B // bm.struct.Bm) * (H // bm.struct.Hm)
+    return per_row * rep
+
+
+def run_gpu(args):
+    import torch
+    import torch.distributed as dist
+
+    import block_sparse_masked_fa_gb300 as fa
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl")
+
+    w = WORKLOADS[args.workload]
+    q_h, k_h, v_h, do_h, docs_np = workload_tensors(w, seed=w.seed + 97 * rank)
+    dev = torch.device("cuda", local)
+    q, k, v, do = (t.to(dev) for t in (q_h, k_h, v_h, do_h))
+    docs = torch.as_tensor(docs_np, dtype=torch.int32, device=dev) if docs_np is not None else None
+    W = torch.tensor([args.window if w.windows else 1024], dtype=torch.int32, device=dev)
+    nodes = []
+    for node in w.mask.nodes:
+        if node[0] == "same_doc":
+            nodes.append(("same_doc", docs))
+        elif node[0] == "window":
+            nodes.append(("window", W if w.windows else int(node[1])))
+        elif node[0] == "sink":
+            nodes.append(("sink", int(node[1])))
+        else:
+            nodes.append((node[0],))
+    spec, keep = fa.make_mask_spec(nodes, device=dev)
+    score = None
+    if w.score[0] == "softcap":
+        score = fa.make_score_spec("softcap", [float(w.score[1])], device=dev)
+    elif w.score[0] == "alibi":
+        from synth import make_alibi_slopes
+        score = fa.make_score_spec("alibi", torch.as_tensor(make_alibi_slopes(w.H)), device=dev)
+    stream = torch.cuda.current_stream()
+    bm_buf = torch.empty(fa.fa_block_mask_bytes(1, 1, w.S, w.S, 128), dtype=torch.uint8, device=dev)
+    ws = torch.empty(fa.fa_backward_workspace_bytes(w.B, w.H, w.S, w.D), dtype=torch.uint8, device=dev)
+    out = torch.empty_like(q)
+    lse = torch.empty(w.B, w.H, w.S, dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+
+    have_bwd = True
+    bm0 = fa.fa_create_block_mask((spec, keep), 1, 1, w.S, w.S, 128, buffer=bm_buf)
+    fa.fa_forward(q, k, v, bm0, score=score, out=out, lse=lse)
+    try:
+        fa.fa_backward(q, k, v, out, lse, do, bm0, score=score, dq=dq, dk=dk, dv=dv, workspace=ws)
+    except fa.FaError:
+        have_bwd = False
+    torch.cuda.synchronize()
+
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+    marks = []
+
+    def step(record):
+        e = [ev() for _ in range(4)] if record else None
+        if record:
+            e[0].record(stream)
+        bm = fa.fa_create_block_mask((spec, keep), 1, 1, w.S, w.S, 128, buffer=bm_buf)
+        if record:
+            e[1].record(stream)
+        fa.fa_forward(q, k, v, bm, score=score, out=out, lse=lse)
+        if record:
+            e[2].record(stream)
+        if have_bwd:
+            fa.fa_backward(q, k, v, out, lse, do, bm, score=score, dq=dq, dk=dk, dv=dv, workspace=ws)
+        if record:
+            e[3].record(stream)
+            marks.append(e)
+        return bm
+
+    for _ in range(args.warmup):
+        bm = step(False)
+    torch.cuda.synchronize()
+    n_vis = visible_tiles(fa, bm, w.B, w.H)
+    fwd_flops = n_vis * 4.0 * 128 * 128 * w.D
+    bwd_flops = 2.5 * fwd_flops
+    step_flops = fwd_flops + (bwd_flops if have_bwd else 0.0)
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0, t1 = ev(), ev()
+    t0.record(stream)
+    for _ in range(args.steps):
+        step(True)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    ms_total = t0.elapsed_time(t1)
+    if world > 1:
+        tt = torch.tensor([ms_total], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms_total = float(tt.item())
+    ms_step = ms_total / args.steps
+    build_ms = sum(m[0].elapsed_time(m[1]) for m in marks) / args.steps
+    fwd_ms = sum(m[1].elapsed_time(m[2]) for m in marks) / args.steps
+    bwd_ms = sum(m[2].elapsed_time(m[3]) for m in marks) / args.steps
+    assert fa.fa_get_status(bm) == 0, "device status reported an error"
+
+    # end to end through the public API: pinned host inputs in, results back to host
+    pin = lambda t: t.pin_memory()
+    hq, hk, hv, hdo = (pin(t) for t in (q_h, k_h, v_h, do_h))
+    hdocs = pin(torch.as_tensor(docs_np, dtype=torch.int32)) if docs_np is not None else None
+    h_out, h_lse = pin(torch.empty_like(q_h)), pin(torch.empty(w.B, w.H, w.S, dtype=torch.float32))
+    h_dq, h_dk, h_dv = (pin(torch.empty_like(t)) for t in (q_h, k_h, v_h))
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo)) + \
+        (hdocs.numel() * 4 if hdocs is not None else 0)
+    d2h = h_out.numel() * 2 + h_lse.numel() * 4 + (3 * h_dq.numel() * 2 if have_bwd else 0)
+
+    def e2e_step():
+        q.copy_(hq, non_blocking=True)
+        k.copy_(hk, non_blocking=True)
+        v.copy_(hv, non_blocking=True)
+        do.copy_(hdo, non_blocking=True)
+        if hdocs is not None:
+            docs.copy_(hdocs, non_blocking=True)
+        bm = step(False)
+        h_out.copy_(out, non_blocking=True)
+        h_lse.copy_(lse, non_blocking=True)
+        if have_bwd:
+            h_dq.copy_(dq, non_blocking=True)
+            h_dk.copy_(dk, non_blocking=True)
+            h_dv.copy_(dv, non_blocking=True)
+        return bm
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = ev(), ev()
+    e2e_steps = max(3, args.steps // 2)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+
+    peaks, peak_src = load_peaks()
+    peak = float(peaks["bf16_tflops"])
+    dominant = "bwd" if (have_bwd and bwd_ms > fwd_ms) else "fwd"
+    dom_ms = bwd_ms if dominant == "bwd" else fwd_ms
+    dom_flops = bwd_flops if dominant == "bwd" else fwd_flops
+    achieved = dom_flops / (dom_ms * 1e-3) / 1e12
+    value = world * step_flops / (ms_step * 1e-3) / 1e12
+    launches_per_step = (5 if docs is not None else 4) + 1 + (4 if have_bwd else 0)
+    res = {
+        "metric": METRIC if have_bwd else "attention TFLOP/s over visible tiles (fwd only; bwd not built)",
+        "value": round(value, 2),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) q/k/v/dO in bf16, log-normal document lengths)",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "S": w.S, "D": w.D,
+                   "mask": " ".join(n[0] if len(n) == 1 else f"{n[0]}:{n[1]}" for n in w.mask.nodes),
+                   "score_mod": w.score[0], "block": 128, "visible_tiles": int(n_vis),
+                   "l2": "inputs larger than L2 (q, k, v, dO: 4 x %d MiB)" % (q.numel() * 2 >> 20),
+                   "parallelism": f"replicas x{world}"},
+        "breakdown_ms": {"create_block_mask": round(build_ms, 4), "forward": round(fwd_ms, 4),
+                         "backward": round(bwd_ms, 4) if have_bwd else None},
+        "fwd_tflops": round(fwd_flops / (fwd_ms * 1e-3) / 1e12, 2),
+        "bwd_tflops": round(bwd_flops / (bwd_ms * 1e-3) / 1e12, 2) if have_bwd else None,
+        "roofline": {"kernel": dominant, "bound": "tensor", "achieved": round(achieved, 2), "peak": peak,
+                     "peak_source": f"bf16_tflops ({peak_src}, burst)", "unit": "TFLOP/s",
+                     "frac": round(achieved / peak, 4), "traffic": None},
+        "e2e": {"value": round(world * step_flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+                "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = cpu_baseline(w, args.cpu_sample_tokens)
+    if world > 1:
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+
+
+def _sample_visible_tiles(mask, docs_row, S):
+    import oracle
+
+    cls = oracle.classify_tiles(oracle.Program(mask, doc_row=docs_row), S, S, 128)
+    return int((cls > 0).sum())
+
+
+def cpu_baseline(w, tokens, heads=1):
+    """The oracle, as it stands, on the first `tokens` positions of `heads` heads.
+
+    The workload's masks are causal, so a prefix of the sequence is a
+    self-contained problem of the same kind; its visible tiles give the FLOP
+    count in the metric's convention."""
+    import torch
+
+    import oracle
+
+    S = min(tokens, w.S)
+    q, k, v, do = make_qkv(1, heads, S, w.D, w.seed)
+    docs = make_doc_ids(w.docs, w.S, w.doc_seed or w.seed)[0][:S] if w.docs is not None else None
+    mask = w.mask.with_window(1024) if w.windows else w.mask
+    prog = oracle.Program(mask, doc_row=docs)
+    score = ("none",)
+    if w.score[0] == "softcap":
+        score = ("softcap", float(w.score[1]))
+    elif w.score[0] == "alibi":
+        from synth import make_alibi_slopes
+        score = ("alibi", make_alibi_slopes(w.H))
+    scale = 1.0 / np.sqrt(w.D)
+    t = time.perf_counter()
+    for h in range(heads):
+        f = lambda x: x[0, h].to(torch.float64).numpy()
+        oracle.forward_head(f(q), f(k), f(v), prog, score, h, scale)
+        oracle.backward_head(f(q), f(k), f(v), f(do), prog, score, h, scale)
+    dt = time.perf_counter() - t
+    n_vis = _sample_visible_tiles(mask, docs, S) * heads
+    flops = 3.5 * n_vis * 4.0 * 128 * 128 * w.D
+    cores = int(os.environ.get("OMP_NUM_THREADS", len(os.sched_getaffinity(0))))
+    return {"value": round(flops / dt / 1e12, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "seconds": round(dt, 2),
+            "sample": f"fwd+bwd of {heads} head(s) on the first {S} tokens of {w.name} "
+                      f"({n_vis} visible tiles, same mask and score mod)"}
+
+
+def run_reference(args):
+    """--impl reference: the CPU oracle as it stands, on a bounded sample per step."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    w = WORKLOADS[args.workload]
+    vals = []
+    for _ in range(args.warmup):
+        cpu_baseline(w, args.ref_sample_tokens)
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        vals.append(cpu_baseline(w, args.ref_sample_tokens))
+    total = time.perf_counter() - t
+    v = statistics.median(x["value"] for x in vals)
+    res = {"impl": "reference", "metric": METRIC, "value": v, "unit": "TFLOP/s", "n_gpus": args.gpus,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1000 * total / max(1, args.steps), 2),
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+           "data": "synthetic", "config": {"workload": w.name, "B": w.B, "H": w.H, "S": w.S, "D": w.D},
+           "cpu_baseline": {"value": v, "unit": "TFLOP/s", "kind": "oracle", "cores": vals[0]["cores"],
+                            "sample": vals[0]["sample"]},
+           "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(res), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--workload", type=int, default=2, choices=sorted(WORKLOADS))
+    ap.add_argument("--window", type=int, default=1024, help="window of the sweep workload (5)")
+    ap.add_argument("--cpu-sample-tokens", type=int, default=32768,
+                    help="tokens of the oracle sample timed as cpu_baseline")
+    ap.add_argument("--ref-sample-tokens", type=int, default=16384,
+                    help="tokens of the oracle sample per step of --impl reference")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -214,12 +214,12 @@ __global__ void __launch_bounds__(192, 2)
   } else {
     // ------------------------------------------------------------ softmax + epilogue
     const int r = threadIdx.x;  // 0..127, TMEM lane
-    const int64_t i = (int64_t)I * 128 + r;
+    const int i = I * 128 + r;
     const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
     const uint32_t tS = tmem + lane_off;
     const uint32_t tO = tmem + lane_off + 128;
     const int32_t* doc_row = p.mask.has_doc ? p.mask.doc + (int64_t)bm * p.mask.doc_len : nullptr;
-    const int32_t doc_i = doc_row ? __ldg(doc_row + min(i, (int64_t)p.q_len - 1)) : 0;
+    const int32_t doc_i = doc_row ? __ldg(doc_row + min(i, p.q_len - 1)) : 0;
 
     const float sc_l2 = p.scale * kLog2e;  // logit -> log2 units
     float cap_l2 = 0.f, sc_over_cap = 0.f, slope_l2 = 0.f;
@@ -238,27 +238,13 @@ __global__ void __launch_bounds__(192, 2)
       const int J = tile_of(jj);
       const int64_t j0 = (int64_t)J * 128;
       const bool ragged = j0 + 128 > p.kv_len;
-      if (!warp_wait(b_s, jj & 1, &ctl->abort)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      float s[128];
-      tmem_ld128f(tS, s);
-
-      // logits in log2 units (SCORE_NONE keeps raw q.k and folds the scale into the exponent)
-      if constexpr (SCORE == FA_S_SOFTCAP) {
-#pragma unroll
-        for (int e = 0; e < 128; ++e) s[e] = cap_l2 * tanh_fast(s[e] * sc_over_cap);
-      } else if constexpr (SCORE == FA_S_ALIBI) {
-        const float base = slope_l2 * (float)(i - j0);
-#pragma unroll
-        for (int e = 0; e < 128; ++e) s[e] = fmaf(s[e], sc_l2, fmaf(slope_l2, (float)e, -base));
-      }
-      if (partial || ragged) {
-#pragma unroll
+      const bool msk = partial || ragged;
+      // visibility words of the 4 x 32 key columns, computed before S is loaded
+      uint32_t wd[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};
+      if (msk) {
+#pragma unroll 1
         for (int c = 0; c < 4; ++c) {
-          const int64_t jc = j0 + 32 * c;
+          const int jc = (int)j0 + 32 * c;
           uint32_t w = low_bits((int64_t)p.kv_len - jc);
           if (partial) {
             // doc ids of the 32 key columns: the same addresses for every thread (broadcast loads)
@@ -273,21 +259,60 @@ __global__ void __launch_bounds__(192, 2)
                           (uint32_t)(d.z == doc_i) << (4 * q4 + 2) | (uint32_t)(d.w == doc_i) << (4 * q4 + 3);
                 }
               } else {
-                const int64_t jn = min(jc + 32, (int64_t)p.kv_len);
-                for (int64_t j = jc; j < jn; ++j) bits |= (uint32_t)(__ldg(doc_row + j) == doc_i) << (uint32_t)(j - jc);
+                const int jn = min(jc + 32, p.kv_len);
+                for (int j = jc; j < jn; ++j) bits |= (uint32_t)(__ldg(doc_row + j) == doc_i) << (uint32_t)(j - jc);
               }
               return bits;
             };
-            w &= mask_word(p.mask, ctl->arg, i, jc, eq);
+            w &= mask_word_rolled(p.mask, ctl->arg, i, jc, eq);
           }
-#pragma unroll
-          for (int e = 0; e < 32; ++e) s[32 * c + e] = ((w >> e) & 1u) ? s[32 * c + e] : -INFINITY;
+          // select by c without dynamic indexing
+          wd[0] = (c == 0) ? w : wd[0];
+          wd[1] = (c == 1) ? w : wd[1];
+          wd[2] = (c == 2) ? w : wd[2];
+          wd[3] = (c == 3) ? w : wd[3];
         }
       }
-      float mx = s[0];
+      if (!warp_wait(b_s, jj & 1, &ctl->abort)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      float s[128];
+      tmem_ld128f(tS, s);
+      if (msk) {
 #pragma unroll
-      for (int e = 1; e < 128; ++e) mx = fmaxf(mx, s[e]);
-      if constexpr (SCORE == FA_S_NONE) mx *= sc_l2;  // scale > 0 keeps the order
+        for (int e = 0; e < 128; ++e) s[e] = ((wd[e >> 5] >> (e & 31)) & 1u) ? s[e] : -INFINITY;
+      }
+
+      const float base = slope_l2 * (float)(i - (int)j0);  // ALiBi: -slope (i - j) = -base + slope * e
+      // -- row maximum in log2 units (4 independent chains)
+      float mx;
+      {
+        float a0 = -INFINITY, a1 = -INFINITY, a2 = -INFINITY, a3 = -INFINITY;
+#pragma unroll
+        for (int e = 0; e < 128; e += 4) {
+          if constexpr (SCORE == FA_S_ALIBI) {
+            a0 = fmaxf(a0, fmaf(s[e], sc_l2, slope_l2 * (float)e));
+            a1 = fmaxf(a1, fmaf(s[e + 1], sc_l2, slope_l2 * (float)(e + 1)));
+            a2 = fmaxf(a2, fmaf(s[e + 2], sc_l2, slope_l2 * (float)(e + 2)));
+            a3 = fmaxf(a3, fmaf(s[e + 3], sc_l2, slope_l2 * (float)(e + 3)));
+          } else {
+            a0 = fmaxf(a0, s[e]);
+            a1 = fmaxf(a1, s[e + 1]);
+            a2 = fmaxf(a2, s[e + 2]);
+            a3 = fmaxf(a3, s[e + 3]);
+          }
+        }
+        mx = fmaxf(fmaxf(a0, a1), fmaxf(a2, a3));
+        if constexpr (SCORE == FA_S_NONE) {
+          mx *= sc_l2;  // scale > 0 keeps the order
+        } else if constexpr (SCORE == FA_S_SOFTCAP) {
+          mx = (mx == -INFINITY) ? -INFINITY : cap_l2 * tanh_fast(mx * sc_over_cap);  // soft-cap is increasing
+        } else {
+          mx -= base;
+        }
+      }
 
       const float m_new = fmaxf(m, mx);
       bool need = false;
@@ -301,7 +326,7 @@ __global__ void __launch_bounds__(192, 2)
           l *= alpha;
           m = m_new;
         }
-#pragma unroll
+#pragma unroll 1
         for (int c = 0; c < D / 32; ++c) {
           float o[32];
           tmem_ld32f(tO + 32 * c, o);
@@ -311,27 +336,40 @@ __global__ void __launch_bounds__(192, 2)
         }
       }
       const float m_use = (m == -INFINITY) ? 0.f : m;
-      float rs = 0.f;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t pk[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          float x0 = s[32 * c + 2 * e], x1 = s[32 * c + 2 * e + 1];
+      // -- P = 2^(x - m) as bf16 into TMEM (over the consumed S columns), row sum (4 chains)
+      {
+        float c0 = 0.f, c1 = 0.f, c2 = 0.f, c3 = 0.f;
+        const float off = -(base + m_use);
+        auto pexp = [&](int e) -> float {
+          float x;
           if constexpr (SCORE == FA_S_NONE) {
-            x0 = fmaf(x0, sc_l2, -m_use);
-            x1 = fmaf(x1, sc_l2, -m_use);
+            x = fmaf(s[e], sc_l2, -m_use);
+          } else if constexpr (SCORE == FA_S_SOFTCAP) {
+            x = fmaf(cap_l2, tanh_fast(s[e] * sc_over_cap), -m_use);
+            if (msk) x = (s[e] == -INFINITY) ? -INFINITY : x;
           } else {
-            x0 -= m_use;
-            x1 -= m_use;
+            x = fmaf(s[e], sc_l2, fmaf(slope_l2, (float)e, off));
           }
-          const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-          rs += p0 + p1;
-          pk[e] = pack_bf16x2(p0, p1);
+          return ex2_approx(x);
+        };
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int e2 = 0; e2 < 16; e2 += 2) {
+            const int e = 32 * c + 2 * e2;
+            const float p0 = pexp(e), p1 = pexp(e + 1), p2 = pexp(e + 2), p3 = pexp(e + 3);
+            c0 += p0;
+            c1 += p1;
+            c2 += p2;
+            c3 += p3;
+            pk[e2] = pack_bf16x2(p0, p1);
+            pk[e2 + 1] = pack_bf16x2(p2, p3);
+          }
+          tmem_st16(tS + 16 * c, pk);
         }
-        tmem_st16(tS + 16 * c, pk);
+        l += (c0 + c1) + (c2 + c3);
       }
-      l += rs;
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(b_p);
