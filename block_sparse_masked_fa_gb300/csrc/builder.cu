@@ -5,38 +5,48 @@
 // empty, partial or full).
 //
 // Kernels, all stream-ordered, no host synchronisation:
-//  1. tile_summary  -- doc-id min / max of every query and key tile (only when
-//                      the program has SAME_DOC); reads the doc ids once.
-//  2. classify_rows -- one warp per query-tile row.  Each lane classifies one
-//                      tile of a 32-tile chunk with a three-valued interval
-//                      test per atom (nothing / everything / undecided visible,
-//                      combined with Kleene AND / OR); undecided tiles are
-//                      settled exactly by evaluating all their pairs with the
-//                      whole warp.  Ballot + popcount prefix sums compact the
-//                      PARTIAL and FULL column indices; tails are zeroed.
-//  3. classify_cols -- one warp per key-tile column, same compaction over the
-//                      tile classes written by (2): the backward's lists.
-//  4. order         -- rows (then columns) sorted by descending tile count
-//                      with a counting sort, the order the attention kernels
-//                      take their work in (longest first).
+//  1. tile_summary -- doc-id min / max of every query and key tile (only when
+//                     the program has SAME_DOC); reads the doc ids once.
+//  2. classify     -- one warp per (query-tile row, chunk of 32 key tiles).
+//                     Each lane classifies one tile with a three-valued
+//                     interval test per atom (nothing / everything / undecided
+//                     visible, combined with Kleene AND / OR); undecided tiles
+//                     are settled exactly by evaluating all their pairs with
+//                     the whole warp.  Writes one class byte per tile.
+//  3. compact      -- one warp per query-tile row and one per key-tile
+//                     column: ballot + popcount prefix sums turn the class
+//                     bytes into ascending PARTIAL and FULL index lists with
+//                     zeroed tails (the columns' lists feed the backward).
+//  4. order        -- rows and columns sorted by descending tile count with a
+//                     counting sort, the order the attention kernels take
+//                     their work in (longest first).
 #include "internal.h"
 
 namespace fa {
 namespace {
 
-enum : int { K_NONE = 0, K_ALL = 1, K_SOME = 2 };
+// Interval classes of a predicate over a tile: nothing visible, everything
+// visible, certainly partial (both kinds of pairs exist), or unknown.
+enum : int { K_NONE = 0, K_ALL = 1, K_PART = 2, K_SOME = 3 };
 
 __device__ __forceinline__ int kleene_and(int a, int b) {
-  return (a == K_NONE || b == K_NONE) ? K_NONE : ((a == K_ALL && b == K_ALL) ? K_ALL : K_SOME);
+  if (a == K_NONE || b == K_NONE) return K_NONE;
+  if (a == K_ALL) return b;
+  if (b == K_ALL) return a;
+  return K_SOME;  // two partial or unknown operands: the conjunction may be empty
 }
 __device__ __forceinline__ int kleene_or(int a, int b) {
-  return (a == K_ALL || b == K_ALL) ? K_ALL : ((a == K_NONE && b == K_NONE) ? K_NONE : K_SOME);
+  if (a == K_ALL || b == K_ALL) return K_ALL;
+  if (a == K_NONE) return b;
+  if (b == K_NONE) return a;
+  return K_SOME;
 }
 
-// Three-valued class of the whole program over rows [i0, i1] x cols [j0, j1]
-// (inclusive).  q_mn/q_mx and k_mn/k_mx bound the doc ids of the two ranges.
+// Class of the whole program over rows [i0, i1] x cols [j0, j1] (inclusive).
+// q_mn/q_mx (k_mn/k_mx) bound the doc ids of the row (column) range; *_run is
+// set when the ids there step by 0 or +1 only, so every id in [mn, mx] occurs.
 __device__ int program_interval(const DevMask& m, const int32_t* arg, int64_t i0, int64_t i1, int64_t j0, int64_t j1,
-                                int q_mn, int q_mx, int k_mn, int k_mx) {
+                                int q_mn, int q_mx, int q_run, int k_mn, int k_mx, int k_run) {
   int s0 = 0, s1 = 0, s2 = 0, s3 = 0, s4 = 0, s5 = 0, s6 = 0, s7 = 0;
 #pragma unroll
   for (int k = 0; k < FA_MAX_MASK_NODES; ++k) {
@@ -48,15 +58,20 @@ __device__ int program_interval(const DevMask& m, const int32_t* arg, int64_t i0
       } else {
         int c;
         const int64_t a = arg[k];
+        // the three monotone atoms are exactly partial when neither extreme holds
         if (op == FA_M_CAUSAL) {            // i >= j
-          c = (i0 >= j1) ? K_ALL : (i1 < j0 ? K_NONE : K_SOME);
+          c = (i0 >= j1) ? K_ALL : (i1 < j0 ? K_NONE : K_PART);
         } else if (op == FA_M_WINDOW) {     // i - j < W
-          c = (i1 - j0 < a) ? K_ALL : (i0 - j1 >= a ? K_NONE : K_SOME);
+          c = (i1 - j0 < a) ? K_ALL : (i0 - j1 >= a ? K_NONE : K_PART);
         } else if (op == FA_M_SINK || op == FA_M_PREFIX) {  // j < n
-          c = (j1 < a) ? K_ALL : (j0 >= a ? K_NONE : K_SOME);
+          c = (j1 < a) ? K_ALL : (j0 >= a ? K_NONE : K_PART);
         } else if (op == FA_M_SAME_DOC) {
-          c = (q_mx < k_mn || k_mx < q_mn) ? K_NONE
-                                           : ((q_mn == q_mx && k_mn == k_mx && q_mn == k_mn) ? K_ALL : K_SOME);
+          if (q_mx < k_mn || k_mx < q_mn)
+            c = K_NONE;
+          else if (q_mn == q_mx && k_mn == k_mx && q_mn == k_mn)
+            c = K_ALL;
+          else  // overlapping ranges in which every id occurs share an id and hold a distinct one
+            c = (q_run && k_run) ? K_PART : K_SOME;
         } else {
           c = K_ALL;
         }
@@ -83,27 +98,41 @@ __global__ void tile_summary_kernel(BuildArgs a) {
   const int64_t i0 = (int64_t)t * a.block;
   const int64_t i1 = min(i0 + a.block, len);
   int mn = INT_MAX, mx = INT_MIN;
+  bool run = true;
   for (int64_t i = i0 + lane; i < i1; i += 32) {
     const int d = __ldg(doc + i);
     mn = min(mn, d);
     mx = max(mx, d);
+    if (i + 1 < i1) {
+      const int step = __ldg(doc + i + 1) - d;
+      run = run && (step == 0 || step == 1);
+    }
   }
   mn = __reduce_min_sync(0xffffffffu, mn);
   mx = __reduce_max_sync(0xffffffffu, mx);
+  run = __all_sync(0xffffffffu, run);
   if (lane == 0) {
-    int32_t* s = a.summary + (((int64_t)bm * 2 + which) * tmax + t) * 2;
+    int32_t* s = a.summary + (((int64_t)bm * 2 + which) * tmax + t) * 4;
     s[0] = mn;
     s[1] = mx;
+    s[2] = run ? 1 : 0;
+    s[3] = 0;
   }
 }
 
 constexpr int kBuildWarps = 8;
 
-__global__ void __launch_bounds__(kBuildWarps * 32) classify_rows_kernel(BuildArgs a) {
+// One warp per (query-tile row, chunk of 32 key tiles): each lane classifies
+// one tile; undecided tiles are settled exactly by the whole warp.  Writes
+// the class bytes only; compaction into lists is a separate pass.
+__global__ void __launch_bounds__(kBuildWarps * 32) classify_kernel(BuildArgs a) {
   __shared__ int32_t s_arg[kBuildWarps][FA_MAX_MASK_NODES];
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int64_t row = (int64_t)blockIdx.x * kBuildWarps + warp;  // (bm, hm, I)
-  if (row >= (int64_t)a.Bm * a.Hm * a.nq) return;
+  const int nchunk = (a.nkv + 31) / 32;
+  const int64_t wid = (int64_t)blockIdx.x * kBuildWarps + warp;
+  if (wid >= (int64_t)a.Bm * a.Hm * a.nq * nchunk) return;
+  const int64_t row = wid / nchunk;  // (bm, hm, I)
+  const int c0 = (int)(wid % nchunk) * 32;
   const int I = (int)(row % a.nq);
   const int bm = (int)(row / ((int64_t)a.Hm * a.nq));
   if (lane < a.mask.n) s_arg[warp][lane] = node_arg(a.mask, lane, bm);
@@ -111,113 +140,116 @@ __global__ void __launch_bounds__(kBuildWarps * 32) classify_rows_kernel(BuildAr
   const int32_t* arg = s_arg[warp];
   const int tmax = max(a.nq, a.nkv);
   const int32_t* doc = a.mask.has_doc ? a.mask.doc + (int64_t)bm * a.mask.doc_len : nullptr;
+  const bool doc_vec = a.mask.doc_vec_ok != 0;
 
   const int64_t i0 = (int64_t)I * a.block;
   const int64_t i1 = min(i0 + a.block, a.q_len) - 1;
-  int q_mn = 0, q_mx = 0;
-  if (a.mask.has_doc) {
-    const int32_t* s = a.summary + (((int64_t)bm * 2 + 0) * tmax + I) * 2;
-    q_mn = s[0];
-    q_mx = s[1];
+  int q_mn = 0, q_mx = 0, q_run = 0;
+  if (doc) {
+    const int32_t* sm = a.summary + (((int64_t)bm * 2 + 0) * tmax + I) * 4;
+    q_mn = sm[0];
+    q_mx = sm[1];
+    q_run = sm[2];
   }
-  const int64_t base = row * a.nkv;
-  int n_part = 0, n_full = 0;
-  for (int c0 = 0; c0 < a.nkv; c0 += 32) {
-    const int J = c0 + lane;
-    const bool valid = J < a.nkv;
-    int cls = 0;
-    int k3 = K_NONE;
-    if (valid) {
-      const int64_t j0 = (int64_t)J * a.block;
-      const int64_t j1 = min(j0 + a.block, a.kv_len) - 1;
-      int k_mn = 0, k_mx = 0;
-      if (a.mask.has_doc) {
-        const int32_t* s = a.summary + (((int64_t)bm * 2 + 1) * tmax + J) * 2;
-        k_mn = s[0];
-        k_mx = s[1];
-      }
-      k3 = program_interval(a.mask, arg, i0, i1, j0, j1, q_mn, q_mx, k_mn, k_mx);
-      cls = (k3 == K_ALL) ? 2 : 0;
+  const int J = c0 + lane;
+  const bool valid = J < a.nkv;
+  int cls = 0, k3 = K_NONE;
+  if (valid) {
+    const int64_t j0 = (int64_t)J * a.block;
+    const int64_t j1 = min(j0 + a.block, a.kv_len) - 1;
+    int k_mn = 0, k_mx = 0, k_run = 0;
+    if (doc) {
+      const int32_t* sm = a.summary + (((int64_t)bm * 2 + 1) * tmax + J) * 4;
+      k_mn = sm[0];
+      k_mx = sm[1];
+      k_run = sm[2];
     }
-    // Settle undecided tiles exactly, one at a time with the whole warp.
-    uint32_t undecided = __ballot_sync(0xffffffffu, valid && k3 == K_SOME);
-    while (undecided) {
-      const int t = __ffs(undecided) - 1;
-      undecided &= undecided - 1;
-      const int Jt = c0 + t;
-      const int64_t j0 = (int64_t)Jt * a.block;
-      const int64_t j1 = min(j0 + a.block, a.kv_len) - 1;
-      const int64_t rows = i1 - i0 + 1, cols = j1 - j0 + 1;
-      long long cnt = 0;
-      for (int64_t r = lane; r < rows; r += 32) {
-        const int64_t i = i0 + r;
-        const int32_t doc_i = doc ? __ldg(doc + i) : 0;
-        for (int64_t jc = j0; jc <= j1; jc += 32) {
-          auto eq = [&]() {
-            uint32_t w = 0;
+    k3 = program_interval(a.mask, arg, i0, i1, j0, j1, q_mn, q_mx, q_run, k_mn, k_mx, k_run);
+    cls = (k3 == K_ALL) ? 2 : (k3 == K_PART ? 1 : 0);
+  }
+  uint32_t undecided = __ballot_sync(0xffffffffu, valid && k3 == K_SOME);
+  while (undecided) {
+    const int t = __ffs(undecided) - 1;
+    undecided &= undecided - 1;
+    const int64_t j0 = (int64_t)(c0 + t) * a.block;
+    const int64_t j1 = min(j0 + a.block, a.kv_len) - 1;
+    const int64_t rows = i1 - i0 + 1, cols = j1 - j0 + 1;
+    int cnt = 0;
+    for (int64_t r = lane; r < rows; r += 32) {
+      const int64_t i = i0 + r;
+      const int32_t doc_i = doc ? __ldg(doc + i) : 0;
+      for (int64_t jc = j0; jc <= j1; jc += 32) {
+        auto eq = [&]() {
+          uint32_t w = 0;
+          if (doc_vec && jc + 32 <= j1 + 1) {
+            const int4* dv = reinterpret_cast<const int4*>(doc + jc);  // same addresses in every lane
+#pragma unroll
+            for (int q4 = 0; q4 < 8; ++q4) {
+              const int4 d = __ldg(dv + q4);
+              w |= (uint32_t)(d.x == doc_i) << (4 * q4) | (uint32_t)(d.y == doc_i) << (4 * q4 + 1) |
+                   (uint32_t)(d.z == doc_i) << (4 * q4 + 2) | (uint32_t)(d.w == doc_i) << (4 * q4 + 3);
+            }
+          } else {
             const int64_t jn = min(jc + 32, j1 + 1);
             for (int64_t j = jc; j < jn; ++j) w |= (uint32_t)(__ldg(doc + j) == doc_i) << (uint32_t)(j - jc);
-            return w;
-          };
-          const uint32_t w = mask_word(a.mask, arg, i, jc, eq) & low_bits(j1 + 1 - jc);
-          cnt += __popc(w);
-        }
+          }
+          return w;
+        };
+        cnt += __popc(mask_word_rolled(a.mask, arg, i, jc, eq) & low_bits(j1 + 1 - jc));
       }
-      // warp sum (counts fit in 32 bits: at most 128 * 128 per tile)
-      const int total = __reduce_add_sync(0xffffffffu, (unsigned)cnt);
-      const int c = (total == 0) ? 0 : ((int64_t)total == rows * cols ? 2 : 1);
-      if (lane == t) cls = c;
     }
-    if (valid) a.tile_class[base + J] = (uint8_t)cls;
-    const uint32_t pb = __ballot_sync(0xffffffffu, cls == 1);
-    const uint32_t fb = __ballot_sync(0xffffffffu, cls == 2);
-    const uint32_t lt = (1u << lane) - 1u;
-    if (cls == 1) a.kv_idx[base + n_part + __popc(pb & lt)] = J;
-    if (cls == 2) a.full_idx[base + n_full + __popc(fb & lt)] = J;
-    n_part += __popc(pb);
-    n_full += __popc(fb);
+    const int total = (int)__reduce_add_sync(0xffffffffu, (unsigned)cnt);
+    const int c = (total == 0) ? 0 : ((int64_t)total == rows * cols ? 2 : 1);
+    if (lane == t) cls = c;
   }
-  for (int k = n_part + lane; k < a.nkv; k += 32) a.kv_idx[base + k] = 0;
-  for (int k = n_full + lane; k < a.nkv; k += 32) a.full_idx[base + k] = 0;
-  if (lane == 0) {
-    a.kv_num[row] = n_part;
-    a.full_num[row] = n_full;
-  }
+  if (valid) a.tile_class[row * a.nkv + J] = (uint8_t)cls;
 }
 
-__global__ void __launch_bounds__(kBuildWarps * 32) classify_cols_kernel(BuildArgs a) {
+// Compaction: warps [0, rows) build the per-row lists, the next [0, cols)
+// warps the per-column lists, both with ballots over the class bytes.
+__global__ void __launch_bounds__(kBuildWarps * 32) compact_kernel(BuildArgs a) {
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int64_t col = (int64_t)blockIdx.x * kBuildWarps + warp;  // (bm, hm, J)
-  if (col >= (int64_t)a.Bm * a.Hm * a.nkv) return;
-  const int J = (int)(col % a.nkv);
-  const int64_t bmhm = col / a.nkv;
-  const uint8_t* cls_base = a.tile_class + bmhm * a.nq * a.nkv + J;
-  const int64_t base = col * a.nq;
+  const int64_t wid = (int64_t)blockIdx.x * kBuildWarps + warp;
+  const int64_t rows = (int64_t)a.Bm * a.Hm * a.nq, cols = (int64_t)a.Bm * a.Hm * a.nkv;
+  if (wid >= rows + cols) return;
+  const bool by_row = wid < rows;
+  const int64_t id = by_row ? wid : wid - rows;
+  const int n = by_row ? a.nkv : a.nq;                    // list length
+  const int64_t stride = by_row ? 1 : a.nkv;              // class-byte stride along the list
+  const uint8_t* cls_base = by_row ? a.tile_class + id * a.nkv
+                                   : a.tile_class + (id / a.nkv) * a.nq * a.nkv + (id % a.nkv);
+  int32_t* part_idx = (by_row ? a.kv_idx : a.q_idx) + id * n;
+  int32_t* full_idx = (by_row ? a.full_idx : a.full_q_idx) + id * n;
   int n_part = 0, n_full = 0;
-  for (int c0 = 0; c0 < a.nq; c0 += 32) {
-    const int I = c0 + lane;
-    const int cls = (I < a.nq) ? cls_base[(int64_t)I * a.nkv] : 0;
+  for (int c0 = 0; c0 < n; c0 += 32) {
+    const int x = c0 + lane;
+    const int cls = (x < n) ? cls_base[(int64_t)x * stride] : 0;
     const uint32_t pb = __ballot_sync(0xffffffffu, cls == 1);
     const uint32_t fb = __ballot_sync(0xffffffffu, cls == 2);
     const uint32_t lt = (1u << lane) - 1u;
-    if (cls == 1) a.q_idx[base + n_part + __popc(pb & lt)] = I;
-    if (cls == 2) a.full_q_idx[base + n_full + __popc(fb & lt)] = I;
+    if (cls == 1) part_idx[n_part + __popc(pb & lt)] = x;
+    if (cls == 2) full_idx[n_full + __popc(fb & lt)] = x;
     n_part += __popc(pb);
     n_full += __popc(fb);
   }
-  for (int k = n_part + lane; k < a.nq; k += 32) a.q_idx[base + k] = 0;
-  for (int k = n_full + lane; k < a.nq; k += 32) a.full_q_idx[base + k] = 0;
+  for (int k = n_part + lane; k < n; k += 32) part_idx[k] = 0;
+  for (int k = n_full + lane; k < n; k += 32) full_idx[k] = 0;
   if (lane == 0) {
-    a.q_num[col] = n_part;
-    a.full_q_num[col] = n_full;
+    (by_row ? a.kv_num : a.q_num)[id] = n_part;
+    (by_row ? a.full_num : a.full_q_num)[id] = n_full;
   }
 }
 
-// Counting sort of n items by descending (num + full_num); one block.
-// hist has max_count + 1 buckets in dynamic shared memory.
-__global__ void __launch_bounds__(1024) order_kernel(const int32_t* num, const int32_t* full_num, int32_t n,
-                                                     int32_t max_count, int32_t* order) {
+// Counting sort by descending (num + full_num): block 0 orders the rows,
+// block 1 the columns.  hist has max(nq, nkv) + 1 buckets in shared memory.
+__global__ void __launch_bounds__(1024) order_kernel(BuildArgs a) {
   extern __shared__ int32_t hist[];
+  const bool rows = blockIdx.x == 0;
+  const int32_t* num = rows ? a.kv_num : a.q_num;
+  const int32_t* full_num = rows ? a.full_num : a.full_q_num;
+  int32_t* order = rows ? a.row_order : a.col_order;
+  const int n = rows ? a.Bm * a.Hm * a.nq : a.Bm * a.Hm * a.nkv;
+  const int max_count = rows ? a.nkv : a.nq;
   const int nb = max_count + 1;
   for (int k = threadIdx.x; k < nb; k += blockDim.x) hist[k] = 0;
   __syncthreads();
@@ -226,12 +258,20 @@ __global__ void __launch_bounds__(1024) order_kernel(const int32_t* num, const i
     atomicAdd(&hist[max_count - c], 1);
   }
   __syncthreads();
-  if (threadIdx.x == 0) {
-    int run = 0;
-    for (int k = 0; k < nb; ++k) {
-      const int h = hist[k];
-      hist[k] = run;
-      run += h;
+  // exclusive scan, one warp
+  if (threadIdx.x < 32) {
+    int carry = 0;
+    for (int base = 0; base < nb; base += 32) {
+      const int k = base + threadIdx.x;
+      const int h = (k < nb) ? hist[k] : 0;
+      int incl = h;
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, d);
+        if ((int)threadIdx.x >= d) incl += y;
+      }
+      if (k < nb) hist[k] = carry + incl - h;
+      carry += __shfl_sync(0xffffffffu, incl, 31);
     }
   }
   __syncthreads();
@@ -241,23 +281,14 @@ __global__ void __launch_bounds__(1024) order_kernel(const int32_t* num, const i
   }
 }
 
-__global__ void identity_order_kernel(int32_t n, int32_t* order) {
+__global__ void identity_order_kernel(BuildArgs a) {
+  const int64_t rows = (int64_t)a.Bm * a.Hm * a.nq, cols = (int64_t)a.Bm * a.Hm * a.nkv;
   const int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (r < n) order[r] = (int32_t)r;
+  if (r < rows) a.row_order[r] = (int32_t)r;
+  else if (r < rows + cols) a.col_order[r - rows] = (int32_t)(r - rows);
 }
 
 constexpr int kMaxSortBuckets = 12 * 1024;  // 48 KB of shared memory
-
-cudaError_t launch_order(const int32_t* num, const int32_t* full_num, int64_t n, int32_t max_count, int32_t* order,
-                         cudaStream_t stream) {
-  if (max_count + 1 <= kMaxSortBuckets) {
-    order_kernel<<<1, 1024, (size_t)(max_count + 1) * sizeof(int32_t), stream>>>(num, full_num, (int32_t)n,
-                                                                                max_count, order);
-  } else {
-    identity_order_kernel<<<(unsigned)((n + 255) / 256), 256, 0, stream>>>((int32_t)n, order);
-  }
-  return cudaGetLastError();
-}
 
 }  // namespace
 
@@ -269,13 +300,14 @@ cudaError_t launch_build(const BuildArgs& a, cudaStream_t stream) {
   }
   const int64_t rows = (int64_t)a.Bm * a.Hm * a.nq;
   const int64_t cols = (int64_t)a.Bm * a.Hm * a.nkv;
-  classify_rows_kernel<<<(unsigned)((rows + kBuildWarps - 1) / kBuildWarps), kBuildWarps * 32, 0, stream>>>(a);
-  classify_cols_kernel<<<(unsigned)((cols + kBuildWarps - 1) / kBuildWarps), kBuildWarps * 32, 0, stream>>>(a);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  e = launch_order(a.kv_num, a.full_num, rows, a.nkv, a.row_order, stream);
-  if (e != cudaSuccess) return e;
-  return launch_order(a.q_num, a.full_q_num, cols, a.nq, a.col_order, stream);
+  const int64_t cwarps = rows * ((a.nkv + 31) / 32);
+  classify_kernel<<<(unsigned)((cwarps + kBuildWarps - 1) / kBuildWarps), kBuildWarps * 32, 0, stream>>>(a);
+  compact_kernel<<<(unsigned)((rows + cols + kBuildWarps - 1) / kBuildWarps), kBuildWarps * 32, 0, stream>>>(a);
+  if (tmax + 1 <= kMaxSortBuckets)
+    order_kernel<<<2, 1024, (size_t)(tmax + 1) * sizeof(int32_t), stream>>>(a);
+  else
+    identity_order_kernel<<<(unsigned)((rows + cols + 255) / 256), 256, 0, stream>>>(a);
+  return cudaGetLastError();
 }
 
 }  // namespace fa

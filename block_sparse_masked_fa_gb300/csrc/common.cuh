@@ -108,4 +108,36 @@ __device__ __forceinline__ uint32_t mask_word_rolled(const DevMask& m, const int
   return s0;
 }
 
+// Transposed visibility word: key column j fixed, query rows i0 .. i0+31
+// (bit c is pair (i0 + c, j)); used where a thread owns a key row.
+//  eq_doc()  word of (doc[i0 + c] == doc[j]) for c = 0..31
+template <class EqDoc>
+__device__ __forceinline__ uint32_t mask_word_t_rolled(const DevMask& m, const int32_t* arg, int64_t j, int64_t i0,
+                                                       EqDoc eq_doc) {
+  uint32_t s0 = 0, s1 = 0, s2 = 0, s3 = 0, s4 = 0, s5 = 0, s6 = 0, s7 = 0;
+#pragma unroll 1
+  for (int k = 0; k < m.n; ++k) {
+    const int op = m.op[k];
+    if (op == FA_M_AND || op == FA_M_OR) {
+      s0 = (op == FA_M_AND) ? (s1 & s0) : (s1 | s0);
+      s1 = s2; s2 = s3; s3 = s4; s4 = s5; s5 = s6; s6 = s7; s7 = 0;
+    } else {
+      uint32_t w;
+      if (op == FA_M_CAUSAL) {
+        w = ~low_bits(j - i0);                              // i >= j
+      } else if (op == FA_M_WINDOW) {
+        w = low_bits(j + (int64_t)arg[k] - i0);             // i < j + W
+      } else if (op == FA_M_SINK || op == FA_M_PREFIX) {
+        w = (j < (int64_t)arg[k]) ? 0xffffffffu : 0u;       // j < n
+      } else if (op == FA_M_SAME_DOC) {
+        w = eq_doc();
+      } else {
+        w = 0xffffffffu;
+      }
+      s7 = s6; s6 = s5; s5 = s4; s4 = s3; s3 = s2; s2 = s1; s1 = s0; s0 = w;
+    }
+  }
+  return s0;
+}
+
 }  // namespace fa

@@ -15,7 +15,7 @@ struct BuildArgs {
   int32_t *q_num, *q_idx, *full_q_num, *full_q_idx;
   int32_t *row_order, *col_order;
   uint8_t* tile_class;
-  int32_t* summary;  // [Bm][2][max(nq, nkv)][2]: doc-id min / max per query and key tile
+  int32_t* summary;  // [Bm][2][max(nq, nkv)][4]: doc-id min, max, step-0/1 flag per query / key tile
   uint32_t* status;
 };
 

@@ -1,0 +1,153 @@
+"""Backward parity: dq, dk, dv of the CUDA path (through the C ABI) against
+the fp64 oracle's gradients of L = sum(out * dO) on the same seeded inputs.
+
+Bar: max |g - g_ref| / max |g_ref| <= 5e-2 for each gradient (written once in
+fa_testutil).  The CUDA backward consumes the CUDA forward's out and LSE, as a
+training step would.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from fa_testutil import (check_grad, device_nodes, head64, oracle_program, oracle_score, score_arg)
+from synth import WORKLOADS, MaskProgram, make_alibi_slopes, make_doc_ids, make_qkv, make_workload_inputs
+
+pytestmark = pytest.mark.gpu
+
+fa = pytest.importorskip("block_sparse_masked_fa_gb300")
+
+P = lambda *n: MaskProgram(tuple(n))
+
+
+def run_fa(inp, mask, Bm=1, prefix=None, score=None, window_tensor=None):
+    q, k, v, do = (inp[n].cuda() for n in ("q", "k", "v", "do"))
+    S, kv_len = q.shape[2], k.shape[2]
+    bm = fa.fa_create_block_mask(device_nodes(mask, inp.get("docs"), prefix, window_tensor), Bm, 1, S, kv_len, 128)
+    out, lse = fa.fa_forward(q, k, v, bm, score=score)
+    dq, dk, dv = fa.fa_backward(q, k, v, out, lse, do, bm, score=score)
+    torch.cuda.synchronize()
+    assert fa.fa_get_status(bm) == 0
+    return tuple(t.float().cpu().numpy() for t in (dq, dk, dv))
+
+
+def oracle_grads(inp, mask, b, h, score, Bm=1, prefix=None, rows=None, cols=None):
+    D = inp["q"].shape[-1]
+    prog = oracle_program(mask, inp.get("docs"), prefix, b, Bm)
+    dq, dk, dv, _, _ = oracle.backward_head(head64(inp["q"], b, h), head64(inp["k"], b, h), head64(inp["v"], b, h),
+                                            head64(inp["do"], b, h), prog, score, h, 1.0 / np.sqrt(D),
+                                            rows=rows, cols=cols)
+    return dq, dk, dv
+
+
+def check_all(got, ref, what):
+    for name, g, r in zip(("dq", "dk", "dv"), got, ref):
+        check_grad(g, r, f"{what} {name}")
+
+
+@pytest.mark.parametrize("wnum", [1, 2, 3, 4, 5])
+@pytest.mark.parametrize("S", [1000, 1280])
+def test_workload_recipe_reduced_size_all_elements(wnum, S):
+    w = WORKLOADS[wnum]
+    H = min(w.H, 2)
+    inp = make_workload_inputs(w, S=S, B=1, H=H, seed=8000 + wnum)
+    mask = w.mask.with_window(256) if w.windows else w.mask
+    got = run_fa(inp, mask, score=score_arg(w.score, inp["slopes"], inp["softcap"]))
+    for h in range(H):
+        ref = oracle_grads(inp, mask, 0, h, oracle_score(w.score, inp["slopes"], inp["softcap"]))
+        check_all([g[0, h] for g in got], ref, f"w{wnum} S{S} h{h}")
+
+
+def _sample(S, rng, n=40):
+    rows = set(rng.integers(0, S, size=n).tolist())
+    rows.update([0, S - 1, 127, 128])
+    return np.array(sorted(rows), dtype=np.int64)
+
+
+@pytest.mark.parametrize("wnum", [1, 2, 3, 4, 5])
+def test_workload_full_size_sampled(wnum):
+    """Full workload shape; dq on sampled rows, dk / dv on sampled columns of two heads."""
+    w = WORKLOADS[wnum]
+    inp = make_workload_inputs(w)
+    mask, W = w.mask, None
+    if w.windows:
+        W = torch.tensor([1024], dtype=torch.int32, device="cuda")
+        mask = w.mask.with_window(1024)
+    got = run_fa(inp, mask, score=score_arg(w.score, inp["slopes"], inp["softcap"]), window_tensor=W)
+    rng = np.random.default_rng(100 + wnum)
+    for b, h in [(0, 0), (w.B - 1, w.H - 1)]:
+        rows = None if w.S <= 512 else _sample(w.S, rng)
+        cols = None if w.S <= 512 else _sample(w.S, rng)
+        ref = oracle_grads(inp, mask, b, h, oracle_score(w.score, inp["slopes"], inp["softcap"]), rows=rows, cols=cols)
+        dq, dk, dv = (g[b, h] for g in got)
+        if rows is not None:
+            dq, dk, dv = dq[rows], dk[cols], dv[cols]
+        check_all((dq, dk, dv), ref, f"w{wnum} b{b} h{h}")
+
+
+def _inputs(B, H, S, D, seed, kv_len=None, docs=None):
+    q, k, v, do = make_qkv(B, H, S, D, seed, kv_len=kv_len)
+    return {"q": q, "k": k, "v": v, "do": do, "docs": docs}
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_diagonal_only(D):
+    """Only the diagonal visible: P = 1, so dv = dO and dq = dk = 0."""
+    inp = _inputs(1, 2, 300, D, 21)
+    dq, dk, dv = run_fa(inp, P(("causal",), ("window", 1), ("and",)))
+    np.testing.assert_allclose(dv, inp["do"].float().numpy(), atol=1e-2)
+    assert np.abs(dq).max() < 1e-2 and np.abs(dk).max() < 1e-2
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_fully_masked_rows_and_columns(D):
+    """same_doc & sink(10): documents after the first see nothing, so their dq
+    rows are zero, and only the 10 sink keys get dk / dv."""
+    S = 640
+    docs = np.repeat(np.arange(5), 128).astype(np.int32)[None]
+    docs[0, :200] = 0
+    inp = _inputs(1, 2, S, D, 22, docs=docs)
+    mask = P(("same_doc",), ("sink", 10), ("and",))
+    dq, dk, dv = run_fa(inp, mask)
+    assert np.all(dq[:, :, 200:] == 0)
+    assert np.all(dk[:, :, 10:] == 0) and np.all(dv[:, :, 10:] == 0)
+    for h in range(2):
+        check_all([g[0, h] for g in (dq, dk, dv)], oracle_grads(inp, mask, 0, h, ("none",)), f"h{h}")
+
+
+def test_everything_masked_gives_zero_gradients():
+    inp = _inputs(1, 1, 256, 64, 23)
+    dq, dk, dv = run_fa(inp, P(("causal",), ("window", 0), ("and",)))
+    assert not dq.any() and not dk.any() and not dv.any()
+
+
+@pytest.mark.parametrize("S", [1, 77, 129])
+def test_tiny_sizes(S):
+    inp = _inputs(1, 2, S, 128, 24)
+    mask = P(("causal",))
+    got = run_fa(inp, mask)
+    for h in range(2):
+        check_all([g[0, h] for g in got], oracle_grads(inp, mask, 0, h, ("none",)), f"S{S} h{h}")
+
+
+@pytest.mark.parametrize("q_len,kv_len", [(256, 1000), (1000, 300)])
+def test_cross_lengths(q_len, kv_len):
+    inp = _inputs(1, 2, q_len, 64, 25, kv_len=kv_len)
+    mask = P(("causal",), ("sink", 5), ("or",))
+    got = run_fa(inp, mask, score=("softcap", [20.0]))
+    for h in range(2):
+        check_all([g[0, h] for g in got], oracle_grads(inp, mask, 0, h, ("softcap", 20.0)), f"{q_len}x{kv_len}")
+
+
+def test_batch_broadcast_docs_prefix_alibi():
+    S = 768
+    docs = make_doc_ids(("geometric", 150.0), S, 26, batch=2)
+    inp = _inputs(2, 2, S, 128, 27, docs=docs)
+    prefix = np.array([90, 260], dtype=np.int32)
+    mask = P(("causal",), ("prefix",), ("or",), ("same_doc",), ("and",))
+    sl = make_alibi_slopes(2)
+    got = run_fa(inp, mask, Bm=2, prefix=prefix, score=("alibi", torch.as_tensor(sl)))
+    for b in range(2):
+        for h in range(2):
+            ref = oracle_grads(inp, mask, b, h, ("alibi", sl), Bm=2, prefix=prefix)
+            check_all([g[b, h] for g in got], ref, f"b{b} h{h}")
