@@ -10,6 +10,7 @@ from .binding import (  # noqa: F401
     BlockMask,
     FaError,
     fa_backward,
+    fa_backward_noalloc,
     fa_backward_workspace_bytes,
     fa_block_mask_bytes,
     fa_block_mask_summary,

@@ -77,17 +77,23 @@ _lib.fa_backward.argtypes = [_c.c_void_p] * 6 + [_c.c_int32, _c.c_int32, _c.c_in
                                                  _c.POINTER(BlockMaskStruct), _c.POINTER(ScoreSpec), _c.c_float,
                                                  _c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_void_p,
                                                  _c.c_size_t, _c.c_void_p]
+_lib.fa_backward_noalloc.argtypes = [_c.c_void_p] * 6 + [_c.c_int32, _c.c_int32, _c.c_int64, _c.c_int64,
+                                                         _c.c_int32, _c.POINTER(BlockMaskStruct),
+                                                         _c.POINTER(ScoreSpec), _c.c_float, _c.c_void_p,
+                                                         _c.c_void_p, _c.c_void_p, _c.c_void_p]
 _lib.fa_get_status.argtypes = [_c.POINTER(BlockMaskStruct), _c.c_int32, _c.c_void_p]
 _lib.fa_block_mask_summary.argtypes = [_c.POINTER(BlockMaskStruct), _c.POINTER(_c.c_int64 * 3), _c.c_void_p]
 _lib.fa_status_string.argtypes = [_c.c_int]
 _lib.fa_status_string.restype = _c.c_char_p
 for _f in (_lib.fa_block_mask_bytes, _lib.fa_create_block_mask, _lib.fa_forward, _lib.fa_backward_workspace_bytes,
-           _lib.fa_backward, _lib.fa_get_status, _lib.fa_block_mask_summary):
+           _lib.fa_backward, _lib.fa_backward_noalloc, _lib.fa_get_status, _lib.fa_block_mask_summary):
     _f.restype = _c.c_int
 _lib.fa_version.restype = _c.c_int32
 
 EXPORTED = ("fa_block_mask_bytes", "fa_create_block_mask", "fa_forward", "fa_backward_workspace_bytes",
-            "fa_backward", "fa_get_status", "fa_block_mask_summary", "fa_status_string", "fa_version")
+            "fa_backward", "fa_backward_noalloc", "fa_get_status", "fa_block_mask_summary", "fa_status_string",
+            "fa_version")
+NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
 def _check(code: int, where: str):
@@ -260,6 +266,23 @@ def fa_backward(q, k, v, out, lse, dout, block_mask: BlockMask, score=None, scal
     _check(_lib.fa_backward(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout), B, H, q_len, kv_len, D,
                             ctypes.byref(block_mask.struct), ctypes.byref(sspec), float(scale), _ptr(dq), _ptr(dk),
                             _ptr(dv), _ptr(workspace), workspace.numel(), _stream(stream)), "fa_backward")
+    return dq, dk, dv
+
+
+def fa_backward_noalloc(q, k, v, out, lse, dout, block_mask: BlockMask, score=None, scale: float = 0.0,
+                        dq=None, dk=None, dv=None, stream=None):
+    """fa_backward without a workspace: for callers that cannot allocate device
+    memory at call time (the library's static scratch holds the fp32 dq
+    accumulator; see include/fa.h for the size limit and the sharing rules)."""
+    B, H, q_len, D = q.shape
+    kv_len = k.shape[2]
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    sspec, keep = _score(score)
+    _check(_lib.fa_backward_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout), B, H, q_len, kv_len,
+                                    D, ctypes.byref(block_mask.struct), ctypes.byref(sspec), float(scale), _ptr(dq),
+                                    _ptr(dk), _ptr(dv), _stream(stream)), "fa_backward_noalloc")
     return dq, dk, dv
 
 

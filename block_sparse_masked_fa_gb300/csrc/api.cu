@@ -352,6 +352,45 @@ fa_status fa_backward(const void* q, const void* k, const void* v, const void* o
   return cuda_status(e);
 }
 
+fa_status fa_backward_noalloc(const void* q, const void* k, const void* v, const void* out, const float* lse,
+                              const void* dout, int32_t B, int32_t H, int64_t q_len, int64_t kv_len, int32_t D,
+                              const fa_block_mask* bm, const fa_score_spec* score, float scale, void* dq, void* dk,
+                              void* dv, cudaStream_t stream) {
+  if (!q || !k || !v || !out || !lse || !dout || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(dout) || !aligned16(dq) ||
+      !aligned16(dk) || !aligned16(dv) || !aligned4(lse))
+    return FA_ERR_ALIGNMENT;
+  fa_status st = check_attn(B, H, q_len, kv_len, D, bm, score, &scale);
+  if (st != FA_OK) return st;
+  size_t need = 0;
+  st = fa_backward_workspace_bytes(B, H, q_len, D, &need);
+  if (st != FA_OK) return st;
+  if (need > (size_t)FA_NOALLOC_SCRATCH_BYTES) return FA_ERR_WORKSPACE;  // too large for the static scratch
+  DevMask dm;
+  st = check_mask(&bm->spec, q_len, kv_len, &dm);
+  if (st != FA_OK) return st;
+  void* scratch = nullptr;
+  if (noalloc_scratch(&scratch) != cudaSuccess) return FA_ERR_CUDA;
+  const AttnArgs a = attn_args(B, H, q_len, kv_len, D, bm, score, scale, dm);
+  const size_t rows = (size_t)B * H * (size_t)q_len;
+  BwdTensors t;
+  t.q = q;
+  t.k = k;
+  t.v = v;
+  t.out = out;
+  t.dout = dout;
+  t.lse = lse;
+  t.dq = dq;
+  t.dk = dk;
+  t.dv = dv;
+  t.dq_acc = static_cast<float*>(scratch);
+  t.delta = reinterpret_cast<float*>(static_cast<uint8_t*>(scratch) + align_up(rows * D * 4));
+  bool enc_failed = false;
+  const cudaError_t e = launch_backward(a, t, stream, &enc_failed);
+  if (enc_failed) return FA_ERR_CUDA;
+  return cuda_status(e);
+}
+
 fa_status fa_get_status(const fa_block_mask* bm, int32_t clear, cudaStream_t stream) {
   if (bm == nullptr || bm->status == nullptr) return FA_ERR_INVALID_ARG;
   if (cudaStreamSynchronize(stream) != cudaSuccess) return FA_ERR_CUDA;

@@ -28,6 +28,8 @@
 #include <cfloat>
 #include <cmath>
 
+#include <mutex>
+
 #include <cuda_bf16.h>
 
 #include "internal.h"
@@ -525,7 +527,35 @@ cudaError_t launch_bwd_t(const AttnArgs& a, const BwdTensors& t, cudaStream_t st
   return cudaGetLastError();
 }
 
+// Scratch of fa_backward_noalloc: the fp32 dq accumulator and Delta, in
+// library-owned device memory instead of a caller workspace.  Every call
+// shares it; bwd_pre_kernel rewrites all of it that a call uses (zeroed dq
+// accumulator, fresh Delta) before the main kernel reads it.
+__device__ __align__(256) uint8_t g_noalloc_scratch[FA_NOALLOC_SCRATCH_BYTES];
+
 }  // namespace
+
+cudaError_t noalloc_scratch(void** ptr) {
+  // Device address of the scratch array on the current device, looked up once
+  // per device with that device current.  (In host code the array's name is
+  // only a stand-in for the symbol, never a device address.)
+  constexpr int kMaxDevices = 64;
+  static std::mutex mu;
+  static void* addr[kMaxDevices] = {};
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (addr[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return e;
+    addr[dev] = p;
+  }
+  *ptr = addr[dev];
+  return cudaSuccess;
+}
 
 cudaError_t launch_backward(const AttnArgs& a, const BwdTensors& t, cudaStream_t stream, bool* enc_failed) {
   *enc_failed = false;

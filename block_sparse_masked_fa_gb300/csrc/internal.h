@@ -54,6 +54,9 @@ struct BwdTensors {
 cudaError_t launch_forward(const AttnArgs& a, const FwdTensors& t, cudaStream_t stream, bool* enc_failed);
 cudaError_t launch_backward(const AttnArgs& a, const BwdTensors& t, cudaStream_t stream, bool* enc_failed);
 
+// Device address (current device) of the library-owned scratch of fa_backward_noalloc.
+cudaError_t noalloc_scratch(void** ptr);
+
 // Tensor-map encoding through the driver entry point (no libcuda link).
 bool encode_tmap_3d(CUtensorMap* map, CUtensorMapDataType dtype, int elem_bytes, const void* base, uint64_t d0,
                     uint64_t d1, uint64_t d2, uint32_t box0, uint32_t box1, CUtensorMapSwizzle swizzle);

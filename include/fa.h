@@ -207,6 +207,38 @@ fa_status fa_backward(const void* q, const void* k, const void* v, const void* o
                       const fa_block_mask* bm, const fa_score_spec* score, float scale, void* dq, void* dk,
                       void* dv, void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
+/* Backward without a caller-provided workspace.  The pages have no
+ * counterpart: this entry point exists for callers that cannot allocate
+ * device memory when they call the backward -- for example code running
+ * inside a framework that reserves the GPU's memory for its own pool at start
+ * up and allows no further cudaMalloc, or a latency-critical path that cannot
+ * afford the implicit device synchronisation of an allocation.
+ *
+ * It computes exactly what fa_backward computes, with the same arguments
+ * except the workspace: the fp32 dq accumulator and the per-row
+ * sum(dO * out) live in a static device array of FA_NOALLOC_SCRATCH_BYTES
+ * owned by the library.  Every GPU that loads the library holds that array
+ * until the process exits.  The caller still passes (and owns) every input
+ * and output.  The call allocates nothing: no cudaMalloc, cudaFree or
+ * allocating library routine.
+ *  - Size limit: returns FA_ERR_WORKSPACE, before any GPU work, when
+ *    fa_backward_workspace_bytes(B, H, q_len, D) exceeds
+ *    FA_NOALLOC_SCRATCH_BYTES (16 MiB: e.g. B*H*q_len up to 32,512 rows at
+ *    D = 128 or 64,527 rows at D = 64).
+ *  - Set-up: the first call on each device looks up the array's device address
+ *    (cudaGetSymbolAddress, with that device current) and caches it; make that
+ *    first call before any stream capture.
+ *  - Sharing: all calls on a device use the same array, which keeps the last
+ *    call's contents; each call re-initialises the part it uses.  Calls whose
+ *    GPU work overlaps (different streams, no ordering between them) race on
+ *    the array and give wrong gradients: order them on one stream or with
+ *    events. */
+#define FA_NOALLOC_SCRATCH_BYTES (16u << 20)
+fa_status fa_backward_noalloc(const void* q, const void* k, const void* v, const void* out, const float* lse,
+                              const void* dout, int32_t B, int32_t H, int64_t q_len, int64_t kv_len, int32_t D,
+                              const fa_block_mask* bm, const fa_score_spec* score, float scale, void* dq,
+                              void* dk, void* dv, cudaStream_t stream);
+
 /* Synchronises `stream`, reads the block mask's device status word and
  * returns FA_OK, FA_ERR_TIMEOUT or FA_ERR_DEVICE_CHECK.  clear != 0 resets the
  * word to 0. */
