@@ -44,28 +44,30 @@ template <int D>
 struct BwdCfg {
   static constexpr int NC = D / 64;
   static constexpr uint32_t TILE = 128u * D * 2u;  // one 128 x D bf16 tile
-  static constexpr int NS = (D == 64) ? 2 : 1;     // Q / dO stages
+  static constexpr int NQ = 2;                     // Q ring slots (with LSE / Delta)
+  static constexpr int NDO = (D == 64) ? 2 : 1;    // dO ring slots
   static constexpr uint32_t DS_BYTES = 128u * 128u * 2u;
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t T_S = 0, T_DP = 128, T_DV = 256, T_DK = 256 + D;
+  static constexpr int THREADS = 448;  // 8 key-row warps, 4 dq warps, producer, MMA
 };
 
 struct BwdCtl {
   uint64_t kv_full;
-  uint64_t q_full[2];
-  uint64_t q_empty[2];
+  uint64_t q_full[2], q_empty[2];
+  uint64_t do_full[2], do_empty[2];
   uint64_t s_full, p_full, dq_full, dq_free, acc_full, fin;
   uint32_t tmem;
   int abort;
   int32_t arg[FA_MAX_MASK_NODES];
-  float lse[2][128];    // LSE * log2(e) of the stage's query rows
-  float delta[2][128];  // Delta of the stage's query rows
+  float lse[2][128];    // LSE * log2(e) of the Q slot's query rows
+  float delta[2][128];  // Delta of the Q slot's query rows
 };
 
 template <int D>
 constexpr size_t bwd_smem_bytes() {
   using C = BwdCfg<D>;
-  return 1024 + (size_t)C::TILE * 2 + (size_t)C::TILE * 2 * C::NS + C::DS_BYTES + sizeof(BwdCtl);
+  return 1024 + (size_t)C::TILE * (2 + C::NQ + C::NDO) + C::DS_BYTES + sizeof(BwdCtl);
 }
 
 __device__ __forceinline__ void fail(const AttnArgs& p, BwdCtl* ctl) {
@@ -85,6 +87,10 @@ __device__ __forceinline__ float tanh_fast(float t) {
   return fmaf(-2.0f, r, 1.0f);
 }
 
+__device__ __forceinline__ void red_add_v4(float* p, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d) : "memory");
+}
+
 // Writes 32 bf16 values (16 packed words) of row r into a 128-byte-swizzled
 // [chunks][128 rows][64] tile at columns [32 c, 32 c + 32).
 __device__ __forceinline__ void store_row32(uint8_t* tile, int r, int c, const uint32_t (&w)[16]) {
@@ -98,7 +104,7 @@ __device__ __forceinline__ void store_row32(uint8_t* tile, int r, int c, const u
 }
 
 template <int D, int SCORE>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(448, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_dv,
@@ -109,11 +115,12 @@ __global__ void __launch_bounds__(320, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sK = smem;
   uint8_t* sV = sK + C::TILE;
-  uint8_t* sQ0 = sV + C::TILE;  // stage s: Q at sQ0 + 2 s TILE, dO right after it
-  uint8_t* sDS = sQ0 + 2 * C::NS * C::TILE;
+  uint8_t* sQ0 = sV + C::TILE;             // Q ring
+  uint8_t* sDO0 = sQ0 + C::NQ * C::TILE;   // dO ring
+  uint8_t* sDS = sDO0 + C::NDO * C::TILE;
   BwdCtl* ctl = reinterpret_cast<BwdCtl*>(sDS + C::DS_BYTES);
-  auto sQ = [&](int st) { return sQ0 + 2 * st * C::TILE; };
-  auto sDO = [&](int st) { return sQ0 + (2 * st + 1) * C::TILE; };
+  auto sQ = [&](int st) { return sQ0 + st * C::TILE; };
+  auto sDO = [&](int st) { return sDO0 + st * C::TILE; };
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
@@ -136,12 +143,14 @@ __global__ void __launch_bounds__(320, 1)
                  b_acc = smem_u32(&ctl->acc_full), b_fin = smem_u32(&ctl->fin);
   if (threadIdx.x == 0) {
     mbar_init(b_kv, 1);
-    for (int s = 0; s < C::NS; ++s) {
-      mbar_init(smem_u32(&ctl->q_full[s]), 32);  // the producer warp's 32 lanes (one with the byte count)
-      mbar_init(smem_u32(&ctl->q_empty[s]), 1);
+    for (int s2 = 0; s2 < 2; ++s2) {
+      mbar_init(smem_u32(&ctl->q_full[s2]), 32);  // the producer warp's 32 lanes (one with the byte count)
+      mbar_init(smem_u32(&ctl->q_empty[s2]), 1);
+      mbar_init(smem_u32(&ctl->do_full[s2]), 1);
+      mbar_init(smem_u32(&ctl->do_empty[s2]), 1);
     }
     mbar_init(b_s, 1);
-    mbar_init(b_p, 128);
+    mbar_init(b_p, 256);
     mbar_init(b_dq, 1);
     mbar_init(b_dqf, 128);
     mbar_init(b_acc, 1);
@@ -150,7 +159,7 @@ __global__ void __launch_bounds__(320, 1)
     fence_mbar_init();
   }
   if (threadIdx.x < p.mask.n) ctl->arg[threadIdx.x] = node_arg(p.mask, threadIdx.x, bm);
-  if (warp == 8) {
+  if (warp == 12) {
     tmem_alloc(smem_u32(&ctl->tmem), C::TMEM_COLS);
     tmem_relinquish();
   }
@@ -163,7 +172,7 @@ __global__ void __launch_bounds__(320, 1)
 
   auto tile_of = [&](int it) -> int { return it < n_full ? p.full_q_idx[list + it] : p.q_idx[list + it - n_full]; };
 
-  if (warp == 8) {
+  if (warp == 12) {
     // ------------------------------------------------------------ producer
     if (n > 0) {
       if (lane == 0) {
@@ -177,16 +186,17 @@ __global__ void __launch_bounds__(320, 1)
           tma_load_3d(smem_u32(sV + c * 16384), &tm_v, b_kv, c * 64, J * 128, bh);
         }
       }
-      int issued = 0;
+      int q_issued = 0, do_issued = 0;
       bool ok = true;
+      const int64_t base = (int64_t)bh * p.q_len;
       for (int it = 0; it < n; ++it) {
-        const int st = it % C::NS, use = it / C::NS;
-        if (use > 0 && !warp_wait(smem_u32(&ctl->q_empty[st]), (use - 1) & 1, &ctl->abort)) {
+        const int I = tile_of(it);
+        // Q slot, with the tile's LSE (log2 units) and Delta
+        const int qs = it % C::NQ, quse = it / C::NQ;
+        if (quse > 0 && !warp_wait(smem_u32(&ctl->q_empty[qs]), (quse - 1) & 1, &ctl->abort)) {
           ok = false;
           break;
         }
-        const int I = tile_of(it);
-        const int64_t base = (int64_t)bh * p.q_len;
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           const int r = lane + 32 * k;
@@ -196,30 +206,43 @@ __global__ void __launch_bounds__(320, 1)
             lv = __ldg(lse_g + base + row) * kLog2e;
             dv = __ldg(delta_g + base + row);
           }
-          ctl->lse[st][r] = lv;
-          ctl->delta[st][r] = dv;
+          ctl->lse[qs][r] = lv;
+          ctl->delta[qs][r] = dv;
         }
-        const uint32_t bar = smem_u32(&ctl->q_full[st]);
+        const uint32_t qbar = smem_u32(&ctl->q_full[qs]);
         if (lane == 0) {
-          mbar_arrive_expect_tx(bar, 2 * C::TILE);
-          for (int c = 0; c < C::NC; ++c) {
-            tma_load_3d(smem_u32(sQ(st) + c * 16384), &tm_q, bar, c * 64, I * 128, bh);
-            tma_load_3d(smem_u32(sDO(st) + c * 16384), &tm_do, bar, c * 64, I * 128, bh);
-          }
+          mbar_arrive_expect_tx(qbar, C::TILE);
+          for (int c = 0; c < C::NC; ++c)
+            tma_load_3d(smem_u32(sQ(qs) + c * 16384), &tm_q, qbar, c * 64, I * 128, bh);
         } else {
-          mbar_arrive(bar);
+          mbar_arrive(qbar);
         }
-        issued = it + 1;
+        q_issued = it + 1;
+        // dO slot
+        const int ds = it % C::NDO, duse = it / C::NDO;
+        if (duse > 0 && !warp_wait(smem_u32(&ctl->do_empty[ds]), (duse - 1) & 1, &ctl->abort)) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
+          const uint32_t dbar = smem_u32(&ctl->do_full[ds]);
+          mbar_arrive_expect_tx(dbar, C::TILE);
+          for (int c = 0; c < C::NC; ++c)
+            tma_load_3d(smem_u32(sDO(ds) + c * 16384), &tm_do, dbar, c * 64, I * 128, bh);
+        }
+        do_issued = it + 1;
       }
       if (!ok && lane == 0) fail(p, ctl);
       // drain: every copy this CTA started lands before it exits
       if (lane == 0) {
         mbar_wait(b_kv, 0, nullptr);
-        for (int it = max(0, issued - C::NS); it < issued; ++it)
-          mbar_wait(smem_u32(&ctl->q_full[it % C::NS]), (it / C::NS) & 1, nullptr);
+        for (int it = max(0, q_issued - C::NQ); it < q_issued; ++it)
+          mbar_wait(smem_u32(&ctl->q_full[it % C::NQ]), (it / C::NQ) & 1, nullptr);
+        for (int it = max(0, do_issued - C::NDO); it < do_issued; ++it)
+          mbar_wait(smem_u32(&ctl->do_full[it % C::NDO]), (it / C::NDO) & 1, nullptr);
       }
     }
-  } else if (warp == 9) {
+  } else if (warp == 13) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && n > 0) {
       constexpr uint32_t kIdKK = idesc_bf16(128, 128, false, false);  // S^T, dP^T
@@ -228,8 +251,21 @@ __global__ void __launch_bounds__(320, 1)
       const uint32_t k_base = smem_u32(sK), v_base = smem_u32(sV), ds_base = smem_u32(sDS);
       bool ok = mbar_wait(b_kv, 0, &ctl->abort);
       for (int it = 0; ok && it < n; ++it) {
-        const int st = it % C::NS;
-        if (!mbar_wait(smem_u32(&ctl->q_full[st]), (it / C::NS) & 1, &ctl->abort)) {
+        const int qs = it % C::NQ, ds = it % C::NDO;
+        if (!mbar_wait(smem_u32(&ctl->q_full[qs]), (it / C::NQ) & 1, &ctl->abort)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t q_base = smem_u32(sQ(qs)), do_base = smem_u32(sDO(ds));
+        // S^T = K Q^T: its columns held P^T of the last step, read by the dV MMA issued before
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;
+          mma_ss(tmem + C::T_S, sdesc_sw128(k_base + off, 16, 1024), sdesc_sw128(q_base + off, 16, 1024), kIdKK,
+                 kk > 0);
+        }
+        if (!mbar_wait(smem_u32(&ctl->do_full[ds]), (it / C::NDO) & 1, &ctl->abort)) {
           ok = false;
           break;
         }
@@ -238,13 +274,6 @@ __global__ void __launch_bounds__(320, 1)
           break;
         }
         tc_fence_after();
-        const uint32_t q_base = smem_u32(sQ(st)), do_base = smem_u32(sDO(st));
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;
-          mma_ss(tmem + C::T_S, sdesc_sw128(k_base + off, 16, 1024), sdesc_sw128(q_base + off, 16, 1024), kIdKK,
-                 kk > 0);
-        }
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;
@@ -257,10 +286,12 @@ __global__ void __launch_bounds__(320, 1)
           break;
         }
         tc_fence_after();
+        // dV += P^T dO; P^T of query columns [64 h, 64 h + 64) sits at TMEM columns [64 h, 64 h + 32)
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)  // dV += P^T dO
-          mma_ts(tmem + C::T_DV, tmem + C::T_S + kk * 8, sdesc_sw128(do_base + kk * 2048, 16384, 1024), kIdKM,
-                 (it > 0 || kk > 0));
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ts(tmem + C::T_DV, tmem + C::T_S + (kk / 4) * 64 + (kk % 4) * 8,
+                 sdesc_sw128(do_base + kk * 2048, 16384, 1024), kIdKM, (it > 0 || kk > 0));
+        mma_commit(smem_u32(&ctl->do_empty[ds]));
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)  // dK += dS^T Q
           mma_ss(tmem + C::T_DK, sdesc_sw128(ds_base + (kk / 4) * 16384 + (kk % 4) * 32, 16, 1024),
@@ -270,7 +301,7 @@ __global__ void __launch_bounds__(320, 1)
           mma_ss(tmem + C::T_DP, sdesc_sw128(ds_base + kk * 2048, 16384, 1024),
                  sdesc_sw128(k_base + kk * 2048, 16384, 1024), kIdMM, kk > 0);
         mma_commit(b_dq);
-        mma_commit(smem_u32(&ctl->q_empty[st]));
+        mma_commit(smem_u32(&ctl->q_empty[qs]));
       }
       if (ok)
         mma_commit(b_acc);
@@ -279,9 +310,9 @@ __global__ void __launch_bounds__(320, 1)
       mma_commit(b_fin);
       mbar_wait(b_fin, 0, nullptr);
     }
-  } else if (warp >= 4) {
+  } else if (warp >= 8) {
     // ------------------------------------------------------------ dq reducers
-    const int r = threadIdx.x - 128;  // TMEM lane = query row within the tile
+    const int r = (warp % 4) * 32 + lane;  // TMEM lane = query row within the tile
     const uint32_t tq = tmem + ((uint32_t)((warp % 4) * 32) << 16) + C::T_DP;
     bool ok = true;
     for (int it = 0; ok && it < n; ++it) {
@@ -291,27 +322,31 @@ __global__ void __launch_bounds__(320, 1)
         break;
       }
       tc_fence_after();
-      float v[D];
-      if constexpr (D == 128) {
-        tmem_ld128f(tq, v);
-      } else {
-        tmem_ld64f(tq, v);
-      }
-      tc_fence_before();
-      mbar_arrive(b_dqf);
       const int row = I * 128 + r;
-      if (row < p.q_len) {
-        float4* dst = reinterpret_cast<float4*>(dq_acc + ((int64_t)bh * p.q_len + row) * D);
+      float* dst = dq_acc + ((int64_t)bh * p.q_len + row) * D;
 #pragma unroll
-        for (int k = 0; k < D / 4; ++k) atomicAdd(dst + k, make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]));
+      for (int h2 = 0; h2 < D / 64; ++h2) {
+        float v[64];
+        tmem_ld64f(tq + 64 * h2, v);
+        if (h2 == D / 64 - 1) {
+          tc_fence_before();
+          mbar_arrive(b_dqf);  // TMEM columns free for the next dP^T
+        }
+        if (row < p.q_len) {
+#pragma unroll
+          for (int k = 0; k < 16; ++k)
+            red_add_v4(dst + 64 * h2 + 4 * k, v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+        }
       }
     }
     if (!ok) fail(p, ctl);
   } else {
     // ------------------------------------------------------------ P^T / dS^T, then the epilogue
-    const int r = threadIdx.x;
+    // warps 0-7: key row r = 32 (warp % 4) + lane; query columns [64 half, 64 half + 64)
+    const int r = (warp % 4) * 32 + lane;
+    const int half = warp / 4;
     const int j = J * 128 + r;  // key row
-    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    const uint32_t lane_off = (uint32_t)((warp % 4) * 32) << 16;
     const uint32_t tS = tmem + lane_off + C::T_S, tP = tmem + lane_off + C::T_DP;
     const int32_t* doc_row = p.mask.has_doc ? p.mask.doc + (int64_t)bm * p.mask.doc_len : nullptr;
     const int32_t doc_j = doc_row ? __ldg(doc_row + min(j, p.kv_len - 1)) : 0;
@@ -328,16 +363,17 @@ __global__ void __launch_bounds__(320, 1)
     for (int it = 0; it < n; ++it) {
       const int I = tile_of(it);
       const bool partial = it >= n_full;
-      const int st = it % C::NS;
+      const int qs = it % C::NQ;
       if (!warp_wait(b_s, it & 1, &ctl->abort)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const float* lse_s = ctl->lse[st];
-      const float* del_s = ctl->delta[st];
+      const float* lse_s = ctl->lse[qs];
+      const float* del_s = ctl->delta[qs];
 #pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
+      for (int c2 = 0; c2 < 2; ++c2) {
+        const int c = 2 * half + c2;  // 32-column chunk of the 128 query columns
         const int i0 = I * 128 + 32 * c;
         uint32_t w = row_ok ? 0xffffffffu : 0u;
         if (partial && row_ok) {
@@ -387,7 +423,8 @@ __global__ void __launch_bounds__(320, 1)
           pk[e / 2] = pack_bf16x2(pe[0], pe[1]);
           dk[e / 2] = pack_bf16x2(de[0], de[1]);
         }
-        tmem_st16(tS + 16 * c, pk);  // P^T over the S^T columns already read
+        // P^T over this half's own S^T columns, already read: [64 half + 16 c2, +16)
+        tmem_st16(tS + 64 * half + 16 * c2, pk);
         store_row32(sDS, r, c, dk);
       }
       tmem_st_wait();
@@ -396,7 +433,7 @@ __global__ void __launch_bounds__(320, 1)
       mbar_arrive(b_p);
     }
     if (!ok) fail(p, ctl);
-    // ---- epilogue: dV and scale * dK from TMEM, once per key tile
+    // ---- epilogue: dV and scale * dK from TMEM, once per key tile; each half writes D/2 columns
     if (ok && n > 0) {
       if (!warp_wait(b_acc, 0, &ctl->abort)) {
         ok = false;
@@ -405,10 +442,11 @@ __global__ void __launch_bounds__(320, 1)
       tc_fence_after();
     }
     uint8_t* stage_v = sQ(0);
-    uint8_t* stage_k = sDO(0);
+    uint8_t* stage_k = sQ(1);
     if (ok && !skip) {
 #pragma unroll 1
-      for (int c = 0; c < D / 32; ++c) {
+      for (int c2 = 0; c2 < D / 64; ++c2) {
+        const int c = half * (D / 64) + c2;  // 32-column chunk of D
         float a[32], g[32];
         if (n > 0) {
           tmem_ld32f(tmem + lane_off + C::T_DV + 32 * c, a);
@@ -428,8 +466,8 @@ __global__ void __launch_bounds__(320, 1)
       }
       fence_proxy_async_smem();
     }
-    named_bar_sync(1, 128);
-    if (r == 0 && !skip && !*reinterpret_cast<volatile int*>(&ctl->abort)) {
+    named_bar_sync(1, 256);
+    if (threadIdx.x == 0 && !skip && !*reinterpret_cast<volatile int*>(&ctl->abort)) {
       for (int c = 0; c < C::NC; ++c) {
         tma_store_3d(&tm_dv, smem_u32(stage_v + c * 16384), c * 64, J * 128, bh);
         tma_store_3d(&tm_dk, smem_u32(stage_k + c * 16384), c * 64, J * 128, bh);
@@ -441,7 +479,7 @@ __global__ void __launch_bounds__(320, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 8) {
+  if (warp == 12) {
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, C::TMEM_COLS);
@@ -519,7 +557,7 @@ cudaError_t launch_bwd_t(const AttnArgs& a, const BwdTensors& t, cudaStream_t st
     attr_set = true;
   }
   const int64_t items = (int64_t)a.B * a.H * a.nkv;
-  bwd_kernel<D, SCORE><<<(unsigned)items, 320, smem, stream>>>(mq, mk, mv, mdo, mdk, mdv, a, t.lse, t.delta,
+  bwd_kernel<D, SCORE><<<(unsigned)items, BwdCfg<D>::THREADS, smem, stream>>>(mq, mk, mv, mdo, mdk, mdv, a, t.lse, t.delta,
                                                               t.dq_acc);
   const int64_t n8 = rows * D / 8;
   bwd_dq_convert_kernel<<<(unsigned)((n8 + 255) / 256), 256, 0, stream>>>(
