@@ -58,7 +58,7 @@ class BlockMaskStruct(ctypes.Structure):
                [(name, ctypes.c_void_p) for name in (
                    "kv_num_blocks", "kv_indices", "full_kv_num_blocks", "full_kv_indices",
                    "q_num_blocks", "q_indices", "full_q_num_blocks", "full_q_indices",
-                   "row_order", "col_order", "tile_class", "tile_summary", "status")] + \
+                   "row_order", "col_order", "tile_class", "tile_summary", "doc_runs", "status")] + \
                [("spec", MaskSpec)]
 
 

@@ -5,8 +5,9 @@
 // empty, partial or full).
 //
 // Kernels, all stream-ordered, no host synchronisation:
-//  1. tile_summary -- doc-id min / max of every query and key tile (only when
-//                     the program has SAME_DOC); reads the doc ids once.
+//  1. tile_summary -- doc-id min / max of every query and key tile, and
+//     doc_runs        the run of equal ids around every position (only when
+//                     the program has SAME_DOC).
 //  2. classify     -- one warp per (query-tile row, chunk of 32 key tiles).
 //                     Each lane classifies one tile with a three-valued
 //                     interval test per atom (nothing / everything / undecided
@@ -18,8 +19,8 @@
 //                     bytes into ascending PARTIAL and FULL index lists with
 //                     zeroed tails (the columns' lists feed the backward).
 //  4. order        -- rows and columns sorted by descending tile count with a
-//                     counting sort, the order the attention kernels take
-//                     their work in (longest first).
+//                     stable counting sort, the order the attention kernels
+//                     take their work in (longest first, then by index).
 #include "internal.h"
 
 namespace fa {
@@ -120,6 +121,144 @@ __global__ void tile_summary_kernel(BuildArgs a) {
   }
 }
 
+// Runs of equal document ids, for PARTIAL tiles: for every position x < L =
+// max(q_len, kv_len) of batch row bm, [lo, hi) is the maximal run of
+// neighbouring positions whose id equals doc[x], and sorted[bm] says whether
+// the ids never decrease -- then doc[y] == doc[x] exactly when y lies in x's
+// run.  A position q is a run start when q == 0 or doc[q] != doc[q - 1];
+// lo[x] is the last run start <= x and hi[x] the first run start > x (or L).
+// Two passes over segments of kSegLen positions:
+//   doc_runs_local   -- per segment: run starts found inside the segment
+//                       (block scans), the segment's last / first run start and
+//                       whether its ids decrease;
+//   doc_runs_combine -- folds in the other segments' aggregates.
+constexpr int kRunE = 16;
+constexpr int kRunThreads = 256;
+constexpr int kSegLen = kRunE * kRunThreads;  // 4096 positions
+
+__device__ __forceinline__ int block_scan_max_excl(int v, int* s_warp, int identity) {
+  // exclusive max-scan over threadIdx.x; also leaves the block max in s_warp[32]
+  const int lane = threadIdx.x % 32, warp = threadIdx.x / 32;
+  const int nwarps = blockDim.x / 32;
+  int incl = v;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, d);
+    if (lane >= d) incl = max(incl, y);
+  }
+  if (lane == 31) s_warp[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int w = (lane < nwarps) ? s_warp[lane] : identity;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, w, d);
+      if (lane >= d) w = max(w, y);
+    }
+    s_warp[lane] = w;  // inclusive over warps
+    if (lane == 31) s_warp[32] = w;
+  }
+  __syncthreads();
+  const int before_warp = (warp > 0) ? s_warp[warp - 1] : identity;
+  const int excl_lane = __shfl_up_sync(0xffffffffu, incl, 1);
+  const int r = max(before_warp, lane > 0 ? excl_lane : identity);
+  __syncthreads();
+  return r;
+}
+
+// Segment aggregates live after the runs and the sorted flags:
+// [Bm][nseg][3] = last run start in the segment (-1 if none), first run
+// start after the segment's first position... (see below), unsorted flag.
+__device__ __forceinline__ int32_t* seg_aggr(const BuildArgs& a, int64_t L) {
+  return a.doc_runs + (int64_t)a.Bm * L * 2 + a.Bm;
+}
+
+__global__ void __launch_bounds__(kRunThreads) doc_runs_local_kernel(BuildArgs a) {
+  __shared__ int s_warp[33];
+  __shared__ int s_unsorted;
+  const int L = (int)max(a.q_len, a.kv_len);
+  const int nseg = (L + kSegLen - 1) / kSegLen;
+  const int bm = blockIdx.x / nseg, seg = blockIdx.x % nseg;
+  const int32_t* doc = a.mask.doc + (int64_t)bm * a.mask.doc_len;
+  int32_t* run = a.doc_runs + (int64_t)bm * L * 2;
+  if (threadIdx.x == 0) s_unsorted = 0;
+  __syncthreads();
+  const int x0 = seg * kSegLen + threadIdx.x * kRunE;
+  // left to right: last run start <= x inside the segment (-1: none)
+  int last = -1;
+  bool unsorted = false;
+  int lo_local[kRunE];
+#pragma unroll
+  for (int k = 0; k < kRunE; ++k) {
+    const int x = x0 + k;
+    if (x < L) {
+      const int d = __ldg(doc + x);
+      const int dp = (x > 0) ? __ldg(doc + x - 1) : d;
+      if (x == 0 || d != dp) last = x;
+      unsorted |= d < dp;
+    }
+    lo_local[k] = last;
+  }
+  if (unsorted) s_unsorted = 1;
+  const int before = block_scan_max_excl(last, s_warp, -1);
+  const int seg_last = s_warp[32];
+#pragma unroll
+  for (int k = 0; k < kRunE; ++k)
+    if (x0 + k < L) run[2 * (x0 + k)] = max(lo_local[k], before);
+  // right to left: first run start q > x with q inside (x, segment end] or q == L
+  // (max-scan of negated positions over mirrored threads; -2^30 = none)
+  const int mx0 = seg * kSegLen + (kRunThreads - 1 - threadIdx.x) * kRunE;
+  const int seg_end = min(seg * kSegLen + kSegLen, L);  // q may equal seg_end
+  int first = -(1 << 30);
+  int hi_local[kRunE];
+#pragma unroll
+  for (int k = kRunE - 1; k >= 0; --k) {
+    const int x = mx0 + k;
+    if (x < L) {
+      const int q = x + 1;
+      if (q == L || (q <= seg_end && __ldg(doc + q) != __ldg(doc + x))) first = -q;
+    }
+    hi_local[k] = first;
+  }
+  const int before_r = block_scan_max_excl(first, s_warp, -(1 << 30));
+  const int seg_first = s_warp[32];  // -(first run start in (seg start, seg end]), or -2^30
+#pragma unroll
+  for (int k = 0; k < kRunE; ++k)
+    if (mx0 + k < L) run[2 * (mx0 + k) + 1] = -max(hi_local[k], before_r);
+  if (threadIdx.x == 0) {
+    int32_t* g = seg_aggr(a, L) + ((int64_t)bm * nseg + seg) * 3;
+    g[0] = seg_last;
+    g[1] = seg_first;
+    g[2] = s_unsorted;
+  }
+}
+
+__global__ void __launch_bounds__(kRunThreads) doc_runs_combine_kernel(BuildArgs a) {
+  __shared__ int s_lo, s_hi, s_unsorted;
+  const int L = (int)max(a.q_len, a.kv_len);
+  const int nseg = (L + kSegLen - 1) / kSegLen;
+  const int bm = blockIdx.x / nseg, seg = blockIdx.x % nseg;
+  const int32_t* g = seg_aggr(a, L) + (int64_t)bm * nseg * 3;
+  if (threadIdx.x == 0) {
+    int lo = -1, hi = -(1 << 30), uns = 0;
+    for (int s2 = 0; s2 < seg; ++s2) lo = max(lo, g[3 * s2]);
+    for (int s2 = nseg - 1; s2 > seg; --s2) hi = max(hi, g[3 * s2 + 1]);
+    for (int s2 = 0; s2 < nseg; ++s2) uns |= g[3 * s2 + 2];
+    s_lo = lo;
+    s_hi = hi;
+    s_unsorted = uns;
+  }
+  __syncthreads();
+  int32_t* run = a.doc_runs + (int64_t)bm * L * 2;
+  const int x_end = min(seg * kSegLen + kSegLen, L);
+  for (int x = seg * kSegLen + threadIdx.x; x < x_end; x += blockDim.x) {
+    run[2 * x] = max(run[2 * x], s_lo);
+    const int h = run[2 * x + 1];
+    if (h == (1 << 30)) run[2 * x + 1] = (s_hi == -(1 << 30)) ? L : -s_hi;
+  }
+  if (seg == 0 && threadIdx.x == 0) a.doc_runs[(int64_t)a.Bm * L * 2 + bm] = s_unsorted ? 0 : 1;
+}
+
 constexpr int kBuildWarps = 8;
 
 // One warp per (query-tile row, chunk of 32 key tiles): each lane classifies
@@ -178,8 +317,11 @@ __global__ void __launch_bounds__(kBuildWarps * 32) classify_kernel(BuildArgs a)
     for (int64_t r = lane; r < rows; r += 32) {
       const int64_t i = i0 + r;
       const int32_t doc_i = doc ? __ldg(doc + i) : 0;
+      int run_lo = 0, run_hi = 0;
+      const bool use_run = doc != nullptr && doc_run(a.mask, bm, i, run_lo, run_hi);
       for (int64_t jc = j0; jc <= j1; jc += 32) {
         auto eq = [&]() {
+          if (use_run) return range_bits(run_lo, run_hi, (int)jc);
           uint32_t w = 0;
           if (doc_vec && jc + 32 <= j1 + 1) {
             const int4* dv = reinterpret_cast<const int4*>(doc + jc);  // same addresses in every lane
@@ -240,8 +382,10 @@ __global__ void __launch_bounds__(kBuildWarps * 32) compact_kernel(BuildArgs a) 
   }
 }
 
-// Counting sort by descending (num + full_num): block 0 orders the rows,
-// block 1 the columns.  hist has max(nq, nkv) + 1 buckets in shared memory.
+// Stable counting sort by descending (num + full_num): block 0 orders the
+// rows, block 1 the columns.  Stable, so items of equal length keep their
+// index order and neighbouring tiles run together (L2 reuse of K / V, Q / dO
+// and the dq accumulator).  hist has max(nq, nkv) + 1 buckets in shared memory.
 __global__ void __launch_bounds__(1024) order_kernel(BuildArgs a) {
   extern __shared__ int32_t hist[];
   const bool rows = blockIdx.x == 0;
@@ -251,6 +395,7 @@ __global__ void __launch_bounds__(1024) order_kernel(BuildArgs a) {
   const int n = rows ? a.Bm * a.Hm * a.nq : a.Bm * a.Hm * a.nkv;
   const int max_count = rows ? a.nkv : a.nq;
   const int nb = max_count + 1;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   for (int k = threadIdx.x; k < nb; k += blockDim.x) hist[k] = 0;
   __syncthreads();
   for (int r = threadIdx.x; r < n; r += blockDim.x) {
@@ -259,25 +404,40 @@ __global__ void __launch_bounds__(1024) order_kernel(BuildArgs a) {
   }
   __syncthreads();
   // exclusive scan, one warp
-  if (threadIdx.x < 32) {
+  if (warp == 0) {
     int carry = 0;
     for (int base = 0; base < nb; base += 32) {
-      const int k = base + threadIdx.x;
+      const int k = base + lane;
       const int h = (k < nb) ? hist[k] : 0;
       int incl = h;
 #pragma unroll
       for (int d = 1; d < 32; d <<= 1) {
         const int y = __shfl_up_sync(0xffffffffu, incl, d);
-        if ((int)threadIdx.x >= d) incl += y;
+        if (lane >= d) incl += y;
       }
       if (k < nb) hist[k] = carry + incl - h;
       carry += __shfl_sync(0xffffffffu, incl, 31);
     }
   }
   __syncthreads();
-  for (int r = threadIdx.x; r < n; r += blockDim.x) {
-    const int c = min(num[r] + full_num[r], max_count);
-    order[atomicAdd(&hist[max_count - c], 1)] = r;
+  // scatter in index order: warps take their turn inside each round of blockDim items
+  const uint32_t lt = (1u << lane) - 1u;
+  for (int round = 0; round < n; round += blockDim.x) {
+    const int r = round + threadIdx.x;
+    const bool valid = r < n;
+    const int bucket = valid ? max_count - min(num[r] + full_num[r], max_count) : -1;
+    const uint32_t peers = __match_any_sync(0xffffffffu, bucket);
+    const int leader = __ffs(peers) - 1;
+    int off = 0;
+    for (int w = 0; w < (int)(blockDim.x / 32); ++w) {
+      if (warp == w && valid && lane == leader) {
+        off = hist[bucket];
+        hist[bucket] = off + __popc(peers);
+      }
+      __syncthreads();
+    }
+    off = __shfl_sync(0xffffffffu, off, leader);
+    if (valid) order[off + __popc(peers & lt)] = r;
   }
 }
 
@@ -297,6 +457,10 @@ cudaError_t launch_build(const BuildArgs& a, cudaStream_t stream) {
   if (a.mask.has_doc) {
     const int64_t warps = (int64_t)a.Bm * 2 * tmax;
     tile_summary_kernel<<<(unsigned)((warps + 7) / 8), 256, 0, stream>>>(a);
+    const int L = (int)(a.q_len > a.kv_len ? a.q_len : a.kv_len);
+    const unsigned segs = (unsigned)(a.Bm * ((L + kSegLen - 1) / kSegLen));
+    doc_runs_local_kernel<<<segs, kRunThreads, 0, stream>>>(a);
+    doc_runs_combine_kernel<<<segs, kRunThreads, 0, stream>>>(a);
   }
   const int64_t rows = (int64_t)a.Bm * a.Hm * a.nq;
   const int64_t cols = (int64_t)a.Bm * a.Hm * a.nkv;

@@ -350,6 +350,8 @@ __global__ void __launch_bounds__(448, 1)
     const uint32_t tS = tmem + lane_off + C::T_S, tP = tmem + lane_off + C::T_DP;
     const int32_t* doc_row = p.mask.has_doc ? p.mask.doc + (int64_t)bm * p.mask.doc_len : nullptr;
     const int32_t doc_j = doc_row ? __ldg(doc_row + min(j, p.kv_len - 1)) : 0;
+    int run_lo = 0, run_hi = 0;  // with sorted ids: doc[i] == doc[j] exactly for i in [run_lo, run_hi)
+    const bool use_run = doc_row != nullptr && doc_run(p.mask, bm, min(j, p.kv_len - 1), run_lo, run_hi);
     const float sc_l2 = p.scale * kLog2e;
     float cap_l2 = 0.f, sc_over_cap = 0.f, slope_l2 = 0.f;
     if constexpr (SCORE == FA_S_SOFTCAP) {
@@ -378,6 +380,7 @@ __global__ void __launch_bounds__(448, 1)
         uint32_t w = row_ok ? 0xffffffffu : 0u;
         if (partial && row_ok) {
           auto eq = [&]() {
+            if (use_run) return range_bits(run_lo, run_hi, i0);
             uint32_t bits = 0;
             if (i0 + 32 <= p.q_len && p.mask.doc_vec_ok) {
               const int4* dv = reinterpret_cast<const int4*>(doc_row + i0);
@@ -396,8 +399,7 @@ __global__ void __launch_bounds__(448, 1)
           w = mask_word_t_rolled(p.mask, ctl->arg, j, i0, eq);
         }
         float sv[32], dp[32];
-        tmem_ld32f(tS + 32 * c, sv);
-        tmem_ld32f(tP + 32 * c, dp);
+        tmem_ld32x2f(tS + 32 * c, sv, tP + 32 * c, dp);
         uint32_t pk[16], dk[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {

@@ -26,6 +26,11 @@ struct DevMask {
   int32_t doc_vec_ok;  // doc rows are 16-byte aligned (base and doc_len % 4 == 0)
   int64_t doc_len;
   const int32_t* doc;
+  // runs of equal ids: [Bm][run_len] pairs (lo, hi) and per batch row a flag
+  // set when that row's ids never decrease (filled by the builder)
+  const int32_t* runs;
+  const int32_t* sorted;
+  int64_t run_len;
   int32_t op[FA_MAX_MASK_NODES];
   const int32_t* param[FA_MAX_MASK_NODES];
 };
@@ -41,6 +46,22 @@ __device__ __forceinline__ int32_t node_arg(const DevMask& m, int k, int bm) {
 // Bits [0, n) set, n clamped to [0, 32].
 __device__ __forceinline__ uint32_t low_bits(int64_t n) {
   return n <= 0 ? 0u : (n >= 32 ? 0xffffffffu : ((1u << (uint32_t)n) - 1u));
+}
+
+// Word of the positions x0 .. x0+31 inside [lo, hi).
+__device__ __forceinline__ uint32_t range_bits(int lo, int hi, int x0) {
+  return low_bits((int64_t)hi - x0) & ~low_bits((int64_t)lo - x0);
+}
+
+// The run [lo, hi) of position x in batch row bm when that row's ids never
+// decrease, so that doc[y] == doc[x] exactly for y in [lo, hi).  Returns false
+// (and the caller compares ids one by one) otherwise.
+__device__ __forceinline__ bool doc_run(const DevMask& m, int bm, int64_t x, int& lo, int& hi) {
+  if (m.runs == nullptr || __ldg(m.sorted + bm) == 0) return false;
+  const int2 r = __ldg(reinterpret_cast<const int2*>(m.runs) + (int64_t)bm * m.run_len + x);
+  lo = r.x;
+  hi = r.y;
+  return true;
 }
 
 // Visibility word of query row i over key columns j0 .. j0+31.

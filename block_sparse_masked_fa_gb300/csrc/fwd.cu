@@ -220,6 +220,8 @@ __global__ void __launch_bounds__(192, 2)
     const uint32_t tO = tmem + lane_off + 128;
     const int32_t* doc_row = p.mask.has_doc ? p.mask.doc + (int64_t)bm * p.mask.doc_len : nullptr;
     const int32_t doc_i = doc_row ? __ldg(doc_row + min(i, p.q_len - 1)) : 0;
+    int run_lo = 0, run_hi = 0;  // with sorted ids: doc[j] == doc[i] exactly for j in [run_lo, run_hi)
+    const bool use_run = doc_row != nullptr && doc_run(p.mask, bm, min(i, p.q_len - 1), run_lo, run_hi);
 
     const float sc_l2 = p.scale * kLog2e;  // logit -> log2 units
     float cap_l2 = 0.f, sc_over_cap = 0.f, slope_l2 = 0.f;
@@ -249,6 +251,7 @@ __global__ void __launch_bounds__(192, 2)
           if (partial) {
             // doc ids of the 32 key columns: the same addresses for every thread (broadcast loads)
             auto eq = [&]() {
+              if (use_run) return range_bits(run_lo, run_hi, jc);
               uint32_t bits = 0;
               if (!ragged && p.mask.doc_vec_ok) {
                 const int4* dv = reinterpret_cast<const int4*>(doc_row + jc);
@@ -320,21 +323,13 @@ __global__ void __launch_bounds__(192, 2)
         m = m_new;
       else
         need = m_new > m + kRescaleThreshold;
-      if (__any_sync(0xffffffffu, need)) {
-        const float alpha = need ? ex2_approx(m - m_new) : 1.0f;
-        if (need) {
-          l *= alpha;
-          m = m_new;
-        }
-#pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
-          float o[32];
-          tmem_ld32f(tO + 32 * c, o);
-#pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] *= alpha;
-          tmem_st32f(tO + 32 * c, o);
-        }
+      float alpha = 1.0f;
+      if (need) {
+        alpha = ex2_approx(m - m_new);
+        l *= alpha;
+        m = m_new;
       }
+      const bool rescale = __any_sync(0xffffffffu, need);  // O is rescaled below, once S is no longer live
       const float m_use = (m == -INFINITY) ? 0.f : m;
       // -- P = 2^(x - m) as bf16 into TMEM (over the consumed S columns), row sum (4 chains)
       {
@@ -369,6 +364,16 @@ __global__ void __launch_bounds__(192, 2)
           tmem_st16(tS + 16 * c, pk);
         }
         l += (c0 + c1) + (c2 + c3);
+      }
+      if (rescale) {
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          float o[32];
+          tmem_ld32f(tO + 32 * c, o);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] *= alpha;
+          tmem_st32f(tO + 32 * c, o);
+        }
       }
       tmem_st_wait();
       tc_fence_before();

@@ -16,6 +16,7 @@ struct BuildArgs {
   int32_t *row_order, *col_order;
   uint8_t* tile_class;
   int32_t* summary;  // [Bm][2][max(nq, nkv)][4]: doc-id min, max, step-0/1 flag per query / key tile
+  int32_t* doc_runs;  // [Bm][max(q_len, kv_len)][2] runs, then [Bm] sorted flags
   uint32_t* status;
 };
 

@@ -135,6 +135,13 @@ typedef struct {
  *   row_order, col_order: rows / columns sorted by descending tile count (the
  *                      order the attention kernels take their work in).
  *   tile_class         uint8 [Bm][Hm][nq][nkv]: 0 EMPTY, 1 PARTIAL, 2 FULL.
+ *   doc_runs           int32 [Bm][max(q_len, kv_len)][2], int32 [Bm] (then
+ *                      builder scratch): for
+ *                      every position the run [lo, hi) of neighbouring positions
+ *                      with the same document id, and per batch row a flag set
+ *                      when the ids never decrease (then doc[i] == doc[j] iff j
+ *                      lies in i's run, which the kernels use on PARTIAL tiles).
+ *                      Filled only when the program has SAME_DOC.
  *   status             device status word (bit 0: a wait timed out).
  *
  * The union kv_num_blocks + full_kv_num_blocks is the count of "tiles that are
@@ -160,6 +167,7 @@ typedef struct {
   int32_t* col_order;
   uint8_t* tile_class;
   int32_t* tile_summary;
+  int32_t* doc_runs;
   uint32_t* status;
   fa_mask_spec spec;
 } fa_block_mask;

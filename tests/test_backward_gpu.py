@@ -151,3 +151,14 @@ def test_batch_broadcast_docs_prefix_alibi():
         for h in range(2):
             ref = oracle_grads(inp, mask, b, h, ("alibi", sl), Bm=2, prefix=prefix)
             check_all([g[b, h] for g in got], ref, f"b{b} h{h}")
+
+
+def test_unsorted_document_ids():
+    S = 900
+    rng = np.random.default_rng(33)
+    docs = np.repeat(rng.integers(0, 4, size=9), 100).astype(np.int32)[None]
+    inp = _inputs(1, 2, S, 64, 34, docs=docs)
+    mask = P(("same_doc",), ("window", 500), ("and",))
+    got = run_fa(inp, mask)
+    for h in range(2):
+        check_all([g[0, h] for g in got], oracle_grads(inp, mask, 0, h, ("none",)), f"unsorted h{h}")

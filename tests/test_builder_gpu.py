@@ -37,6 +37,8 @@ def compare(bm, cls, lists):
     assert sorted(order.tolist()) == list(range(order.size))
     work = (got["kv_num_blocks"] + got["full_kv_num_blocks"]).reshape(-1)[order]
     assert np.all(np.diff(work) <= 0)                     # longest rows first
+    ties = np.diff(work) == 0
+    assert np.all(np.diff(order)[ties] > 0)               # stable: index order among equal lengths
     assert fa.fa_get_status(bm) == 0
 
 
@@ -105,3 +107,45 @@ def test_random_programs_ragged_broadcast(seed):
     bm = fa.fa_create_block_mask(device_nodes(mask, docs, prefix), Bm, Hm, q_len, kv_len, block)
     cls, lists = expected(mask, docs, prefix, Bm, Hm, q_len, kv_len, block)
     compare(bm, cls, lists)
+
+
+def _runs_expected(doc, L):
+    d = np.asarray(doc[:L], dtype=np.int64)
+    change = np.ones(L, dtype=bool)
+    change[1:] = d[1:] != d[:-1]
+    starts = np.nonzero(change)[0]
+    lo = starts[np.searchsorted(starts, np.arange(L), side="right") - 1]
+    ends = np.append(starts[1:], L)
+    hi = ends[np.searchsorted(starts, np.arange(L), side="right") - 1]
+    return lo, hi, int(np.all(d[1:] >= d[:-1]))
+
+
+@pytest.mark.parametrize("case", ["sorted_multi_chunk", "unsorted_repeats", "ragged_cross", "one_doc"])
+def test_doc_runs_table(case):
+    """The per-position run table the kernels use on PARTIAL tiles, bit-exact."""
+    rng = np.random.default_rng(7)
+    if case == "sorted_multi_chunk":
+        q_len = kv_len = 40000                       # several 16K-position chunks
+        docs = make_doc_ids(("lognormal", 600.0, 1.0, 16, 16384), q_len, 3, batch=2)
+    elif case == "unsorted_repeats":
+        q_len = kv_len = 3000
+        docs = np.stack([np.repeat(rng.integers(0, 5, size=30), 100).astype(np.int32) for _ in range(2)])
+    elif case == "ragged_cross":
+        q_len, kv_len = 777, 1300
+        docs = make_doc_ids(("geometric", 90.0), 1300, 4, batch=2)
+    else:
+        q_len = kv_len = 5000
+        docs = np.zeros((2, 5000), dtype=np.int32)
+    L = max(q_len, kv_len)
+    mask = MaskProgram((("causal",), ("same_doc",), ("and",)))
+    bm = fa.fa_create_block_mask(device_nodes(mask, docs), 2, 1, q_len, kv_len, 128)
+    torch.cuda.synchronize()
+    off = bm.struct.doc_runs - bm.buffer.data_ptr()
+    raw = bm.buffer[off:off + (2 * L * 2 + 2) * 4].view(torch.int32).cpu().numpy()
+    runs = raw[:2 * L * 2].reshape(2, L, 2)
+    flags = raw[2 * L * 2:]
+    for b in range(2):
+        lo, hi, srt = _runs_expected(docs[b], L)
+        np.testing.assert_array_equal(runs[b, :, 0], lo)
+        np.testing.assert_array_equal(runs[b, :, 1], hi)
+        assert flags[b] == srt

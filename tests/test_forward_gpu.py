@@ -189,3 +189,18 @@ def test_full_tiles_as_partial_give_same_result():
     np.testing.assert_allclose(out2.float().cpu().numpy(), out1, atol=2e-2)
     np.testing.assert_allclose(lse2.cpu().numpy(), lse1, atol=1e-4)
     assert nkv == 8
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_unsorted_document_ids(D):
+    """Document ids that decrease and repeat (doc 2 appears in two separate runs):
+    the kernels compare ids one by one instead of using runs."""
+    S = 900
+    rng = np.random.default_rng(31)
+    docs = np.repeat(rng.integers(0, 4, size=9), 100).astype(np.int32)[None]
+    inp = _inputs(1, 2, S, D, 32, docs=docs)
+    mask = P(("same_doc",), ("window", 500), ("and",))
+    out, lse, _ = run_fa(inp, mask)
+    for h in range(2):
+        ref_out, ref_lse = oracle_rows(inp, mask, 0, h, None, ("none",))
+        check_forward(out[0, h], lse[0, h], ref_out, ref_lse, f"unsorted h{h}")
