@@ -327,7 +327,8 @@ fa_status fa_backward_workspace_bytes(int32_t B, int32_t H, int64_t q_len, int32
   if (B < 1 || H < 1 || q_len < 1) return FA_ERR_SHAPE;
   if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
   const size_t rows = (size_t)B * H * (size_t)q_len;
-  *bytes = align_up(rows * D * 4) + align_up(rows * 4);
+  const size_t tiles = (size_t)B * H * (size_t)((q_len + 127) / 128);
+  *bytes = align_up(rows * D * 4) + align_up(tiles * 256 * 4);
   return FA_OK;
 }
 
@@ -361,7 +362,7 @@ fa_status fa_backward(const void* q, const void* k, const void* v, const void* o
   t.dk = dk;
   t.dv = dv;
   t.dq_acc = static_cast<float*>(workspace);
-  t.delta = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + align_up(rows * D * 4));
+  t.stats = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + align_up(rows * D * 4));
   bool enc_failed = false;
   const cudaError_t e = launch_backward(a, t, stream, &enc_failed);
   if (enc_failed) return FA_ERR_CUDA;
@@ -400,7 +401,7 @@ fa_status fa_backward_noalloc(const void* q, const void* k, const void* v, const
   t.dk = dk;
   t.dv = dv;
   t.dq_acc = static_cast<float*>(scratch);
-  t.delta = reinterpret_cast<float*>(static_cast<uint8_t*>(scratch) + align_up(rows * D * 4));
+  t.stats = reinterpret_cast<float*>(static_cast<uint8_t*>(scratch) + align_up(rows * D * 4));
   bool enc_failed = false;
   const cudaError_t e = launch_backward(a, t, stream, &enc_failed);
   if (enc_failed) return FA_ERR_CUDA;

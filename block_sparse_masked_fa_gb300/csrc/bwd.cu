@@ -11,7 +11,8 @@
 // its column lists (FULL first, then PARTIAL with the mask per element).
 //
 // Kernels:
-//  1. bwd_pre   -- Delta_i = dO_i . out_i (fp32) and a zeroed fp32 dq accumulator.
+//  1. bwd_pre   -- Delta_i = dO_i . out_i (fp32) and LSE, laid out per query
+//                  tile for one bulk copy each, and a zeroed fp32 dq accumulator.
 //  2. bwd_kernel -- one CTA per (b, h, key tile J), key tiles longest first:
 //       warps 0-3  thread r owns key row r (TMEM lane r): P^T, dS^T
 //       warps 4-7  dq reducers: dQ tile from TMEM, fp32 atomics into the accumulator
@@ -52,7 +53,13 @@ struct BwdCfg {
   static constexpr int THREADS = 448;  // 8 key-row warps, 4 dq warps, producer, MMA
 };
 
+struct TileStats {  // one bulk copy per query tile, from the workspace
+  float nlse[128];    // -LSE * log2(e) of the tile's query rows
+  float ndelta[128];  // -Delta of the tile's query rows
+};
+
 struct BwdCtl {
+  alignas(16) TileStats stats[2];  // per Q slot
   uint64_t kv_full;
   uint64_t q_full[2], q_empty[2];
   uint64_t do_full[2], do_empty[2];
@@ -60,8 +67,6 @@ struct BwdCtl {
   uint32_t tmem;
   int abort;
   int32_t arg[FA_MAX_MASK_NODES];
-  float lse[2][128];    // LSE * log2(e) of the Q slot's query rows
-  float delta[2][128];  // Delta of the Q slot's query rows
 };
 
 template <int D>
@@ -108,8 +113,8 @@ __global__ void __launch_bounds__(448, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_dv,
-               const __grid_constant__ AttnArgs p, const float* __restrict__ lse_g,
-               const float* __restrict__ delta_g, float* __restrict__ dq_acc) {
+               const __grid_constant__ AttnArgs p, const float* __restrict__ stats_g,
+               float* __restrict__ dq_acc) {
   using C = BwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -144,7 +149,7 @@ __global__ void __launch_bounds__(448, 1)
   if (threadIdx.x == 0) {
     mbar_init(b_kv, 1);
     for (int s2 = 0; s2 < 2; ++s2) {
-      mbar_init(smem_u32(&ctl->q_full[s2]), 32);  // the producer warp's 32 lanes (one with the byte count)
+      mbar_init(smem_u32(&ctl->q_full[s2]), 1);
       mbar_init(smem_u32(&ctl->q_empty[s2]), 1);
       mbar_init(smem_u32(&ctl->do_full[s2]), 1);
       mbar_init(smem_u32(&ctl->do_empty[s2]), 1);
@@ -188,34 +193,21 @@ __global__ void __launch_bounds__(448, 1)
       }
       int q_issued = 0, do_issued = 0;
       bool ok = true;
-      const int64_t base = (int64_t)bh * p.q_len;
       for (int it = 0; it < n; ++it) {
         const int I = tile_of(it);
-        // Q slot, with the tile's LSE (log2 units) and Delta
+        // Q slot, with the tile's -LSE (log2 units) and -Delta
         const int qs = it % C::NQ, quse = it / C::NQ;
         if (quse > 0 && !warp_wait(smem_u32(&ctl->q_empty[qs]), (quse - 1) & 1, &ctl->abort)) {
           ok = false;
           break;
         }
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int r = lane + 32 * k;
-          const int row = I * 128 + r;
-          float lv = 0.f, dv = 0.f;
-          if (row < p.q_len) {
-            lv = __ldg(lse_g + base + row) * kLog2e;
-            dv = __ldg(delta_g + base + row);
-          }
-          ctl->lse[qs][r] = lv;
-          ctl->delta[qs][r] = dv;
-        }
-        const uint32_t qbar = smem_u32(&ctl->q_full[qs]);
         if (lane == 0) {
-          mbar_arrive_expect_tx(qbar, C::TILE);
+          const uint32_t qbar = smem_u32(&ctl->q_full[qs]);
+          mbar_arrive_expect_tx(qbar, C::TILE + (uint32_t)sizeof(TileStats));
           for (int c = 0; c < C::NC; ++c)
             tma_load_3d(smem_u32(sQ(qs) + c * 16384), &tm_q, qbar, c * 64, I * 128, bh);
-        } else {
-          mbar_arrive(qbar);
+          bulk_load(smem_u32(&ctl->stats[qs]), stats_g + ((int64_t)bh * p.nq + I) * 256,
+                    (uint32_t)sizeof(TileStats), qbar);
         }
         q_issued = it + 1;
         // dO slot
@@ -371,8 +363,8 @@ __global__ void __launch_bounds__(448, 1)
         break;
       }
       tc_fence_after();
-      const float* lse_s = ctl->lse[qs];
-      const float* del_s = ctl->delta[qs];
+      const float* nlse_s = ctl->stats[qs].nlse;
+      const float* ndel_s = ctl->stats[qs].ndelta;
 #pragma unroll 1
       for (int c2 = 0; c2 < 2; ++c2) {
         const int c = 2 * half + c2;  // 32-column chunk of the 128 query columns
@@ -401,29 +393,30 @@ __global__ void __launch_bounds__(448, 1)
         float sv[32], dp[32];
         tmem_ld32x2f(tS + 32 * c, sv, tP + 32 * c, dp);
         uint32_t pk[16], dk[16];
+        const float2* nl2 = reinterpret_cast<const float2*>(nlse_s + 32 * c);
+        const float2* nd2 = reinterpret_cast<const float2*>(ndel_s + 32 * c);
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
-          float pe[2], de[2];
-#pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int ee = e + u;
-            const float lse = lse_s[32 * c + ee];
-            float a, g = 1.0f;
-            if constexpr (SCORE == FA_S_SOFTCAP) {
-              const float th = tanh_fast(sv[ee] * sc_over_cap);
-              a = fmaf(cap_l2, th, -lse);
-              g = fmaf(-th, th, 1.0f);
-            } else if constexpr (SCORE == FA_S_ALIBI) {
-              a = fmaf(sv[ee], sc_l2, fmaf(-slope_l2, (float)(i0 + ee - j), -lse));
-            } else {
-              a = fmaf(sv[ee], sc_l2, -lse);
-            }
-            const float pv = ((w >> ee) & 1u) ? ex2_approx(a) : 0.f;
-            pe[u] = pv;
-            de[u] = pv * (dp[ee] - del_s[32 * c + ee]) * g;
+          const float2 nl = nl2[e / 2], nd = nd2[e / 2];
+          float2 a, g = make_float2(1.0f, 1.0f);
+          if constexpr (SCORE == FA_S_SOFTCAP) {
+            const float t0 = tanh_fast(sv[e] * sc_over_cap), t1 = tanh_fast(sv[e + 1] * sc_over_cap);
+            a = fma2(make_float2(cap_l2, cap_l2), make_float2(t0, t1), nl);
+            g = fma2(make_float2(-t0, -t1), make_float2(t0, t1), make_float2(1.0f, 1.0f));
+          } else if constexpr (SCORE == FA_S_ALIBI) {
+            a = fma2(make_float2(sv[e], sv[e + 1]), make_float2(sc_l2, sc_l2),
+                     make_float2(fmaf(-slope_l2, (float)(i0 + e - j), nl.x),
+                                 fmaf(-slope_l2, (float)(i0 + e + 1 - j), nl.y)));
+          } else {
+            a = fma2(make_float2(sv[e], sv[e + 1]), make_float2(sc_l2, sc_l2), nl);
           }
-          pk[e / 2] = pack_bf16x2(pe[0], pe[1]);
-          dk[e / 2] = pack_bf16x2(de[0], de[1]);
+          float2 pv;
+          pv.x = ((w >> e) & 1u) ? ex2_approx(a.x) : 0.f;
+          pv.y = ((w >> (e + 1)) & 1u) ? ex2_approx(a.y) : 0.f;
+          float2 dsv = mul2(pv, add2(make_float2(dp[e], dp[e + 1]), nd));
+          if constexpr (SCORE == FA_S_SOFTCAP) dsv = mul2(dsv, g);
+          pk[e / 2] = pack_bf16x2(pv.x, pv.y);
+          dk[e / 2] = pack_bf16x2(dsv.x, dsv.y);
         }
         // P^T over this half's own S^T columns, already read: [64 half + 16 c2, +16)
         tmem_st16(tS + 64 * half + 16 * c2, pk);
@@ -488,13 +481,15 @@ __global__ void __launch_bounds__(448, 1)
   }
 }
 
-// Delta_i = dO_i . out_i in fp32, and the fp32 dq accumulator rows set to zero.
+// Per query row: -LSE * log2(e) and -Delta (Delta_i = dO_i . out_i, fp32)
+// into the per-tile stats array [B*H][nq][2][128], zero for the rows past
+// q_len in the last tile; and the fp32 dq accumulator rows set to zero.
 // 16 threads per row, 16 rows per 256-thread block.
 template <int D>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __restrict__ out,
                                                       const __nv_bfloat16* __restrict__ dout,
-                                                      float* __restrict__ delta, float* __restrict__ dq_acc,
-                                                      int64_t rows) {
+                                                      const float* __restrict__ lse, float* __restrict__ stats,
+                                                      float* __restrict__ dq_acc, int64_t rows, int q_len, int nq) {
   constexpr int E = D / 16;  // elements per thread
   const int64_t row = (int64_t)blockIdx.x * 16 + threadIdx.x / 16;
   const int t = threadIdx.x % 16;
@@ -514,7 +509,15 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __res
   }
 #pragma unroll
   for (int d = 8; d >= 1; d >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, d);
-  if (row < rows && t == 0) delta[row] = acc;
+  if (row < rows && t == 0) {
+    const int64_t bh = row / q_len;
+    const int i = (int)(row % q_len);
+    float* st = stats + (bh * nq + i / 128) * 256;
+    st[i % 128] = -__ldg(lse + row) * kLog2e;
+    st[128 + i % 128] = -acc;
+    if (i == q_len - 1)  // rows past q_len in the last tile
+      for (int k = i % 128 + 1; k < 128; ++k) st[k] = st[128 + k] = 0.f;
+  }
 }
 
 // dq = bf16(scale * accumulator), 8 elements per thread.
@@ -538,7 +541,8 @@ cudaError_t launch_bwd_t(const AttnArgs& a, const BwdTensors& t, cudaStream_t st
   const uint64_t bh = (uint64_t)a.B * a.H;
   const int64_t rows = (int64_t)bh * a.q_len;
   bwd_pre_kernel<D><<<(unsigned)((rows + 15) / 16), 256, 0, stream>>>(
-      static_cast<const __nv_bfloat16*>(t.out), static_cast<const __nv_bfloat16*>(t.dout), t.delta, t.dq_acc, rows);
+      static_cast<const __nv_bfloat16*>(t.out), static_cast<const __nv_bfloat16*>(t.dout), t.lse, t.stats, t.dq_acc,
+      rows, a.q_len, a.nq);
 
   CUtensorMap mq, mk, mv, mdo, mdk, mdv;
   auto enc = [&](CUtensorMap* m, const void* ptr, int64_t len) {
@@ -559,8 +563,7 @@ cudaError_t launch_bwd_t(const AttnArgs& a, const BwdTensors& t, cudaStream_t st
     attr_set = true;
   }
   const int64_t items = (int64_t)a.B * a.H * a.nkv;
-  bwd_kernel<D, SCORE><<<(unsigned)items, BwdCfg<D>::THREADS, smem, stream>>>(mq, mk, mv, mdo, mdk, mdv, a, t.lse, t.delta,
-                                                              t.dq_acc);
+  bwd_kernel<D, SCORE><<<(unsigned)items, BwdCfg<D>::THREADS, smem, stream>>>(mq, mk, mv, mdo, mdk, mdv, a, t.stats, t.dq_acc);
   const int64_t n8 = rows * D / 8;
   bwd_dq_convert_kernel<<<(unsigned)((n8 + 255) / 256), 256, 0, stream>>>(
       t.dq_acc, static_cast<__nv_bfloat16*>(t.dq), n8, a.scale);

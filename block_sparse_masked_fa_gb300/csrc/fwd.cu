@@ -294,17 +294,25 @@ __global__ void __launch_bounds__(192, 2)
       {
         float a0 = -INFINITY, a1 = -INFINITY, a2 = -INFINITY, a3 = -INFINITY;
 #pragma unroll
-        for (int e = 0; e < 128; e += 4) {
+        for (int e = 0; e < 128; e += 8) {
           if constexpr (SCORE == FA_S_ALIBI) {
-            a0 = fmaxf(a0, fmaf(s[e], sc_l2, slope_l2 * (float)e));
-            a1 = fmaxf(a1, fmaf(s[e + 1], sc_l2, slope_l2 * (float)(e + 1)));
-            a2 = fmaxf(a2, fmaf(s[e + 2], sc_l2, slope_l2 * (float)(e + 2)));
-            a3 = fmaxf(a3, fmaf(s[e + 3], sc_l2, slope_l2 * (float)(e + 3)));
+            float t[8];
+#pragma unroll
+            for (int u = 0; u < 8; u += 2) {
+              const float2 v = fma2(make_float2(s[e + u], s[e + u + 1]), make_float2(sc_l2, sc_l2),
+                                    make_float2(slope_l2 * (float)(e + u), slope_l2 * (float)(e + u + 1)));
+              t[u] = v.x;
+              t[u + 1] = v.y;
+            }
+            a0 = max3f(a0, t[0], t[1]);
+            a1 = max3f(a1, t[2], t[3]);
+            a2 = max3f(a2, t[4], t[5]);
+            a3 = max3f(a3, t[6], t[7]);
           } else {
-            a0 = fmaxf(a0, s[e]);
-            a1 = fmaxf(a1, s[e + 1]);
-            a2 = fmaxf(a2, s[e + 2]);
-            a3 = fmaxf(a3, s[e + 3]);
+            a0 = max3f(a0, s[e], s[e + 1]);
+            a1 = max3f(a1, s[e + 2], s[e + 3]);
+            a2 = max3f(a2, s[e + 4], s[e + 5]);
+            a3 = max3f(a3, s[e + 6], s[e + 7]);
           }
         }
         mx = fmaxf(fmaxf(a0, a1), fmaxf(a2, a3));
@@ -333,19 +341,25 @@ __global__ void __launch_bounds__(192, 2)
       const float m_use = (m == -INFINITY) ? 0.f : m;
       // -- P = 2^(x - m) as bf16 into TMEM (over the consumed S columns), row sum (4 chains)
       {
-        float c0 = 0.f, c1 = 0.f, c2 = 0.f, c3 = 0.f;
+        float2 c01 = make_float2(0.f, 0.f), c23 = make_float2(0.f, 0.f);
         const float off = -(base + m_use);
-        auto pexp = [&](int e) -> float {
-          float x;
+        // exponent arguments of elements e, e + 1 (two lanes of packed arithmetic)
+        auto parg = [&](int e) -> float2 {
           if constexpr (SCORE == FA_S_NONE) {
-            x = fmaf(s[e], sc_l2, -m_use);
+            return fma2(make_float2(s[e], s[e + 1]), make_float2(sc_l2, sc_l2), make_float2(-m_use, -m_use));
           } else if constexpr (SCORE == FA_S_SOFTCAP) {
-            x = fmaf(cap_l2, tanh_fast(s[e] * sc_over_cap), -m_use);
-            if (msk) x = (s[e] == -INFINITY) ? -INFINITY : x;
+            float2 x = fma2(make_float2(cap_l2, cap_l2),
+                            make_float2(tanh_fast(s[e] * sc_over_cap), tanh_fast(s[e + 1] * sc_over_cap)),
+                            make_float2(-m_use, -m_use));
+            if (msk) {
+              x.x = (s[e] == -INFINITY) ? -INFINITY : x.x;
+              x.y = (s[e + 1] == -INFINITY) ? -INFINITY : x.y;
+            }
+            return x;
           } else {
-            x = fmaf(s[e], sc_l2, fmaf(slope_l2, (float)e, off));
+            return fma2(make_float2(s[e], s[e + 1]), make_float2(sc_l2, sc_l2),
+                        make_float2(fmaf(slope_l2, (float)e, off), fmaf(slope_l2, (float)(e + 1), off)));
           }
-          return ex2_approx(x);
         };
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
@@ -353,17 +367,18 @@ __global__ void __launch_bounds__(192, 2)
 #pragma unroll
           for (int e2 = 0; e2 < 16; e2 += 2) {
             const int e = 32 * c + 2 * e2;
-            const float p0 = pexp(e), p1 = pexp(e + 1), p2 = pexp(e + 2), p3 = pexp(e + 3);
-            c0 += p0;
-            c1 += p1;
-            c2 += p2;
-            c3 += p3;
-            pk[e2] = pack_bf16x2(p0, p1);
-            pk[e2 + 1] = pack_bf16x2(p2, p3);
+            const float2 x01 = parg(e), x23 = parg(e + 2);
+            const float2 p01 = make_float2(ex2_approx(x01.x), ex2_approx(x01.y));
+            const float2 p23 = make_float2(ex2_approx(x23.x), ex2_approx(x23.y));
+            c01 = add2(c01, p01);
+            c23 = add2(c23, p23);
+            pk[e2] = pack_bf16x2(p01.x, p01.y);
+            pk[e2 + 1] = pack_bf16x2(p23.x, p23.y);
           }
           tmem_st16(tS + 16 * c, pk);
         }
-        l += (c0 + c1) + (c2 + c3);
+        const float2 cs = add2(c01, c23);
+        l += cs.x + cs.y;
       }
       if (rescale) {
 #pragma unroll 1

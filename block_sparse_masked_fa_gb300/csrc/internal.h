@@ -47,7 +47,7 @@ struct BwdTensors {
   const float* lse;
   void *dq, *dk, *dv;
   float* dq_acc;  // fp32 [B, H, q_len, D]
-  float* delta;   // fp32 [B, H, q_len]
+  float* stats;   // fp32 [B, H, nq][2][128]: -LSE * log2(e) and -Delta per query tile
 };
 
 // Returns a CUDA error, or cudaErrorUnknown with *enc_failed set when a

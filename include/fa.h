@@ -201,8 +201,9 @@ fa_status fa_forward(const void* q, const void* k, const void* v, int32_t B, int
                      int64_t kv_len, int32_t D, const fa_block_mask* bm, const fa_score_spec* score, float scale,
                      void* out, float* lse, cudaStream_t stream);
 
-/* Device workspace fa_backward needs: an fp32 dq accumulator and the per-row
- * sum(dO * out). */
+/* Device workspace fa_backward needs: an fp32 dq accumulator
+ * (B*H*q_len*D floats) and, per 128-row query tile, the rows' LSE and
+ * sum(dO * out) (B*H*ceil(q_len/128)*256 floats), each 256-byte aligned. */
 fa_status fa_backward_workspace_bytes(int32_t B, int32_t H, int64_t q_len, int32_t D, size_t* bytes);
 
 /* Backward: dq, dk, dv of L = sum(out * dO) (tutorial, Pattern 3: the
@@ -231,8 +232,8 @@ fa_status fa_backward(const void* q, const void* k, const void* v, const void* o
  * allocating library routine.
  *  - Size limit: returns FA_ERR_WORKSPACE, before any GPU work, when
  *    fa_backward_workspace_bytes(B, H, q_len, D) exceeds
- *    FA_NOALLOC_SCRATCH_BYTES (16 MiB: e.g. B*H*q_len up to 32,512 rows at
- *    D = 128 or 64,527 rows at D = 64).
+ *    FA_NOALLOC_SCRATCH_BYTES (16 MiB: e.g. B*H*q_len up to about 32,000
+ *    rows at D = 128 or 63,000 rows at D = 64).
  *  - Set-up: the first call on each device looks up the array's device address
  *    (cudaGetSymbolAddress, with that device current) and caches it; make that
  *    first call before any stream capture.

@@ -159,7 +159,7 @@ def test_forward_rejects():
 
 
 def test_backward_workspace_and_rejects():
-    assert fa.fa_backward_workspace_bytes(2, 3, 1000, 128) == _align(2 * 3 * 1000 * 128 * 4) + _align(2 * 3 * 1000 * 4)
+    assert fa.fa_backward_workspace_bytes(2, 3, 1000, 128) == _align(2 * 3 * 1000 * 128 * 4) + _align(2 * 3 * 8 * 256 * 4)
     n = ctypes.c_size_t()
     assert B._lib.fa_backward_workspace_bytes(1, 1, 100, 80, ctypes.byref(n)) == UNSUPPORTED
     bm = _bm()
