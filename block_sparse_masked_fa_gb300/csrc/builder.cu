@@ -337,7 +337,7 @@ __global__ void __launch_bounds__(kBuildWarps * 32) classify_kernel(BuildArgs a)
           }
           return w;
         };
-        cnt += __popc(mask_word_rolled(a.mask, arg, i, jc, eq) & low_bits(j1 + 1 - jc));
+        cnt += __popc(mask_word_rolled(a.mask, arg, bm, i, jc, eq) & low_bits(j1 + 1 - jc));
       }
     }
     const int total = (int)__reduce_add_sync(0xffffffffu, (unsigned)cnt);

@@ -388,7 +388,7 @@ __global__ void __launch_bounds__(448, 1)
             }
             return bits;
           };
-          w = mask_word_t_rolled(p.mask, ctl->arg, j, i0, eq);
+          w = mask_word_t_rolled(p.mask, ctl->arg, bm, j, i0, eq);
         }
         float sv[32], dp[32];
         tmem_ld32x2f(tS + 32 * c, sv, tP + 32 * c, dp);

@@ -100,9 +100,10 @@ __device__ __forceinline__ uint32_t mask_word(const DevMask& m, const int32_t* a
 
 // Same as mask_word, with the node loop kept rolled: small code for the
 // attention kernels' partial tiles, where it runs 4 times per tile.
+// arg: resolved W / n_sink (node_arg); a PREFIX node reads prefix_len[bm] itself.
 template <class EqDoc>
-__device__ __forceinline__ uint32_t mask_word_rolled(const DevMask& m, const int32_t* arg, int64_t i, int64_t j0,
-                                                     EqDoc eq_doc) {
+__device__ __forceinline__ uint32_t mask_word_rolled(const DevMask& m, const int32_t* arg, int bm, int64_t i,
+                                                     int64_t j0, EqDoc eq_doc) {
   uint32_t s0 = 0, s1 = 0, s2 = 0, s3 = 0, s4 = 0, s5 = 0, s6 = 0, s7 = 0;
 #pragma unroll 1
   for (int k = 0; k < m.n; ++k) {
@@ -116,8 +117,10 @@ __device__ __forceinline__ uint32_t mask_word_rolled(const DevMask& m, const int
         w = low_bits(i - j0 + 1);
       } else if (op == FA_M_WINDOW) {
         w = ~low_bits(i - (int64_t)arg[k] + 1 - j0);
-      } else if (op == FA_M_SINK || op == FA_M_PREFIX) {
+      } else if (op == FA_M_SINK) {
         w = low_bits((int64_t)arg[k] - j0);
+      } else if (op == FA_M_PREFIX) {
+        w = low_bits((int64_t)__ldg(m.param[k] + bm) - j0);
       } else if (op == FA_M_SAME_DOC) {
         w = eq_doc();
       } else {
@@ -133,8 +136,8 @@ __device__ __forceinline__ uint32_t mask_word_rolled(const DevMask& m, const int
 // (bit c is pair (i0 + c, j)); used where a thread owns a key row.
 //  eq_doc()  word of (doc[i0 + c] == doc[j]) for c = 0..31
 template <class EqDoc>
-__device__ __forceinline__ uint32_t mask_word_t_rolled(const DevMask& m, const int32_t* arg, int64_t j, int64_t i0,
-                                                       EqDoc eq_doc) {
+__device__ __forceinline__ uint32_t mask_word_t_rolled(const DevMask& m, const int32_t* arg, int bm, int64_t j,
+                                                       int64_t i0, EqDoc eq_doc) {
   uint32_t s0 = 0, s1 = 0, s2 = 0, s3 = 0, s4 = 0, s5 = 0, s6 = 0, s7 = 0;
 #pragma unroll 1
   for (int k = 0; k < m.n; ++k) {
@@ -148,8 +151,10 @@ __device__ __forceinline__ uint32_t mask_word_t_rolled(const DevMask& m, const i
         w = ~low_bits(j - i0);                              // i >= j
       } else if (op == FA_M_WINDOW) {
         w = low_bits(j + (int64_t)arg[k] - i0);             // i < j + W
-      } else if (op == FA_M_SINK || op == FA_M_PREFIX) {
+      } else if (op == FA_M_SINK) {
         w = (j < (int64_t)arg[k]) ? 0xffffffffu : 0u;       // j < n
+      } else if (op == FA_M_PREFIX) {
+        w = (j < (int64_t)__ldg(m.param[k] + bm)) ? 0xffffffffu : 0u;
       } else if (op == FA_M_SAME_DOC) {
         w = eq_doc();
       } else {

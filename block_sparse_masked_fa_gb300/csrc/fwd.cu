@@ -267,7 +267,7 @@ __global__ void __launch_bounds__(192, 2)
               }
               return bits;
             };
-            w &= mask_word_rolled(p.mask, ctl->arg, i, jc, eq);
+            w &= mask_word_rolled(p.mask, ctl->arg, bm, i, jc, eq);
           }
           // select by c without dynamic indexing
           wd[0] = (c == 0) ? w : wd[0];
