@@ -15,7 +15,7 @@
 //                  tile for one bulk copy each, and a zeroed fp32 dq accumulator.
 //  2. bwd_kernel -- one CTA per (b, h, key tile J), key tiles longest first:
 //       warps 0-3  thread r owns key row r (TMEM lane r): P^T, dS^T
-//       warps 4-7  dq reducers: dQ tile from TMEM, fp32 atomics into the accumulator
+//       warps 8-11 dq reducers: dQ tile from TMEM, TMA bulk reduce-add into the accumulator
 //       warp 8     TMA producer: K_J, V_J once; Q_I, dO_I (+ LSE_I, Delta_I) per step
 //       warp 9     MMA issuer, five tcgen05 GEMMs per (I, J):
 //                    S^T  = K Q^T           (TMEM [0,128))
@@ -113,8 +113,8 @@ __global__ void __launch_bounds__(448, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_dv,
-               const __grid_constant__ AttnArgs p, const float* __restrict__ stats_g,
-               float* __restrict__ dq_acc) {
+               const __grid_constant__ CUtensorMap tm_dq, const __grid_constant__ AttnArgs p,
+               const float* __restrict__ stats_g) {
   using C = BwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -292,8 +292,7 @@ __global__ void __launch_bounds__(448, 1)
         for (int kk = 0; kk < 8; ++kk)  // dQ = dS K
           mma_ss(tmem + C::T_DP, sdesc_sw128(ds_base + kk * 2048, 16384, 1024),
                  sdesc_sw128(k_base + kk * 2048, 16384, 1024), kIdMM, kk > 0);
-        mma_commit(b_dq);
-        mma_commit(smem_u32(&ctl->q_empty[qs]));
+        mma_commit(b_dq);  // the dq reducers release the Q slot (they stage dQ in it)
       }
       if (ok)
         mma_commit(b_acc);
@@ -304,34 +303,59 @@ __global__ void __launch_bounds__(448, 1)
     }
   } else if (warp >= 8) {
     // ------------------------------------------------------------ dq reducers
+    // dQ tile: TMEM -> registers -> 128-byte-swizzled fp32 boxes (32 columns x
+    // 128 rows) staged in this step's Q slot (free: dK, the last reader of Q,
+    // is done) -> TMA bulk reduce-add into the fp32 accumulator.  Half of the
+    // tile fits the slot at a time.
     const int r = (warp % 4) * 32 + lane;  // TMEM lane = query row within the tile
     const uint32_t tq = tmem + ((uint32_t)((warp % 4) * 32) << 16) + C::T_DP;
+    constexpr int kHalfCols = D / 2;  // dQ columns per staging round
     bool ok = true;
     for (int it = 0; ok && it < n; ++it) {
       const int I = tile_of(it);
-      if (!warp_wait(b_dq, it & 1, &ctl->abort)) {
-        ok = false;
-        break;
-      }
+      const int qs = it % C::NQ;
+      ok = named_bar_and(2, 128, warp_wait(b_dq, it & 1, &ctl->abort));
+      if (!ok) break;
       tc_fence_after();
-      const int row = I * 128 + r;
-      float* dst = dq_acc + ((int64_t)bh * p.q_len + row) * D;
-#pragma unroll
-      for (int h2 = 0; h2 < D / 64; ++h2) {
-        float v[64];
-        tmem_ld64f(tq + 64 * h2, v);
-        if (h2 == D / 64 - 1) {
+      uint8_t* stage = sQ(qs);
+#pragma unroll 1
+      for (int h2 = 0; h2 < 2; ++h2) {
+        float v[kHalfCols];
+        if constexpr (kHalfCols == 64) {
+          tmem_ld64f(tq + kHalfCols * h2, v);
+        } else {
+          tmem_ld32f(tq + kHalfCols * h2, v);
+        }
+        if (h2 == 1) {
           tc_fence_before();
           mbar_arrive(b_dqf);  // TMEM columns free for the next dP^T
+          if (r == 0) bulk_wait_read0();  // the first half's reduce has read the staging
+          named_bar_sync(2, 128);
         }
-        if (row < p.q_len) {
 #pragma unroll
-          for (int k = 0; k < 16; ++k)
-            red_add_v4(dst + 64 * h2 + 4 * k, v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+        for (int bx = 0; bx < kHalfCols / 32; ++bx) {
+          uint8_t* rowp = stage + bx * 16384 + r * 128;
+#pragma unroll
+          for (int q4 = 0; q4 < 8; ++q4)
+            *reinterpret_cast<float4*>(rowp + ((q4 ^ (r & 7)) << 4)) =
+                make_float4(v[32 * bx + 4 * q4], v[32 * bx + 4 * q4 + 1], v[32 * bx + 4 * q4 + 2],
+                            v[32 * bx + 4 * q4 + 3]);
         }
+        fence_proxy_async_smem();
+        named_bar_sync(2, 128);
+        if (r == 0) {
+          for (int bx = 0; bx < kHalfCols / 32; ++bx)
+            tma_reduce_add_3d(&tm_dq, smem_u32(stage + bx * 16384), kHalfCols * h2 + 32 * bx, I * 128, bh);
+          bulk_commit();
+        }
+      }
+      if (r == 0) {
+        bulk_wait_read0();
+        mbar_arrive(smem_u32(&ctl->q_empty[qs]));  // the Q slot may be reloaded
       }
     }
     if (!ok) fail(p, ctl);
+    if (r == 0) bulk_wait0();  // every reduce of this CTA has completed
   } else {
     // ------------------------------------------------------------ P^T / dS^T, then the epilogue
     // warps 0-7: key row r = 32 (warp % 4) + lane; query columns [64 half, 64 half + 64)
@@ -436,8 +460,11 @@ __global__ void __launch_bounds__(448, 1)
       }
       tc_fence_after();
     }
-    uint8_t* stage_v = sQ(0);
-    uint8_t* stage_k = sQ(1);
+    // staging for dV / dK: the dS buffer and the first dO slot, whose last readers
+    // (the dK / dQ and dV MMAs) are done once acc_full completes; the Q slots may
+    // still hold the dq reducers' last staged tile
+    uint8_t* stage_v = sDS;
+    uint8_t* stage_k = sDO(0);
     if (ok && !skip) {
 #pragma unroll 1
       for (int c2 = 0; c2 < D / 64; ++c2) {
@@ -549,8 +576,11 @@ cudaError_t launch_bwd_t(const AttnArgs& a, const BwdTensors& t, cudaStream_t st
     return encode_tmap_3d(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, ptr, D, len, bh, 64, 128,
                           CU_TENSOR_MAP_SWIZZLE_128B);
   };
+  CUtensorMap mdq;
   const bool ok = enc(&mq, t.q, a.q_len) && enc(&mk, t.k, a.kv_len) && enc(&mv, t.v, a.kv_len) &&
-                  enc(&mdo, t.dout, a.q_len) && enc(&mdk, t.dk, a.kv_len) && enc(&mdv, t.dv, a.kv_len);
+                  enc(&mdo, t.dout, a.q_len) && enc(&mdk, t.dk, a.kv_len) && enc(&mdv, t.dv, a.kv_len) &&
+                  encode_tmap_3d(&mdq, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, t.dq_acc, D, a.q_len, bh, 32, 128,
+                                 CU_TENSOR_MAP_SWIZZLE_128B);
   if (!ok) {
     *enc_failed = true;
     return cudaErrorUnknown;
@@ -563,7 +593,7 @@ cudaError_t launch_bwd_t(const AttnArgs& a, const BwdTensors& t, cudaStream_t st
     attr_set = true;
   }
   const int64_t items = (int64_t)a.B * a.H * a.nkv;
-  bwd_kernel<D, SCORE><<<(unsigned)items, BwdCfg<D>::THREADS, smem, stream>>>(mq, mk, mv, mdo, mdk, mdv, a, t.stats, t.dq_acc);
+  bwd_kernel<D, SCORE><<<(unsigned)items, BwdCfg<D>::THREADS, smem, stream>>>(mq, mk, mv, mdo, mdk, mdv, mdq, a, t.stats);
   const int64_t n8 = rows * D / 8;
   bwd_dq_convert_kernel<<<(unsigned)((n8 + 255) / 256), 256, 0, stream>>>(
       t.dq_acc, static_cast<__nv_bfloat16*>(t.dq), n8, a.scale);
