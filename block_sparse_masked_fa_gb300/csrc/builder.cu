@@ -18,9 +18,9 @@
 //                     column: ballot + popcount prefix sums turn the class
 //                     bytes into ascending PARTIAL and FULL index lists with
 //                     zeroed tails (the columns' lists feed the backward).
-//  4. order        -- rows and columns sorted by descending tile count with a
-//                     stable counting sort, the order the attention kernels
-//                     take their work in (longest first, then by index).
+//  4. order        -- the order the attention kernels take rows and columns
+//                     in: longest first (rows by exact, columns by quantized
+//                     tile count), index order within a bucket.
 #include "internal.h"
 
 namespace fa {
@@ -382,26 +382,42 @@ __global__ void __launch_bounds__(kBuildWarps * 32) compact_kernel(BuildArgs a) 
   }
 }
 
-// Stable counting sort by descending (num + full_num): block 0 orders the
-// rows, block 1 the columns.  Stable, so items of equal length keep their
-// index order and neighbouring tiles run together (L2 reuse of K / V, Q / dO
-// and the dq accumulator).  hist has max(nq, nkv) + 1 buckets in shared memory.
+// Work order: block 0 orders the rows (forward), block 1 the columns
+// (backward), longest first so that long lists do not end the grid.  The
+// forward's rows are sorted by exact count.  For the backward, exact count
+// order scatters neighbouring tiles when counts are noisy (document masks)
+// and loses the L2 reuse of Q / dO and of the dq accumulator, so its key is
+// the count quantized to q = ceil(cmax / 16) (cmax: the largest count), with
+// everything in one bucket (index order) when cmax <= 16.  A stable counting
+// sort keeps index order inside each bucket.  The histogram has kOrderBuckets
+// entries; coarser buckets are used if the counts would need more.
+constexpr int kOrderBuckets = 4096;
+
 __global__ void __launch_bounds__(1024) order_kernel(BuildArgs a) {
-  extern __shared__ int32_t hist[];
+  extern __shared__ int32_t hist[];  // kOrderBuckets entries
+  __shared__ int s_cmax;
   const bool rows = blockIdx.x == 0;
   const int32_t* num = rows ? a.kv_num : a.q_num;
   const int32_t* full_num = rows ? a.full_num : a.full_q_num;
   int32_t* order = rows ? a.row_order : a.col_order;
   const int n = rows ? a.Bm * a.Hm * a.nq : a.Bm * a.Hm * a.nkv;
-  const int max_count = rows ? a.nkv : a.nq;
-  const int nb = max_count + 1;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  if (threadIdx.x == 0) s_cmax = 0;
+  __syncthreads();
+  int cm = 0;
+  for (int r = threadIdx.x; r < n; r += blockDim.x) cm = max(cm, num[r] + full_num[r]);
+  cm = __reduce_max_sync(0xffffffffu, cm);
+  if (lane == 0) atomicMax(&s_cmax, cm);
+  __syncthreads();
+  const int cmax = s_cmax;
+  int qz = rows ? 1 : ((cmax <= 16) ? cmax + 1 : (cmax + 15) / 16);  // bucket width
+  qz = max(qz, (cmax + kOrderBuckets) / kOrderBuckets);              // at most kOrderBuckets buckets
+  const int top = min(cmax / qz, kOrderBuckets - 1);                 // largest bucket
+  const int nb = top + 1;
   for (int k = threadIdx.x; k < nb; k += blockDim.x) hist[k] = 0;
   __syncthreads();
-  for (int r = threadIdx.x; r < n; r += blockDim.x) {
-    const int c = min(num[r] + full_num[r], max_count);
-    atomicAdd(&hist[max_count - c], 1);
-  }
+  for (int r = threadIdx.x; r < n; r += blockDim.x)
+    atomicAdd(&hist[top - min((num[r] + full_num[r]) / qz, top)], 1);
   __syncthreads();
   // exclusive scan, one warp
   if (warp == 0) {
@@ -425,7 +441,7 @@ __global__ void __launch_bounds__(1024) order_kernel(BuildArgs a) {
   for (int round = 0; round < n; round += blockDim.x) {
     const int r = round + threadIdx.x;
     const bool valid = r < n;
-    const int bucket = valid ? max_count - min(num[r] + full_num[r], max_count) : -1;
+    const int bucket = valid ? top - min((num[r] + full_num[r]) / qz, top) : -1;
     const uint32_t peers = __match_any_sync(0xffffffffu, bucket);
     const int leader = __ffs(peers) - 1;
     int off = 0;
@@ -441,14 +457,6 @@ __global__ void __launch_bounds__(1024) order_kernel(BuildArgs a) {
   }
 }
 
-__global__ void identity_order_kernel(BuildArgs a) {
-  const int64_t rows = (int64_t)a.Bm * a.Hm * a.nq, cols = (int64_t)a.Bm * a.Hm * a.nkv;
-  const int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (r < rows) a.row_order[r] = (int32_t)r;
-  else if (r < rows + cols) a.col_order[r - rows] = (int32_t)(r - rows);
-}
-
-constexpr int kMaxSortBuckets = 12 * 1024;  // 48 KB of shared memory
 
 }  // namespace
 
@@ -467,10 +475,7 @@ cudaError_t launch_build(const BuildArgs& a, cudaStream_t stream) {
   const int64_t cwarps = rows * ((a.nkv + 31) / 32);
   classify_kernel<<<(unsigned)((cwarps + kBuildWarps - 1) / kBuildWarps), kBuildWarps * 32, 0, stream>>>(a);
   compact_kernel<<<(unsigned)((rows + cols + kBuildWarps - 1) / kBuildWarps), kBuildWarps * 32, 0, stream>>>(a);
-  if (tmax + 1 <= kMaxSortBuckets)
-    order_kernel<<<2, 1024, (size_t)(tmax + 1) * sizeof(int32_t), stream>>>(a);
-  else
-    identity_order_kernel<<<(unsigned)((rows + cols + 255) / 256), 256, 0, stream>>>(a);
+  order_kernel<<<2, 1024, kOrderBuckets * sizeof(int32_t), stream>>>(a);
   return cudaGetLastError();
 }
 

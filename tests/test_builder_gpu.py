@@ -33,12 +33,17 @@ def compare(bm, cls, lists):
     np.testing.assert_array_equal(bm.tile_class().cpu().numpy(), cls.astype(np.uint8))
     for n in LIST_NAMES:
         np.testing.assert_array_equal(got[n], lists[n], err_msg=n)
-    order = bm.row_order().cpu().numpy()
-    assert sorted(order.tolist()) == list(range(order.size))
-    work = (got["kv_num_blocks"] + got["full_kv_num_blocks"]).reshape(-1)[order]
-    assert np.all(np.diff(work) <= 0)                     # longest rows first
-    ties = np.diff(work) == 0
-    assert np.all(np.diff(order)[ties] > 0)               # stable: index order among equal lengths
+    # work orders: rows by exact count, columns by count quantized to ceil(cmax / 16)
+    # (one bucket when cmax <= 16); longest bucket first, index order inside a bucket
+    for field, n_key, f_key, quantized in (("row_order", "kv_num_blocks", "full_kv_num_blocks", False),
+                                           ("col_order", "q_num_blocks", "full_q_num_blocks", True)):
+        work = (got[n_key] + got[f_key]).reshape(-1)
+        off = getattr(bm.struct, field) - bm.buffer.data_ptr()
+        order = bm.buffer[off:off + 4 * work.size].view(torch.int32).cpu().numpy()
+        cmax = int(work.max())
+        qz = (cmax + 1 if cmax <= 16 else -(-cmax // 16)) if quantized else 1
+        expect = sorted(range(work.size), key=lambda r: (-(work[r] // qz), r))
+        np.testing.assert_array_equal(order, np.array(expect), err_msg=field)
     assert fa.fa_get_status(bm) == 0
 
 
