@@ -45,8 +45,7 @@ fa_status make_layout(int32_t Bm, int32_t Hm, int64_t q_len, int64_t kv_len, int
       (size_t)cols * 4,  (size_t)tiles * 4, (size_t)cols * 4, (size_t)tiles * 4,
       (size_t)rows * 4,  (size_t)cols * 4,  (size_t)tiles,
       (size_t)Bm * 2 * (size_t)(nq > nkv ? nq : nkv) * 4 * 4,
-      (size_t)Bm * (size_t)(q_len > kv_len ? q_len : kv_len) * 8 + (size_t)Bm * 4 +
-          (size_t)Bm * (size_t)(((q_len > kv_len ? q_len : kv_len) + 4095) / 4096) * 12,
+      (size_t)Bm * (size_t)(q_len > kv_len ? q_len : kv_len) * 8 + (size_t)Bm * 4,
       4};
   size_t at = 0;
   for (int k = 0; k < Layout::N; ++k) {

@@ -6,7 +6,7 @@
 //
 // Kernels, all stream-ordered, no host synchronisation:
 //  1. tile_summary -- doc-id min / max of every query and key tile, and
-//     doc_runs        the run of equal ids around every position (only when
+//     doc_runs        the range of equal ids around every position (only when
 //                     the program has SAME_DOC).
 //  2. classify     -- one warp per (query-tile row, chunk of 32 key tiles).
 //                     Each lane classifies one tile with a three-valued
@@ -83,11 +83,15 @@ __device__ int program_interval(const DevMask& m, const int32_t* arg, int64_t i0
   return s0;
 }
 
-__global__ void tile_summary_kernel(BuildArgs a) {
+__global__ void tile_summary_kernel(const __grid_constant__ BuildArgs a) {
   const int warps = blockDim.x / 32;
   const int64_t w = (int64_t)blockIdx.x * warps + threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
   const int tmax = max(a.nq, a.nkv);
+  if (w < a.Bm && lane == 0) {  // preset "sorted"; doc_runs clears it at the first decrease
+    const int64_t L = max(a.q_len, a.kv_len);
+    a.doc_runs[(int64_t)a.Bm * L * 2 + w] = 1;
+  }
   if (w >= (int64_t)a.Bm * 2 * tmax) return;
   const int t = (int)(w % tmax);
   const int which = (int)((w / tmax) % 2);  // 0: query tiles, 1: key tiles
@@ -122,141 +126,30 @@ __global__ void tile_summary_kernel(BuildArgs a) {
 }
 
 // Runs of equal document ids, for PARTIAL tiles: for every position x < L =
-// max(q_len, kv_len) of batch row bm, [lo, hi) is the maximal run of
-// neighbouring positions whose id equals doc[x], and sorted[bm] says whether
-// the ids never decrease -- then doc[y] == doc[x] exactly when y lies in x's
-// run.  A position q is a run start when q == 0 or doc[q] != doc[q - 1];
-// lo[x] is the last run start <= x and hi[x] the first run start > x (or L).
-// Two passes over segments of kSegLen positions:
-//   doc_runs_local   -- per segment: run starts found inside the segment
-//                       (block scans), the segment's last / first run start and
-//                       whether its ids decrease;
-//   doc_runs_combine -- folds in the other segments' aggregates.
-constexpr int kRunE = 16;
-constexpr int kRunThreads = 256;
-constexpr int kSegLen = kRunE * kRunThreads;  // 4096 positions
-
-__device__ __forceinline__ int block_scan_max_excl(int v, int* s_warp, int identity) {
-  // exclusive max-scan over threadIdx.x; also leaves the block max in s_warp[32]
-  const int lane = threadIdx.x % 32, warp = threadIdx.x / 32;
-  const int nwarps = blockDim.x / 32;
-  int incl = v;
-#pragma unroll
-  for (int d = 1; d < 32; d <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, incl, d);
-    if (lane >= d) incl = max(incl, y);
-  }
-  if (lane == 31) s_warp[warp] = incl;
-  __syncthreads();
-  if (warp == 0) {
-    int w = (lane < nwarps) ? s_warp[lane] : identity;
-#pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, w, d);
-      if (lane >= d) w = max(w, y);
-    }
-    s_warp[lane] = w;  // inclusive over warps
-    if (lane == 31) s_warp[32] = w;
-  }
-  __syncthreads();
-  const int before_warp = (warp > 0) ? s_warp[warp - 1] : identity;
-  const int excl_lane = __shfl_up_sync(0xffffffffu, incl, 1);
-  const int r = max(before_warp, lane > 0 ? excl_lane : identity);
-  __syncthreads();
-  return r;
-}
-
-// Segment aggregates live after the runs and the sorted flags:
-// [Bm][nseg][3] = last run start in the segment (-1 if none), first run
-// start after the segment's first position... (see below), unsorted flag.
-__device__ __forceinline__ int32_t* seg_aggr(const BuildArgs& a, int64_t L) {
-  return a.doc_runs + (int64_t)a.Bm * L * 2 + a.Bm;
-}
-
-__global__ void __launch_bounds__(kRunThreads) doc_runs_local_kernel(BuildArgs a) {
-  __shared__ int s_warp[33];
-  __shared__ int s_unsorted;
+// max(q_len, kv_len) of batch row bm, [lo, hi) is the range of positions whose
+// id equals doc[x], valid when the row's ids never decrease (sorted[bm] = 1,
+// preset by tile_summary and cleared here at the first decrease): then
+// doc[y] == doc[x] exactly for y in [lo, hi), and lo / hi are the lower /
+// upper bound of doc[x] in the row, found by binary search.
+__global__ void __launch_bounds__(256) doc_runs_kernel(const __grid_constant__ BuildArgs a) {
   const int L = (int)max(a.q_len, a.kv_len);
-  const int nseg = (L + kSegLen - 1) / kSegLen;
-  const int bm = blockIdx.x / nseg, seg = blockIdx.x % nseg;
+  const int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (gid >= (int64_t)a.Bm * L) return;
+  const int bm = (int)(gid / L), x = (int)(gid % L);
   const int32_t* doc = a.mask.doc + (int64_t)bm * a.mask.doc_len;
-  int32_t* run = a.doc_runs + (int64_t)bm * L * 2;
-  if (threadIdx.x == 0) s_unsorted = 0;
-  __syncthreads();
-  const int x0 = seg * kSegLen + threadIdx.x * kRunE;
-  // left to right: last run start <= x inside the segment (-1: none)
-  int last = -1;
-  bool unsorted = false;
-  int lo_local[kRunE];
-#pragma unroll
-  for (int k = 0; k < kRunE; ++k) {
-    const int x = x0 + k;
-    if (x < L) {
-      const int d = __ldg(doc + x);
-      const int dp = (x > 0) ? __ldg(doc + x - 1) : d;
-      if (x == 0 || d != dp) last = x;
-      unsorted |= d < dp;
-    }
-    lo_local[k] = last;
+  const int d = __ldg(doc + x);
+  if (x > 0 && __ldg(doc + x - 1) > d) atomicAnd(a.doc_runs + (int64_t)a.Bm * L * 2 + bm, 0);
+  int lo = 0, hi = x;  // first position with id >= d lies in [0, x]
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (__ldg(doc + mid) < d) lo = mid + 1; else hi = mid;
   }
-  if (unsorted) s_unsorted = 1;
-  const int before = block_scan_max_excl(last, s_warp, -1);
-  const int seg_last = s_warp[32];
-#pragma unroll
-  for (int k = 0; k < kRunE; ++k)
-    if (x0 + k < L) run[2 * (x0 + k)] = max(lo_local[k], before);
-  // right to left: first run start q > x with q inside (x, segment end] or q == L
-  // (max-scan of negated positions over mirrored threads; -2^30 = none)
-  const int mx0 = seg * kSegLen + (kRunThreads - 1 - threadIdx.x) * kRunE;
-  const int seg_end = min(seg * kSegLen + kSegLen, L);  // q may equal seg_end
-  int first = -(1 << 30);
-  int hi_local[kRunE];
-#pragma unroll
-  for (int k = kRunE - 1; k >= 0; --k) {
-    const int x = mx0 + k;
-    if (x < L) {
-      const int q = x + 1;
-      if (q == L || (q <= seg_end && __ldg(doc + q) != __ldg(doc + x))) first = -q;
-    }
-    hi_local[k] = first;
+  int lo2 = x + 1, hi2 = L;  // first position with id > d lies in [x + 1, L]
+  while (lo2 < hi2) {
+    const int mid = (lo2 + hi2) >> 1;
+    if (__ldg(doc + mid) <= d) lo2 = mid + 1; else hi2 = mid;
   }
-  const int before_r = block_scan_max_excl(first, s_warp, -(1 << 30));
-  const int seg_first = s_warp[32];  // -(first run start in (seg start, seg end]), or -2^30
-#pragma unroll
-  for (int k = 0; k < kRunE; ++k)
-    if (mx0 + k < L) run[2 * (mx0 + k) + 1] = -max(hi_local[k], before_r);
-  if (threadIdx.x == 0) {
-    int32_t* g = seg_aggr(a, L) + ((int64_t)bm * nseg + seg) * 3;
-    g[0] = seg_last;
-    g[1] = seg_first;
-    g[2] = s_unsorted;
-  }
-}
-
-__global__ void __launch_bounds__(kRunThreads) doc_runs_combine_kernel(BuildArgs a) {
-  __shared__ int s_lo, s_hi, s_unsorted;
-  const int L = (int)max(a.q_len, a.kv_len);
-  const int nseg = (L + kSegLen - 1) / kSegLen;
-  const int bm = blockIdx.x / nseg, seg = blockIdx.x % nseg;
-  const int32_t* g = seg_aggr(a, L) + (int64_t)bm * nseg * 3;
-  if (threadIdx.x == 0) {
-    int lo = -1, hi = -(1 << 30), uns = 0;
-    for (int s2 = 0; s2 < seg; ++s2) lo = max(lo, g[3 * s2]);
-    for (int s2 = nseg - 1; s2 > seg; --s2) hi = max(hi, g[3 * s2 + 1]);
-    for (int s2 = 0; s2 < nseg; ++s2) uns |= g[3 * s2 + 2];
-    s_lo = lo;
-    s_hi = hi;
-    s_unsorted = uns;
-  }
-  __syncthreads();
-  int32_t* run = a.doc_runs + (int64_t)bm * L * 2;
-  const int x_end = min(seg * kSegLen + kSegLen, L);
-  for (int x = seg * kSegLen + threadIdx.x; x < x_end; x += blockDim.x) {
-    run[2 * x] = max(run[2 * x], s_lo);
-    const int h = run[2 * x + 1];
-    if (h == (1 << 30)) run[2 * x + 1] = (s_hi == -(1 << 30)) ? L : -s_hi;
-  }
-  if (seg == 0 && threadIdx.x == 0) a.doc_runs[(int64_t)a.Bm * L * 2 + bm] = s_unsorted ? 0 : 1;
+  reinterpret_cast<int2*>(a.doc_runs)[gid] = make_int2(lo, lo2);
 }
 
 constexpr int kBuildWarps = 8;
@@ -264,7 +157,7 @@ constexpr int kBuildWarps = 8;
 // One warp per (query-tile row, chunk of 32 key tiles): each lane classifies
 // one tile; undecided tiles are settled exactly by the whole warp.  Writes
 // the class bytes only; compaction into lists is a separate pass.
-__global__ void __launch_bounds__(kBuildWarps * 32) classify_kernel(BuildArgs a) {
+__global__ void __launch_bounds__(kBuildWarps * 32) classify_kernel(const __grid_constant__ BuildArgs a) {
   __shared__ int32_t s_arg[kBuildWarps][FA_MAX_MASK_NODES];
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int nchunk = (a.nkv + 31) / 32;
@@ -349,7 +242,7 @@ __global__ void __launch_bounds__(kBuildWarps * 32) classify_kernel(BuildArgs a)
 
 // Compaction: warps [0, rows) build the per-row lists, the next [0, cols)
 // warps the per-column lists, both with ballots over the class bytes.
-__global__ void __launch_bounds__(kBuildWarps * 32) compact_kernel(BuildArgs a) {
+__global__ void __launch_bounds__(kBuildWarps * 32) compact_kernel(const __grid_constant__ BuildArgs a) {
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int64_t wid = (int64_t)blockIdx.x * kBuildWarps + warp;
   const int64_t rows = (int64_t)a.Bm * a.Hm * a.nq, cols = (int64_t)a.Bm * a.Hm * a.nkv;
@@ -393,7 +286,7 @@ __global__ void __launch_bounds__(kBuildWarps * 32) compact_kernel(BuildArgs a) 
 // entries; coarser buckets are used if the counts would need more.
 constexpr int kOrderBuckets = 4096;
 
-__global__ void __launch_bounds__(1024) order_kernel(BuildArgs a) {
+__global__ void __launch_bounds__(1024) order_kernel(const __grid_constant__ BuildArgs a) {
   extern __shared__ int32_t hist[];  // kOrderBuckets entries
   __shared__ int s_cmax;
   const bool rows = blockIdx.x == 0;
@@ -465,10 +358,8 @@ cudaError_t launch_build(const BuildArgs& a, cudaStream_t stream) {
   if (a.mask.has_doc) {
     const int64_t warps = (int64_t)a.Bm * 2 * tmax;
     tile_summary_kernel<<<(unsigned)((warps + 7) / 8), 256, 0, stream>>>(a);
-    const int L = (int)(a.q_len > a.kv_len ? a.q_len : a.kv_len);
-    const unsigned segs = (unsigned)(a.Bm * ((L + kSegLen - 1) / kSegLen));
-    doc_runs_local_kernel<<<segs, kRunThreads, 0, stream>>>(a);
-    doc_runs_combine_kernel<<<segs, kRunThreads, 0, stream>>>(a);
+    const int64_t L = a.q_len > a.kv_len ? a.q_len : a.kv_len;
+    doc_runs_kernel<<<(unsigned)((a.Bm * L + 255) / 256), 256, 0, stream>>>(a);
   }
   const int64_t rows = (int64_t)a.Bm * a.Hm * a.nq;
   const int64_t cols = (int64_t)a.Bm * a.Hm * a.nkv;

@@ -135,8 +135,7 @@ typedef struct {
  *   row_order, col_order: rows / columns sorted by descending tile count (the
  *                      order the attention kernels take their work in).
  *   tile_class         uint8 [Bm][Hm][nq][nkv]: 0 EMPTY, 1 PARTIAL, 2 FULL.
- *   doc_runs           int32 [Bm][max(q_len, kv_len)][2], int32 [Bm] (then
- *                      builder scratch): for
+ *   doc_runs           int32 [Bm][max(q_len, kv_len)][2] then int32 [Bm]: for
  *                      every position the run [lo, hi) of neighbouring positions
  *                      with the same document id, and per batch row a flag set
  *                      when the ids never decrease (then doc[i] == doc[j] iff j

@@ -127,7 +127,8 @@ def _runs_expected(doc, L):
 
 @pytest.mark.parametrize("case", ["sorted_multi_chunk", "unsorted_repeats", "ragged_cross", "one_doc"])
 def test_doc_runs_table(case):
-    """The per-position run table the kernels use on PARTIAL tiles, bit-exact."""
+    """The per-position run table the kernels use on PARTIAL tiles, bit-exact
+    (the ranges for rows with sorted ids, the sorted flag for every row)."""
     rng = np.random.default_rng(7)
     if case == "sorted_multi_chunk":
         q_len = kv_len = 40000                       # several 16K-position chunks
@@ -151,6 +152,7 @@ def test_doc_runs_table(case):
     flags = raw[2 * L * 2:]
     for b in range(2):
         lo, hi, srt = _runs_expected(docs[b], L)
-        np.testing.assert_array_equal(runs[b, :, 0], lo)
-        np.testing.assert_array_equal(runs[b, :, 1], hi)
         assert flags[b] == srt
+        if srt:  # the kernels use the ranges only for rows whose ids never decrease
+            np.testing.assert_array_equal(runs[b, :, 0], lo)
+            np.testing.assert_array_equal(runs[b, :, 1], hi)
