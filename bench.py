@@ -33,6 +33,36 @@ PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}
 METRIC = "attention TFLOP/s over visible tiles (fwd+bwd)"
 
 
+def source_digest() -> str:
+    """sha256 over the CUDA sources and the C header: the kernels the counters describe."""
+    import hashlib
+
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "block_sparse_masked_fa_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + b"\0" + f.read())
+    with open(os.path.join(ROOT, "include", "fa.h"), "rb") as f:
+        h.update(f.read())
+    return h.hexdigest()
+
+
+def recorded_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch of `kernel` from the committed ncu record, or None when
+    the record is missing or was taken on other sources or another workload."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    entry = rec.get("kernels", {}).get(kernel)
+    if not entry or rec.get("source_sha256") != source_digest() or entry.get("workload") != workload:
+        return None
+    return entry.get("dram_bytes_per_launch")
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -286,7 +316,8 @@ def run_gpu(args):
         "bwd_tflops": round(bwd_flops / (bwd_ms * 1e-3) / 1e12, 2) if have_bwd else None,
         "roofline": {"kernel": dominant, "bound": "tensor", "achieved": round(achieved, 2), "peak": peak,
                      "peak_source": f"bf16_tflops ({peak_src}, burst)", "unit": "TFLOP/s",
-                     "frac": round(achieved / peak, 4), "traffic": None},
+                     "frac": round(achieved / peak, 4),
+                     "traffic": recorded_traffic("bwd_kernel" if dominant == "bwd" else "fwd_kernel", w.name)},
         "e2e": {"value": round(world * step_flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
                 "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
         "gpu_launches": launches_per_step * args.steps,
