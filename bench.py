@@ -290,8 +290,9 @@ def run_gpu(args):
     dom_flops = bwd_flops if dominant == "bwd" else fwd_flops
     achieved = dom_flops / (dom_ms * 1e-3) / 1e12
     value = world * step_flops / (ms_step * 1e-3) / 1e12
-    # builder: (tile_summary) + classify + compact + order; forward 1; backward pre + main + dq convert
-    launches_per_step = (4 if docs is not None else 3) + 1 + (3 if have_bwd else 0)
+    # builder: (tile_summary + doc_runs) + row_segs + classify + compact + order; forward 1;
+    # backward pre + main + dq convert
+    launches_per_step = (6 if docs is not None else 4) + 1 + (3 if have_bwd else 0)
     res = {
         "metric": METRIC if have_bwd else "attention TFLOP/s over visible tiles (fwd only; bwd not built)",
         "value": round(value, 2),

@@ -58,7 +58,7 @@ class BlockMaskStruct(ctypes.Structure):
                [(name, ctypes.c_void_p) for name in (
                    "kv_num_blocks", "kv_indices", "full_kv_num_blocks", "full_kv_indices",
                    "q_num_blocks", "q_indices", "full_q_num_blocks", "full_q_indices",
-                   "row_order", "col_order", "tile_class", "tile_summary", "doc_runs", "status")] + \
+                   "row_order", "col_order", "tile_class", "tile_summary", "doc_runs", "row_segs", "status")] + \
                [("spec", MaskSpec)]
 
 
@@ -201,6 +201,12 @@ class BlockMask:
     def row_order(self) -> torch.Tensor:
         s = self.struct
         return self._view("row_order", (s.Bm * s.Hm * s.nq,))
+
+    def row_segs(self) -> torch.Tensor:
+        """[Bm, 2, max(q_len, kv_len), 4] int32: per query row (0) / key column (1)
+        the visible intervals [lo0, hi0) and [lo1, hi1), lo0 = -1 if not summarised."""
+        s = self.struct
+        return self._view("row_segs", (s.Bm, 2, max(s.q_len, s.kv_len), 4))
 
 
 def fa_block_mask_bytes(Bm: int, Hm: int, q_len: int, kv_len: int, block: int = 128) -> int:

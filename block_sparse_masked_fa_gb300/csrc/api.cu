@@ -24,7 +24,7 @@ bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0
 struct Layout {
   enum {
     KV_NUM, KV_IDX, FULL_NUM, FULL_IDX, Q_NUM, Q_IDX, FULL_Q_NUM, FULL_Q_IDX, ROW_ORDER, COL_ORDER, TILE_CLASS,
-    SUMMARY, DOC_RUNS, STATUS, N
+    SUMMARY, DOC_RUNS, ROW_SEGS, STATUS, N
   };
   size_t off[N];
   size_t total;
@@ -46,6 +46,7 @@ fa_status make_layout(int32_t Bm, int32_t Hm, int64_t q_len, int64_t kv_len, int
       (size_t)rows * 4,  (size_t)cols * 4,  (size_t)tiles,
       (size_t)Bm * 2 * (size_t)(nq > nkv ? nq : nkv) * 4 * 4,
       (size_t)Bm * (size_t)(q_len > kv_len ? q_len : kv_len) * 8 + (size_t)Bm * 4,
+      (size_t)Bm * 2 * (size_t)(q_len > kv_len ? q_len : kv_len) * 16,
       4};
   size_t at = 0;
   for (int k = 0; k < Layout::N; ++k) {
@@ -174,6 +175,8 @@ AttnArgs attn_args(int32_t B, int32_t H, int64_t q_len, int64_t kv_len, int32_t 
   a.score_param = score ? score->param : nullptr;
   a.status = bm->status;
   a.mask = dm;
+  a.row_segs = reinterpret_cast<const int4*>(bm->row_segs);
+  a.seg_len = bm->q_len > bm->kv_len ? bm->q_len : bm->kv_len;
   if (dm.has_doc && bm->doc_runs != nullptr) {
     const int64_t run_len = bm->q_len > bm->kv_len ? bm->q_len : bm->kv_len;
     a.mask.runs = bm->doc_runs;
@@ -265,6 +268,7 @@ fa_status fa_create_block_mask(const fa_mask_spec* spec, int32_t Bm, int32_t Hm,
   bm->tile_class = base + L.off[Layout::TILE_CLASS];
   bm->tile_summary = i32(Layout::SUMMARY);
   bm->doc_runs = i32(Layout::DOC_RUNS);
+  bm->row_segs = i32(Layout::ROW_SEGS);
   bm->status = reinterpret_cast<uint32_t*>(base + L.off[Layout::STATUS]);
   bm->spec = *spec;
 
@@ -293,6 +297,7 @@ fa_status fa_create_block_mask(const fa_mask_spec* spec, int32_t Bm, int32_t Hm,
   a.tile_class = bm->tile_class;
   a.summary = bm->tile_summary;
   a.doc_runs = bm->doc_runs;
+  a.row_segs = bm->row_segs;
   a.status = bm->status;
   if (dm.has_doc) {  // classify reads the run table that the builder fills first
     const int64_t run_len = q_len > kv_len ? q_len : kv_len;

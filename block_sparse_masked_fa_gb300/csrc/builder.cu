@@ -21,6 +21,10 @@
 //  4. order        -- the order the attention kernels take rows and columns
 //                     in: longest first (rows by exact, columns by quantized
 //                     tile count), index order within a bucket.
+//  and row_segs    -- every query row's visible key columns (and every key
+//                     column's visible query rows) as at most two intervals,
+//                     which the attention kernels' PARTIAL tiles read instead
+//                     of running the program per word.
 #include "internal.h"
 
 namespace fa {
@@ -152,6 +156,153 @@ __global__ void __launch_bounds__(256) doc_runs_kernel(const __grid_constant__ B
   reinterpret_cast<int2*>(a.doc_runs)[gid] = make_int2(lo, lo2);
 }
 
+// ---- The visible set of one row as intervals
+//
+// Fix one index x and let the other, y, vary: x = query row i and y = key
+// column j, or (transposed) x = key column j and y = query row i.  Every atom
+// is then visible on an interval of y -- SAME_DOC too when the ids never
+// decrease, through the run [lo, hi) holding x -- so the program's value can
+// only change at the atoms' interval ends.  row_segments evaluates the program
+// once between consecutive ends and keeps the visible pieces, merged, when
+// there are at most two; the attention kernels then build a 32-bit word from
+// two range tests (seg_word) instead of running the program.  Rows that need
+// more pieces, or ids that decrease somewhere, keep the per-word evaluation.
+struct RowSegs {
+  int n;  // visible intervals (0..2), or -1 when the row is not represented
+  int lo0, hi0, lo1, hi1;
+};
+
+// The program's value at one pair (x, y).
+__device__ __forceinline__ bool mask_bit(int nn, uint64_t ops, const int32_t* arg, bool transposed, int64_t x,
+                                         int64_t y, int run_lo, int run_hi) {
+  const int64_t i = transposed ? y : x, j = transposed ? x : y;
+  uint32_t st = 0;  // bit stack, top at bit 0
+#pragma unroll 1
+  for (int k = 0; k < nn; ++k, ops >>= 4) {
+    const int op = (int)(ops & 15u);
+    if (op == FA_M_AND || op == FA_M_OR) {
+      const uint32_t a = st & 1u, b = (st >> 1) & 1u;
+      st = ((st >> 2) << 1) | (op == FA_M_AND ? (a & b) : (a | b));
+    } else {
+      bool v = true;
+      if (op == FA_M_CAUSAL) v = i >= j;
+      else if (op == FA_M_WINDOW) v = i - j < (int64_t)arg[k];
+      else if (op == FA_M_SINK || op == FA_M_PREFIX) v = j < (int64_t)arg[k];
+      else if (op == FA_M_SAME_DOC) v = y >= run_lo && y < run_hi;
+      st = (st << 1) | (v ? 1u : 0u);
+    }
+  }
+  return (st & 1u) != 0;
+}
+
+//  len            extent of y (kv_len, or q_len when transposed)
+//  have_run       the ids never decrease and [run_lo, run_hi) is x's run
+// Everything stays in registers (constant indices only): at most kRowBreaks
+// interval ends besides 0, else the row is left to the per-word evaluation.
+constexpr int kRowBreaks = 8;
+
+__device__ __forceinline__ void cswap(int64_t& a, int64_t& b) {
+  const int64_t lo = a < b ? a : b, hi = a < b ? b : a;
+  a = lo;
+  b = hi;
+}
+
+__device__ RowSegs row_segments(int nn, uint64_t ops, const int32_t* arg, bool transposed,
+                                                    int64_t x, bool have_run, int run_lo, int run_hi, int64_t len) {
+  RowSegs seg{-1, 0, 0, 0, 0};
+  int64_t bp[kRowBreaks];
+#pragma unroll
+  for (int t = 0; t < kRowBreaks; ++t) bp[t] = len;
+  bp[0] = 0;
+  int nb = 1;
+  uint64_t o = ops;
+#pragma unroll 1
+  for (int k = 0; k < nn; ++k, o >>= 4) {
+    const int op = (int)(o & 15u);
+    int64_t v0 = 0, v1 = 0;
+    int add = 0;
+    if (op == FA_M_SAME_DOC) {
+      if (!have_run) return seg;
+      v0 = run_lo;
+      v1 = run_hi;
+      add = 2;
+    } else if (op == FA_M_CAUSAL) {
+      v0 = transposed ? x : x + 1;
+      add = 1;
+    } else if (op == FA_M_WINDOW) {
+      v0 = transposed ? x + (int64_t)arg[k] : x - (int64_t)arg[k] + 1;
+      add = 1;
+    } else if (!transposed && (op == FA_M_SINK || op == FA_M_PREFIX)) {
+      v0 = arg[k];
+      add = 1;
+    }
+    if (nb + add > kRowBreaks) return seg;
+#pragma unroll
+    for (int t = 0; t < kRowBreaks; ++t) {
+      if (add >= 1 && t == nb) bp[t] = v0;
+      if (add == 2 && t == nb + 1) bp[t] = v1;
+    }
+    nb += add;
+  }
+#pragma unroll
+  for (int t = 0; t < kRowBreaks; ++t) bp[t] = bp[t] < 0 ? 0 : (bp[t] > len ? len : bp[t]);
+  // sorting network for 8 values (19 compare-exchanges)
+  cswap(bp[0], bp[2]); cswap(bp[1], bp[3]); cswap(bp[4], bp[6]); cswap(bp[5], bp[7]);
+  cswap(bp[0], bp[4]); cswap(bp[1], bp[5]); cswap(bp[2], bp[6]); cswap(bp[3], bp[7]);
+  cswap(bp[0], bp[1]); cswap(bp[2], bp[3]); cswap(bp[4], bp[5]); cswap(bp[6], bp[7]);
+  cswap(bp[2], bp[4]); cswap(bp[3], bp[5]);
+  cswap(bp[1], bp[4]); cswap(bp[3], bp[6]);
+  cswap(bp[1], bp[2]); cswap(bp[3], bp[4]); cswap(bp[5], bp[6]);
+  int n = 0;
+  int lo0 = 0, hi0 = 0, lo1 = 0, hi1 = 0;
+#pragma unroll
+  for (int t = 0; t + 1 < kRowBreaks; ++t) {
+    const int64_t y0 = bp[t], y1 = bp[t + 1];
+    if (y0 < y1 && mask_bit(nn, ops, arg, transposed, x, y0, run_lo, run_hi)) {
+      if (n == 1 && hi0 == (int)y0) {
+        hi0 = (int)y1;
+      } else if (n == 2 && hi1 == (int)y0) {
+        hi1 = (int)y1;
+      } else if (n == 0) {
+        lo0 = (int)y0;
+        hi0 = (int)y1;
+        n = 1;
+      } else if (n == 1) {
+        lo1 = (int)y0;
+        hi1 = (int)y1;
+        n = 2;
+      } else {
+        return seg;  // a third interval
+      }
+    }
+  }
+  seg.n = n;
+  seg.lo0 = lo0;
+  seg.hi0 = hi0;
+  seg.lo1 = lo1;
+  seg.hi1 = hi1;
+  return seg;
+}
+
+// Visible intervals of every query row over the key columns ([bm][0][x]) and
+// of every key column over the query rows ([bm][1][x]), for x < L =
+// max(q_len, kv_len); lo0 = -1 where two intervals do not describe the row.
+__global__ void __launch_bounds__(256) row_segs_kernel(const __grid_constant__ BuildArgs a) {
+  const int64_t L = max(a.q_len, a.kv_len);
+  const int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (gid >= (int64_t)a.Bm * 2 * L) return;
+  const int64_t x = gid % L;
+  const int which = (int)((gid / L) % 2);
+  const int bm = (int)(gid / (2 * L));
+  int32_t arg[FA_MAX_MASK_NODES];
+  for (int k = 0; k < a.mask.n; ++k) arg[k] = node_arg(a.mask, k, bm);
+  int lo = 0, hi = 0;
+  const bool have_run = a.mask.has_doc && doc_run(a.mask, bm, x, lo, hi);
+  const RowSegs s = row_segments(a.mask.n, pack_ops(a.mask), arg, which == 1, x, have_run, lo, hi,
+                                 which ? a.q_len : a.kv_len);
+  reinterpret_cast<int4*>(a.row_segs)[gid] = (s.n < 0) ? make_int4(-1, -1, 0, 0) : make_int4(s.lo0, s.hi0, s.lo1, s.hi1);
+}
+
 constexpr int kBuildWarps = 8;
 
 // One warp per (query-tile row, chunk of 32 key tiles): each lane classifies
@@ -170,6 +321,7 @@ __global__ void __launch_bounds__(kBuildWarps * 32) classify_kernel(const __grid
   if (lane < a.mask.n) s_arg[warp][lane] = node_arg(a.mask, lane, bm);
   __syncwarp();
   const int32_t* arg = s_arg[warp];
+  const uint64_t ops = pack_ops(a.mask);
   const int tmax = max(a.nq, a.nkv);
   const int32_t* doc = a.mask.has_doc ? a.mask.doc + (int64_t)bm * a.mask.doc_len : nullptr;
   const bool doc_vec = a.mask.doc_vec_ok != 0;
@@ -230,7 +382,7 @@ __global__ void __launch_bounds__(kBuildWarps * 32) classify_kernel(const __grid
           }
           return w;
         };
-        cnt += __popc(mask_word_rolled(a.mask, arg, bm, i, jc, eq) & low_bits(j1 + 1 - jc));
+        cnt += __popc(mask_word_rolled(a.mask.n, ops, arg, i, jc, eq) & low_bits(j1 + 1 - jc));
       }
     }
     const int total = (int)__reduce_add_sync(0xffffffffu, (unsigned)cnt);
@@ -360,6 +512,10 @@ cudaError_t launch_build(const BuildArgs& a, cudaStream_t stream) {
     tile_summary_kernel<<<(unsigned)((warps + 7) / 8), 256, 0, stream>>>(a);
     const int64_t L = a.q_len > a.kv_len ? a.q_len : a.kv_len;
     doc_runs_kernel<<<(unsigned)((a.Bm * L + 255) / 256), 256, 0, stream>>>(a);
+  }
+  {
+    const int64_t L = a.q_len > a.kv_len ? a.q_len : a.kv_len;
+    row_segs_kernel<<<(unsigned)((a.Bm * 2 * L + 255) / 256), 256, 0, stream>>>(a);
   }
   const int64_t rows = (int64_t)a.Bm * a.Hm * a.nq;
   const int64_t cols = (int64_t)a.Bm * a.Hm * a.nkv;

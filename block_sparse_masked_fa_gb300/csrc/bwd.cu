@@ -12,17 +12,25 @@
 //
 // Kernels:
 //  1. bwd_pre   -- Delta_i = dO_i . out_i (fp32) and LSE, laid out per query
-//                  tile for one bulk copy each, and a zeroed fp32 dq accumulator.
+//                  tile (the key-row warps copy a tile's values in per step),
+//                  and a zeroed fp32 dq accumulator.
 //  2. bwd_kernel -- one CTA per (b, h, key tile J), key tiles longest first:
-//       warps 0-3  thread r owns key row r (TMEM lane r): P^T, dS^T
-//       warps 8-11 dq reducers: dQ tile from TMEM, TMA bulk reduce-add into the accumulator
-//       warp 8     TMA producer: K_J, V_J once; Q_I, dO_I (+ LSE_I, Delta_I) per step
-//       warp 9     MMA issuer, five tcgen05 GEMMs per (I, J):
-//                    S^T  = K Q^T           (TMEM [0,128))
-//                    dP^T = V dO^T          (TMEM [128,256))
-//                    dV  += P^T dO          (P^T bf16 read from TMEM [0,64))
-//                    dK  += dS^T Q          (dS in shared memory, K-major)
-//                    dQ   = dS K            (same shared buffer read MN-major; TMEM [128,128+D))
+//       warps 0-7    TMEM lane r = 32 (warp % 4) + lane = key row r, query columns
+//                    [64 (warp / 4), +64): phase A, P^T into TMEM; phase B, dS^T
+//                    into shared memory; LSE_I, Delta_I copied in per step
+//       warps 8-11   dQ rows [32 (warp % 4), +32) out of TMEM, staged 32 x 32 at a
+//                    time and TMA bulk reduce-added into the fp32 accumulator
+//       warp 12      TMA producer: K_J, V_J once; Q_I, dO_I per step
+//       warp 13      MMA issuer, five tcgen05 GEMMs per (I, J):
+//                     once P^T is in:  dV  += P^T dO   (P^T bf16 read from TMEM [0,64))
+//                     once dS is in:   dQ   = dS K     (dS read MN-major; TMEM [128,128+D))
+//                                      S^T  = K Q^T    (next step; TMEM [0,128))
+//                                      dK  += dS^T Q   (dS read K-major)
+//                                      dP^T = V dO^T   (next step; TMEM [128,256), once dQ is read out)
+//     dV runs while the key-row warps compute dS, and the next S^T before dK
+//     so that phase A of the next step can start early.  Registers are split
+//     per warpgroup (setmaxnreg) so that the key-row warps hold a row's 64
+//     probabilities across the two phases.
 //     dK and dV stay in TMEM for the whole key tile and are written once
 //     (no atomics); dQ partial tiles are added into the fp32 accumulator.
 //  3. bwd_dq_convert -- dq = bf16(scale * accumulator).
@@ -45,25 +53,31 @@ template <int D>
 struct BwdCfg {
   static constexpr int NC = D / 64;
   static constexpr uint32_t TILE = 128u * D * 2u;  // one 128 x D bf16 tile
-  static constexpr int NQ = 2;                     // Q ring slots (with LSE / Delta)
+  static constexpr int NQ = 2;                     // Q ring slots
   static constexpr int NDO = (D == 64) ? 2 : 1;    // dO ring slots
   static constexpr uint32_t DS_BYTES = 128u * 128u * 2u;
+  static constexpr uint32_t BOX_BYTES = 32u * 32u * 4u;    // one fp32 dQ box: 32 rows x 32 columns
+  static constexpr uint32_t STG_BYTES = 4u * 2u * BOX_BYTES;  // two boxes per dQ warp
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t T_S = 0, T_DP = 128, T_DV = 256, T_DK = 256 + D;
-  static constexpr int THREADS = 448;  // 8 key-row warps, 4 dq warps, producer, MMA
+  static constexpr int KEY_THREADS = 256;  // warps 0-7: P^T / dS^T, epilogue
+  static constexpr int DQ_WARP0 = 8;       // warps 8-11: dQ out of TMEM into the accumulator
+  static constexpr int DQ_THREADS = 128;
+  static constexpr int PRODUCER_WARP = 12, MMA_WARP = 13;  // (warps 14, 15 idle)
+  static constexpr int THREADS = 512;
 };
 
-struct TileStats {  // one bulk copy per query tile, from the workspace
+struct TileStats {  // per query tile, from the workspace
   float nlse[128];    // -LSE * log2(e) of the tile's query rows
   float ndelta[128];  // -Delta of the tile's query rows
 };
 
 struct BwdCtl {
-  alignas(16) TileStats stats[2];  // per Q slot
+  alignas(16) TileStats stats;  // of the current step, copied in by the key-row warps
   uint64_t kv_full;
   uint64_t q_full[2], q_empty[2];
   uint64_t do_full[2], do_empty[2];
-  uint64_t s_full, p_full, dq_full, dq_free, acc_full, fin;
+  uint64_t s_full, dp_full, pa_full, pb_full, dq_full, dq_free, acc_full, fin;
   uint32_t tmem;
   int abort;
   int32_t arg[FA_MAX_MASK_NODES];
@@ -72,7 +86,7 @@ struct BwdCtl {
 template <int D>
 constexpr size_t bwd_smem_bytes() {
   using C = BwdCfg<D>;
-  return 1024 + (size_t)C::TILE * (2 + C::NQ + C::NDO) + C::DS_BYTES + sizeof(BwdCtl);
+  return 1024 + (size_t)C::TILE * (2 + C::NQ + C::NDO) + C::DS_BYTES + C::STG_BYTES + sizeof(BwdCtl);
 }
 
 __device__ __forceinline__ void fail(const AttnArgs& p, BwdCtl* ctl) {
@@ -92,9 +106,16 @@ __device__ __forceinline__ float tanh_fast(float t) {
   return fmaf(-2.0f, r, 1.0f);
 }
 
-__device__ __forceinline__ void red_add_v4(float* p, float a, float b, float c, float d) {
-  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d) : "memory");
+// Shared-memory descriptor of MMA step kk (16 elements of the contraction) from
+// the descriptor of step 0.  K-major: a 128-row tile stored as 64-column
+// chunks of 16 KB, step kk at chunk kk / 4, byte 32 (kk % 4) of the row.
+// MN-major: step kk starts 2048 bytes (16 rows of 128 bytes) further.  The
+// start-address field counts 16-byte units and never carries for addresses
+// inside the 227 KB of shared memory.
+__device__ __forceinline__ uint64_t kmajor_step(uint64_t desc, int kk) {
+  return desc + (uint64_t)((kk >> 2) * (16384 >> 4) + (kk & 3) * (32 >> 4));
 }
+__device__ __forceinline__ uint64_t mnmajor_step(uint64_t desc, int kk) { return desc + (uint64_t)(kk * (2048 >> 4)); }
 
 // Writes 32 bf16 values (16 packed words) of row r into a 128-byte-swizzled
 // [chunks][128 rows][64] tile at columns [32 c, 32 c + 32).
@@ -109,7 +130,7 @@ __device__ __forceinline__ void store_row32(uint8_t* tile, int r, int c, const u
 }
 
 template <int D, int SCORE>
-__global__ void __launch_bounds__(448, 1)
+__global__ void __launch_bounds__(512, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_dv,
@@ -123,7 +144,8 @@ __global__ void __launch_bounds__(448, 1)
   uint8_t* sQ0 = sV + C::TILE;             // Q ring
   uint8_t* sDO0 = sQ0 + C::NQ * C::TILE;   // dO ring
   uint8_t* sDS = sDO0 + C::NDO * C::TILE;
-  BwdCtl* ctl = reinterpret_cast<BwdCtl*>(sDS + C::DS_BYTES);
+  uint8_t* sSTG = sDS + C::DS_BYTES;       // dQ staging: per dQ warp two 32 x 32 fp32 boxes
+  BwdCtl* ctl = reinterpret_cast<BwdCtl*>(sSTG + C::STG_BYTES);
   auto sQ = [&](int st) { return sQ0 + st * C::TILE; };
   auto sDO = [&](int st) { return sDO0 + st * C::TILE; };
 
@@ -143,9 +165,9 @@ __global__ void __launch_bounds__(448, 1)
   int n = n_full + p.q_num[col];
   const int64_t list = (int64_t)col * p.nq;
 
-  const uint32_t b_kv = smem_u32(&ctl->kv_full), b_s = smem_u32(&ctl->s_full), b_p = smem_u32(&ctl->p_full),
-                 b_dq = smem_u32(&ctl->dq_full), b_dqf = smem_u32(&ctl->dq_free),
-                 b_acc = smem_u32(&ctl->acc_full), b_fin = smem_u32(&ctl->fin);
+  const uint32_t b_kv = smem_u32(&ctl->kv_full), b_s = smem_u32(&ctl->s_full), b_dp = smem_u32(&ctl->dp_full),
+                 b_pa = smem_u32(&ctl->pa_full), b_pb = smem_u32(&ctl->pb_full), b_dq = smem_u32(&ctl->dq_full),
+                 b_dqf = smem_u32(&ctl->dq_free), b_acc = smem_u32(&ctl->acc_full), b_fin = smem_u32(&ctl->fin);
   if (threadIdx.x == 0) {
     mbar_init(b_kv, 1);
     for (int s2 = 0; s2 < 2; ++s2) {
@@ -155,16 +177,18 @@ __global__ void __launch_bounds__(448, 1)
       mbar_init(smem_u32(&ctl->do_empty[s2]), 1);
     }
     mbar_init(b_s, 1);
-    mbar_init(b_p, 256);
+    mbar_init(b_dp, 1);
+    mbar_init(b_pa, C::KEY_THREADS);
+    mbar_init(b_pb, C::KEY_THREADS);
     mbar_init(b_dq, 1);
-    mbar_init(b_dqf, 128);
+    mbar_init(b_dqf, C::DQ_THREADS);
     mbar_init(b_acc, 1);
     mbar_init(b_fin, 1);
     ctl->abort = (*reinterpret_cast<volatile uint32_t*>(p.status) & kStatusTimeout) ? 1 : 0;
     fence_mbar_init();
   }
   if (threadIdx.x < p.mask.n) ctl->arg[threadIdx.x] = node_arg(p.mask, threadIdx.x, bm);
-  if (warp == 12) {
+  if (warp == C::PRODUCER_WARP) {
     tmem_alloc(smem_u32(&ctl->tmem), C::TMEM_COLS);
     tmem_relinquish();
   }
@@ -177,197 +201,246 @@ __global__ void __launch_bounds__(448, 1)
 
   auto tile_of = [&](int it) -> int { return it < n_full ? p.full_q_idx[list + it] : p.q_idx[list + it - n_full]; };
 
-  if (warp == 12) {
-    // ------------------------------------------------------------ producer
-    if (n > 0) {
-      if (lane == 0) {
-        prefetch_tmap(&tm_q);
-        prefetch_tmap(&tm_k);
-        prefetch_tmap(&tm_v);
-        prefetch_tmap(&tm_do);
-        mbar_arrive_expect_tx(b_kv, 2 * C::TILE);
-        for (int c = 0; c < C::NC; ++c) {
-          tma_load_3d(smem_u32(sK + c * 16384), &tm_k, b_kv, c * 64, J * 128, bh);
-          tma_load_3d(smem_u32(sV + c * 16384), &tm_v, b_kv, c * 64, J * 128, bh);
-        }
-      }
-      int q_issued = 0, do_issued = 0;
-      bool ok = true;
-      for (int it = 0; it < n; ++it) {
-        const int I = tile_of(it);
-        // Q slot, with the tile's -LSE (log2 units) and -Delta
-        const int qs = it % C::NQ, quse = it / C::NQ;
-        if (quse > 0 && !warp_wait(smem_u32(&ctl->q_empty[qs]), (quse - 1) & 1, &ctl->abort)) {
-          ok = false;
-          break;
-        }
-        if (lane == 0) {
-          const uint32_t qbar = smem_u32(&ctl->q_full[qs]);
-          mbar_arrive_expect_tx(qbar, C::TILE + (uint32_t)sizeof(TileStats));
-          for (int c = 0; c < C::NC; ++c)
-            tma_load_3d(smem_u32(sQ(qs) + c * 16384), &tm_q, qbar, c * 64, I * 128, bh);
-          bulk_load(smem_u32(&ctl->stats[qs]), stats_g + ((int64_t)bh * p.nq + I) * 256,
-                    (uint32_t)sizeof(TileStats), qbar);
-        }
-        q_issued = it + 1;
-        // dO slot
-        const int ds = it % C::NDO, duse = it / C::NDO;
-        if (duse > 0 && !warp_wait(smem_u32(&ctl->do_empty[ds]), (duse - 1) & 1, &ctl->abort)) {
-          ok = false;
-          break;
-        }
-        if (lane == 0) {
-          const uint32_t dbar = smem_u32(&ctl->do_full[ds]);
-          mbar_arrive_expect_tx(dbar, C::TILE);
-          for (int c = 0; c < C::NC; ++c)
-            tma_load_3d(smem_u32(sDO(ds) + c * 16384), &tm_do, dbar, c * 64, I * 128, bh);
-        }
-        do_issued = it + 1;
-      }
-      if (!ok && lane == 0) fail(p, ctl);
-      // drain: every copy this CTA started lands before it exits
-      if (lane == 0) {
-        mbar_wait(b_kv, 0, nullptr);
-        for (int it = max(0, q_issued - C::NQ); it < q_issued; ++it)
-          mbar_wait(smem_u32(&ctl->q_full[it % C::NQ]), (it / C::NQ) & 1, nullptr);
-        for (int it = max(0, do_issued - C::NDO); it < do_issued; ++it)
-          mbar_wait(smem_u32(&ctl->do_full[it % C::NDO]), (it / C::NDO) & 1, nullptr);
-      }
-    }
-  } else if (warp == 13) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0 && n > 0) {
-      constexpr uint32_t kIdKK = idesc_bf16(128, 128, false, false);  // S^T, dP^T
-      constexpr uint32_t kIdKM = idesc_bf16(128, D, false, true);     // dV (A in TMEM), dK
-      constexpr uint32_t kIdMM = idesc_bf16(128, D, true, true);      // dQ
-      const uint32_t k_base = smem_u32(sK), v_base = smem_u32(sV), ds_base = smem_u32(sDS);
-      bool ok = mbar_wait(b_kv, 0, &ctl->abort);
-      for (int it = 0; ok && it < n; ++it) {
-        const int qs = it % C::NQ, ds = it % C::NDO;
-        if (!mbar_wait(smem_u32(&ctl->q_full[qs]), (it / C::NQ) & 1, &ctl->abort)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t q_base = smem_u32(sQ(qs)), do_base = smem_u32(sDO(ds));
-        // S^T = K Q^T: its columns held P^T of the last step, read by the dV MMA issued before
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;
-          mma_ss(tmem + C::T_S, sdesc_sw128(k_base + off, 16, 1024), sdesc_sw128(q_base + off, 16, 1024), kIdKK,
-                 kk > 0);
-        }
-        if (!mbar_wait(smem_u32(&ctl->do_full[ds]), (it / C::NDO) & 1, &ctl->abort)) {
-          ok = false;
-          break;
-        }
-        if (it > 0 && !mbar_wait(b_dqf, (it - 1) & 1, &ctl->abort)) {  // dQ of the last step read out
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;
-          mma_ss(tmem + C::T_DP, sdesc_sw128(v_base + off, 16, 1024), sdesc_sw128(do_base + off, 16, 1024), kIdKK,
-                 kk > 0);
-        }
-        mma_commit(b_s);
-        if (!mbar_wait(b_p, it & 1, &ctl->abort)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        // dV += P^T dO; P^T of query columns [64 h, 64 h + 64) sits at TMEM columns [64 h, 64 h + 32)
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          mma_ts(tmem + C::T_DV, tmem + C::T_S + (kk / 4) * 64 + (kk % 4) * 8,
-                 sdesc_sw128(do_base + kk * 2048, 16384, 1024), kIdKM, (it > 0 || kk > 0));
-        mma_commit(smem_u32(&ctl->do_empty[ds]));
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)  // dK += dS^T Q
-          mma_ss(tmem + C::T_DK, sdesc_sw128(ds_base + (kk / 4) * 16384 + (kk % 4) * 32, 16, 1024),
-                 sdesc_sw128(q_base + kk * 2048, 16384, 1024), kIdKM, (it > 0 || kk > 0));
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)  // dQ = dS K
-          mma_ss(tmem + C::T_DP, sdesc_sw128(ds_base + kk * 2048, 16384, 1024),
-                 sdesc_sw128(k_base + kk * 2048, 16384, 1024), kIdMM, kk > 0);
-        mma_commit(b_dq);  // the dq reducers release the Q slot (they stage dQ in it)
-      }
-      if (ok)
-        mma_commit(b_acc);
-      else
-        fail(p, ctl);
-      mma_commit(b_fin);
-      mbar_wait(b_fin, 0, nullptr);
-    }
-  } else if (warp >= 8) {
-    // ------------------------------------------------------------ dq reducers
-    // dQ tile: TMEM -> registers -> 128-byte-swizzled fp32 boxes (32 columns x
-    // 128 rows) staged in this step's Q slot (free: dK, the last reader of Q,
-    // is done) -> TMA bulk reduce-add into the fp32 accumulator.  Half of the
-    // tile fits the slot at a time.
-    const int r = (warp % 4) * 32 + lane;  // TMEM lane = query row within the tile
-    const uint32_t tq = tmem + ((uint32_t)((warp % 4) * 32) << 16) + C::T_DP;
-    constexpr int kHalfCols = D / 2;  // dQ columns per staging round
-    bool ok = true;
-    for (int it = 0; ok && it < n; ++it) {
-      const int I = tile_of(it);
-      const int qs = it % C::NQ;
-      ok = named_bar_and(2, 128, warp_wait(b_dq, it & 1, &ctl->abort));
-      if (!ok) break;
+  // teardown, at the end of every role: all threads past their last TMEM
+  // access, then the allocating warp frees the columns
+  auto teardown = [&]() {
+    tc_fence_before();
+    named_bar_sync(15, C::THREADS);
+    if (warp == C::PRODUCER_WARP) {
+      __syncwarp();
       tc_fence_after();
-      uint8_t* stage = sQ(qs);
-#pragma unroll 1
-      for (int h2 = 0; h2 < 2; ++h2) {
-        float v[kHalfCols];
-        if constexpr (kHalfCols == 64) {
-          tmem_ld64f(tq + kHalfCols * h2, v);
-        } else {
-          tmem_ld32f(tq + kHalfCols * h2, v);
+      tmem_dealloc(tmem, C::TMEM_COLS);
+    }
+  };
+
+  // Register budgets per warpgroup, set at the top of each warpgroup's branch
+  // (launched with 128 per thread): key-row warps 176, dQ warps 104, producer /
+  // MMA warpgroup 56 -- 256 x 176 + 128 x 104 + 128 x 56 = 512 x 128.
+  if (warp >= C::PRODUCER_WARP) {
+    setmaxnreg_dec<56>();
+    if (warp == C::PRODUCER_WARP) {
+      // ------------------------------------------------------------ producer
+      if (n > 0) {
+        if (lane == 0) {
+          prefetch_tmap(&tm_q);
+          prefetch_tmap(&tm_k);
+          prefetch_tmap(&tm_v);
+          prefetch_tmap(&tm_do);
+          mbar_arrive_expect_tx(b_kv, 2 * C::TILE);
+          for (int c = 0; c < C::NC; ++c) {
+            tma_load_3d(smem_u32(sK + c * 16384), &tm_k, b_kv, c * 64, J * 128, bh);
+            tma_load_3d(smem_u32(sV + c * 16384), &tm_v, b_kv, c * 64, J * 128, bh);
+          }
         }
-        if (h2 == 1) {
+        int q_issued = 0, do_issued = 0;
+        bool ok = true;
+        for (int it = 0; it < n; ++it) {
+          const int I = tile_of(it);
+          // Q slot (freed by the MMA warp once dK, its last reader, is done)
+          const int qs = it % C::NQ, quse = it / C::NQ;
+          if (quse > 0 && !warp_wait(smem_u32(&ctl->q_empty[qs]), (quse - 1) & 1, &ctl->abort)) {
+            ok = false;
+            break;
+          }
+          if (lane == 0) {
+            const uint32_t qbar = smem_u32(&ctl->q_full[qs]);
+            mbar_arrive_expect_tx(qbar, C::TILE);
+            for (int c = 0; c < C::NC; ++c)
+              tma_load_3d(smem_u32(sQ(qs) + c * 16384), &tm_q, qbar, c * 64, I * 128, bh);
+          }
+          q_issued = it + 1;
+          // dO slot (freed once dV, its last reader, is done)
+          const int ds = it % C::NDO, duse = it / C::NDO;
+          if (duse > 0 && !warp_wait(smem_u32(&ctl->do_empty[ds]), (duse - 1) & 1, &ctl->abort)) {
+            ok = false;
+            break;
+          }
+          if (lane == 0) {
+            const uint32_t dbar = smem_u32(&ctl->do_full[ds]);
+            mbar_arrive_expect_tx(dbar, C::TILE);
+            for (int c = 0; c < C::NC; ++c)
+              tma_load_3d(smem_u32(sDO(ds) + c * 16384), &tm_do, dbar, c * 64, I * 128, bh);
+          }
+          do_issued = it + 1;
+        }
+        if (!ok && lane == 0) fail(p, ctl);
+        // drain: every copy this CTA started lands before it exits
+        if (lane == 0) {
+          mbar_wait(b_kv, 0, nullptr);
+          for (int it = max(0, q_issued - C::NQ); it < q_issued; ++it)
+            mbar_wait(smem_u32(&ctl->q_full[it % C::NQ]), (it / C::NQ) & 1, nullptr);
+          for (int it = max(0, do_issued - C::NDO); it < do_issued; ++it)
+            mbar_wait(smem_u32(&ctl->do_full[it % C::NDO]), (it / C::NDO) & 1, nullptr);
+        }
+      }
+    } else if (warp == C::MMA_WARP) {
+      // ------------------------------------------------------------ MMA issuer
+      if (lane == 0 && n > 0) {
+        constexpr uint32_t kIdKK = idesc_bf16(128, 128, false, false);  // S^T, dP^T
+        constexpr uint32_t kIdKM = idesc_bf16(128, D, false, true);     // dV (A in TMEM), dK
+        constexpr uint32_t kIdMM = idesc_bf16(128, D, true, true);      // dQ
+        const uint32_t k_base = smem_u32(sK), v_base = smem_u32(sV), ds_base = smem_u32(sDS);
+        // S^T = K Q^T of step it, into columns the dV MMA of the step before has read
+        auto issue_s = [&](int it) -> bool {
+          const int qs = it % C::NQ;
+          if (!mbar_wait(smem_u32(&ctl->q_full[qs]), (it / C::NQ) & 1, &ctl->abort)) return false;
+          tc_fence_after();
+          const uint64_t a0 = sdesc_sw128(k_base, 16, 1024), b0 = sdesc_sw128(smem_u32(sQ(qs)), 16, 1024);
+#pragma unroll 1
+          for (int kk = 0; kk < D / 16; ++kk)
+            mma_ss(tmem + C::T_S, kmajor_step(a0, kk), kmajor_step(b0, kk), kIdKK, kk > 0);
+          mma_commit(b_s);
+          return true;
+        };
+        // dP^T = V dO^T of step it, into the columns dQ of the step before was
+        // computed in: it waits until the dQ warps have read that dQ out
+        auto issue_dp = [&](int it) -> bool {
+          const int ds = it % C::NDO;
+          if (!mbar_wait(smem_u32(&ctl->do_full[ds]), (it / C::NDO) & 1, &ctl->abort)) return false;
+          if (it > 0 && !mbar_wait(b_dqf, (it - 1) & 1, &ctl->abort)) return false;
+          tc_fence_after();
+          const uint64_t a0 = sdesc_sw128(v_base, 16, 1024), b0 = sdesc_sw128(smem_u32(sDO(ds)), 16, 1024);
+#pragma unroll 1
+          for (int kk = 0; kk < D / 16; ++kk)
+            mma_ss(tmem + C::T_DP, kmajor_step(a0, kk), kmajor_step(b0, kk), kIdKK, kk > 0);
+          mma_commit(b_dp);
+          return true;
+        };
+        bool ok = mbar_wait(b_kv, 0, &ctl->abort);
+        if (ok) {
+          tc_fence_after();
+          ok = issue_s(0) && issue_dp(0);
+        }
+        for (int it = 0; ok && it < n; ++it) {
+          const int qs = it % C::NQ, ds = it % C::NDO;
+          const uint32_t q_base = smem_u32(sQ(qs)), do_base = smem_u32(sDO(ds));
+          if (!mbar_wait(b_pa, it & 1, &ctl->abort)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          // dV += P^T dO; P^T of query columns [64 h, 64 h + 64) sits at TMEM columns [64 h, 64 h + 32).
+          // It runs while the key-row warps compute dS.
+          {
+            const uint64_t b0 = sdesc_sw128(do_base, 16384, 1024);
+#pragma unroll 1
+            for (int kk = 0; kk < 8; ++kk)
+              mma_ts(tmem + C::T_DV, tmem + C::T_S + (kk / 4) * 64 + (kk % 4) * 8, mnmajor_step(b0, kk), kIdKM,
+                     (it > 0 || kk > 0));
+          }
+          mma_commit(smem_u32(&ctl->do_empty[ds]));
+          if (!mbar_wait(b_pb, it & 1, &ctl->abort)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          {  // dQ = dS K, over the dP^T columns the key-row warps have read
+            const uint64_t a0 = sdesc_sw128(ds_base, 16384, 1024), b0 = sdesc_sw128(k_base, 16384, 1024);
+#pragma unroll 1
+            for (int kk = 0; kk < 8; ++kk) mma_ss(tmem + C::T_DP, mnmajor_step(a0, kk), mnmajor_step(b0, kk), kIdMM, kk > 0);
+          }
+          mma_commit(b_dq);
+          if (it + 1 < n && !issue_s(it + 1)) {
+            ok = false;
+            break;
+          }
+          {  // dK += dS^T Q
+            const uint64_t a0 = sdesc_sw128(ds_base, 16, 1024), b0 = sdesc_sw128(q_base, 16384, 1024);
+#pragma unroll 1
+            for (int kk = 0; kk < 8; ++kk)
+              mma_ss(tmem + C::T_DK, kmajor_step(a0, kk), mnmajor_step(b0, kk), kIdKM, (it > 0 || kk > 0));
+          }
+          mma_commit(smem_u32(&ctl->q_empty[qs]));  // Q read for the last time
+          if (it + 1 < n && !issue_dp(it + 1)) {
+            ok = false;
+            break;
+          }
+        }
+        if (ok)
+          mma_commit(b_acc);
+        else
+          fail(p, ctl);
+        mma_commit(b_fin);
+        mbar_wait(b_fin, 0, nullptr);
+      }
+    }
+    __syncwarp();
+    teardown();
+  } else if (warp >= C::DQ_WARP0) {
+    setmaxnreg_dec<104>();
+    // ------------------------------------------------------------ dQ warps
+    // Warp w drains dQ rows [32 (w % 4), +32) (its TMEM lanes) of each step:
+    // 32 columns at a time into one of its two 128-byte-swizzled 32 x 32 fp32
+    // boxes, which lane 0 TMA bulk reduce-adds into the fp32 accumulator.  A
+    // box is rewritten only once the reduce issued from it two rounds before
+    // has read it.
+    const int rw = (warp % 4) * 32;  // first dQ row of this warp
+    const uint32_t tq = tmem + ((uint32_t)rw << 16) + C::T_DP;
+    uint8_t* box0 = sSTG + (warp % 4) * (2 * C::BOX_BYTES);
+    int round = 0;
+    bool ok = true;
+    for (int it = 0; it < n; ++it) {
+      const int I = tile_of(it);
+      if (!warp_wait(b_dq, it & 1, &ctl->abort)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+#pragma unroll 1
+      for (int h2 = 0; h2 < D / 64; ++h2) {
+        float v[64];
+        tmem_ld64f(tq + 64 * h2, v);
+        if (h2 == D / 64 - 1) {
           tc_fence_before();
           mbar_arrive(b_dqf);  // TMEM columns free for the next dP^T
-          if (r == 0) bulk_wait_read0();  // the first half's reduce has read the staging
-          named_bar_sync(2, 128);
         }
 #pragma unroll
-        for (int bx = 0; bx < kHalfCols / 32; ++bx) {
-          uint8_t* rowp = stage + bx * 16384 + r * 128;
+        for (int bx = 0; bx < 2; ++bx, ++round) {
+          uint8_t* box = box0 + (round & 1) * C::BOX_BYTES;
+          if (lane == 0) bulk_wait_read1();  // the reduce from this box two rounds ago has read it
+          __syncwarp();
+          uint8_t* rowp = box + lane * 128;
 #pragma unroll
           for (int q4 = 0; q4 < 8; ++q4)
-            *reinterpret_cast<float4*>(rowp + ((q4 ^ (r & 7)) << 4)) =
+            *reinterpret_cast<float4*>(rowp + ((q4 ^ (lane & 7)) << 4)) =
                 make_float4(v[32 * bx + 4 * q4], v[32 * bx + 4 * q4 + 1], v[32 * bx + 4 * q4 + 2],
                             v[32 * bx + 4 * q4 + 3]);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_reduce_add_3d(&tm_dq, smem_u32(box), 64 * h2 + 32 * bx, I * 128 + rw, bh);
+            bulk_commit();
+          }
         }
-        fence_proxy_async_smem();
-        named_bar_sync(2, 128);
-        if (r == 0) {
-          for (int bx = 0; bx < kHalfCols / 32; ++bx)
-            tma_reduce_add_3d(&tm_dq, smem_u32(stage + bx * 16384), kHalfCols * h2 + 32 * bx, I * 128, bh);
-          bulk_commit();
-        }
-      }
-      if (r == 0) {
-        bulk_wait_read0();
-        mbar_arrive(smem_u32(&ctl->q_empty[qs]));  // the Q slot may be reloaded
       }
     }
     if (!ok) fail(p, ctl);
-    if (r == 0) bulk_wait0();  // every reduce of this CTA has completed
+    if (lane == 0) bulk_wait0();  // every reduce of this warp has completed
+    __syncwarp();
+    teardown();
   } else {
-    // ------------------------------------------------------------ P^T / dS^T, then the epilogue
-    // warps 0-7: key row r = 32 (warp % 4) + lane; query columns [64 half, 64 half + 64)
+    setmaxnreg_inc<176>();
+    // ------------------------------------------------------------ key-row warps
+    // Thread (warp w, lane) owns TMEM lane r = 32 (w % 4) + lane = key row r, of
+    // which it handles query columns [64 half, 64 half + 64) (half = w / 4).
     const int r = (warp % 4) * 32 + lane;
     const int half = warp / 4;
     const int j = J * 128 + r;  // key row
     const uint32_t lane_off = (uint32_t)((warp % 4) * 32) << 16;
     const uint32_t tS = tmem + lane_off + C::T_S, tP = tmem + lane_off + C::T_DP;
+    // this key's visible query rows as two intervals, when they are; the
+    // document id and run of the key only where they are not, for the per-word
+    // evaluation of the program
+    const int4 seg = __ldg(p.row_segs + ((int64_t)bm * 2 + 1) * p.seg_len + min(j, p.kv_len - 1));
     const int32_t* doc_row = p.mask.has_doc ? p.mask.doc + (int64_t)bm * p.mask.doc_len : nullptr;
-    const int32_t doc_j = doc_row ? __ldg(doc_row + min(j, p.kv_len - 1)) : 0;
+    int32_t doc_j = 0;
     int run_lo = 0, run_hi = 0;  // with sorted ids: doc[i] == doc[j] exactly for i in [run_lo, run_hi)
-    const bool use_run = doc_row != nullptr && doc_run(p.mask, bm, min(j, p.kv_len - 1), run_lo, run_hi);
+    bool use_run = false;
+    if (seg.x < 0 && doc_row != nullptr) {
+      doc_j = __ldg(doc_row + min(j, p.kv_len - 1));
+      use_run = doc_run(p.mask, bm, min(j, p.kv_len - 1), run_lo, run_hi);
+    }
+    const uint64_t mask_ops = pack_ops(p.mask);
     const float sc_l2 = p.scale * kLog2e;
     float cap_l2 = 0.f, sc_over_cap = 0.f, slope_l2 = 0.f;
     if constexpr (SCORE == FA_S_SOFTCAP) {
@@ -377,24 +450,36 @@ __global__ void __launch_bounds__(448, 1)
     }
     if constexpr (SCORE == FA_S_ALIBI) slope_l2 = __ldg(p.score_param + h) * kLog2e;
     const bool row_ok = j < p.kv_len;
-    bool ok = true;
+    // -LSE (log2 units) and -Delta of the query columns this half handles: one
+    // value per thread of the half, copied into shared memory once per step
+    const int st_idx = (r < 64) ? (64 * half + r) : (128 + 64 * half + r - 64);
+    auto stat_of = [&](int I) { return __ldg(stats_g + ((int64_t)bh * p.nq + I) * 256 + st_idx); };
+    int I_next = n > 0 ? tile_of(0) : 0;
+    if (n > 0) reinterpret_cast<float*>(&ctl->stats)[st_idx] = stat_of(I_next);
+    bool ok = true, lok = true;
     for (int it = 0; it < n; ++it) {
-      const int I = tile_of(it);
-      const bool partial = it >= n_full;
-      const int qs = it % C::NQ;
-      if (!warp_wait(b_s, it & 1, &ctl->abort)) {
-        ok = false;
-        break;
+      // collective per half: this step's stats are in place, and every wait of
+      // the last step succeeded for all of the half (a failed wait is acted on
+      // here; until then the thread goes on with whatever TMEM holds, writing
+      // only TMEM and shared memory)
+      ok = named_bar_and(2 + half, 128, lok);
+      if (!ok) break;
+      const int I = I_next;
+      float st_next = 0.f;
+      if (it + 1 < n) {
+        I_next = tile_of(it + 1);
+        st_next = stat_of(I_next);
       }
-      tc_fence_after();
-      const float* nlse_s = ctl->stats[qs].nlse;
-      const float* ndel_s = ctl->stats[qs].ndelta;
+      const bool partial = it >= n_full;
+      // visibility words of this thread's two 32-column chunks, built before S^T is waited for
+      uint32_t wm0 = row_ok ? 0xffffffffu : 0u, wm1 = wm0;
+      if (partial && row_ok && seg.x >= 0) {
+        wm0 = seg_word(seg, I * 128 + 64 * half);
+        wm1 = seg_word(seg, I * 128 + 64 * half + 32);
+      } else if (partial && row_ok) {
 #pragma unroll 1
-      for (int c2 = 0; c2 < 2; ++c2) {
-        const int c = 2 * half + c2;  // 32-column chunk of the 128 query columns
-        const int i0 = I * 128 + 32 * c;
-        uint32_t w = row_ok ? 0xffffffffu : 0u;
-        if (partial && row_ok) {
+        for (int c2 = 0; c2 < 2; ++c2) {
+          const int i0 = I * 128 + 32 * (2 * half + c2);
           auto eq = [&]() {
             if (use_run) return range_bits(run_lo, run_hi, i0);
             uint32_t bits = 0;
@@ -412,16 +497,32 @@ __global__ void __launch_bounds__(448, 1)
             }
             return bits;
           };
-          w = mask_word_t_rolled(p.mask, ctl->arg, bm, j, i0, eq);
+          const uint32_t w = mask_word_t_rolled(p.mask.n, mask_ops, ctl->arg, j, i0, eq);
+          wm0 = (c2 == 0) ? w : wm0;
+          wm1 = (c2 == 1) ? w : wm1;
         }
-        float sv[32], dp[32];
-        tmem_ld32x2f(tS + 32 * c, sv, tP + 32 * c, dp);
-        uint32_t pk[16], dk[16];
-        const float2* nl2 = reinterpret_cast<const float2*>(nlse_s + 32 * c);
-        const float2* nd2 = reinterpret_cast<const float2*>(ndel_s + 32 * c);
+      }
+      const float* nlse_s = ctl->stats.nlse;
+      const float* ndel_s = ctl->stats.ndelta;
+      // -- phase A: P = exp2(s - LSE) over this thread's 64 query columns; P^T
+      //    (bf16) over the S^T columns already read, for the dV MMA.  pg keeps
+      //    P times the score mod's derivative (P itself unless soft-capped).
+      lok = warp_wait(b_s, it & 1, &ctl->abort);
+      tc_fence_after();
+      float pg[64];
+#pragma unroll
+      for (int c2 = 0; c2 < 2; ++c2) {
+        const int c = 2 * half + c2;  // 32-column chunk of the 128 query columns
+        const int i0 = I * 128 + 32 * c;
+        const uint32_t w = (c2 == 0) ? wm0 : wm1;
+        float sv[32];
+        tmem_ld32f(tS + 32 * c, sv);
+        uint32_t pk[16];
+        const float4* nl4 = reinterpret_cast<const float4*>(nlse_s + 32 * c);
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
-          const float2 nl = nl2[e / 2], nd = nd2[e / 2];
+          const float4 nlq = nl4[e / 4];
+          const float2 nl = (e % 4 == 0) ? make_float2(nlq.x, nlq.y) : make_float2(nlq.z, nlq.w);
           float2 a, g = make_float2(1.0f, 1.0f);
           if constexpr (SCORE == FA_S_SOFTCAP) {
             const float t0 = tanh_fast(sv[e] * sc_over_cap), t1 = tanh_fast(sv[e + 1] * sc_over_cap);
@@ -437,20 +538,45 @@ __global__ void __launch_bounds__(448, 1)
           float2 pv;
           pv.x = ((w >> e) & 1u) ? ex2_approx(a.x) : 0.f;
           pv.y = ((w >> (e + 1)) & 1u) ? ex2_approx(a.y) : 0.f;
-          float2 dsv = mul2(pv, add2(make_float2(dp[e], dp[e + 1]), nd));
-          if constexpr (SCORE == FA_S_SOFTCAP) dsv = mul2(dsv, g);
           pk[e / 2] = pack_bf16x2(pv.x, pv.y);
-          dk[e / 2] = pack_bf16x2(dsv.x, dsv.y);
+          if constexpr (SCORE == FA_S_SOFTCAP) pv = mul2(pv, g);
+          pg[32 * c2 + e] = pv.x;
+          pg[32 * c2 + e + 1] = pv.y;
         }
-        // P^T over this half's own S^T columns, already read: [64 half + 16 c2, +16)
         tmem_st16(tS + 64 * half + 16 * c2, pk);
-        store_row32(sDS, r, c, dk);
       }
       tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(b_pa);
+      // -- phase B: dS = P (dP - Delta) [* d softcap], K-major into the dS buffer
+      //    (free: dP^T of this step was issued after dK of the step before)
+      lok = warp_wait(b_dp, it & 1, &ctl->abort) && lok;
+      tc_fence_after();
+#pragma unroll
+      for (int c2 = 0; c2 < 2; ++c2) {
+        const int c = 2 * half + c2;
+        float dp[32];
+        tmem_ld32f(tP + 32 * c, dp);
+        uint32_t dk[16];
+        const float4* nd4 = reinterpret_cast<const float4*>(ndel_s + 32 * c);
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          const float4 ndq = nd4[e / 4];
+          const float2 nd = (e % 4 == 0) ? make_float2(ndq.x, ndq.y) : make_float2(ndq.z, ndq.w);
+          const float2 dsv = mul2(make_float2(pg[32 * c2 + e], pg[32 * c2 + e + 1]),
+                                  add2(make_float2(dp[e], dp[e + 1]), nd));
+          dk[e / 2] = pack_bf16x2(dsv.x, dsv.y);
+        }
+        store_row32(sDS, r, c, dk);
+      }
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(b_p);
+      mbar_arrive(b_pb);
+      // every thread of this half is done with this step's stats: publish the next step's
+      named_bar_sync(2 + half, 128);
+      if (it + 1 < n) reinterpret_cast<float*>(&ctl->stats)[st_idx] = st_next;
     }
+    if (ok && !lok) ok = false;
     if (!ok) fail(p, ctl);
     // ---- epilogue: dV and scale * dK from TMEM, once per key tile; each half writes D/2 columns
     if (ok && n > 0) {
@@ -460,9 +586,8 @@ __global__ void __launch_bounds__(448, 1)
       }
       tc_fence_after();
     }
-    // staging for dV / dK: the dS buffer and the first dO slot, whose last readers
-    // (the dK / dQ and dV MMAs) are done once acc_full completes; the Q slots may
-    // still hold the dq reducers' last staged tile
+    // staging for dV / dK: the dS buffer and the first dO slot, whose last
+    // readers (the dQ / dK and dV MMAs) are done once acc_full completes
     uint8_t* stage_v = sDS;
     uint8_t* stage_k = sDO(0);
     if (ok && !skip) {
@@ -488,7 +613,7 @@ __global__ void __launch_bounds__(448, 1)
       }
       fence_proxy_async_smem();
     }
-    named_bar_sync(1, 256);
+    named_bar_sync(1, C::KEY_THREADS);
     if (threadIdx.x == 0 && !skip && !*reinterpret_cast<volatile int*>(&ctl->abort)) {
       for (int c = 0; c < C::NC; ++c) {
         tma_store_3d(&tm_dv, smem_u32(stage_v + c * 16384), c * 64, J * 128, bh);
@@ -497,14 +622,7 @@ __global__ void __launch_bounds__(448, 1)
       bulk_commit();
       bulk_wait_read0();
     }
-  }
-
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 12) {
-    __syncwarp();
-    tc_fence_after();
-    tmem_dealloc(tmem, C::TMEM_COLS);
+    teardown();
   }
 }
 
@@ -579,7 +697,7 @@ cudaError_t launch_bwd_t(const AttnArgs& a, const BwdTensors& t, cudaStream_t st
   CUtensorMap mdq;
   const bool ok = enc(&mq, t.q, a.q_len) && enc(&mk, t.k, a.kv_len) && enc(&mv, t.v, a.kv_len) &&
                   enc(&mdo, t.dout, a.q_len) && enc(&mdk, t.dk, a.kv_len) && enc(&mdv, t.dv, a.kv_len) &&
-                  encode_tmap_3d(&mdq, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, t.dq_acc, D, a.q_len, bh, 32, 128,
+                  encode_tmap_3d(&mdq, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, t.dq_acc, D, a.q_len, bh, 32, 32,
                                  CU_TENSOR_MAP_SWIZZLE_128B);
   if (!ok) {
     *enc_failed = true;

@@ -98,29 +98,42 @@ __device__ __forceinline__ uint32_t mask_word(const DevMask& m, const int32_t* a
   return s0;
 }
 
+// Node kinds of a mask program packed four bits each (node k in bits
+// [4k, 4k + 4)).  Built once per thread from the kernel argument with constant
+// indices, so that the rolled evaluators below read registers only: indexing
+// the argument's op[] with a loop counter goes through a generic pointer into
+// parameter space, which costs hundreds of cycles per node.
+__device__ __forceinline__ uint64_t pack_ops(const DevMask& m) {
+  static_assert(FA_MAX_MASK_NODES * 4 <= 64, "node kinds must fit one 64-bit word");
+  uint64_t ops = 0;
+#pragma unroll
+  for (int k = 0; k < FA_MAX_MASK_NODES; ++k)
+    if (k < m.n) ops |= (uint64_t)(m.op[k] & 15) << (4 * k);
+  return ops;
+}
+
 // Same as mask_word, with the node loop kept rolled: small code for the
-// attention kernels' partial tiles, where it runs 4 times per tile.
-// arg: resolved W / n_sink (node_arg); a PREFIX node reads prefix_len[bm] itself.
+// attention kernels' partial tiles.
+//  n, ops    node count and packed node kinds (pack_ops)
+//  arg[k]    resolved scalar parameter of node k for this batch row (node_arg)
 template <class EqDoc>
-__device__ __forceinline__ uint32_t mask_word_rolled(const DevMask& m, const int32_t* arg, int bm, int64_t i,
+__device__ __forceinline__ uint32_t mask_word_rolled(int n, uint64_t ops, const int32_t* arg, int64_t i,
                                                      int64_t j0, EqDoc eq_doc) {
   uint32_t s0 = 0, s1 = 0, s2 = 0, s3 = 0, s4 = 0, s5 = 0, s6 = 0, s7 = 0;
 #pragma unroll 1
-  for (int k = 0; k < m.n; ++k) {
-    const int op = m.op[k];
+  for (int k = 0; k < n; ++k, ops >>= 4) {
+    const int op = (int)(ops & 15u);
     if (op == FA_M_AND || op == FA_M_OR) {
       s0 = (op == FA_M_AND) ? (s1 & s0) : (s1 | s0);
       s1 = s2; s2 = s3; s3 = s4; s4 = s5; s5 = s6; s6 = s7; s7 = 0;
     } else {
       uint32_t w;
       if (op == FA_M_CAUSAL) {
-        w = low_bits(i - j0 + 1);
+        w = low_bits(i - j0 + 1);                          // j <= i
       } else if (op == FA_M_WINDOW) {
-        w = ~low_bits(i - (int64_t)arg[k] + 1 - j0);
-      } else if (op == FA_M_SINK) {
-        w = low_bits((int64_t)arg[k] - j0);
-      } else if (op == FA_M_PREFIX) {
-        w = low_bits((int64_t)__ldg(m.param[k] + bm) - j0);
+        w = ~low_bits(i - (int64_t)arg[k] + 1 - j0);       // j >= i - W + 1
+      } else if (op == FA_M_SINK || op == FA_M_PREFIX) {
+        w = low_bits((int64_t)arg[k] - j0);                // j < n
       } else if (op == FA_M_SAME_DOC) {
         w = eq_doc();
       } else {
@@ -136,12 +149,12 @@ __device__ __forceinline__ uint32_t mask_word_rolled(const DevMask& m, const int
 // (bit c is pair (i0 + c, j)); used where a thread owns a key row.
 //  eq_doc()  word of (doc[i0 + c] == doc[j]) for c = 0..31
 template <class EqDoc>
-__device__ __forceinline__ uint32_t mask_word_t_rolled(const DevMask& m, const int32_t* arg, int bm, int64_t j,
+__device__ __forceinline__ uint32_t mask_word_t_rolled(int n, uint64_t ops, const int32_t* arg, int64_t j,
                                                        int64_t i0, EqDoc eq_doc) {
   uint32_t s0 = 0, s1 = 0, s2 = 0, s3 = 0, s4 = 0, s5 = 0, s6 = 0, s7 = 0;
 #pragma unroll 1
-  for (int k = 0; k < m.n; ++k) {
-    const int op = m.op[k];
+  for (int k = 0; k < n; ++k, ops >>= 4) {
+    const int op = (int)(ops & 15u);
     if (op == FA_M_AND || op == FA_M_OR) {
       s0 = (op == FA_M_AND) ? (s1 & s0) : (s1 | s0);
       s1 = s2; s2 = s3; s3 = s4; s4 = s5; s5 = s6; s6 = s7; s7 = 0;
@@ -151,10 +164,8 @@ __device__ __forceinline__ uint32_t mask_word_t_rolled(const DevMask& m, const i
         w = ~low_bits(j - i0);                              // i >= j
       } else if (op == FA_M_WINDOW) {
         w = low_bits(j + (int64_t)arg[k] - i0);             // i < j + W
-      } else if (op == FA_M_SINK) {
+      } else if (op == FA_M_SINK || op == FA_M_PREFIX) {
         w = (j < (int64_t)arg[k]) ? 0xffffffffu : 0u;       // j < n
-      } else if (op == FA_M_PREFIX) {
-        w = (j < (int64_t)__ldg(m.param[k] + bm)) ? 0xffffffffu : 0u;
       } else if (op == FA_M_SAME_DOC) {
         w = eq_doc();
       } else {
@@ -164,6 +175,12 @@ __device__ __forceinline__ uint32_t mask_word_t_rolled(const DevMask& m, const i
     }
   }
   return s0;
+}
+
+// Word of positions y0 .. y0+31 from a row's two visible intervals [s.x, s.y)
+// and [s.z, s.w) (fa_block_mask::row_segs, where s.x >= 0).
+__device__ __forceinline__ uint32_t seg_word(int4 s, int y0) {
+  return range_bits(s.x, s.y, y0) | range_bits(s.z, s.w, y0);
 }
 
 }  // namespace fa

@@ -51,6 +51,7 @@ struct FwdCtl {
   uint32_t tmem;
   int abort;
   int32_t arg[FA_MAX_MASK_NODES];
+  int4 seg[128];  // per query row: its two visible key intervals (block mask row_segs)
 };
 
 template <int D>
@@ -218,11 +219,23 @@ __global__ void __launch_bounds__(192, 2)
     const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
     const uint32_t tS = tmem + lane_off;
     const uint32_t tO = tmem + lane_off + 128;
+    // the list entry of the first step and this row's visible key columns as
+    // two intervals (kept in shared memory: read on partial tiles only); the
+    // document id and run of the row only for rows the intervals do not
+    // describe, which evaluate the program per word
+    int J_next = n > 0 ? tile_of(0) : 0;
+    const int4 seg0 = __ldg(p.row_segs + (int64_t)bm * 2 * p.seg_len + min(i, p.q_len - 1));
+    ctl->seg[r] = seg0;
     const int32_t* doc_row = p.mask.has_doc ? p.mask.doc + (int64_t)bm * p.mask.doc_len : nullptr;
-    const int32_t doc_i = doc_row ? __ldg(doc_row + min(i, p.q_len - 1)) : 0;
+    int32_t doc_i = 0;
     int run_lo = 0, run_hi = 0;  // with sorted ids: doc[j] == doc[i] exactly for j in [run_lo, run_hi)
-    const bool use_run = doc_row != nullptr && doc_run(p.mask, bm, min(i, p.q_len - 1), run_lo, run_hi);
+    bool use_run = false;
+    if (seg0.x < 0 && doc_row != nullptr) {
+      doc_i = __ldg(doc_row + min(i, p.q_len - 1));
+      use_run = doc_run(p.mask, bm, min(i, p.q_len - 1), run_lo, run_hi);
+    }
 
+    const uint64_t mask_ops = pack_ops(p.mask);
     const float sc_l2 = p.scale * kLog2e;  // logit -> log2 units
     float cap_l2 = 0.f, sc_over_cap = 0.f, slope_l2 = 0.f;
     if constexpr (SCORE == FA_S_SOFTCAP) {
@@ -235,9 +248,12 @@ __global__ void __launch_bounds__(192, 2)
     float m = -INFINITY;  // reference maximum, log2 units
     float l = 0.f;
     bool ok = true;
+    // the list entry of the next step is fetched one step ahead, off the path
+    // from the S wait to the mask words
     for (int jj = 0; jj < n; ++jj) {
       const bool partial = jj >= n_full;
-      const int J = tile_of(jj);
+      const int J = J_next;
+      if (jj + 1 < n) J_next = tile_of(jj + 1);
       const int64_t j0 = (int64_t)J * 128;
       const bool ragged = j0 + 128 > p.kv_len;
       const bool msk = partial || ragged;
@@ -248,7 +264,10 @@ __global__ void __launch_bounds__(192, 2)
         for (int c = 0; c < 4; ++c) {
           const int jc = (int)j0 + 32 * c;
           uint32_t w = low_bits((int64_t)p.kv_len - jc);
-          if (partial) {
+          const int4 sg = ctl->seg[r];
+          if (partial && sg.x >= 0) {
+            w &= seg_word(sg, jc);
+          } else if (partial) {
             // doc ids of the 32 key columns: the same addresses for every thread (broadcast loads)
             auto eq = [&]() {
               if (use_run) return range_bits(run_lo, run_hi, jc);
@@ -267,7 +286,7 @@ __global__ void __launch_bounds__(192, 2)
               }
               return bits;
             };
-            w &= mask_word_rolled(p.mask, ctl->arg, bm, i, jc, eq);
+            w &= mask_word_rolled(p.mask.n, mask_ops, ctl->arg, i, jc, eq);
           }
           // select by c without dynamic indexing
           wd[0] = (c == 0) ? w : wd[0];

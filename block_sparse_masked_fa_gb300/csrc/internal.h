@@ -17,6 +17,7 @@ struct BuildArgs {
   uint8_t* tile_class;
   int32_t* summary;  // [Bm][2][max(nq, nkv)][4]: doc-id min, max, step-0/1 flag per query / key tile
   int32_t* doc_runs;  // [Bm][max(q_len, kv_len)][2] runs, then [Bm] sorted flags
+  int32_t* row_segs;  // [Bm][2][max(q_len, kv_len)][4] visible intervals per row / column
   uint32_t* status;
 };
 
@@ -34,6 +35,8 @@ struct AttnArgs {
   const float* score_param;
   uint32_t* status;
   DevMask mask;
+  const int4* row_segs;  // [Bm][2][seg_len]: see fa_block_mask
+  int64_t seg_len;
 };
 
 struct FwdTensors {

@@ -141,6 +141,15 @@ typedef struct {
  *                      when the ids never decrease (then doc[i] == doc[j] iff j
  *                      lies in i's run, which the kernels use on PARTIAL tiles).
  *                      Filled only when the program has SAME_DOC.
+ *   row_segs           int32 [Bm][2][max(q_len, kv_len)][4]: for every query
+ *                      row i ([bm][0][i]) the key columns it sees, and for
+ *                      every key column j ([bm][1][j]) the query rows that see
+ *                      it, as two intervals [lo0, hi0) and [lo1, hi1) (empty
+ *                      when lo == hi) -- or lo0 = -1 where that does not
+ *                      describe the row (more pieces, or document ids that
+ *                      decrease somewhere).  The attention kernels build their
+ *                      PARTIAL tiles' mask words from it, and evaluate the
+ *                      program per element where lo0 = -1.
  *   status             device status word (bit 0: a wait timed out).
  *
  * The union kv_num_blocks + full_kv_num_blocks is the count of "tiles that are
@@ -167,6 +176,7 @@ typedef struct {
   uint8_t* tile_class;
   int32_t* tile_summary;
   int32_t* doc_runs;
+  int32_t* row_segs;
   uint32_t* status;
   fa_mask_spec spec;
 } fa_block_mask;
@@ -183,7 +193,7 @@ fa_status fa_block_mask_bytes(int32_t Bm, int32_t Hm, int64_t q_len, int64_t kv_
  * buffer: device memory of at least fa_block_mask_bytes() bytes, 256-byte
  * aligned, owned by the caller and used until the block mask is dropped.
  * bm: host struct, filled with pointers into `buffer` and a copy of `spec`.
- * Queues 4-5 kernels on `stream`; clears the status word. */
+ * Queues 4-6 kernels on `stream`; clears the status word. */
 fa_status fa_create_block_mask(const fa_mask_spec* spec, int32_t Bm, int32_t Hm, int64_t q_len, int64_t kv_len,
                                int32_t block, void* buffer, size_t buffer_bytes, fa_block_mask* bm,
                                cudaStream_t stream);

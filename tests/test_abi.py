@@ -55,7 +55,7 @@ def test_block_mask_bytes_layout(Bm, Hm, q, kv, block):
     nq, nkv = -(-q // block), -(-kv // block)
     rows, cols, tiles = Bm * Hm * nq, Bm * Hm * nkv, Bm * Hm * nq * nkv
     sizes = [rows * 4, tiles * 4, rows * 4, tiles * 4, cols * 4, tiles * 4, cols * 4, tiles * 4, rows * 4, cols * 4,
-             tiles, Bm * 2 * max(nq, nkv) * 4 * 4, Bm * max(q, kv) * 8 + Bm * 4, 4]
+             tiles, Bm * 2 * max(nq, nkv) * 4 * 4, Bm * max(q, kv) * 8 + Bm * 4, Bm * 2 * max(q, kv) * 16, 4]
     assert fa.fa_block_mask_bytes(Bm, Hm, q, kv, block) == sum(_align(s) for s in sizes)
 
 

@@ -162,3 +162,16 @@ def test_unsorted_document_ids():
     got = run_fa(inp, mask)
     for h in range(2):
         check_all([g[0, h] for g in got], oracle_grads(inp, mask, 0, h, ("none",)), f"unsorted h{h}")
+
+
+def test_rows_of_three_intervals():
+    """Key columns seen by up to three separate query ranges (fallback to the
+    per-word program) and by at most two (interval summary), against the oracle."""
+    S = 1100
+    docs = np.repeat(np.arange(11), 100).astype(np.int32)[None]
+    inp = _inputs(1, 2, S, 64, 36, docs=docs)
+    for mask in (P(("sink", 10), ("causal",), ("window", 64), ("and",), ("or",), ("same_doc",), ("or",)),
+                 P(("sink", 10), ("causal",), ("window", 64), ("and",), ("or",))):
+        got = run_fa(inp, mask)
+        for h in range(2):
+            check_all([g[0, h] for g in got], oracle_grads(inp, mask, 0, h, ("none",)), f"{len(mask.nodes)} nodes h{h}")

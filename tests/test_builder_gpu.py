@@ -156,3 +156,80 @@ def test_doc_runs_table(case):
         if srt:  # the kernels use the ranges only for rows whose ids never decrease
             np.testing.assert_array_equal(runs[b, :, 0], lo)
             np.testing.assert_array_equal(runs[b, :, 1], hi)
+
+
+def _true_runs(v):
+    """[lo, hi) runs of True in a boolean vector."""
+    d = np.diff(np.concatenate([[0], v.astype(np.int8), [0]]))
+    return list(zip(np.nonzero(d == 1)[0], np.nonzero(d == -1)[0]))
+
+
+def _breaks(mask, transposed):
+    """Interval ends the program's atoms contribute for one row (see the row_segs kernel)."""
+    per = {"causal": 1, "window": 1, "same_doc": 2, "sink": 0 if transposed else 1, "prefix": 0 if transposed else 1}
+    return sum(per.get(n[0], 0) for n in mask.nodes)
+
+
+def check_row_segs(bm, mask, docs, prefix, Bm, q_len, kv_len):
+    """Every summarised row equals the oracle's visible set exactly, and every
+    row that two intervals describe is summarised (when the ids are sorted and
+    the program has at most seven interval ends)."""
+    segs = bm.row_segs().cpu().numpy()
+    L = max(q_len, kv_len)
+    has_doc = any(n[0] == "same_doc" for n in mask.nodes)
+    for b in range(Bm):
+        prog = oracle.Program(mask, doc_row=None if docs is None else docs[b],
+                              prefix_len=None if prefix is None else int(prefix[b]))
+        M = oracle.mask_dense(prog, q_len, kv_len)
+        sorted_ids = not has_doc or bool(np.all(np.diff(np.asarray(docs[b][:L], dtype=np.int64)) >= 0))
+        for which, R in ((0, M), (1, M.T)):
+            must = sorted_ids and _breaks(mask, which == 1) <= 7
+            for x in range(R.shape[0]):
+                lo0, hi0, lo1, hi1 = (int(v) for v in segs[b, which, x])
+                if must and len(_true_runs(R[x])) <= 2:
+                    assert lo0 >= 0, (b, which, x)
+                if lo0 >= 0:
+                    got = np.zeros(R.shape[1], dtype=bool)
+                    got[lo0:hi0] = True
+                    got[lo1:hi1] = True
+                    np.testing.assert_array_equal(got, R[x], err_msg=f"b{b} {'col' if which else 'row'} {x}")
+
+
+@pytest.mark.parametrize("wnum", [1, 2, 3, 4, 5])
+def test_row_segs_workload_programs(wnum):
+    """The row interval summary of each workload's program, at reduced sizes
+    with a ragged tail and q_len != kv_len."""
+    w = WORKLOADS[wnum]
+    q_len, kv_len = 1111, 1300
+    docs = None if w.docs is None else make_doc_ids(w.docs, max(q_len, kv_len), 40 + wnum, batch=2)
+    mask = w.mask.with_window(300) if w.windows else w.mask
+    bm = fa.fa_create_block_mask(device_nodes(mask, docs), 2 if docs is not None else 1, 1, q_len, kv_len, 128)
+    check_row_segs(bm, mask, docs, None, 2 if docs is not None else 1, q_len, kv_len)
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_row_segs_random_programs(seed):
+    rng = np.random.default_rng(300 + seed)
+    nodes = _random_program(rng)
+    if len(nodes) > 16:
+        nodes = nodes[:1]
+    mask = MaskProgram(tuple(nodes))
+    q_len, kv_len = int(rng.integers(1, 900)), int(rng.integers(1, 900))
+    Bm = 2
+    docs = make_doc_ids(("geometric", float(rng.integers(20, 300))), max(q_len, kv_len), seed, batch=Bm)
+    prefix = rng.integers(0, 800, size=Bm).astype(np.int32)
+    bm = fa.fa_create_block_mask(device_nodes(mask, docs, prefix), Bm, 1, q_len, kv_len, 64)
+    check_row_segs(bm, mask, docs, prefix, Bm, q_len, kv_len)
+
+
+def test_row_segs_unsorted_ids_not_summarised():
+    """Ids that decrease somewhere: rows of a SAME_DOC program are left to the
+    per-word evaluation (lo0 = -1); a program without SAME_DOC is unaffected."""
+    rng = np.random.default_rng(9)
+    docs = np.repeat(rng.integers(0, 4, size=9), 100).astype(np.int32)[None]
+    for mask, summarised in ((MaskProgram((("same_doc",), ("causal",), ("and",))), False),
+                             (MaskProgram((("causal",), ("window", 200), ("and",))), True)):
+        bm = fa.fa_create_block_mask(device_nodes(mask, docs), 1, 1, 900, 900, 128)
+        segs = bm.row_segs().cpu().numpy()
+        assert bool(np.all(segs[0, :, :, 0] >= 0)) == summarised
+        check_row_segs(bm, mask, docs, None, 1, 900, 900)

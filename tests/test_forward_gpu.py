@@ -204,3 +204,19 @@ def test_unsorted_document_ids(D):
     for h in range(2):
         ref_out, ref_lse = oracle_rows(inp, mask, 0, h, None, ("none",))
         check_forward(out[0, h], lse[0, h], ref_out, ref_lse, f"unsorted h{h}")
+
+
+def test_rows_of_three_intervals():
+    """sink | (causal & window) | same_doc: a row sees up to three separate key
+    ranges, more than the two-interval row summary holds, so the kernels fall
+    back to evaluating the program per word; a second program with at most two
+    per row takes the summary path.  Both against the oracle."""
+    S = 1100
+    docs = np.repeat(np.arange(11), 100).astype(np.int32)[None]
+    inp = _inputs(1, 2, S, 64, 35, docs=docs)
+    for mask in (P(("sink", 10), ("causal",), ("window", 64), ("and",), ("or",), ("same_doc",), ("or",)),
+                 P(("sink", 10), ("causal",), ("window", 64), ("and",), ("or",))):
+        out, lse, _ = run_fa(inp, mask)
+        for h in range(2):
+            ref_out, ref_lse = oracle_rows(inp, mask, 0, h, None, ("none",))
+            check_forward(out[0, h], lse[0, h], ref_out, ref_lse, f"{len(mask.nodes)} nodes h{h}")
