@@ -116,6 +116,14 @@ __device__ __forceinline__ uint64_t kmajor_step(uint64_t desc, int kk) {
   return desc + (uint64_t)((kk >> 2) * (16384 >> 4) + (kk & 3) * (32 >> 4));
 }
 __device__ __forceinline__ uint64_t mnmajor_step(uint64_t desc, int kk) { return desc + (uint64_t)(kk * (2048 >> 4)); }
+// A value the compiler cannot move out of the loop it is computed in: the MMA
+// issue loops are unrolled, and holding every step's descriptor of every GEMM
+// in registers across the work loop would not fit the MMA warp's budget.
+__device__ __forceinline__ uint64_t opaque(uint64_t x) {
+  uint64_t r;
+  asm volatile("mov.b64 %0, %1;" : "=l"(r) : "l"(x));
+  return r;
+}
 
 // Writes 32 bf16 values (16 packed words) of row r into a 128-byte-swizzled
 // [chunks][128 rows][64] tile at columns [32 c, 32 c + 32).
@@ -285,8 +293,8 @@ __global__ void __launch_bounds__(512, 1)
           const int qs = it % C::NQ;
           if (!mbar_wait(smem_u32(&ctl->q_full[qs]), (it / C::NQ) & 1, &ctl->abort)) return false;
           tc_fence_after();
-          const uint64_t a0 = sdesc_sw128(k_base, 16, 1024), b0 = sdesc_sw128(smem_u32(sQ(qs)), 16, 1024);
-#pragma unroll 1
+          const uint64_t a0 = opaque(sdesc_sw128(k_base, 16, 1024)), b0 = opaque(sdesc_sw128(smem_u32(sQ(qs)), 16, 1024));
+#pragma unroll
           for (int kk = 0; kk < D / 16; ++kk)
             mma_ss(tmem + C::T_S, kmajor_step(a0, kk), kmajor_step(b0, kk), kIdKK, kk > 0);
           mma_commit(b_s);
@@ -299,8 +307,8 @@ __global__ void __launch_bounds__(512, 1)
           if (!mbar_wait(smem_u32(&ctl->do_full[ds]), (it / C::NDO) & 1, &ctl->abort)) return false;
           if (it > 0 && !mbar_wait(b_dqf, (it - 1) & 1, &ctl->abort)) return false;
           tc_fence_after();
-          const uint64_t a0 = sdesc_sw128(v_base, 16, 1024), b0 = sdesc_sw128(smem_u32(sDO(ds)), 16, 1024);
-#pragma unroll 1
+          const uint64_t a0 = opaque(sdesc_sw128(v_base, 16, 1024)), b0 = opaque(sdesc_sw128(smem_u32(sDO(ds)), 16, 1024));
+#pragma unroll
           for (int kk = 0; kk < D / 16; ++kk)
             mma_ss(tmem + C::T_DP, kmajor_step(a0, kk), kmajor_step(b0, kk), kIdKK, kk > 0);
           mma_commit(b_dp);
@@ -322,8 +330,8 @@ __global__ void __launch_bounds__(512, 1)
           // dV += P^T dO; P^T of query columns [64 h, 64 h + 64) sits at TMEM columns [64 h, 64 h + 32).
           // It runs while the key-row warps compute dS.
           {
-            const uint64_t b0 = sdesc_sw128(do_base, 16384, 1024);
-#pragma unroll 1
+            const uint64_t b0 = opaque(sdesc_sw128(do_base, 16384, 1024));
+#pragma unroll
             for (int kk = 0; kk < 8; ++kk)
               mma_ts(tmem + C::T_DV, tmem + C::T_S + (kk / 4) * 64 + (kk % 4) * 8, mnmajor_step(b0, kk), kIdKM,
                      (it > 0 || kk > 0));
@@ -335,8 +343,8 @@ __global__ void __launch_bounds__(512, 1)
           }
           tc_fence_after();
           {  // dQ = dS K, over the dP^T columns the key-row warps have read
-            const uint64_t a0 = sdesc_sw128(ds_base, 16384, 1024), b0 = sdesc_sw128(k_base, 16384, 1024);
-#pragma unroll 1
+            const uint64_t a0 = opaque(sdesc_sw128(ds_base, 16384, 1024)), b0 = opaque(sdesc_sw128(k_base, 16384, 1024));
+#pragma unroll
             for (int kk = 0; kk < 8; ++kk) mma_ss(tmem + C::T_DP, mnmajor_step(a0, kk), mnmajor_step(b0, kk), kIdMM, kk > 0);
           }
           mma_commit(b_dq);
@@ -345,8 +353,8 @@ __global__ void __launch_bounds__(512, 1)
             break;
           }
           {  // dK += dS^T Q
-            const uint64_t a0 = sdesc_sw128(ds_base, 16, 1024), b0 = sdesc_sw128(q_base, 16384, 1024);
-#pragma unroll 1
+            const uint64_t a0 = opaque(sdesc_sw128(ds_base, 16, 1024)), b0 = opaque(sdesc_sw128(q_base, 16384, 1024));
+#pragma unroll
             for (int kk = 0; kk < 8; ++kk)
               mma_ss(tmem + C::T_DK, kmajor_step(a0, kk), mnmajor_step(b0, kk), kIdKM, (it > 0 || kk > 0));
           }
