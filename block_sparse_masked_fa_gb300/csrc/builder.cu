@@ -12,8 +12,10 @@
 //                     Each lane classifies one tile with a three-valued
 //                     interval test per atom (nothing / everything / undecided
 //                     visible, combined with Kleene AND / OR); undecided tiles
-//                     are settled exactly by evaluating all their pairs with
-//                     the whole warp.  Writes one class byte per tile.
+//                     are settled exactly by the whole warp, counting each
+//                     row's visible pairs from its row_segs intervals (or, for
+//                     rows they do not describe, evaluating all its pairs).
+//                     Writes one class byte per tile.
 //  3. compact      -- one warp per query-tile row and one per key-tile
 //                     column: ballot + popcount prefix sums turn the class
 //                     bytes into ascending PARTIAL and FULL index lists with
@@ -359,8 +361,17 @@ __global__ void __launch_bounds__(kBuildWarps * 32) classify_kernel(const __grid
     const int64_t j1 = min(j0 + a.block, a.kv_len) - 1;
     const int64_t rows = i1 - i0 + 1, cols = j1 - j0 + 1;
     int cnt = 0;
+    const int64_t L = max(a.q_len, a.kv_len);
     for (int64_t r = lane; r < rows; r += 32) {
       const int64_t i = i0 + r;
+      // the row's visible columns as two intervals (row_segs_kernel ran first):
+      // its count inside the tile is two overlaps
+      const int4 sg = reinterpret_cast<const int4*>(a.row_segs)[((int64_t)bm * 2) * L + i];
+      if (sg.x >= 0) {
+        cnt += (int)(max((int64_t)0, min((int64_t)sg.y, j1 + 1) - max((int64_t)sg.x, j0)) +
+                     max((int64_t)0, min((int64_t)sg.w, j1 + 1) - max((int64_t)sg.z, j0)));
+        continue;
+      }
       const int32_t doc_i = doc ? __ldg(doc + i) : 0;
       int run_lo = 0, run_hi = 0;
       const bool use_run = doc != nullptr && doc_run(a.mask, bm, i, run_lo, run_hi);
