@@ -14,13 +14,16 @@
 //  1. bwd_pre   -- Delta_i = dO_i . out_i (fp32) and LSE, laid out per query
 //                  tile (the key-row warps copy a tile's values in per step),
 //                  and a zeroed fp32 dq accumulator.
-//  2. bwd_kernel -- one CTA per (b, h, key tile J), key tiles longest first:
+//  2. bwd_kernel -- persistent, one CTA per SM, each taking every gridDim.x-th
+//     (b, h, key tile J) of the longest-first order:
 //       warps 0-7    TMEM lane r = 32 (warp % 4) + lane = key row r, query columns
 //                    [64 (warp / 4), +64): phase A, P^T into TMEM; phase B, dS^T
 //                    into shared memory; LSE_I, Delta_I copied in per step
 //       warps 8-11   dQ rows [32 (warp % 4), +32) out of TMEM, staged 32 x 32 at a
-//                    time and TMA bulk reduce-added into the fp32 accumulator
-//       warp 12      TMA producer: K_J, V_J once; Q_I, dO_I per step
+//                    time and TMA bulk reduce-added into the fp32 accumulator;
+//                    after a key tile's last step, its dV and dK rows out of TMEM,
+//                    staged the same way and TMA-stored
+//       warp 12      TMA producer: V_J, then Q_I, dO_I per step, K_J with the first
 //       warp 13      MMA issuer, five tcgen05 GEMMs per (I, J):
 //                     once P^T is in:  dV  += P^T dO   (P^T bf16 read from TMEM [0,64))
 //                     once dS is in:   dQ   = dS K     (dS read MN-major; TMEM [128,128+D))
@@ -28,15 +31,20 @@
 //                                      dK  += dS^T Q   (dS read K-major)
 //                                      dP^T = V dO^T   (next step; TMEM [128,256), once dQ is read out)
 //     dV runs while the key-row warps compute dS, and the next S^T before dK
-//     so that phase A of the next step can start early.  Registers are split
+//     (with D = 64, right after dV) so that phase A of the next step can start
+//     early.  Registers are split
 //     per warpgroup (setmaxnreg) so that the key-row warps hold a row's 64
 //     probabilities across the two phases.
 //     dK and dV stay in TMEM for the whole key tile and are written once
 //     (no atomics); dQ partial tiles are added into the fp32 accumulator.
+//     Across key tiles the pipeline keeps going: the next tile's V loads once
+//     its last dP^T is done, its K once its last dQ is, and the dK / dV write-out
+//     of one key tile overlaps the first step of the next.
 //  3. bwd_dq_convert -- dq = bf16(scale * accumulator).
 #include <cfloat>
 #include <cmath>
 
+#include <algorithm>
 #include <mutex>
 
 #include <cuda_bf16.h>
@@ -74,13 +82,13 @@ struct TileStats {  // per query tile, from the workspace
 
 struct BwdCtl {
   alignas(16) TileStats stats;  // of the current step, copied in by the key-row warps
-  uint64_t kv_full;
+  uint64_t k_full, v_full, k_empty, v_empty;
   uint64_t q_full[2], q_empty[2];
   uint64_t do_full[2], do_empty[2];
-  uint64_t s_full, dp_full, pa_full, pb_full, dq_full, dq_free, acc_full, fin;
+  uint64_t s_full, dp_full, pa_full, pb_full, dq_full, dq_free, acc_full, acc_free, fin;
   uint32_t tmem;
   int abort;
-  int32_t arg[FA_MAX_MASK_NODES];
+  int32_t arg[2][FA_MAX_MASK_NODES];  // mask program arguments of the current item, per key-row half
 };
 
 template <int D>
@@ -88,6 +96,7 @@ constexpr size_t bwd_smem_bytes() {
   using C = BwdCfg<D>;
   return 1024 + (size_t)C::TILE * (2 + C::NQ + C::NDO) + C::DS_BYTES + C::STG_BYTES + sizeof(BwdCtl);
 }
+static_assert(bwd_smem_bytes<128>() <= 227 * 1024, "backward shared memory");
 
 __device__ __forceinline__ void fail(const AttnArgs& p, BwdCtl* ctl) {
   atomicOr(p.status, kStatusTimeout);
@@ -137,6 +146,44 @@ __device__ __forceinline__ void store_row32(uint8_t* tile, int r, int c, const u
   }
 }
 
+// One work item: the key tile J of head (b, h), with the query tiles of its
+// column lists (FULL first, then PARTIAL).
+struct BwdItem {
+  int J, bh, bm, h, n_full, n;
+  int64_t list;  // offset of the column's lists
+};
+
+__device__ __forceinline__ BwdItem bwd_item(const AttnArgs& p, int k) {
+  const int rep = (p.B / p.Bm) * (p.H / p.Hm);
+  const int col = __ldg(p.col_order + k / rep);  // index into [Bm][Hm][nkv], longest first
+  const int t = k % rep;
+  BwdItem it;
+  it.J = col % p.nkv;
+  const int hm = (col / p.nkv) % p.Hm;
+  it.bm = col / (p.nkv * p.Hm);
+  const int b = (p.Bm == 1) ? t / (p.H / p.Hm) : it.bm;
+  it.h = (p.Hm == 1) ? t % (p.H / p.Hm) : hm;
+  it.bh = b * p.H + it.h;
+  it.n_full = __ldg(p.full_q_num + col);
+  it.n = it.n_full + __ldg(p.q_num + col);
+  it.list = (int64_t)col * p.nq;
+  return it;
+}
+
+__device__ __forceinline__ int tile_of(const AttnArgs& p, const BwdItem& it, int s) {
+  return s < it.n_full ? __ldg(p.full_q_idx + it.list + s) : __ldg(p.q_idx + it.list + s - it.n_full);
+}
+
+// This CTA's first item at or after k (its items are k, k + gridDim.x, ...)
+// with at least one visible query tile; a value >= items when none is left.
+__device__ __forceinline__ int next_live(const AttnArgs& p, int k, int items, BwdItem& it) {
+  for (; k < items; k += (int)gridDim.x) {
+    it = bwd_item(p, k);
+    if (it.n > 0) break;
+  }
+  return k;
+}
+
 template <int D, int SCORE>
 __global__ void __launch_bounds__(512, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -158,26 +205,18 @@ __global__ void __launch_bounds__(512, 1)
   auto sDO = [&](int st) { return sDO0 + st * C::TILE; };
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int items = p.B * p.H * p.nkv;  // below 2^31: checked at launch
 
-  // ---- work item: (b, h, key tile J), columns taken longest first
-  const int rep = (p.B / p.Bm) * (p.H / p.Hm);
-  const int col = p.col_order[blockIdx.x / rep];  // index into [Bm][Hm][nkv]
-  const int t = blockIdx.x % rep;
-  const int J = col % p.nkv;
-  const int hm = (col / p.nkv) % p.Hm;
-  const int bm = col / (p.nkv * p.Hm);
-  const int b = (p.Bm == 1) ? t / (p.H / p.Hm) : bm;
-  const int h = (p.Hm == 1) ? t % (p.H / p.Hm) : hm;
-  const int bh = b * p.H + h;
-  const int n_full = p.full_q_num[col];
-  int n = n_full + p.q_num[col];
-  const int64_t list = (int64_t)col * p.nq;
-
-  const uint32_t b_kv = smem_u32(&ctl->kv_full), b_s = smem_u32(&ctl->s_full), b_dp = smem_u32(&ctl->dp_full),
+  const uint32_t b_kf = smem_u32(&ctl->k_full), b_vf = smem_u32(&ctl->v_full), b_ke = smem_u32(&ctl->k_empty),
+                 b_ve = smem_u32(&ctl->v_empty), b_s = smem_u32(&ctl->s_full), b_dp = smem_u32(&ctl->dp_full),
                  b_pa = smem_u32(&ctl->pa_full), b_pb = smem_u32(&ctl->pb_full), b_dq = smem_u32(&ctl->dq_full),
-                 b_dqf = smem_u32(&ctl->dq_free), b_acc = smem_u32(&ctl->acc_full), b_fin = smem_u32(&ctl->fin);
+                 b_dqf = smem_u32(&ctl->dq_free), b_acc = smem_u32(&ctl->acc_full),
+                 b_accf = smem_u32(&ctl->acc_free), b_fin = smem_u32(&ctl->fin);
   if (threadIdx.x == 0) {
-    mbar_init(b_kv, 1);
+    mbar_init(b_kf, 1);
+    mbar_init(b_vf, 1);
+    mbar_init(b_ke, 1);
+    mbar_init(b_ve, 1);
     for (int s2 = 0; s2 < 2; ++s2) {
       mbar_init(smem_u32(&ctl->q_full[s2]), 1);
       mbar_init(smem_u32(&ctl->q_empty[s2]), 1);
@@ -191,11 +230,11 @@ __global__ void __launch_bounds__(512, 1)
     mbar_init(b_dq, 1);
     mbar_init(b_dqf, C::DQ_THREADS);
     mbar_init(b_acc, 1);
+    mbar_init(b_accf, C::DQ_THREADS);
     mbar_init(b_fin, 1);
     ctl->abort = (*reinterpret_cast<volatile uint32_t*>(p.status) & kStatusTimeout) ? 1 : 0;
     fence_mbar_init();
   }
-  if (threadIdx.x < p.mask.n) ctl->arg[threadIdx.x] = node_arg(p.mask, threadIdx.x, bm);
   if (warp == C::PRODUCER_WARP) {
     tmem_alloc(smem_u32(&ctl->tmem), C::TMEM_COLS);
     tmem_relinquish();
@@ -205,9 +244,7 @@ __global__ void __launch_bounds__(512, 1)
   tc_fence_after();
   const uint32_t tmem = ctl->tmem;
   const bool skip = ctl->abort != 0;
-  if (skip) n = 0;
-
-  auto tile_of = [&](int it) -> int { return it < n_full ? p.full_q_idx[list + it] : p.q_idx[list + it - n_full]; };
+  const int first = skip ? items : (int)blockIdx.x;
 
   // teardown, at the end of every role: all threads past their last TMEM
   // access, then the allocating warp frees the columns
@@ -221,31 +258,47 @@ __global__ void __launch_bounds__(512, 1)
     }
   };
 
+  // The CTA stays resident and takes the items blockIdx.x, blockIdx.x +
+  // gridDim.x, ...; every role walks the same sequence.  Steps (I, J) are
+  // numbered across items (g) for the per-step barriers and the Q / dO rings;
+  // items with visible query tiles are numbered (u) for the K / V buffers and
+  // the dK / dV accumulators.
+  //
   // Register budgets per warpgroup, set at the top of each warpgroup's branch
-  // (launched with 128 per thread): key-row warps 176, dQ warps 104, producer /
-  // MMA warpgroup 56 -- 256 x 176 + 128 x 104 + 128 x 56 = 512 x 128.
+  // (launched with 128 per thread): key-row warps 176, dQ warps 112, producer /
+  // MMA warpgroup 48 -- 256 x 176 + 128 x 112 + 128 x 48 = 512 x 128.
   if (warp >= C::PRODUCER_WARP) {
-    setmaxnreg_dec<56>();
+    setmaxnreg_dec<48>();
     if (warp == C::PRODUCER_WARP) {
       // ------------------------------------------------------------ producer
-      if (n > 0) {
-        if (lane == 0) {
-          prefetch_tmap(&tm_q);
-          prefetch_tmap(&tm_k);
-          prefetch_tmap(&tm_v);
-          prefetch_tmap(&tm_do);
-          mbar_arrive_expect_tx(b_kv, 2 * C::TILE);
-          for (int c = 0; c < C::NC; ++c) {
-            tma_load_3d(smem_u32(sK + c * 16384), &tm_k, b_kv, c * 64, J * 128, bh);
-            tma_load_3d(smem_u32(sV + c * 16384), &tm_v, b_kv, c * 64, J * 128, bh);
-          }
+      // Per item: V once dP of the last item's last step is done with it, then
+      // the step's Q and dO, and K once dQ of the last item's last step is.
+      if (lane == 0) {
+        prefetch_tmap(&tm_q);
+        prefetch_tmap(&tm_k);
+        prefetch_tmap(&tm_v);
+        prefetch_tmap(&tm_do);
+      }
+      int g = 0, q_issued = 0, do_issued = 0, v_issued = 0, k_issued = 0;
+      int u = 0;
+      bool ok = true;
+      BwdItem cur;
+      for (int k = next_live(p, first, items, cur); ok && k < items; ++u) {
+        BwdItem nxt;
+        const int kn = next_live(p, k + (int)gridDim.x, items, nxt);
+        if (u > 0 && !warp_wait(b_ve, (u - 1) & 1, &ctl->abort)) {
+          ok = false;
+          break;
         }
-        int q_issued = 0, do_issued = 0;
-        bool ok = true;
-        for (int it = 0; it < n; ++it) {
-          const int I = tile_of(it);
+        if (lane == 0) {
+          mbar_arrive_expect_tx(b_vf, C::TILE);
+          for (int c = 0; c < C::NC; ++c) tma_load_3d(smem_u32(sV + c * 16384), &tm_v, b_vf, c * 64, cur.J * 128, cur.bh);
+        }
+        v_issued = u + 1;
+        for (int s = 0; s < cur.n; ++s, ++g) {
+          const int I = tile_of(p, cur, s);
           // Q slot (freed by the MMA warp once dK, its last reader, is done)
-          const int qs = it % C::NQ, quse = it / C::NQ;
+          const int qs = g % C::NQ, quse = g / C::NQ;
           if (quse > 0 && !warp_wait(smem_u32(&ctl->q_empty[qs]), (quse - 1) & 1, &ctl->abort)) {
             ok = false;
             break;
@@ -253,12 +306,11 @@ __global__ void __launch_bounds__(512, 1)
           if (lane == 0) {
             const uint32_t qbar = smem_u32(&ctl->q_full[qs]);
             mbar_arrive_expect_tx(qbar, C::TILE);
-            for (int c = 0; c < C::NC; ++c)
-              tma_load_3d(smem_u32(sQ(qs) + c * 16384), &tm_q, qbar, c * 64, I * 128, bh);
+            for (int c = 0; c < C::NC; ++c) tma_load_3d(smem_u32(sQ(qs) + c * 16384), &tm_q, qbar, c * 64, I * 128, cur.bh);
           }
-          q_issued = it + 1;
+          q_issued = g + 1;
           // dO slot (freed once dV, its last reader, is done)
-          const int ds = it % C::NDO, duse = it / C::NDO;
+          const int ds = g % C::NDO, duse = g / C::NDO;
           if (duse > 0 && !warp_wait(smem_u32(&ctl->do_empty[ds]), (duse - 1) & 1, &ctl->abort)) {
             ok = false;
             break;
@@ -267,31 +319,56 @@ __global__ void __launch_bounds__(512, 1)
             const uint32_t dbar = smem_u32(&ctl->do_full[ds]);
             mbar_arrive_expect_tx(dbar, C::TILE);
             for (int c = 0; c < C::NC; ++c)
-              tma_load_3d(smem_u32(sDO(ds) + c * 16384), &tm_do, dbar, c * 64, I * 128, bh);
+              tma_load_3d(smem_u32(sDO(ds) + c * 16384), &tm_do, dbar, c * 64, I * 128, cur.bh);
           }
-          do_issued = it + 1;
+          do_issued = g + 1;
+          if (s == 0) {
+            if (u > 0 && !warp_wait(b_ke, (u - 1) & 1, &ctl->abort)) {
+              ok = false;
+              break;
+            }
+            if (lane == 0) {
+              mbar_arrive_expect_tx(b_kf, C::TILE);
+              for (int c = 0; c < C::NC; ++c)
+                tma_load_3d(smem_u32(sK + c * 16384), &tm_k, b_kf, c * 64, cur.J * 128, cur.bh);
+            }
+            k_issued = u + 1;
+          }
         }
-        if (!ok && lane == 0) fail(p, ctl);
-        // drain: every copy this CTA started lands before it exits
-        if (lane == 0) {
-          mbar_wait(b_kv, 0, nullptr);
-          for (int it = max(0, q_issued - C::NQ); it < q_issued; ++it)
-            mbar_wait(smem_u32(&ctl->q_full[it % C::NQ]), (it / C::NQ) & 1, nullptr);
-          for (int it = max(0, do_issued - C::NDO); it < do_issued; ++it)
-            mbar_wait(smem_u32(&ctl->do_full[it % C::NDO]), (it / C::NDO) & 1, nullptr);
-        }
+        cur = nxt;
+        k = kn;
+      }
+      if (!ok && lane == 0) fail(p, ctl);
+      // drain: every copy this CTA started lands before it exits (each buffer's
+      // earlier loads were waited for before the last one was issued)
+      if (lane == 0) {
+        if (v_issued > 0) mbar_wait(b_vf, (v_issued - 1) & 1, nullptr);
+        if (k_issued > 0) mbar_wait(b_kf, (k_issued - 1) & 1, nullptr);
+        for (int s = max(0, q_issued - C::NQ); s < q_issued; ++s)
+          mbar_wait(smem_u32(&ctl->q_full[s % C::NQ]), (s / C::NQ) & 1, nullptr);
+        for (int s = max(0, do_issued - C::NDO); s < do_issued; ++s)
+          mbar_wait(smem_u32(&ctl->do_full[s % C::NDO]), (s / C::NDO) & 1, nullptr);
       }
     } else if (warp == C::MMA_WARP) {
       // ------------------------------------------------------------ MMA issuer
-      if (lane == 0 && n > 0) {
+      if (lane == 0) {
         constexpr uint32_t kIdKK = idesc_bf16(128, 128, false, false);  // S^T, dP^T
         constexpr uint32_t kIdKM = idesc_bf16(128, D, false, true);     // dV (A in TMEM), dK
         constexpr uint32_t kIdMM = idesc_bf16(128, D, true, true);      // dQ
+        // Where the next step's S^T goes in the MMA order.  Each step's chain
+        // runs dS -> dQ -> dQ read out of TMEM -> next dP^T -> next dS, with
+        // phase A off it; with D = 128 the S^T MMA goes after dQ so as not to
+        // delay that chain, with D = 64 (shorter MMAs) right after dV, so that
+        // phase A of the next step can start as soon as dS is in (measured
+        // faster each way on the packed-document workloads).
+        constexpr bool kEarlyS = (D == 64);
         const uint32_t k_base = smem_u32(sK), v_base = smem_u32(sV), ds_base = smem_u32(sDS);
-        // S^T = K Q^T of step it, into columns the dV MMA of the step before has read
-        auto issue_s = [&](int it) -> bool {
-          const int qs = it % C::NQ;
-          if (!mbar_wait(smem_u32(&ctl->q_full[qs]), (it / C::NQ) & 1, &ctl->abort)) return false;
+        // S^T = K Q^T of step g (step s of item u), into columns the dV MMA of
+        // the step before has read
+        auto issue_s = [&](int g, int s, int u) -> bool {
+          const int qs = g % C::NQ;
+          if (s == 0 && !mbar_wait(b_kf, u & 1, &ctl->abort)) return false;
+          if (!mbar_wait(smem_u32(&ctl->q_full[qs]), (g / C::NQ) & 1, &ctl->abort)) return false;
           tc_fence_after();
           const uint64_t a0 = opaque(sdesc_sw128(k_base, 16, 1024)), b0 = opaque(sdesc_sw128(smem_u32(sQ(qs)), 16, 1024));
 #pragma unroll
@@ -300,74 +377,95 @@ __global__ void __launch_bounds__(512, 1)
           mma_commit(b_s);
           return true;
         };
-        // dP^T = V dO^T of step it, into the columns dQ of the step before was
-        // computed in: it waits until the dQ warps have read that dQ out
-        auto issue_dp = [&](int it) -> bool {
-          const int ds = it % C::NDO;
-          if (!mbar_wait(smem_u32(&ctl->do_full[ds]), (it / C::NDO) & 1, &ctl->abort)) return false;
-          if (it > 0 && !mbar_wait(b_dqf, (it - 1) & 1, &ctl->abort)) return false;
+        // dP^T = V dO^T of step g, into the columns dQ of the step before was
+        // computed in: it waits until the dQ warps have read that dQ out.  The
+        // item's last dP^T is the last reader of V.
+        auto issue_dp = [&](int g, int s, int n, int u) -> bool {
+          const int ds = g % C::NDO;
+          if (s == 0 && !mbar_wait(b_vf, u & 1, &ctl->abort)) return false;
+          if (!mbar_wait(smem_u32(&ctl->do_full[ds]), (g / C::NDO) & 1, &ctl->abort)) return false;
+          if (g > 0 && !mbar_wait(b_dqf, (g - 1) & 1, &ctl->abort)) return false;
           tc_fence_after();
           const uint64_t a0 = opaque(sdesc_sw128(v_base, 16, 1024)), b0 = opaque(sdesc_sw128(smem_u32(sDO(ds)), 16, 1024));
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk)
             mma_ss(tmem + C::T_DP, kmajor_step(a0, kk), kmajor_step(b0, kk), kIdKK, kk > 0);
           mma_commit(b_dp);
+          if (s == n - 1) mma_commit(b_ve);
           return true;
         };
-        bool ok = mbar_wait(b_kv, 0, &ctl->abort);
-        if (ok) {
-          tc_fence_after();
-          ok = issue_s(0) && issue_dp(0);
+        int g = 0, u = 0;
+        bool ok = true;
+        BwdItem cur;
+        for (int k = next_live(p, first, items, cur); ok && k < items; ++u) {
+          const int n = cur.n;
+          if (!issue_s(g, 0, u) || !issue_dp(g, 0, n, u)) {
+            ok = false;
+            break;
+          }
+          BwdItem nxt;
+          const int kn = next_live(p, k + (int)gridDim.x, items, nxt);
+          for (int s = 0; s < n; ++s, ++g) {
+            const int qs = g % C::NQ, ds = g % C::NDO;
+            const uint32_t q_base = smem_u32(sQ(qs)), do_base = smem_u32(sDO(ds));
+            if (!mbar_wait(b_pa, g & 1, &ctl->abort)) {
+              ok = false;
+              break;
+            }
+            // the dV / dK accumulators of the last item have been read out
+            if (s == 0 && u > 0 && !mbar_wait(b_accf, (u - 1) & 1, &ctl->abort)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            // dV += P^T dO; P^T of query columns [64 h, 64 h + 64) sits at TMEM columns [64 h, 64 h + 32).
+            // It runs while the key-row warps compute dS.
+            {
+              const uint64_t b0 = opaque(sdesc_sw128(do_base, 16384, 1024));
+#pragma unroll
+              for (int kk = 0; kk < 8; ++kk)
+                mma_ts(tmem + C::T_DV, tmem + C::T_S + (kk / 4) * 64 + (kk % 4) * 8, mnmajor_step(b0, kk), kIdKM,
+                       (s > 0 || kk > 0));
+            }
+            mma_commit(smem_u32(&ctl->do_empty[ds]));
+            if (kEarlyS && s + 1 < n && !issue_s(g + 1, s + 1, u)) {
+              ok = false;
+              break;
+            }
+            if (!mbar_wait(b_pb, g & 1, &ctl->abort)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            {  // dQ = dS K, over the dP^T columns the key-row warps have read
+              const uint64_t a0 = opaque(sdesc_sw128(ds_base, 16384, 1024)), b0 = opaque(sdesc_sw128(k_base, 16384, 1024));
+#pragma unroll
+              for (int kk = 0; kk < 8; ++kk) mma_ss(tmem + C::T_DP, mnmajor_step(a0, kk), mnmajor_step(b0, kk), kIdMM, kk > 0);
+            }
+            mma_commit(b_dq);
+            if (!kEarlyS && s + 1 < n && !issue_s(g + 1, s + 1, u)) {
+              ok = false;
+              break;
+            }
+            if (s + 1 == n) mma_commit(b_ke);  // K read for the last time in this item
+            {  // dK += dS^T Q
+              const uint64_t a0 = opaque(sdesc_sw128(ds_base, 16, 1024)), b0 = opaque(sdesc_sw128(q_base, 16384, 1024));
+#pragma unroll
+              for (int kk = 0; kk < 8; ++kk)
+                mma_ss(tmem + C::T_DK, kmajor_step(a0, kk), mnmajor_step(b0, kk), kIdKM, (s > 0 || kk > 0));
+            }
+            mma_commit(smem_u32(&ctl->q_empty[qs]));  // Q read for the last time
+            if (s + 1 < n && !issue_dp(g + 1, s + 1, n, u)) {
+              ok = false;
+              break;
+            }
+          }
+          if (!ok) break;
+          mma_commit(b_acc);  // dV, dK of the item complete
+          cur = nxt;
+          k = kn;
         }
-        for (int it = 0; ok && it < n; ++it) {
-          const int qs = it % C::NQ, ds = it % C::NDO;
-          const uint32_t q_base = smem_u32(sQ(qs)), do_base = smem_u32(sDO(ds));
-          if (!mbar_wait(b_pa, it & 1, &ctl->abort)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          // dV += P^T dO; P^T of query columns [64 h, 64 h + 64) sits at TMEM columns [64 h, 64 h + 32).
-          // It runs while the key-row warps compute dS.
-          {
-            const uint64_t b0 = opaque(sdesc_sw128(do_base, 16384, 1024));
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-              mma_ts(tmem + C::T_DV, tmem + C::T_S + (kk / 4) * 64 + (kk % 4) * 8, mnmajor_step(b0, kk), kIdKM,
-                     (it > 0 || kk > 0));
-          }
-          mma_commit(smem_u32(&ctl->do_empty[ds]));
-          if (!mbar_wait(b_pb, it & 1, &ctl->abort)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          {  // dQ = dS K, over the dP^T columns the key-row warps have read
-            const uint64_t a0 = opaque(sdesc_sw128(ds_base, 16384, 1024)), b0 = opaque(sdesc_sw128(k_base, 16384, 1024));
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) mma_ss(tmem + C::T_DP, mnmajor_step(a0, kk), mnmajor_step(b0, kk), kIdMM, kk > 0);
-          }
-          mma_commit(b_dq);
-          if (it + 1 < n && !issue_s(it + 1)) {
-            ok = false;
-            break;
-          }
-          {  // dK += dS^T Q
-            const uint64_t a0 = opaque(sdesc_sw128(ds_base, 16, 1024)), b0 = opaque(sdesc_sw128(q_base, 16384, 1024));
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-              mma_ss(tmem + C::T_DK, kmajor_step(a0, kk), mnmajor_step(b0, kk), kIdKM, (it > 0 || kk > 0));
-          }
-          mma_commit(smem_u32(&ctl->q_empty[qs]));  // Q read for the last time
-          if (it + 1 < n && !issue_dp(it + 1)) {
-            ok = false;
-            break;
-          }
-        }
-        if (ok)
-          mma_commit(b_acc);
-        else
-          fail(p, ctl);
+        if (!ok) fail(p, ctl);
         mma_commit(b_fin);
         mbar_wait(b_fin, 0, nullptr);
       }
@@ -375,55 +473,105 @@ __global__ void __launch_bounds__(512, 1)
     __syncwarp();
     teardown();
   } else if (warp >= C::DQ_WARP0) {
-    setmaxnreg_dec<104>();
+    setmaxnreg_dec<112>();
     // ------------------------------------------------------------ dQ warps
     // Warp w drains dQ rows [32 (w % 4), +32) (its TMEM lanes) of each step:
     // 32 columns at a time into one of its two 128-byte-swizzled 32 x 32 fp32
     // boxes, which lane 0 TMA bulk reduce-adds into the fp32 accumulator.  A
-    // box is rewritten only once the reduce issued from it two rounds before
-    // has read it.
-    const int rw = (warp % 4) * 32;  // first dQ row of this warp
-    const uint32_t tq = tmem + ((uint32_t)rw << 16) + C::T_DP;
+    // box is rewritten only once the bulk copy issued from it two rounds before
+    // has read it.  After an item's last step the same rows of dV and
+    // scale * dK leave TMEM through the same boxes (as 32 x 64 bf16) by TMA
+    // store (zeros for a key tile that no query tile sees).
+    const int rw = (warp % 4) * 32;  // first dQ / key row of this warp
+    const uint32_t t_lane = tmem + ((uint32_t)rw << 16);
+    const uint32_t tq = t_lane + C::T_DP;
     uint8_t* box0 = sSTG + (warp % 4) * (2 * C::BOX_BYTES);
-    int round = 0;
+    int round = 0, u = 0, g = 0;
     bool ok = true;
-    for (int it = 0; it < n; ++it) {
-      const int I = tile_of(it);
-      if (!warp_wait(b_dq, it & 1, &ctl->abort)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-#pragma unroll 1
-      for (int h2 = 0; h2 < D / 64; ++h2) {
-        float v[64];
-        tmem_ld64f(tq + 64 * h2, v);
-        if (h2 == D / 64 - 1) {
-          tc_fence_before();
-          mbar_arrive(b_dqf);  // TMEM columns free for the next dP^T
+    for (int k = first; ok && k < items; k += (int)gridDim.x) {
+      const BwdItem cur = bwd_item(p, k);
+      for (int s = 0; s < cur.n; ++s, ++g) {
+        const int I = tile_of(p, cur, s);
+        if (!warp_wait(b_dq, g & 1, &ctl->abort)) {
+          ok = false;
+          break;
         }
+        tc_fence_after();
+#pragma unroll 1
+        for (int h2 = 0; h2 < D / 64; ++h2) {
+          float v[64];
+          tmem_ld64f(tq + 64 * h2, v);
+          if (h2 == D / 64 - 1) {
+            tc_fence_before();
+            mbar_arrive(b_dqf);  // TMEM columns free for the next dP^T
+          }
 #pragma unroll
-        for (int bx = 0; bx < 2; ++bx, ++round) {
-          uint8_t* box = box0 + (round & 1) * C::BOX_BYTES;
-          if (lane == 0) bulk_wait_read1();  // the reduce from this box two rounds ago has read it
-          __syncwarp();
-          uint8_t* rowp = box + lane * 128;
+          for (int bx = 0; bx < 2; ++bx, ++round) {
+            uint8_t* box = box0 + (round & 1) * C::BOX_BYTES;
+            if (lane == 0) bulk_wait_read1();  // the copy from this box two rounds ago has read it
+            __syncwarp();
+            uint8_t* rowp = box + lane * 128;
 #pragma unroll
-          for (int q4 = 0; q4 < 8; ++q4)
-            *reinterpret_cast<float4*>(rowp + ((q4 ^ (lane & 7)) << 4)) =
-                make_float4(v[32 * bx + 4 * q4], v[32 * bx + 4 * q4 + 1], v[32 * bx + 4 * q4 + 2],
-                            v[32 * bx + 4 * q4 + 3]);
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            tma_reduce_add_3d(&tm_dq, smem_u32(box), 64 * h2 + 32 * bx, I * 128 + rw, bh);
-            bulk_commit();
+            for (int q4 = 0; q4 < 8; ++q4)
+              *reinterpret_cast<float4*>(rowp + ((q4 ^ (lane & 7)) << 4)) =
+                  make_float4(v[32 * bx + 4 * q4], v[32 * bx + 4 * q4 + 1], v[32 * bx + 4 * q4 + 2],
+                              v[32 * bx + 4 * q4 + 3]);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_reduce_add_3d(&tm_dq, smem_u32(box), 64 * h2 + 32 * bx, I * 128 + rw, cur.bh);
+              bulk_commit();
+            }
           }
         }
       }
+      if (!ok) break;
+      // dV, then scale * dK, 64 columns at a time; the accumulators are free for
+      // the next item once the last columns are read
+      const bool live = cur.n > 0;
+      if (live) {
+        if (!warp_wait(b_acc, u & 1, &ctl->abort)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+      }
+#pragma unroll 1
+      for (int c = 0; c < 2 * (D / 64); ++c, ++round) {
+        const bool is_k = c >= D / 64;
+        const int h2 = is_k ? c - D / 64 : c;
+        float a[64];
+        if (live) {
+          tmem_ld64f(t_lane + (is_k ? C::T_DK : C::T_DV) + 64 * h2, a);
+          if (c == 2 * (D / 64) - 1) {
+            tc_fence_before();
+            mbar_arrive(b_accf);
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < 64; ++e) a[e] = 0.f;
+        }
+        const float sc = is_k ? p.scale : 1.0f;
+        uint8_t* box = box0 + (round & 1) * C::BOX_BYTES;
+        if (lane == 0) bulk_wait_read1();
+        __syncwarp();
+        uint8_t* rowp = box + lane * 128;
+#pragma unroll
+        for (int q4 = 0; q4 < 8; ++q4)
+          *reinterpret_cast<uint4*>(rowp + ((q4 ^ (lane & 7)) << 4)) =
+              make_uint4(pack_bf16x2(a[8 * q4] * sc, a[8 * q4 + 1] * sc), pack_bf16x2(a[8 * q4 + 2] * sc, a[8 * q4 + 3] * sc),
+                         pack_bf16x2(a[8 * q4 + 4] * sc, a[8 * q4 + 5] * sc), pack_bf16x2(a[8 * q4 + 6] * sc, a[8 * q4 + 7] * sc));
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_3d(is_k ? &tm_dk : &tm_dv, smem_u32(box), 64 * h2, cur.J * 128 + rw, cur.bh);
+          bulk_commit();
+        }
+      }
+      if (live) ++u;
     }
     if (!ok) fail(p, ctl);
-    if (lane == 0) bulk_wait0();  // every reduce of this warp has completed
+    if (lane == 0) bulk_wait0();  // every reduce and store of this warp has completed
     __syncwarp();
     teardown();
   } else {
@@ -433,203 +581,193 @@ __global__ void __launch_bounds__(512, 1)
     // which it handles query columns [64 half, 64 half + 64) (half = w / 4).
     const int r = (warp % 4) * 32 + lane;
     const int half = warp / 4;
-    const int j = J * 128 + r;  // key row
     const uint32_t lane_off = (uint32_t)((warp % 4) * 32) << 16;
     const uint32_t tS = tmem + lane_off + C::T_S, tP = tmem + lane_off + C::T_DP;
-    // this key's visible query rows as two intervals, when they are; the
-    // document id and run of the key only where they are not, for the per-word
-    // evaluation of the program
-    const int4 seg = __ldg(p.row_segs + ((int64_t)bm * 2 + 1) * p.seg_len + min(j, p.kv_len - 1));
-    const int32_t* doc_row = p.mask.has_doc ? p.mask.doc + (int64_t)bm * p.mask.doc_len : nullptr;
-    int32_t doc_j = 0;
-    int run_lo = 0, run_hi = 0;  // with sorted ids: doc[i] == doc[j] exactly for i in [run_lo, run_hi)
-    bool use_run = false;
-    if (seg.x < 0 && doc_row != nullptr) {
-      doc_j = __ldg(doc_row + min(j, p.kv_len - 1));
-      use_run = doc_run(p.mask, bm, min(j, p.kv_len - 1), run_lo, run_hi);
-    }
     const uint64_t mask_ops = pack_ops(p.mask);
     const float sc_l2 = p.scale * kLog2e;
-    float cap_l2 = 0.f, sc_over_cap = 0.f, slope_l2 = 0.f;
+    float cap_l2 = 0.f, sc_over_cap = 0.f;
     if constexpr (SCORE == FA_S_SOFTCAP) {
       const float cap = __ldg(p.score_param);
       cap_l2 = cap * kLog2e;
       sc_over_cap = p.scale / cap;
     }
-    if constexpr (SCORE == FA_S_ALIBI) slope_l2 = __ldg(p.score_param + h) * kLog2e;
-    const bool row_ok = j < p.kv_len;
     // -LSE (log2 units) and -Delta of the query columns this half handles: one
-    // value per thread of the half, copied into shared memory once per step
+    // value per thread of the half, copied into shared memory once per step;
+    // the mask program's arguments (per mask batch), once per item
     const int st_idx = (r < 64) ? (64 * half + r) : (128 + 64 * half + r - 64);
-    auto stat_of = [&](int I) { return __ldg(stats_g + ((int64_t)bh * p.nq + I) * 256 + st_idx); };
-    int I_next = n > 0 ? tile_of(0) : 0;
-    if (n > 0) reinterpret_cast<float*>(&ctl->stats)[st_idx] = stat_of(I_next);
+    auto stat_of = [&](int bh, int I) { return __ldg(stats_g + ((int64_t)bh * p.nq + I) * 256 + st_idx); };
+    int32_t* arg_s = ctl->arg[half];
+    int k = first, I_next = 0;  // the query tile of the next step
+    {
+      BwdItem it0;
+      k = next_live(p, first, items, it0);
+      if (k < items) {
+        I_next = tile_of(p, it0, 0);
+        reinterpret_cast<float*>(&ctl->stats)[st_idx] = stat_of(it0.bh, I_next);
+        if (r < p.mask.n) arg_s[r] = node_arg(p.mask, r, it0.bm);
+      }
+    }
+    int g = 0;
     bool ok = true, lok = true;
-    for (int it = 0; it < n; ++it) {
-      // collective per half: this step's stats are in place, and every wait of
-      // the last step succeeded for all of the half (a failed wait is acted on
-      // here; until then the thread goes on with whatever TMEM holds, writing
-      // only TMEM and shared memory)
-      ok = named_bar_and(2 + half, 128, lok);
-      if (!ok) break;
-      const int I = I_next;
-      float st_next = 0.f;
-      if (it + 1 < n) {
-        I_next = tile_of(it + 1);
-        st_next = stat_of(I_next);
+    while (ok && k < items) {
+      const BwdItem cur = bwd_item(p, k);
+      // of the next item only what the last step hands over: its first query
+      // tile (for the stats), head and mask batch
+      int kn, nxt_i0 = 0, nxt_bh = 0, nxt_bm = 0;
+      {
+        BwdItem nxt;
+        kn = next_live(p, k + (int)gridDim.x, items, nxt);
+        if (kn < items) {
+          nxt_i0 = tile_of(p, nxt, 0);
+          nxt_bh = nxt.bh;
+          nxt_bm = nxt.bm;
+        }
       }
-      const bool partial = it >= n_full;
-      // visibility words of this thread's two 32-column chunks, built before S^T is waited for
-      uint32_t wm0 = row_ok ? 0xffffffffu : 0u, wm1 = wm0;
-      if (partial && row_ok && seg.x >= 0) {
-        wm0 = seg_word(seg, I * 128 + 64 * half);
-        wm1 = seg_word(seg, I * 128 + 64 * half + 32);
-      } else if (partial && row_ok) {
+      const int n = cur.n, bh = cur.bh;
+      const int j = cur.J * 128 + r;  // key row
+      // this key's visible query rows as two intervals, when they are; the
+      // document id and run of the key only where they are not, for the
+      // per-word evaluation of the program
+      const int4 seg = __ldg(p.row_segs + ((int64_t)cur.bm * 2 + 1) * p.seg_len + min(j, p.kv_len - 1));
+      const int32_t* doc_row = p.mask.has_doc ? p.mask.doc + (int64_t)cur.bm * p.mask.doc_len : nullptr;
+      int32_t doc_j = 0;
+      int run_lo = 0, run_hi = 0;  // with sorted ids: doc[i] == doc[j] exactly for i in [run_lo, run_hi)
+      bool use_run = false;
+      if (seg.x < 0 && doc_row != nullptr) {
+        doc_j = __ldg(doc_row + min(j, p.kv_len - 1));
+        use_run = doc_run(p.mask, cur.bm, min(j, p.kv_len - 1), run_lo, run_hi);
+      }
+      float slope_l2 = 0.f;
+      if constexpr (SCORE == FA_S_ALIBI) slope_l2 = __ldg(p.score_param + cur.h) * kLog2e;
+      const bool row_ok = j < p.kv_len;
+      for (int s = 0; s < n; ++s, ++g) {
+        // collective per half: this step's stats are in place, and every wait of
+        // the last step succeeded for all of the half (a failed wait is acted on
+        // here; until then the thread goes on with whatever TMEM holds, writing
+        // only TMEM and shared memory)
+        ok = named_bar_and(2 + half, 128, lok);
+        if (!ok) break;
+        const int I = I_next;
+        float st_next = 0.f;
+        if (s + 1 < n) {
+          I_next = tile_of(p, cur, s + 1);
+          st_next = stat_of(bh, I_next);
+        } else if (kn < items) {
+          I_next = nxt_i0;
+          st_next = stat_of(nxt_bh, nxt_i0);
+        }
+        const bool partial = s >= cur.n_full;
+        // visibility words of this thread's two 32-column chunks, built before S^T is waited for
+        uint32_t wm0 = row_ok ? 0xffffffffu : 0u, wm1 = wm0;
+        if (partial && row_ok && seg.x >= 0) {
+          wm0 = seg_word(seg, I * 128 + 64 * half);
+          wm1 = seg_word(seg, I * 128 + 64 * half + 32);
+        } else if (partial && row_ok) {
 #pragma unroll 1
-        for (int c2 = 0; c2 < 2; ++c2) {
-          const int i0 = I * 128 + 32 * (2 * half + c2);
-          auto eq = [&]() {
-            if (use_run) return range_bits(run_lo, run_hi, i0);
-            uint32_t bits = 0;
-            if (i0 + 32 <= p.q_len && p.mask.doc_vec_ok) {
-              const int4* dv = reinterpret_cast<const int4*>(doc_row + i0);
+          for (int c2 = 0; c2 < 2; ++c2) {
+            const int i0 = I * 128 + 32 * (2 * half + c2);
+            auto eq = [&]() {
+              if (use_run) return range_bits(run_lo, run_hi, i0);
+              uint32_t bits = 0;
+              if (i0 + 32 <= p.q_len && p.mask.doc_vec_ok) {
+                const int4* dv = reinterpret_cast<const int4*>(doc_row + i0);
 #pragma unroll
-              for (int q4 = 0; q4 < 8; ++q4) {
-                const int4 d = __ldg(dv + q4);
-                bits |= (uint32_t)(d.x == doc_j) << (4 * q4) | (uint32_t)(d.y == doc_j) << (4 * q4 + 1) |
-                        (uint32_t)(d.z == doc_j) << (4 * q4 + 2) | (uint32_t)(d.w == doc_j) << (4 * q4 + 3);
+                for (int q4 = 0; q4 < 8; ++q4) {
+                  const int4 d = __ldg(dv + q4);
+                  bits |= (uint32_t)(d.x == doc_j) << (4 * q4) | (uint32_t)(d.y == doc_j) << (4 * q4 + 1) |
+                          (uint32_t)(d.z == doc_j) << (4 * q4 + 2) | (uint32_t)(d.w == doc_j) << (4 * q4 + 3);
+                }
+              } else {
+                const int in = min(i0 + 32, p.q_len);
+                for (int i = i0; i < in; ++i) bits |= (uint32_t)(__ldg(doc_row + i) == doc_j) << (uint32_t)(i - i0);
               }
-            } else {
-              const int in = min(i0 + 32, p.q_len);
-              for (int i = i0; i < in; ++i) bits |= (uint32_t)(__ldg(doc_row + i) == doc_j) << (uint32_t)(i - i0);
-            }
-            return bits;
-          };
-          const uint32_t w = mask_word_t_rolled(p.mask.n, mask_ops, ctl->arg, j, i0, eq);
-          wm0 = (c2 == 0) ? w : wm0;
-          wm1 = (c2 == 1) ? w : wm1;
-        }
-      }
-      const float* nlse_s = ctl->stats.nlse;
-      const float* ndel_s = ctl->stats.ndelta;
-      // -- phase A: P = exp2(s - LSE) over this thread's 64 query columns; P^T
-      //    (bf16) over the S^T columns already read, for the dV MMA.  pg keeps
-      //    P times the score mod's derivative (P itself unless soft-capped).
-      lok = warp_wait(b_s, it & 1, &ctl->abort);
-      tc_fence_after();
-      float pg[64];
-#pragma unroll
-      for (int c2 = 0; c2 < 2; ++c2) {
-        const int c = 2 * half + c2;  // 32-column chunk of the 128 query columns
-        const int i0 = I * 128 + 32 * c;
-        const uint32_t w = (c2 == 0) ? wm0 : wm1;
-        float sv[32];
-        tmem_ld32f(tS + 32 * c, sv);
-        uint32_t pk[16];
-        const float4* nl4 = reinterpret_cast<const float4*>(nlse_s + 32 * c);
-#pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          const float4 nlq = nl4[e / 4];
-          const float2 nl = (e % 4 == 0) ? make_float2(nlq.x, nlq.y) : make_float2(nlq.z, nlq.w);
-          float2 a, g = make_float2(1.0f, 1.0f);
-          if constexpr (SCORE == FA_S_SOFTCAP) {
-            const float t0 = tanh_fast(sv[e] * sc_over_cap), t1 = tanh_fast(sv[e + 1] * sc_over_cap);
-            a = fma2(make_float2(cap_l2, cap_l2), make_float2(t0, t1), nl);
-            g = fma2(make_float2(-t0, -t1), make_float2(t0, t1), make_float2(1.0f, 1.0f));
-          } else if constexpr (SCORE == FA_S_ALIBI) {
-            a = fma2(make_float2(sv[e], sv[e + 1]), make_float2(sc_l2, sc_l2),
-                     make_float2(fmaf(-slope_l2, (float)(i0 + e - j), nl.x),
-                                 fmaf(-slope_l2, (float)(i0 + e + 1 - j), nl.y)));
-          } else {
-            a = fma2(make_float2(sv[e], sv[e + 1]), make_float2(sc_l2, sc_l2), nl);
+              return bits;
+            };
+            const uint32_t w = mask_word_t_rolled(p.mask.n, mask_ops, arg_s, j, i0, eq);
+            wm0 = (c2 == 0) ? w : wm0;
+            wm1 = (c2 == 1) ? w : wm1;
           }
-          float2 pv;
-          pv.x = ((w >> e) & 1u) ? ex2_approx(a.x) : 0.f;
-          pv.y = ((w >> (e + 1)) & 1u) ? ex2_approx(a.y) : 0.f;
-          pk[e / 2] = pack_bf16x2(pv.x, pv.y);
-          if constexpr (SCORE == FA_S_SOFTCAP) pv = mul2(pv, g);
-          pg[32 * c2 + e] = pv.x;
-          pg[32 * c2 + e + 1] = pv.y;
         }
-        tmem_st16(tS + 64 * half + 16 * c2, pk);
-      }
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(b_pa);
-      // -- phase B: dS = P (dP - Delta) [* d softcap], K-major into the dS buffer
-      //    (free: dP^T of this step was issued after dK of the step before)
-      lok = warp_wait(b_dp, it & 1, &ctl->abort) && lok;
-      tc_fence_after();
+        const float* nlse_s = ctl->stats.nlse;
+        const float* ndel_s = ctl->stats.ndelta;
+        // -- phase A: P = exp2(s - LSE) over this thread's 64 query columns; P^T
+        //    (bf16) over the S^T columns already read, for the dV MMA.  pg keeps
+        //    P times the score mod's derivative (P itself unless soft-capped).
+        lok = warp_wait(b_s, g & 1, &ctl->abort);
+        tc_fence_after();
+        float pg[64];
 #pragma unroll
-      for (int c2 = 0; c2 < 2; ++c2) {
-        const int c = 2 * half + c2;
-        float dp[32];
-        tmem_ld32f(tP + 32 * c, dp);
-        uint32_t dk[16];
-        const float4* nd4 = reinterpret_cast<const float4*>(ndel_s + 32 * c);
+        for (int c2 = 0; c2 < 2; ++c2) {
+          const int c = 2 * half + c2;  // 32-column chunk of the 128 query columns
+          const int i0 = I * 128 + 32 * c;
+          const uint32_t w = (c2 == 0) ? wm0 : wm1;
+          float sv[32];
+          tmem_ld32f(tS + 32 * c, sv);
+          uint32_t pk[16];
+          const float4* nl4 = reinterpret_cast<const float4*>(nlse_s + 32 * c);
 #pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          const float4 ndq = nd4[e / 4];
-          const float2 nd = (e % 4 == 0) ? make_float2(ndq.x, ndq.y) : make_float2(ndq.z, ndq.w);
-          const float2 dsv = mul2(make_float2(pg[32 * c2 + e], pg[32 * c2 + e + 1]),
-                                  add2(make_float2(dp[e], dp[e + 1]), nd));
-          dk[e / 2] = pack_bf16x2(dsv.x, dsv.y);
+          for (int e = 0; e < 32; e += 2) {
+            const float4 nlq = nl4[e / 4];
+            const float2 nl = (e % 4 == 0) ? make_float2(nlq.x, nlq.y) : make_float2(nlq.z, nlq.w);
+            float2 a, gd = make_float2(1.0f, 1.0f);
+            if constexpr (SCORE == FA_S_SOFTCAP) {
+              const float t0 = tanh_fast(sv[e] * sc_over_cap), t1 = tanh_fast(sv[e + 1] * sc_over_cap);
+              a = fma2(make_float2(cap_l2, cap_l2), make_float2(t0, t1), nl);
+              gd = fma2(make_float2(-t0, -t1), make_float2(t0, t1), make_float2(1.0f, 1.0f));
+            } else if constexpr (SCORE == FA_S_ALIBI) {
+              a = fma2(make_float2(sv[e], sv[e + 1]), make_float2(sc_l2, sc_l2),
+                       make_float2(fmaf(-slope_l2, (float)(i0 + e - j), nl.x),
+                                   fmaf(-slope_l2, (float)(i0 + e + 1 - j), nl.y)));
+            } else {
+              a = fma2(make_float2(sv[e], sv[e + 1]), make_float2(sc_l2, sc_l2), nl);
+            }
+            float2 pv;
+            pv.x = ((w >> e) & 1u) ? ex2_approx(a.x) : 0.f;
+            pv.y = ((w >> (e + 1)) & 1u) ? ex2_approx(a.y) : 0.f;
+            pk[e / 2] = pack_bf16x2(pv.x, pv.y);
+            if constexpr (SCORE == FA_S_SOFTCAP) pv = mul2(pv, gd);
+            pg[32 * c2 + e] = pv.x;
+            pg[32 * c2 + e + 1] = pv.y;
+          }
+          tmem_st16(tS + 64 * half + 16 * c2, pk);
         }
-        store_row32(sDS, r, c, dk);
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(b_pa);
+        // -- phase B: dS = P (dP - Delta) [* d softcap], K-major into the dS buffer
+        //    (free: dP^T of this step was issued after dK of the step before)
+        lok = warp_wait(b_dp, g & 1, &ctl->abort) && lok;
+        tc_fence_after();
+#pragma unroll
+        for (int c2 = 0; c2 < 2; ++c2) {
+          const int c = 2 * half + c2;
+          float dp[32];
+          tmem_ld32f(tP + 32 * c, dp);
+          uint32_t dk[16];
+          const float4* nd4 = reinterpret_cast<const float4*>(ndel_s + 32 * c);
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            const float4 ndq = nd4[e / 4];
+            const float2 nd = (e % 4 == 0) ? make_float2(ndq.x, ndq.y) : make_float2(ndq.z, ndq.w);
+            const float2 dsv = mul2(make_float2(pg[32 * c2 + e], pg[32 * c2 + e + 1]),
+                                    add2(make_float2(dp[e], dp[e + 1]), nd));
+            dk[e / 2] = pack_bf16x2(dsv.x, dsv.y);
+          }
+          store_row32(sDS, r, c, dk);
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(b_pb);
+        // every thread of this half is done with this step's stats (and the
+        // item's mask arguments): publish the next step's
+        named_bar_sync(2 + half, 128);
+        if (s + 1 < n || kn < items) reinterpret_cast<float*>(&ctl->stats)[st_idx] = st_next;
+        if (s + 1 == n && kn < items && r < p.mask.n) arg_s[r] = node_arg(p.mask, r, nxt_bm);
       }
-      fence_proxy_async_smem();
-      tc_fence_before();
-      mbar_arrive(b_pb);
-      // every thread of this half is done with this step's stats: publish the next step's
-      named_bar_sync(2 + half, 128);
-      if (it + 1 < n) reinterpret_cast<float*>(&ctl->stats)[st_idx] = st_next;
+      k = kn;
     }
     if (ok && !lok) ok = false;
     if (!ok) fail(p, ctl);
-    // ---- epilogue: dV and scale * dK from TMEM, once per key tile; each half writes D/2 columns
-    if (ok && n > 0) {
-      if (!warp_wait(b_acc, 0, &ctl->abort)) {
-        ok = false;
-        fail(p, ctl);
-      }
-      tc_fence_after();
-    }
-    // staging for dV / dK: the dS buffer and the first dO slot, whose last
-    // readers (the dQ / dK and dV MMAs) are done once acc_full completes
-    uint8_t* stage_v = sDS;
-    uint8_t* stage_k = sDO(0);
-    if (ok && !skip) {
-#pragma unroll 1
-      for (int c2 = 0; c2 < D / 64; ++c2) {
-        const int c = half * (D / 64) + c2;  // 32-column chunk of D
-        float a[32], g[32];
-        if (n > 0) {
-          tmem_ld32f(tmem + lane_off + C::T_DV + 32 * c, a);
-          tmem_ld32f(tmem + lane_off + C::T_DK + 32 * c, g);
-        } else {
-#pragma unroll
-          for (int e = 0; e < 32; ++e) a[e] = g[e] = 0.f;
-        }
-        uint32_t wv[16], wk[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          wv[e] = pack_bf16x2(a[2 * e], a[2 * e + 1]);
-          wk[e] = pack_bf16x2(g[2 * e] * p.scale, g[2 * e + 1] * p.scale);
-        }
-        store_row32(stage_v, r, c, wv);
-        store_row32(stage_k, r, c, wk);
-      }
-      fence_proxy_async_smem();
-    }
-    named_bar_sync(1, C::KEY_THREADS);
-    if (threadIdx.x == 0 && !skip && !*reinterpret_cast<volatile int*>(&ctl->abort)) {
-      for (int c = 0; c < C::NC; ++c) {
-        tma_store_3d(&tm_dv, smem_u32(stage_v + c * 16384), c * 64, J * 128, bh);
-        tma_store_3d(&tm_dk, smem_u32(stage_k + c * 16384), c * 64, J * 128, bh);
-      }
-      bulk_commit();
-      bulk_wait_read0();
-    }
     teardown();
   }
 }
@@ -698,13 +836,13 @@ cudaError_t launch_bwd_t(const AttnArgs& a, const BwdTensors& t, cudaStream_t st
       rows, a.q_len, a.nq);
 
   CUtensorMap mq, mk, mv, mdo, mdk, mdv;
-  auto enc = [&](CUtensorMap* m, const void* ptr, int64_t len) {
-    return encode_tmap_3d(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, ptr, D, len, bh, 64, 128,
+  auto enc = [&](CUtensorMap* m, const void* ptr, int64_t len, uint32_t rows) {
+    return encode_tmap_3d(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, ptr, D, len, bh, 64, rows,
                           CU_TENSOR_MAP_SWIZZLE_128B);
   };
   CUtensorMap mdq;
-  const bool ok = enc(&mq, t.q, a.q_len) && enc(&mk, t.k, a.kv_len) && enc(&mv, t.v, a.kv_len) &&
-                  enc(&mdo, t.dout, a.q_len) && enc(&mdk, t.dk, a.kv_len) && enc(&mdv, t.dv, a.kv_len) &&
+  const bool ok = enc(&mq, t.q, a.q_len, 128) && enc(&mk, t.k, a.kv_len, 128) && enc(&mv, t.v, a.kv_len, 128) &&
+                  enc(&mdo, t.dout, a.q_len, 128) && enc(&mdk, t.dk, a.kv_len, 32) && enc(&mdv, t.dv, a.kv_len, 32) &&
                   encode_tmap_3d(&mdq, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, t.dq_acc, D, a.q_len, bh, 32, 32,
                                  CU_TENSOR_MAP_SWIZZLE_128B);
   if (!ok) {
@@ -718,8 +856,17 @@ cudaError_t launch_bwd_t(const AttnArgs& a, const BwdTensors& t, cudaStream_t st
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
+  // persistent: one CTA per SM (or per item, when there are fewer)
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
   const int64_t items = (int64_t)a.B * a.H * a.nkv;
-  bwd_kernel<D, SCORE><<<(unsigned)items, BwdCfg<D>::THREADS, smem, stream>>>(mq, mk, mv, mdo, mdk, mdv, mdq, a, t.stats);
+  if (items >= ((int64_t)1 << 31)) return cudaErrorInvalidValue;
+  const unsigned grid = (unsigned)std::min<int64_t>(items, sms);
+  if (grid > 0)
+    bwd_kernel<D, SCORE><<<grid, BwdCfg<D>::THREADS, smem, stream>>>(
+        mq, mk, mv, mdo, mdk, mdv, mdq, a, t.stats);
   const int64_t n8 = rows * D / 8;
   bwd_dq_convert_kernel<<<(unsigned)((n8 + 255) / 256), 256, 0, stream>>>(
       t.dq_acc, static_cast<__nv_bfloat16*>(t.dq), n8, a.scale);
