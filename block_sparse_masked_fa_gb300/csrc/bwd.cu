@@ -115,25 +115,6 @@ __device__ __forceinline__ float tanh_fast(float t) {
   return fmaf(-2.0f, r, 1.0f);
 }
 
-// Shared-memory descriptor of MMA step kk (16 elements of the contraction) from
-// the descriptor of step 0.  K-major: a 128-row tile stored as 64-column
-// chunks of 16 KB, step kk at chunk kk / 4, byte 32 (kk % 4) of the row.
-// MN-major: step kk starts 2048 bytes (16 rows of 128 bytes) further.  The
-// start-address field counts 16-byte units and never carries for addresses
-// inside the 227 KB of shared memory.
-__device__ __forceinline__ uint64_t kmajor_step(uint64_t desc, int kk) {
-  return desc + (uint64_t)((kk >> 2) * (16384 >> 4) + (kk & 3) * (32 >> 4));
-}
-__device__ __forceinline__ uint64_t mnmajor_step(uint64_t desc, int kk) { return desc + (uint64_t)(kk * (2048 >> 4)); }
-// A value the compiler cannot move out of the loop it is computed in: the MMA
-// issue loops are unrolled, and holding every step's descriptor of every GEMM
-// in registers across the work loop would not fit the MMA warp's budget.
-__device__ __forceinline__ uint64_t opaque(uint64_t x) {
-  uint64_t r;
-  asm volatile("mov.b64 %0, %1;" : "=l"(r) : "l"(x));
-  return r;
-}
-
 // Writes 32 bf16 values (16 packed words) of row r into a 128-byte-swizzled
 // [chunks][128 rows][64] tile at columns [32 c, 32 c + 32).
 __device__ __forceinline__ void store_row32(uint8_t* tile, int r, int c, const uint32_t (&w)[16]) {

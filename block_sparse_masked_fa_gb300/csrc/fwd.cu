@@ -301,11 +301,9 @@ __global__ void __launch_bounds__(192, 2)
           }
           tc_fence_after();
           const uint32_t k_base = smem_u32(sKV + sk * C::TILE);
+          const uint64_t a0 = opaque(sdesc_sw128(q_base, 16, 1024)), b0 = opaque(sdesc_sw128(k_base, 16, 1024));
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;
-            mma_ss(tmem, sdesc_sw128(q_base + off, 16, 1024), sdesc_sw128(k_base + off, 16, 1024), kIdS, kk > 0);
-          }
+          for (int kk = 0; kk < D / 16; ++kk) mma_ss(tmem, kmajor_step(a0, kk), kmajor_step(b0, kk), kIdS, kk > 0);
           mma_commit(smem_u32(&ctl->kv_empty[sk]));
           if (jj == n - 1) mma_commit(b_qe);  // Q read for the last time in this item
           mma_commit(b_s);
@@ -327,9 +325,9 @@ __global__ void __launch_bounds__(192, 2)
           }
           tc_fence_after();
           const uint32_t v_base = smem_u32(sKV + sv * C::TILE);
+          const uint64_t v0 = opaque(sdesc_sw128(v_base, 16384, 1024));
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            mma_ts(tmem + 128, tmem + kk * 8, sdesc_sw128(v_base + kk * 2048, 16384, 1024), kIdO, (jj > 0 || kk > 0));
+          for (int kk = 0; kk < 8; ++kk) mma_ts(tmem + 128, tmem + kk * 8, mnmajor_step(v0, kk), kIdO, (jj > 0 || kk > 0));
           mma_commit(smem_u32(&ctl->kv_empty[sv]));
         }
         if (!ok) break;

@@ -201,6 +201,25 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_byt
 #define FA_R8(i) "=r"(r[i]), "=r"(r[i + 1]), "=r"(r[i + 2]), "=r"(r[i + 3]), "=r"(r[i + 4]), "=r"(r[i + 5]), \
                  "=r"(r[i + 6]), "=r"(r[i + 7])
 // Loads 32 consecutive columns of this thread's lane, and waits for them.
+// Shared-memory descriptor of MMA step kk (16 elements of the contraction) from
+// the descriptor of step 0.  K-major: a 128-row tile stored as 64-column
+// chunks of 16 KB, step kk at chunk kk / 4, byte 32 (kk % 4) of the row.
+// MN-major: step kk starts 2048 bytes (16 rows of 128 bytes) further.  The
+// start-address field counts 16-byte units and never carries for addresses
+// inside the 227 KB of shared memory.
+__device__ __forceinline__ uint64_t kmajor_step(uint64_t desc, int kk) {
+  return desc + (uint64_t)((kk >> 2) * (16384 >> 4) + (kk & 3) * (32 >> 4));
+}
+__device__ __forceinline__ uint64_t mnmajor_step(uint64_t desc, int kk) { return desc + (uint64_t)(kk * (2048 >> 4)); }
+// A value the compiler cannot rebuild or hoist inside the unrolled MMA issue
+// loops: each step's descriptor is then one 64-bit add from it, and holding
+// every step's descriptor in registers is avoided.
+__device__ __forceinline__ uint64_t opaque(uint64_t x) {
+  uint64_t r;
+  asm volatile("mov.b64 %0, %1;" : "=l"(r) : "l"(x));
+  return r;
+}
+
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
