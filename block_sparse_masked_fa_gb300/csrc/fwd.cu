@@ -62,7 +62,7 @@ struct FwdCtl {
   uint64_t kv_full[4];
   uint64_t kv_empty[4];
   uint64_t s_full;
-  uint64_t p_full;
+  uint64_t p_half, p_full;  // P of the first 64 keys, of all 128 keys
   uint64_t o_full, o_free;
   uint64_t stg_free;
   uint64_t fin;
@@ -157,7 +157,8 @@ __global__ void __launch_bounds__(192, 2)
   const int items = p.B * p.H * p.nq;  // below 2^31: checked at launch
 
   const uint32_t b_q = smem_u32(&ctl->q_full), b_qe = smem_u32(&ctl->q_empty), b_s = smem_u32(&ctl->s_full),
-                 b_p = smem_u32(&ctl->p_full), b_o = smem_u32(&ctl->o_full), b_of = smem_u32(&ctl->o_free),
+                 b_p = smem_u32(&ctl->p_full), b_ph = smem_u32(&ctl->p_half), b_o = smem_u32(&ctl->o_full),
+                 b_of = smem_u32(&ctl->o_free),
                  b_stg = smem_u32(&ctl->stg_free), b_fin = smem_u32(&ctl->fin);
   if (threadIdx.x == 0) {
     mbar_init(b_q, 1);
@@ -168,6 +169,7 @@ __global__ void __launch_bounds__(192, 2)
     }
     mbar_init(b_s, 1);
     mbar_init(b_p, 128);
+    mbar_init(b_ph, 128);
     mbar_init(b_o, 1);
     mbar_init(b_of, 128);
     mbar_init(b_stg, 1);
@@ -309,7 +311,9 @@ __global__ void __launch_bounds__(192, 2)
           mma_commit(b_s);
           // the next item, looked up while the softmax runs
           if (jj == 0) kn = next_live(p, k + (int)gridDim.x, items, nxt);
-          if (!mbar_wait(b_p, t & 1, &ctl->abort)) {
+          // P V in two halves: keys [0, 64) as soon as their P is in TMEM, while
+          // the softmax warps compute the rest
+          if (!mbar_wait(b_ph, t & 1, &ctl->abort)) {
             ok = false;
             break;
           }
@@ -327,7 +331,14 @@ __global__ void __launch_bounds__(192, 2)
           const uint32_t v_base = smem_u32(sKV + sv * C::TILE);
           const uint64_t v0 = opaque(sdesc_sw128(v_base, 16384, 1024));
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) mma_ts(tmem + 128, tmem + kk * 8, mnmajor_step(v0, kk), kIdO, (jj > 0 || kk > 0));
+          for (int kk = 0; kk < 4; ++kk) mma_ts(tmem + 128, tmem + kk * 8, mnmajor_step(v0, kk), kIdO, (jj > 0 || kk > 0));
+          if (!mbar_wait(b_p, t & 1, &ctl->abort)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 4; kk < 8; ++kk) mma_ts(tmem + 128, tmem + kk * 8, mnmajor_step(v0, kk), kIdO, true);
           mma_commit(smem_u32(&ctl->kv_empty[sv]));
         }
         if (!ok) break;
@@ -554,19 +565,26 @@ __global__ void __launch_bounds__(192, 2)
               pk[e2 + 1] = pack_bf16x2(p23.x, p23.y);
             }
             tmem_st16(tS + 16 * c, pk);
+            if (c == 1) {
+              // P of the first 64 keys is in: P V over them may start, once O has
+              // been rescaled (the last P V is done: S of this step came after it)
+              if (rescale) {
+  #pragma unroll 1
+                for (int c3 = 0; c3 < D / 32; ++c3) {
+                  float o[32];
+                  tmem_ld32f(tO + 32 * c3, o);
+  #pragma unroll
+                  for (int e = 0; e < 32; ++e) o[e] *= alpha;
+                  tmem_st32f(tO + 32 * c3, o);
+                }
+              }
+              tmem_st_wait();
+              tc_fence_before();
+              mbar_arrive(b_ph);
+            }
           }
           const float2 cs = add2(c01, c23);
           l += cs.x + cs.y;
-        }
-        if (rescale) {
-  #pragma unroll 1
-          for (int c = 0; c < D / 32; ++c) {
-            float o[32];
-            tmem_ld32f(tO + 32 * c, o);
-  #pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] *= alpha;
-            tmem_st32f(tO + 32 * c, o);
-          }
         }
         tmem_st_wait();
         tc_fence_before();
