@@ -175,3 +175,26 @@ def test_rows_of_three_intervals():
         got = run_fa(inp, mask)
         for h in range(2):
             check_all([g[0, h] for g in got], oracle_grads(inp, mask, 0, h, ("none",)), f"{len(mask.nodes)} nodes h{h}")
+
+
+def test_many_items_per_cta_with_per_batch_masks():
+    """More key tiles than resident CTAs, so every CTA walks several items: the
+    mask arguments change between items (one prefix length and document layout
+    per batch row), and many key tiles see no query at all."""
+    B, H, S = 4, 2, 4096
+    docs = make_doc_ids(("geometric", 300.0), S, 51, batch=B)
+    inp = _inputs(B, H, S, 128, 52, docs=docs)
+    prefix = np.array([0, 200, 700, 1500], dtype=np.int32)
+    mask = P(("same_doc",), ("sink", 64), ("prefix",), ("or",), ("and",))
+    got = run_fa(inp, mask, Bm=B, prefix=prefix)
+    assert B * H * (S // 128) > torch.cuda.get_device_properties(0).multi_processor_count
+    rng = np.random.default_rng(53)
+    for b in range(B):
+        h = b % H
+        rows, cols = _sample(S, rng), _sample(S, rng)
+        ref = oracle_grads(inp, mask, b, h, ("none",), Bm=B, prefix=prefix, rows=rows, cols=cols)
+        dq, dk, dv = (g[b, h] for g in got)
+        check_all((dq[rows], dk[cols], dv[cols]), ref, f"b{b} h{h}")
+        # keys past the sink and the prefix are seen by no query: zero gradients
+        hidden = np.arange(S) >= max(64, int(prefix[b]))
+        assert not dk[hidden].any() and not dv[hidden].any()

@@ -220,3 +220,26 @@ def test_rows_of_three_intervals():
         for h in range(2):
             ref_out, ref_lse = oracle_rows(inp, mask, 0, h, None, ("none",))
             check_forward(out[0, h], lse[0, h], ref_out, ref_lse, f"{len(mask.nodes)} nodes h{h}")
+
+
+def test_many_items_per_cta_with_per_batch_masks():
+    """More query tiles than resident CTAs, so every CTA walks several items:
+    the mask arguments change between items (one prefix length and document
+    layout per batch row), and many tiles see no key at all (same_doc & (sink |
+    prefix) hides every document that starts after the sink and the prefix)."""
+    B, H, S = 4, 4, 4096
+    docs = make_doc_ids(("geometric", 300.0), S, 41, batch=B)
+    inp = _inputs(B, H, S, 64, 42, docs=docs)
+    prefix = np.array([0, 200, 700, 1500], dtype=np.int32)
+    mask = P(("same_doc",), ("sink", 64), ("prefix",), ("or",), ("and",))
+    out, lse, bm = run_fa(inp, mask, Bm=B, prefix=prefix)
+    lists = bm.lists()
+    visible = (lists["kv_num_blocks"].long() + lists["full_kv_num_blocks"].long()).cpu().numpy()
+    assert (visible == 0).any() and (visible > 0).any()
+    assert B * H * (S // 128) > 2 * torch.cuda.get_device_properties(0).multi_processor_count
+    rng = np.random.default_rng(43)
+    rows = np.unique(np.concatenate([rng.choice(S, 80, replace=False), [0, 63, 64, S - 1]])).astype(np.int64)
+    for b in range(B):
+        for h in (0, H - 1):
+            ref_out, ref_lse = oracle_rows(inp, mask, b, h, rows, ("none",), Bm=B, prefix=prefix)
+            check_forward(out[b, h][rows], lse[b, h][rows], ref_out, ref_lse, f"b{b} h{h}")
