@@ -131,6 +131,48 @@ def workload_tensors(w, seed=None):
     return q, k, v, do, docs
 
 
+def mask_nodes(w, docs, W):
+    """The binding's node list of the workload's mask program (docs / W on the device)."""
+    nodes = []
+    for node in w.mask.nodes:
+        if node[0] == "same_doc":
+            nodes.append(("same_doc", docs))
+        elif node[0] == "window":
+            nodes.append(("window", W if w.windows else int(node[1])))
+        elif node[0] == "sink":
+            nodes.append(("sink", int(node[1])))
+        else:
+            nodes.append((node[0],))
+    return nodes
+
+
+def builder_scaled(fa, w, W, dev, S=262144, reps=10):
+    """fa_create_block_mask alone at a scaled length (the workload's mask program,
+    documents drawn for S tokens): its time and achieved bandwidth over the
+    algorithmic bytes -- doc ids read, four count vectors and four padded tile
+    lists written."""
+    import torch
+
+    docs = None
+    if w.docs is not None:
+        docs = torch.as_tensor(make_doc_ids(w.docs, S, w.doc_seed or w.seed), dtype=torch.int32, device=dev)
+    spec = fa.make_mask_spec(mask_nodes(w, docs, W), device=dev)
+    buf = torch.empty(fa.fa_block_mask_bytes(1, 1, S, S, 128), dtype=torch.uint8, device=dev)
+    for _ in range(3):
+        fa.fa_create_block_mask(spec, 1, 1, S, S, 128, buffer=buf)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        fa.fa_create_block_mask(spec, 1, 1, S, S, 128, buffer=buf)
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / reps
+    nt = S // 128
+    nbytes = (S * 4 if docs is not None else 0) + 4 * nt * 4 + 4 * nt * nt * 4
+    return {"S": S, "ms": round(ms, 4), "algorithmic_bytes": int(nbytes), "GB_s": round(nbytes / (ms * 1e-3) / 1e9, 1)}
+
+
 def visible_tiles(fa, bm, B, H):
     """Sum over (b, h) of non-empty tiles, from the block mask's counts."""
     L = bm.lists()
@@ -158,16 +200,7 @@ def run_gpu(args):
     q, k, v, do = (t.to(dev) for t in (q_h, k_h, v_h, do_h))
     docs = torch.as_tensor(docs_np, dtype=torch.int32, device=dev) if docs_np is not None else None
     W = torch.tensor([args.window if w.windows else 1024], dtype=torch.int32, device=dev)
-    nodes = []
-    for node in w.mask.nodes:
-        if node[0] == "same_doc":
-            nodes.append(("same_doc", docs))
-        elif node[0] == "window":
-            nodes.append(("window", W if w.windows else int(node[1])))
-        elif node[0] == "sink":
-            nodes.append(("sink", int(node[1])))
-        else:
-            nodes.append((node[0],))
+    nodes = mask_nodes(w, docs, W)
     spec, keep = fa.make_mask_spec(nodes, device=dev)
     score = None
     if w.score[0] == "softcap":
@@ -356,6 +389,8 @@ def run_gpu(args):
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,
     }
+    if rank == 0:
+        res["builder_scaled"] = builder_scaled(fa, w, W, dev)
     if rank == 0 and not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline(w, args.cpu_sample_tokens)
     if world > 1:
