@@ -28,6 +28,7 @@
 //                     which the attention kernels' PARTIAL tiles read instead
 //                     of running the program per word.
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace fa {
 namespace {
@@ -90,6 +91,7 @@ __device__ int program_interval(const DevMask& m, const int32_t* arg, int64_t i0
 }
 
 __global__ void tile_summary_kernel(const __grid_constant__ BuildArgs a) {
+  pdl_wait_then_release();
   const int warps = blockDim.x / 32;
   const int64_t w = (int64_t)blockIdx.x * warps + threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
@@ -138,6 +140,7 @@ __global__ void tile_summary_kernel(const __grid_constant__ BuildArgs a) {
 // doc[y] == doc[x] exactly for y in [lo, hi), and lo / hi are the lower /
 // upper bound of doc[x] in the row, found by binary search.
 __global__ void __launch_bounds__(256) doc_runs_kernel(const __grid_constant__ BuildArgs a) {
+  pdl_wait_then_release();
   const int L = (int)max(a.q_len, a.kv_len);
   const int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (gid >= (int64_t)a.Bm * L) return;
@@ -290,6 +293,7 @@ __device__ RowSegs row_segments(int nn, uint64_t ops, const int32_t* arg, bool t
 // of every key column over the query rows ([bm][1][x]), for x < L =
 // max(q_len, kv_len); lo0 = -1 where two intervals do not describe the row.
 __global__ void __launch_bounds__(256) row_segs_kernel(const __grid_constant__ BuildArgs a) {
+  pdl_wait_then_release();
   const int64_t L = max(a.q_len, a.kv_len);
   const int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (gid >= (int64_t)a.Bm * 2 * L) return;
@@ -311,6 +315,7 @@ constexpr int kBuildWarps = 8;
 // one tile; undecided tiles are settled exactly by the whole warp.  Writes
 // the class bytes only; compaction into lists is a separate pass.
 __global__ void __launch_bounds__(kBuildWarps * 32) classify_kernel(const __grid_constant__ BuildArgs a) {
+  pdl_wait_then_release();
   __shared__ int32_t s_arg[kBuildWarps][FA_MAX_MASK_NODES];
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int nchunk = (a.nkv + 31) / 32;
@@ -406,6 +411,7 @@ __global__ void __launch_bounds__(kBuildWarps * 32) classify_kernel(const __grid
 // Compaction: warps [0, rows) build the per-row lists, the next [0, cols)
 // warps the per-column lists, both with ballots over the class bytes.
 __global__ void __launch_bounds__(kBuildWarps * 32) compact_kernel(const __grid_constant__ BuildArgs a) {
+  pdl_wait_then_release();
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int64_t wid = (int64_t)blockIdx.x * kBuildWarps + warp;
   const int64_t rows = (int64_t)a.Bm * a.Hm * a.nq, cols = (int64_t)a.Bm * a.Hm * a.nkv;
@@ -450,6 +456,7 @@ __global__ void __launch_bounds__(kBuildWarps * 32) compact_kernel(const __grid_
 constexpr int kOrderBuckets = 4096;
 
 __global__ void __launch_bounds__(1024) order_kernel(const __grid_constant__ BuildArgs a) {
+  pdl_wait_then_release();
   extern __shared__ int32_t hist[];  // kOrderBuckets entries
   __shared__ int s_cmax;
   const bool rows = blockIdx.x == 0;
@@ -518,23 +525,30 @@ __global__ void __launch_bounds__(1024) order_kernel(const __grid_constant__ Bui
 
 cudaError_t launch_build(const BuildArgs& a, cudaStream_t stream) {
   const int tmax = a.nq > a.nkv ? a.nq : a.nkv;
+  cudaError_t e = cudaSuccess;
   if (a.mask.has_doc) {
     const int64_t warps = (int64_t)a.Bm * 2 * tmax;
-    tile_summary_kernel<<<(unsigned)((warps + 7) / 8), 256, 0, stream>>>(a);
+    e = launch_k(tile_summary_kernel, dim3((unsigned)((warps + 7) / 8)), dim3(256), 0, stream, a);
+    if (e != cudaSuccess) return e;
     const int64_t L = a.q_len > a.kv_len ? a.q_len : a.kv_len;
-    doc_runs_kernel<<<(unsigned)((a.Bm * L + 255) / 256), 256, 0, stream>>>(a);
+    e = launch_k(doc_runs_kernel, dim3((unsigned)((a.Bm * L + 255) / 256)), dim3(256), 0, stream, a);
+    if (e != cudaSuccess) return e;
   }
   {
     const int64_t L = a.q_len > a.kv_len ? a.q_len : a.kv_len;
-    row_segs_kernel<<<(unsigned)((a.Bm * 2 * L + 255) / 256), 256, 0, stream>>>(a);
+    e = launch_k(row_segs_kernel, dim3((unsigned)((a.Bm * 2 * L + 255) / 256)), dim3(256), 0, stream, a);
+    if (e != cudaSuccess) return e;
   }
   const int64_t rows = (int64_t)a.Bm * a.Hm * a.nq;
   const int64_t cols = (int64_t)a.Bm * a.Hm * a.nkv;
   const int64_t cwarps = rows * ((a.nkv + 31) / 32);
-  classify_kernel<<<(unsigned)((cwarps + kBuildWarps - 1) / kBuildWarps), kBuildWarps * 32, 0, stream>>>(a);
-  compact_kernel<<<(unsigned)((rows + cols + kBuildWarps - 1) / kBuildWarps), kBuildWarps * 32, 0, stream>>>(a);
-  order_kernel<<<2, 1024, kOrderBuckets * sizeof(int32_t), stream>>>(a);
-  return cudaGetLastError();
+  e = launch_k(classify_kernel, dim3((unsigned)((cwarps + kBuildWarps - 1) / kBuildWarps)), dim3(kBuildWarps * 32), 0,
+               stream, a);
+  if (e != cudaSuccess) return e;
+  e = launch_k(compact_kernel, dim3((unsigned)((rows + cols + kBuildWarps - 1) / kBuildWarps)), dim3(kBuildWarps * 32),
+               0, stream, a);
+  if (e != cudaSuccess) return e;
+  return launch_k(order_kernel, dim3(2), dim3(1024), kOrderBuckets * sizeof(int32_t), stream, a);
 }
 
 }  // namespace fa

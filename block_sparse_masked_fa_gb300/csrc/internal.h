@@ -21,6 +21,27 @@ struct BuildArgs {
   uint32_t* status;
 };
 
+// Launches a kernel on `stream` allowed to start while the kernel before it
+// drains (programmatic stream serialization); the kernel itself waits for that
+// one to complete before touching memory (pdl_wait_then_release).  Used for the
+// builder's chain of short kernels; the attention kernels, which fill every SM,
+// measured slower launched this way and are launched plainly.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                     Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
+
 cudaError_t launch_build(const BuildArgs& a, cudaStream_t stream);
 
 // Work description shared by the forward and backward kernels.

@@ -23,6 +23,16 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 }
 
 // ------------------------------------------------------------------ mbarrier
+// Programmatic dependent launch: wait until the grid this one was queued behind
+// has completed and its memory is visible (a no-op when there is none), then
+// let the grid queued behind this one start launching.  The block-mask
+// builder's kernels do this before they touch global memory, so the order of
+// their memory accesses is that of the stream; only launch latency overlaps.
+__device__ __forceinline__ void pdl_wait_then_release() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
 }
