@@ -10,7 +10,7 @@ import pytest
 import torch
 
 import oracle
-from fa_testutil import (check_grad, device_nodes, head64, oracle_program, oracle_score, score_arg)
+from fa_testutil import (check_forward, check_grad, device_nodes, head64, oracle_program, oracle_score, score_arg)
 from synth import WORKLOADS, MaskProgram, make_alibi_slopes, make_doc_ids, make_qkv, make_workload_inputs
 
 pytestmark = pytest.mark.gpu
@@ -198,3 +198,29 @@ def test_many_items_per_cta_with_per_batch_masks():
         # keys past the sink and the prefix are seen by no query: zero gradients
         hidden = np.arange(S) >= max(64, int(prefix[b]))
         assert not dk[hidden].any() and not dv[hidden].any()
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("score", ["none", "softcap", "alibi"])
+def test_every_kernel_instantiation(D, score):
+    """Each (head dim, score mod) kernel pair, forward and backward, on every
+    element of a ragged size with partial and full tiles."""
+    S, H = 700, 2
+    inp = _inputs(1, H, S, D, 60 + D + len(score))
+    mask = P(("causal",), ("window", 300), ("and",), ("sink", 8), ("or",), ("causal",), ("and",))
+    sl = make_alibi_slopes(H)
+    dev_score = {"none": None, "softcap": ("softcap", [25.0]), "alibi": ("alibi", torch.as_tensor(sl))}[score]
+    ref_score = {"none": ("none",), "softcap": ("softcap", 25.0), "alibi": ("alibi", sl)}[score]
+    q, k, v, do = (inp[n].cuda() for n in ("q", "k", "v", "do"))
+    bm = fa.fa_create_block_mask(device_nodes(mask), 1, 1, S, S, 128)
+    out, lse = fa.fa_forward(q, k, v, bm, score=dev_score)
+    dq, dk, dv = fa.fa_backward(q, k, v, out, lse, do, bm, score=dev_score)
+    torch.cuda.synchronize()
+    assert fa.fa_get_status(bm) == 0
+    for h in range(H):
+        prog = oracle_program(mask, None, None, 0, 1)
+        args = (head64(inp["q"], 0, h), head64(inp["k"], 0, h), head64(inp["v"], 0, h))
+        ref_out, ref_lse = oracle.forward_head(*args, prog, ref_score, h, 1.0 / np.sqrt(D))
+        check_forward(out[0, h].float().cpu().numpy(), lse[0, h].cpu().numpy(), ref_out, ref_lse, f"D{D} {score} h{h}")
+        ref = oracle_grads(inp, mask, 0, h, ref_score)
+        check_all([g[0, h].float().cpu().numpy() for g in (dq, dk, dv)], ref, f"D{D} {score} h{h}")
