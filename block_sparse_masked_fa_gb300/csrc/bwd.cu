@@ -25,16 +25,16 @@
 //                    staged the same way and TMA-stored
 //       warp 12      TMA producer: V_J, then Q_I, dO_I per step, K_J with the first
 //       warp 13      MMA issuer, five tcgen05 GEMMs per (I, J):
-//                     once P^T is in:  dV  += P^T dO   (P^T bf16 read from TMEM [0,64))
+//                     once P^T is in:  dV  += P^T dO   (P^T bf16 read from TMEM [0,32), [64,96))
 //                     once dS is in:   dQ   = dS K     (dS read MN-major; TMEM [128,128+D))
 //                                      S^T  = K Q^T    (next step; TMEM [0,128))
 //                                      dK  += dS^T Q   (dS read K-major)
 //                                      dP^T = V dO^T   (next step; TMEM [128,256), once dQ is read out)
 //     dV runs while the key-row warps compute dS, and the next S^T before dK
 //     (with D = 64, right after dV) so that phase A of the next step can start
-//     early.  Registers are split
-//     per warpgroup (setmaxnreg) so that the key-row warps hold a row's 64
-//     probabilities across the two phases.
+//     early.  Registers are split per warpgroup (setmaxnreg): the dQ and
+//     producer / MMA warpgroups give theirs up to the key-row warps, which hold
+//     a row's 64 probabilities across the two phases.
 //     dK and dV stay in TMEM for the whole key tile and are written once
 //     (no atomics); dQ partial tiles are added into the fp32 accumulator.
 //     Across key tiles the pipeline keeps going: the next tile's V loads once

@@ -13,13 +13,14 @@
 // other's matrix multiplies.  Warp roles:
 //   warps 0-3  softmax + epilogue: thread r owns query row r (TMEM lane r)
 //   warp 4     TMA producer (item descriptors, Q per item, K_j / V_j through a
-//              ring of slots, the output by TMA store) and TMEM allocator
+//              ring of slots) and TMEM allocator
 //   warp 5     MMA issuer (one thread): S = Q K_j^T into TMEM, then
-//              O += P V_j with P read from TMEM
+//              O += P V_j with P read from TMEM, in two halves: keys [0, 64)
+//              as soon as the softmax warps have written their P
 // Across items the pipeline keeps going: the next item's Q loads once the last
 // S has read the buffer, its first S runs while the epilogue reads O out of
 // TMEM, and the output is staged in shared memory (the last V slot with two
-// slots) and stored by TMA without waiting.
+// slots) and stored by TMA (thread 0) without waiting.
 // TMEM (256 columns): S at [0, 128) -- P (bf16 pairs) overwrites its first 64
 // columns after the softmax has read S -- and O at [128, 128 + D).
 // The running maximum is only moved (and O rescaled) when a new row maximum
