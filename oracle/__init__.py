@@ -48,7 +48,8 @@ def build(force: bool = False) -> str:
 
 class _Program(ctypes.Structure):
     _fields_ = [("n", ctypes.c_int32), ("op", ctypes.c_int32 * 16), ("arg", ctypes.c_int64 * 16),
-                ("doc", ctypes.POINTER(ctypes.c_int32))]
+                ("doc", ctypes.POINTER(ctypes.c_int32)), ("sel", ctypes.POINTER(ctypes.c_int8)),
+                ("sel_block", ctypes.c_int64), ("sel_nkv", ctypes.c_int64)]
 
 
 def _load():
@@ -76,9 +77,16 @@ def _load():
 
 
 class Program:
-    """A mask program resolved for one batch row (doc ids and prefix length bound)."""
+    """A mask program resolved for one batch row (doc ids and prefix length bound).
 
-    def __init__(self, mask, doc_row: Optional[np.ndarray] = None, prefix_len: Optional[int] = None):
+    ``selection`` (optional, int8 [nq, nkv], see ``selection_from_lists``)
+    restricts it to caller-chosen tiles of ``block`` x ``block``: a pair is
+    visible when its tile is selected as full (2), or selected as partial (1)
+    and the program holds there.
+    """
+
+    def __init__(self, mask, doc_row: Optional[np.ndarray] = None, prefix_len: Optional[int] = None,
+                 selection: Optional[np.ndarray] = None, block: int = 128):
         nodes = mask.nodes if hasattr(mask, "nodes") else tuple(mask)
         if len(nodes) > 16:
             raise ValueError("at most 16 nodes")
@@ -99,7 +107,59 @@ class Program:
                 s.arg[t] = int(prefix_len)
         if self._doc is not None:
             s.doc = self._doc.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
+        self._sel = None
+        if selection is not None:
+            self._sel = np.ascontiguousarray(selection, dtype=np.int8)
+            if self._sel.ndim != 2 or block < 1:
+                raise ValueError("selection must be [nq, nkv] with a positive block")
+            s.sel = self._sel.ctypes.data_as(ctypes.POINTER(ctypes.c_int8))
+            s.sel_block = int(block)
+            s.sel_nkv = self._sel.shape[1]
         self.struct = s
+
+
+def selection_from_lists(kv_num, kv_idx, full_num=None, full_idx=None, nkv: int = 0,
+                         drop_invalid: bool = False) -> np.ndarray:
+    """Tile selection [nq, nkv] of caller-supplied lists for one (batch, head).
+
+    Row I lists ``kv_num[I]`` partial tiles in ``kv_idx[I, :kv_num[I]]`` and
+    ``full_num[I]`` full tiles in ``full_idx[I, :full_num[I]]``, in any order
+    (tutorial "FlexAttention in PyTorch", "Decoding and paged KV caches":
+    BlockMask.from_kv_blocks).  Result: 0 not listed, 1 partial, 2 full.
+    A count outside [0, min(nkv, row length)], an index outside [0, nkv) or a
+    tile listed twice is invalid: ValueError, or with ``drop_invalid`` the
+    entry is skipped (a count is clamped; a tile in both lists stays full).
+    Returns (selection, n_invalid) when ``drop_invalid`` is set.
+    """
+    kv_num = np.asarray(kv_num)
+    nq = kv_num.shape[0]
+    sel = np.zeros((nq, nkv), dtype=np.int8)
+    bad = 0
+    lists = [(kv_num, np.asarray(kv_idx), 1)]
+    if full_num is not None:
+        lists.append((np.asarray(full_num), np.asarray(full_idx), 2))
+    for num, idx, code in lists:
+        for I in range(nq):
+            n = int(num[I])
+            cap = min(nkv, idx.shape[1])
+            if n < 0 or n > cap:
+                if not drop_invalid:
+                    raise ValueError(f"row {I}: count {n} outside [0, {cap}]")
+                bad += 1
+                n = max(0, min(n, cap))
+            for t in range(n):
+                J = int(idx[I, t])
+                if J < 0 or J >= nkv:
+                    if not drop_invalid:
+                        raise ValueError(f"row {I}: tile index {J} outside [0, {nkv})")
+                    bad += 1
+                    continue
+                if sel[I, J] != 0:
+                    if not drop_invalid:
+                        raise ValueError(f"row {I}: tile {J} listed twice")
+                    bad += 1
+                sel[I, J] = max(int(sel[I, J]), code)
+    return (sel, bad) if drop_invalid else sel
 
 
 def _dptr(a: np.ndarray):
@@ -253,6 +313,14 @@ def np_mask(mask, q_len: int, kv_len: int, doc_row=None, prefix_len=None) -> np.
             raise ValueError(node)
     (M,) = stack
     return np.array(M, dtype=bool)
+
+
+def np_select(M: np.ndarray, selection: np.ndarray, block: int) -> np.ndarray:
+    """Mask M restricted to selected tiles (see Program): the selection grid is
+    expanded to one code per pair, then full -> visible, partial -> M, else hidden."""
+    q_len, kv_len = M.shape
+    E = np.repeat(np.repeat(np.asarray(selection), block, axis=0), block, axis=1)[:q_len, :kv_len]
+    return (E == 2) | ((E == 1) & M)
 
 
 def np_classify(M: np.ndarray, block: int) -> np.ndarray:

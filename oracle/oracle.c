@@ -14,6 +14,11 @@
  *    Context paragraph; tutorial "The two hooks: score_mod and mask_mod",
  *    Pattern 1 document masking, Pattern 2 sliding window with sinks, and the
  *    and_masks / or_masks composition in Pattern 3);
+ *  - for caller-chosen tiles (tutorial, opening section: sparse patterns that
+ *    attend only to a selected subset of blocks; "Decoding and paged KV
+ *    caches": BlockMask.from_kv_blocks), the mask those tiles leave: a pair is
+ *    visible when its tile is listed as full, or listed as partial and the
+ *    program holds there, and never when its tile is not listed;
  *  - the tile classes of a BLOCK x BLOCK grid by brute force: a tile is EMPTY
  *    when no in-range entry is visible, FULL when every one is, PARTIAL
  *    otherwise (tutorial, "The two hooks": empty / partially masked / full
@@ -65,10 +70,14 @@ typedef struct {
     int32_t op[16];
     int64_t arg[16];       /* window W, sink count or prefix length      */
     const int32_t *doc;    /* document id of each position of this batch row */
+    /* Optional selection of tiles, row-major [nq][sel_nkv] of sel_block x
+     * sel_block tiles: 0 not listed, 1 listed partial, 2 listed full. */
+    const int8_t *sel;
+    int64_t sel_block, sel_nkv;
 } or_program;
 
-/* M[i][j] of the program, evaluated with an explicit stack. */
-static int mask_at(const or_program *p, int64_t i, int64_t j)
+/* The program's value at (i, j), evaluated with an explicit stack. */
+static int program_at(const or_program *p, int64_t i, int64_t j)
 {
     int st[16];
     int sp = 0;
@@ -86,6 +95,19 @@ static int mask_at(const or_program *p, int64_t i, int64_t j)
         }
     }
     return st[0];
+}
+
+/* M[i][j]: the program's value, restricted by the tile selection if any. */
+static int mask_at(const or_program *p, int64_t i, int64_t j)
+{
+    if (p->sel != NULL) {
+        const int8_t c = p->sel[(i / p->sel_block) * p->sel_nkv + j / p->sel_block];
+        if (c == 2)
+            return 1;
+        if (c != 1)
+            return 0;
+    }
+    return program_at(p, i, j);
 }
 
 /* Explicit [q_len][kv_len] byte mask. */

@@ -388,3 +388,160 @@ def test_backward_subsets_match_full():
     np.testing.assert_array_equal(dq2, dq[rows])
     np.testing.assert_array_equal(dk2, dk[cols])
     np.testing.assert_array_equal(dv2, dv[cols])
+
+
+# ------------------------------------------------- caller-chosen tiles (from_kv_blocks)
+
+def _random_selection(rng, nq, nkv, p_partial=0.3, p_full=0.3):
+    u = rng.random((nq, nkv))
+    return np.where(u < p_partial, 1, np.where(u < p_partial + p_full, 2, 0)).astype(np.int8)
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_selection_of_own_classes_leaves_mask_unchanged(seed):
+    """Selecting exactly a program's own PARTIAL and FULL tiles changes nothing:
+    FULL tiles are all visible anyway and EMPTY ones hold no visible pair.  A
+    swapped class code or a transposed tile index breaks this for the random,
+    asymmetric programs here (ragged lengths, several block sizes)."""
+    rng = np.random.default_rng(100 + seed)
+    nodes = _random_program(rng)
+    if len(nodes) > 16:
+        nodes = nodes[:1]
+    q_len, kv_len = int(rng.integers(40, 260)), int(rng.integers(40, 260))
+    docs = make_doc_ids(("geometric", 30.0), max(q_len, kv_len), seed)[0]
+    prefix = int(rng.integers(0, 120))
+    plain = oracle.Program(P(*nodes), doc_row=docs, prefix_len=prefix)
+    M = oracle.mask_dense(plain, q_len, kv_len)
+    for block in (16, 32, 64):
+        cls = oracle.classify_tiles(plain, q_len, kv_len, block)
+        sel = oracle.Program(P(*nodes), doc_row=docs, prefix_len=prefix, selection=cls, block=block)
+        np.testing.assert_array_equal(oracle.mask_dense(sel, q_len, kv_len), M)
+
+
+def test_selection_lists_round_trip_in_any_order():
+    """Lists in any order give the grid they were made from; the class grid's
+    own ascending lists give it back too."""
+    rng = np.random.default_rng(7)
+    nq, nkv = 9, 13
+    sel = _random_selection(rng, nq, nkv)
+    kv_num = np.zeros(nq, np.int32)
+    full_num = np.zeros(nq, np.int32)
+    kv_idx = np.full((nq, 5 + nkv), -7, np.int32)      # wider rows, junk past the counts
+    full_idx = np.full((nq, nkv), 99, np.int32)
+    for I in range(nq):
+        p = rng.permutation(np.nonzero(sel[I] == 1)[0])
+        f = rng.permutation(np.nonzero(sel[I] == 2)[0])
+        kv_num[I], full_num[I] = len(p), len(f)
+        kv_idx[I, :len(p)] = p
+        full_idx[I, :len(f)] = f
+    np.testing.assert_array_equal(oracle.selection_from_lists(kv_num, kv_idx, full_num, full_idx, nkv), sel)
+    L = oracle.tile_lists(sel)
+    np.testing.assert_array_equal(
+        oracle.selection_from_lists(L["kv_num_blocks"], L["kv_indices"], L["full_kv_num_blocks"],
+                                    L["full_kv_indices"], nkv), sel)
+    # partial lists alone
+    np.testing.assert_array_equal(oracle.selection_from_lists(kv_num, kv_idx, nkv=nkv), np.where(sel == 1, 1, 0))
+
+
+def test_selection_from_lists_rejects_invalid_entries():
+    nkv = 4
+    ok_num, ok_idx = np.array([1]), np.array([[2, 0, 0, 0]])
+    for num, idx, fnum, fidx in [
+        (np.array([1]), np.array([[4, 0, 0, 0]]), None, None),       # index past the last tile
+        (np.array([1]), np.array([[-1, 0, 0, 0]]), None, None),      # negative index
+        (np.array([2]), np.array([[1, 1, 0, 0]]), None, None),       # listed twice
+        (np.array([5]), np.array([[0, 1, 2, 3, 0]]), None, None),    # count above nkv
+        (np.array([-1]), np.array([[0, 0, 0, 0]]), None, None),      # negative count
+        (ok_num, ok_idx, np.array([1]), np.array([[2, 0, 0, 0]])),   # partial and full
+    ]:
+        with pytest.raises(ValueError):
+            oracle.selection_from_lists(num, idx, fnum, fidx, nkv)
+    sel, bad = oracle.selection_from_lists(ok_num, ok_idx, np.array([2]), np.array([[2, 5, 0, 0]]), nkv,
+                                           drop_invalid=True)
+    assert bad == 2 and sel.tolist() == [[0, 0, 2, 0]]   # both-listed tile stays full; index 5 dropped
+
+
+def test_selection_true_program_is_tile_expansion():
+    """With an everywhere-true program the mask is the selected tiles, whole
+    (built here tile by tile), cut at ragged lengths."""
+    rng = np.random.default_rng(3)
+    q_len, kv_len, b = 150, 201, 32
+    nq, nkv = -(-q_len // b), -(-kv_len // b)
+    sel = _random_selection(rng, nq, nkv)
+    M = oracle.mask_dense(oracle.Program(P(("true",)), selection=sel, block=b), q_len, kv_len)
+    ref = np.zeros((q_len, kv_len), bool)
+    for I in range(nq):
+        for J in range(nkv):
+            if sel[I, J]:
+                ref[I * b:(I + 1) * b, J * b:(J + 1) * b] = True
+    np.testing.assert_array_equal(M, ref)
+
+
+def test_selection_partial_tiles_take_the_program_full_tiles_do_not():
+    S, b = 96, 32
+    n = S // b
+    i, j = np.arange(S)[:, None], np.arange(S)[None, :]
+    every = lambda c: np.full((n, n), c, np.int8)
+    M = lambda c: oracle.mask_dense(oracle.Program(CAUSAL, selection=every(c), block=b), S, S)
+    np.testing.assert_array_equal(M(1), i >= j)                 # partial everywhere: causal
+    np.testing.assert_array_equal(M(2), np.ones((S, S), bool))  # full everywhere: dense
+    np.testing.assert_array_equal(M(0), np.zeros((S, S), bool))  # nothing listed
+    q, k, v, _ = _qkv(S, 64, 30)
+    out, lse = oracle.forward_head(q, k, v, oracle.Program(CAUSAL, selection=every(0), block=b), ("none",), 0, 0.125)
+    assert np.all(out == 0) and np.all(np.isneginf(lse))
+
+
+def test_selection_block_diagonal_is_independent_blocks():
+    """Each query tile sees only its own key tile (full): per-block textbook
+    attention (torch SDPA on each block, fp64)."""
+    S, D, b = 200, 64, 64
+    q, k, v, _ = _qkv(S, D, 31)
+    n = -(-S // b)
+    sel = np.eye(n, dtype=np.int8) * 2
+    out, lse = oracle.forward_head(q, k, v, oracle.Program(P(("true",)), selection=sel, block=b), ("none",), 0,
+                                   1 / np.sqrt(D))
+    for I in range(n):
+        r = slice(I * b, min(S, (I + 1) * b))
+        tq, tk, tv = (torch.from_numpy(a[r])[None, None] for a in (q, k, v))
+        ref = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv)[0, 0].numpy()
+        np.testing.assert_allclose(out[r], ref, atol=1e-12, rtol=0)
+        ref_lse = torch.logsumexp(torch.from_numpy(q[r] @ k[r].T / np.sqrt(D)), 1).numpy()
+        np.testing.assert_allclose(lse[r], ref_lse, atol=1e-12, rtol=0)
+
+
+def test_selection_q_zero_closed_form():
+    """q = 0: out_i is the mean of the v_j it sees and LSE_i = ln |V_i|, where
+    V_i holds the keys of its full tiles and the causal keys of its partial ones."""
+    S, D, b = 160, 32, 32
+    _, k, v, _ = _qkv(S, D, 32)
+    q = np.zeros((S, D))
+    sel = _random_selection(np.random.default_rng(33), S // b, S // b, 0.4, 0.4)
+    sel[:, 0] = 1                                   # every row sees key 0 through a partial tile
+    out, lse = oracle.forward_head(q, k, v, oracle.Program(CAUSAL, selection=sel, block=b), ("none",), 0, 0.3)
+    for i in range(S):
+        js = [j for j in range(S) if sel[i // b, j // b] == 2 or (sel[i // b, j // b] == 1 and j <= i)]
+        np.testing.assert_allclose(out[i], v[js].mean(axis=0), atol=1e-12)
+        assert abs(lse[i] - np.log(len(js))) < 1e-12
+
+
+@pytest.mark.parametrize("score", ["none", "softcap", "alibi"])
+def test_selection_forward_backward_match_numpy_twin(score):
+    """C loops over a selection vs the numpy twin's expanded dense mask."""
+    S, kv_len, D, b = 130, 170, 32, 32
+    q, k, v, do = _qkv(S, D, 34, kv_len=kv_len)
+    docs = make_doc_ids(("geometric", 30.0), kv_len, 35)[0]
+    mask = P(("causal",), ("same_doc",), ("and",))
+    sel = _random_selection(np.random.default_rng(36), -(-S // b), -(-kv_len // b))
+    sc = {"none": ("none",), "softcap": ("softcap", 4.0), "alibi": ("alibi", [0.0625])}[score]
+    prog = oracle.Program(mask, doc_row=docs, selection=sel, block=b)
+    out, lse = oracle.forward_head(q, k, v, prog, sc, 0, 0.3)
+    M = oracle.np_select(oracle.np_mask(mask, S, kv_len, doc_row=docs), sel, b)
+    tw = sc if score != "alibi" else ("alibi",)
+    ref_out, ref_lse, _ = oracle.np_forward(q, k, v, M, tw, 0.0625, 0.3)
+    np.testing.assert_allclose(out, ref_out, atol=1e-12)
+    np.testing.assert_array_equal(np.isneginf(lse), np.isneginf(ref_lse))
+    fin = np.isfinite(ref_lse)
+    np.testing.assert_allclose(lse[fin], ref_lse[fin], atol=1e-12)
+    dq, dk, dv, _, _ = oracle.backward_head(q, k, v, do, prog, sc, 0, 0.3)
+    for a, r in zip((dq, dk, dv), oracle.np_backward(q, k, v, do, M, tw, 0.0625, 0.3)):
+        np.testing.assert_allclose(a, r, atol=1e-11)
