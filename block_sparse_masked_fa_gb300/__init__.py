@@ -13,6 +13,7 @@ from .binding import (  # noqa: F401
     fa_backward_noalloc,
     fa_backward_workspace_bytes,
     fa_block_mask_bytes,
+    fa_block_mask_from_kv_blocks,
     fa_block_mask_summary,
     fa_create_block_mask,
     fa_forward,

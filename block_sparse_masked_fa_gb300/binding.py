@@ -1,7 +1,7 @@
 """ctypes binding of the C ABI in include/fa.h (argument marshalling only).
 
 Names mirror the C entry points: fa_block_mask_bytes, fa_create_block_mask,
-fa_forward, fa_backward_workspace_bytes, fa_backward, fa_get_status,
+fa_block_mask_from_kv_blocks, fa_forward, fa_backward_workspace_bytes, fa_backward, fa_get_status,
 fa_block_mask_summary, fa_status_string.  Tensors are torch CUDA tensors; the
 binding passes their device pointers and the current CUDA stream.  Every step
 of the computation runs in the library's kernels; importing this module fails
@@ -68,6 +68,10 @@ _lib.fa_block_mask_bytes.argtypes = [_c.c_int32, _c.c_int32, _c.c_int64, _c.c_in
 _lib.fa_create_block_mask.argtypes = [_c.POINTER(MaskSpec), _c.c_int32, _c.c_int32, _c.c_int64, _c.c_int64,
                                       _c.c_int32, _c.c_void_p, _c.c_size_t, _c.POINTER(BlockMaskStruct),
                                       _c.c_void_p]
+_lib.fa_block_mask_from_kv_blocks.argtypes = [_c.c_void_p] * 4 + [_c.c_int32, _c.POINTER(MaskSpec), _c.c_int32,
+                                                                  _c.c_int32, _c.c_int64, _c.c_int64, _c.c_int32,
+                                                                  _c.c_void_p, _c.c_size_t,
+                                                                  _c.POINTER(BlockMaskStruct), _c.c_void_p]
 _lib.fa_forward.argtypes = [_c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_int32, _c.c_int32, _c.c_int64,
                             _c.c_int64, _c.c_int32, _c.POINTER(BlockMaskStruct), _c.POINTER(ScoreSpec),
                             _c.c_float, _c.c_void_p, _c.c_void_p, _c.c_void_p]
@@ -85,12 +89,12 @@ _lib.fa_get_status.argtypes = [_c.POINTER(BlockMaskStruct), _c.c_int32, _c.c_voi
 _lib.fa_block_mask_summary.argtypes = [_c.POINTER(BlockMaskStruct), _c.POINTER(_c.c_int64 * 3), _c.c_void_p]
 _lib.fa_status_string.argtypes = [_c.c_int]
 _lib.fa_status_string.restype = _c.c_char_p
-for _f in (_lib.fa_block_mask_bytes, _lib.fa_create_block_mask, _lib.fa_forward, _lib.fa_backward_workspace_bytes,
+for _f in (_lib.fa_block_mask_bytes, _lib.fa_create_block_mask, _lib.fa_block_mask_from_kv_blocks, _lib.fa_forward, _lib.fa_backward_workspace_bytes,
            _lib.fa_backward, _lib.fa_backward_noalloc, _lib.fa_get_status, _lib.fa_block_mask_summary):
     _f.restype = _c.c_int
 _lib.fa_version.restype = _c.c_int32
 
-EXPORTED = ("fa_block_mask_bytes", "fa_create_block_mask", "fa_forward", "fa_backward_workspace_bytes",
+EXPORTED = ("fa_block_mask_bytes", "fa_create_block_mask", "fa_block_mask_from_kv_blocks", "fa_forward", "fa_backward_workspace_bytes",
             "fa_backward", "fa_backward_noalloc", "fa_get_status", "fa_block_mask_summary", "fa_status_string",
             "fa_version")
 NOALLOC_SCRATCH_BYTES = 16 << 20
@@ -226,6 +230,46 @@ def fa_create_block_mask(nodes: Sequence[tuple], Bm: int, Hm: int, q_len: int, k
     _check(_lib.fa_create_block_mask(ctypes.byref(spec), Bm, Hm, q_len, kv_len, block, buffer.data_ptr(),
                                      buffer.numel(), ctypes.byref(st), _stream(stream)), "fa_create_block_mask")
     return BlockMask(st, buffer, keep + [spec])
+
+
+def fa_block_mask_from_kv_blocks(kv_num_blocks: torch.Tensor, kv_indices: torch.Tensor, q_len: int, kv_len: int,
+                                 full_kv_num_blocks: Optional[torch.Tensor] = None,
+                                 full_kv_indices: Optional[torch.Tensor] = None, block: int = 128,
+                                 nodes: Optional[Sequence[tuple]] = None, buffer: Optional[torch.Tensor] = None,
+                                 stream=None) -> BlockMask:
+    """Block mask of caller-chosen tiles: int32 CUDA tensors kv_num_blocks
+    [Bm, Hm, nq] and kv_indices [Bm, Hm, nq, stride] (PARTIAL tiles, any
+    order), optionally the same for FULL tiles.  ``nodes``: the mask program
+    applied on PARTIAL tiles (None: all their pairs are visible).  Invalid
+    lists are reported by fa_get_status (FA_ERR_DEVICE_CHECK)."""
+    tensors = [kv_num_blocks, kv_indices] + ([] if full_kv_num_blocks is None else
+                                             [full_kv_num_blocks, full_kv_indices])
+    for t in tensors:
+        if t is None or t.dtype != torch.int32 or not t.is_cuda or not t.is_contiguous():
+            raise ValueError("tile lists must be contiguous int32 CUDA tensors")
+    if kv_num_blocks.dim() != 3 or kv_indices.dim() != 4 or kv_indices.shape[:3] != kv_num_blocks.shape:
+        raise ValueError("kv_num_blocks must be [Bm, Hm, nq] and kv_indices [Bm, Hm, nq, stride]")
+    if full_kv_num_blocks is not None and (full_kv_num_blocks.shape != kv_num_blocks.shape or
+                                           full_kv_indices.shape != kv_indices.shape):
+        raise ValueError("full lists must be shaped like the partial ones")
+    Bm, Hm, nq = kv_num_blocks.shape
+    if nq != -(-q_len // block):
+        raise ValueError(f"lists have {nq} query-tile rows; q_len {q_len} at block {block} has {-(-q_len // block)}")
+    keep = list(tensors)
+    spec = None
+    if nodes is not None:
+        spec, k2 = nodes if isinstance(nodes, tuple) and isinstance(nodes[0], MaskSpec) else make_mask_spec(nodes)
+        keep += k2 + [spec]
+    nbytes = fa_block_mask_bytes(Bm, Hm, q_len, kv_len, block)
+    if buffer is None:
+        buffer = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    st = BlockMaskStruct()
+    _check(_lib.fa_block_mask_from_kv_blocks(_ptr(kv_num_blocks), _ptr(kv_indices), _ptr(full_kv_num_blocks),
+                                             _ptr(full_kv_indices), kv_indices.shape[3],
+                                             ctypes.byref(spec) if spec is not None else None, Bm, Hm, q_len,
+                                             kv_len, block, buffer.data_ptr(), buffer.numel(), ctypes.byref(st),
+                                             _stream(stream)), "fa_block_mask_from_kv_blocks")
+    return BlockMask(st, buffer, keep)
 
 
 def _score(score):

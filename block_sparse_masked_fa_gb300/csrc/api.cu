@@ -200,41 +200,12 @@ bool encode_tmap_3d(CUtensorMap* map, CUtensorMapDataType dtype, int elem_bytes,
                   swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-}  // namespace fa
-
-using namespace fa;
-
-extern "C" {
-
-int32_t fa_version(void) { return 100; }
-
-const char* fa_status_string(fa_status s) {
-  switch (s) {
-    case FA_OK: return "ok";
-    case FA_ERR_INVALID_ARG: return "invalid argument";
-    case FA_ERR_UNSUPPORTED: return "unsupported configuration";
-    case FA_ERR_SHAPE: return "bad or inconsistent shape";
-    case FA_ERR_ALIGNMENT: return "pointer not 16-byte aligned";
-    case FA_ERR_CUDA: return "CUDA call failed";
-    case FA_ERR_TIMEOUT: return "device wait timed out";
-    case FA_ERR_DEVICE_CHECK: return "device range check failed";
-    case FA_ERR_WORKSPACE: return "buffer too small";
-  }
-  return "unknown status";
-}
-
-fa_status fa_block_mask_bytes(int32_t Bm, int32_t Hm, int64_t q_len, int64_t kv_len, int32_t block, size_t* bytes) {
-  if (bytes == nullptr) return FA_ERR_INVALID_ARG;
-  Layout L;
-  const fa_status st = make_layout(Bm, Hm, q_len, kv_len, block, &L);
-  if (st != FA_OK) return st;
-  *bytes = L.total;
-  return FA_OK;
-}
-
-fa_status fa_create_block_mask(const fa_mask_spec* spec, int32_t Bm, int32_t Hm, int64_t q_len, int64_t kv_len,
-                               int32_t block, void* buffer, size_t buffer_bytes, fa_block_mask* bm,
-                               cudaStream_t stream) {
+// Shared body of fa_create_block_mask and fa_block_mask_from_kv_blocks: lays
+// out `buffer`, fills `bm` and queues the builder (with the caller's tile lists
+// in place of classification when `sel` is set).
+static fa_status build_block_mask(const fa_mask_spec* spec, int32_t Bm, int32_t Hm, int64_t q_len, int64_t kv_len,
+                                  int32_t block, void* buffer, size_t buffer_bytes, fa_block_mask* bm,
+                                  const BuildArgs* sel, cudaStream_t stream) {
   if (bm == nullptr || buffer == nullptr) return FA_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(buffer) & (kAlign - 1)) != 0) return FA_ERR_ALIGNMENT;
   Layout L;
@@ -299,6 +270,13 @@ fa_status fa_create_block_mask(const fa_mask_spec* spec, int32_t Bm, int32_t Hm,
   a.doc_runs = bm->doc_runs;
   a.row_segs = bm->row_segs;
   a.status = bm->status;
+  if (sel != nullptr) {
+    a.sel_num = sel->sel_num;
+    a.sel_idx = sel->sel_idx;
+    a.sel_full_num = sel->sel_full_num;
+    a.sel_full_idx = sel->sel_full_idx;
+    a.sel_stride = sel->sel_stride;
+  }
   if (dm.has_doc) {  // classify reads the run table that the builder fills first
     const int64_t run_len = q_len > kv_len ? q_len : kv_len;
     a.mask.runs = bm->doc_runs;
@@ -306,6 +284,72 @@ fa_status fa_create_block_mask(const fa_mask_spec* spec, int32_t Bm, int32_t Hm,
     a.mask.run_len = run_len;
   }
   return cuda_status(launch_build(a, stream));
+}
+
+}  // namespace fa
+
+using namespace fa;
+
+extern "C" {
+
+int32_t fa_version(void) { return 100; }
+
+const char* fa_status_string(fa_status s) {
+  switch (s) {
+    case FA_OK: return "ok";
+    case FA_ERR_INVALID_ARG: return "invalid argument";
+    case FA_ERR_UNSUPPORTED: return "unsupported configuration";
+    case FA_ERR_SHAPE: return "bad or inconsistent shape";
+    case FA_ERR_ALIGNMENT: return "pointer not 16-byte aligned";
+    case FA_ERR_CUDA: return "CUDA call failed";
+    case FA_ERR_TIMEOUT: return "device wait timed out";
+    case FA_ERR_DEVICE_CHECK: return "device range check failed";
+    case FA_ERR_WORKSPACE: return "buffer too small";
+  }
+  return "unknown status";
+}
+
+fa_status fa_block_mask_bytes(int32_t Bm, int32_t Hm, int64_t q_len, int64_t kv_len, int32_t block, size_t* bytes) {
+  if (bytes == nullptr) return FA_ERR_INVALID_ARG;
+  Layout L;
+  const fa_status st = make_layout(Bm, Hm, q_len, kv_len, block, &L);
+  if (st != FA_OK) return st;
+  *bytes = L.total;
+  return FA_OK;
+}
+
+fa_status fa_create_block_mask(const fa_mask_spec* spec, int32_t Bm, int32_t Hm, int64_t q_len, int64_t kv_len,
+                               int32_t block, void* buffer, size_t buffer_bytes, fa_block_mask* bm,
+                               cudaStream_t stream) {
+  return build_block_mask(spec, Bm, Hm, q_len, kv_len, block, buffer, buffer_bytes, bm, nullptr, stream);
+}
+
+fa_status fa_block_mask_from_kv_blocks(const int32_t* kv_num_blocks, const int32_t* kv_indices,
+                                       const int32_t* full_kv_num_blocks, const int32_t* full_kv_indices,
+                                       int32_t idx_stride, const fa_mask_spec* spec, int32_t Bm, int32_t Hm,
+                                       int64_t q_len, int64_t kv_len, int32_t block, void* buffer,
+                                       size_t buffer_bytes, fa_block_mask* bm, cudaStream_t stream) {
+  if (kv_num_blocks == nullptr || kv_indices == nullptr) return FA_ERR_INVALID_ARG;
+  if ((full_kv_num_blocks == nullptr) != (full_kv_indices == nullptr)) return FA_ERR_INVALID_ARG;
+  if (!aligned4(kv_num_blocks) || !aligned4(kv_indices) || !aligned4(full_kv_num_blocks) ||
+      !aligned4(full_kv_indices))
+    return FA_ERR_ALIGNMENT;
+  if (idx_stride < 1) return FA_ERR_SHAPE;
+  fa_mask_spec all;  // no program: every pair of a listed PARTIAL tile is visible
+  if (spec == nullptr) {
+    std::memset(&all, 0, sizeof(all));
+    all.n = 1;
+    all.node[0].op = FA_M_TRUE;
+    spec = &all;
+  }
+  BuildArgs sel;
+  std::memset(&sel, 0, sizeof(sel));
+  sel.sel_num = kv_num_blocks;
+  sel.sel_idx = kv_indices;
+  sel.sel_full_num = full_kv_num_blocks;
+  sel.sel_full_idx = full_kv_indices;
+  sel.sel_stride = idx_stride;
+  return build_block_mask(spec, Bm, Hm, q_len, kv_len, block, buffer, buffer_bytes, bm, &sel, stream);
 }
 
 fa_status fa_forward(const void* q, const void* k, const void* v, int32_t B, int32_t H, int64_t q_len,

@@ -16,6 +16,8 @@
 //                     row's visible pairs from its row_segs intervals (or, for
 //                     rows they do not describe, evaluating all its pairs).
 //                     Writes one class byte per tile.
+//     or select    -- for caller-chosen tiles, one warp per query-tile row
+//                     writes the class bytes from the caller's lists instead.
 //  3. compact      -- one warp per query-tile row and one per key-tile
 //                     column: ballot + popcount prefix sums turn the class
 //                     bytes into ascending PARTIAL and FULL index lists with
@@ -408,6 +410,55 @@ __global__ void __launch_bounds__(kBuildWarps * 32) classify_kernel(const __grid
   if (valid) a.tile_class[row * a.nkv + J] = (uint8_t)cls;
 }
 
+// Caller-chosen tiles (tutorial "FlexAttention in PyTorch": block-selection
+// sparse patterns; "Decoding and paged KV caches": BlockMask.from_kv_blocks).
+// One warp per query-tile row clears the row's class bytes, marks the listed
+// PARTIAL tiles 1 and then the listed FULL tiles 2 (a tile in both lists ends
+// FULL), and checks the lists: a count outside [0, min(nkv, stride)] (clamped),
+// an index outside [0, nkv) (dropped) or a tile listed twice sets the status
+// word's check bit.  Compaction then rebuilds the lists ascending, with the
+// per-column lists the backward needs.
+__global__ void __launch_bounds__(kBuildWarps * 32) select_kernel(const __grid_constant__ BuildArgs a) {
+  pdl_wait_then_release();
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int64_t row = (int64_t)blockIdx.x * kBuildWarps + warp;  // (bm, hm, I)
+  if (row >= (int64_t)a.Bm * a.Hm * a.nq) return;
+  uint8_t* cls = a.tile_class + row * a.nkv;
+  for (int J = lane; J < a.nkv; J += 32) cls[J] = 0;
+  __syncwarp();
+  const int cap = min(a.nkv, a.sel_stride);
+  bool bad = false;
+  int listed = 0;
+  for (int code = 1; code <= 2; ++code) {
+    const int32_t* num = (code == 1) ? a.sel_num : a.sel_full_num;
+    if (num == nullptr) continue;
+    const int32_t* idx = ((code == 1) ? a.sel_idx : a.sel_full_idx) + row * (int64_t)a.sel_stride;
+    int n = __ldg(num + row);
+    if (n < 0 || n > cap) {
+      bad = true;
+      n = max(0, min(n, cap));
+    }
+    for (int t = lane; t < n; t += 32) {
+      const int J = __ldg(idx + t);
+      if (J < 0 || J >= a.nkv) {
+        bad = true;
+        continue;
+      }
+      cls[J] = (uint8_t)code;
+      ++listed;
+    }
+    __syncwarp();  // the FULL marks land after every PARTIAL one
+  }
+  // a tile listed twice leaves fewer marked tiles than valid entries
+  int marked = 0;
+  for (int J = lane; J < a.nkv; J += 32) marked += cls[J] != 0;
+  const unsigned tot_marked = __reduce_add_sync(0xffffffffu, (unsigned)marked);
+  const unsigned tot_listed = __reduce_add_sync(0xffffffffu, (unsigned)listed);
+  if (__any_sync(0xffffffffu, bad) || tot_marked != tot_listed) {
+    if (lane == 0) atomicOr(a.status, kStatusCheck);
+  }
+}
+
 // Compaction: warps [0, rows) build the per-row lists, the next [0, cols)
 // warps the per-column lists, both with ballots over the class bytes.
 __global__ void __launch_bounds__(kBuildWarps * 32) compact_kernel(const __grid_constant__ BuildArgs a) {
@@ -542,8 +593,12 @@ cudaError_t launch_build(const BuildArgs& a, cudaStream_t stream) {
   const int64_t rows = (int64_t)a.Bm * a.Hm * a.nq;
   const int64_t cols = (int64_t)a.Bm * a.Hm * a.nkv;
   const int64_t cwarps = rows * ((a.nkv + 31) / 32);
-  e = launch_k(classify_kernel, dim3((unsigned)((cwarps + kBuildWarps - 1) / kBuildWarps)), dim3(kBuildWarps * 32), 0,
-               stream, a);
+  if (a.sel_num != nullptr)
+    e = launch_k(select_kernel, dim3((unsigned)((rows + kBuildWarps - 1) / kBuildWarps)), dim3(kBuildWarps * 32), 0,
+                 stream, a);
+  else
+    e = launch_k(classify_kernel, dim3((unsigned)((cwarps + kBuildWarps - 1) / kBuildWarps)),
+                 dim3(kBuildWarps * 32), 0, stream, a);
   if (e != cudaSuccess) return e;
   e = launch_k(compact_kernel, dim3((unsigned)((rows + cols + kBuildWarps - 1) / kBuildWarps)), dim3(kBuildWarps * 32),
                0, stream, a);

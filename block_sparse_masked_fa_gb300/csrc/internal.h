@@ -19,6 +19,11 @@ struct BuildArgs {
   int32_t* doc_runs;  // [Bm][max(q_len, kv_len)][2] runs, then [Bm] sorted flags
   int32_t* row_segs;  // [Bm][2][max(q_len, kv_len)][4] visible intervals per row / column
   uint32_t* status;
+  // Caller-chosen tiles (fa_block_mask_from_kv_blocks), else null: per query-tile
+  // row a count and sel_stride indices of PARTIAL (sel_*) and FULL (sel_full_*)
+  // tiles, [Bm][Hm][nq] and [Bm][Hm][nq][sel_stride]; they replace classification.
+  const int32_t *sel_num, *sel_idx, *sel_full_num, *sel_full_idx;
+  int32_t sel_stride;
 };
 
 // Launches a kernel on `stream` allowed to start while the kernel before it

@@ -150,7 +150,8 @@ typedef struct {
  *                      decrease somewhere).  The attention kernels build their
  *                      PARTIAL tiles' mask words from it, and evaluate the
  *                      program per element where lo0 = -1.
- *   status             device status word (bit 0: a wait timed out).
+ *   status             device status word (bit 0: a wait timed out; bit 1: a
+ *                      device check failed, e.g. invalid caller tile lists).
  *
  * The union kv_num_blocks + full_kv_num_blocks is the count of "tiles that are
  * not fully masked" of the speedrun notes' tile-summary paragraph.  Bm is 1 or
@@ -197,6 +198,35 @@ fa_status fa_block_mask_bytes(int32_t Bm, int32_t Hm, int64_t q_len, int64_t kv_
 fa_status fa_create_block_mask(const fa_mask_spec* spec, int32_t Bm, int32_t Hm, int64_t q_len, int64_t kv_len,
                                int32_t block, void* buffer, size_t buffer_bytes, fa_block_mask* bm,
                                cudaStream_t stream);
+
+/* Builds a block mask from caller-chosen tiles instead of a program's tile
+ * classes (tutorial "FlexAttention in PyTorch": sparse patterns that attend
+ * only to a selected subset of blocks; "Decoding and paged KV caches":
+ * BlockMask.from_kv_blocks).  The visible pairs are every in-range pair of a
+ * tile listed as FULL, and the pairs of a tile listed as PARTIAL where `spec`
+ * holds; nothing else.
+ *   kv_num_blocks       device int32 [Bm][Hm][nq]              PARTIAL tiles per query-tile row
+ *   kv_indices          device int32 [Bm][Hm][nq][idx_stride]  their J, in any order
+ *   full_kv_num_blocks, full_kv_indices: the same for FULL tiles; both NULL for none
+ *   idx_stride          row length of the index arrays, >= 1 (nkv for the lists
+ *                       of another fa_block_mask); entries past a row's count
+ *                       are not read
+ *   spec                mask program applied on PARTIAL tiles, or NULL: every
+ *                       pair of a PARTIAL tile is visible (one FA_M_TRUE node)
+ * The caller's lists are only read, by the first kernel; they may be freed or
+ * reused once it has run (stream order).  The block mask's own lists are
+ * rebuilt from them: ascending, zero padded, with the per-column lists and
+ * work orders of fa_create_block_mask.  The lists are checked on the device:
+ * a count outside [0, min(nkv, idx_stride)] (clamped), an index outside
+ * [0, nkv) (dropped) or a tile listed twice (a tile in both lists stays FULL)
+ * sets the status word's check bit, which fa_get_status reports as
+ * FA_ERR_DEVICE_CHECK.  Other arguments and errors as fa_create_block_mask;
+ * the pointers must be 4-byte aligned (FA_ERR_ALIGNMENT). */
+fa_status fa_block_mask_from_kv_blocks(const int32_t* kv_num_blocks, const int32_t* kv_indices,
+                                       const int32_t* full_kv_num_blocks, const int32_t* full_kv_indices,
+                                       int32_t idx_stride, const fa_mask_spec* spec, int32_t Bm, int32_t Hm,
+                                       int64_t q_len, int64_t kv_len, int32_t block, void* buffer,
+                                       size_t buffer_bytes, fa_block_mask* bm, cudaStream_t stream);
 
 /* Forward: out and LSE (speedrun notes, Context: the two matmuls and the
  * softmax fused in one tiled kernel that never writes the score matrix; the

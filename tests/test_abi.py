@@ -116,6 +116,31 @@ def test_create_block_mask_rejects():
     assert _create(too_many) == INVALID
 
 
+def _from_lists(num=FAKE, idx=FAKE, fnum=None, fidx=None, stride=4, spec=None, block=128, buf=FAKE,
+                nbytes=1 << 30, bm=True):
+    st = B.BlockMaskStruct()
+    return B._lib.fa_block_mask_from_kv_blocks(num, idx, fnum, fidx, stride,
+                                               ctypes.byref(spec) if spec is not None else None, 1, 1, 512, 512,
+                                               block, buf, nbytes, ctypes.byref(st) if bm else None, None)
+
+
+def test_from_kv_blocks_rejects():
+    """Host-side errors of the caller-chosen tiles entry, all before any GPU work."""
+    assert _from_lists(num=None) == INVALID
+    assert _from_lists(idx=None) == INVALID
+    assert _from_lists(fnum=FAKE) == INVALID                       # full counts without indices
+    assert _from_lists(fidx=FAKE) == INVALID                       # full indices without counts
+    assert _from_lists(idx=FAKE + 2) == ALIGN
+    assert _from_lists(fnum=FAKE + 1, fidx=FAKE) == ALIGN
+    assert _from_lists(stride=0) == SHAPE
+    assert _from_lists(spec=_spec([])) == INVALID                   # an empty program is not "no program"
+    assert _from_lists(spec=_spec([(M["window"], None)])) == INVALID
+    assert _from_lists(block=48) == UNSUPPORTED
+    assert _from_lists(bm=False) == INVALID
+    assert _from_lists(buf=FAKE + 16) == ALIGN
+    assert _from_lists(nbytes=100) == WORKSPACE
+
+
 def _bm(block=128, q=1024, kv=1024, Bm=1, Hm=1):
     st = B.BlockMaskStruct()
     st.Bm, st.Hm, st.block, st.q_len, st.kv_len = Bm, Hm, block, q, kv
