@@ -69,6 +69,9 @@ def _load():
         lib.oracle_backward_head.argtypes = [d, d, d, d, ctypes.c_int64, ctypes.c_int64, ctypes.c_int32,
                                              P(_Program), ctypes.c_int32, ctypes.c_double, ctypes.c_double,
                                              i64p, ctypes.c_int64, i64p, ctypes.c_int64, d, d, d, d, d]
+        lib.oracle_score_param_grad_head.argtypes = [d, d, d, d, ctypes.c_int64, ctypes.c_int64, ctypes.c_int32,
+                                                     P(_Program), ctypes.c_int32, ctypes.c_double, ctypes.c_double]
+        lib.oracle_score_param_grad_head.restype = ctypes.c_double
         for f in (lib.oracle_mask_dense, lib.oracle_classify_tiles, lib.oracle_forward_head,
                   lib.oracle_backward_head):
             f.restype = None
@@ -272,6 +275,16 @@ def backward_head(q, k, v, do, prog: Program, score: tuple, h: int, scale: float
     return dq, dk, dv, lse, delta
 
 
+def score_param_grad_head(q, k, v, do, prog: Program, score: tuple, h: int, scale: float) -> float:
+    """dL/dparam of L = sum(out * dO) for one head: the soft-cap c, or the ALiBi
+    slope of head h (0.0 for a score mod without a parameter)."""
+    arrs = [np.ascontiguousarray(a, dtype=np.float64) for a in (q, k, v, do)]
+    op, param = _score_args(score, h)
+    return float(_load().oracle_score_param_grad_head(*(_dptr(a) for a in arrs), arrs[0].shape[0],
+                                                      arrs[1].shape[0], arrs[0].shape[1],
+                                                      ctypes.byref(prog.struct), op, param, float(scale)))
+
+
 def head_score(score_kind: tuple, slopes=None, softcap=None) -> tuple:
     """Score tuple for forward_head/backward_head from workload fields."""
     if score_kind[0] == "alibi":
@@ -375,3 +388,23 @@ def np_backward(q, k, v, do, M, score=("none",), slope=0.0, scale=None):
     dk = scale * dS.T @ q
     dv = P.T @ do
     return dq, dk, dv
+
+
+def np_score_param_grad(q, k, v, do, M, score=("none",), slope=0.0, scale=None) -> float:
+    """dL/dparam in matrix form: sum of P * (dP - Delta) * ds/dparam over the mask."""
+    q_len, D = q.shape
+    kv_len = k.shape[0]
+    scale = 1.0 / np.sqrt(D) if scale is None else scale
+    _, _, P = np_forward(q, k, v, M, score, slope, scale)
+    dP = do @ v.T
+    delta = (P * dP).sum(axis=1, keepdims=True)
+    x = scale * (q @ k.T)
+    if score[0] == "softcap":
+        c = float(score[1])
+        t = np.tanh(x / c)
+        dsdp = t - (x / c) * (1.0 - t * t)
+    elif score[0] == "alibi":
+        dsdp = -(np.arange(q_len)[:, None] - np.arange(kv_len)[None, :]).astype(np.float64)
+    else:
+        dsdp = np.zeros_like(x)
+    return float(np.where(M, P * (dP - delta) * dsdp, 0.0).sum())

@@ -42,6 +42,12 @@
  * Score mods: none (s = x); soft-cap s = c tanh(x / c), ds/dx = 1 - tanh^2(x / c);
  * ALiBi s = x - slope_h (i - j), ds/dx = 1.
  *
+ *  - the gradient of L with respect to the score mod's parameter (tutorial
+ *    Pattern 3: a learned relative-position bias trains through the fused
+ *    backward):  dL/dparam = sum_{i, j in V_i} P_ij (dP_ij - Delta_i) ds_ij/dparam
+ *    with ds/dslope_h = -(i - j) for ALiBi and ds/dc = tanh(x/c) - (x/c)(1 - tanh^2(x/c))
+ *    for the soft-cap.
+ *
  * All arithmetic is double precision on the bf16-rounded inputs that the
  * caller widens to double.  Loops are parallel over independent rows or
  * columns only (OpenMP); there is no tiling, fusion or reordering.
@@ -163,6 +169,18 @@ static double score_mod(int op, double param, double x, int64_t i, int64_t j, do
     }
     if (dsdx) *dsdx = 1.0;
     return x;
+}
+
+/* ds/dparam for one pair: the soft-cap c or the ALiBi slope (0 without a parameter). */
+static double score_mod_dparam(int op, double param, double x, int64_t i, int64_t j)
+{
+    if (op == OR_SCORE_SOFTCAP) {
+        const double t = tanh(x / param);
+        return t - (x / param) * (1.0 - t * t);
+    }
+    if (op == OR_SCORE_ALIBI)
+        return -(double)(i - j);
+    return 0.0;
 }
 
 /*
@@ -317,4 +335,55 @@ void oracle_backward_head(const double *q, const double *k, const double *v, con
     if (delta_all) memcpy(delta_all, delta, sizeof(double) * (size_t)q_len);
     free(lse);
     free(delta);
+}
+
+/*
+ * dL/d(score parameter) for one (b, h): the sum over every visible pair of
+ * P_ij (dP_ij - Delta_i) ds_ij/dparam, with LSE_i and Delta_i = sum_j P_ij dP_ij
+ * of each row computed first (row by row, as in the backward above).
+ */
+double oracle_score_param_grad_head(const double *q, const double *k, const double *v, const double *dout,
+                                    int64_t q_len, int64_t kv_len, int32_t D,
+                                    const or_program *p, int32_t score_op, double score_param, double scale)
+{
+    double total = 0.0;
+    #pragma omp parallel reduction(+ : total)
+    {
+        double *s = (double *)malloc(sizeof(double) * (size_t)(kv_len > 0 ? kv_len : 1));
+        double *x = (double *)malloc(sizeof(double) * (size_t)(kv_len > 0 ? kv_len : 1));
+        double *dp = (double *)malloc(sizeof(double) * (size_t)(kv_len > 0 ? kv_len : 1));
+        uint8_t *vis = (uint8_t *)malloc((size_t)(kv_len > 0 ? kv_len : 1));
+        #pragma omp for schedule(dynamic, 16)
+        for (int64_t i = 0; i < q_len; ++i) {
+            double m = -INFINITY;
+            int64_t nvis = 0;
+            for (int64_t j = 0; j < kv_len; ++j) {
+                vis[j] = (uint8_t)mask_at(p, i, j);
+                if (!vis[j]) continue;
+                x[j] = scale * dot(q + i * D, k + j * D, D);
+                s[j] = score_mod(score_op, score_param, x[j], i, j, NULL);
+                dp[j] = dot(dout + i * D, v + j * D, D);
+                if (s[j] > m) m = s[j];
+                ++nvis;
+            }
+            if (nvis == 0) continue;
+            double l = 0.0;
+            for (int64_t j = 0; j < kv_len; ++j)
+                if (vis[j]) l += exp(s[j] - m);
+            const double lse = m + log(l);
+            double delta = 0.0;
+            for (int64_t j = 0; j < kv_len; ++j)
+                if (vis[j]) delta += exp(s[j] - lse) * dp[j];
+            for (int64_t j = 0; j < kv_len; ++j) {
+                if (!vis[j]) continue;
+                const double P = exp(s[j] - lse);
+                total += P * (dp[j] - delta) * score_mod_dparam(score_op, score_param, x[j], i, j);
+            }
+        }
+        free(s);
+        free(x);
+        free(dp);
+        free(vis);
+    }
+    return total;
 }

@@ -545,3 +545,56 @@ def test_selection_forward_backward_match_numpy_twin(score):
     dq, dk, dv, _, _ = oracle.backward_head(q, k, v, do, prog, sc, 0, 0.3)
     for a, r in zip((dq, dk, dv), oracle.np_backward(q, k, v, do, M, tw, 0.0625, 0.3)):
         np.testing.assert_allclose(a, r, atol=1e-11)
+
+
+# ------------------------------------------------- gradient of the score mod's parameter
+
+@pytest.mark.parametrize("score", ["softcap", "alibi"])
+def test_score_param_grad_finite_differences(score):
+    """dL/dparam (soft-cap c, ALiBi slope) against central differences of
+    L = sum(out * dO) through the oracle forward, on a document program."""
+    S, D = 60, 16
+    q, k, v, do = _qkv(S, D, 40)
+    docs = make_doc_ids(("geometric", 15.0), S, 41)[0]
+    prog = oracle.Program(P(("causal",), ("same_doc",), ("and",), ("sink", 3), ("or",)), doc_row=docs)
+    base = 1.5 if score == "softcap" else 0.3125   # ALiBi slopes are stored fp32: base +- eps exact there
+    scale = 0.7
+
+    def sc(val):
+        return ("softcap", val) if score == "softcap" else ("alibi", [val])
+
+    def loss(val):
+        o, _ = oracle.forward_head(q, k, v, prog, sc(val), 0, scale)
+        return float((o * do).sum())
+
+    g = oracle.score_param_grad_head(q, k, v, do, prog, sc(base), 0, scale)
+    eps = 2.0 ** -20
+    num = (loss(base + eps) - loss(base - eps)) / (2 * eps)
+    assert abs(g) > 1e-3                                   # a non-trivial case
+    assert abs(num - g) < 1e-7 * max(1.0, abs(num)), (num, g)
+
+
+@pytest.mark.parametrize("score", ["none", "softcap", "alibi"])
+def test_score_param_grad_matches_numpy_twin(score):
+    S, kv_len, D = 120, 150, 32
+    q, k, v, do = _qkv(S, D, 42, kv_len=kv_len)
+    docs = make_doc_ids(("geometric", 30.0), kv_len, 43)[0]
+    mask = P(("causal",), ("same_doc",), ("and",), ("window", 60), ("and",))
+    sc = {"none": ("none",), "softcap": ("softcap", 4.0), "alibi": ("alibi", [0.0625])}[score]
+    g = oracle.score_param_grad_head(q, k, v, do, oracle.Program(mask, doc_row=docs), sc, 0, 0.3)
+    M = oracle.np_mask(mask, S, kv_len, doc_row=docs)
+    ref = oracle.np_score_param_grad(q, k, v, do, M, sc if score != "alibi" else ("alibi",), 0.0625, 0.3)
+    assert abs(g - ref) < 1e-10 * max(1.0, abs(ref))
+    if score == "none":
+        assert g == 0.0
+
+
+def test_score_param_grad_vanishes_where_out_cannot_move():
+    """V = 1 makes out = 1 whatever the weights, and a diagonal-only mask gives
+    P = 1 on one key: in both dL/dslope is exactly zero (dP - Delta = 0 per row)."""
+    S, D = 90, 32
+    q, k, v, do = _qkv(S, D, 44)
+    g = oracle.score_param_grad_head(q, k, np.ones_like(v), do, oracle.Program(CAUSAL), ("alibi", [0.2]), 0, 0.2)
+    assert abs(g) < 1e-12
+    diag = oracle.Program(P(("causal",), ("window", 1), ("and",)))
+    assert oracle.score_param_grad_head(q, k, v, do, diag, ("alibi", [0.2]), 0, 0.2) == 0.0
