@@ -48,7 +48,7 @@ class MaskSpec(ctypes.Structure):
 
 
 class ScoreSpec(ctypes.Structure):
-    _fields_ = [("op", ctypes.c_int32), ("param", ctypes.c_void_p)]
+    _fields_ = [("op", ctypes.c_int32), ("param", ctypes.c_void_p), ("param_grad", ctypes.c_void_p)]
 
 
 class BlockMaskStruct(ctypes.Structure):
@@ -296,6 +296,20 @@ def fa_forward(q, k, v, block_mask: BlockMask, score=None, scale: float = 0.0, o
     return out, lse
 
 
+def _backward_score(score, score_param_grad, H: int):
+    """Score spec for the backward: a copy of the caller's, with the device
+    pointer of ``score_param_grad`` (fp32 [H], receives dL/dslope for ALiBi)."""
+    sspec, keep = _score(score)
+    spec = ScoreSpec()
+    spec.op, spec.param, spec.param_grad = sspec.op, sspec.param, None
+    if score_param_grad is not None:
+        g = score_param_grad
+        if g.dtype != torch.float32 or not g.is_cuda or not g.is_contiguous() or g.numel() != H:
+            raise ValueError("score_param_grad must be a contiguous fp32 CUDA tensor of H elements")
+        spec.param_grad = g.data_ptr()
+    return spec, keep + [sspec]
+
+
 def fa_backward_workspace_bytes(B: int, H: int, q_len: int, D: int) -> int:
     n = ctypes.c_size_t()
     _check(_lib.fa_backward_workspace_bytes(B, H, q_len, D, ctypes.byref(n)), "fa_backward_workspace_bytes")
@@ -303,8 +317,9 @@ def fa_backward_workspace_bytes(B: int, H: int, q_len: int, D: int) -> int:
 
 
 def fa_backward(q, k, v, out, lse, dout, block_mask: BlockMask, score=None, scale: float = 0.0,
-                dq=None, dk=None, dv=None, workspace=None, stream=None):
-    """dq, dk, dv (bf16, shaped like q, k, v)."""
+                dq=None, dk=None, dv=None, workspace=None, stream=None, score_param_grad=None):
+    """dq, dk, dv (bf16, shaped like q, k, v); with ALiBi, ``score_param_grad``
+    (fp32 [H] CUDA tensor) receives dL/dslope of every head."""
     B, H, q_len, D = q.shape
     kv_len = k.shape[2]
     dq = torch.empty_like(q) if dq is None else dq
@@ -312,7 +327,7 @@ def fa_backward(q, k, v, out, lse, dout, block_mask: BlockMask, score=None, scal
     dv = torch.empty_like(v) if dv is None else dv
     if workspace is None:
         workspace = torch.empty(fa_backward_workspace_bytes(B, H, q_len, D), dtype=torch.uint8, device=q.device)
-    sspec, keep = _score(score)
+    sspec, keep = _backward_score(score, score_param_grad, H)
     _check(_lib.fa_backward(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout), B, H, q_len, kv_len, D,
                             ctypes.byref(block_mask.struct), ctypes.byref(sspec), float(scale), _ptr(dq), _ptr(dk),
                             _ptr(dv), _ptr(workspace), workspace.numel(), _stream(stream)), "fa_backward")
@@ -320,7 +335,7 @@ def fa_backward(q, k, v, out, lse, dout, block_mask: BlockMask, score=None, scal
 
 
 def fa_backward_noalloc(q, k, v, out, lse, dout, block_mask: BlockMask, score=None, scale: float = 0.0,
-                        dq=None, dk=None, dv=None, stream=None):
+                        dq=None, dk=None, dv=None, stream=None, score_param_grad=None):
     """fa_backward without a workspace: for callers that cannot allocate device
     memory at call time (the library's static scratch holds the fp32 dq
     accumulator; see include/fa.h for the size limit and the sharing rules)."""
@@ -329,7 +344,7 @@ def fa_backward_noalloc(q, k, v, out, lse, dout, block_mask: BlockMask, score=No
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
-    sspec, keep = _score(score)
+    sspec, keep = _backward_score(score, score_param_grad, H)
     _check(_lib.fa_backward_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout), B, H, q_len, kv_len,
                                     D, ctypes.byref(block_mask.struct), ctypes.byref(sspec), float(scale), _ptr(dq),
                                     _ptr(dk), _ptr(dv), _stream(stream)), "fa_backward_noalloc")

@@ -128,7 +128,7 @@ fa_status cuda_status(cudaError_t e) { return e == cudaSuccess ? FA_OK : FA_ERR_
 
 // Shared shape checks of fa_forward / fa_backward.
 fa_status check_attn(int32_t B, int32_t H, int64_t q_len, int64_t kv_len, int32_t D, const fa_block_mask* bm,
-                     const fa_score_spec* score, float* scale) {
+                     const fa_score_spec* score, float* scale, bool backward) {
   if (bm == nullptr) return FA_ERR_INVALID_ARG;
   if (B < 1 || H < 1 || q_len < 1 || kv_len < 1) return FA_ERR_SHAPE;
   if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
@@ -141,6 +141,10 @@ fa_status check_attn(int32_t B, int32_t H, int64_t q_len, int64_t kv_len, int32_
   if (score != nullptr) {
     if (score->op < FA_S_NONE || score->op > FA_S_ALIBI) return FA_ERR_INVALID_ARG;
     if (score->op != FA_S_NONE && (score->param == nullptr || !aligned4(score->param))) return FA_ERR_INVALID_ARG;
+    if (backward && score->param_grad != nullptr) {
+      if (score->op != FA_S_ALIBI) return FA_ERR_UNSUPPORTED;
+      if (!aligned4(score->param_grad)) return FA_ERR_ALIGNMENT;
+    }
   }
   if (!(*scale >= 0.f) || std::isinf(*scale)) return FA_ERR_INVALID_ARG;
   if (*scale == 0.f) *scale = 1.0f / std::sqrt((float)D);
@@ -148,7 +152,7 @@ fa_status check_attn(int32_t B, int32_t H, int64_t q_len, int64_t kv_len, int32_
 }
 
 AttnArgs attn_args(int32_t B, int32_t H, int64_t q_len, int64_t kv_len, int32_t D, const fa_block_mask* bm,
-                   const fa_score_spec* score, float scale, DevMask dm) {
+                   const fa_score_spec* score, float scale, DevMask dm, bool backward) {
   AttnArgs a;
   std::memset(&a, 0, sizeof(a));
   a.B = B;
@@ -173,6 +177,7 @@ AttnArgs attn_args(int32_t B, int32_t H, int64_t q_len, int64_t kv_len, int32_t 
   a.scale = scale;
   a.score_op = score ? score->op : FA_S_NONE;
   a.score_param = score ? score->param : nullptr;
+  a.param_grad = (backward && score) ? score->param_grad : nullptr;
   a.status = bm->status;
   a.mask = dm;
   a.row_segs = reinterpret_cast<const int4*>(bm->row_segs);
@@ -357,12 +362,12 @@ fa_status fa_forward(const void* q, const void* k, const void* v, int32_t B, int
                      void* out, float* lse, cudaStream_t stream) {
   if (!q || !k || !v || !out || !lse) return FA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned4(lse)) return FA_ERR_ALIGNMENT;
-  fa_status st = check_attn(B, H, q_len, kv_len, D, bm, score, &scale);
+  fa_status st = check_attn(B, H, q_len, kv_len, D, bm, score, &scale, false);
   if (st != FA_OK) return st;
   DevMask dm;
   st = check_mask(&bm->spec, q_len, kv_len, &dm);
   if (st != FA_OK) return st;
-  const AttnArgs a = attn_args(B, H, q_len, kv_len, D, bm, score, scale, dm);
+  const AttnArgs a = attn_args(B, H, q_len, kv_len, D, bm, score, scale, dm, false);
   FwdTensors t{q, k, v, out, lse};
   bool enc_failed = false;
   const cudaError_t e = launch_forward(a, t, stream, &enc_failed);
@@ -388,7 +393,7 @@ fa_status fa_backward(const void* q, const void* k, const void* v, const void* o
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(dout) || !aligned16(dq) ||
       !aligned16(dk) || !aligned16(dv) || !aligned16(workspace) || !aligned4(lse))
     return FA_ERR_ALIGNMENT;
-  fa_status st = check_attn(B, H, q_len, kv_len, D, bm, score, &scale);
+  fa_status st = check_attn(B, H, q_len, kv_len, D, bm, score, &scale, true);
   if (st != FA_OK) return st;
   size_t need = 0;
   st = fa_backward_workspace_bytes(B, H, q_len, D, &need);
@@ -397,7 +402,7 @@ fa_status fa_backward(const void* q, const void* k, const void* v, const void* o
   DevMask dm;
   st = check_mask(&bm->spec, q_len, kv_len, &dm);
   if (st != FA_OK) return st;
-  const AttnArgs a = attn_args(B, H, q_len, kv_len, D, bm, score, scale, dm);
+  const AttnArgs a = attn_args(B, H, q_len, kv_len, D, bm, score, scale, dm, true);
   const size_t rows = (size_t)B * H * (size_t)q_len;
   BwdTensors t;
   t.q = q;
@@ -425,7 +430,7 @@ fa_status fa_backward_noalloc(const void* q, const void* k, const void* v, const
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(dout) || !aligned16(dq) ||
       !aligned16(dk) || !aligned16(dv) || !aligned4(lse))
     return FA_ERR_ALIGNMENT;
-  fa_status st = check_attn(B, H, q_len, kv_len, D, bm, score, &scale);
+  fa_status st = check_attn(B, H, q_len, kv_len, D, bm, score, &scale, true);
   if (st != FA_OK) return st;
   size_t need = 0;
   st = fa_backward_workspace_bytes(B, H, q_len, D, &need);
@@ -436,7 +441,7 @@ fa_status fa_backward_noalloc(const void* q, const void* k, const void* v, const
   if (st != FA_OK) return st;
   void* scratch = nullptr;
   if (noalloc_scratch(&scratch) != cudaSuccess) return FA_ERR_CUDA;
-  const AttnArgs a = attn_args(B, H, q_len, kv_len, D, bm, score, scale, dm);
+  const AttnArgs a = attn_args(B, H, q_len, kv_len, D, bm, score, scale, dm, true);
   const size_t rows = (size_t)B * H * (size_t)q_len;
   BwdTensors t;
   t.q = q;

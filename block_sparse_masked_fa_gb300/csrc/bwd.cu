@@ -165,7 +165,7 @@ __device__ __forceinline__ int next_live(const AttnArgs& p, int k, int items, Bw
   return k;
 }
 
-template <int D, int SCORE>
+template <int D, int SCORE, bool PGRAD>
 __global__ void __launch_bounds__(512, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -621,6 +621,7 @@ __global__ void __launch_bounds__(512, 1)
       float slope_l2 = 0.f;
       if constexpr (SCORE == FA_S_ALIBI) slope_l2 = __ldg(p.score_param + cur.h) * kLog2e;
       const bool row_ok = j < p.kv_len;
+      float2 pacc = make_float2(0.f, 0.f);  // PGRAD: this thread's share of dL/dslope[h] in this item
       for (int s = 0; s < n; ++s, ++g) {
         // collective per half: this step's stats are in place, and every wait of
         // the last step succeeded for all of the half (a failed wait is acted on
@@ -733,17 +734,38 @@ __global__ void __launch_bounds__(512, 1)
             const float2 dsv = mul2(make_float2(pg[32 * c2 + e], pg[32 * c2 + e + 1]),
                                     add2(make_float2(dp[e], dp[e + 1]), nd));
             dk[e / 2] = pack_bf16x2(dsv.x, dsv.y);
+            if constexpr (PGRAD) {  // kept for the slope gradient below
+              pg[32 * c2 + e] = dsv.x;
+              pg[32 * c2 + e + 1] = dsv.y;
+            }
           }
           store_row32(sDS, r, c, dk);
         }
         fence_proxy_async_smem();
         tc_fence_before();
         mbar_arrive(b_pb);
+        if constexpr (PGRAD) {
+          // dL/dslope += dS * ds/dslope, ds/dslope = -(i - j) = j - i, once dS is
+          // handed over (the dQ MMA does not wait for it)
+          const float jb = (float)(j - (I * 128 + 64 * half));  // j - i of this half's first column (exact)
+#pragma unroll
+          for (int e = 0; e < 64; e += 2)
+            pacc = fma2(make_float2(pg[e], pg[e + 1]), make_float2(jb - (float)e, jb - (float)(e + 1)), pacc);
+        }
         // every thread of this half is done with this step's stats (and the
         // item's mask arguments): publish the next step's
         named_bar_sync(2 + half, 128);
         if (s + 1 < n || kn < items) reinterpret_cast<float*>(&ctl->stats)[st_idx] = st_next;
         if (s + 1 == n && kn < items && r < p.mask.n) arg_s[r] = node_arg(p.mask, r, nxt_bm);
+      }
+      if constexpr (PGRAD) {
+        // the item's part of dL/dslope[h]: one atomic per warp (ok is uniform per half)
+        if (ok) {
+          float sum = pacc.x + pacc.y;
+#pragma unroll
+          for (int d = 16; d >= 1; d >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, d);
+          if (lane == 0 && sum != 0.f) atomicAdd(p.param_grad + cur.h, sum);
+        }
       }
       k = kn;
     }
@@ -755,13 +777,17 @@ __global__ void __launch_bounds__(512, 1)
 
 // Per query row: -LSE * log2(e) and -Delta (Delta_i = dO_i . out_i, fp32)
 // into the per-tile stats array [B*H][nq][2][128], zero for the rows past
-// q_len in the last tile; and the fp32 dq accumulator rows set to zero.
+// q_len in the last tile; the fp32 dq accumulator rows and the score
+// parameter's gradient (if requested) set to zero.
 // 16 threads per row, 16 rows per 256-thread block.
 template <int D>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __restrict__ out,
                                                       const __nv_bfloat16* __restrict__ dout,
                                                       const float* __restrict__ lse, float* __restrict__ stats,
-                                                      float* __restrict__ dq_acc, int64_t rows, int q_len, int nq) {
+                                                      float* __restrict__ dq_acc, int64_t rows, int q_len, int nq,
+                                                      float* __restrict__ param_grad, int n_param_grad) {
+  if (blockIdx.x == 0)  // the main kernel adds into it
+    for (int k = threadIdx.x; k < n_param_grad; k += blockDim.x) param_grad[k] = 0.f;
   constexpr int E = D / 16;  // elements per thread
   const int64_t row = (int64_t)blockIdx.x * 16 + threadIdx.x / 16;
   const int t = threadIdx.x % 16;
@@ -808,13 +834,13 @@ __global__ void __launch_bounds__(256) bwd_dq_convert_kernel(const float* __rest
   reinterpret_cast<uint4*>(dq)[k] = o;
 }
 
-template <int D, int SCORE>
+template <int D, int SCORE, bool PGRAD>
 cudaError_t launch_bwd_t(const AttnArgs& a, const BwdTensors& t, cudaStream_t stream, bool* enc_failed) {
   const uint64_t bh = (uint64_t)a.B * a.H;
   const int64_t rows = (int64_t)bh * a.q_len;
   bwd_pre_kernel<D><<<(unsigned)((rows + 15) / 16), 256, 0, stream>>>(
       static_cast<const __nv_bfloat16*>(t.out), static_cast<const __nv_bfloat16*>(t.dout), t.lse, t.stats, t.dq_acc,
-      rows, a.q_len, a.nq);
+      rows, a.q_len, a.nq, a.param_grad, PGRAD ? a.H : 0);
 
   CUtensorMap mq, mk, mv, mdo, mdk, mdv;
   auto enc = [&](CUtensorMap* m, const void* ptr, int64_t len, uint32_t rows) {
@@ -833,7 +859,8 @@ cudaError_t launch_bwd_t(const AttnArgs& a, const BwdTensors& t, cudaStream_t st
   constexpr size_t smem = bwd_smem_bytes<D>();
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(bwd_kernel<D, SCORE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e =
+        cudaFuncSetAttribute(bwd_kernel<D, SCORE, PGRAD>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
@@ -846,7 +873,7 @@ cudaError_t launch_bwd_t(const AttnArgs& a, const BwdTensors& t, cudaStream_t st
   if (items >= ((int64_t)1 << 31)) return cudaErrorInvalidValue;
   const unsigned grid = (unsigned)std::min<int64_t>(items, sms);
   if (grid > 0)
-    bwd_kernel<D, SCORE><<<grid, BwdCfg<D>::THREADS, smem, stream>>>(
+    bwd_kernel<D, SCORE, PGRAD><<<grid, BwdCfg<D>::THREADS, smem, stream>>>(
         mq, mk, mv, mdo, mdk, mdv, mdq, a, t.stats);
   const int64_t n8 = rows * D / 8;
   bwd_dq_convert_kernel<<<(unsigned)((n8 + 255) / 256), 256, 0, stream>>>(
@@ -886,14 +913,17 @@ cudaError_t noalloc_scratch(void** ptr) {
 
 cudaError_t launch_backward(const AttnArgs& a, const BwdTensors& t, cudaStream_t stream, bool* enc_failed) {
   *enc_failed = false;
+  const bool pgrad = a.score_op == FA_S_ALIBI && a.param_grad != nullptr;  // learned ALiBi slopes
   if (a.D == 64) {
-    if (a.score_op == FA_S_SOFTCAP) return launch_bwd_t<64, FA_S_SOFTCAP>(a, t, stream, enc_failed);
-    if (a.score_op == FA_S_ALIBI) return launch_bwd_t<64, FA_S_ALIBI>(a, t, stream, enc_failed);
-    return launch_bwd_t<64, FA_S_NONE>(a, t, stream, enc_failed);
+    if (a.score_op == FA_S_SOFTCAP) return launch_bwd_t<64, FA_S_SOFTCAP, false>(a, t, stream, enc_failed);
+    if (pgrad) return launch_bwd_t<64, FA_S_ALIBI, true>(a, t, stream, enc_failed);
+    if (a.score_op == FA_S_ALIBI) return launch_bwd_t<64, FA_S_ALIBI, false>(a, t, stream, enc_failed);
+    return launch_bwd_t<64, FA_S_NONE, false>(a, t, stream, enc_failed);
   }
-  if (a.score_op == FA_S_SOFTCAP) return launch_bwd_t<128, FA_S_SOFTCAP>(a, t, stream, enc_failed);
-  if (a.score_op == FA_S_ALIBI) return launch_bwd_t<128, FA_S_ALIBI>(a, t, stream, enc_failed);
-  return launch_bwd_t<128, FA_S_NONE>(a, t, stream, enc_failed);
+  if (a.score_op == FA_S_SOFTCAP) return launch_bwd_t<128, FA_S_SOFTCAP, false>(a, t, stream, enc_failed);
+  if (pgrad) return launch_bwd_t<128, FA_S_ALIBI, true>(a, t, stream, enc_failed);
+  if (a.score_op == FA_S_ALIBI) return launch_bwd_t<128, FA_S_ALIBI, false>(a, t, stream, enc_failed);
+  return launch_bwd_t<128, FA_S_NONE, false>(a, t, stream, enc_failed);
 }
 
 }  // namespace fa

@@ -59,6 +59,7 @@ struct AttnArgs {
   float scale;
   int32_t score_op;
   const float* score_param;
+  float* param_grad;  // backward only: dL/dslope[H] (ALiBi), or null
   uint32_t* status;
   DevMask mask;
   const int4* row_segs;  // [Bm][2][seg_len]: see fa_block_mask

@@ -115,6 +115,13 @@ typedef enum { FA_S_NONE = 0, FA_S_SOFTCAP = 1, FA_S_ALIBI = 2 } fa_score_op;
 typedef struct {
   int32_t op;          /* fa_score_op */
   const float* param;  /* device pointer, see the table */
+  /* fa_backward / fa_backward_noalloc only (fa_forward ignores it): device fp32
+   * [H] receiving dL/dslope[h] of L = sum(out * dO) for FA_S_ALIBI -- learned
+   * slopes (tutorial Pattern 3: a learned relative-position bias trains
+   * through the fused backward) -- overwritten, not accumulated; or NULL for
+   * no parameter gradient.  Non-NULL with another op: FA_ERR_UNSUPPORTED (the
+   * soft-cap constant is not a learned parameter on the pages). */
+  float* param_grad;
 } fa_score_spec;
 
 /* ------------------------------------------------------------------------

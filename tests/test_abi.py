@@ -202,6 +202,25 @@ def test_backward_workspace_and_rejects():
     assert B._lib.fa_backward(*bad, 1 << 30, None) == UNSUPPORTED
 
 
+def test_score_param_grad_rejects():
+    """A gradient buffer for the score parameter: ALiBi only, 4-byte aligned;
+    the forward ignores it."""
+    bm = _bm()
+    base = [FAKE] * 6 + [1, 1, 1024, 1024, 64, ctypes.byref(bm)]
+    for op, grad, want in ((0, FAKE, UNSUPPORTED), (1, FAKE, UNSUPPORTED), (2, FAKE + 2, ALIGN)):
+        sc = B.ScoreSpec()
+        sc.op, sc.param, sc.param_grad = op, (FAKE if op else None), grad
+        args = base + [ctypes.byref(sc), 0.0] + [FAKE] * 4
+        assert B._lib.fa_backward(*args, 1 << 30, None) == want
+        assert B._lib.fa_backward_noalloc(*(base + [ctypes.byref(sc), 0.0] + [FAKE] * 3), None) == want
+    # op none with a gradient buffer: the backward refuses it at the score check,
+    # the forward passes it and stops at the later scale check instead
+    sc = B.ScoreSpec()
+    sc.param_grad = FAKE
+    assert B._lib.fa_backward(*(base + [ctypes.byref(sc), -1.0] + [FAKE] * 4), 1 << 30, None) == UNSUPPORTED
+    assert _fwd(score=sc, scale=-1.0) == INVALID
+
+
 def test_status_calls_reject_null():
     assert B._lib.fa_get_status(None, 0, None) == INVALID
     counts = (ctypes.c_int64 * 3)()

@@ -224,3 +224,43 @@ def test_every_kernel_instantiation(D, score):
         check_forward(out[0, h].float().cpu().numpy(), lse[0, h].cpu().numpy(), ref_out, ref_lse, f"D{D} {score} h{h}")
         ref = oracle_grads(inp, mask, 0, h, ref_score)
         check_all([g[0, h].float().cpu().numpy() for g in (dq, dk, dv)], ref, f"D{D} {score} h{h}")
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_alibi_slope_gradient(D):
+    """dL/dslope[h] of learned ALiBi slopes (tutorial Pattern 3: a learned
+    relative-position bias trains through the fused backward) against the
+    oracle summed over the batch, on a ragged document + window + sink program.
+    dk and dv are the same bits as without the slope gradient; dq, summed by
+    reduce-adds in no fixed order, agrees to bf16 rounding."""
+    B, H, S = 2, 4, 1900
+    docs = make_doc_ids(("geometric", 400.0), S, 90, batch=B)
+    inp = _inputs(B, H, S, D, 91 + D, docs=docs)
+    mask = P(("causal",), ("same_doc",), ("and",), ("window", 700), ("and",), ("sink", 5), ("or",), ("causal",),
+             ("and",))
+    slopes = make_alibi_slopes(H)
+    score = ("alibi", torch.as_tensor(slopes))
+    q, k, v, do = (inp[n].cuda() for n in ("q", "k", "v", "do"))
+    bm = fa.fa_create_block_mask(device_nodes(mask, docs), B, 1, S, S, 128)
+    out, lse = fa.fa_forward(q, k, v, bm, score=score)
+    g_plain = fa.fa_backward(q, k, v, out, lse, do, bm, score=score)
+    dslope = torch.full((H,), float("nan"), device="cuda")       # overwritten, not accumulated
+    g_slope = fa.fa_backward(q, k, v, out, lse, do, bm, score=score, score_param_grad=dslope)
+    dslope2 = torch.full((H,), 7.0, device="cuda")
+    fa.fa_backward_noalloc(q, k, v, out, lse, do, bm, score=score, score_param_grad=dslope2)
+    torch.cuda.synchronize()
+    assert fa.fa_get_status(bm) == 0
+    assert torch.equal(g_plain[1], g_slope[1]) and torch.equal(g_plain[2], g_slope[2])
+    dq0, dq1 = g_plain[0].float(), g_slope[0].float()
+    assert (dq0 - dq1).abs().max() <= 1e-2 * dq0.abs().max()
+    ref = np.zeros(H)
+    for b in range(B):
+        prog = oracle_program(mask, docs, None, b, B)
+        for h in range(H):
+            ref[h] += oracle.score_param_grad_head(head64(inp["q"], b, h), head64(inp["k"], b, h),
+                                                   head64(inp["v"], b, h), head64(inp["do"], b, h), prog,
+                                                   ("alibi", slopes), h, 1.0 / np.sqrt(D))
+    got = dslope.cpu().numpy().astype(np.float64)
+    assert np.abs(ref).max() > 0
+    check_grad(got, ref, f"dslope D{D}")
+    np.testing.assert_allclose(dslope2.cpu().numpy(), got, rtol=1e-5, atol=1e-6 * np.abs(ref).max())
