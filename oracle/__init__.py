@@ -275,6 +275,29 @@ def backward_head(q, k, v, do, prog: Program, score: tuple, h: int, scale: float
     return dq, dk, dv, lse, delta
 
 
+def paged_gather(pool: np.ndarray, page_table: np.ndarray, kv_len: int, block: int = 128) -> np.ndarray:
+    """Logical keys (or values) of a paged cache (tutorial "FlexAttention in
+    PyTorch", "Decoding and paged KV caches": logical tile indices go through a
+    page table to physical blocks).  pool [H, n_pages * block, D]; page_table
+    [B, nkv]: the page holding logical tile J of batch row b.  Returns
+    [B, H, kv_len, D] with row j of batch b taken from row j mod block of page
+    page_table[b, j // block].  A page index outside [0, n_pages) is an error."""
+    H, rows, D = pool.shape
+    n_pages = rows // block
+    B, nkv = page_table.shape
+    if nkv * block < kv_len:
+        raise ValueError("page table shorter than kv_len")
+    out = np.zeros((B, H, kv_len, D), dtype=pool.dtype)
+    for b in range(B):
+        for J in range(-(-kv_len // block)):
+            page = int(page_table[b, J])
+            if page < 0 or page >= n_pages:
+                raise ValueError(f"batch {b} tile {J}: page {page} outside [0, {n_pages})")
+            n = min(block, kv_len - J * block)
+            out[b, :, J * block:J * block + n] = pool[:, page * block:page * block + n]
+    return out
+
+
 def score_param_grad_head(q, k, v, do, prog: Program, score: tuple, h: int, scale: float) -> float:
     """dL/dparam of L = sum(out * dO) for one head: the soft-cap c, or the ALiBi
     slope of head h (0.0 for a score mod without a parameter)."""

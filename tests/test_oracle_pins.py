@@ -598,3 +598,36 @@ def test_score_param_grad_vanishes_where_out_cannot_move():
     assert abs(g) < 1e-12
     diag = oracle.Program(P(("causal",), ("window", 1), ("and",)))
     assert oracle.score_param_grad_head(q, k, v, do, diag, ("alibi", [0.2]), 0, 0.2) == 0.0
+
+
+# ------------------------------------------------- paged key / value cache
+
+def test_paged_gather_inverts_the_scatter_into_pages():
+    """Write each logical tile of every batch row into the page its table names
+    (pages shuffled across the pool and shared by nothing); the gather gives the
+    logical tensor back, ragged last tile included."""
+    rng = np.random.default_rng(50)
+    B, H, kv_len, D, blk = 3, 2, 300, 8, 64
+    nkv = -(-kv_len // blk)
+    n_pages = B * nkv + 5
+    logical = rng.standard_normal((B, H, kv_len, D))
+    table = rng.permutation(n_pages)[:B * nkv].reshape(B, nkv).astype(np.int32)
+    pool = np.full((H, n_pages * blk, D), 99.0)
+    for b in range(B):
+        for J in range(nkv):
+            n = min(blk, kv_len - J * blk)
+            pool[:, table[b, J] * blk:table[b, J] * blk + n] = logical[b, :, J * blk:J * blk + n]
+    np.testing.assert_array_equal(oracle.paged_gather(pool, table, kv_len, blk), logical)
+
+
+def test_paged_gather_identity_table_and_invalid_pages():
+    pool = np.arange(2 * 6 * 4 * 3, dtype=np.float64).reshape(2, 24, 3)   # H=2, 6 pages of 4 rows
+    ident = np.arange(6, dtype=np.int32)[None]
+    np.testing.assert_array_equal(oracle.paged_gather(pool, ident, 22, 4)[0], pool[:, :22])
+    for bad in (6, -1):
+        t = ident.copy()
+        t[0, 2] = bad
+        with pytest.raises(ValueError):
+            oracle.paged_gather(pool, t, 22, 4)
+    with pytest.raises(ValueError):
+        oracle.paged_gather(pool, ident[:, :5], 22, 4)                       # table too short
