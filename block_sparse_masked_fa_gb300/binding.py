@@ -1,8 +1,9 @@
 """ctypes binding of the C ABI in include/fa.h (argument marshalling only).
 
 Names mirror the C entry points: fa_block_mask_bytes, fa_create_block_mask,
-fa_block_mask_from_kv_blocks, fa_forward, fa_backward_workspace_bytes, fa_backward, fa_get_status,
-fa_block_mask_summary, fa_status_string.  Tensors are torch CUDA tensors; the
+fa_block_mask_from_kv_blocks, fa_forward, fa_forward_paged,
+fa_backward_workspace_bytes, fa_backward, fa_get_status, fa_block_mask_summary,
+fa_status_string.  Tensors are torch CUDA tensors; the
 binding passes their device pointers and the current CUDA stream.  Every step
 of the computation runs in the library's kernels; importing this module fails
 loudly when the library has not been built.
@@ -75,6 +76,9 @@ _lib.fa_block_mask_from_kv_blocks.argtypes = [_c.c_void_p] * 4 + [_c.c_int32, _c
 _lib.fa_forward.argtypes = [_c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_int32, _c.c_int32, _c.c_int64,
                             _c.c_int64, _c.c_int32, _c.POINTER(BlockMaskStruct), _c.POINTER(ScoreSpec),
                             _c.c_float, _c.c_void_p, _c.c_void_p, _c.c_void_p]
+_lib.fa_forward_paged.argtypes = [_c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_int32, _c.c_int32,
+                                  _c.c_int32, _c.c_int64, _c.c_int64, _c.c_int32, _c.POINTER(BlockMaskStruct),
+                                  _c.POINTER(ScoreSpec), _c.c_float, _c.c_void_p, _c.c_void_p, _c.c_void_p]
 _lib.fa_backward_workspace_bytes.argtypes = [_c.c_int32, _c.c_int32, _c.c_int64, _c.c_int32,
                                              _c.POINTER(_c.c_size_t)]
 _lib.fa_backward.argtypes = [_c.c_void_p] * 6 + [_c.c_int32, _c.c_int32, _c.c_int64, _c.c_int64, _c.c_int32,
@@ -89,12 +93,14 @@ _lib.fa_get_status.argtypes = [_c.POINTER(BlockMaskStruct), _c.c_int32, _c.c_voi
 _lib.fa_block_mask_summary.argtypes = [_c.POINTER(BlockMaskStruct), _c.POINTER(_c.c_int64 * 3), _c.c_void_p]
 _lib.fa_status_string.argtypes = [_c.c_int]
 _lib.fa_status_string.restype = _c.c_char_p
-for _f in (_lib.fa_block_mask_bytes, _lib.fa_create_block_mask, _lib.fa_block_mask_from_kv_blocks, _lib.fa_forward, _lib.fa_backward_workspace_bytes,
+for _f in (_lib.fa_block_mask_bytes, _lib.fa_create_block_mask, _lib.fa_block_mask_from_kv_blocks, _lib.fa_forward,
+           _lib.fa_forward_paged, _lib.fa_backward_workspace_bytes,
            _lib.fa_backward, _lib.fa_backward_noalloc, _lib.fa_get_status, _lib.fa_block_mask_summary):
     _f.restype = _c.c_int
 _lib.fa_version.restype = _c.c_int32
 
-EXPORTED = ("fa_block_mask_bytes", "fa_create_block_mask", "fa_block_mask_from_kv_blocks", "fa_forward", "fa_backward_workspace_bytes",
+EXPORTED = ("fa_block_mask_bytes", "fa_create_block_mask", "fa_block_mask_from_kv_blocks", "fa_forward",
+            "fa_forward_paged", "fa_backward_workspace_bytes",
             "fa_backward", "fa_backward_noalloc", "fa_get_status", "fa_block_mask_summary", "fa_status_string",
             "fa_version")
 NOALLOC_SCRATCH_BYTES = 16 << 20
@@ -308,6 +314,30 @@ def _backward_score(score, score_param_grad, H: int):
             raise ValueError("score_param_grad must be a contiguous fp32 CUDA tensor of H elements")
         spec.param_grad = g.data_ptr()
     return spec, keep + [sspec]
+
+
+def fa_forward_paged(q, k_pool, v_pool, page_table, block_mask: BlockMask, score=None, scale: float = 0.0, out=None,
+                     lse=None, stream=None):
+    """Forward over paged keys / values: k_pool, v_pool bf16 [H, n_pages * 128, D],
+    page_table int32 [B, nkv] (page of each logical key tile).  out, lse as fa_forward."""
+    B, H, q_len, D = q.shape
+    kv_len = block_mask.struct.kv_len
+    nkv = -(-kv_len // 128)
+    if k_pool.dim() != 3 or k_pool.shape != v_pool.shape or k_pool.shape[0] != H or k_pool.shape[2] != D \
+            or k_pool.shape[1] % 128 != 0:
+        raise ValueError("k_pool / v_pool must be [H, n_pages * 128, D]")
+    if page_table.dtype != torch.int32 or not page_table.is_cuda or not page_table.is_contiguous() \
+            or tuple(page_table.shape) != (B, nkv):
+        raise ValueError(f"page_table must be a contiguous int32 CUDA tensor [B, {nkv}]")
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty(B, H, q_len, dtype=torch.float32, device=q.device)
+    sspec, keep = _score(score)
+    _check(_lib.fa_forward_paged(_ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(page_table), k_pool.shape[1] // 128, B, H,
+                                 q_len, kv_len, D, ctypes.byref(block_mask.struct), ctypes.byref(sspec), float(scale),
+                                 _ptr(out), _ptr(lse), _stream(stream)), "fa_forward_paged")
+    return out, lse
 
 
 def fa_backward_workspace_bytes(B: int, H: int, q_len: int, D: int) -> int:

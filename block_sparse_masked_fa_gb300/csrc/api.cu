@@ -360,14 +360,26 @@ fa_status fa_block_mask_from_kv_blocks(const int32_t* kv_num_blocks, const int32
 fa_status fa_forward(const void* q, const void* k, const void* v, int32_t B, int32_t H, int64_t q_len,
                      int64_t kv_len, int32_t D, const fa_block_mask* bm, const fa_score_spec* score, float scale,
                      void* out, float* lse, cudaStream_t stream) {
+  return fa_forward_paged(q, k, v, nullptr, 0, B, H, q_len, kv_len, D, bm, score, scale, out, lse, stream);
+}
+
+fa_status fa_forward_paged(const void* q, const void* k, const void* v, const int32_t* page_table, int32_t n_pages,
+                           int32_t B, int32_t H, int64_t q_len, int64_t kv_len, int32_t D, const fa_block_mask* bm,
+                           const fa_score_spec* score, float scale, void* out, float* lse, cudaStream_t stream) {
   if (!q || !k || !v || !out || !lse) return FA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned4(lse)) return FA_ERR_ALIGNMENT;
+  if (page_table != nullptr) {  // fa_forward passes none
+    if (!aligned4(page_table)) return FA_ERR_ALIGNMENT;
+    if (n_pages < 1 || (int64_t)n_pages * 128 > (int64_t)INT32_MAX) return FA_ERR_SHAPE;
+  }
   fa_status st = check_attn(B, H, q_len, kv_len, D, bm, score, &scale, false);
   if (st != FA_OK) return st;
   DevMask dm;
   st = check_mask(&bm->spec, q_len, kv_len, &dm);
   if (st != FA_OK) return st;
-  const AttnArgs a = attn_args(B, H, q_len, kv_len, D, bm, score, scale, dm, false);
+  AttnArgs a = attn_args(B, H, q_len, kv_len, D, bm, score, scale, dm, false);
+  a.page_table = page_table;
+  a.n_pages = page_table != nullptr ? n_pages : 0;
   FwdTensors t{q, k, v, out, lse};
   bool enc_failed = false;
   const cudaError_t e = launch_forward(a, t, stream, &enc_failed);

@@ -247,6 +247,18 @@ __global__ void __launch_bounds__(192, 2)
       q_issued = u + 1;
       for (int jj = 0; ok && jj < cur.n; ++jj, ++t) {
         const int J = jj == 0 ? cur.J0 : tile_of(p, cur, jj);
+        // rows of key tile J: in the caller's [B*H][kv_len] tensors, or (paged)
+        // in the page the table names, of this head's [n_pages * 128] pool rows
+        int kv_row = J * 128, kv_z = cur.bh;
+        if (p.page_table != nullptr && lane == 0) {
+          int page = __ldg(p.page_table + (int64_t)(cur.bh / p.H) * p.nkv + J);
+          if (page < 0 || page >= p.n_pages) {  // reported; page 0 is read instead
+            atomicOr(p.status, kStatusCheck);
+            page = 0;
+          }
+          kv_row = page * 128;
+          kv_z = cur.h;
+        }
         for (int kv = 0; kv < 2; ++kv) {
           const int pos = 2 * t + kv, slot = pos % C::NS, use = pos / C::NS;
           if (use > 0 && !warp_wait(smem_u32(&ctl->kv_empty[slot]), (use - 1) & 1, &ctl->abort)) {
@@ -262,7 +274,7 @@ __global__ void __launch_bounds__(192, 2)
             mbar_arrive_expect_tx(bar, C::TILE);
             const CUtensorMap* m = kv ? &tm_v : &tm_k;
             for (int c = 0; c < C::NC; ++c)
-              tma_load_3d(smem_u32(sKV + slot * C::TILE + c * 16384), m, bar, c * 64, J * 128, cur.bh);
+              tma_load_3d(smem_u32(sKV + slot * C::TILE + c * 16384), m, bar, c * 64, kv_row, kv_z);
           }
           issued = pos + 1;
         }
@@ -651,12 +663,16 @@ __global__ void __launch_bounds__(192, 2)
 template <int D, int SCORE>
 cudaError_t launch_fwd_t(const AttnArgs& a, const FwdTensors& t, cudaStream_t stream, bool* enc_failed) {
   const uint64_t bh = (uint64_t)a.B * a.H;
+  // keys / values: [B*H][kv_len][D], or the paged pools [H][n_pages * 128][D]
+  const bool paged = a.page_table != nullptr;
+  const uint64_t kv_rows = paged ? (uint64_t)a.n_pages * 128 : (uint64_t)a.kv_len;
+  const uint64_t kv_z = paged ? (uint64_t)a.H : bh;
   CUtensorMap mq, mk, mv, mo;
   const bool ok = encode_tmap_3d(&mq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, t.q, D, a.q_len, bh, 64, 128,
                                  CU_TENSOR_MAP_SWIZZLE_128B) &&
-                  encode_tmap_3d(&mk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, t.k, D, a.kv_len, bh, 64, 128,
+                  encode_tmap_3d(&mk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, t.k, D, kv_rows, kv_z, 64, 128,
                                  CU_TENSOR_MAP_SWIZZLE_128B) &&
-                  encode_tmap_3d(&mv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, t.v, D, a.kv_len, bh, 64, 128,
+                  encode_tmap_3d(&mv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, t.v, D, kv_rows, kv_z, 64, 128,
                                  CU_TENSOR_MAP_SWIZZLE_128B) &&
                   encode_tmap_3d(&mo, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, t.out, D, a.q_len, bh, 64, 128,
                                  CU_TENSOR_MAP_SWIZZLE_128B);

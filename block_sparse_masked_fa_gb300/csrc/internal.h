@@ -60,6 +60,10 @@ struct AttnArgs {
   int32_t score_op;
   const float* score_param;
   float* param_grad;  // backward only: dL/dslope[H] (ALiBi), or null
+  // forward only: paged keys / values -- page of logical key tile J of batch b
+  // at page_table[b * nkv + J], pages of 128 rows in [H][n_pages * 128][D] pools; or null
+  const int32_t* page_table;
+  int32_t n_pages;
   uint32_t* status;
   DevMask mask;
   const int4* row_segs;  // [Bm][2][seg_len]: see fa_block_mask

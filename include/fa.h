@@ -247,6 +247,28 @@ fa_status fa_forward(const void* q, const void* k, const void* v, int32_t B, int
                      int64_t kv_len, int32_t D, const fa_block_mask* bm, const fa_score_spec* score, float scale,
                      void* out, float* lse, cudaStream_t stream);
 
+/* Forward over a paged key / value cache (tutorial "FlexAttention in
+ * PyTorch", "Decoding and paged KV caches": the logical tile indices go
+ * through a page table to physical blocks, so any mask works on a paged cache
+ * without a kernel per variant).  Computes exactly what fa_forward computes on
+ * the logical keys and values
+ *   k[b][h][j] = k_pool[h][128 * page_table[b][j / 128] + j % 128]   (v alike).
+ *   k_pool, v_pool  bf16 [H][n_pages * 128][D], 16-byte aligned; a page holds
+ *                   128 rows of every head
+ *   page_table      device int32 [B][bm->nkv]: page of each logical key tile,
+ *                   4-byte aligned; a page may serve several tiles or batch rows
+ *   n_pages         pages in the pools, 1 .. (2^31 - 1) / 128
+ * The block mask is built on logical positions (q_len, kv_len).  Rows of the
+ * last key tile's page past kv_len are read and masked out; they must hold
+ * finite values (their weight is 0, but 0 * NaN is NaN).  A page index outside
+ * [0, n_pages) sets the status word's check bit (FA_ERR_DEVICE_CHECK from
+ * fa_get_status) and page 0 is read in its place.  Other arguments, results
+ * and errors as fa_forward; there is no paged backward. */
+fa_status fa_forward_paged(const void* q, const void* k_pool, const void* v_pool, const int32_t* page_table,
+                           int32_t n_pages, int32_t B, int32_t H, int64_t q_len, int64_t kv_len, int32_t D,
+                           const fa_block_mask* bm, const fa_score_spec* score, float scale, void* out, float* lse,
+                           cudaStream_t stream);
+
 /* Device workspace fa_backward needs: an fp32 dq accumulator
  * (B*H*q_len*D floats) and, per 128-row query tile, the rows' LSE and
  * sum(dO * out) (B*H*ceil(q_len/128)*256 floats), each 256-byte aligned. */

@@ -202,6 +202,21 @@ def test_backward_workspace_and_rejects():
     assert B._lib.fa_backward(*bad, 1 << 30, None) == UNSUPPORTED
 
 
+def test_forward_paged_rejects():
+    """Host-side errors of the paged forward, before any GPU work."""
+    bm = _bm()
+    sc = B.ScoreSpec()
+
+    def call(table=FAKE, n_pages=16, q=FAKE, scale=0.0):
+        return B._lib.fa_forward_paged(q, FAKE, FAKE, table, n_pages, 1, 1, 1024, 1024, 64, ctypes.byref(bm),
+                                       ctypes.byref(sc), scale, FAKE, FAKE, None)
+    assert call(q=None) == INVALID
+    assert call(table=FAKE + 2) == ALIGN
+    assert call(n_pages=0) == SHAPE
+    assert call(n_pages=1 << 24) == SHAPE                  # pool rows past 2^31
+    assert call(scale=-1.0) == INVALID                     # then the checks of fa_forward
+
+
 def test_score_param_grad_rejects():
     """A gradient buffer for the score parameter: ALiBi only, 4-byte aligned;
     the forward ignores it."""
