@@ -17,6 +17,8 @@ from .binding import (  # noqa: F401
     fa_block_mask_summary,
     fa_create_block_mask,
     fa_forward,
+    fa_forward_decode,
+    fa_forward_decode_workspace_bytes,
     fa_forward_paged,
     fa_get_status,
     fa_status_string,

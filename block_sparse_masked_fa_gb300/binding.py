@@ -2,9 +2,10 @@
 
 Names mirror the C entry points: fa_block_mask_bytes, fa_create_block_mask,
 fa_block_mask_from_kv_blocks, fa_forward, fa_forward_paged,
+fa_forward_decode_workspace_bytes, fa_forward_decode,
 fa_backward_workspace_bytes, fa_backward, fa_get_status, fa_block_mask_summary,
-fa_status_string.  Tensors are torch CUDA tensors; the
-binding passes their device pointers and the current CUDA stream.  Every step
+fa_status_string.  Tensors are torch CUDA tensors; the binding passes their
+device pointers and the current CUDA stream.  Every step
 of the computation runs in the library's kernels; importing this module fails
 loudly when the library has not been built.
 """
@@ -79,6 +80,12 @@ _lib.fa_forward.argtypes = [_c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_int32, _
 _lib.fa_forward_paged.argtypes = [_c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_int32, _c.c_int32,
                                   _c.c_int32, _c.c_int64, _c.c_int64, _c.c_int32, _c.POINTER(BlockMaskStruct),
                                   _c.POINTER(ScoreSpec), _c.c_float, _c.c_void_p, _c.c_void_p, _c.c_void_p]
+_lib.fa_forward_decode_workspace_bytes.argtypes = [_c.c_int32, _c.c_int32, _c.c_int64, _c.c_int64, _c.c_int32,
+                                                   _c.POINTER(_c.c_size_t)]
+_lib.fa_forward_decode.argtypes = [_c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_int32, _c.c_int32,
+                                   _c.c_int32, _c.c_int64, _c.c_int64, _c.c_int32, _c.POINTER(BlockMaskStruct),
+                                   _c.POINTER(ScoreSpec), _c.c_float, _c.c_void_p, _c.c_void_p, _c.c_void_p,
+                                   _c.c_size_t, _c.c_void_p]
 _lib.fa_backward_workspace_bytes.argtypes = [_c.c_int32, _c.c_int32, _c.c_int64, _c.c_int32,
                                              _c.POINTER(_c.c_size_t)]
 _lib.fa_backward.argtypes = [_c.c_void_p] * 6 + [_c.c_int32, _c.c_int32, _c.c_int64, _c.c_int64, _c.c_int32,
@@ -94,13 +101,13 @@ _lib.fa_block_mask_summary.argtypes = [_c.POINTER(BlockMaskStruct), _c.POINTER(_
 _lib.fa_status_string.argtypes = [_c.c_int]
 _lib.fa_status_string.restype = _c.c_char_p
 for _f in (_lib.fa_block_mask_bytes, _lib.fa_create_block_mask, _lib.fa_block_mask_from_kv_blocks, _lib.fa_forward,
-           _lib.fa_forward_paged, _lib.fa_backward_workspace_bytes,
+           _lib.fa_forward_paged, _lib.fa_forward_decode_workspace_bytes, _lib.fa_forward_decode, _lib.fa_backward_workspace_bytes,
            _lib.fa_backward, _lib.fa_backward_noalloc, _lib.fa_get_status, _lib.fa_block_mask_summary):
     _f.restype = _c.c_int
 _lib.fa_version.restype = _c.c_int32
 
 EXPORTED = ("fa_block_mask_bytes", "fa_create_block_mask", "fa_block_mask_from_kv_blocks", "fa_forward",
-            "fa_forward_paged", "fa_backward_workspace_bytes",
+            "fa_forward_paged", "fa_forward_decode_workspace_bytes", "fa_forward_decode", "fa_backward_workspace_bytes",
             "fa_backward", "fa_backward_noalloc", "fa_get_status", "fa_block_mask_summary", "fa_status_string",
             "fa_version")
 NOALLOC_SCRATCH_BYTES = 16 << 20
@@ -337,6 +344,45 @@ def fa_forward_paged(q, k_pool, v_pool, page_table, block_mask: BlockMask, score
     _check(_lib.fa_forward_paged(_ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(page_table), k_pool.shape[1] // 128, B, H,
                                  q_len, kv_len, D, ctypes.byref(block_mask.struct), ctypes.byref(sspec), float(scale),
                                  _ptr(out), _ptr(lse), _stream(stream)), "fa_forward_paged")
+    return out, lse
+
+
+DECODE_MAX_Q = 16
+
+
+def fa_forward_decode_workspace_bytes(B: int, H: int, q_len: int, kv_len: int, D: int) -> int:
+    n = ctypes.c_size_t()
+    _check(_lib.fa_forward_decode_workspace_bytes(B, H, q_len, kv_len, D, ctypes.byref(n)),
+           "fa_forward_decode_workspace_bytes")
+    return n.value
+
+
+def fa_forward_decode(q, k, v, block_mask: BlockMask, score=None, scale: float = 0.0, page_table=None, out=None,
+                      lse=None, workspace=None, stream=None):
+    """Short-query forward (q_len <= 16): k, v [B, H, kv_len, D]; or, with an
+    int32 page_table [B, nkv], pools [H, n_pages * 128, D].  out, lse as fa_forward."""
+    B, H, q_len, D = q.shape
+    kv_len = block_mask.struct.kv_len
+    n_pages = 0
+    if page_table is not None:
+        if page_table.dtype != torch.int32 or not page_table.is_cuda or not page_table.is_contiguous() \
+                or tuple(page_table.shape) != (B, -(-kv_len // 128)):
+            raise ValueError("page_table must be a contiguous int32 CUDA tensor [B, nkv]")
+        if k.dim() != 3 or k.shape[1] % 128 != 0:
+            raise ValueError("paged k / v must be [H, n_pages * 128, D]")
+        n_pages = k.shape[1] // 128
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty(B, H, q_len, dtype=torch.float32, device=q.device)
+    if workspace is None:
+        workspace = torch.empty(fa_forward_decode_workspace_bytes(B, H, q_len, kv_len, D), dtype=torch.uint8,
+                                device=q.device)
+    sspec, keep = _score(score)
+    _check(_lib.fa_forward_decode(_ptr(q), _ptr(k), _ptr(v), _ptr(page_table), n_pages, B, H, q_len, kv_len, D,
+                                  ctypes.byref(block_mask.struct), ctypes.byref(sspec), float(scale), _ptr(out),
+                                  _ptr(lse), _ptr(workspace), workspace.numel(), _stream(stream)),
+           "fa_forward_decode")
     return out, lse
 
 

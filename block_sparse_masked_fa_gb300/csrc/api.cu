@@ -387,6 +387,50 @@ fa_status fa_forward_paged(const void* q, const void* k, const void* v, const in
   return cuda_status(e);
 }
 
+fa_status fa_forward_decode_workspace_bytes(int32_t B, int32_t H, int64_t q_len, int64_t kv_len, int32_t D,
+                                            size_t* bytes) {
+  if (bytes == nullptr) return FA_ERR_INVALID_ARG;
+  if (B < 1 || H < 1 || q_len < 1 || kv_len < 1) return FA_ERR_SHAPE;
+  if (q_len > FA_DECODE_MAX_Q || (D != 64 && D != 128)) return FA_ERR_UNSUPPORTED;
+  if ((int64_t)B * H > (int64_t)INT32_MAX / FA_DECODE_MAX_Q || kv_len > (int64_t)INT32_MAX - 256) return FA_ERR_SHAPE;
+  int splits = 0;
+  size_t need = 0;
+  if (decode_plan(B, H, q_len, kv_len, D, &splits, &need) != cudaSuccess) return FA_ERR_CUDA;
+  *bytes = need;
+  return FA_OK;
+}
+
+fa_status fa_forward_decode(const void* q, const void* k, const void* v, const int32_t* page_table, int32_t n_pages,
+                            int32_t B, int32_t H, int64_t q_len, int64_t kv_len, int32_t D, const fa_block_mask* bm,
+                            const fa_score_spec* score, float scale, void* out, float* lse, void* workspace,
+                            size_t workspace_bytes, cudaStream_t stream) {
+  if (!q || !k || !v || !out || !lse || !workspace) return FA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned4(lse) || !aligned16(workspace))
+    return FA_ERR_ALIGNMENT;
+  if (page_table != nullptr) {
+    if (!aligned4(page_table)) return FA_ERR_ALIGNMENT;
+    if (n_pages < 1 || (int64_t)n_pages * 128 > (int64_t)INT32_MAX) return FA_ERR_SHAPE;
+  }
+  if (q_len < 1 || q_len > FA_DECODE_MAX_Q) return q_len < 1 ? FA_ERR_SHAPE : FA_ERR_UNSUPPORTED;
+  fa_status st = check_attn(B, H, q_len, kv_len, D, bm, score, &scale, false);
+  if (st != FA_OK) return st;
+  size_t need = 0;
+  int splits = 0;
+  if (decode_plan(B, H, q_len, kv_len, D, &splits, &need) != cudaSuccess) return FA_ERR_CUDA;
+  if (workspace_bytes < need) return FA_ERR_WORKSPACE;
+  DevMask dm;
+  st = check_mask(&bm->spec, q_len, kv_len, &dm);
+  if (st != FA_OK) return st;
+  AttnArgs a = attn_args(B, H, q_len, kv_len, D, bm, score, scale, dm, false);
+  a.page_table = page_table;
+  a.n_pages = page_table != nullptr ? n_pages : 0;
+  FwdTensors t{q, k, v, out, lse};
+  bool enc_failed = false;
+  const cudaError_t e = launch_decode(a, t, workspace, splits, stream, &enc_failed);
+  if (enc_failed) return FA_ERR_CUDA;
+  return cuda_status(e);
+}
+
 fa_status fa_backward_workspace_bytes(int32_t B, int32_t H, int64_t q_len, int32_t D, size_t* bytes) {
   if (bytes == nullptr) return FA_ERR_INVALID_ARG;
   if (B < 1 || H < 1 || q_len < 1) return FA_ERR_SHAPE;

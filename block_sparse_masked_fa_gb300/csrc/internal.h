@@ -89,6 +89,14 @@ struct BwdTensors {
 cudaError_t launch_forward(const AttnArgs& a, const FwdTensors& t, cudaStream_t stream, bool* enc_failed);
 cudaError_t launch_backward(const AttnArgs& a, const BwdTensors& t, cudaStream_t stream, bool* enc_failed);
 
+// Short-query forward: the split of every (b, h)'s key tiles over CTAs on the
+// current device and the workspace it needs (partial out and LSE per split),
+// and the launch (decode_partial_kernel, then decode_combine_kernel).
+cudaError_t decode_plan(int32_t B, int32_t H, int64_t q_len, int64_t kv_len, int32_t D, int* splits,
+                        size_t* ws_bytes);
+cudaError_t launch_decode(const AttnArgs& a, const FwdTensors& t, void* workspace, int splits, cudaStream_t stream,
+                          bool* enc_failed);
+
 // Device address (current device) of the library-owned scratch of fa_backward_noalloc.
 cudaError_t noalloc_scratch(void** ptr);
 

@@ -269,6 +269,33 @@ fa_status fa_forward_paged(const void* q, const void* k_pool, const void* v_pool
                            const fa_block_mask* bm, const fa_score_spec* score, float scale, void* out, float* lse,
                            cudaStream_t stream);
 
+/* ------------------------------------------------------------------------
+ * Short-query forward (tutorial "FlexAttention in PyTorch", "Decoding and
+ * paged KV caches": a dedicated decoding path optimised for short queries).
+ * Computes what fa_forward or fa_forward_paged computes, for q_len up to
+ * FA_DECODE_MAX_Q, with the listed key tiles of every (b, h) split over
+ * several CTAs and the shares merged by their LSE.
+ * ---------------------------------------------------------------------- */
+#define FA_DECODE_MAX_Q 16
+
+/* Workspace fa_forward_decode needs on the current device (fp32 partial
+ * results of every share: splits * B * H * q_len * (D + 1) floats).
+ * q_len in [1, FA_DECODE_MAX_Q] (else FA_ERR_UNSUPPORTED); D 64 or 128. */
+fa_status fa_forward_decode_workspace_bytes(int32_t B, int32_t H, int64_t q_len, int64_t kv_len, int32_t D,
+                                            size_t* bytes);
+
+/* The short-query forward: out and LSE exactly as fa_forward (page_table =
+ * NULL, k / v [B][H][kv_len][D]) or fa_forward_paged (page_table != NULL,
+ * k / v pools [H][n_pages * 128][D]) define them, for q_len <= FA_DECODE_MAX_Q
+ * (bm built for this q_len, so nq = 1).  Keys past kv_len are never read.
+ * workspace: device memory of fa_forward_decode_workspace_bytes() bytes,
+ * 16-byte aligned, caller-owned (FA_ERR_WORKSPACE when smaller).  Queues two
+ * kernels on `stream`; errors as fa_forward / fa_forward_paged. */
+fa_status fa_forward_decode(const void* q, const void* k, const void* v, const int32_t* page_table, int32_t n_pages,
+                            int32_t B, int32_t H, int64_t q_len, int64_t kv_len, int32_t D, const fa_block_mask* bm,
+                            const fa_score_spec* score, float scale, void* out, float* lse, void* workspace,
+                            size_t workspace_bytes, cudaStream_t stream);
+
 /* Device workspace fa_backward needs: an fp32 dq accumulator
  * (B*H*q_len*D floats) and, per 128-row query tile, the rows' LSE and
  * sum(dO * out) (B*H*ceil(q_len/128)*256 floats), each 256-byte aligned. */

@@ -217,6 +217,27 @@ def test_forward_paged_rejects():
     assert call(scale=-1.0) == INVALID                     # then the checks of fa_forward
 
 
+def test_forward_decode_rejects():
+    """Host-side errors of the short-query forward, before any device query."""
+    bm = _bm(q=1)
+    sc = B.ScoreSpec()
+
+    def call(q_len=1, table=None, n_pages=0, ws=FAKE, q=FAKE):
+        return B._lib.fa_forward_decode(q, FAKE, FAKE, table, n_pages, 1, 1, q_len, 1024, 64, ctypes.byref(bm),
+                                        ctypes.byref(sc), 0.0, FAKE, FAKE, ws, 1 << 30, None)
+    assert call(q_len=17) == UNSUPPORTED
+    assert call(q_len=0) == SHAPE
+    assert call(ws=None) == INVALID
+    assert call(ws=FAKE + 8) == ALIGN
+    assert call(q=None) == INVALID
+    assert call(table=FAKE + 2, n_pages=4) == ALIGN
+    assert call(table=FAKE, n_pages=0) == SHAPE
+    n = ctypes.c_size_t()
+    assert B._lib.fa_forward_decode_workspace_bytes(1, 1, 17, 1024, 64, ctypes.byref(n)) == UNSUPPORTED
+    assert B._lib.fa_forward_decode_workspace_bytes(1, 1, 1, 1024, 80, ctypes.byref(n)) == UNSUPPORTED
+    assert B._lib.fa_forward_decode_workspace_bytes(1, 1, 1, 1024, 64, None) == INVALID
+
+
 def test_score_param_grad_rejects():
     """A gradient buffer for the score parameter: ALiBi only, 4-byte aligned;
     the forward ignores it."""
