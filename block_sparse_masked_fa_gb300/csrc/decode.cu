@@ -7,18 +7,19 @@
 // tiles of every (b, h) are split over several CTAs (split-KV) so that a small
 // batch still keeps every SM loading:
 //
-//  decode_partial_kernel  grid (splits, B*H), 256 threads.  Its share of the
-//      (b, h)'s listed key tiles (FULL ones first, then PARTIAL, as the
-//      forward), three K / V stages loaded by thread 0 with the forward's
-//      swizzled TMA maps (so a paged pool works the same way).  Per tile:
-//      scores with two threads per key row, each over half of the head dim
-//      (the 128-byte swizzle makes the row reads conflict-free; q is read as
-//      a broadcast), the mask on PARTIAL tiles (row intervals, else the
-//      program) and the score mod; an online softmax per query row (a warp
-//      per row); P V with a column pair per thread over a group of keys, the
-//      groups added after the last tile.  Keys past kv_len are never read, so
-//      the rows of a last page past kv_len do not matter.  Writes the share's
-//      out (normalised) and LSE to the workspace.
+//  decode_partial_kernel  grid (splits, B*H), 8 compute warps and a loader
+//      warp.  Its share of the (b, h)'s listed key tiles (FULL ones first,
+//      then PARTIAL, as the forward), three K / V stages loaded by TMA with
+//      the forward's swizzled maps (so a paged pool works the same way) and
+//      released by the compute warps through mbarriers.  Each compute warp
+//      owns 16 keys of every tile and runs on its own: scores with a lane
+//      pair per key (half of the head dim each), the mask on PARTIAL tiles
+//      (row intervals, else the program) and the score mod, an online softmax
+//      over its keys, and P V into its own accumulators (4 or 2 output columns
+//      per lane); the warps merge by their running maxima after the last tile.
+//      Keys past kv_len are never read, so the rows of a last page past kv_len
+//      do not matter.  Writes the share's out (normalised) and LSE to the
+//      workspace.
 //  decode_combine_kernel  one block per (b, h, query row):
 //      lse = log sum_s e^{lse_s},  out = sum_s e^{lse_s - lse} out_s.
 #include <cfloat>
@@ -36,26 +37,26 @@ namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
-constexpr int kDecThreads = 256;
+constexpr int kDecWarps = 8;                       // compute warps; warp kDecWarps loads
+constexpr int kDecThreads = 32 * (kDecWarps + 1);
 constexpr int kDecStages = 3;
 constexpr int kDecMaxSplits = 64;
+constexpr int kKeysPerWarp = 128 / kDecWarps;     // 16 keys of every tile per compute warp
 
 template <int D>
 struct DecCfg {
-  static constexpr int TILE = 128 * D * 2;       // bytes of one K or V tile: D / 64 swizzled boxes of 128 x 64
-  static constexpr int NCH = D / 8;              // 16-byte chunks of a key row
-  static constexpr int PAIRS = D / 2;            // column pairs of the P V phase
-  static constexpr int NG = kDecThreads / PAIRS; // key groups of the P V phase
-  static constexpr int KPG = 128 / NG;           // keys per group
+  static constexpr int TILE = 128 * D * 2;  // bytes of one K or V tile: D / 64 swizzled boxes of 128 x 64
+  static constexpr int NH = D / 16;         // 16-byte chunks in half a key row
+  static constexpr int CPL = D / 32;        // output columns per lane
 };
 
 template <int D>
 constexpr size_t dec_smem_bytes() {
   return 1024 + (size_t)kDecStages * 2 * DecCfg<D>::TILE  // K / V stages (1024-aligned for the swizzle)
          + (size_t)FA_DECODE_MAX_Q * D * 4                // q, fp32
-         + (size_t)FA_DECODE_MAX_Q * 128 * 4              // scores, then probabilities
-         + 3 * FA_DECODE_MAX_Q * 4                        // alpha, m, l per row
-         + kDecStages * 8;                                // mbarriers
+         + (size_t)kDecWarps * FA_DECODE_MAX_Q * kKeysPerWarp * 4  // each warp's probabilities
+         + (size_t)2 * kDecWarps * FA_DECODE_MAX_Q * 4    // each warp's running max and sum per row
+         + 2 * kDecStages * 8 + 16;                       // mbarriers, abort flag
 }
 
 // tanh(t) = 1 - 2 / (1 + e^{2t}); exact at both saturations, absolute error a few ulp of 1.
@@ -66,30 +67,29 @@ __device__ __forceinline__ float tanh_fast(float t) {
   return fmaf(-2.0f, r, 1.0f);
 }
 
-// Thread roles per tile (256 threads):
-//   scores   thread (half, key r): t = 128 * half + r sums q . k over chunks
-//            [half * NCH / 2, (half + 1) * NCH / 2) of key row r; the halves
-//            meet in shared memory, half 0 applies mask and score mod;
-//   softmax  warp w owns query rows w, w + 8;
-//   P V      thread (group g, pair c): t = PAIRS * g + c accumulates columns
-//            2c, 2c + 1 over keys [KPG g, KPG (g + 1)); the groups' sums are
-//            added once, after the last tile.
+// Warp roles: warps 0..7 compute, each on keys [16 w, 16 w + 16) of every tile
+// with its own online softmax and output accumulators (no block barrier per
+// tile); warp 8 loads K / V into the stages.  Within a compute warp, lane
+// pair (2k, 2k + 1) owns key 16 w + k for the scores (one half of the head dim
+// each; the second half starts four chunks on, so that with the 128-byte
+// swizzle the eight lanes of a shared-memory phase hit eight distinct bank
+// groups), and lane l owns output columns [CPL l, CPL l + CPL) for P V.
 template <int D, int SCORE, int QB>
 __global__ void __launch_bounds__(kDecThreads, 1)
     decode_partial_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                           const __grid_constant__ AttnArgs p, const __nv_bfloat16* __restrict__ q,
                           float* __restrict__ ws_out, float* __restrict__ ws_lse, int splits) {
   using C = DecCfg<D>;
-  constexpr int RW = (QB + 7) / 8;  // query rows per warp in the softmax
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   uint8_t* sKV = base;
   float* sQ = reinterpret_cast<float*>(base + kDecStages * 2 * C::TILE);
-  float* sP = sQ + FA_DECODE_MAX_Q * D;
-  float* sAlpha = sP + FA_DECODE_MAX_Q * 128;
-  float* sM = sAlpha + FA_DECODE_MAX_Q;
-  float* sL = sM + FA_DECODE_MAX_Q;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sL + FA_DECODE_MAX_Q);
+  float* sPw = sQ + FA_DECODE_MAX_Q * D;                              // [warp][row][key]
+  float* sMw = sPw + kDecWarps * FA_DECODE_MAX_Q * kKeysPerWarp;      // [warp][row]
+  float* sLw = sMw + kDecWarps * FA_DECODE_MAX_Q;
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(sLw + kDecWarps * FA_DECODE_MAX_Q);
+  uint64_t* empty_bar = full_bar + kDecStages;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(empty_bar + kDecStages);
   __shared__ int32_t s_arg[FA_MAX_MASK_NODES];
 
   const int t = threadIdx.x, warp = t / 32, lane = t % 32;
@@ -108,122 +108,138 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   for (int e = t; e < ql * D; e += kDecThreads) sQ[e] = __bfloat162float(q[(int64_t)bh * ql * D + e]);
   if (t < p.mask.n) s_arg[t] = node_arg(p.mask, t, bm);
   if (t == 0) {
-    for (int s = 0; s < kDecStages; ++s) mbar_init(smem_u32(&bars[s]), 1);
+    for (int s = 0; s < kDecStages; ++s) {
+      mbar_init(smem_u32(&full_bar[s]), 1);
+      mbar_init(smem_u32(&empty_bar[s]), kDecWarps);
+    }
+    *abort_flag = 0;
     fence_mbar_init();
   }
   __syncthreads();
 
-  // K and V of list position pos into its stage (thread 0, which counts them)
-  int issued_end = p0;
-  auto issue = [&](int pos) {
-    issued_end = pos + 1;
-    const int st = (pos - p0) % kDecStages;
-    const int J = tile_at(pos);
-    int kv_row = J * 128, kv_z = bh;
-    if (p.page_table != nullptr) {
-      int page = __ldg(p.page_table + (int64_t)b * p.nkv + J);
-      if (page < 0 || page >= p.n_pages) {  // reported; page 0 is read instead
-        atomicOr(p.status, kStatusCheck);
-        page = 0;
-      }
-      kv_row = page * 128;
-      kv_z = h;
-    }
-    const uint32_t bar = smem_u32(&bars[st]);
-    mbar_arrive_expect_tx(bar, 2 * C::TILE);
-    uint8_t* dk = sKV + (size_t)st * 2 * C::TILE;
-    for (int c = 0; c < D / 64; ++c) {
-      tma_load_3d(smem_u32(dk + c * 16384), &tm_k, bar, c * 64, kv_row, kv_z);
-      tma_load_3d(smem_u32(dk + C::TILE + c * 16384), &tm_v, bar, c * 64, kv_row, kv_z);
-    }
-  };
-  if (t == 0) {
-    prefetch_tmap(&tm_k);
-    prefetch_tmap(&tm_v);
-    for (int pos = p0; pos < min(p1, p0 + kDecStages); ++pos) issue(pos);
-  }
-
-  const uint64_t mask_ops = pack_ops(p.mask);
-  const int32_t* doc_row = p.mask.has_doc ? p.mask.doc + (int64_t)bm * p.mask.doc_len : nullptr;
-  float slope_l2 = 0.f, cap = 1.f;
-  if constexpr (SCORE == FA_S_ALIBI) slope_l2 = __ldg(p.score_param + h) * kLog2e;
-  if constexpr (SCORE == FA_S_SOFTCAP) cap = __ldg(p.score_param);
-  float m_run[RW], l_run[RW];
-#pragma unroll
-  for (int k = 0; k < RW; ++k) m_run[k] = -INFINITY, l_run[k] = 0.f;
-  float2 o[QB];  // P V: columns 2c, 2c + 1 of every query row, this thread's key group
-#pragma unroll
-  for (int i = 0; i < QB; ++i) o[i] = make_float2(0.f, 0.f);
-  const int half = t / 128, r = t % 128;          // scores
-  const int pc = t % C::PAIRS, grp = t / C::PAIRS;  // P V
-  const int pbox = (2 * pc) / 64, pdc = (2 * pc) % 64;
-  const int pchunk = pdc / 8, pbyte = (pdc % 8) * 2;
-
   bool ok = true;
-  for (int pos = p0; pos < p1; ++pos) {
-    const int st = (pos - p0) % kDecStages, use = (pos - p0) / kDecStages;
-    const bool got = mbar_wait(smem_u32(&bars[st]), use & 1, nullptr);
-    if (!__syncthreads_and(got)) {
-      ok = false;
-      break;
-    }
-    const int J = tile_at(pos);
-    const bool full = pos < n_full;
-    const int rows_valid = min(128, p.kv_len - J * 128);
-    const uint8_t* sK = sKV + (size_t)st * 2 * C::TILE;
-    const uint8_t* sV = sK + C::TILE;
-
-    // -- scores: this thread's half of q . k for key row r
-    float s[QB];
-#pragma unroll
-    for (int i = 0; i < QB; ++i) s[i] = 0.f;
-    if (r < rows_valid) {
-#pragma unroll
-      for (int cc = 0; cc < C::NCH / 2; ++cc) {
-        const int c = half * (C::NCH / 2) + cc;  // 16-byte chunk of the key row, at its swizzled place
-        const uint4 kw = *reinterpret_cast<const uint4*>(sK + (c / 8) * 16384 + r * 128 + (((c % 8) ^ (r & 7)) << 4));
-        float kf[8];
-        const __nv_bfloat162* k2 = reinterpret_cast<const __nv_bfloat162*>(&kw);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float2 f = __bfloat1622float2(k2[e]);
-          kf[2 * e] = f.x;
-          kf[2 * e + 1] = f.y;
+  float m_run[QB], l_run[QB];
+  float o[QB][C::CPL];
+  if (warp == kDecWarps) {
+    // ------------------------------------------------------------ loader
+    if (lane == 0) {
+      prefetch_tmap(&tm_k);
+      prefetch_tmap(&tm_v);
+      int issued_end = p0;
+      for (int pos = p0; pos < p1; ++pos) {
+        const int st = (pos - p0) % kDecStages, use = (pos - p0) / kDecStages;
+        if (use > 0 && !mbar_wait(smem_u32(&empty_bar[st]), (use - 1) & 1, abort_flag)) {
+          ok = false;
+          break;
         }
+        const int J = tile_at(pos);
+        int kv_row = J * 128, kv_z = bh;
+        if (p.page_table != nullptr) {
+          int page = __ldg(p.page_table + (int64_t)b * p.nkv + J);
+          if (page < 0 || page >= p.n_pages) {  // reported; page 0 is read instead
+            atomicOr(p.status, kStatusCheck);
+            page = 0;
+          }
+          kv_row = page * 128;
+          kv_z = h;
+        }
+        const uint32_t bar = smem_u32(&full_bar[st]);
+        mbar_arrive_expect_tx(bar, 2 * C::TILE);
+        uint8_t* dk = sKV + (size_t)st * 2 * C::TILE;
+        for (int c = 0; c < D / 64; ++c) {
+          tma_load_3d(smem_u32(dk + c * 16384), &tm_k, bar, c * 64, kv_row, kv_z);
+          tma_load_3d(smem_u32(dk + C::TILE + c * 16384), &tm_v, bar, c * 64, kv_row, kv_z);
+        }
+        issued_end = pos + 1;
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        atomicOr(p.status, kStatusTimeout);
+      }
+      // every copy issued lands before the CTA moves on (bounded waits)
+      for (int pos = max(p0, issued_end - kDecStages); pos < issued_end; ++pos)
+        mbar_wait(smem_u32(&full_bar[(pos - p0) % kDecStages]), ((pos - p0) / kDecStages) & 1, nullptr);
+    }
+  } else {
+    // ------------------------------------------------------------ compute warps
+    const uint64_t mask_ops = pack_ops(p.mask);
+    const int32_t* doc_row = p.mask.has_doc ? p.mask.doc + (int64_t)bm * p.mask.doc_len : nullptr;
+    float slope_l2 = 0.f, cap = 1.f;
+    if constexpr (SCORE == FA_S_ALIBI) slope_l2 = __ldg(p.score_param + h) * kLog2e;
+    if constexpr (SCORE == FA_S_SOFTCAP) cap = __ldg(p.score_param);
 #pragma unroll
-        for (int i = 0; i < QB; ++i) {
-          if (i < ql) {
-            const float4 qa = *reinterpret_cast<const float4*>(sQ + i * D + c * 8);
-            const float4 qb = *reinterpret_cast<const float4*>(sQ + i * D + c * 8 + 4);
-            float a = s[i];
-            a = fmaf(qa.x, kf[0], a);
-            a = fmaf(qa.y, kf[1], a);
-            a = fmaf(qa.z, kf[2], a);
-            a = fmaf(qa.w, kf[3], a);
-            a = fmaf(qb.x, kf[4], a);
-            a = fmaf(qb.y, kf[5], a);
-            a = fmaf(qb.z, kf[6], a);
-            a = fmaf(qb.w, kf[7], a);
-            s[i] = a;
+    for (int i = 0; i < QB; ++i) {
+      m_run[i] = -INFINITY;
+      l_run[i] = 0.f;
+#pragma unroll
+      for (int c = 0; c < C::CPL; ++c) o[i][c] = 0.f;
+    }
+    const int kk = lane / 2, half = lane % 2;
+    const int r = kKeysPerWarp * warp + kk;  // this lane pair's key row in the tile
+    float* pw = sPw + warp * FA_DECODE_MAX_Q * kKeysPerWarp;
+    // P V: columns [CPL lane, CPL lane + CPL): box, 16-byte chunk and byte within it
+    const int col0 = C::CPL * lane;
+    const int vbox = col0 / 64, vchunk = (col0 % 64) / 8, vbyte = (col0 % 8) * 2;
+    for (int pos = p0; pos < p1; ++pos) {
+      const int st = (pos - p0) % kDecStages, use = (pos - p0) / kDecStages;
+      const bool got = mbar_wait(smem_u32(&full_bar[st]), use & 1, abort_flag);
+      if (!__all_sync(0xffffffffu, got)) {
+        ok = false;
+        break;
+      }
+      const int J = tile_at(pos);
+      const bool full = pos < n_full;
+      const int rows_valid = min(128, p.kv_len - J * 128);
+      const uint8_t* sK = sKV + (size_t)st * 2 * C::TILE;
+      const uint8_t* sV = sK + C::TILE;
+      const bool key_ok = r < rows_valid;
+      const int j = J * 128 + r;
+
+      // -- scores of key r: this lane's half of q . k, the pair's sum by a shuffle
+      float a[QB];
+#pragma unroll
+      for (int i = 0; i < QB; ++i) a[i] = 0.f;
+      if (key_ok) {
+#pragma unroll
+        for (int cc = 0; cc < C::NH; ++cc) {
+          const int c = half * C::NH + ((cc + 4 * half) % C::NH);
+          const uint4 kw =
+              *reinterpret_cast<const uint4*>(sK + (c / 8) * 16384 + r * 128 + (((c % 8) ^ (r & 7)) << 4));
+          float kf[8];
+          const __nv_bfloat162* k2 = reinterpret_cast<const __nv_bfloat162*>(&kw);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 f = __bfloat1622float2(k2[e]);
+            kf[2 * e] = f.x;
+            kf[2 * e + 1] = f.y;
+          }
+#pragma unroll
+          for (int i = 0; i < QB; ++i) {
+            if (i < ql) {
+              const float4 qa = *reinterpret_cast<const float4*>(sQ + i * D + c * 8);
+              const float4 qb = *reinterpret_cast<const float4*>(sQ + i * D + c * 8 + 4);
+              float x = a[i];
+              x = fmaf(qa.x, kf[0], x);
+              x = fmaf(qa.y, kf[1], x);
+              x = fmaf(qa.z, kf[2], x);
+              x = fmaf(qa.w, kf[3], x);
+              x = fmaf(qb.x, kf[4], x);
+              x = fmaf(qb.y, kf[5], x);
+              x = fmaf(qb.z, kf[6], x);
+              x = fmaf(qb.w, kf[7], x);
+              a[i] = x;
+            }
           }
         }
       }
-    }
-    if (half == 1) {
 #pragma unroll
-      for (int i = 0; i < QB; ++i)
-        if (i < ql) sP[i * 128 + r] = s[i];
-    }
-    __syncthreads();
-    if (half == 0) {
-      // key j: mask (FULL tiles: every in-range pair) and score mod, log2 units
-      const int j = J * 128 + r;
+      for (int i = 0; i < QB; ++i) a[i] += __shfl_xor_sync(0xffffffffu, a[i], 1);
+      // mask (FULL tiles: every in-range pair) and score mod, log2 units
       uint32_t w = 0;  // bit i: (i, j) visible
-      if (r < rows_valid) {
+      if (key_ok) {
         if (full) {
           w = 0xffffffffu;
         } else {
-          // this key's visible query rows: two intervals, else the program per row
           const int4 seg = __ldg(p.row_segs + ((int64_t)bm * 2 + 1) * p.seg_len + j);
           if (seg.x >= 0) {
             w = seg_word(seg, 0);
@@ -241,121 +257,115 @@ __global__ void __launch_bounds__(kDecThreads, 1)
           }
         }
       }
+      // -- online softmax over this warp's 16 keys (lane pairs hold equal values,
+      //    so the reductions run over the lanes of one parity)
 #pragma unroll
       for (int i = 0; i < QB; ++i) {
         if (i < ql) {
-          float a = -INFINITY;
+          float sc = -INFINITY;
           if ((w >> i) & 1u) {
-            const float x = (s[i] + sP[i * 128 + r]) * p.scale;
+            const float x = a[i] * p.scale;
             if constexpr (SCORE == FA_S_SOFTCAP) {
-              a = cap * tanh_fast(x / cap) * kLog2e;
+              sc = cap * tanh_fast(x / cap) * kLog2e;
             } else if constexpr (SCORE == FA_S_ALIBI) {
-              a = fmaf(x, kLog2e, -slope_l2 * (float)(i - j));
+              sc = fmaf(x, kLog2e, -slope_l2 * (float)(i - j));
             } else {
-              a = x * kLog2e;
+              sc = x * kLog2e;
             }
           }
-          sP[i * 128 + r] = a;
+          float mx = sc;
+#pragma unroll
+          for (int o2 = 2; o2 <= 16; o2 <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o2));
+          const float m_new = fmaxf(m_run[i], mx);
+          const float mu = (m_new == -INFINITY) ? 0.f : m_new;
+          const float pv = ex2_approx(sc - mu);
+          float sum = pv;
+#pragma unroll
+          for (int o2 = 2; o2 <= 16; o2 <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o2);
+          const float alpha = ex2_approx(m_run[i] - mu);
+          l_run[i] = fmaf(l_run[i], alpha, sum);
+          m_run[i] = m_new;
+#pragma unroll
+          for (int c = 0; c < C::CPL; ++c) o[i][c] *= alpha;
+          if (half == 0) pw[i * kKeysPerWarp + kk] = pv;
         }
       }
-    }
-    __syncthreads();
-
-    // -- online softmax: warp w owns query rows w, w + 8
-#pragma unroll
-    for (int k = 0; k < RW; ++k) {
-      const int i = warp + 8 * k;
-      if (i < ql) {
-        float4 a = *reinterpret_cast<const float4*>(sP + i * 128 + 4 * lane);
-        float mx = fmaxf(fmaxf(a.x, a.y), fmaxf(a.z, a.w));
-#pragma unroll
-        for (int o2 = 16; o2 >= 1; o2 >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o2));
-        const float m_new = fmaxf(m_run[k], mx);
-        const float mu = (m_new == -INFINITY) ? 0.f : m_new;
-        a.x = ex2_approx(a.x - mu);
-        a.y = ex2_approx(a.y - mu);
-        a.z = ex2_approx(a.z - mu);
-        a.w = ex2_approx(a.w - mu);
-        float sum = (a.x + a.y) + (a.z + a.w);
-#pragma unroll
-        for (int o2 = 16; o2 >= 1; o2 >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o2);
-        const float alpha = ex2_approx(m_run[k] - mu);
-        l_run[k] = fmaf(l_run[k], alpha, sum);
-        m_run[k] = m_new;
-        *reinterpret_cast<float4*>(sP + i * 128 + 4 * lane) = a;
-        if (lane == 0) sAlpha[i] = alpha;
-      }
-    }
-    __syncthreads();
-
-    // -- P V: column pair pc of every query row over this group's valid keys
-    {
-#pragma unroll
-      for (int i = 0; i < QB; ++i) {
-        if (i < ql) {
-          const float al = sAlpha[i];
-          o[i].x *= al;
-          o[i].y *= al;
-        }
-      }
-      const uint8_t* vcol = sV + pbox * 16384 + pbyte;
-      const int j0 = grp * C::KPG, j1 = min(j0 + C::KPG, rows_valid);
+      __syncwarp();
+      // -- P V over this warp's valid keys
+      const int kn = min(kKeysPerWarp, rows_valid - kKeysPerWarp * warp);
 #pragma unroll 4
-      for (int jj = j0; jj < j1; ++jj) {
-        const float2 vv = __bfloat1622float2(
-            *reinterpret_cast<const __nv_bfloat162*>(vcol + jj * 128 + ((pchunk ^ (jj & 7)) << 4)));
+      for (int k2 = 0; k2 < kn; ++k2) {
+        const int jr = kKeysPerWarp * warp + k2;
+        const uint8_t* vp = sV + vbox * 16384 + jr * 128 + ((vchunk ^ (jr & 7)) << 4) + vbyte;
+        float vv[C::CPL];
+        if constexpr (C::CPL == 4) {
+          const uint2 raw = *reinterpret_cast<const uint2*>(vp);
+          const float2 v01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.x));
+          const float2 v23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.y));
+          vv[0] = v01.x;
+          vv[1] = v01.y;
+          vv[2] = v23.x;
+          vv[3] = v23.y;
+        } else {
+          const float2 v01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(vp));
+          vv[0] = v01.x;
+          vv[1] = v01.y;
+        }
 #pragma unroll
         for (int i = 0; i < QB; ++i) {
           if (i < ql) {
-            const float pij = sP[i * 128 + jj];
-            o[i].x = fmaf(pij, vv.x, o[i].x);
-            o[i].y = fmaf(pij, vv.y, o[i].y);
+            const float pij = pw[i * kKeysPerWarp + k2];
+#pragma unroll
+            for (int c = 0; c < C::CPL; ++c) o[i][c] = fmaf(pij, vv[c], o[i][c]);
           }
         }
       }
+      __syncwarp();  // this warp is done with the stage and its probabilities
+      if (lane == 0) mbar_arrive(smem_u32(&empty_bar[st]));
     }
-    __syncthreads();  // the stage and the scores are free
-    if (t == 0 && pos + kDecStages < p1) {
-      fence_proxy_async_smem();
-      issue(pos + kDecStages);
-    }
-  }
-
-  if (!ok) {
-    if (t == 0) {
+    if (!ok && lane == 0) {
+      *abort_flag = 1;
       atomicOr(p.status, kStatusTimeout);
-      // the last copy issued into each stage lands before the CTA exits (bounded waits)
-      for (int pos = max(p0, issued_end - kDecStages); pos < issued_end; ++pos)
-        mbar_wait(smem_u32(&bars[(pos - p0) % kDecStages]), ((pos - p0) / kDecStages) & 1, nullptr);
     }
-    return;
   }
-  // the key groups' sums meet in the (now idle) stage memory: [group][row][D]
-  float* red = reinterpret_cast<float*>(sKV);
+  __syncthreads();  // every warp is done with the stages
+  if (*abort_flag) return;
+
+  // the warps' rows merge: running max and sum per warp, outputs through the idle stages
+  float* red = reinterpret_cast<float*>(sKV);  // [warp][row][D]
+  if (warp < kDecWarps) {
 #pragma unroll
-  for (int i = 0; i < QB; ++i)
-    if (i < ql) *reinterpret_cast<float2*>(red + ((size_t)grp * FA_DECODE_MAX_Q + i) * D + 2 * pc) = o[i];
+    for (int i = 0; i < QB; ++i) {
+      if (i < ql) {
 #pragma unroll
-  for (int k = 0; k < RW; ++k) {
-    const int i = warp + 8 * k;
-    if (i < ql && lane == 0) {
-      sM[i] = m_run[k];
-      sL[i] = l_run[k];
+        for (int c = 0; c < C::CPL; ++c) red[((size_t)warp * FA_DECODE_MAX_Q + i) * D + C::CPL * lane + c] = o[i][c];
+        if (lane == 0) {
+          sMw[warp * FA_DECODE_MAX_Q + i] = m_run[i];
+          sLw[warp * FA_DECODE_MAX_Q + i] = l_run[i];
+        }
+      }
     }
   }
   __syncthreads();
   const int64_t r0 = ((int64_t)split * p.B * p.H + bh) * ql;  // this share's first row in the workspace
   for (int e = t; e < ql * D; e += kDecThreads) {
     const int i = e / D, dd = e % D;
-    float acc = 0.f;
+    float mx = -INFINITY;
 #pragma unroll
-    for (int g2 = 0; g2 < C::NG; ++g2) acc += red[((size_t)g2 * FA_DECODE_MAX_Q + i) * D + dd];
-    const float l = sL[i];
+    for (int w2 = 0; w2 < kDecWarps; ++w2) mx = fmaxf(mx, sMw[w2 * FA_DECODE_MAX_Q + i]);
+    float acc = 0.f, l = 0.f;
+    if (mx != -INFINITY) {
+#pragma unroll
+      for (int w2 = 0; w2 < kDecWarps; ++w2) {
+        const float mw = sMw[w2 * FA_DECODE_MAX_Q + i];
+        if (mw == -INFINITY) continue;
+        const float sc = ex2_approx(mw - mx);
+        l = fmaf(sLw[w2 * FA_DECODE_MAX_Q + i], sc, l);
+        acc = fmaf(red[((size_t)w2 * FA_DECODE_MAX_Q + i) * D + dd], sc, acc);
+      }
+    }
     ws_out[(r0 + i) * D + dd] = (l > 0.f) ? acc / l : 0.f;
-  }
-  if (t < ql) {
-    const float l = sL[t];
-    ws_lse[r0 + t] = (l > 0.f) ? (sM[t] + log2f(l)) * kLn2 : -INFINITY;
+    if (dd == 0) ws_lse[r0 + i] = (l > 0.f) ? (mx + log2f(l)) * kLn2 : -INFINITY;
   }
 }
 
@@ -400,8 +410,12 @@ cudaError_t launch_decode_t(const AttnArgs& a, const FwdTensors& t, float* ws, i
   constexpr size_t smem = dec_smem_bytes<D>();
   static bool attr_set = false;
   if (!attr_set) {
-    const cudaError_t e = cudaFuncSetAttribute(decode_partial_kernel<D, SCORE, QB>,
-                                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = cudaFuncSetAttribute(decode_partial_kernel<D, SCORE, QB>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    // all of the unified L1 as shared memory, so that two CTAs fit an SM at D = 64
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(decode_partial_kernel<D, SCORE, QB>,
+                               cudaFuncAttributePreferredSharedMemoryCarveout, 100);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
@@ -431,12 +445,23 @@ cudaError_t decode_plan(int32_t B, int32_t H, int64_t q_len, int64_t kv_len, int
   cudaError_t e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
-  // about one wave of CTAs (one per SM at D = 128, two at D = 64), at most one per key tile
-  const int64_t per_sm = (D == 128) ? 1 : 2;
+  // CTAs that fit at once: one per SM at D = 128, two at D = 64 with one query
+  // row (registers); the split minimises waves x (tiles per share + a CTA's
+  // start-up, about 1.5 tiles), taking the key tiles as all listed
+  const int64_t slots = (int64_t)sms * ((D == 64 && q_len == 1) ? 2 : 1);
   const int64_t items = (int64_t)B * H;
   const int64_t nkv = (kv_len + 127) / 128;
-  int64_t s = (sms * per_sm + items - 1) / items;
-  s = std::max<int64_t>(1, std::min<int64_t>(s, std::min<int64_t>(nkv, kDecMaxSplits)));
+  const int64_t s_max = std::max<int64_t>(1, std::min<int64_t>(nkv, kDecMaxSplits));
+  int64_t s = 1;
+  double best = 0.0;
+  for (int64_t c = 1; c <= s_max; ++c) {
+    const double waves = (double)((items * c + slots - 1) / slots);
+    const double cost = waves * ((double)((nkv + c - 1) / c) + 1.5);
+    if (c == 1 || cost < best) {
+      best = cost;
+      s = c;
+    }
+  }
   *splits = (int)s;
   *ws_bytes = (size_t)s * items * q_len * (D + 1) * sizeof(float);
   return cudaSuccess;
