@@ -173,6 +173,40 @@ def builder_scaled(fa, w, W, dev, S=262144, reps=10):
     return {"S": S, "ms": round(ms, 4), "algorithmic_bytes": int(nbytes), "GB_s": round(nbytes / (ms * 1e-3) / 1e9, 1)}
 
 
+def decode_point(fa, dev, hbm_gbs, B=1, H=16, kv_len=65536, D=128, reps=20):
+    """The short-query forward alone (q_len 1, every key visible, a single long
+    context per head): its time and achieved bandwidth over the algorithmic
+    bytes -- K and V of every key, read once -- between L2 flushes."""
+    import torch
+
+    g = torch.Generator(device=dev).manual_seed(7)
+    q = torch.randn(B, H, 1, D, device=dev, generator=g).to(torch.bfloat16)
+    k = torch.randn(B, H, kv_len, D, device=dev, generator=g).to(torch.bfloat16)
+    v = torch.randn(B, H, kv_len, D, device=dev, generator=g).to(torch.bfloat16)
+    bm = fa.fa_create_block_mask([("true",)], 1, 1, 1, kv_len, 128)
+    ws = torch.empty(fa.fa_forward_decode_workspace_bytes(B, H, 1, kv_len, D), dtype=torch.uint8, device=dev)
+    out = torch.empty_like(q)
+    lse = torch.empty(B, H, 1, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    for _ in range(3):
+        fa.fa_forward_decode(q, k, v, bm, out=out, lse=lse, workspace=ws)
+    times = []
+    for _ in range(reps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        fa.fa_forward_decode(q, k, v, bm, out=out, lse=lse, workspace=ws)
+        e1.record()
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1))
+    ms = sorted(times)[reps // 2]
+    nbytes = 2 * k.numel() * k.element_size()
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    assert fa.fa_get_status(bm) == 0
+    return {"shape": f"B{B} H{H} q_len 1 kv_len {kv_len} D{D}", "ms": round(ms, 4), "algorithmic_bytes": int(nbytes),
+            "GB_s": round(gbs, 1), "frac_of_hbm": round(gbs / hbm_gbs, 3)}
+
+
 def visible_tiles(fa, bm, B, H):
     """Sum over (b, h) of non-empty tiles, from the block mask's counts."""
     L = bm.lists()
@@ -391,6 +425,7 @@ def run_gpu(args):
     }
     if rank == 0:
         res["builder_scaled"] = builder_scaled(fa, w, W, dev)
+        res["decode"] = decode_point(fa, dev, float(peaks.get("hbm_gbs", PEAKS_FALLBACK["hbm_gbs"])))
     if rank == 0 and not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline(w, args.cpu_sample_tokens)
     if world > 1:

@@ -20,7 +20,9 @@
 //      Keys past kv_len are never read, so the rows of a last page past kv_len
 //      do not matter.  Writes the share's out (normalised) and LSE to the
 //      workspace.
-//  decode_combine_kernel  one block per (b, h, query row):
+//  decode_combine_kernel  one block per (b, h, query row), launched as a
+//      programmatic dependent of the partial kernel (its launch overlaps the
+//      partial kernel's tail; it waits for its results before reading):
 //      lse = log sum_s e^{lse_s},  out = sum_s e^{lse_s - lse} out_s.
 #include <cfloat>
 #include <cmath>
@@ -374,6 +376,7 @@ __global__ void __launch_bounds__(D) decode_combine_kernel(const float* __restri
                                                            const float* __restrict__ ws_lse, int splits,
                                                            int64_t rows, __nv_bfloat16* __restrict__ out,
                                                            float* __restrict__ lse) {
+  pdl_wait_then_release();       // launched while the partial kernel drains
   const int64_t r = blockIdx.x;  // (b, h, query row)
   const int d = threadIdx.x;
   float m = -INFINITY;
@@ -424,9 +427,10 @@ cudaError_t launch_decode_t(const AttnArgs& a, const FwdTensors& t, float* ws, i
   float* ws_lse = ws + (size_t)splits * rows * D;
   decode_partial_kernel<D, SCORE, QB><<<dim3((unsigned)splits, (unsigned)bh), kDecThreads, smem, stream>>>(
       mk, mv, a, static_cast<const __nv_bfloat16*>(t.q), ws_out, ws_lse, splits);
-  decode_combine_kernel<D><<<(unsigned)rows, D, 0, stream>>>(ws_out, ws_lse, splits, rows,
-                                                             static_cast<__nv_bfloat16*>(t.out), t.lse);
-  return cudaGetLastError();
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  return launch_k(decode_combine_kernel<D>, dim3((unsigned)rows), dim3(D), 0, stream, (const float*)ws_out,
+                  (const float*)ws_lse, splits, rows, static_cast<__nv_bfloat16*>(t.out), t.lse);
 }
 
 template <int D, int SCORE>

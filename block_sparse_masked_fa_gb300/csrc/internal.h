@@ -29,8 +29,9 @@ struct BuildArgs {
 // Launches a kernel on `stream` allowed to start while the kernel before it
 // drains (programmatic stream serialization); the kernel itself waits for that
 // one to complete before touching memory (pdl_wait_then_release).  Used for the
-// builder's chain of short kernels; the attention kernels, which fill every SM,
-// measured slower launched this way and are launched plainly.
+// builder's chain of short kernels and the decode combine; the attention
+// kernels, which fill every SM, measured slower launched this way and are
+// launched plainly.
 template <typename... KArgs, typename... Args>
 cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
                      Args&&... args) {
