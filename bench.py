@@ -215,21 +215,44 @@ def visible_tiles(fa, bm, B, H):
     return per_row * rep
 
 
+def rank_env():
+    """(world size, rank, local rank) from the launcher's environment; (1, 0, 0) alone."""
+    return (int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def replica_seed(w, rank):
+    """Each rank runs an independent replica of the workload with its own seed
+    (its own documents and inputs), as data-parallel ranks each hold a sequence."""
+    return w.seed + 97 * rank
+
+
+def reduce_over_ranks(dist, device, times_ms, work):
+    """Max over ranks of each timed region (the job is as slow as its slowest
+    rank) and the sum over ranks of the work (the replicas' visible tiles differ
+    with their documents)."""
+    import torch
+
+    t = torch.tensor([float(x) for x in times_ms], dtype=torch.float64, device=device)
+    f = torch.tensor([float(work)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(f, op=dist.ReduceOp.SUM)
+    return [float(x) for x in t.tolist()], float(f.item())
+
+
 def run_gpu(args):
     import torch
     import torch.distributed as dist
 
     import block_sparse_masked_fa_gb300 as fa
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
+    world, rank, local = rank_env()
     torch.cuda.set_device(local)
     if world > 1:
         dist.init_process_group("nccl")
 
     w = WORKLOADS[args.workload]
-    q_h, k_h, v_h, do_h, docs_np = workload_tensors(w, seed=w.seed + 97 * rank)
+    q_h, k_h, v_h, do_h, docs_np = workload_tensors(w, seed=replica_seed(w, rank))
     dev = torch.device("cuda", local)
     q, k, v, do = (t.to(dev) for t in (q_h, k_h, v_h, do_h))
     docs = torch.as_tensor(docs_np, dtype=torch.int32, device=dev) if docs_np is not None else None
@@ -302,11 +325,6 @@ def run_gpu(args):
         dist.barrier()
     clk = clocks.stop()
     ms_total = t0.elapsed_time(t1)
-    if world > 1:
-        tt = torch.tensor([ms_total], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms_total = float(tt.item())
-    ms_step = ms_total / args.steps
     build_ms = sum(m[0].elapsed_time(m[1]) for m in marks) / args.steps
     fwd_ms = sum(m[1].elapsed_time(m[2]) for m in marks) / args.steps
     bwd_ms = sum(m[2].elapsed_time(m[3]) for m in marks) / args.steps
@@ -379,6 +397,10 @@ def run_gpu(args):
     e1.record(s_out)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    job_flops = step_flops  # the work of all ranks
+    if world > 1:
+        (ms_total, e2e_ms), job_flops = reduce_over_ranks(dist, dev, (ms_total, e2e_ms), step_flops)
+    ms_step = ms_total / args.steps
     assert torch.equal(h_out, out.cpu()), "e2e results differ from the device-timed run"
 
     peaks, peak_src = load_peaks()
@@ -387,7 +409,7 @@ def run_gpu(args):
     dom_ms = bwd_ms if dominant == "bwd" else fwd_ms
     dom_flops = bwd_flops if dominant == "bwd" else fwd_flops
     achieved = dom_flops / (dom_ms * 1e-3) / 1e12
-    value = world * step_flops / (ms_step * 1e-3) / 1e12
+    value = job_flops / (ms_step * 1e-3) / 1e12
     # builder: (tile_summary + doc_runs) + row_segs + classify + compact + order; forward 1;
     # backward pre + main + dq convert
     launches_per_step = (6 if docs is not None else 4) + 1 + (3 if have_bwd else 0)
@@ -417,7 +439,7 @@ def run_gpu(args):
                      "peak_source": f"bf16_tflops ({peak_src}, burst)", "unit": "TFLOP/s",
                      "frac": round(achieved / peak, 4),
                      "traffic": recorded_traffic("bwd_kernel" if dominant == "bwd" else "fwd_kernel", w.name)},
-        "e2e": {"value": round(world * step_flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+        "e2e": {"value": round(job_flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
                 "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                 "overlap": "two device buffer sets; copies of a step overlap neighbouring steps' compute"},
         "gpu_launches": launches_per_step * args.steps,
@@ -480,8 +502,8 @@ def cpu_baseline(w, tokens, heads=1):
 
 def run_reference(args):
     """--impl reference: the CPU oracle as it stands, on a bounded sample per step."""
-    rank = int(os.environ.get("RANK", "0"))
-    if rank != 0:
+    _, rank, _ = rank_env()
+    if rank != 0:  # under torchrun only rank 0 runs and prints
         return
     w = WORKLOADS[args.workload]
     vals = []
