@@ -33,24 +33,36 @@ PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}
 METRIC = "attention TFLOP/s over visible tiles (fwd+bwd)"
 
 
-def source_digest() -> str:
-    """sha256 over the CUDA sources and the C header: the kernels the counters describe."""
+# The translation unit each profiled kernel is compiled from; every kernel also
+# includes the shared headers and the C header.
+KERNEL_SOURCES = {"fwd_kernel": "fwd.cu", "bwd_kernel": "bwd.cu", "classify_kernel": "builder.cu",
+                  "row_segs_kernel": "builder.cu", "decode_partial_kernel": "decode.cu"}
+SHARED_HEADERS = ("common.cuh", "internal.h", "ptx.cuh")
+
+
+def source_digest(kernel: str, read=None) -> str:
+    """sha256 over the files `kernel` is compiled from: its .cu, the shared
+    headers and include/fa.h.  `read(relpath) -> bytes` defaults to the
+    working tree (a recording script passes the sources of the capture)."""
     import hashlib
 
+    def _read(rel):
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            return f.read()
+
+    read = read or _read
     h = hashlib.sha256()
-    csrc = os.path.join(ROOT, "block_sparse_masked_fa_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode() + b"\0" + f.read())
-    with open(os.path.join(ROOT, "include", "fa.h"), "rb") as f:
-        h.update(f.read())
+    csrc = "block_sparse_masked_fa_gb300/csrc/"
+    for name in sorted((KERNEL_SOURCES[kernel],) + SHARED_HEADERS):
+        h.update(name.encode() + b"\0" + read(csrc + name))
+    h.update(read("include/fa.h"))
     return h.hexdigest()
 
 
 def recorded_traffic(kernel: str, workload: str):
     """DRAM bytes per launch of `kernel` from the committed ncu record, or None when
-    the record is missing or was taken on other sources or another workload."""
+    the record is missing, was taken on another workload, or the kernel's sources
+    have changed since."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     try:
         with open(path) as f:
@@ -58,7 +70,7 @@ def recorded_traffic(kernel: str, workload: str):
     except (OSError, ValueError):
         return None
     entry = rec.get("kernels", {}).get(kernel)
-    if not entry or rec.get("source_sha256") != source_digest() or entry.get("workload") != workload:
+    if not entry or entry.get("workload") != workload or entry.get("source_sha256") != source_digest(kernel):
         return None
     return entry.get("dram_bytes_per_launch")
 

@@ -476,16 +476,29 @@ __global__ void __launch_bounds__(kBuildWarps * 32) compact_kernel(const __grid_
   int32_t* part_idx = (by_row ? a.kv_idx : a.q_idx) + id * n;
   int32_t* full_idx = (by_row ? a.full_idx : a.full_q_idx) + id * n;
   int n_part = 0, n_full = 0;
-  for (int c0 = 0; c0 < n; c0 += 32) {
-    const int x = c0 + lane;
-    const int cls = (x < n) ? cls_base[(int64_t)x * stride] : 0;
-    const uint32_t pb = __ballot_sync(0xffffffffu, cls == 1);
-    const uint32_t fb = __ballot_sync(0xffffffffu, cls == 2);
-    const uint32_t lt = (1u << lane) - 1u;
-    if (cls == 1) part_idx[n_part + __popc(pb & lt)] = x;
-    if (cls == 2) full_idx[n_full + __popc(fb & lt)] = x;
-    n_part += __popc(pb);
-    n_full += __popc(fb);
+  // class bytes of eight 32-tile chunks are loaded before any list entry is
+  // stored: the stores (int32) could alias the bytes for the compiler, which
+  // would otherwise keep each load behind the stores of the chunk before it
+  // (for a column, 32 cache lines a load)
+  constexpr int kBatch = 8;
+  const uint32_t lt = (1u << lane) - 1u;
+  for (int c0 = 0; c0 < n; c0 += 32 * kBatch) {
+    int cls[kBatch];
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int x = c0 + 32 * u + lane;
+      cls[u] = (x < n) ? __ldg(cls_base + (int64_t)x * stride) : 0;
+    }
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int x = c0 + 32 * u + lane;
+      const uint32_t pb = __ballot_sync(0xffffffffu, cls[u] == 1);
+      const uint32_t fb = __ballot_sync(0xffffffffu, cls[u] == 2);
+      if (cls[u] == 1) part_idx[n_part + __popc(pb & lt)] = x;
+      if (cls[u] == 2) full_idx[n_full + __popc(fb & lt)] = x;
+      n_part += __popc(pb);
+      n_full += __popc(fb);
+    }
   }
   for (int k = n_part + lane; k < n; k += 32) part_idx[k] = 0;
   for (int k = n_full + lane; k < n; k += 32) full_idx[k] = 0;
