@@ -1,0 +1,60 @@
+"""The Python binding's own argument checks for the entries that take tensors
+(caller-chosen tiles, paged and short-query forwards, the slope gradient):
+malformed tensors are refused with ValueError before the C ABI is called, so
+these run on CPU."""
+import pytest
+import torch
+
+B = pytest.importorskip("block_sparse_masked_fa_gb300.binding")
+
+
+class _Mask:
+    """Stand-in for a BlockMask: only the fields the checks read."""
+
+    def __init__(self, q_len=1, kv_len=1000):
+        self.struct = B.BlockMaskStruct()
+        self.struct.q_len, self.struct.kv_len = q_len, kv_len
+
+
+def test_from_kv_blocks_refuses_malformed_lists():
+    num = torch.zeros(1, 1, 8, dtype=torch.int32)
+    idx = torch.zeros(1, 1, 8, 8, dtype=torch.int32)
+    with pytest.raises(ValueError, match="CUDA"):
+        B.fa_block_mask_from_kv_blocks(num, idx, 1024, 1024)                   # host tensors
+    with pytest.raises(ValueError):
+        B.fa_block_mask_from_kv_blocks(num.long(), idx, 1024, 1024)            # wrong dtype
+
+
+def test_forward_paged_refuses_bad_pools_and_tables():
+    q = torch.zeros(2, 4, 16, 64, dtype=torch.bfloat16)
+    mask = _Mask(q_len=16, kv_len=1000)                                         # 8 key tiles
+    pool = torch.zeros(4, 10 * 128, 64, dtype=torch.bfloat16)
+    table = torch.zeros(2, 8, dtype=torch.int32)
+    with pytest.raises(ValueError, match="k_pool"):
+        B.fa_forward_paged(q, pool[:, :1000], pool[:, :1000], table, mask)      # rows not whole pages
+    with pytest.raises(ValueError, match="k_pool"):
+        B.fa_forward_paged(q, pool[:2], pool[:2], table, mask)                  # heads differ from q
+    with pytest.raises(ValueError, match="page_table"):
+        B.fa_forward_paged(q, pool, pool, table, mask)                          # table on the host
+    with pytest.raises(ValueError, match="page_table"):
+        B.fa_forward_paged(q, pool, pool, table[:, :7], mask)                   # too few tiles
+
+
+def test_forward_decode_refuses_bad_page_tables():
+    q = torch.zeros(2, 4, 1, 64, dtype=torch.bfloat16)
+    pool = torch.zeros(4, 10 * 128, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="page_table"):
+        B.fa_forward_decode(q, pool, pool, _Mask(), page_table=torch.zeros(2, 8, dtype=torch.int32))
+
+
+def test_slope_gradient_buffer_checked():
+    alibi = B.ScoreSpec()
+    alibi.op = B.SCORE_OPS["alibi"]
+    score = (alibi, [])                                                          # a prebuilt spec
+    with pytest.raises(ValueError, match="score_param_grad"):
+        B._backward_score(score, torch.zeros(4), 4)                             # host tensor
+    with pytest.raises(ValueError, match="score_param_grad"):
+        B._backward_score(score, torch.zeros(4, dtype=torch.float64), 4)
+    spec, _ = B._backward_score(score, None, 4)
+    assert spec.op == B.SCORE_OPS["alibi"] and not spec.param_grad
+    assert spec is not alibi                                                     # the caller's spec is not modified
