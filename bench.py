@@ -118,9 +118,15 @@ class ClockSampler:
             self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
+        return self.summarise(self.lines)
+
+    @staticmethod
+    def summarise(lines):
+        """Median and maximum SM clock and the throttle reasons seen active, from
+        nvidia-smi lines of FIELDS (unparsable lines are skipped)."""
         sm, smax, reasons = [], [], set()
         names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
-        for line in self.lines:
+        for line in lines:
             parts = [p.strip() for p in line.split(",")]
             if len(parts) < 7:
                 continue
