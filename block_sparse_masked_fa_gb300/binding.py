@@ -285,6 +285,31 @@ def fa_block_mask_from_kv_blocks(kv_num_blocks: torch.Tensor, kv_indices: torch.
     return BlockMask(st, buffer, keep)
 
 
+def _check_shapes(q, kv=(), like_q=(), lse=None):
+    """Refuses tensors whose sizes disagree with q [B, H, q_len, D] (the kernels'
+    tensor maps are built from these sizes): keys, values and their gradients
+    [B, H, kv_len, D] with one kv_len, out / dO / dq shaped as q, LSE [B, H, q_len].
+    None entries are skipped."""
+    if q.dim() != 4:
+        raise ValueError("q must be [B, H, q_len, D]")
+    B, H, q_len, D = q.shape
+    kv_len = None
+    for name, t in kv:
+        if t is None:
+            continue
+        if t.dim() != 4 or t.shape[0] != B or t.shape[1] != H or t.shape[3] != D:
+            raise ValueError(f"{name} must be [{B}, {H}, kv_len, {D}], got {tuple(t.shape)}")
+        if kv_len is None:
+            kv_len = t.shape[2]
+        elif t.shape[2] != kv_len:
+            raise ValueError(f"{name} has {t.shape[2]} rows, the other keys / values {kv_len}")
+    for name, t in like_q:
+        if t is not None and tuple(t.shape) != tuple(q.shape):
+            raise ValueError(f"{name} must be shaped like q {tuple(q.shape)}, got {tuple(t.shape)}")
+    if lse is not None and tuple(lse.shape) != (B, H, q_len):
+        raise ValueError(f"lse must be [{B}, {H}, {q_len}], got {tuple(lse.shape)}")
+
+
 def _score(score):
     if score is None:
         return make_score_spec("none")
@@ -297,6 +322,7 @@ def _score(score):
 
 def fa_forward(q, k, v, block_mask: BlockMask, score=None, scale: float = 0.0, out=None, lse=None, stream=None):
     """out [B,H,q_len,D] bf16 and lse [B,H,q_len] fp32."""
+    _check_shapes(q, kv=(("k", k), ("v", v)), like_q=(("out", out),), lse=lse)
     B, H, q_len, D = q.shape
     kv_len = k.shape[2]
     if out is None:
@@ -327,6 +353,7 @@ def fa_forward_paged(q, k_pool, v_pool, page_table, block_mask: BlockMask, score
                      lse=None, stream=None):
     """Forward over paged keys / values: k_pool, v_pool bf16 [H, n_pages * 128, D],
     page_table int32 [B, nkv] (page of each logical key tile).  out, lse as fa_forward."""
+    _check_shapes(q, like_q=(("out", out),), lse=lse)
     B, H, q_len, D = q.shape
     kv_len = block_mask.struct.kv_len
     nkv = -(-kv_len // 128)
@@ -361,9 +388,16 @@ def fa_forward_decode(q, k, v, block_mask: BlockMask, score=None, scale: float =
                       lse=None, workspace=None, stream=None):
     """Short-query forward (q_len <= 16): k, v [B, H, kv_len, D]; or, with an
     int32 page_table [B, nkv], pools [H, n_pages * 128, D].  out, lse as fa_forward."""
+    _check_shapes(q, like_q=(("out", out),), lse=lse)
     B, H, q_len, D = q.shape
     kv_len = block_mask.struct.kv_len
+    if q_len != block_mask.struct.q_len:
+        raise ValueError(f"q has {q_len} rows; the block mask was built for q_len {block_mask.struct.q_len}")
     n_pages = 0
+    if page_table is None and (tuple(k.shape) != (B, H, kv_len, D) or tuple(v.shape) != (B, H, kv_len, D)):
+        raise ValueError(f"k and v must be [{B}, {H}, {kv_len}, {D}] (kv_len of the block mask)")
+    if page_table is not None and v.shape != k.shape:
+        raise ValueError("paged k and v pools must have the same shape")
     if page_table is not None:
         if page_table.dtype != torch.int32 or not page_table.is_cuda or not page_table.is_contiguous() \
                 or tuple(page_table.shape) != (B, -(-kv_len // 128)):
@@ -396,6 +430,8 @@ def fa_backward(q, k, v, out, lse, dout, block_mask: BlockMask, score=None, scal
                 dq=None, dk=None, dv=None, workspace=None, stream=None, score_param_grad=None):
     """dq, dk, dv (bf16, shaped like q, k, v); with ALiBi, ``score_param_grad``
     (fp32 [H] CUDA tensor) receives dL/dslope of every head."""
+    _check_shapes(q, kv=(("k", k), ("v", v), ("dk", dk), ("dv", dv)),
+                  like_q=(("out", out), ("dout", dout), ("dq", dq)), lse=lse)
     B, H, q_len, D = q.shape
     kv_len = k.shape[2]
     dq = torch.empty_like(q) if dq is None else dq
@@ -415,6 +451,8 @@ def fa_backward_noalloc(q, k, v, out, lse, dout, block_mask: BlockMask, score=No
     """fa_backward without a workspace: for callers that cannot allocate device
     memory at call time (the library's static scratch holds the fp32 dq
     accumulator; see include/fa.h for the size limit and the sharing rules)."""
+    _check_shapes(q, kv=(("k", k), ("v", v), ("dk", dk), ("dv", dv)),
+                  like_q=(("out", out), ("dout", dout), ("dq", dq)), lse=lse)
     B, H, q_len, D = q.shape
     kv_len = k.shape[2]
     dq = torch.empty_like(q) if dq is None else dq

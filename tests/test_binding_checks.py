@@ -45,6 +45,17 @@ def test_forward_decode_refuses_bad_page_tables():
     pool = torch.zeros(4, 10 * 128, 64, dtype=torch.bfloat16)
     with pytest.raises(ValueError, match="page_table"):
         B.fa_forward_decode(q, pool, pool, _Mask(), page_table=torch.zeros(2, 8, dtype=torch.int32))
+    with pytest.raises(ValueError, match="same shape"):
+        B.fa_forward_decode(q, pool, pool[:, :128], _Mask(), page_table=torch.zeros(2, 8, dtype=torch.int32))
+
+
+def test_forward_decode_refuses_keys_shorter_than_the_mask():
+    q = torch.zeros(2, 4, 1, 64, dtype=torch.bfloat16)
+    k = torch.zeros(2, 4, 900, 64, dtype=torch.bfloat16)                      # the mask says 1000 keys
+    with pytest.raises(ValueError, match="kv_len"):
+        B.fa_forward_decode(q, k, k, _Mask(kv_len=1000))
+    with pytest.raises(ValueError, match="q_len"):
+        B.fa_forward_decode(q, k, k, _Mask(q_len=2, kv_len=900))
 
 
 def test_slope_gradient_buffer_checked():
@@ -58,3 +69,39 @@ def test_slope_gradient_buffer_checked():
     spec, _ = B._backward_score(score, None, 4)
     assert spec.op == B.SCORE_OPS["alibi"] and not spec.param_grad
     assert spec is not alibi                                                     # the caller's spec is not modified
+
+
+def test_shape_checks_accept_consistent_tensors():
+    q = torch.zeros(2, 3, 100, 64)
+    k = torch.zeros(2, 3, 250, 64)
+    B._check_shapes(q, kv=(("k", k), ("v", k), ("dk", None)), like_q=(("out", q), ("dq", None)),
+                    lse=torch.zeros(2, 3, 100))
+    B._check_shapes(q)                                                         # nothing else given
+
+
+@pytest.mark.parametrize("bad", ["k_heads", "k_dim", "v_len", "out", "lse", "q_rank"])
+def test_shape_checks_refuse_disagreeing_tensors(bad):
+    q = torch.zeros(2, 3, 100, 64)
+    k = torch.zeros(2, 3, 250, 64)
+    args = {"kv": [("k", k), ("v", k)], "like_q": [("out", q)], "lse": torch.zeros(2, 3, 100)}
+    if bad == "k_heads":
+        args["kv"][0] = ("k", torch.zeros(2, 1, 250, 64))
+    elif bad == "k_dim":
+        args["kv"][0] = ("k", torch.zeros(2, 3, 250, 128))
+    elif bad == "v_len":
+        args["kv"][1] = ("v", torch.zeros(2, 3, 200, 64))
+    elif bad == "out":
+        args["like_q"][0] = ("out", torch.zeros(2, 3, 99, 64))
+    elif bad == "lse":
+        args["lse"] = torch.zeros(2, 3, 101)
+    else:
+        q = q[0]
+    with pytest.raises(ValueError):
+        B._check_shapes(q, **args)
+
+
+def test_forward_refuses_keys_with_other_heads_before_the_library():
+    q = torch.zeros(1, 4, 128, 64, dtype=torch.bfloat16)
+    k = torch.zeros(1, 2, 128, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="k must be"):
+        B.fa_forward(q, k, k, _Mask(q_len=128, kv_len=128))
