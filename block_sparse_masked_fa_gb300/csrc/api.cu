@@ -15,6 +15,7 @@ namespace fa {
 namespace {
 
 constexpr size_t kAlign = 256;
+constexpr int64_t kDecodeMaxHeads = 65535;  // the decode grid's second dimension is B * H
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -392,7 +393,8 @@ fa_status fa_forward_decode_workspace_bytes(int32_t B, int32_t H, int64_t q_len,
   if (bytes == nullptr) return FA_ERR_INVALID_ARG;
   if (B < 1 || H < 1 || q_len < 1 || kv_len < 1) return FA_ERR_SHAPE;
   if (q_len > FA_DECODE_MAX_Q || (D != 64 && D != 128)) return FA_ERR_UNSUPPORTED;
-  if ((int64_t)B * H > (int64_t)INT32_MAX / FA_DECODE_MAX_Q || kv_len > (int64_t)INT32_MAX - 256) return FA_ERR_SHAPE;
+  if ((int64_t)B * H > kDecodeMaxHeads) return FA_ERR_UNSUPPORTED;  // one grid row per (b, h)
+  if (kv_len > (int64_t)INT32_MAX - 256) return FA_ERR_SHAPE;
   int splits = 0;
   size_t need = 0;
   if (decode_plan(B, H, q_len, kv_len, D, &splits, &need) != cudaSuccess) return FA_ERR_CUDA;
@@ -412,6 +414,7 @@ fa_status fa_forward_decode(const void* q, const void* k, const void* v, const i
     if (n_pages < 1 || (int64_t)n_pages * 128 > (int64_t)INT32_MAX) return FA_ERR_SHAPE;
   }
   if (q_len < 1 || q_len > FA_DECODE_MAX_Q) return q_len < 1 ? FA_ERR_SHAPE : FA_ERR_UNSUPPORTED;
+  if ((int64_t)B * H > kDecodeMaxHeads) return FA_ERR_UNSUPPORTED;
   fa_status st = check_attn(B, H, q_len, kv_len, D, bm, score, &scale, false);
   if (st != FA_OK) return st;
   size_t need = 0;

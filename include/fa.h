@@ -280,7 +280,8 @@ fa_status fa_forward_paged(const void* q, const void* k_pool, const void* v_pool
 
 /* Workspace fa_forward_decode needs on the current device (fp32 partial
  * results of every share: splits * B * H * q_len * (D + 1) floats).
- * q_len in [1, FA_DECODE_MAX_Q] (else FA_ERR_UNSUPPORTED); D 64 or 128. */
+ * q_len in [1, FA_DECODE_MAX_Q], D 64 or 128 and B * H <= 65535 (else
+ * FA_ERR_UNSUPPORTED). */
 fa_status fa_forward_decode_workspace_bytes(int32_t B, int32_t H, int64_t q_len, int64_t kv_len, int32_t D,
                                             size_t* bytes);
 

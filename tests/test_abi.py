@@ -236,6 +236,11 @@ def test_forward_decode_rejects():
     assert B._lib.fa_forward_decode_workspace_bytes(1, 1, 17, 1024, 64, ctypes.byref(n)) == UNSUPPORTED
     assert B._lib.fa_forward_decode_workspace_bytes(1, 1, 1, 1024, 80, ctypes.byref(n)) == UNSUPPORTED
     assert B._lib.fa_forward_decode_workspace_bytes(1, 1, 1, 1024, 64, None) == INVALID
+    assert B._lib.fa_forward_decode_workspace_bytes(256, 256, 1, 1024, 64, ctypes.byref(n)) == UNSUPPORTED
+    big = _bm(q=1)
+    big_args = [FAKE, FAKE, FAKE, None, 0, 256, 256, 1, 1024, 64, ctypes.byref(big), ctypes.byref(sc), 0.0,
+                FAKE, FAKE, FAKE, 1 << 30, None]
+    assert B._lib.fa_forward_decode(*big_args) == UNSUPPORTED          # B * H = 65,536 grid rows
 
 
 def test_score_param_grad_rejects():
