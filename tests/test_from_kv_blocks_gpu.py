@@ -9,7 +9,8 @@ patterns of its opening section), CUDA path through the C ABI:
   valid entries;
 * forward and backward match the oracle restricted to the selected tiles on
   every element (mask program on partial tiles, or none), including a
-  decoding shape and an empty selection.
+  decoding shape and an empty selection;
+* a program's EMPTY tiles listed as PARTIAL change nothing (-inf is masked).
 """
 import numpy as np
 import pytest
@@ -222,3 +223,43 @@ def test_empty_selection():
     out, lse, grads = _run_and_check(S, S, 64, 1, 2, sel, None, None, "none", 33, "empty")
     assert torch.all(out == 0) and torch.all(torch.isneginf(lse))
     assert all(torch.all(g == 0) for g in grads)
+
+
+def test_empty_tiles_listed_as_partial_change_nothing():
+    """-inf is the same as masked (tutorial "The two hooks"; speedrun notes,
+    tile summary): listing a program's EMPTY tiles as PARTIAL, where the
+    program hides every pair, leaves out, LSE and the gradients as they were."""
+    S, D, H = 1000, 64, 2
+    docs = make_doc_ids(("geometric", 200.0), S, 41)
+    mask = P(("causal",), ("same_doc",), ("and",), ("window", 300), ("and",))
+    nodes = device_nodes(mask, docs)
+    q, k, v, do = (t.cuda() for t in make_qkv(1, H, S, D, 42))
+    bm1 = fa.fa_create_block_mask(nodes, 1, 1, S, S, 128)
+    L = {n: t.cpu().numpy() for n, t in bm1.lists().items()}
+    cls = bm1.tile_class().cpu().numpy()[0, 0]
+    nq, nkv = cls.shape
+    num = L["kv_num_blocks"].copy()
+    idx = np.zeros((1, 1, nq, nkv), np.int32)
+    added = 0
+    for I in range(nq):
+        part = list(L["kv_indices"][0, 0, I, :num[0, 0, I]])
+        empty = [J for J in range(nkv) if cls[I, J] == 0][:3]       # up to three hidden tiles per row
+        added += len(empty)
+        lst = part + empty
+        idx[0, 0, I, :len(lst)] = lst
+        num[0, 0, I] = len(lst)
+    assert added > 0
+    bm2 = fa.fa_block_mask_from_kv_blocks(torch.as_tensor(num).cuda(), torch.as_tensor(idx).cuda(), S, S,
+                                          bm1.lists()["full_kv_num_blocks"], bm1.lists()["full_kv_indices"],
+                                          nodes=nodes)
+    o1, l1 = fa.fa_forward(q, k, v, bm1)
+    o2, l2 = fa.fa_forward(q, k, v, bm2)
+    g1 = fa.fa_backward(q, k, v, o1, l1, do, bm1)
+    g2 = fa.fa_backward(q, k, v, o2, l2, do, bm2)
+    torch.cuda.synchronize()
+    assert fa.fa_get_status(bm1) == 0 and fa.fa_get_status(bm2) == 0
+    assert int((bm2.tile_class() == 1).sum()) == int((bm1.tile_class() == 1).sum()) + added
+    check_forward(o2.float().cpu().numpy(), l2.cpu().numpy(), o1.float().cpu().numpy(),
+                  l1.cpu().numpy().astype(np.float64), "empty tiles as partial")
+    for a, b, name in zip(g2, g1, ("dq", "dk", "dv")):
+        check_grad(a.float().cpu().numpy(), b.float().cpu().numpy().astype(np.float64), name)
