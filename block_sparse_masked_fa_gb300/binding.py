@@ -225,6 +225,36 @@ class BlockMask:
         s = self.struct
         return self._view("row_segs", (s.Bm, 2, max(s.q_len, s.kv_len), 4))
 
+    def to_string(self, bm: int = 0, hm: int = 0, max_cols: int = 64) -> str:
+        """ASCII map of the tile classes of (bm, hm) and the share of tiles skipped
+        (tutorial, sharp edge 6: check the mask visually)."""
+        s = self.struct
+        return sparsity_map(self.tile_class()[bm, hm].cpu().numpy(), s.block, max_cols)
+
+
+def sparsity_map(cls, block: int, max_cols: int = 64) -> str:
+    """ASCII map of a tile-class grid [nq, nkv] (0 empty, 1 partial, 2 full):
+    '.' every tile of a cell skipped, '#' every tile full, '+' otherwise.  A cell
+    covers ceil(n / max_cols) tiles a side when the grid is wider than max_cols.
+    The last line gives the counts and the share of tiles skipped."""
+    import numpy as np
+
+    cls = np.asarray(cls)
+    nq, nkv = cls.shape
+    f = max(1, -(-max(nq, nkv) // max_cols))
+    lines = []
+    for r0 in range(0, nq, f):
+        row = []
+        for c0 in range(0, nkv, f):
+            cell = cls[r0:r0 + f, c0:c0 + f]
+            row.append("." if not cell.any() else ("#" if (cell == 2).all() else "+"))
+        lines.append("".join(row))
+    empty, part, full = int((cls == 0).sum()), int((cls == 1).sum()), int((cls == 2).sum())
+    total = max(1, cls.size)
+    lines.append(f"{nq} x {nkv} tiles of {block} (one cell: {f} x {f}): {empty} empty, {part} partial, "
+                 f"{full} full; {100.0 * empty / total:.2f}% skipped")
+    return "\n".join(lines)
+
 
 def fa_block_mask_bytes(Bm: int, Hm: int, q_len: int, kv_len: int, block: int = 128) -> int:
     n = ctypes.c_size_t()

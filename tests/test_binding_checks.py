@@ -105,3 +105,16 @@ def test_forward_refuses_keys_with_other_heads_before_the_library():
     k = torch.zeros(1, 2, 128, 64, dtype=torch.bfloat16)
     with pytest.raises(ValueError, match="k must be"):
         B.fa_forward(q, k, k, _Mask(q_len=128, kv_len=128))
+
+
+def test_sparsity_map():
+    """The ASCII map of a causal 4 x 4 tile grid, and a coarsened 8 x 8 one."""
+    import numpy as np
+
+    causal = np.array([[1, 0, 0, 0], [2, 1, 0, 0], [2, 2, 1, 0], [2, 2, 2, 1]])
+    lines = B.sparsity_map(causal, 128).split("\n")
+    assert lines[:4] == ["+...", "#+..", "##+.", "###+"]
+    assert lines[4] == "4 x 4 tiles of 128 (one cell: 1 x 1): 6 empty, 4 partial, 6 full; 37.50% skipped"
+    big = np.kron(causal, np.ones((2, 2), dtype=int))        # 8 x 8, two-by-two cells at max_cols 4
+    lines = B.sparsity_map(big, 64, max_cols=4).split("\n")
+    assert lines[:4] == ["+...", "#+..", "##+.", "###+"] and "one cell: 2 x 2" in lines[4]
