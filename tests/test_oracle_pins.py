@@ -153,6 +153,41 @@ def test_tile_lists_shape_and_order():
     assert L["full_q_num_blocks"].sum() == L["full_kv_num_blocks"].sum()
 
 
+def test_column_lists_causal_closed_form():
+    """Causal key-tile column J: PARTIAL only on the diagonal (row J), FULL on rows J+1 .. n-1
+    (the transpose of the row rule: row I sees J < I whole and J = I in part)."""
+    S = 2048
+    n = S // 128
+    L = oracle.tile_lists(oracle.classify_tiles(oracle.Program(CAUSAL), S, S))
+    for J in range(n):
+        assert L["q_num_blocks"][J] == 1 and L["q_indices"][J, 0] == J
+        assert not L["q_indices"][J, 1:].any()
+        nf = n - 1 - J
+        assert L["full_q_num_blocks"][J] == nf
+        assert list(L["full_q_indices"][J, :nf]) == list(range(J + 1, n))
+        assert not L["full_q_indices"][J, nf:].any()
+
+
+@pytest.mark.parametrize("block", [32, 128])
+def test_column_lists_are_rows_of_the_transposed_mask(block):
+    """On a ragged, non-square mask that is not symmetric (documents, window, sinks), the
+    column lists must equal the row lists of the transposed mask, classified from the numpy
+    twin's dense [kv, q] matrix.  A row / column swap in the list builder fails this."""
+    q_len, kv_len = 1000, 1300
+    docs = make_doc_ids(("geometric", 90.0), kv_len, 11)[0]
+    prog = P(("causal",), ("same_doc",), ("and",), ("window", 300), ("sink", 70), ("or",), ("and",))
+    cp = oracle.Program(prog, doc_row=docs)
+    L = oracle.tile_lists(oracle.classify_tiles(cp, q_len, kv_len, block))
+    M = oracle.np_mask(prog, q_len, kv_len, doc_row=docs)
+    LT = oracle.tile_lists(oracle.np_classify(np.ascontiguousarray(M.T), block))
+    assert L["q_num_blocks"].shape == (-(-kv_len // block),)
+    assert L["q_indices"].shape == (-(-kv_len // block), -(-q_len // block))
+    for mine, theirs in (("q", "kv"), ("full_q", "full_kv")):
+        np.testing.assert_array_equal(L[f"{mine}_num_blocks"], LT[f"{theirs}_num_blocks"])
+        np.testing.assert_array_equal(L[f"{mine}_indices"], LT[f"{theirs}_indices"])
+    assert L["q_num_blocks"].sum() > 0 and L["full_q_num_blocks"].sum() > 0
+
+
 # ---------------------------------------------------------------- forward
 
 def _qkv(S, D, seed, kv_len=None):
