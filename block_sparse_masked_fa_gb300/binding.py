@@ -262,6 +262,12 @@ def fa_block_mask_bytes(Bm: int, Hm: int, q_len: int, kv_len: int, block: int = 
     return n.value
 
 
+def _check_buffer(buffer: torch.Tensor):
+    """A block-mask buffer is a contiguous uint8 CUDA tensor (its numel is the byte count the library checks)."""
+    if buffer.dtype != torch.uint8 or not buffer.is_contiguous() or not buffer.is_cuda:
+        raise ValueError("the block-mask buffer must be a contiguous uint8 CUDA tensor")
+
+
 def fa_create_block_mask(nodes: Sequence[tuple], Bm: int, Hm: int, q_len: int, kv_len: int, block: int = 128,
                          buffer: Optional[torch.Tensor] = None, stream=None) -> BlockMask:
     """Builds the block mask of a postfix mask program (see make_mask_spec)."""
@@ -269,6 +275,7 @@ def fa_create_block_mask(nodes: Sequence[tuple], Bm: int, Hm: int, q_len: int, k
     nbytes = fa_block_mask_bytes(Bm, Hm, q_len, kv_len, block)
     if buffer is None:
         buffer = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    _check_buffer(buffer)
     st = BlockMaskStruct()
     _check(_lib.fa_create_block_mask(ctypes.byref(spec), Bm, Hm, q_len, kv_len, block, buffer.data_ptr(),
                                      buffer.numel(), ctypes.byref(st), _stream(stream)), "fa_create_block_mask")
@@ -306,6 +313,7 @@ def fa_block_mask_from_kv_blocks(kv_num_blocks: torch.Tensor, kv_indices: torch.
     nbytes = fa_block_mask_bytes(Bm, Hm, q_len, kv_len, block)
     if buffer is None:
         buffer = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    _check_buffer(buffer)
     st = BlockMaskStruct()
     _check(_lib.fa_block_mask_from_kv_blocks(_ptr(kv_num_blocks), _ptr(kv_indices), _ptr(full_kv_num_blocks),
                                              _ptr(full_kv_indices), kv_indices.shape[3],
@@ -340,6 +348,31 @@ def _check_shapes(q, kv=(), like_q=(), lse=None):
         raise ValueError(f"lse must be [{B}, {H}, {q_len}], got {tuple(lse.shape)}")
 
 
+_BF16, _F32, _I32, _U8 = torch.bfloat16, torch.float32, torch.int32, torch.uint8
+
+
+def _check_storage(q, tensors):
+    """Refuses tensors the kernels cannot address as plain dense arrays: the
+    library gets bare device pointers and builds its tensor maps (and the dq
+    conversion its indexing) on dense [B, H, len, D] storage, so an expanded,
+    transposed or sliced view would make it read and write outside the tensor.
+    Each (name, tensor, dtype) must have that dtype, be contiguous and live on
+    q's CUDA device; None entries are skipped.  q itself is checked as bf16."""
+    given = [(name, t, dtype) for name, t, dtype in (("q", q, _BF16),) + tuple(tensors) if t is not None]
+    for name, t, dtype in given:
+        if t.dtype != dtype:
+            raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    for name, t, _ in given:
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous (an expanded, transposed or sliced view is not), "
+                             f"got strides {tuple(t.stride())} for shape {tuple(t.shape)}")
+    for name, t, _ in given:
+        if not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
+        if t.device != q.device:
+            raise ValueError(f"{name} is on {t.device}, q on {q.device}")
+
+
 def _score(score):
     if score is None:
         return make_score_spec("none")
@@ -359,6 +392,7 @@ def fa_forward(q, k, v, block_mask: BlockMask, score=None, scale: float = 0.0, o
         out = torch.empty_like(q)
     if lse is None:
         lse = torch.empty(B, H, q_len, dtype=torch.float32, device=q.device)
+    _check_storage(q, (("k", k, _BF16), ("v", v, _BF16), ("out", out, _BF16), ("lse", lse, _F32)))
     sspec, keep = _score(score)
     _check(_lib.fa_forward(_ptr(q), _ptr(k), _ptr(v), B, H, q_len, kv_len, D, ctypes.byref(block_mask.struct),
                            ctypes.byref(sspec), float(scale), _ptr(out), _ptr(lse), _stream(stream)), "fa_forward")
@@ -397,6 +431,8 @@ def fa_forward_paged(q, k_pool, v_pool, page_table, block_mask: BlockMask, score
         out = torch.empty_like(q)
     if lse is None:
         lse = torch.empty(B, H, q_len, dtype=torch.float32, device=q.device)
+    _check_storage(q, (("k_pool", k_pool, _BF16), ("v_pool", v_pool, _BF16), ("page_table", page_table, _I32),
+                       ("out", out, _BF16), ("lse", lse, _F32)))
     sspec, keep = _score(score)
     _check(_lib.fa_forward_paged(_ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(page_table), k_pool.shape[1] // 128, B, H,
                                  q_len, kv_len, D, ctypes.byref(block_mask.struct), ctypes.byref(sspec), float(scale),
@@ -442,6 +478,8 @@ def fa_forward_decode(q, k, v, block_mask: BlockMask, score=None, scale: float =
     if workspace is None:
         workspace = torch.empty(fa_forward_decode_workspace_bytes(B, H, q_len, kv_len, D), dtype=torch.uint8,
                                 device=q.device)
+    _check_storage(q, (("k", k, _BF16), ("v", v, _BF16), ("page_table", page_table, _I32), ("out", out, _BF16),
+                       ("lse", lse, _F32), ("workspace", workspace, _U8)))
     sspec, keep = _score(score)
     _check(_lib.fa_forward_decode(_ptr(q), _ptr(k), _ptr(v), _ptr(page_table), n_pages, B, H, q_len, kv_len, D,
                                   ctypes.byref(block_mask.struct), ctypes.byref(sspec), float(scale), _ptr(out),
@@ -454,6 +492,11 @@ def fa_backward_workspace_bytes(B: int, H: int, q_len: int, D: int) -> int:
     n = ctypes.c_size_t()
     _check(_lib.fa_backward_workspace_bytes(B, H, q_len, D, ctypes.byref(n)), "fa_backward_workspace_bytes")
     return n.value
+
+
+def _backward_tensors(k, v, out, lse, dout, dq, dk, dv):
+    return (("k", k, _BF16), ("v", v, _BF16), ("out", out, _BF16), ("lse", lse, _F32), ("dout", dout, _BF16),
+            ("dq", dq, _BF16), ("dk", dk, _BF16), ("dv", dv, _BF16))
 
 
 def fa_backward(q, k, v, out, lse, dout, block_mask: BlockMask, score=None, scale: float = 0.0,
@@ -469,6 +512,7 @@ def fa_backward(q, k, v, out, lse, dout, block_mask: BlockMask, score=None, scal
     dv = torch.empty_like(v) if dv is None else dv
     if workspace is None:
         workspace = torch.empty(fa_backward_workspace_bytes(B, H, q_len, D), dtype=torch.uint8, device=q.device)
+    _check_storage(q, _backward_tensors(k, v, out, lse, dout, dq, dk, dv) + (("workspace", workspace, _U8),))
     sspec, keep = _backward_score(score, score_param_grad, H)
     _check(_lib.fa_backward(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout), B, H, q_len, kv_len, D,
                             ctypes.byref(block_mask.struct), ctypes.byref(sspec), float(scale), _ptr(dq), _ptr(dk),
@@ -488,6 +532,7 @@ def fa_backward_noalloc(q, k, v, out, lse, dout, block_mask: BlockMask, score=No
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
+    _check_storage(q, _backward_tensors(k, v, out, lse, dout, dq, dk, dv))
     sspec, keep = _backward_score(score, score_param_grad, H)
     _check(_lib.fa_backward_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout), B, H, q_len, kv_len,
                                     D, ctypes.byref(block_mask.struct), ctypes.byref(sspec), float(scale), _ptr(dq),

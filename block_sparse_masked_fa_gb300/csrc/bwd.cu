@@ -857,16 +857,14 @@ cudaError_t launch_bwd_t(const AttnArgs& a, const BwdTensors& t, cudaStream_t st
     return cudaErrorUnknown;
   }
   constexpr size_t smem = bwd_smem_bytes<D>();
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e =
-        cudaFuncSetAttribute(bwd_kernel<D, SCORE, PGRAD>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static PerDeviceOnce attr_once;
+  cudaError_t e = attr_once.run([] {
+    return cudaFuncSetAttribute(bwd_kernel<D, SCORE, PGRAD>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  });
+  if (e != cudaSuccess) return e;
   // persistent: one CTA per SM (or per item, when there are fewer)
   int dev = 0, sms = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
   const int64_t items = (int64_t)a.B * a.H * a.nkv;

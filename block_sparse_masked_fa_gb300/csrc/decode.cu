@@ -411,17 +411,17 @@ cudaError_t launch_decode_t(const AttnArgs& a, const FwdTensors& t, float* ws, i
     return cudaErrorUnknown;
   }
   constexpr size_t smem = dec_smem_bytes<D>();
-  static bool attr_set = false;
-  if (!attr_set) {
+  static PerDeviceOnce attr_once;
+  cudaError_t e0 = attr_once.run([] {
     cudaError_t e = cudaFuncSetAttribute(decode_partial_kernel<D, SCORE, QB>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     // all of the unified L1 as shared memory, so that two CTAs fit an SM at D = 64
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(decode_partial_kernel<D, SCORE, QB>,
                                cudaFuncAttributePreferredSharedMemoryCarveout, 100);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+    return e;
+  });
+  if (e0 != cudaSuccess) return e0;
   const int64_t rows = (int64_t)bh * a.q_len;
   float* ws_out = ws;
   float* ws_lse = ws + (size_t)splits * rows * D;

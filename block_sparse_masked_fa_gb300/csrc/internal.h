@@ -3,9 +3,34 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <mutex>
+
 #include "common.cuh"
 
 namespace fa {
+
+// Runs a setter once per device: function attributes such as the dynamic
+// shared-memory limit belong to the device that was current when they were set,
+// so a launcher keeps one flag per device index, guarded against host threads
+// that launch at the same time.  A failed setter is retried on the next call.
+struct PerDeviceOnce {
+  static constexpr int kMaxDevices = 64;
+  std::mutex mu;
+  bool done[kMaxDevices] = {};
+
+  template <typename F>
+  cudaError_t run(F&& setter) {
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu);
+    if (done[dev]) return cudaSuccess;
+    e = setter();
+    if (e == cudaSuccess) done[dev] = true;
+    return e;
+  }
+};
 
 struct BuildArgs {
   DevMask mask;

@@ -332,7 +332,10 @@ fa_status fa_backward(const void* q, const void* k, const void* v, const void* o
  *    rows at D = 128 or 63,000 rows at D = 64).
  *  - Set-up: the first call on each device looks up the array's device address
  *    (cudaGetSymbolAddress, with that device current) and caches it; make that
- *    first call before any stream capture.
+ *    first call before any stream capture.  The cached address belongs to the
+ *    device's context: after cudaDeviceReset (or any loss of the primary
+ *    context) it is stale, so a device that was reset must not be used with
+ *    this entry point again in the same process.
  *  - Sharing: all calls on a device use the same array, which keeps the last
  *    call's contents; each call re-initialises the part it uses.  Calls whose
  *    GPU work overlaps (different streams, no ordering between them) race on

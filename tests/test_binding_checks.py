@@ -118,3 +118,64 @@ def test_sparsity_map():
     big = np.kron(causal, np.ones((2, 2), dtype=int))        # 8 x 8, two-by-two cells at max_cols 4
     lines = B.sparsity_map(big, 64, max_cols=4).split("\n")
     assert lines[:4] == ["+...", "#+..", "##+.", "###+"] and "one cell: 2 x 2" in lines[4]
+
+
+def _fwd_args(S=128, D=64):
+    q = torch.zeros(1, 4, S, D, dtype=torch.bfloat16)
+    return q, q.clone(), q.clone()
+
+
+@pytest.mark.parametrize("bad", ["k_expand", "q_transpose", "v_float32", "lse_float64", "out_slice"])
+def test_forward_refuses_views_and_wrong_dtypes(bad):
+    """Views the kernels cannot address as dense [B, H, len, D] arrays (expanded, transposed,
+    sliced) and tensors of another dtype are refused before the library is called."""
+    q, k, v = _fwd_args()
+    out = lse = None
+    match = "contiguous"
+    if bad == "k_expand":
+        k = torch.zeros(1, 1, 128, 64, dtype=torch.bfloat16).expand(1, 4, 128, 64)
+    elif bad == "q_transpose":
+        q = torch.zeros(1, 4, 64, 128, dtype=torch.bfloat16).transpose(2, 3)
+    elif bad == "v_float32":
+        v, match = v.float(), "v must be torch.bfloat16"
+    elif bad == "lse_float64":
+        lse, match = torch.zeros(1, 4, 128, dtype=torch.float64), "lse must be torch.float32"
+    else:
+        out = torch.zeros(1, 4, 128, 128, dtype=torch.bfloat16)[..., :64]
+    with pytest.raises(ValueError, match=match):
+        B.fa_forward(q, k, v, _Mask(q_len=128, kv_len=128), out=out, lse=lse)
+
+
+def test_forward_refuses_host_tensors():
+    q, k, v = _fwd_args()
+    with pytest.raises(ValueError, match="CUDA"):
+        B.fa_forward(q, k, v, _Mask(q_len=128, kv_len=128))
+
+
+@pytest.mark.parametrize("bad", ["dq_expand", "dk_float32", "dout_transpose", "workspace_float32"])
+def test_backward_refuses_views_and_wrong_dtypes(bad):
+    q, k, v = _fwd_args()
+    out, dout = q.clone(), q.clone()
+    lse = torch.zeros(1, 4, 128)
+    kw = {}
+    match = "contiguous"
+    if bad == "dq_expand":
+        kw["dq"] = torch.zeros(1, 1, 128, 64, dtype=torch.bfloat16).expand(1, 4, 128, 64)
+    elif bad == "dk_float32":
+        kw["dk"], match = torch.zeros(1, 4, 128, 64), "dk must be torch.bfloat16"
+    elif bad == "dout_transpose":
+        dout = torch.zeros(1, 4, 64, 128, dtype=torch.bfloat16).transpose(2, 3)
+    else:
+        kw["workspace"], match = torch.zeros(16, dtype=torch.float32), "workspace must be torch.uint8"
+    with pytest.raises(ValueError, match=match):
+        B.fa_backward(q, k, v, out, lse, dout, _Mask(q_len=128, kv_len=128), **kw)
+    if bad != "workspace_float32":
+        with pytest.raises(ValueError, match=match):
+            B.fa_backward_noalloc(q, k, v, out, lse, dout, _Mask(q_len=128, kv_len=128), **kw)
+
+
+def test_block_mask_buffer_checked():
+    with pytest.raises(ValueError, match="buffer"):
+        B._check_buffer(torch.zeros(64, dtype=torch.uint8))                  # host memory
+    with pytest.raises(ValueError, match="buffer"):
+        B._check_buffer(torch.zeros(64, dtype=torch.int32))
