@@ -1,11 +1,14 @@
 """Throughput of the tile-sparse masked attention hot path on one GB300.
 
 A step is one pass of the whole path over one batch of synthetic input:
-fa_create_block_mask + fa_forward + fa_backward, on the packed 64K-token
-workload (B=1, H=6, S=65536, D=128, causal & same document & 1024 window,
-log-normal document lengths).  The metric is attention TFLOP/s counted over
-visible tiles only: forward 4*128*128*D per visible tile per (b, h), backward
-2.5x that (five tile GEMMs against two).
+fa_create_block_mask + fa_forward + fa_backward.  The default workload is the
+largest single-GPU one, the window-growth sweep (B=1, H=16, S=65536, D=128,
+causal & same document & window W, ALiBi, log-normal document lengths): one
+step runs the path once for every W of the sweep, 64..1792 in steps of 64,
+each W read by the kernels from a device int32 (no rebuild).  The metric is
+attention TFLOP/s counted over visible tiles only: forward 4*128*128*D per
+visible tile per (b, h), backward 2.5x that (five tile GEMMs against two).
+The other workloads are timed in the same run for the per-config keys.
 
 Prints ONE JSON line (rank 0).  --impl reference times the CPU oracle on a
 bounded sample of the same workload instead.
@@ -13,6 +16,7 @@ bounded sample of the same workload instead.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import os
 import statistics
@@ -258,6 +262,125 @@ def reduce_over_ranks(dist, device, times_ms, work):
     return [float(x) for x in t.tolist()], float(f.item())
 
 
+class Problem:
+    """One workload resident on the device: inputs, outputs, the backward's
+    workspace, the block-mask buffer and one mask spec per window of the sweep
+    (one spec for a fixed mask).  Every spec of a sweep reads its W from its own
+    element of one device int32 tensor, so the sweep changes W with no rebuild of
+    anything but the block mask (speedrun notes, Record #13)."""
+
+    def __init__(self, fa, w, dev, host, windows):
+        import torch
+
+        self.fa, self.w, self.dev = fa, w, dev
+        q_h, k_h, v_h, do_h, docs_np = host
+        self.q, self.k, self.v, self.do = (t.to(dev) for t in (q_h, k_h, v_h, do_h))
+        self.docs = torch.as_tensor(docs_np, dtype=torch.int32, device=dev) if docs_np is not None else None
+        self.windows = list(windows)
+        self.W = torch.tensor([x or 0 for x in self.windows], dtype=torch.int32, device=dev)
+        self.specs = [fa.make_mask_spec(mask_nodes(w, self.docs, self.W[i:i + 1]), device=dev)
+                      for i in range(len(self.windows))]
+        self.score = None
+        if w.score[0] == "softcap":
+            self.score = fa.make_score_spec("softcap", [float(w.score[1])], device=dev)
+        elif w.score[0] == "alibi":
+            from synth import make_alibi_slopes
+            self.score = fa.make_score_spec("alibi", torch.as_tensor(make_alibi_slopes(w.H)), device=dev)
+        self.bm_buf = torch.empty(fa.fa_block_mask_bytes(1, 1, w.S, w.S, 128), dtype=torch.uint8, device=dev)
+        self.ws = torch.empty(fa.fa_backward_workspace_bytes(w.B, w.H, w.S, w.D), dtype=torch.uint8, device=dev)
+        self.out = torch.empty_like(self.q)
+        self.lse = torch.empty(w.B, w.H, w.S, dtype=torch.float32, device=dev)
+        self.dq, self.dk, self.dv = (torch.empty_like(t) for t in (self.q, self.k, self.v))
+
+    def sub_step(self, i, stream, ev=None):
+        """Block mask of window i, forward, backward; events 0..3 around them when given."""
+        fa, w = self.fa, self.w
+        if ev:
+            ev[0].record(stream)
+        bm = fa.fa_create_block_mask(self.specs[i], 1, 1, w.S, w.S, 128, buffer=self.bm_buf)
+        if ev:
+            ev[1].record(stream)
+        fa.fa_forward(self.q, self.k, self.v, bm, score=self.score, out=self.out, lse=self.lse)
+        if ev:
+            ev[2].record(stream)
+        fa.fa_backward(self.q, self.k, self.v, self.out, self.lse, self.do, bm, score=self.score, dq=self.dq,
+                       dk=self.dk, dv=self.dv, workspace=self.ws)
+        if ev:
+            ev[3].record(stream)
+        return bm
+
+    def visible_tiles(self, stream):
+        """Visible tiles (all b, h) of every window's block mask."""
+        import torch
+
+        out = []
+        for i in range(len(self.windows)):
+            bm = self.fa.fa_create_block_mask(self.specs[i], 1, 1, self.w.S, self.w.S, 128, buffer=self.bm_buf)
+            torch.cuda.synchronize()
+            out.append(visible_tiles(self.fa, bm, self.w.B, self.w.H))
+        return out
+
+
+def launches_per_sub_step(w):
+    # builder: tile_summary + doc_runs (documents only) + row_segs + classify + compact + order;
+    # forward 1; backward pre + main + dq convert
+    return (6 if w.docs is not None else 4) + 1 + 3
+
+
+def timed_steps(prob, stream, steps):
+    """Runs `steps` steps (each a pass over every window) between CUDA events on
+    `stream`; returns total ms and per-window summed ms of build, forward, backward."""
+    import torch
+
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+    n = len(prob.windows)
+    marks = []
+    t0, t1 = ev(), ev()
+    t0.record(stream)
+    for _ in range(steps):
+        for i in range(n):
+            e = [ev() for _ in range(4)]
+            prob.sub_step(i, stream, e)
+            marks.append((i, e))
+    t1.record(stream)
+    torch.cuda.synchronize()
+    per = [[0.0, 0.0, 0.0] for _ in range(n)]
+    for i, e in marks:
+        for j in range(3):
+            per[i][j] += e[j].elapsed_time(e[j + 1])
+    return t0.elapsed_time(t1), per
+
+
+def tile_flops(n_vis, D):
+    """Forward FLOPs of n_vis visible 128 x 128 tiles at head dim D (two tile GEMMs)."""
+    return n_vis * 4.0 * 128 * 128 * D
+
+
+def per_config(fa, w, dev, steps, warmup, peak):
+    """Device-timed fwd / bwd throughput of one more workload (no e2e): the same
+    step as the headline, for the per-config keys of the line."""
+    import torch
+
+    prob = Problem(fa, w, dev, workload_tensors(w), [None])
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        prob.sub_step(0, stream)
+    n_vis = prob.visible_tiles(stream)[0]
+    ms, per = timed_steps(prob, stream, steps)
+    assert fa.fa_get_status(prob.sub_step(0, stream)) == 0
+    ff = tile_flops(n_vis, w.D)
+    b, f, d = (x / steps for x in per[0])
+    res = {"workload": w.name, "visible_tiles": int(n_vis), "ms_per_step": round(ms / steps, 4),
+           "tflops": round(3.5 * ff / (ms / steps * 1e-3) / 1e12, 2),
+           "build_ms": round(b, 4), "fwd_ms": round(f, 4), "bwd_ms": round(d, 4),
+           "fwd_tflops": round(ff / (f * 1e-3) / 1e12, 2), "bwd_tflops": round(2.5 * ff / (d * 1e-3) / 1e12, 2)}
+    res["fwd_frac"] = round(res["fwd_tflops"] / peak, 4)
+    res["bwd_frac"] = round(res["bwd_tflops"] / peak, 4)
+    del prob
+    torch.cuda.empty_cache()
+    return res
+
+
 def run_gpu(args):
     import torch
     import torch.distributed as dist
@@ -270,62 +393,26 @@ def run_gpu(args):
         dist.init_process_group("nccl")
 
     w = WORKLOADS[args.workload]
-    q_h, k_h, v_h, do_h, docs_np = workload_tensors(w, seed=replica_seed(w, rank))
+    if args.heads:
+        if not args.profile:
+            raise SystemExit("--heads is for --profile runs only (the headline keeps the workload's heads)")
+        w = dataclasses.replace(w, H=args.heads)
     dev = torch.device("cuda", local)
-    q, k, v, do = (t.to(dev) for t in (q_h, k_h, v_h, do_h))
-    docs = torch.as_tensor(docs_np, dtype=torch.int32, device=dev) if docs_np is not None else None
-    W = torch.tensor([args.window if w.windows else 1024], dtype=torch.int32, device=dev)
-    nodes = mask_nodes(w, docs, W)
-    spec, keep = fa.make_mask_spec(nodes, device=dev)
-    score = None
-    if w.score[0] == "softcap":
-        score = fa.make_score_spec("softcap", [float(w.score[1])], device=dev)
-    elif w.score[0] == "alibi":
-        from synth import make_alibi_slopes
-        score = fa.make_score_spec("alibi", torch.as_tensor(make_alibi_slopes(w.H)), device=dev)
+    windows = [args.window] if (w.windows and args.window) else (list(w.windows) or [None])
+    host = workload_tensors(w, seed=replica_seed(w, rank))
+    prob = Problem(fa, w, dev, host, windows)
     stream = torch.cuda.current_stream()
-    bm_buf = torch.empty(fa.fa_block_mask_bytes(1, 1, w.S, w.S, 128), dtype=torch.uint8, device=dev)
-    ws = torch.empty(fa.fa_backward_workspace_bytes(w.B, w.H, w.S, w.D), dtype=torch.uint8, device=dev)
-    out = torch.empty_like(q)
-    lse = torch.empty(w.B, w.H, w.S, dtype=torch.float32, device=dev)
-    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-
-    have_bwd = True
-    bm0 = fa.fa_create_block_mask((spec, keep), 1, 1, w.S, w.S, 128, buffer=bm_buf)
-    fa.fa_forward(q, k, v, bm0, score=score, out=out, lse=lse)
-    try:
-        fa.fa_backward(q, k, v, out, lse, do, bm0, score=score, dq=dq, dk=dk, dv=dv, workspace=ws)
-    except fa.FaError:
-        have_bwd = False
-    torch.cuda.synchronize()
-
-    ev = lambda: torch.cuda.Event(enable_timing=True)
-    marks = []
-
-    def step(record):
-        e = [ev() for _ in range(4)] if record else None
-        if record:
-            e[0].record(stream)
-        bm = fa.fa_create_block_mask((spec, keep), 1, 1, w.S, w.S, 128, buffer=bm_buf)
-        if record:
-            e[1].record(stream)
-        fa.fa_forward(q, k, v, bm, score=score, out=out, lse=lse)
-        if record:
-            e[2].record(stream)
-        if have_bwd:
-            fa.fa_backward(q, k, v, out, lse, do, bm, score=score, dq=dq, dk=dk, dv=dv, workspace=ws)
-        if record:
-            e[3].record(stream)
-            marks.append(e)
-        return bm
+    n_sub = len(windows)
 
     for _ in range(args.warmup):
-        bm = step(False)
+        for i in range(n_sub):
+            prob.sub_step(i, stream)
     torch.cuda.synchronize()
-    n_vis = visible_tiles(fa, bm, w.B, w.H)
-    fwd_flops = n_vis * 4.0 * 128 * 128 * w.D
+    n_vis = prob.visible_tiles(stream)
+    fwd_w = [tile_flops(n, w.D) for n in n_vis]
+    fwd_flops = sum(fwd_w)
     bwd_flops = 2.5 * fwd_flops
-    step_flops = fwd_flops + (bwd_flops if have_bwd else 0.0)
+    step_flops = fwd_flops + bwd_flops
 
     clocks = ClockSampler(local)
     clocks.start()
@@ -333,106 +420,37 @@ def run_gpu(args):
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
-    t0, t1 = ev(), ev()
-    t0.record(stream)
-    for _ in range(args.steps):
-        step(True)
-    t1.record(stream)
-    torch.cuda.synchronize()
+    ms_total, per = timed_steps(prob, stream, args.steps)
     if world > 1:
         dist.barrier()
     clk = clocks.stop()
-    ms_total = t0.elapsed_time(t1)
-    build_ms = sum(m[0].elapsed_time(m[1]) for m in marks) / args.steps
-    fwd_ms = sum(m[1].elapsed_time(m[2]) for m in marks) / args.steps
-    bwd_ms = sum(m[2].elapsed_time(m[3]) for m in marks) / args.steps
-    assert fa.fa_get_status(bm) == 0, "device status reported an error"
-
-    # end to end through the public API: every step copies its inputs in from
-    # pinned host memory and its results back.  Two device buffer sets and three
-    # streams let the copies of one step overlap the compute of its neighbours
-    # (the inputs of step i + 1 load while step i computes, the results of step
-    # i return while step i + 1 computes), as a training loop that prefetches
-    # its batches does; each step still moves all of its own bytes.
-    pin = lambda t: t.pin_memory()
-    hq, hk, hv, hdo = (pin(t) for t in (q_h, k_h, v_h, do_h))
-    hdocs = pin(torch.as_tensor(docs_np, dtype=torch.int32)) if docs_np is not None else None
-    h_out, h_lse = pin(torch.empty_like(q_h)), pin(torch.empty(w.B, w.H, w.S, dtype=torch.float32))
-    h_dq, h_dk, h_dv = (pin(torch.empty_like(t)) for t in (q_h, k_h, v_h))
-    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo)) + \
-        (hdocs.numel() * 4 if hdocs is not None else 0)
-    d2h = h_out.numel() * 2 + h_lse.numel() * 4 + (3 * h_dq.numel() * 2 if have_bwd else 0)
-
-    sets = [dict(q=q, k=k, v=v, do=do, docs=docs, spec=(spec, keep), out=out, lse=lse, dq=dq, dk=dk, dv=dv)]
-    q2, k2, v2, do2 = (torch.empty_like(t) for t in (q, k, v, do))
-    docs2 = torch.empty_like(docs) if docs is not None else None
-    nodes2 = [("same_doc", docs2) if nd[0] == "same_doc" else nd for nd in nodes]
-    sets.append(dict(q=q2, k=k2, v=v2, do=do2, docs=docs2, spec=fa.make_mask_spec(nodes2, device=dev),
-                     out=torch.empty_like(out), lse=torch.empty_like(lse), dq=torch.empty_like(dq),
-                     dk=torch.empty_like(dk), dv=torch.empty_like(dv)))
-    s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
-    ev_in, ev_comp, ev_out = ([torch.cuda.Event() for _ in range(2)] for _ in range(3))
-
-    def e2e_step(i):
-        b = i % 2
-        st = sets[b]
-        with torch.cuda.stream(s_in):  # this set's inputs, once step i - 2 has finished with them
-            s_in.wait_event(ev_comp[b])
-            st["q"].copy_(hq, non_blocking=True)
-            st["k"].copy_(hk, non_blocking=True)
-            st["v"].copy_(hv, non_blocking=True)
-            st["do"].copy_(hdo, non_blocking=True)
-            if hdocs is not None:
-                st["docs"].copy_(hdocs, non_blocking=True)
-            ev_in[b].record(s_in)
-        stream.wait_event(ev_in[b])
-        stream.wait_event(ev_out[b])  # step i - 2's results have left this set
-        bm = fa.fa_create_block_mask(st["spec"], 1, 1, w.S, w.S, 128, buffer=bm_buf)
-        fa.fa_forward(st["q"], st["k"], st["v"], bm, score=score, out=st["out"], lse=st["lse"])
-        if have_bwd:
-            fa.fa_backward(st["q"], st["k"], st["v"], st["out"], st["lse"], st["do"], bm, score=score,
-                           dq=st["dq"], dk=st["dk"], dv=st["dv"], workspace=ws)
-        ev_comp[b].record(stream)
-        with torch.cuda.stream(s_out):
-            s_out.wait_event(ev_comp[b])
-            h_out.copy_(st["out"], non_blocking=True)
-            h_lse.copy_(st["lse"], non_blocking=True)
-            if have_bwd:
-                h_dq.copy_(st["dq"], non_blocking=True)
-                h_dk.copy_(st["dk"], non_blocking=True)
-                h_dv.copy_(st["dv"], non_blocking=True)
-            ev_out[b].record(s_out)
-        return bm
-
-    for i in range(2):
-        e2e_step(i)
-    torch.cuda.synchronize()
-    e0, e1 = ev(), ev()
-    e2e_steps = max(4, args.steps // 2)
-    e0.record(s_in)
-    for i in range(e2e_steps):
-        e2e_step(i)
-    e1.record(s_out)
-    torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / e2e_steps
-    job_flops = step_flops  # the work of all ranks
-    if world > 1:
-        (ms_total, e2e_ms), job_flops = reduce_over_ranks(dist, dev, (ms_total, e2e_ms), step_flops)
-    ms_step = ms_total / args.steps
-    assert torch.equal(h_out, out.cpu()), "e2e results differ from the device-timed run"
+    build_ms = sum(p[0] for p in per) / args.steps
+    fwd_ms = sum(p[1] for p in per) / args.steps
+    bwd_ms = sum(p[2] for p in per) / args.steps
+    assert fa.fa_get_status(prob.sub_step(n_sub - 1, stream)) == 0, "device status reported an error"
 
     peaks, peak_src = load_peaks()
     peak = float(peaks["bf16_tflops"])
-    dominant = "bwd" if (have_bwd and bwd_ms > fwd_ms) else "fwd"
+    e2e = None
+    if not args.profile:
+        ref_out = prob.out.cpu()  # the last window's output, for the e2e run's check
+        e2e = run_e2e(fa, w, dev, host, windows, prob, stream, max(4, args.steps // 2), ref_out)
+    job_flops = step_flops  # the work of all ranks
+    e2e_ms = e2e["ms"] if e2e else 0.0
+    if world > 1:
+        (ms_total, e2e_ms), job_flops = reduce_over_ranks(dist, dev, (ms_total, e2e_ms), step_flops)
+    ms_step = ms_total / args.steps
+
+    dominant = "bwd" if bwd_ms > fwd_ms else "fwd"
     dom_ms = bwd_ms if dominant == "bwd" else fwd_ms
     dom_flops = bwd_flops if dominant == "bwd" else fwd_flops
     achieved = dom_flops / (dom_ms * 1e-3) / 1e12
     value = job_flops / (ms_step * 1e-3) / 1e12
-    # builder: (tile_summary + doc_runs) + row_segs + classify + compact + order; forward 1;
-    # backward pre + main + dq convert
-    launches_per_step = (6 if docs is not None else 4) + 1 + (3 if have_bwd else 0)
+    sweep = len(windows) > 1
+    name = w.name + (f" (W {windows[0]}..{windows[-1]} step {windows[1] - windows[0]}, one sweep of "
+                     f"{len(windows)} windows per step)" if sweep else (f" (W {windows[0]})" if windows[0] else ""))
     res = {
-        "metric": METRIC if have_bwd else "attention TFLOP/s over visible tiles (fwd only; bwd not built)",
+        "metric": METRIC,
         "value": round(value, 2),
         "unit": "TFLOP/s",
         "n_gpus": world,
@@ -444,34 +462,113 @@ def run_gpu(args):
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) q/k/v/dO in bf16, log-normal document lengths)",
-        "config": {"workload": w.name, "B": w.B, "H": w.H, "S": w.S, "D": w.D,
-                   "mask": " ".join(n[0] if len(n) == 1 else f"{n[0]}:{n[1]}" for n in w.mask.nodes),
-                   "score_mod": w.score[0], "block": 128, "visible_tiles": int(n_vis),
-                   "l2": "inputs larger than L2 (q, k, v, dO: 4 x %d MiB)" % (q.numel() * 2 >> 20),
+        "config": {"workload": name, "B": w.B, "H": w.H, "S": w.S, "D": w.D,
+                   "mask": " ".join(n[0] if len(n) == 1 else f"{n[0]}:{n[1]}" for n in w.mask.nodes)
+                   + (" (W from a device int32, swept)" if sweep else ""),
+                   "score_mod": w.score[0], "block": 128, "visible_tiles": int(sum(n_vis)),
+                   "l2": "inputs larger than L2 (q, k, v, dO: 4 x %d MiB)" % (prob.q.numel() * 2 >> 20),
                    "parallelism": f"replicas x{world}"},
         "breakdown_ms": {"create_block_mask": round(build_ms, 4), "forward": round(fwd_ms, 4),
-                         "backward": round(bwd_ms, 4) if have_bwd else None},
+                         "backward": round(bwd_ms, 4)},
         "fwd_tflops": round(fwd_flops / (fwd_ms * 1e-3) / 1e12, 2),
-        "bwd_tflops": round(bwd_flops / (bwd_ms * 1e-3) / 1e12, 2) if have_bwd else None,
+        "bwd_tflops": round(bwd_flops / (bwd_ms * 1e-3) / 1e12, 2),
         "roofline": {"kernel": dominant, "bound": "tensor", "achieved": round(achieved, 2), "peak": peak,
                      "peak_source": f"bf16_tflops ({peak_src}, burst)", "unit": "TFLOP/s",
                      "frac": round(achieved / peak, 4),
                      "traffic": recorded_traffic("bwd_kernel" if dominant == "bwd" else "fwd_kernel", w.name)},
-        "e2e": {"value": round(job_flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
-                "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-                "overlap": "two device buffer sets; copies of a step overlap neighbouring steps' compute"},
-        "gpu_launches": launches_per_step * args.steps,
+        "gpu_launches": launches_per_sub_step(w) * n_sub * args.steps,
         "clocks": clk,
     }
-    if rank == 0:
-        res["builder_scaled"] = builder_scaled(fa, w, W, dev)
+    if sweep:
+        pick = [i for i, x in enumerate(windows) if x in (64, 1024, 1792)]
+        res["per_window"] = {str(windows[i]): {
+            "visible_tiles": int(n_vis[i]),
+            "fwd_tflops": round(fwd_w[i] / (per[i][1] / args.steps * 1e-3) / 1e12, 2),
+            "bwd_tflops": round(2.5 * fwd_w[i] / (per[i][2] / args.steps * 1e-3) / 1e12, 2),
+            "build_ms": round(per[i][0] / args.steps, 4)} for i in pick}
+    if e2e:
+        res["e2e"] = {"value": round(job_flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+                      "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": e2e["h2d"],
+                      "d2h_bytes_per_step": e2e["d2h"],
+                      "overlap": "two device buffer sets; copies of a window's step overlap its neighbours' compute"}
+    del prob
+    torch.cuda.empty_cache()
+    if rank == 0 and not args.profile:
+        res["builder_scaled"] = builder_scaled(fa, w, prob_window(w, windows), dev)
         res["decode"] = decode_point(fa, dev, float(peaks.get("hbm_gbs", PEAKS_FALLBACK["hbm_gbs"])))
-    if rank == 0 and not args.no_cpu_baseline:
+        res["per_config"] = {str(n): per_config(fa, WORKLOADS[n], dev, max(3, args.steps // 2), 3, peak)
+                             for n in sorted(WORKLOADS) if n != args.workload}
+    if rank == 0 and not args.no_cpu_baseline and not args.profile:
         res["cpu_baseline"] = cpu_baseline(w, args.cpu_sample_tokens)
     if world > 1:
         dist.destroy_process_group()
     if rank == 0:
         print(json.dumps(res), flush=True)
+
+
+def prob_window(w, windows):
+    """A device W for builder_scaled: the largest window of the run (or the fixed one)."""
+    import torch
+
+    return torch.tensor([max(x or 0 for x in windows) or 1024], dtype=torch.int32, device="cuda")
+
+
+def run_e2e(fa, w, dev, host, windows, prob, stream, steps, ref_out):
+    """End to end through the public API: every window's step copies its inputs in
+    from pinned host memory and its results back.  Two device buffer sets and
+    three streams let the copies of one window's step overlap the compute of its
+    neighbours (the inputs of the next load while one computes, the results of
+    one return while the next computes), as a training loop that prefetches its
+    batches does; each window's step still moves all of its own bytes."""
+    import torch
+
+    q_h, k_h, v_h, do_h, docs_np = host
+    pin = lambda t: t.pin_memory()
+    hq, hk, hv, hdo = (pin(t) for t in (q_h, k_h, v_h, do_h))
+    hdocs = pin(torch.as_tensor(docs_np, dtype=torch.int32)) if docs_np is not None else None
+    h_out, h_lse = pin(torch.empty_like(q_h)), pin(torch.empty(w.B, w.H, w.S, dtype=torch.float32))
+    h_dq, h_dk, h_dv = (pin(torch.empty_like(t)) for t in (q_h, k_h, v_h))
+    n = len(windows)
+    h2d = n * (sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo)) +
+               (hdocs.numel() * 4 if hdocs is not None else 0))
+    d2h = n * (h_out.numel() * 2 + h_lse.numel() * 4 + 3 * h_dq.numel() * 2)
+    sets = [prob, Problem(fa, w, dev, host, windows)]
+    s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    ev_in, ev_comp, ev_out = ([torch.cuda.Event() for _ in range(2)] for _ in range(3))
+
+    def e2e_sub(j):
+        b = j % 2
+        st = sets[b]
+        with torch.cuda.stream(s_in):  # this set's inputs, once step j - 2 has finished with them
+            s_in.wait_event(ev_comp[b])
+            for dst, src in ((st.q, hq), (st.k, hk), (st.v, hv), (st.do, hdo)):
+                dst.copy_(src, non_blocking=True)
+            if hdocs is not None:
+                st.docs.copy_(hdocs, non_blocking=True)
+            ev_in[b].record(s_in)
+        stream.wait_event(ev_in[b])
+        stream.wait_event(ev_out[b])  # step j - 2's results have left this set
+        st.sub_step(j % n, stream)
+        ev_comp[b].record(stream)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(ev_comp[b])
+            for dst, src in ((h_out, st.out), (h_lse, st.lse), (h_dq, st.dq), (h_dk, st.dk), (h_dv, st.dv)):
+                dst.copy_(src, non_blocking=True)
+            ev_out[b].record(s_out)
+
+    for j in range(2):
+        e2e_sub(j)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(s_in)
+    for j in range(steps * n):
+        e2e_sub(j)
+    e1.record(s_out)
+    torch.cuda.synchronize()
+    # the device-timed run ended on the same window with the same inputs
+    assert torch.equal(h_out, ref_out), "e2e results differ from the device-timed run"
+    del sets[1]
+    return {"ms": e0.elapsed_time(e1) / steps, "h2d": int(h2d), "d2h": int(d2h)}
 
 
 def _sample_visible_tiles(mask, docs_row, S):
@@ -515,7 +612,8 @@ def cpu_baseline(w, tokens, heads=1):
     return {"value": round(flops / dt / 1e12, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
             "seconds": round(dt, 2),
             "sample": f"fwd+bwd of {heads} head(s) on the first {S} tokens of {w.name} "
-                      f"({n_vis} visible tiles, same mask and score mod)"}
+                      f"({n_vis} visible tiles, same mask and score mod"
+                      + (", W 1024 of the sweep)" if w.windows else ")")}
 
 
 def run_reference(args):
@@ -548,8 +646,14 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
-    ap.add_argument("--workload", type=int, default=2, choices=sorted(WORKLOADS))
-    ap.add_argument("--window", type=int, default=1024, help="window of the sweep workload (5)")
+    ap.add_argument("--workload", type=int, default=5, choices=sorted(WORKLOADS))
+    ap.add_argument("--window", type=int, default=None,
+                    help="one fixed window for the sweep workload (5) instead of the whole sweep")
+    ap.add_argument("--heads", type=int, default=0,
+                    help="with --profile: fewer heads than the workload's, for a smaller profiler capture")
+    ap.add_argument("--profile", action="store_true",
+                    help="the timed steps only (no e2e buffer set, scaled builder, decode point, other "
+                         "configs or CPU baseline): a small device footprint for profiler captures")
     ap.add_argument("--cpu-sample-tokens", type=int, default=32768,
                     help="tokens of the oracle sample timed as cpu_baseline")
     ap.add_argument("--ref-sample-tokens", type=int, default=16384,

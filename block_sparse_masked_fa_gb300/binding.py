@@ -61,50 +61,64 @@ class BlockMaskStruct(ctypes.Structure):
                    "kv_num_blocks", "kv_indices", "full_kv_num_blocks", "full_kv_indices",
                    "q_num_blocks", "q_indices", "full_q_num_blocks", "full_q_indices",
                    "row_order", "col_order", "tile_class", "tile_summary", "doc_runs", "row_segs", "status")] + \
-               [("spec", MaskSpec)]
+               [("spec", MaskSpec), ("from_blocks", ctypes.c_int32)] + \
+               [(name, ctypes.c_int32) for name in ("fwd_kv_block", "fwd_nq", "fwd_nkv", "bwd_nq", "bwd_nkv")] + \
+               [(name, ctypes.c_void_p) for name in (
+                   "fwd_kv_num_blocks", "fwd_kv_indices", "fwd_full_kv_num_blocks", "fwd_full_kv_indices",
+                   "fwd_row_order", "fwd_tile_class", "bwd_q_num_blocks", "bwd_q_indices", "bwd_full_q_num_blocks",
+                   "bwd_full_q_indices", "bwd_col_order", "bwd_tile_class")]
 
 
 _c = ctypes
-_lib.fa_block_mask_bytes.argtypes = [_c.c_int32, _c.c_int32, _c.c_int64, _c.c_int64, _c.c_int32,
-                                     _c.POINTER(_c.c_size_t)]
-_lib.fa_create_block_mask.argtypes = [_c.POINTER(MaskSpec), _c.c_int32, _c.c_int32, _c.c_int64, _c.c_int64,
-                                      _c.c_int32, _c.c_void_p, _c.c_size_t, _c.POINTER(BlockMaskStruct),
-                                      _c.c_void_p]
-_lib.fa_block_mask_from_kv_blocks.argtypes = [_c.c_void_p] * 4 + [_c.c_int32, _c.POINTER(MaskSpec), _c.c_int32,
-                                                                  _c.c_int32, _c.c_int64, _c.c_int64, _c.c_int32,
-                                                                  _c.c_void_p, _c.c_size_t,
-                                                                  _c.POINTER(BlockMaskStruct), _c.c_void_p]
-_lib.fa_forward.argtypes = [_c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_int32, _c.c_int32, _c.c_int64,
-                            _c.c_int64, _c.c_int32, _c.POINTER(BlockMaskStruct), _c.POINTER(ScoreSpec),
-                            _c.c_float, _c.c_void_p, _c.c_void_p, _c.c_void_p]
-_lib.fa_forward_paged.argtypes = [_c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_int32, _c.c_int32,
-                                  _c.c_int32, _c.c_int64, _c.c_int64, _c.c_int32, _c.POINTER(BlockMaskStruct),
-                                  _c.POINTER(ScoreSpec), _c.c_float, _c.c_void_p, _c.c_void_p, _c.c_void_p]
-_lib.fa_forward_decode_workspace_bytes.argtypes = [_c.c_int32, _c.c_int32, _c.c_int64, _c.c_int64, _c.c_int32,
-                                                   _c.POINTER(_c.c_size_t)]
-_lib.fa_forward_decode.argtypes = [_c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_int32, _c.c_int32,
-                                   _c.c_int32, _c.c_int64, _c.c_int64, _c.c_int32, _c.POINTER(BlockMaskStruct),
-                                   _c.POINTER(ScoreSpec), _c.c_float, _c.c_void_p, _c.c_void_p, _c.c_void_p,
-                                   _c.c_size_t, _c.c_void_p]
-_lib.fa_backward_workspace_bytes.argtypes = [_c.c_int32, _c.c_int32, _c.c_int64, _c.c_int32,
-                                             _c.POINTER(_c.c_size_t)]
-_lib.fa_backward.argtypes = [_c.c_void_p] * 6 + [_c.c_int32, _c.c_int32, _c.c_int64, _c.c_int64, _c.c_int32,
-                                                 _c.POINTER(BlockMaskStruct), _c.POINTER(ScoreSpec), _c.c_float,
-                                                 _c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_void_p,
-                                                 _c.c_size_t, _c.c_void_p]
-_lib.fa_backward_noalloc.argtypes = [_c.c_void_p] * 6 + [_c.c_int32, _c.c_int32, _c.c_int64, _c.c_int64,
-                                                         _c.c_int32, _c.POINTER(BlockMaskStruct),
-                                                         _c.POINTER(ScoreSpec), _c.c_float, _c.c_void_p,
-                                                         _c.c_void_p, _c.c_void_p, _c.c_void_p]
-_lib.fa_get_status.argtypes = [_c.POINTER(BlockMaskStruct), _c.c_int32, _c.c_void_p]
-_lib.fa_block_mask_summary.argtypes = [_c.POINTER(BlockMaskStruct), _c.POINTER(_c.c_int64 * 3), _c.c_void_p]
-_lib.fa_status_string.argtypes = [_c.c_int]
-_lib.fa_status_string.restype = _c.c_char_p
-for _f in (_lib.fa_block_mask_bytes, _lib.fa_create_block_mask, _lib.fa_block_mask_from_kv_blocks, _lib.fa_forward,
-           _lib.fa_forward_paged, _lib.fa_forward_decode_workspace_bytes, _lib.fa_forward_decode, _lib.fa_backward_workspace_bytes,
-           _lib.fa_backward, _lib.fa_backward_noalloc, _lib.fa_get_status, _lib.fa_block_mask_summary):
-    _f.restype = _c.c_int
-_lib.fa_version.restype = _c.c_int32
+
+
+def _bind(lib):
+    """Declares the C signatures on a loaded library (the package's own, or the test
+    library built from the same sources) and returns it."""
+    lib.fa_block_mask_bytes.argtypes = [_c.c_int32, _c.c_int32, _c.c_int64, _c.c_int64, _c.c_int32,
+                                         _c.POINTER(_c.c_size_t)]
+    lib.fa_create_block_mask.argtypes = [_c.POINTER(MaskSpec), _c.c_int32, _c.c_int32, _c.c_int64, _c.c_int64,
+                                          _c.c_int32, _c.c_void_p, _c.c_size_t, _c.POINTER(BlockMaskStruct),
+                                          _c.c_void_p]
+    lib.fa_block_mask_from_kv_blocks.argtypes = [_c.c_void_p] * 4 + [_c.c_int32, _c.POINTER(MaskSpec), _c.c_int32,
+                                                                      _c.c_int32, _c.c_int64, _c.c_int64, _c.c_int32,
+                                                                      _c.c_void_p, _c.c_size_t,
+                                                                      _c.POINTER(BlockMaskStruct), _c.c_void_p]
+    lib.fa_forward.argtypes = [_c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_int32, _c.c_int32, _c.c_int64,
+                                _c.c_int64, _c.c_int32, _c.POINTER(BlockMaskStruct), _c.POINTER(ScoreSpec),
+                                _c.c_float, _c.c_void_p, _c.c_void_p, _c.c_void_p]
+    lib.fa_forward_paged.argtypes = [_c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_int32, _c.c_int32,
+                                      _c.c_int32, _c.c_int64, _c.c_int64, _c.c_int32, _c.POINTER(BlockMaskStruct),
+                                      _c.POINTER(ScoreSpec), _c.c_float, _c.c_void_p, _c.c_void_p, _c.c_void_p]
+    lib.fa_forward_decode_workspace_bytes.argtypes = [_c.c_int32, _c.c_int32, _c.c_int64, _c.c_int64, _c.c_int32,
+                                                       _c.POINTER(_c.c_size_t)]
+    lib.fa_forward_decode.argtypes = [_c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_int32, _c.c_int32,
+                                       _c.c_int32, _c.c_int64, _c.c_int64, _c.c_int32, _c.POINTER(BlockMaskStruct),
+                                       _c.POINTER(ScoreSpec), _c.c_float, _c.c_void_p, _c.c_void_p, _c.c_void_p,
+                                       _c.c_size_t, _c.c_void_p]
+    lib.fa_backward_workspace_bytes.argtypes = [_c.c_int32, _c.c_int32, _c.c_int64, _c.c_int32,
+                                                 _c.POINTER(_c.c_size_t)]
+    lib.fa_backward.argtypes = [_c.c_void_p] * 6 + [_c.c_int32, _c.c_int32, _c.c_int64, _c.c_int64, _c.c_int32,
+                                                     _c.POINTER(BlockMaskStruct), _c.POINTER(ScoreSpec), _c.c_float,
+                                                     _c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_void_p,
+                                                     _c.c_size_t, _c.c_void_p]
+    lib.fa_backward_noalloc.argtypes = [_c.c_void_p] * 6 + [_c.c_int32, _c.c_int32, _c.c_int64, _c.c_int64,
+                                                             _c.c_int32, _c.POINTER(BlockMaskStruct),
+                                                             _c.POINTER(ScoreSpec), _c.c_float, _c.c_void_p,
+                                                             _c.c_void_p, _c.c_void_p, _c.c_void_p]
+    lib.fa_get_status.argtypes = [_c.POINTER(BlockMaskStruct), _c.c_int32, _c.c_void_p]
+    lib.fa_block_mask_summary.argtypes = [_c.POINTER(BlockMaskStruct), _c.POINTER(_c.c_int64 * 3), _c.c_void_p]
+    lib.fa_status_string.argtypes = [_c.c_int]
+    lib.fa_status_string.restype = _c.c_char_p
+    for _f in (lib.fa_block_mask_bytes, lib.fa_create_block_mask, lib.fa_block_mask_from_kv_blocks, lib.fa_forward,
+               lib.fa_forward_paged, lib.fa_forward_decode_workspace_bytes, lib.fa_forward_decode, lib.fa_backward_workspace_bytes,
+               lib.fa_backward, lib.fa_backward_noalloc, lib.fa_get_status, lib.fa_block_mask_summary):
+        _f.restype = _c.c_int
+    lib.fa_version.restype = _c.c_int32
+    return lib
+
+
+_lib = _bind(_lib)
 
 EXPORTED = ("fa_block_mask_bytes", "fa_create_block_mask", "fa_block_mask_from_kv_blocks", "fa_forward",
             "fa_forward_paged", "fa_forward_decode_workspace_bytes", "fa_forward_decode", "fa_backward_workspace_bytes",
@@ -209,6 +223,28 @@ class BlockMask:
             "q_indices": self._view("q_indices", c + (s.nq,)),
             "full_q_num_blocks": self._view("full_q_num_blocks", c),
             "full_q_indices": self._view("full_q_indices", c + (s.nq,)),
+        }
+
+    def kernel_lists(self) -> dict:
+        """Below block 128: the coarser tiles the attention kernels walk (see
+        fa_block_mask in fa.h) -- the forward's query-tile rows of 128 over key
+        tiles of fwd_kv_block, the backward's key-tile columns of 128 over query
+        tiles of 128, with their class grids.  Empty at block 128."""
+        s = self.struct
+        if not s.fwd_kv_num_blocks:
+            return {}
+        fr, br = (s.Bm, s.Hm, s.fwd_nq), (s.Bm, s.Hm, s.bwd_nkv)
+        return {
+            "fwd_kv_num_blocks": self._view("fwd_kv_num_blocks", fr),
+            "fwd_kv_indices": self._view("fwd_kv_indices", fr + (s.fwd_nkv,)),
+            "fwd_full_kv_num_blocks": self._view("fwd_full_kv_num_blocks", fr),
+            "fwd_full_kv_indices": self._view("fwd_full_kv_indices", fr + (s.fwd_nkv,)),
+            "fwd_tile_class": self._view("fwd_tile_class", fr + (s.fwd_nkv,), torch.uint8),
+            "bwd_q_num_blocks": self._view("bwd_q_num_blocks", br),
+            "bwd_q_indices": self._view("bwd_q_indices", br + (s.bwd_nq,)),
+            "bwd_full_q_num_blocks": self._view("bwd_full_q_num_blocks", br),
+            "bwd_full_q_indices": self._view("bwd_full_q_indices", br + (s.bwd_nq,)),
+            "bwd_tile_class": self._view("bwd_tile_class", (s.Bm, s.Hm, s.bwd_nq, s.bwd_nkv), torch.uint8),
         }
 
     def tile_class(self) -> torch.Tensor:

@@ -16,6 +16,11 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libfa_gb300.so")
+# The test library: the same sources with FA_TEST_HOOKS (short device wait
+# limit, a hook that starves one wait, fa_test_hook exported).  Built only by
+# the test that uses it; never loaded by the package.
+HOOKS_BUILD = os.path.join(PKG, "_build_hooks")
+HOOKS_LIB = os.path.join(PKG, "libfa_gb300_hooks.so")
 SOURCES = ["api.cu", "builder.cu", "fwd.cu", "bwd.cu", "decode.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
@@ -29,22 +34,28 @@ def _nvcc() -> str:
     return "nvcc"
 
 
-def _needs_rebuild() -> bool:
-    if not os.path.exists(LIB):
+def _needs_rebuild(lib: str) -> bool:
+    if not os.path.exists(lib):
         return True
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     deps = [os.path.join(CSRC, f) for f in os.listdir(CSRC)] + [os.path.join(ROOT, "include", "fa.h")]
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    if not force and not _needs_rebuild():
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
+def build_test_hooks(force: bool = False) -> str:
+    """Builds libfa_gb300_hooks.so, the library of the device-timeout tests."""
+    return build(force=force, extra_flags=("-DFA_TEST_HOOKS",), build_dir=HOOKS_BUILD, lib=HOOKS_LIB)
+
+
+def build(force: bool = False, verbose: bool = False, extra_flags=(), build_dir: str = BUILD,
+          lib: str = LIB) -> str:
+    if not force and not _needs_rebuild(lib):
+        return lib
+    os.makedirs(build_dir, exist_ok=True)
     nvcc = _nvcc()
 
     def compile_one(src):
-        obj = os.path.join(BUILD, src.replace(".cu", ".o"))
+        obj = os.path.join(build_dir, src.replace(".cu", ".o"))
         cmd = [nvcc, *ARCH, *FLAGS, *extra_flags, "-c", os.path.join(CSRC, src), "-o", obj]
         if verbose:
             cmd.insert(1, "-Xptxas=-v")
@@ -58,13 +69,13 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     if verbose:
         for _, log in results:
             sys.stderr.write(log)
-    tmp = LIB + ".tmp"
+    tmp = lib + ".tmp"
     r = subprocess.run([nvcc, *ARCH, "-shared", "-o", tmp, *[o for o, _ in results], "-cudart", "static"],
                        capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

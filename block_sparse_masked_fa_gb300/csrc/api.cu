@@ -25,12 +25,18 @@ bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0
 struct Layout {
   enum {
     KV_NUM, KV_IDX, FULL_NUM, FULL_IDX, Q_NUM, Q_IDX, FULL_Q_NUM, FULL_Q_IDX, ROW_ORDER, COL_ORDER, TILE_CLASS,
-    SUMMARY, DOC_RUNS, ROW_SEGS, STATUS, N
+    SUMMARY, DOC_RUNS, ROW_SEGS, STATUS,
+    // block < 128 only (empty otherwise): the attention kernels' coarser tiles
+    FWD_NUM, FWD_IDX, FWD_FULL_NUM, FWD_FULL_IDX, FWD_ORDER, FWD_CLASS,
+    BWD_NUM, BWD_IDX, BWD_FULL_NUM, BWD_FULL_IDX, BWD_ORDER, BWD_CLASS, N
   };
   size_t off[N];
   size_t total;
   int64_t nq, nkv;
+  int64_t fwd_nq, fwd_nkv, bwd_nq, bwd_nkv;  // 0 at block 128
 };
+
+constexpr int kFwdSmallKvBlock = 64;  // the forward's key tile below block 128
 
 fa_status make_layout(int32_t Bm, int32_t Hm, int64_t q_len, int64_t kv_len, int32_t block, Layout* L) {
   if (Bm < 1 || Hm < 1 || q_len < 1 || kv_len < 1) return FA_ERR_SHAPE;
@@ -41,6 +47,10 @@ fa_status make_layout(int32_t Bm, int32_t Hm, int64_t q_len, int64_t kv_len, int
   const int64_t tiles = rows * nkv;
   if (tiles > (int64_t)INT32_MAX || rows > (int64_t)INT32_MAX / 2 || cols > (int64_t)INT32_MAX / 2)
     return FA_ERR_SHAPE;
+  const bool coarse = block < 128;
+  const int64_t fnq = coarse ? (q_len + 127) / 128 : 0, fnkv = coarse ? (kv_len + kFwdSmallKvBlock - 1) / kFwdSmallKvBlock : 0;
+  const int64_t bnq = fnq, bnkv = coarse ? (kv_len + 127) / 128 : 0;
+  const size_t planes = (size_t)Bm * Hm;
   const size_t sizes[Layout::N] = {
       (size_t)rows * 4,  (size_t)tiles * 4, (size_t)rows * 4, (size_t)tiles * 4,
       (size_t)cols * 4,  (size_t)tiles * 4, (size_t)cols * 4, (size_t)tiles * 4,
@@ -48,7 +58,11 @@ fa_status make_layout(int32_t Bm, int32_t Hm, int64_t q_len, int64_t kv_len, int
       (size_t)Bm * 2 * (size_t)(nq > nkv ? nq : nkv) * 4 * 4,
       (size_t)Bm * (size_t)(q_len > kv_len ? q_len : kv_len) * 8 + (size_t)Bm * 4,
       (size_t)Bm * 2 * (size_t)(q_len > kv_len ? q_len : kv_len) * 16,
-      4};
+      4,
+      planes * fnq * 4, planes * fnq * fnkv * 4, planes * fnq * 4, planes * fnq * fnkv * 4, planes * fnq * 4,
+      planes * fnq * fnkv,
+      planes * bnkv * 4, planes * bnkv * bnq * 4, planes * bnkv * 4, planes * bnkv * bnq * 4, planes * bnkv * 4,
+      planes * bnq * bnkv};
   size_t at = 0;
   for (int k = 0; k < Layout::N; ++k) {
     L->off[k] = at;
@@ -57,6 +71,10 @@ fa_status make_layout(int32_t Bm, int32_t Hm, int64_t q_len, int64_t kv_len, int
   L->total = at;
   L->nq = nq;
   L->nkv = nkv;
+  L->fwd_nq = fnq;
+  L->fwd_nkv = fnkv;
+  L->bwd_nq = bnq;
+  L->bwd_nkv = bnkv;
   return FA_OK;
 }
 
@@ -127,13 +145,22 @@ void load_encode() {
 
 fa_status cuda_status(cudaError_t e) { return e == cudaSuccess ? FA_OK : FA_ERR_CUDA; }
 
+enum AttnKind { kForward, kForwardPagedOrDecode, kBackward };
+
 // Shared shape checks of fa_forward / fa_backward.
 fa_status check_attn(int32_t B, int32_t H, int64_t q_len, int64_t kv_len, int32_t D, const fa_block_mask* bm,
-                     const fa_score_spec* score, float* scale, bool backward) {
+                     const fa_score_spec* score, float* scale, AttnKind kind) {
+  const bool backward = kind == kBackward;
   if (bm == nullptr) return FA_ERR_INVALID_ARG;
   if (B < 1 || H < 1 || q_len < 1 || kv_len < 1) return FA_ERR_SHAPE;
   if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
-  if (bm->block != 128) return FA_ERR_UNSUPPORTED;
+  if (bm->block != 128) {  // the kernels walk the coarser lists the builder derived
+    if (kind == kForwardPagedOrDecode || bm->from_blocks) return FA_ERR_UNSUPPORTED;
+    if (bm->block > 128 || bm->fwd_kv_block != kFwdSmallKvBlock) return FA_ERR_INVALID_ARG;
+    if (backward ? (bm->bwd_q_num_blocks == nullptr || bm->bwd_col_order == nullptr)
+                 : (bm->fwd_kv_num_blocks == nullptr || bm->fwd_row_order == nullptr))
+      return FA_ERR_INVALID_ARG;
+  }
   if (bm->q_len != q_len || bm->kv_len != kv_len) return FA_ERR_SHAPE;
   if (!(bm->Bm == 1 || bm->Bm == B) || !(bm->Hm == 1 || bm->Hm == H)) return FA_ERR_SHAPE;
   if ((int64_t)B * H * ((q_len + 127) / 128) > (int64_t)INT32_MAX) return FA_ERR_SHAPE;
@@ -181,6 +208,27 @@ AttnArgs attn_args(int32_t B, int32_t H, int64_t q_len, int64_t kv_len, int32_t 
   a.param_grad = (backward && score) ? score->param_grad : nullptr;
   a.status = bm->status;
   a.mask = dm;
+  a.kv_block = 128;
+  if (bm->block != 128 && !backward) {  // the forward's 128 x 64 tiles
+    a.nq = bm->fwd_nq;
+    a.nkv = bm->fwd_nkv;
+    a.kv_block = bm->fwd_kv_block;
+    a.kv_num = bm->fwd_kv_num_blocks;
+    a.kv_idx = bm->fwd_kv_indices;
+    a.full_num = bm->fwd_full_kv_num_blocks;
+    a.full_idx = bm->fwd_full_kv_indices;
+    a.row_order = bm->fwd_row_order;
+    a.q_num = a.q_idx = a.full_q_num = a.full_q_idx = a.col_order = nullptr;
+  } else if (bm->block != 128) {  // the backward's 128 x 128 tiles
+    a.nq = bm->bwd_nq;
+    a.nkv = bm->bwd_nkv;
+    a.q_num = bm->bwd_q_num_blocks;
+    a.q_idx = bm->bwd_q_indices;
+    a.full_q_num = bm->bwd_full_q_num_blocks;
+    a.full_q_idx = bm->bwd_full_q_indices;
+    a.col_order = bm->bwd_col_order;
+    a.kv_num = a.kv_idx = a.full_num = a.full_idx = a.row_order = nullptr;
+  }
   a.row_segs = reinterpret_cast<const int4*>(bm->row_segs);
   a.seg_len = bm->q_len > bm->kv_len ? bm->q_len : bm->kv_len;
   if (dm.has_doc && bm->doc_runs != nullptr) {
@@ -248,6 +296,26 @@ static fa_status build_block_mask(const fa_mask_spec* spec, int32_t Bm, int32_t 
   bm->row_segs = i32(Layout::ROW_SEGS);
   bm->status = reinterpret_cast<uint32_t*>(base + L.off[Layout::STATUS]);
   bm->spec = *spec;
+  bm->from_blocks = sel != nullptr ? 1 : 0;
+  if (block < 128) {
+    bm->fwd_kv_block = kFwdSmallKvBlock;
+    bm->fwd_nq = (int32_t)L.fwd_nq;
+    bm->fwd_nkv = (int32_t)L.fwd_nkv;
+    bm->bwd_nq = (int32_t)L.bwd_nq;
+    bm->bwd_nkv = (int32_t)L.bwd_nkv;
+    bm->fwd_kv_num_blocks = i32(Layout::FWD_NUM);
+    bm->fwd_kv_indices = i32(Layout::FWD_IDX);
+    bm->fwd_full_kv_num_blocks = i32(Layout::FWD_FULL_NUM);
+    bm->fwd_full_kv_indices = i32(Layout::FWD_FULL_IDX);
+    bm->fwd_row_order = i32(Layout::FWD_ORDER);
+    bm->fwd_tile_class = base + L.off[Layout::FWD_CLASS];
+    bm->bwd_q_num_blocks = i32(Layout::BWD_NUM);
+    bm->bwd_q_indices = i32(Layout::BWD_IDX);
+    bm->bwd_full_q_num_blocks = i32(Layout::BWD_FULL_NUM);
+    bm->bwd_full_q_indices = i32(Layout::BWD_FULL_IDX);
+    bm->bwd_col_order = i32(Layout::BWD_ORDER);
+    bm->bwd_tile_class = base + L.off[Layout::BWD_CLASS];
+  }
 
   cudaError_t e = cudaMemsetAsync(bm->status, 0, 4, stream);
   if (e != cudaSuccess) return FA_ERR_CUDA;
@@ -276,6 +344,27 @@ static fa_status build_block_mask(const fa_mask_spec* spec, int32_t Bm, int32_t 
   a.doc_runs = bm->doc_runs;
   a.row_segs = bm->row_segs;
   a.status = bm->status;
+  if (block < 128) {
+    a.fwd_kv_block = bm->fwd_kv_block;
+    a.fwd.cls = bm->fwd_tile_class;
+    a.fwd.planes = Bm * Hm;
+    a.fwd.n_r = bm->fwd_nq;
+    a.fwd.n_c = bm->fwd_nkv;
+    a.fwd.row_num = bm->fwd_kv_num_blocks;
+    a.fwd.row_idx = bm->fwd_kv_indices;
+    a.fwd.row_full_num = bm->fwd_full_kv_num_blocks;
+    a.fwd.row_full_idx = bm->fwd_full_kv_indices;
+    a.fwd.row_order = bm->fwd_row_order;
+    a.bwd.cls = bm->bwd_tile_class;
+    a.bwd.planes = Bm * Hm;
+    a.bwd.n_r = bm->bwd_nq;
+    a.bwd.n_c = bm->bwd_nkv;
+    a.bwd.col_num = bm->bwd_q_num_blocks;
+    a.bwd.col_idx = bm->bwd_q_indices;
+    a.bwd.col_full_num = bm->bwd_full_q_num_blocks;
+    a.bwd.col_full_idx = bm->bwd_full_q_indices;
+    a.bwd.col_order = bm->bwd_col_order;
+  }
   if (sel != nullptr) {
     a.sel_num = sel->sel_num;
     a.sel_idx = sel->sel_idx;
@@ -299,6 +388,18 @@ using namespace fa;
 extern "C" {
 
 int32_t fa_version(void) { return 100; }
+
+#ifdef FA_TEST_HOOKS
+// Exported by the test library only (never by the product build): which = 0
+// clears both hooks, 1 starves the forward's first key-tile load, 2 the
+// backward's (see test_hook_forward in internal.h).
+fa_status fa_test_hook(int32_t which) {
+  if (which < 0 || which > 2) return FA_ERR_INVALID_ARG;
+  if (fa::test_hook_forward(which == 1) != cudaSuccess || fa::test_hook_backward(which == 2) != cudaSuccess)
+    return FA_ERR_CUDA;
+  return FA_OK;
+}
+#endif
 
 const char* fa_status_string(fa_status s) {
   switch (s) {
@@ -373,7 +474,8 @@ fa_status fa_forward_paged(const void* q, const void* k, const void* v, const in
     if (!aligned4(page_table)) return FA_ERR_ALIGNMENT;
     if (n_pages < 1 || (int64_t)n_pages * 128 > (int64_t)INT32_MAX) return FA_ERR_SHAPE;
   }
-  fa_status st = check_attn(B, H, q_len, kv_len, D, bm, score, &scale, false);
+  fa_status st = check_attn(B, H, q_len, kv_len, D, bm, score, &scale,
+                            page_table != nullptr ? kForwardPagedOrDecode : kForward);
   if (st != FA_OK) return st;
   DevMask dm;
   st = check_mask(&bm->spec, q_len, kv_len, &dm);
@@ -415,7 +517,7 @@ fa_status fa_forward_decode(const void* q, const void* k, const void* v, const i
   }
   if (q_len < 1 || q_len > FA_DECODE_MAX_Q) return q_len < 1 ? FA_ERR_SHAPE : FA_ERR_UNSUPPORTED;
   if ((int64_t)B * H > kDecodeMaxHeads) return FA_ERR_UNSUPPORTED;
-  fa_status st = check_attn(B, H, q_len, kv_len, D, bm, score, &scale, false);
+  fa_status st = check_attn(B, H, q_len, kv_len, D, bm, score, &scale, kForwardPagedOrDecode);
   if (st != FA_OK) return st;
   size_t need = 0;
   int splits = 0;
@@ -440,7 +542,7 @@ fa_status fa_backward_workspace_bytes(int32_t B, int32_t H, int64_t q_len, int32
   if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
   const size_t rows = (size_t)B * H * (size_t)q_len;
   const size_t tiles = (size_t)B * H * (size_t)((q_len + 127) / 128);
-  *bytes = align_up(rows * D * 4) + align_up(tiles * 256 * 4);
+  *bytes = align_up(rows * D * 4) + align_up(tiles * 256 * 4) + align_up(4);
   return FA_OK;
 }
 
@@ -452,7 +554,7 @@ fa_status fa_backward(const void* q, const void* k, const void* v, const void* o
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(dout) || !aligned16(dq) ||
       !aligned16(dk) || !aligned16(dv) || !aligned16(workspace) || !aligned4(lse))
     return FA_ERR_ALIGNMENT;
-  fa_status st = check_attn(B, H, q_len, kv_len, D, bm, score, &scale, true);
+  fa_status st = check_attn(B, H, q_len, kv_len, D, bm, score, &scale, kBackward);
   if (st != FA_OK) return st;
   size_t need = 0;
   st = fa_backward_workspace_bytes(B, H, q_len, D, &need);
@@ -475,6 +577,8 @@ fa_status fa_backward(const void* q, const void* k, const void* v, const void* o
   t.dv = dv;
   t.dq_acc = static_cast<float*>(workspace);
   t.stats = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + align_up(rows * D * 4));
+  t.sched = reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(t.stats) +
+                                        align_up((size_t)B * H * (size_t)((q_len + 127) / 128) * 256 * 4));
   bool enc_failed = false;
   const cudaError_t e = launch_backward(a, t, stream, &enc_failed);
   if (enc_failed) return FA_ERR_CUDA;
@@ -489,7 +593,7 @@ fa_status fa_backward_noalloc(const void* q, const void* k, const void* v, const
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(dout) || !aligned16(dq) ||
       !aligned16(dk) || !aligned16(dv) || !aligned4(lse))
     return FA_ERR_ALIGNMENT;
-  fa_status st = check_attn(B, H, q_len, kv_len, D, bm, score, &scale, true);
+  fa_status st = check_attn(B, H, q_len, kv_len, D, bm, score, &scale, kBackward);
   if (st != FA_OK) return st;
   size_t need = 0;
   st = fa_backward_workspace_bytes(B, H, q_len, D, &need);
@@ -514,6 +618,8 @@ fa_status fa_backward_noalloc(const void* q, const void* k, const void* v, const
   t.dv = dv;
   t.dq_acc = static_cast<float*>(scratch);
   t.stats = reinterpret_cast<float*>(static_cast<uint8_t*>(scratch) + align_up(rows * D * 4));
+  t.sched = reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(t.stats) +
+                                        align_up((size_t)B * H * (size_t)((q_len + 127) / 128) * 256 * 4));
   bool enc_failed = false;
   const cudaError_t e = launch_backward(a, t, stream, &enc_failed);
   if (enc_failed) return FA_ERR_CUDA;

@@ -459,22 +459,24 @@ __global__ void __launch_bounds__(kBuildWarps * 32) select_kernel(const __grid_c
   }
 }
 
-// Compaction: warps [0, rows) build the per-row lists, the next [0, cols)
-// warps the per-column lists, both with ballots over the class bytes.
-__global__ void __launch_bounds__(kBuildWarps * 32) compact_kernel(const __grid_constant__ BuildArgs a) {
+// Compaction of one class grid [Bm * Hm][n_r][n_c] into lists: warps [0, rows)
+// build the per-row lists, the next [0, cols) warps the per-column lists, both
+// with ballots over the class bytes (rows or columns without list pointers are
+// skipped).
+__global__ void __launch_bounds__(kBuildWarps * 32) compact_kernel(const __grid_constant__ ListJob j) {
   pdl_wait_then_release();
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int64_t wid = (int64_t)blockIdx.x * kBuildWarps + warp;
-  const int64_t rows = (int64_t)a.Bm * a.Hm * a.nq, cols = (int64_t)a.Bm * a.Hm * a.nkv;
+  const int64_t rows = j.row_num ? (int64_t)j.planes * j.n_r : 0, cols = j.col_num ? (int64_t)j.planes * j.n_c : 0;
   if (wid >= rows + cols) return;
   const bool by_row = wid < rows;
   const int64_t id = by_row ? wid : wid - rows;
-  const int n = by_row ? a.nkv : a.nq;                    // list length
-  const int64_t stride = by_row ? 1 : a.nkv;              // class-byte stride along the list
-  const uint8_t* cls_base = by_row ? a.tile_class + id * a.nkv
-                                   : a.tile_class + (id / a.nkv) * a.nq * a.nkv + (id % a.nkv);
-  int32_t* part_idx = (by_row ? a.kv_idx : a.q_idx) + id * n;
-  int32_t* full_idx = (by_row ? a.full_idx : a.full_q_idx) + id * n;
+  const int n = by_row ? j.n_c : j.n_r;                   // list length
+  const int64_t stride = by_row ? 1 : j.n_c;              // class-byte stride along the list
+  const uint8_t* cls_base = by_row ? j.cls + id * j.n_c
+                                   : j.cls + (id / j.n_c) * j.n_r * j.n_c + (id % j.n_c);
+  int32_t* part_idx = (by_row ? j.row_idx : j.col_idx) + id * n;
+  int32_t* full_idx = (by_row ? j.row_full_idx : j.col_full_idx) + id * n;
   int n_part = 0, n_full = 0;
   // class bytes of eight 32-tile chunks are loaded before any list entry is
   // stored: the stores (int32) could alias the bytes for the compiler, which
@@ -503,9 +505,36 @@ __global__ void __launch_bounds__(kBuildWarps * 32) compact_kernel(const __grid_
   for (int k = n_part + lane; k < n; k += 32) part_idx[k] = 0;
   for (int k = n_full + lane; k < n; k += 32) full_idx[k] = 0;
   if (lane == 0) {
-    (by_row ? a.kv_num : a.q_num)[id] = n_part;
-    (by_row ? a.full_num : a.full_q_num)[id] = n_full;
+    (by_row ? j.row_num : j.col_num)[id] = n_part;
+    (by_row ? j.row_full_num : j.col_full_num)[id] = n_full;
   }
+}
+
+// Coarse classes for the attention kernels' tiles when the block mask's tiles
+// are smaller: coarse tile (I, J) of [planes][n_r][n_c] covers fine rows
+// [fr I, fr I + fr) and columns [fc J, fc J + fc) (cut at the fine grid's
+// edge); it is EMPTY when every fine tile there is, FULL when every one is, and
+// PARTIAL otherwise -- exact, since a union of tiles has no visible pair iff
+// none of them has one, and only visible pairs iff all of them have only those.
+__global__ void __launch_bounds__(256) coarsen_kernel(const uint8_t* __restrict__ fine, int fine_nq, int fine_nkv,
+                                                      uint8_t* __restrict__ coarse, int n_r, int n_c, int fr, int fc,
+                                                      int64_t n) {
+  pdl_wait_then_release();
+  const int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (gid >= n) return;
+  const int J = (int)(gid % n_c);
+  const int I = (int)((gid / n_c) % n_r);
+  const int64_t plane = gid / ((int64_t)n_r * n_c);
+  const uint8_t* f = fine + plane * fine_nq * fine_nkv;
+  const int i1 = min((I + 1) * fr, fine_nq), j1 = min((J + 1) * fc, fine_nkv);
+  bool any = false, all = true;
+  for (int i = I * fr; i < i1; ++i)
+    for (int jj = J * fc; jj < j1; ++jj) {
+      const int c = __ldg(f + (int64_t)i * fine_nkv + jj);
+      any = any || c != 0;
+      all = all && c == 2;
+    }
+  coarse[gid] = (uint8_t)(!any ? 0 : (all ? 2 : 1));
 }
 
 // Work order: block 0 orders the rows (forward), block 1 the columns
@@ -519,15 +548,16 @@ __global__ void __launch_bounds__(kBuildWarps * 32) compact_kernel(const __grid_
 // entries; coarser buckets are used if the counts would need more.
 constexpr int kOrderBuckets = 4096;
 
-__global__ void __launch_bounds__(1024) order_kernel(const __grid_constant__ BuildArgs a) {
+__global__ void __launch_bounds__(1024) order_kernel(const __grid_constant__ ListJob j) {
   pdl_wait_then_release();
   extern __shared__ int32_t hist[];  // kOrderBuckets entries
   __shared__ int s_cmax;
   const bool rows = blockIdx.x == 0;
-  const int32_t* num = rows ? a.kv_num : a.q_num;
-  const int32_t* full_num = rows ? a.full_num : a.full_q_num;
-  int32_t* order = rows ? a.row_order : a.col_order;
-  const int n = rows ? a.Bm * a.Hm * a.nq : a.Bm * a.Hm * a.nkv;
+  if ((rows ? j.row_num : j.col_num) == nullptr) return;
+  const int32_t* num = rows ? j.row_num : j.col_num;
+  const int32_t* full_num = rows ? j.row_full_num : j.col_full_num;
+  int32_t* order = rows ? j.row_order : j.col_order;
+  const int n = rows ? j.planes * j.n_r : j.planes * j.n_c;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   if (threadIdx.x == 0) s_cmax = 0;
   __syncthreads();
@@ -585,6 +615,14 @@ __global__ void __launch_bounds__(1024) order_kernel(const __grid_constant__ Bui
 }
 
 
+// Compaction and work order of one class grid (rows / columns: how many lists).
+cudaError_t launch_lists(const ListJob& j, int64_t rows, int64_t cols, cudaStream_t stream) {
+  cudaError_t e = launch_k(compact_kernel, dim3((unsigned)((rows + cols + kBuildWarps - 1) / kBuildWarps)),
+                           dim3(kBuildWarps * 32), 0, stream, j);
+  if (e != cudaSuccess) return e;
+  return launch_k(order_kernel, dim3(2), dim3(1024), kOrderBuckets * sizeof(int32_t), stream, j);
+}
+
 }  // namespace
 
 cudaError_t launch_build(const BuildArgs& a, cudaStream_t stream) {
@@ -613,10 +651,35 @@ cudaError_t launch_build(const BuildArgs& a, cudaStream_t stream) {
     e = launch_k(classify_kernel, dim3((unsigned)((cwarps + kBuildWarps - 1) / kBuildWarps)),
                  dim3(kBuildWarps * 32), 0, stream, a);
   if (e != cudaSuccess) return e;
-  e = launch_k(compact_kernel, dim3((unsigned)((rows + cols + kBuildWarps - 1) / kBuildWarps)), dim3(kBuildWarps * 32),
-               0, stream, a);
-  if (e != cudaSuccess) return e;
-  return launch_k(order_kernel, dim3(2), dim3(1024), kOrderBuckets * sizeof(int32_t), stream, a);
+  ListJob fine;
+  fine.cls = a.tile_class;
+  fine.planes = a.Bm * a.Hm;
+  fine.n_r = a.nq;
+  fine.n_c = a.nkv;
+  fine.row_num = a.kv_num;
+  fine.row_idx = a.kv_idx;
+  fine.row_full_num = a.full_num;
+  fine.row_full_idx = a.full_idx;
+  fine.col_num = a.q_num;
+  fine.col_idx = a.q_idx;
+  fine.col_full_num = a.full_q_num;
+  fine.col_full_idx = a.full_q_idx;
+  fine.row_order = a.row_order;
+  fine.col_order = a.col_order;
+  e = launch_lists(fine, rows, cols, stream);
+  if (e != cudaSuccess || a.fwd.cls == nullptr) return e;
+  // tiles smaller than the attention kernels': their classes, coarsened, and lists
+  for (const ListJob* jb : {&a.fwd, &a.bwd}) {
+    const int64_t n = (int64_t)jb->planes * jb->n_r * jb->n_c;
+    e = launch_k(coarsen_kernel, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, stream, (const uint8_t*)a.tile_class,
+                 a.nq, a.nkv, jb->cls, jb->n_r, jb->n_c, (128 / a.block), (jb == &a.fwd ? a.fwd_kv_block : 128) / a.block,
+                 n);
+    if (e != cudaSuccess) return e;
+    e = launch_lists(*jb, jb->row_num ? (int64_t)jb->planes * jb->n_r : 0,
+                     jb->col_num ? (int64_t)jb->planes * jb->n_c : 0, stream);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 }  // namespace fa

@@ -26,10 +26,12 @@
 //       warp 12      TMA producer: V_J, then Q_I, dO_I per step, K_J with the first
 //       warp 13      MMA issuer, five tcgen05 GEMMs per (I, J):
 //                     once P^T is in:  dV  += P^T dO   (P^T bf16 read from TMEM [0,32), [64,96))
-//                     once dS is in:   dQ   = dS K     (dS read MN-major; TMEM [128,128+D))
+//                     once dS is in:   dQ   = dS K     (dS read MN-major; D = 128: TMEM [128,256),
+//                                                       D = 64: two buffers [384,448), [448,512))
 //                                      S^T  = K Q^T    (next step; TMEM [0,128))
 //                                      dK  += dS^T Q   (dS read K-major)
-//                                      dP^T = V dO^T   (next step; TMEM [128,256), once dQ is read out)
+//                                      dP^T = V dO^T   (next step; TMEM [128,256); with D = 128
+//                                                       once dQ is read out of those columns)
 //     dV runs while the key-row warps compute dS, and the next S^T before dK
 //     (with D = 64, right after dV) so that phase A of the next step can start
 //     early.  Registers are split per warpgroup (setmaxnreg): the dQ and
@@ -68,6 +70,11 @@ struct BwdCfg {
   static constexpr uint32_t STG_BYTES = 4u * 2u * BOX_BYTES;  // two boxes per dQ warp
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t T_S = 0, T_DP = 128, T_DV = 256, T_DK = 256 + D;
+  // dQ buffers: with D = 128 dQ is computed over the dP^T columns (TMEM is full),
+  // so the next dP^T waits until dQ has been read out; with D = 64 two buffers
+  // of their own in the columns left over, so that it does not
+  static constexpr int NDQ = (D == 64) ? 2 : 1;
+  static constexpr uint32_t t_dq(int b) { return NDQ == 1 ? T_DP : 256u + 2u * D + 64u * (uint32_t)b; }
   static constexpr int KEY_THREADS = 256;  // warps 0-7: P^T / dS^T, epilogue
   static constexpr int DQ_WARP0 = 8;       // warps 8-11: dQ out of TMEM into the accumulator
   static constexpr int DQ_THREADS = 128;
@@ -85,11 +92,19 @@ struct BwdCtl {
   uint64_t k_full, v_full, k_empty, v_empty;
   uint64_t q_full[2], q_empty[2];
   uint64_t do_full[2], do_empty[2];
-  uint64_t s_full, dp_full, pa_full, pb_full, dq_full, dq_free, acc_full, acc_free, fin;
+  uint64_t s_full, dp_full, pa_full, pb_full, acc_full, acc_free, fin;
+  uint64_t dq_full[2], dq_free[2];
+  // this CTA's items in the order the producer claimed them (see sched_get)
+  uint64_t sched_full[4], sched_empty[4];
+  int sched_k[4];
   uint32_t tmem;
   int abort;
   int32_t arg[2][FA_MAX_MASK_NODES];  // mask program arguments of the current item, per key-row half
 };
+
+static_assert(BwdCfg<64>::NQ <= 2 && BwdCfg<64>::NDO <= 2 && BwdCfg<64>::NDQ <= 2 && BwdCfg<128>::NQ <= 2 &&
+                  BwdCfg<128>::NDO <= 2 && BwdCfg<128>::NDQ <= 2,
+              "BwdCtl holds two barriers per Q, dO and dQ buffer");
 
 template <int D>
 constexpr size_t bwd_smem_bytes() {
@@ -97,6 +112,10 @@ constexpr size_t bwd_smem_bytes() {
   return 1024 + (size_t)C::TILE * (2 + C::NQ + C::NDO) + C::DS_BYTES + C::STG_BYTES + sizeof(BwdCtl);
 }
 static_assert(bwd_smem_bytes<128>() <= 227 * 1024, "backward shared memory");
+
+#ifdef FA_TEST_HOOKS
+__device__ int g_hook_skip_first_k;  // see test_hook_backward
+#endif
 
 __device__ __forceinline__ void fail(const AttnArgs& p, BwdCtl* ctl) {
   atomicOr(p.status, kStatusTimeout);
@@ -155,14 +174,23 @@ __device__ __forceinline__ int tile_of(const AttnArgs& p, const BwdItem& it, int
   return s < it.n_full ? __ldg(p.full_q_idx + it.list + s) : __ldg(p.q_idx + it.list + s - it.n_full);
 }
 
-// This CTA's first item at or after k (its items are k, k + gridDim.x, ...)
-// with at least one visible query tile; a value >= items when none is left.
-__device__ __forceinline__ int next_live(const AttnArgs& p, int k, int items, BwdItem& it) {
-  for (; k < items; k += (int)gridDim.x) {
-    it = bwd_item(p, k);
-    if (it.n > 0) break;
+// Dynamic schedule: the CTAs claim items from one counter in the longest-first
+// order, so that each takes the next item when its last one is done (the
+// greedy longest-processing-time rule: a few very long columns, such as the
+// sink tokens' column that every query tile sees, no longer pile up on the
+// CTAs that a static round robin gives them to).  Only items with at least one
+// visible query tile are handed out; the key tiles of the others get zero dK /
+// dV from bwd_pre.
+constexpr int kSchedSlots = 4;
+constexpr int kSchedConsumers = 1 + 4 + 8;  // MMA thread, dQ warps, key-row warps (one arrival per warp)
+
+__device__ __forceinline__ int claim_live(const AttnArgs& p, uint32_t* sched, int items) {
+  while (true) {
+    const int k = (int)atomicAdd(sched, 1u);
+    if (k >= items) return items;
+    const BwdItem it = bwd_item(p, k);
+    if (it.n > 0) return k;
   }
-  return k;
 }
 
 template <int D, int SCORE, bool PGRAD>
@@ -171,7 +199,7 @@ __global__ void __launch_bounds__(512, 1)
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_dv,
                const __grid_constant__ CUtensorMap tm_dq, const __grid_constant__ AttnArgs p,
-               const float* __restrict__ stats_g) {
+               const float* __restrict__ stats_g, uint32_t* __restrict__ sched) {
   using C = BwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -190,8 +218,7 @@ __global__ void __launch_bounds__(512, 1)
 
   const uint32_t b_kf = smem_u32(&ctl->k_full), b_vf = smem_u32(&ctl->v_full), b_ke = smem_u32(&ctl->k_empty),
                  b_ve = smem_u32(&ctl->v_empty), b_s = smem_u32(&ctl->s_full), b_dp = smem_u32(&ctl->dp_full),
-                 b_pa = smem_u32(&ctl->pa_full), b_pb = smem_u32(&ctl->pb_full), b_dq = smem_u32(&ctl->dq_full),
-                 b_dqf = smem_u32(&ctl->dq_free), b_acc = smem_u32(&ctl->acc_full),
+                 b_pa = smem_u32(&ctl->pa_full), b_pb = smem_u32(&ctl->pb_full), b_acc = smem_u32(&ctl->acc_full),
                  b_accf = smem_u32(&ctl->acc_free), b_fin = smem_u32(&ctl->fin);
   if (threadIdx.x == 0) {
     mbar_init(b_kf, 1);
@@ -208,11 +235,17 @@ __global__ void __launch_bounds__(512, 1)
     mbar_init(b_dp, 1);
     mbar_init(b_pa, C::KEY_THREADS);
     mbar_init(b_pb, C::KEY_THREADS);
-    mbar_init(b_dq, 1);
-    mbar_init(b_dqf, C::DQ_THREADS);
+    for (int b2 = 0; b2 < 2; ++b2) {
+      mbar_init(smem_u32(&ctl->dq_full[b2]), 1);
+      mbar_init(smem_u32(&ctl->dq_free[b2]), C::DQ_THREADS);
+    }
     mbar_init(b_acc, 1);
     mbar_init(b_accf, C::DQ_THREADS);
     mbar_init(b_fin, 1);
+    for (int sl = 0; sl < kSchedSlots; ++sl) {
+      mbar_init(smem_u32(&ctl->sched_full[sl]), 1);
+      mbar_init(smem_u32(&ctl->sched_empty[sl]), kSchedConsumers);
+    }
     ctl->abort = (*reinterpret_cast<volatile uint32_t*>(p.status) & kStatusTimeout) ? 1 : 0;
     fence_mbar_init();
   }
@@ -225,7 +258,21 @@ __global__ void __launch_bounds__(512, 1)
   tc_fence_after();
   const uint32_t tmem = ctl->tmem;
   const bool skip = ctl->abort != 0;
-  const int first = skip ? items : (int)blockIdx.x;
+
+  // Item u of this CTA's sequence (u = 0, 1, ...; `items` ends it), as the
+  // producer published it; false when the wait gave up.  Every consumer role
+  // releases slot u once it is done with item u.
+  auto sched_get = [&](int u, int& k) -> bool {
+    const int sl = u % kSchedSlots;
+    if (!mbar_wait(smem_u32(&ctl->sched_full[sl]), (u / kSchedSlots) & 1, &ctl->abort)) return false;
+    k = *reinterpret_cast<volatile int*>(&ctl->sched_k[sl]);
+    return true;
+  };
+  auto sched_get_warp = [&](int u, int& k) -> bool {
+    const bool r = __all_sync(0xffffffffu, sched_get(u, k));
+    return r;
+  };
+  auto sched_release = [&](int u) { mbar_arrive(smem_u32(&ctl->sched_empty[u % kSchedSlots])); };
 
   // teardown, at the end of every role: all threads past their last TMEM
   // access, then the allocating warp frees the columns
@@ -239,11 +286,10 @@ __global__ void __launch_bounds__(512, 1)
     }
   };
 
-  // The CTA stays resident and takes the items blockIdx.x, blockIdx.x +
-  // gridDim.x, ...; every role walks the same sequence.  Steps (I, J) are
-  // numbered across items (g) for the per-step barriers and the Q / dO rings;
-  // items with visible query tiles are numbered (u) for the K / V buffers and
-  // the dK / dV accumulators.
+  // The CTA stays resident and takes the items its producer claims; every role
+  // walks that sequence through the item ring.  Steps (I, J) are numbered
+  // across items (g) for the per-step barriers and the Q / dO rings; items are
+  // numbered (u) for the ring, the K / V buffers and the dK / dV accumulators.
   //
   // Register budgets per warpgroup, set at the top of each warpgroup's branch
   // (launched with 128 per thread): key-row warps 176, dQ warps 112, producer /
@@ -263,10 +309,30 @@ __global__ void __launch_bounds__(512, 1)
       int g = 0, q_issued = 0, do_issued = 0, v_issued = 0, k_issued = 0;
       int u = 0;
       bool ok = true;
-      BwdItem cur;
-      for (int k = next_live(p, first, items, cur); ok && k < items; ++u) {
-        BwdItem nxt;
-        const int kn = next_live(p, k + (int)gridDim.x, items, nxt);
+      // claims the next live item (lane 0) and publishes it as item uu
+      auto claim_publish = [&](int uu) -> int {
+        int kc = items;
+        if (lane == 0 && !skip) kc = claim_live(p, sched, items);
+        kc = __shfl_sync(0xffffffffu, kc, 0);
+        const int sl = uu % kSchedSlots;
+        if (uu >= kSchedSlots &&
+            !warp_wait(smem_u32(&ctl->sched_empty[sl]), (uu / kSchedSlots - 1) & 1, &ctl->abort))
+          return -1;
+        if (lane == 0) {
+          ctl->sched_k[sl] = kc;
+          mbar_arrive(smem_u32(&ctl->sched_full[sl]));
+        }
+        return kc;
+      };
+      int k = claim_publish(0);
+      ok = k >= 0;
+      while (ok && k < items) {
+        const BwdItem cur = bwd_item(p, k);
+        const int kn = claim_publish(u + 1);  // the next item, for the consumers' look-ahead
+        if (kn < 0) {
+          ok = false;
+          break;
+        }
         if (u > 0 && !warp_wait(b_ve, (u - 1) & 1, &ctl->abort)) {
           ok = false;
           break;
@@ -308,7 +374,12 @@ __global__ void __launch_bounds__(512, 1)
               ok = false;
               break;
             }
-            if (lane == 0) {
+#ifdef FA_TEST_HOOKS
+            const bool hook_skip = g_hook_skip_first_k != 0 && blockIdx.x == 0 && u == 0;
+#else
+            constexpr bool hook_skip = false;
+#endif
+            if (lane == 0 && !hook_skip) {
               mbar_arrive_expect_tx(b_kf, C::TILE);
               for (int c = 0; c < C::NC; ++c)
                 tma_load_3d(smem_u32(sK + c * 16384), &tm_k, b_kf, c * 64, cur.J * 128, cur.bh);
@@ -316,8 +387,8 @@ __global__ void __launch_bounds__(512, 1)
             k_issued = u + 1;
           }
         }
-        cur = nxt;
         k = kn;
+        ++u;
       }
       if (!ok && lane == 0) fail(p, ctl);
       // drain: every copy this CTA started lands before it exits (each buffer's
@@ -358,14 +429,14 @@ __global__ void __launch_bounds__(512, 1)
           mma_commit(b_s);
           return true;
         };
-        // dP^T = V dO^T of step g, into the columns dQ of the step before was
-        // computed in: it waits until the dQ warps have read that dQ out.  The
-        // item's last dP^T is the last reader of V.
+        // dP^T = V dO^T of step g; with one dQ buffer it goes into the columns dQ
+        // of the step before was computed in, and waits until the dQ warps have
+        // read that dQ out.  The item's last dP^T is the last reader of V.
         auto issue_dp = [&](int g, int s, int n, int u) -> bool {
           const int ds = g % C::NDO;
           if (s == 0 && !mbar_wait(b_vf, u & 1, &ctl->abort)) return false;
           if (!mbar_wait(smem_u32(&ctl->do_full[ds]), (g / C::NDO) & 1, &ctl->abort)) return false;
-          if (g > 0 && !mbar_wait(b_dqf, (g - 1) & 1, &ctl->abort)) return false;
+          if (C::NDQ == 1 && g > 0 && !mbar_wait(smem_u32(&ctl->dq_free[0]), (g - 1) & 1, &ctl->abort)) return false;
           tc_fence_after();
           const uint64_t a0 = opaque(sdesc_sw128(v_base, 16, 1024)), b0 = opaque(sdesc_sw128(smem_u32(sDO(ds)), 16, 1024));
 #pragma unroll
@@ -375,17 +446,20 @@ __global__ void __launch_bounds__(512, 1)
           if (s == n - 1) mma_commit(b_ve);
           return true;
         };
-        int g = 0, u = 0;
-        bool ok = true;
-        BwdItem cur;
-        for (int k = next_live(p, first, items, cur); ok && k < items; ++u) {
+        int g = 0, u = 0, k = items;
+        bool ok = sched_get(0, k);
+        while (ok && k < items) {
+          const BwdItem cur = bwd_item(p, k);
           const int n = cur.n;
           if (!issue_s(g, 0, u) || !issue_dp(g, 0, n, u)) {
             ok = false;
             break;
           }
-          BwdItem nxt;
-          const int kn = next_live(p, k + (int)gridDim.x, items, nxt);
+          int kn = items;
+          if (!sched_get(u + 1, kn)) {
+            ok = false;
+            break;
+          }
           for (int s = 0; s < n; ++s, ++g) {
             const int qs = g % C::NQ, ds = g % C::NDO;
             const uint32_t q_base = smem_u32(sQ(qs)), do_base = smem_u32(sDO(ds));
@@ -417,13 +491,20 @@ __global__ void __launch_bounds__(512, 1)
               ok = false;
               break;
             }
+            // with two dQ buffers, this step's has been read out two steps ago
+            if (C::NDQ == 2 && g >= 2 &&
+                !mbar_wait(smem_u32(&ctl->dq_free[g & 1]), ((g >> 1) - 1) & 1, &ctl->abort)) {
+              ok = false;
+              break;
+            }
             tc_fence_after();
-            {  // dQ = dS K, over the dP^T columns the key-row warps have read
+            {  // dQ = dS K (one buffer: over the dP^T columns the key-row warps have read)
               const uint64_t a0 = opaque(sdesc_sw128(ds_base, 16384, 1024)), b0 = opaque(sdesc_sw128(k_base, 16384, 1024));
 #pragma unroll
-              for (int kk = 0; kk < 8; ++kk) mma_ss(tmem + C::T_DP, mnmajor_step(a0, kk), mnmajor_step(b0, kk), kIdMM, kk > 0);
+              for (int kk = 0; kk < 8; ++kk)
+                mma_ss(tmem + C::t_dq(g % C::NDQ), mnmajor_step(a0, kk), mnmajor_step(b0, kk), kIdMM, kk > 0);
             }
-            mma_commit(b_dq);
+            mma_commit(smem_u32(&ctl->dq_full[g % C::NDQ]));
             if (!kEarlyS && s + 1 < n && !issue_s(g + 1, s + 1, u)) {
               ok = false;
               break;
@@ -443,8 +524,9 @@ __global__ void __launch_bounds__(512, 1)
           }
           if (!ok) break;
           mma_commit(b_acc);  // dV, dK of the item complete
-          cur = nxt;
+          sched_release(u);
           k = kn;
+          ++u;
         }
         if (!ok) fail(p, ctl);
         mma_commit(b_fin);
@@ -462,29 +544,30 @@ __global__ void __launch_bounds__(512, 1)
     // box is rewritten only once the bulk copy issued from it two rounds before
     // has read it.  After an item's last step the same rows of dV and
     // scale * dK leave TMEM through the same boxes (as 32 x 64 bf16) by TMA
-    // store (zeros for a key tile that no query tile sees).
+    // store.
     const int rw = (warp % 4) * 32;  // first dQ / key row of this warp
     const uint32_t t_lane = tmem + ((uint32_t)rw << 16);
-    const uint32_t tq = t_lane + C::T_DP;
     uint8_t* box0 = sSTG + (warp % 4) * (2 * C::BOX_BYTES);
-    int round = 0, u = 0, g = 0;
-    bool ok = true;
-    for (int k = first; ok && k < items; k += (int)gridDim.x) {
+    int round = 0, u = 0, g = 0, k = items;
+    bool ok = sched_get_warp(0, k);
+    while (ok && k < items) {
       const BwdItem cur = bwd_item(p, k);
       for (int s = 0; s < cur.n; ++s, ++g) {
         const int I = tile_of(p, cur, s);
-        if (!warp_wait(b_dq, g & 1, &ctl->abort)) {
+        const int bq = g % C::NDQ;
+        if (!warp_wait(smem_u32(&ctl->dq_full[bq]), (g / C::NDQ) & 1, &ctl->abort)) {
           ok = false;
           break;
         }
         tc_fence_after();
+        const uint32_t tq = t_lane + C::t_dq(bq);
 #pragma unroll 1
         for (int h2 = 0; h2 < D / 64; ++h2) {
           float v[64];
           tmem_ld64f(tq + 64 * h2, v);
           if (h2 == D / 64 - 1) {
             tc_fence_before();
-            mbar_arrive(b_dqf);  // TMEM columns free for the next dP^T
+            mbar_arrive(smem_u32(&ctl->dq_free[bq]));  // TMEM columns free for the next dP^T / dQ
           }
 #pragma unroll
           for (int bx = 0; bx < 2; ++bx, ++round) {
@@ -509,28 +592,20 @@ __global__ void __launch_bounds__(512, 1)
       if (!ok) break;
       // dV, then scale * dK, 64 columns at a time; the accumulators are free for
       // the next item once the last columns are read
-      const bool live = cur.n > 0;
-      if (live) {
-        if (!warp_wait(b_acc, u & 1, &ctl->abort)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
+      if (!warp_wait(b_acc, u & 1, &ctl->abort)) {
+        ok = false;
+        break;
       }
+      tc_fence_after();
 #pragma unroll 1
       for (int c = 0; c < 2 * (D / 64); ++c, ++round) {
         const bool is_k = c >= D / 64;
         const int h2 = is_k ? c - D / 64 : c;
         float a[64];
-        if (live) {
-          tmem_ld64f(t_lane + (is_k ? C::T_DK : C::T_DV) + 64 * h2, a);
-          if (c == 2 * (D / 64) - 1) {
-            tc_fence_before();
-            mbar_arrive(b_accf);
-          }
-        } else {
-#pragma unroll
-          for (int e = 0; e < 64; ++e) a[e] = 0.f;
+        tmem_ld64f(t_lane + (is_k ? C::T_DK : C::T_DV) + 64 * h2, a);
+        if (c == 2 * (D / 64) - 1) {
+          tc_fence_before();
+          mbar_arrive(b_accf);
         }
         const float sc = is_k ? p.scale : 1.0f;
         uint8_t* box = box0 + (round & 1) * C::BOX_BYTES;
@@ -549,7 +624,10 @@ __global__ void __launch_bounds__(512, 1)
           bulk_commit();
         }
       }
-      if (live) ++u;
+      __syncwarp();
+      if (lane == 0) sched_release(u);
+      ++u;
+      ok = sched_get_warp(u, k);
     }
     if (!ok) fail(p, ctl);
     if (lane == 0) bulk_wait0();  // every reduce and store of this warp has completed
@@ -578,31 +656,29 @@ __global__ void __launch_bounds__(512, 1)
     const int st_idx = (r < 64) ? (64 * half + r) : (128 + 64 * half + r - 64);
     auto stat_of = [&](int bh, int I) { return __ldg(stats_g + ((int64_t)bh * p.nq + I) * 256 + st_idx); };
     int32_t* arg_s = ctl->arg[half];
-    int k = first, I_next = 0;  // the query tile of the next step
-    {
-      BwdItem it0;
-      k = next_live(p, first, items, it0);
-      if (k < items) {
-        I_next = tile_of(p, it0, 0);
-        reinterpret_cast<float*>(&ctl->stats)[st_idx] = stat_of(it0.bh, I_next);
-        if (r < p.mask.n) arg_s[r] = node_arg(p.mask, r, it0.bm);
-      }
+    int k = items, I_next = 0;  // the query tile of the next step
+    bool ok = sched_get_warp(0, k), lok = true;
+    if (ok && k < items) {
+      const BwdItem it0 = bwd_item(p, k);
+      I_next = tile_of(p, it0, 0);
+      reinterpret_cast<float*>(&ctl->stats)[st_idx] = stat_of(it0.bh, I_next);
+      if (r < p.mask.n) arg_s[r] = node_arg(p.mask, r, it0.bm);
     }
-    int g = 0;
-    bool ok = true, lok = true;
+    int g = 0, u = 0;
     while (ok && k < items) {
       const BwdItem cur = bwd_item(p, k);
       // of the next item only what the last step hands over: its first query
       // tile (for the stats), head and mask batch
-      int kn, nxt_i0 = 0, nxt_bh = 0, nxt_bm = 0;
-      {
-        BwdItem nxt;
-        kn = next_live(p, k + (int)gridDim.x, items, nxt);
-        if (kn < items) {
-          nxt_i0 = tile_of(p, nxt, 0);
-          nxt_bh = nxt.bh;
-          nxt_bm = nxt.bm;
-        }
+      int kn = items, nxt_i0 = 0, nxt_bh = 0, nxt_bm = 0;
+      if (!sched_get_warp(u + 1, kn)) {
+        ok = false;
+        break;
+      }
+      if (kn < items) {
+        const BwdItem nxt = bwd_item(p, kn);
+        nxt_i0 = tile_of(p, nxt, 0);
+        nxt_bh = nxt.bh;
+        nxt_bm = nxt.bm;
       }
       const int n = cur.n, bh = cur.bh;
       const int j = cur.J * 128 + r;  // key row
@@ -767,7 +843,10 @@ __global__ void __launch_bounds__(512, 1)
           if (lane == 0 && sum != 0.f) atomicAdd(p.param_grad + cur.h, sum);
         }
       }
+      __syncwarp();
+      if (lane == 0) sched_release(u);
       k = kn;
+      ++u;
     }
     if (ok && !lok) ok = false;
     if (!ok) fail(p, ctl);
@@ -777,17 +856,41 @@ __global__ void __launch_bounds__(512, 1)
 
 // Per query row: -LSE * log2(e) and -Delta (Delta_i = dO_i . out_i, fp32)
 // into the per-tile stats array [B*H][nq][2][128], zero for the rows past
-// q_len in the last tile; the fp32 dq accumulator rows and the score
-// parameter's gradient (if requested) set to zero.
-// 16 threads per row, 16 rows per 256-thread block.
+// q_len in the last tile; the fp32 dq accumulator rows, the score parameter's
+// gradient (if requested) and the main kernel's item counter set to zero.
+// 16 threads per row, 16 rows per 256-thread block; the blocks after the rows'
+// take one key tile (b, h, J) each and write zero dK and dV for a key tile
+// that no query tile sees (the main kernel hands out only the others).
 template <int D>
-__global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __restrict__ out,
+__global__ void __launch_bounds__(256) bwd_pre_kernel(const __grid_constant__ AttnArgs p,
+                                                      const __nv_bfloat16* __restrict__ out,
                                                       const __nv_bfloat16* __restrict__ dout,
                                                       const float* __restrict__ lse, float* __restrict__ stats,
-                                                      float* __restrict__ dq_acc, int64_t rows, int q_len, int nq,
-                                                      float* __restrict__ param_grad, int n_param_grad) {
-  if (blockIdx.x == 0)  // the main kernel adds into it
+                                                      float* __restrict__ dq_acc, int64_t rows, int64_t row_blocks,
+                                                      float* __restrict__ param_grad, int n_param_grad,
+                                                      uint32_t* __restrict__ sched, __nv_bfloat16* __restrict__ dk,
+                                                      __nv_bfloat16* __restrict__ dv) {
+  const int q_len = p.q_len, nq = p.nq;
+  if (blockIdx.x == 0) {  // the main kernel adds into them
     for (int k = threadIdx.x; k < n_param_grad; k += blockDim.x) param_grad[k] = 0.f;
+    if (threadIdx.x == 0) *sched = 0u;
+  }
+  if ((int64_t)blockIdx.x >= row_blocks) {
+    const int64_t t = (int64_t)blockIdx.x - row_blocks;  // (b * H + h) * nkv + J
+    const int J = (int)(t % p.nkv);
+    const int bh = (int)(t / p.nkv), b = bh / p.H, h = bh % p.H;
+    const int64_t col = ((int64_t)(p.Bm == 1 ? 0 : b) * p.Hm + (p.Hm == 1 ? 0 : h)) * p.nkv + J;
+    if (__ldg(p.q_num + col) + __ldg(p.full_q_num + col) != 0) return;
+    const int64_t r0 = (int64_t)J * 128, r1 = min((int64_t)p.kv_len, r0 + 128);
+    const int64_t n8 = (r1 - r0) * D / 8;  // 16-byte pieces of each tensor's rows
+    uint4* zk = reinterpret_cast<uint4*>(dk + ((int64_t)bh * p.kv_len + r0) * D);
+    uint4* zv = reinterpret_cast<uint4*>(dv + ((int64_t)bh * p.kv_len + r0) * D);
+    for (int64_t k = threadIdx.x; k < n8; k += blockDim.x) {
+      zk[k] = make_uint4(0u, 0u, 0u, 0u);
+      zv[k] = make_uint4(0u, 0u, 0u, 0u);
+    }
+    return;
+  }
   constexpr int E = D / 16;  // elements per thread
   const int64_t row = (int64_t)blockIdx.x * 16 + threadIdx.x / 16;
   const int t = threadIdx.x % 16;
@@ -838,9 +941,11 @@ template <int D, int SCORE, bool PGRAD>
 cudaError_t launch_bwd_t(const AttnArgs& a, const BwdTensors& t, cudaStream_t stream, bool* enc_failed) {
   const uint64_t bh = (uint64_t)a.B * a.H;
   const int64_t rows = (int64_t)bh * a.q_len;
-  bwd_pre_kernel<D><<<(unsigned)((rows + 15) / 16), 256, 0, stream>>>(
-      static_cast<const __nv_bfloat16*>(t.out), static_cast<const __nv_bfloat16*>(t.dout), t.lse, t.stats, t.dq_acc,
-      rows, a.q_len, a.nq, a.param_grad, PGRAD ? a.H : 0);
+  const int64_t row_blocks = (rows + 15) / 16;
+  bwd_pre_kernel<D><<<(unsigned)(row_blocks + (int64_t)bh * a.nkv), 256, 0, stream>>>(
+      a, static_cast<const __nv_bfloat16*>(t.out), static_cast<const __nv_bfloat16*>(t.dout), t.lse, t.stats,
+      t.dq_acc, rows, row_blocks, a.param_grad, PGRAD ? a.H : 0, t.sched, static_cast<__nv_bfloat16*>(t.dk),
+      static_cast<__nv_bfloat16*>(t.dv));
 
   CUtensorMap mq, mk, mv, mdo, mdk, mdv;
   auto enc = [&](CUtensorMap* m, const void* ptr, int64_t len, uint32_t rows) {
@@ -872,7 +977,7 @@ cudaError_t launch_bwd_t(const AttnArgs& a, const BwdTensors& t, cudaStream_t st
   const unsigned grid = (unsigned)std::min<int64_t>(items, sms);
   if (grid > 0)
     bwd_kernel<D, SCORE, PGRAD><<<grid, BwdCfg<D>::THREADS, smem, stream>>>(
-        mq, mk, mv, mdo, mdk, mdv, mdq, a, t.stats);
+        mq, mk, mv, mdo, mdk, mdv, mdq, a, t.stats, t.sched);
   const int64_t n8 = rows * D / 8;
   bwd_dq_convert_kernel<<<(unsigned)((n8 + 255) / 256), 256, 0, stream>>>(
       t.dq_acc, static_cast<__nv_bfloat16*>(t.dq), n8, a.scale);
@@ -908,6 +1013,13 @@ cudaError_t noalloc_scratch(void** ptr) {
   *ptr = addr[dev];
   return cudaSuccess;
 }
+
+#ifdef FA_TEST_HOOKS
+cudaError_t test_hook_backward(int on) {
+  const int v = on ? 1 : 0;
+  return cudaMemcpyToSymbol(g_hook_skip_first_k, &v, sizeof(v));
+}
+#endif
 
 cudaError_t launch_backward(const AttnArgs& a, const BwdTensors& t, cudaStream_t stream, bool* enc_failed) {
   *enc_failed = false;

@@ -21,8 +21,11 @@
 // S has read the buffer, its first S runs while the epilogue reads O out of
 // TMEM, and the output is staged in shared memory (the last V slot with two
 // slots) and stored by TMA (thread 0) without waiting.
-// TMEM (256 columns): S at [0, 128) -- P (bf16 pairs) overwrites its first 64
+// TMEM (256 columns): S at [0, BK) -- P (bf16 pairs) overwrites its first BK / 2
 // columns after the softmax has read S -- and O at [128, 128 + D).
+// Key tiles are BK = 128 positions, or 64 when the block mask's tiles are
+// smaller (tutorial, sharp edge 4): then S is 128 x 64, the P V of a step is
+// one group of four MMAs, and the output has a staging buffer of its own.
 // The running maximum is only moved (and O rescaled) when a new row maximum
 // exceeds it by more than 2^8, so most tiles need no O round trip.
 #include <algorithm>
@@ -41,12 +44,18 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
-template <int D>
+// BK: key positions per listed key tile -- 128, or 64 for block masks with
+// smaller tiles (the builder's 128 x 64 lists).
+template <int D, int BK>
 struct FwdCfg {
   static constexpr int NC = D / 64;                      // 64-column (128-byte) chunks per tile row
-  static constexpr uint32_t TILE = 128u * D * 2u;        // bytes of one 128 x D bf16 tile
-  static constexpr int NS = (D == 64) ? 4 : 2;           // K/V ring slots
-  static constexpr bool STAGE_IN_RING = (NS == 2);       // output staged in the last V slot
+  static constexpr uint32_t TILE = 128u * D * 2u;        // bytes of one 128 x D bf16 tile (Q, output)
+  static constexpr uint32_t KV_TILE = (uint32_t)BK * D * 2u;  // one K or V tile
+  static constexpr uint32_t KV_CHUNK = (uint32_t)BK * 128u;   // one 64-column chunk of it
+  // K/V ring slots: two CTAs per SM must fit
+  static constexpr int NS = (BK == 128) ? ((D == 64) ? 4 : 2) : ((D == 64) ? 6 : 2);
+  static constexpr bool STAGE_IN_RING = (NS == 2 && BK == 128);  // output staged in the last V slot
+  static constexpr int NW = BK / 32;                     // 32-column mask words per row and step
   static constexpr uint32_t TMEM_COLS = 256;
 };
 
@@ -58,10 +67,12 @@ struct FwdItem {
   int64_t list;  // offset of the row's lists
 };
 
+constexpr int kMaxKvSlots = 8;  // K/V ring slots the control block has barriers for
+
 struct FwdCtl {
   uint64_t q_full, q_empty;
-  uint64_t kv_full[4];
-  uint64_t kv_empty[4];
+  uint64_t kv_full[kMaxKvSlots];
+  uint64_t kv_empty[kMaxKvSlots];
   uint64_t s_full;
   uint64_t p_half, p_full;  // P of the first 64 keys, of all 128 keys
   uint64_t o_full, o_free;
@@ -78,14 +89,30 @@ struct FwdCtl {
   alignas(16) int4 seg[2][128];
 };
 
-template <int D>
+template <int D, int BK>
 constexpr size_t fwd_smem_bytes() {
-  using C = FwdCfg<D>;
-  return 1024 + (size_t)C::TILE * (1 + C::NS + (C::STAGE_IN_RING ? 0 : 1)) + sizeof(FwdCtl);
+  using C = FwdCfg<D, BK>;
+  return 1024 + (size_t)C::TILE * (1 + (C::STAGE_IN_RING ? 0 : 1)) + (size_t)C::KV_TILE * C::NS + sizeof(FwdCtl);
 }
 // two CTAs per SM (228 KB of shared memory, 1 KB of it reserved per CTA)
-static_assert(2 * (fwd_smem_bytes<128>() + 1024) <= 228 * 1024, "forward shared memory, D = 128");
-static_assert(2 * (fwd_smem_bytes<64>() + 1024) <= 228 * 1024, "forward shared memory, D = 64");
+static_assert(2 * (fwd_smem_bytes<128, 128>() + 1024) <= 228 * 1024, "forward shared memory, D = 128");
+static_assert(2 * (fwd_smem_bytes<64, 128>() + 1024) <= 228 * 1024, "forward shared memory, D = 64");
+static_assert(2 * (fwd_smem_bytes<128, 64>() + 1024) <= 228 * 1024, "forward shared memory, D = 128, BK = 64");
+static_assert(2 * (fwd_smem_bytes<64, 64>() + 1024) <= 228 * 1024, "forward shared memory, D = 64, BK = 64");
+static_assert(FwdCfg<128, 128>::NS <= kMaxKvSlots && FwdCfg<64, 128>::NS <= kMaxKvSlots &&
+                  FwdCfg<128, 64>::NS <= kMaxKvSlots && FwdCfg<64, 64>::NS <= kMaxKvSlots,
+              "every K/V ring slot needs its pair of barriers in FwdCtl");
+
+// K-major descriptor of MMA step kk for a tile whose 64-column chunks are
+// `chunk` bytes apart (rows x 128 B): byte 32 (kk % 4) of chunk kk / 4.
+template <uint32_t CHUNK>
+__device__ __forceinline__ uint64_t kmajor_step_c(uint64_t desc, int kk) {
+  return desc + (uint64_t)((kk >> 2) * (CHUNK >> 4) + (kk & 3) * (32 >> 4));
+}
+
+#ifdef FA_TEST_HOOKS
+__device__ int g_hook_skip_first_k;  // see test_hook_forward
+#endif
 
 __device__ __forceinline__ void fail(const AttnArgs& p, FwdCtl* ctl) {
   atomicOr(p.status, kStatusTimeout);
@@ -138,21 +165,25 @@ __device__ __forceinline__ int next_live(const AttnArgs& p, int k, int items, Fw
   return k;
 }
 
-template <int D, int SCORE>
+template <int D, int SCORE, int BK>
 __global__ void __launch_bounds__(192, 2)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                const __grid_constant__ AttnArgs p, float* __restrict__ lse_out,
                __nv_bfloat16* __restrict__ out_g) {
-  using C = FwdCfg<D>;
+  using C = FwdCfg<D, BK>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = smem;
   uint8_t* sKV = smem + C::TILE;
   // output staging: the V slot of an item's last step (with two slots every V
   // goes to slot 1), else a buffer of its own
-  uint8_t* sOut = C::STAGE_IN_RING ? sKV + C::TILE : sKV + C::NS * C::TILE;
-  FwdCtl* ctl = reinterpret_cast<FwdCtl*>(sKV + (C::NS + (C::STAGE_IN_RING ? 0 : 1)) * C::TILE);
+  uint8_t* sOut = C::STAGE_IN_RING ? sKV + C::KV_TILE : sKV + C::NS * C::KV_TILE;
+  // control block after the ring and the output buffer (when there is one)
+  FwdCtl* ctl = reinterpret_cast<FwdCtl*>(sKV + C::NS * C::KV_TILE + (C::STAGE_IN_RING ? 0 : C::TILE));
+  static_assert(C::NS * C::KV_TILE + (C::STAGE_IN_RING ? 0 : C::TILE) + C::TILE + sizeof(FwdCtl) + 1024 <=
+                    fwd_smem_bytes<D, BK>(),
+                "forward shared-memory layout");
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int items = p.B * p.H * p.nq;  // below 2^31: checked at launch
@@ -247,9 +278,10 @@ __global__ void __launch_bounds__(192, 2)
       q_issued = u + 1;
       for (int jj = 0; ok && jj < cur.n; ++jj, ++t) {
         const int J = jj == 0 ? cur.J0 : tile_of(p, cur, jj);
-        // rows of key tile J: in the caller's [B*H][kv_len] tensors, or (paged)
-        // in the page the table names, of this head's [n_pages * 128] pool rows
-        int kv_row = J * 128, kv_z = cur.bh;
+        // rows of key tile J: in the caller's [B*H][kv_len] tensors, or (paged,
+        // BK = 128 only) in the page the table names, of this head's
+        // [n_pages * 128] pool rows
+        int kv_row = J * BK, kv_z = cur.bh;
         if (p.page_table != nullptr && lane == 0) {
           int page = __ldg(p.page_table + (int64_t)(cur.bh / p.H) * p.nkv + J);
           if (page < 0 || page >= p.n_pages) {  // reported; page 0 is read instead
@@ -269,12 +301,17 @@ __global__ void __launch_bounds__(192, 2)
             ok = false;
             break;
           }
-          if (lane == 0) {
+#ifdef FA_TEST_HOOKS
+          const bool hook_skip = g_hook_skip_first_k != 0 && blockIdx.x == 0 && t == 0 && kv == 0;
+#else
+          constexpr bool hook_skip = false;
+#endif
+          if (lane == 0 && !hook_skip) {
             const uint32_t bar = smem_u32(&ctl->kv_full[slot]);
-            mbar_arrive_expect_tx(bar, C::TILE);
+            mbar_arrive_expect_tx(bar, C::KV_TILE);
             const CUtensorMap* m = kv ? &tm_v : &tm_k;
             for (int c = 0; c < C::NC; ++c)
-              tma_load_3d(smem_u32(sKV + slot * C::TILE + c * 16384), m, bar, c * 64, kv_row, kv_z);
+              tma_load_3d(smem_u32(sKV + slot * C::KV_TILE + c * C::KV_CHUNK), m, bar, c * 64, kv_row, kv_z);
           }
           issued = pos + 1;
         }
@@ -294,7 +331,7 @@ __global__ void __launch_bounds__(192, 2)
   } else if (warp == 5) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t kIdS = idesc_bf16(128, 128, false, false);  // Q (K-major) x K (K-major)
+      constexpr uint32_t kIdS = idesc_bf16(128, BK, false, false);   // Q (K-major) x K (K-major)
       constexpr uint32_t kIdO = idesc_bf16(128, D, false, true);     // P (TMEM) x V (MN-major)
       const uint32_t q_base = smem_u32(sQ);
       int t = 0, u = 0;
@@ -315,10 +352,11 @@ __global__ void __launch_bounds__(192, 2)
             break;
           }
           tc_fence_after();
-          const uint32_t k_base = smem_u32(sKV + sk * C::TILE);
+          const uint32_t k_base = smem_u32(sKV + sk * C::KV_TILE);
           const uint64_t a0 = opaque(sdesc_sw128(q_base, 16, 1024)), b0 = opaque(sdesc_sw128(k_base, 16, 1024));
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) mma_ss(tmem, kmajor_step(a0, kk), kmajor_step(b0, kk), kIdS, kk > 0);
+          for (int kk = 0; kk < D / 16; ++kk)
+            mma_ss(tmem, kmajor_step(a0, kk), kmajor_step_c<C::KV_CHUNK>(b0, kk), kIdS, kk > 0);
           mma_commit(smem_u32(&ctl->kv_empty[sk]));
           if (jj == n - 1) mma_commit(b_qe);  // Q read for the last time in this item
           mma_commit(b_s);
@@ -341,17 +379,19 @@ __global__ void __launch_bounds__(192, 2)
             break;
           }
           tc_fence_after();
-          const uint32_t v_base = smem_u32(sKV + sv * C::TILE);
-          const uint64_t v0 = opaque(sdesc_sw128(v_base, 16384, 1024));
+          const uint32_t v_base = smem_u32(sKV + sv * C::KV_TILE);
+          const uint64_t v0 = opaque(sdesc_sw128(v_base, C::KV_CHUNK, 1024));
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) mma_ts(tmem + 128, tmem + kk * 8, mnmajor_step(v0, kk), kIdO, (jj > 0 || kk > 0));
-          if (!mbar_wait(b_p, t & 1, &ctl->abort)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
+          if constexpr (BK == 128) {  // keys [64, 128) once the rest of P is in
+            if (!mbar_wait(b_p, t & 1, &ctl->abort)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
 #pragma unroll
-          for (int kk = 4; kk < 8; ++kk) mma_ts(tmem + 128, tmem + kk * 8, mnmajor_step(v0, kk), kIdO, true);
+            for (int kk = 4; kk < 8; ++kk) mma_ts(tmem + 128, tmem + kk * 8, mnmajor_step(v0, kk), kIdO, true);
+          }
           mma_commit(smem_u32(&ctl->kv_empty[sv]));
         }
         if (!ok) break;
@@ -431,14 +471,16 @@ __global__ void __launch_bounds__(192, 2)
         const bool partial = jj >= n_full;
         const int J = J_next;
         if (jj + 1 < n) J_next = tile_of(p, cur, jj + 1);
-        const int64_t j0 = (int64_t)J * 128;
-        const bool ragged = j0 + 128 > p.kv_len;
+        const int64_t j0 = (int64_t)J * BK;
+        const bool ragged = j0 + BK > p.kv_len;
         const bool msk = partial || ragged;
-        // visibility words of the 4 x 32 key columns, computed before S is loaded
-        uint32_t wd[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};
+        // visibility words of the NW x 32 key columns, computed before S is loaded
+        uint32_t wd[C::NW];
+  #pragma unroll
+        for (int c = 0; c < C::NW; ++c) wd[c] = 0xffffffffu;
         if (msk) {
   #pragma unroll 1
-          for (int c = 0; c < 4; ++c) {
+          for (int c = 0; c < C::NW; ++c) {
             const int jc = (int)j0 + 32 * c;
             uint32_t w = low_bits((int64_t)p.kv_len - jc);
             const int4 sg = *seg_s;
@@ -466,10 +508,8 @@ __global__ void __launch_bounds__(192, 2)
               w &= mask_word_rolled(p.mask.n, mask_ops, ctl->arg, i, jc, eq);
             }
             // select by c without dynamic indexing
-            wd[0] = (c == 0) ? w : wd[0];
-            wd[1] = (c == 1) ? w : wd[1];
-            wd[2] = (c == 2) ? w : wd[2];
-            wd[3] = (c == 3) ? w : wd[3];
+  #pragma unroll
+            for (int c2 = 0; c2 < C::NW; ++c2) wd[c2] = (c == c2) ? w : wd[c2];
           }
         }
         // the staging of the last item's output has been read by its store
@@ -483,11 +523,14 @@ __global__ void __launch_bounds__(192, 2)
           break;
         }
         tc_fence_after();
-        float s[128];
-        tmem_ld128f(tS, s);
+        float s[BK];
+        if constexpr (BK == 128)
+          tmem_ld128f(tS, s);
+        else
+          tmem_ld64f(tS, s);
         if (msk) {
   #pragma unroll
-          for (int e = 0; e < 128; ++e) s[e] = ((wd[e >> 5] >> (e & 31)) & 1u) ? s[e] : -INFINITY;
+          for (int e = 0; e < BK; ++e) s[e] = ((wd[e >> 5] >> (e & 31)) & 1u) ? s[e] : -INFINITY;
         }
 
         const float base = slope_l2 * (float)(i - (int)j0);  // ALiBi: -slope (i - j) = -base + slope * e
@@ -496,7 +539,7 @@ __global__ void __launch_bounds__(192, 2)
         {
           float a0 = -INFINITY, a1 = -INFINITY, a2 = -INFINITY, a3 = -INFINITY;
   #pragma unroll
-          for (int e = 0; e < 128; e += 8) {
+          for (int e = 0; e < BK; e += 8) {
             if constexpr (SCORE == FA_S_ALIBI) {
               float t[8];
   #pragma unroll
@@ -564,7 +607,7 @@ __global__ void __launch_bounds__(192, 2)
             }
           };
   #pragma unroll
-          for (int c = 0; c < 4; ++c) {
+          for (int c = 0; c < C::NW; ++c) {
             uint32_t pk[16];
   #pragma unroll
             for (int e2 = 0; e2 < 16; e2 += 2) {
@@ -660,7 +703,7 @@ __global__ void __launch_bounds__(192, 2)
   }
 }
 
-template <int D, int SCORE>
+template <int D, int SCORE, int BK>
 cudaError_t launch_fwd_t(const AttnArgs& a, const FwdTensors& t, cudaStream_t stream, bool* enc_failed) {
   const uint64_t bh = (uint64_t)a.B * a.H;
   // keys / values: [B*H][kv_len][D], or the paged pools [H][n_pages * 128][D]
@@ -670,9 +713,9 @@ cudaError_t launch_fwd_t(const AttnArgs& a, const FwdTensors& t, cudaStream_t st
   CUtensorMap mq, mk, mv, mo;
   const bool ok = encode_tmap_3d(&mq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, t.q, D, a.q_len, bh, 64, 128,
                                  CU_TENSOR_MAP_SWIZZLE_128B) &&
-                  encode_tmap_3d(&mk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, t.k, D, kv_rows, kv_z, 64, 128,
+                  encode_tmap_3d(&mk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, t.k, D, kv_rows, kv_z, 64, BK,
                                  CU_TENSOR_MAP_SWIZZLE_128B) &&
-                  encode_tmap_3d(&mv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, t.v, D, kv_rows, kv_z, 64, 128,
+                  encode_tmap_3d(&mv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, t.v, D, kv_rows, kv_z, 64, BK,
                                  CU_TENSOR_MAP_SWIZZLE_128B) &&
                   encode_tmap_3d(&mo, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, t.out, D, a.q_len, bh, 64, 128,
                                  CU_TENSOR_MAP_SWIZZLE_128B);
@@ -680,10 +723,10 @@ cudaError_t launch_fwd_t(const AttnArgs& a, const FwdTensors& t, cudaStream_t st
     *enc_failed = true;
     return cudaErrorUnknown;
   }
-  constexpr size_t smem = fwd_smem_bytes<D>();
+  constexpr size_t smem = fwd_smem_bytes<D, BK>();
   static PerDeviceOnce attr_once;
   cudaError_t e = attr_once.run([] {
-    return cudaFuncSetAttribute(fwd_kernel<D, SCORE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    return cudaFuncSetAttribute(fwd_kernel<D, SCORE, BK>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   });
   if (e != cudaSuccess) return e;
   // persistent: two CTAs per SM (or one per item, when there are fewer)
@@ -695,22 +738,39 @@ cudaError_t launch_fwd_t(const AttnArgs& a, const FwdTensors& t, cudaStream_t st
   if (items >= ((int64_t)1 << 31)) return cudaErrorInvalidValue;
   const unsigned grid = (unsigned)std::min<int64_t>(items, 2 * (int64_t)sms);
   if (grid > 0)
-    fwd_kernel<D, SCORE><<<grid, 192, smem, stream>>>(mq, mk, mv, mo, a, t.lse, static_cast<__nv_bfloat16*>(t.out));
+    fwd_kernel<D, SCORE, BK><<<grid, 192, smem, stream>>>(mq, mk, mv, mo, a, t.lse,
+                                                          static_cast<__nv_bfloat16*>(t.out));
   return cudaGetLastError();
 }
 
 }  // namespace
 
+#ifdef FA_TEST_HOOKS
+cudaError_t test_hook_forward(int on) {
+  const int v = on ? 1 : 0;
+  return cudaMemcpyToSymbol(g_hook_skip_first_k, &v, sizeof(v));
+}
+#endif
+
+template <int BK>
+cudaError_t launch_forward_bk(const AttnArgs& a, const FwdTensors& t, cudaStream_t stream, bool* enc_failed) {
+  if (a.D == 64) {
+    if (a.score_op == FA_S_SOFTCAP) return launch_fwd_t<64, FA_S_SOFTCAP, BK>(a, t, stream, enc_failed);
+    if (a.score_op == FA_S_ALIBI) return launch_fwd_t<64, FA_S_ALIBI, BK>(a, t, stream, enc_failed);
+    return launch_fwd_t<64, FA_S_NONE, BK>(a, t, stream, enc_failed);
+  }
+  if (a.score_op == FA_S_SOFTCAP) return launch_fwd_t<128, FA_S_SOFTCAP, BK>(a, t, stream, enc_failed);
+  if (a.score_op == FA_S_ALIBI) return launch_fwd_t<128, FA_S_ALIBI, BK>(a, t, stream, enc_failed);
+  return launch_fwd_t<128, FA_S_NONE, BK>(a, t, stream, enc_failed);
+}
+
 cudaError_t launch_forward(const AttnArgs& a, const FwdTensors& t, cudaStream_t stream, bool* enc_failed) {
   *enc_failed = false;
-  if (a.D == 64) {
-    if (a.score_op == FA_S_SOFTCAP) return launch_fwd_t<64, FA_S_SOFTCAP>(a, t, stream, enc_failed);
-    if (a.score_op == FA_S_ALIBI) return launch_fwd_t<64, FA_S_ALIBI>(a, t, stream, enc_failed);
-    return launch_fwd_t<64, FA_S_NONE>(a, t, stream, enc_failed);
+  if (a.kv_block == 64) {
+    if (a.page_table != nullptr) return cudaErrorInvalidValue;  // paged caches use 128-row pages
+    return launch_forward_bk<64>(a, t, stream, enc_failed);
   }
-  if (a.score_op == FA_S_SOFTCAP) return launch_fwd_t<128, FA_S_SOFTCAP>(a, t, stream, enc_failed);
-  if (a.score_op == FA_S_ALIBI) return launch_fwd_t<128, FA_S_ALIBI>(a, t, stream, enc_failed);
-  return launch_fwd_t<128, FA_S_NONE>(a, t, stream, enc_failed);
+  return launch_forward_bk<128>(a, t, stream, enc_failed);
 }
 
 }  // namespace fa

@@ -32,6 +32,16 @@ struct PerDeviceOnce {
   }
 };
 
+// One class grid [planes][n_r][n_c] (planes = Bm * Hm) and the lists built
+// from it: per row (null row_num: none) and per column (null col_num: none),
+// with their work orders.
+struct ListJob {
+  uint8_t* cls;
+  int32_t planes, n_r, n_c;
+  int32_t *row_num, *row_idx, *row_full_num, *row_full_idx, *row_order;
+  int32_t *col_num, *col_idx, *col_full_num, *col_full_idx, *col_order;
+};
+
 struct BuildArgs {
   DevMask mask;
   int32_t Bm, Hm, block, nq, nkv;
@@ -49,6 +59,12 @@ struct BuildArgs {
   // tiles, [Bm][Hm][nq] and [Bm][Hm][nq][sel_stride]; they replace classification.
   const int32_t *sel_num, *sel_idx, *sel_full_num, *sel_full_idx;
   int32_t sel_stride;
+  // block < 128: the attention kernels' coarser grids, built from tile_class --
+  // the forward's rows of 128 query positions over key tiles of fwd_kv_block,
+  // the backward's columns of 128 key positions over query tiles of 128
+  // (fwd.cls null at block 128)
+  ListJob fwd, bwd;
+  int32_t fwd_kv_block;
 };
 
 // Launches a kernel on `stream` allowed to start while the kernel before it
@@ -94,6 +110,7 @@ struct AttnArgs {
   DevMask mask;
   const int4* row_segs;  // [Bm][2][seg_len]: see fa_block_mask
   int64_t seg_len;
+  int32_t kv_block;  // forward: key positions per listed key tile (128, or 64 below block 128)
 };
 
 struct FwdTensors {
@@ -108,6 +125,7 @@ struct BwdTensors {
   void *dq, *dk, *dv;
   float* dq_acc;  // fp32 [B, H, q_len, D]
   float* stats;   // fp32 [B, H, nq][2][128]: -LSE * log2(e) and -Delta per query tile
+  uint32_t* sched;  // the main kernel's item counter (zeroed by bwd_pre)
 };
 
 // Returns a CUDA error, or cudaErrorUnknown with *enc_failed set when a
@@ -125,6 +143,14 @@ cudaError_t launch_decode(const AttnArgs& a, const FwdTensors& t, void* workspac
 
 // Device address (current device) of the library-owned scratch of fa_backward_noalloc.
 cudaError_t noalloc_scratch(void** ptr);
+
+#ifdef FA_TEST_HOOKS
+// Test library only: make the producer of block 0 skip the load (and the
+// arrive) of the key tile of its first step, so that the MMA warp's bounded
+// wait for it runs out and the kernel takes its give-up path.
+cudaError_t test_hook_forward(int on);
+cudaError_t test_hook_backward(int on);
+#endif
 
 // Tensor-map encoding through the driver entry point (no libcuda link).
 bool encode_tmap_3d(CUtensorMap* map, CUtensorMapDataType dtype, int elem_bytes, const void* base, uint64_t d0,

@@ -10,7 +10,11 @@
 
 namespace fa {
 
+#ifdef FA_TEST_HOOKS
+constexpr uint64_t kWaitLimitNs = 50000000ull;  // test library: 50 ms, so a test that starves a wait ends quickly
+#else
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+#endif
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));

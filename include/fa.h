@@ -160,6 +160,25 @@ typedef struct {
  *   status             device status word (bit 0: a wait timed out; bit 1: a
  *                      device check failed, e.g. invalid caller tile lists).
  *
+ * With block < 128 (tutorial, sharp edge 4: a smaller BLOCK_SIZE captures more
+ * of a fine-grained mask's sparsity) the attention kernels still multiply
+ * 128-row query tiles; the builder also derives, from tile_class, the coarser
+ * tiles they walk (a coarse tile is EMPTY when all of its block tiles are, FULL
+ * when all are, PARTIAL otherwise -- exact):
+ *   fwd_*              the forward's: per query tile of 128 rows (fwd_nq rows)
+ *                      the key tiles of fwd_kv_block = 64 columns (fwd_nkv)
+ *                      that are not EMPTY -- counts [Bm][Hm][fwd_nq], indices
+ *                      [Bm][Hm][fwd_nq][fwd_nkv], PARTIAL and FULL as above --
+ *                      with fwd_row_order and the classes fwd_tile_class;
+ *   bwd_*              the backward's: per key tile of 128 columns (bwd_nkv)
+ *                      the query tiles of 128 rows (bwd_nq), [Bm][Hm][bwd_nkv]
+ *                      and [Bm][Hm][bwd_nkv][bwd_nq], with bwd_col_order and
+ *                      bwd_tile_class.
+ * At block == 128 these pointers are NULL and the kernels walk the lists above.
+ * from_blocks is 1 for a block mask of caller-chosen tiles
+ * (fa_block_mask_from_kv_blocks); the attention kernels take those at block
+ * 128 only.
+ *
  * The union kv_num_blocks + full_kv_num_blocks is the count of "tiles that are
  * not fully masked" of the speedrun notes' tile-summary paragraph.  Bm is 1 or
  * B and Hm is 1 or H: a size of 1 is broadcast over that dimension (tutorial,
@@ -187,6 +206,20 @@ typedef struct {
   int32_t* row_segs;
   uint32_t* status;
   fa_mask_spec spec;
+  int32_t from_blocks;
+  int32_t fwd_kv_block, fwd_nq, fwd_nkv, bwd_nq, bwd_nkv;
+  int32_t* fwd_kv_num_blocks;
+  int32_t* fwd_kv_indices;
+  int32_t* fwd_full_kv_num_blocks;
+  int32_t* fwd_full_kv_indices;
+  int32_t* fwd_row_order;
+  uint8_t* fwd_tile_class;
+  int32_t* bwd_q_num_blocks;
+  int32_t* bwd_q_indices;
+  int32_t* bwd_full_q_num_blocks;
+  int32_t* bwd_full_q_indices;
+  int32_t* bwd_col_order;
+  uint8_t* bwd_tile_class;
 } fa_block_mask;
 
 /* Bytes of device memory a block mask of this shape needs.
@@ -201,7 +234,8 @@ fa_status fa_block_mask_bytes(int32_t Bm, int32_t Hm, int64_t q_len, int64_t kv_
  * buffer: device memory of at least fa_block_mask_bytes() bytes, 256-byte
  * aligned, owned by the caller and used until the block mask is dropped.
  * bm: host struct, filled with pointers into `buffer` and a copy of `spec`.
- * Queues 4-6 kernels on `stream`; clears the status word. */
+ * Queues 4-6 kernels on `stream` (4 more with block < 128, for the attention
+ * kernels' coarser tiles); clears the status word. */
 fa_status fa_create_block_mask(const fa_mask_spec* spec, int32_t Bm, int32_t Hm, int64_t q_len, int64_t kv_len,
                                int32_t block, void* buffer, size_t buffer_bytes, fa_block_mask* bm,
                                cudaStream_t stream);
@@ -241,8 +275,9 @@ fa_status fa_block_mask_from_kv_blocks(const int32_t* kv_num_blocks, const int32
  *   out_i = sum_{j visible} softmax_j(s_i) v_j,  LSE_i = ln sum_{j visible} exp(s_ij)
  * with s_ij = score_mod(scale * q_i . k_j).  A row with no visible key gets
  * out = 0 and LSE = -inf.  scale: > 0, or 0 for 1/sqrt(D).
- * D: 64 or 128.  bm: built with block = 128 for this q_len / kv_len, Bm in
- * {1, B}, Hm in {1, H}. */
+ * D: 64 or 128.  bm: built for this q_len / kv_len with any block (below 128
+ * the kernel walks 128 x 64 tiles, see fa_block_mask; caller-chosen tiles only
+ * at block 128, else FA_ERR_UNSUPPORTED), Bm in {1, B}, Hm in {1, H}. */
 fa_status fa_forward(const void* q, const void* k, const void* v, int32_t B, int32_t H, int64_t q_len,
                      int64_t kv_len, int32_t D, const fa_block_mask* bm, const fa_score_spec* score, float scale,
                      void* out, float* lse, cudaStream_t stream);
@@ -298,8 +333,9 @@ fa_status fa_forward_decode(const void* q, const void* k, const void* v, const i
                             size_t workspace_bytes, cudaStream_t stream);
 
 /* Device workspace fa_backward needs: an fp32 dq accumulator
- * (B*H*q_len*D floats) and, per 128-row query tile, the rows' LSE and
- * sum(dO * out) (B*H*ceil(q_len/128)*256 floats), each 256-byte aligned. */
+ * (B*H*q_len*D floats), per 128-row query tile the rows' LSE and
+ * sum(dO * out) (B*H*ceil(q_len/128)*256 floats), and a work counter (one
+ * uint32), each 256-byte aligned. */
 fa_status fa_backward_workspace_bytes(int32_t B, int32_t H, int64_t q_len, int32_t D, size_t* bytes);
 
 /* Backward: dq, dk, dv of L = sum(out * dO) (tutorial, Pattern 3: the

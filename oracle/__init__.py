@@ -359,13 +359,18 @@ def np_select(M: np.ndarray, selection: np.ndarray, block: int) -> np.ndarray:
     return (E == 2) | ((E == 1) & M)
 
 
-def np_classify(M: np.ndarray, block: int) -> np.ndarray:
+def np_classify(M: np.ndarray, block: int, block_kv: Optional[int] = None) -> np.ndarray:
+    """Tile classes of an explicit mask: 0 EMPTY (no visible pair), 2 FULL (every
+    in-range pair visible), 1 PARTIAL.  Tiles are block x block, or block rows by
+    block_kv columns when given (the rectangular tiles attention kernels walk
+    over a finer block mask: tutorial, sharp edge 4)."""
+    bk = block if block_kv is None else block_kv
     q_len, kv_len = M.shape
-    nq, nkv = -(-q_len // block), -(-kv_len // block)
+    nq, nkv = -(-q_len // block), -(-kv_len // bk)
     cls = np.zeros((nq, nkv), dtype=np.int8)
     for I in range(nq):
         for J in range(nkv):
-            t = M[I * block:(I + 1) * block, J * block:(J + 1) * block]
+            t = M[I * block:(I + 1) * block, J * bk:(J + 1) * bk]
             cls[I, J] = 0 if not t.any() else (2 if t.all() else 1)
     return cls
 

@@ -56,6 +56,10 @@ def test_block_mask_bytes_layout(Bm, Hm, q, kv, block):
     rows, cols, tiles = Bm * Hm * nq, Bm * Hm * nkv, Bm * Hm * nq * nkv
     sizes = [rows * 4, tiles * 4, rows * 4, tiles * 4, cols * 4, tiles * 4, cols * 4, tiles * 4, rows * 4, cols * 4,
              tiles, Bm * 2 * max(nq, nkv) * 4 * 4, Bm * max(q, kv) * 8 + Bm * 4, Bm * 2 * max(q, kv) * 16, 4]
+    if block < 128:  # the attention kernels' coarser tiles: 128 x 64 rows (forward), 128 x 128 columns (backward)
+        P, fnq, fnkv, bnkv = Bm * Hm, -(-q // 128), -(-kv // 64), -(-kv // 128)
+        sizes += [P * fnq * 4, P * fnq * fnkv * 4, P * fnq * 4, P * fnq * fnkv * 4, P * fnq * 4, P * fnq * fnkv,
+                  P * bnkv * 4, P * bnkv * fnq * 4, P * bnkv * 4, P * bnkv * fnq * 4, P * bnkv * 4, P * fnq * bnkv]
     assert fa.fa_block_mask_bytes(Bm, Hm, q, kv, block) == sum(_align(s) for s in sizes)
 
 
@@ -165,7 +169,11 @@ def test_forward_rejects():
     assert _fwd(lse=FAKE + 2) == ALIGN
     assert _fwd(D=96) == UNSUPPORTED
     assert _fwd(D=256) == UNSUPPORTED
-    assert _fwd(bm=_bm(block=64)) == UNSUPPORTED
+    assert _fwd(bm=_bm(block=64)) == INVALID          # block 64 without the builder's coarser lists
+    coarse = _bm(block=64)
+    coarse.fwd_kv_block, coarse.fwd_kv_num_blocks, coarse.fwd_row_order = 64, FAKE, FAKE
+    coarse.from_blocks = 1
+    assert _fwd(bm=coarse) == UNSUPPORTED             # caller-chosen tiles below block 128
     assert _fwd(S=2048) == SHAPE                      # block mask built for another length
     assert _fwd(B_=2, bm=_bm(Bm=3)) == SHAPE         # Bm must be 1 or B
     assert _fwd(H=4, bm=_bm(Hm=2)) == SHAPE          # Hm must be 1 or H
@@ -184,7 +192,8 @@ def test_forward_rejects():
 
 
 def test_backward_workspace_and_rejects():
-    assert fa.fa_backward_workspace_bytes(2, 3, 1000, 128) == _align(2 * 3 * 1000 * 128 * 4) + _align(2 * 3 * 8 * 256 * 4)
+    assert fa.fa_backward_workspace_bytes(2, 3, 1000, 128) == (_align(2 * 3 * 1000 * 128 * 4) + _align(2 * 3 * 8 * 256 * 4)
+                                                               + _align(4))
     n = ctypes.c_size_t()
     assert B._lib.fa_backward_workspace_bytes(1, 1, 100, 80, ctypes.byref(n)) == UNSUPPORTED
     bm = _bm()
@@ -266,3 +275,31 @@ def test_status_calls_reject_null():
     assert B._lib.fa_get_status(None, 0, None) == INVALID
     counts = (ctypes.c_int64 * 3)()
     assert B._lib.fa_block_mask_summary(None, ctypes.byref(counts), None) == INVALID
+
+
+@pytest.mark.parametrize("ctype, cname", [(B.BlockMaskStruct, "fa_block_mask"), (B.MaskSpec, "fa_mask_spec"),
+                                          (B.ScoreSpec, "fa_score_spec")])
+def test_binding_structs_match_the_header(ctype, cname, tmp_path):
+    """The ctypes mirrors of the C structs have the header's size and field offsets
+    (a C program compiled against fa.h prints them)."""
+    import shutil
+    import subprocess
+
+    cc = shutil.which("gcc") or shutil.which("cc")
+    cuda_inc = next((d for d in ("/usr/local/cuda/include",) if os.path.exists(os.path.join(d, "cuda_runtime_api.h"))),
+                    None)
+    if cc is None or cuda_inc is None:
+        pytest.skip("needs a C compiler and the CUDA headers")
+    fields = [f[0] for f in ctype._fields_]
+    lines = [f'printf("{f} %zu\\n", offsetof({cname}, {f}));' for f in fields]
+    src = tmp_path / "layout.c"
+    src.write_text("#include <stdio.h>\n#include <stddef.h>\n#include \"fa.h\"\nint main(void) {\n"
+                   f'printf("sizeof %zu\\n", sizeof({cname}));\n' + "\n".join(lines) + "\nreturn 0;\n}\n")
+    exe = tmp_path / "layout"
+    subprocess.run([cc, "-std=c11", "-I", os.path.join(ROOT, "include"), "-I", cuda_inc, str(src), "-o", str(exe)],
+                   check=True, capture_output=True)
+    got = dict(line.split() for line in subprocess.run([str(exe)], check=True, capture_output=True,
+                                                         text=True).stdout.splitlines())
+    assert int(got["sizeof"]) == ctypes.sizeof(ctype)
+    for f in fields:
+        assert int(got[f]) == getattr(ctype, f).offset, f

@@ -153,6 +153,21 @@ def test_tile_lists_shape_and_order():
     assert L["full_q_num_blocks"].sum() == L["full_kv_num_blocks"].sum()
 
 
+def test_rectangular_tiles_causal_closed_form():
+    """Causal over 128-row by 64-column tiles: query-tile row I has FULL key tiles
+    J < 2I and PARTIAL J = 2I, 2I + 1 (the diagonal 128-block split in two), and
+    nothing after; with square tiles the classes are the C classifier's."""
+    S = 1024
+    M = oracle.np_mask(CAUSAL, S, S)
+    cls = oracle.np_classify(M, 128, 64)
+    n = S // 128
+    assert cls.shape == (n, 2 * n)
+    for I in range(n):
+        assert (cls[I, :2 * I] == 2).all() and (cls[I, 2 * I:2 * I + 2] == 1).all() and not cls[I, 2 * I + 2:].any()
+    for b in (32, 64, 128):
+        np.testing.assert_array_equal(oracle.np_classify(M, b, b), oracle.classify_tiles(oracle.Program(CAUSAL), S, S, b))
+
+
 def test_column_lists_causal_closed_form():
     """Causal key-tile column J: PARTIAL only on the diagonal (row J), FULL on rows J+1 .. n-1
     (the transpose of the row rule: row I sees J < I whole and J = I in part)."""
