@@ -229,6 +229,58 @@ def decode_point(fa, dev, hbm_gbs, B=1, H=16, kv_len=65536, D=128, reps=20):
             "GB_s": round(gbs, 1), "frac_of_hbm": round(gbs / hbm_gbs, 3)}
 
 
+def small_block_point(fa, dev, peak, S=32768, H=16, D=128, reps=10):
+    """A fine-grained mask -- causal & same document, documents of geometric
+    mean length 40 -- with block masks of 128 and of 64 (tutorial, sharp edge
+    4): forward and backward times (median of `reps`, L2 flushed) and the tiles
+    each walks.  At block 64 the forward walks 128 x 64 tiles (FLOPs
+    4 * 128 * 64 * D each), the backward the same 128 x 128 tiles as at 128."""
+    import torch
+
+    q, k, v, do = (t.to(dev) for t in make_qkv(1, H, S, D, 4040))
+    docs = torch.as_tensor(make_doc_ids(("geometric", 40.0), S, 4040), dtype=torch.int32, device=dev)
+    spec = fa.make_mask_spec([("causal",), ("same_doc", docs), ("and",)], device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    out = {"shape": f"B1 H{H} S{S} D{D}, causal & same document, geometric(40) documents"}
+    for block in (128, 64):
+        bm = fa.fa_create_block_mask(spec, 1, 1, S, S, block)
+        o, lse = fa.fa_forward(q, k, v, bm)
+        fa.fa_backward(q, k, v, o, lse, do, bm)
+        torch.cuda.synchronize()
+        assert fa.fa_get_status(bm) == 0
+        times = {"fwd": [], "bwd": []}
+        for _ in range(reps):
+            for what in ("fwd", "bwd"):
+                flush.zero_()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                if what == "fwd":
+                    fa.fa_forward(q, k, v, bm, out=o, lse=lse)
+                else:
+                    fa.fa_backward(q, k, v, o, lse, do, bm)
+                e1.record()
+                torch.cuda.synchronize()
+                times[what].append(e0.elapsed_time(e1))
+        fms, bms = (sorted(times[x])[reps // 2] for x in ("fwd", "bwd"))
+        if block == 128:
+            L = bm.lists()
+            ft = int((L["kv_num_blocks"].long() + L["full_kv_num_blocks"].long()).sum()) * H
+            bt, fkv = ft, 128
+        else:
+            L = bm.kernel_lists()
+            ft = int((L["fwd_kv_num_blocks"].long() + L["fwd_full_kv_num_blocks"].long()).sum()) * H
+            bt = int((L["bwd_q_num_blocks"].long() + L["bwd_full_q_num_blocks"].long()).sum()) * H
+            fkv = 64
+        fflops, bflops = ft * 4.0 * 128 * fkv * D, 2.5 * bt * 4.0 * 128 * 128 * D
+        out[f"block{block}"] = {"fwd_ms": round(fms, 4), "bwd_ms": round(bms, 4),
+                                "fwd_tiles": f"{ft} of 128 x {fkv}", "bwd_tiles": f"{bt} of 128 x 128",
+                                "fwd_tflops": round(fflops / (fms * 1e-3) / 1e12, 2),
+                                "bwd_tflops": round(bflops / (bms * 1e-3) / 1e12, 2),
+                                "fwd_frac": round(fflops / (fms * 1e-3) / 1e12 / peak, 4)}
+    out["fwd_time_ratio_64_over_128"] = round(out["block64"]["fwd_ms"] / out["block128"]["fwd_ms"], 3)
+    return out
+
+
 def visible_tiles(fa, bm, B, H):
     """Sum over (b, h) of non-empty tiles, from the block mask's counts."""
     L = bm.lists()
@@ -496,6 +548,7 @@ def run_gpu(args):
     if rank == 0 and not args.profile:
         res["builder_scaled"] = builder_scaled(fa, w, prob_window(w, windows), dev)
         res["decode"] = decode_point(fa, dev, float(peaks.get("hbm_gbs", PEAKS_FALLBACK["hbm_gbs"])))
+        res["small_block"] = small_block_point(fa, dev, peak)
         res["per_config"] = {str(n): per_config(fa, WORKLOADS[n], dev, max(3, args.steps // 2), 3, peak)
                              for n in sorted(WORKLOADS) if n != args.workload}
     if rank == 0 and not args.no_cpu_baseline and not args.profile:

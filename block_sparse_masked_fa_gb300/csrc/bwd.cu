@@ -80,11 +80,22 @@ struct BwdCfg {
   static constexpr int DQ_THREADS = 128;
   static constexpr int PRODUCER_WARP = 12, MMA_WARP = 13;  // (warps 14, 15 idle)
   static constexpr int THREADS = 512;
+  // registers per thread of each warpgroup after setmaxnreg (launched at 128):
+  // key-row warps, dQ warps, producer / MMA warpgroup
+  static constexpr uint32_t KEY_REGS = (D == 128) ? 160 : 168, DQ_REGS = 104, PM_REGS = (D == 128) ? 88 : 72;
+  static_assert(2 * KEY_REGS + DQ_REGS + PM_REGS == 4 * 128, "the split must add up to the launch's registers");
 };
 
 struct TileStats {  // per query tile, from the workspace
   float nlse[128];    // -LSE * log2(e) of the tile's query rows
   float ndelta[128];  // -Delta of the tile's query rows
+};
+
+// One work item: the key tile J of head (b, h), with the query tiles of its
+// column lists (FULL first, then PARTIAL).
+struct BwdItem {
+  int J, bh, bm, h, n_full, n;
+  int64_t list;  // offset of the column's lists
 };
 
 struct BwdCtl {
@@ -97,6 +108,7 @@ struct BwdCtl {
   // this CTA's items in the order the producer claimed them (see sched_get)
   uint64_t sched_full[4], sched_empty[4];
   int sched_k[4];
+  BwdItem sched_it[4];  // and their descriptors, so that no role reloads them from global memory
   uint32_t tmem;
   int abort;
   int32_t arg[2][FA_MAX_MASK_NODES];  // mask program arguments of the current item, per key-row half
@@ -146,12 +158,6 @@ __device__ __forceinline__ void store_row32(uint8_t* tile, int r, int c, const u
   }
 }
 
-// One work item: the key tile J of head (b, h), with the query tiles of its
-// column lists (FULL first, then PARTIAL).
-struct BwdItem {
-  int J, bh, bm, h, n_full, n;
-  int64_t list;  // offset of the column's lists
-};
 
 __device__ __forceinline__ BwdItem bwd_item(const AttnArgs& p, int k) {
   const int rep = (p.B / p.Bm) * (p.H / p.Hm);
@@ -184,11 +190,11 @@ __device__ __forceinline__ int tile_of(const AttnArgs& p, const BwdItem& it, int
 constexpr int kSchedSlots = 4;
 constexpr int kSchedConsumers = 1 + 4 + 8;  // MMA thread, dQ warps, key-row warps (one arrival per warp)
 
-__device__ __forceinline__ int claim_live(const AttnArgs& p, uint32_t* sched, int items) {
+__device__ __forceinline__ int claim_live(const AttnArgs& p, uint32_t* sched, int items, BwdItem& it) {
   while (true) {
     const int k = (int)atomicAdd(sched, 1u);
     if (k >= items) return items;
-    const BwdItem it = bwd_item(p, k);
+    it = bwd_item(p, k);
     if (it.n > 0) return k;
   }
 }
@@ -262,14 +268,15 @@ __global__ void __launch_bounds__(512, 1)
   // Item u of this CTA's sequence (u = 0, 1, ...; `items` ends it), as the
   // producer published it; false when the wait gave up.  Every consumer role
   // releases slot u once it is done with item u.
-  auto sched_get = [&](int u, int& k) -> bool {
+  auto sched_get = [&](int u, int& k, BwdItem& it) -> bool {
     const int sl = u % kSchedSlots;
     if (!mbar_wait(smem_u32(&ctl->sched_full[sl]), (u / kSchedSlots) & 1, &ctl->abort)) return false;
     k = *reinterpret_cast<volatile int*>(&ctl->sched_k[sl]);
+    it = ctl->sched_it[sl];  // read after the wait (a memory clobber): the producer's values
     return true;
   };
-  auto sched_get_warp = [&](int u, int& k) -> bool {
-    const bool r = __all_sync(0xffffffffu, sched_get(u, k));
+  auto sched_get_warp = [&](int u, int& k, BwdItem& it) -> bool {
+    const bool r = __all_sync(0xffffffffu, sched_get(u, k, it));
     return r;
   };
   auto sched_release = [&](int u) { mbar_arrive(smem_u32(&ctl->sched_empty[u % kSchedSlots])); };
@@ -292,10 +299,12 @@ __global__ void __launch_bounds__(512, 1)
   // numbered (u) for the ring, the K / V buffers and the dK / dV accumulators.
   //
   // Register budgets per warpgroup, set at the top of each warpgroup's branch
-  // (launched with 128 per thread): key-row warps 176, dQ warps 112, producer /
-  // MMA warpgroup 48 -- 256 x 176 + 128 x 112 + 128 x 48 = 512 x 128.
+  // (launched with 128 per thread; BwdCfg): key-row warps 160 (D = 128) or 168,
+  // dQ warps 104, producer / MMA warpgroup 88 or 72 (the item claims and the item
+  // ring need more than the 48 it had before) -- 256 x 160 + 128 x 104 + 128 x 88
+  // = 256 x 168 + 128 x 104 + 128 x 72 = 512 x 128.
   if (warp >= C::PRODUCER_WARP) {
-    setmaxnreg_dec<48>();
+    setmaxnreg_dec<C::PM_REGS>();
     if (warp == C::PRODUCER_WARP) {
       // ------------------------------------------------------------ producer
       // Per item: V once dP of the last item's last step is done with it, then
@@ -312,7 +321,8 @@ __global__ void __launch_bounds__(512, 1)
       // claims the next live item (lane 0) and publishes it as item uu
       auto claim_publish = [&](int uu) -> int {
         int kc = items;
-        if (lane == 0 && !skip) kc = claim_live(p, sched, items);
+        BwdItem it{};
+        if (lane == 0 && !skip) kc = claim_live(p, sched, items, it);
         kc = __shfl_sync(0xffffffffu, kc, 0);
         const int sl = uu % kSchedSlots;
         if (uu >= kSchedSlots &&
@@ -320,19 +330,25 @@ __global__ void __launch_bounds__(512, 1)
           return -1;
         if (lane == 0) {
           ctl->sched_k[sl] = kc;
+          ctl->sched_it[sl] = it;
           mbar_arrive(smem_u32(&ctl->sched_full[sl]));
         }
         return kc;
       };
+      // Items are claimed two ahead: item u + 2 once item u's first loads are
+      // issued, so that the claim's latency (an atomic, then the item's counts)
+      // stays off the path to those loads; the consumers look one item ahead.
       int k = claim_publish(0);
+      int kn = items;
       ok = k >= 0;
+      if (ok && k < items) {
+        kn = claim_publish(1);
+        ok = kn >= 0;
+      }
       while (ok && k < items) {
-        const BwdItem cur = bwd_item(p, k);
-        const int kn = claim_publish(u + 1);  // the next item, for the consumers' look-ahead
-        if (kn < 0) {
-          ok = false;
-          break;
-        }
+        __syncwarp();
+        const BwdItem cur = ctl->sched_it[u % kSchedSlots];  // as lane 0 published it
+        int kn2 = items;  // item u + 2
         if (u > 0 && !warp_wait(b_ve, (u - 1) & 1, &ctl->abort)) {
           ok = false;
           break;
@@ -385,9 +401,17 @@ __global__ void __launch_bounds__(512, 1)
                 tma_load_3d(smem_u32(sK + c * 16384), &tm_k, b_kf, c * 64, cur.J * 128, cur.bh);
             }
             k_issued = u + 1;
+            if (kn < items) {  // item u + 2 (after the end marker nothing more is read)
+              kn2 = claim_publish(u + 2);
+              if (kn2 < 0) {
+                ok = false;
+                break;
+              }
+            }
           }
         }
         k = kn;
+        kn = kn2;
         ++u;
       }
       if (!ok && lane == 0) fail(p, ctl);
@@ -447,16 +471,16 @@ __global__ void __launch_bounds__(512, 1)
           return true;
         };
         int g = 0, u = 0, k = items;
-        bool ok = sched_get(0, k);
+        BwdItem cur, nxt;
+        bool ok = sched_get(0, k, cur);
         while (ok && k < items) {
-          const BwdItem cur = bwd_item(p, k);
           const int n = cur.n;
           if (!issue_s(g, 0, u) || !issue_dp(g, 0, n, u)) {
             ok = false;
             break;
           }
           int kn = items;
-          if (!sched_get(u + 1, kn)) {
+          if (!sched_get(u + 1, kn, nxt)) {
             ok = false;
             break;
           }
@@ -526,6 +550,7 @@ __global__ void __launch_bounds__(512, 1)
           mma_commit(b_acc);  // dV, dK of the item complete
           sched_release(u);
           k = kn;
+          cur = nxt;
           ++u;
         }
         if (!ok) fail(p, ctl);
@@ -536,7 +561,7 @@ __global__ void __launch_bounds__(512, 1)
     __syncwarp();
     teardown();
   } else if (warp >= C::DQ_WARP0) {
-    setmaxnreg_dec<112>();
+    setmaxnreg_dec<C::DQ_REGS>();
     // ------------------------------------------------------------ dQ warps
     // Warp w drains dQ rows [32 (w % 4), +32) (its TMEM lanes) of each step:
     // 32 columns at a time into one of its two 128-byte-swizzled 32 x 32 fp32
@@ -549,9 +574,9 @@ __global__ void __launch_bounds__(512, 1)
     const uint32_t t_lane = tmem + ((uint32_t)rw << 16);
     uint8_t* box0 = sSTG + (warp % 4) * (2 * C::BOX_BYTES);
     int round = 0, u = 0, g = 0, k = items;
-    bool ok = sched_get_warp(0, k);
+    BwdItem cur;
+    bool ok = sched_get_warp(0, k, cur);
     while (ok && k < items) {
-      const BwdItem cur = bwd_item(p, k);
       for (int s = 0; s < cur.n; ++s, ++g) {
         const int I = tile_of(p, cur, s);
         const int bq = g % C::NDQ;
@@ -627,14 +652,14 @@ __global__ void __launch_bounds__(512, 1)
       __syncwarp();
       if (lane == 0) sched_release(u);
       ++u;
-      ok = sched_get_warp(u, k);
+      ok = sched_get_warp(u, k, cur);
     }
     if (!ok) fail(p, ctl);
     if (lane == 0) bulk_wait0();  // every reduce and store of this warp has completed
     __syncwarp();
     teardown();
   } else {
-    setmaxnreg_inc<176>();
+    setmaxnreg_inc<C::KEY_REGS>();
     // ------------------------------------------------------------ key-row warps
     // Thread (warp w, lane) owns TMEM lane r = 32 (w % 4) + lane = key row r, of
     // which it handles query columns [64 half, 64 half + 64) (half = w / 4).
@@ -657,25 +682,24 @@ __global__ void __launch_bounds__(512, 1)
     auto stat_of = [&](int bh, int I) { return __ldg(stats_g + ((int64_t)bh * p.nq + I) * 256 + st_idx); };
     int32_t* arg_s = ctl->arg[half];
     int k = items, I_next = 0;  // the query tile of the next step
-    bool ok = sched_get_warp(0, k), lok = true;
+    BwdItem cur, nxt;
+    bool ok = sched_get_warp(0, k, cur), lok = true;
     if (ok && k < items) {
-      const BwdItem it0 = bwd_item(p, k);
+      const BwdItem& it0 = cur;
       I_next = tile_of(p, it0, 0);
       reinterpret_cast<float*>(&ctl->stats)[st_idx] = stat_of(it0.bh, I_next);
       if (r < p.mask.n) arg_s[r] = node_arg(p.mask, r, it0.bm);
     }
     int g = 0, u = 0;
     while (ok && k < items) {
-      const BwdItem cur = bwd_item(p, k);
       // of the next item only what the last step hands over: its first query
       // tile (for the stats), head and mask batch
       int kn = items, nxt_i0 = 0, nxt_bh = 0, nxt_bm = 0;
-      if (!sched_get_warp(u + 1, kn)) {
+      if (!sched_get_warp(u + 1, kn, nxt)) {
         ok = false;
         break;
       }
       if (kn < items) {
-        const BwdItem nxt = bwd_item(p, kn);
         nxt_i0 = tile_of(p, nxt, 0);
         nxt_bh = nxt.bh;
         nxt_bm = nxt.bm;
@@ -846,6 +870,7 @@ __global__ void __launch_bounds__(512, 1)
       __syncwarp();
       if (lane == 0) sched_release(u);
       k = kn;
+      cur = nxt;
       ++u;
     }
     if (ok && !lok) ok = false;
