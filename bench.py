@@ -73,10 +73,11 @@ def recorded_traffic(kernel: str, workload: str):
             rec = json.load(f)
     except (OSError, ValueError):
         return None
-    entry = rec.get("kernels", {}).get(kernel)
-    if not entry or entry.get("workload") != workload or entry.get("source_sha256") != source_digest(kernel):
-        return None
-    return entry.get("dram_bytes_per_launch")
+    for entry in rec.get("records", []):
+        if (entry.get("kernel") == kernel and entry.get("workload") == workload
+                and entry.get("source_sha256") == source_digest(kernel)):
+            return entry.get("dram_bytes_per_launch")
+    return None
 
 
 def load_peaks():
@@ -527,7 +528,9 @@ def run_gpu(args):
         "roofline": {"kernel": dominant, "bound": "tensor", "achieved": round(achieved, 2), "peak": peak,
                      "peak_source": f"bf16_tflops ({peak_src}, burst)", "unit": "TFLOP/s",
                      "frac": round(achieved / peak, 4),
-                     "traffic": recorded_traffic("bwd_kernel" if dominant == "bwd" else "fwd_kernel", w.name)},
+                     "traffic": recorded_traffic("bwd_kernel" if dominant == "bwd" else "fwd_kernel", w.name),
+                     "traffic_note": "DRAM bytes of one launch at W 1024 (ncu on 4 heads, scaled to 16); "
+                                     "null when the kernel's sources changed since the capture"},
         "gpu_launches": launches_per_sub_step(w) * n_sub * args.steps,
         "clocks": clk,
     }
