@@ -487,22 +487,28 @@ def fa_forward_decode_workspace_bytes(B: int, H: int, q_len: int, kv_len: int, D
 
 
 def fa_forward_decode(q, k, v, block_mask: BlockMask, score=None, scale: float = 0.0, page_table=None, out=None,
-                      lse=None, workspace=None, stream=None):
-    """Short-query forward (q_len <= 16): k, v [B, H, kv_len, D]; or, with an
-    int32 page_table [B, nkv], pools [H, n_pages * 128, D].  out, lse as fa_forward."""
+                      lse=None, workspace=None, stream=None, kv_len: Optional[int] = None):
+    """Short-query forward (q_len <= 16) over the keys [0, kv_len): k, v
+    [B, H, C, D] with C the block mask's kv_len; or, with an int32 page_table
+    [B, nkv], pools [H, n_pages * 128, D].  kv_len defaults to C; a smaller one
+    runs a block mask built for a bucketed cache length C on the current cache.
+    out, lse as fa_forward."""
     _check_shapes(q, like_q=(("out", out),), lse=lse)
     B, H, q_len, D = q.shape
-    kv_len = block_mask.struct.kv_len
+    cap = block_mask.struct.kv_len
+    kv_len = cap if kv_len is None else int(kv_len)
+    if not 1 <= kv_len <= cap:
+        raise ValueError(f"kv_len {kv_len} must be in [1, {cap}] (the block mask's key length)")
     if q_len != block_mask.struct.q_len:
         raise ValueError(f"q has {q_len} rows; the block mask was built for q_len {block_mask.struct.q_len}")
     n_pages = 0
-    if page_table is None and (tuple(k.shape) != (B, H, kv_len, D) or tuple(v.shape) != (B, H, kv_len, D)):
-        raise ValueError(f"k and v must be [{B}, {H}, {kv_len}, {D}] (kv_len of the block mask)")
+    if page_table is None and (tuple(k.shape) != (B, H, cap, D) or tuple(v.shape) != (B, H, cap, D)):
+        raise ValueError(f"k and v must be [{B}, {H}, {cap}, {D}] (kv_len of the block mask)")
     if page_table is not None and v.shape != k.shape:
         raise ValueError("paged k and v pools must have the same shape")
     if page_table is not None:
         if page_table.dtype != torch.int32 or not page_table.is_cuda or not page_table.is_contiguous() \
-                or tuple(page_table.shape) != (B, -(-kv_len // 128)):
+                or tuple(page_table.shape) != (B, -(-cap // 128)):
             raise ValueError("page_table must be a contiguous int32 CUDA tensor [B, nkv]")
         if k.dim() != 3 or k.shape[1] % 128 != 0:
             raise ValueError("paged k / v must be [H, n_pages * 128, D]")

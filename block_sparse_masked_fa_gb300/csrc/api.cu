@@ -145,7 +145,7 @@ void load_encode() {
 
 fa_status cuda_status(cudaError_t e) { return e == cudaSuccess ? FA_OK : FA_ERR_CUDA; }
 
-enum AttnKind { kForward, kForwardPagedOrDecode, kBackward };
+enum AttnKind { kForward, kForwardPagedOrDecode, kDecode, kBackward };
 
 // Shared shape checks of fa_forward / fa_backward.
 fa_status check_attn(int32_t B, int32_t H, int64_t q_len, int64_t kv_len, int32_t D, const fa_block_mask* bm,
@@ -155,13 +155,14 @@ fa_status check_attn(int32_t B, int32_t H, int64_t q_len, int64_t kv_len, int32_
   if (B < 1 || H < 1 || q_len < 1 || kv_len < 1) return FA_ERR_SHAPE;
   if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
   if (bm->block != 128) {  // the kernels walk the coarser lists the builder derived
-    if (kind == kForwardPagedOrDecode || bm->from_blocks) return FA_ERR_UNSUPPORTED;
+    if (kind == kForwardPagedOrDecode || kind == kDecode || bm->from_blocks) return FA_ERR_UNSUPPORTED;
     if (bm->block > 128 || bm->fwd_kv_block != kFwdSmallKvBlock) return FA_ERR_INVALID_ARG;
     if (backward ? (bm->bwd_q_num_blocks == nullptr || bm->bwd_col_order == nullptr)
                  : (bm->fwd_kv_num_blocks == nullptr || bm->fwd_row_order == nullptr))
       return FA_ERR_INVALID_ARG;
   }
-  if (bm->q_len != q_len || bm->kv_len != kv_len) return FA_ERR_SHAPE;
+  // the short-query forward may run on a block mask built for a longer (bucketed) cache
+  if (bm->q_len != q_len || (kind == kDecode ? bm->kv_len < kv_len : bm->kv_len != kv_len)) return FA_ERR_SHAPE;
   if (!(bm->Bm == 1 || bm->Bm == B) || !(bm->Hm == 1 || bm->Hm == H)) return FA_ERR_SHAPE;
   if ((int64_t)B * H * ((q_len + 127) / 128) > (int64_t)INT32_MAX) return FA_ERR_SHAPE;
   if ((int64_t)B * H * ((kv_len + 127) / 128) > (int64_t)INT32_MAX) return FA_ERR_SHAPE;
@@ -209,6 +210,7 @@ AttnArgs attn_args(int32_t B, int32_t H, int64_t q_len, int64_t kv_len, int32_t 
   a.status = bm->status;
   a.mask = dm;
   a.kv_block = 128;
+  a.kv_cap = (int32_t)kv_len;
   if (bm->block != 128 && !backward) {  // the forward's 128 x 64 tiles
     a.nq = bm->fwd_nq;
     a.nkv = bm->fwd_nkv;
@@ -517,7 +519,7 @@ fa_status fa_forward_decode(const void* q, const void* k, const void* v, const i
   }
   if (q_len < 1 || q_len > FA_DECODE_MAX_Q) return q_len < 1 ? FA_ERR_SHAPE : FA_ERR_UNSUPPORTED;
   if ((int64_t)B * H > kDecodeMaxHeads) return FA_ERR_UNSUPPORTED;
-  fa_status st = check_attn(B, H, q_len, kv_len, D, bm, score, &scale, kForwardPagedOrDecode);
+  fa_status st = check_attn(B, H, q_len, kv_len, D, bm, score, &scale, kDecode);
   if (st != FA_OK) return st;
   size_t need = 0;
   int splits = 0;
@@ -529,6 +531,7 @@ fa_status fa_forward_decode(const void* q, const void* k, const void* v, const i
   AttnArgs a = attn_args(B, H, q_len, kv_len, D, bm, score, scale, dm, false);
   a.page_table = page_table;
   a.n_pages = page_table != nullptr ? n_pages : 0;
+  a.kv_cap = (int32_t)bm->kv_len;  // k / v rows per (b, h): the block mask's (bucketed) length
   FwdTensors t{q, k, v, out, lse};
   bool enc_failed = false;
   const cudaError_t e = launch_decode(a, t, workspace, splits, stream, &enc_failed);

@@ -100,12 +100,16 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   const int bm = (p.Bm == 1) ? 0 : b, hm = (p.Hm == 1) ? 0 : h;
   const int ql = p.q_len;
   const int64_t row = ((int64_t)bm * p.Hm + hm) * p.nq;  // the (only) query-tile row
-  const int n_full = __ldg(p.full_num + row);
-  const int n = n_full + __ldg(p.kv_num + row);
-  const int p0 = (int)((int64_t)n * split / splits), p1 = (int)((int64_t)n * (split + 1) / splits);
-  auto tile_at = [&](int pos) {
-    return pos < n_full ? __ldg(p.full_idx + row * p.nkv + pos) : __ldg(p.kv_idx + row * p.nkv + pos - n_full);
-  };
+  __shared__ int s_count[2];
+  if (t == 0) {
+    // A block mask built for a longer, bucketed cache lists key tiles past the
+    // current kv_len too; the lists are ascending, so those are their tails.
+    int nf = __ldg(p.full_num + row), np = __ldg(p.kv_num + row);
+    while (nf > 0 && (int64_t)__ldg(p.full_idx + row * p.nkv + nf - 1) * 128 >= p.kv_len) --nf;
+    while (np > 0 && (int64_t)__ldg(p.kv_idx + row * p.nkv + np - 1) * 128 >= p.kv_len) --np;
+    s_count[0] = nf;
+    s_count[1] = nf + np;
+  }
 
   for (int e = t; e < ql * D; e += kDecThreads) sQ[e] = __bfloat162float(q[(int64_t)bh * ql * D + e]);
   if (t < p.mask.n) s_arg[t] = node_arg(p.mask, t, bm);
@@ -118,6 +122,11 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     fence_mbar_init();
   }
   __syncthreads();
+  const int n_full = s_count[0], n = s_count[1];
+  const int p0 = (int)((int64_t)n * split / splits), p1 = (int)((int64_t)n * (split + 1) / splits);
+  auto tile_at = [&](int pos) {
+    return pos < n_full ? __ldg(p.full_idx + row * p.nkv + pos) : __ldg(p.kv_idx + row * p.nkv + pos - n_full);
+  };
 
   bool ok = true;
   float m_run[QB], l_run[QB];
@@ -400,7 +409,8 @@ cudaError_t launch_decode_t(const AttnArgs& a, const FwdTensors& t, float* ws, i
                             bool* enc_failed) {
   const uint64_t bh = (uint64_t)a.B * a.H;
   const bool paged = a.page_table != nullptr;
-  const uint64_t kv_rows = paged ? (uint64_t)a.n_pages * 128 : (uint64_t)a.kv_len;
+  // rows of each (b, h) in the key / value tensors: the block mask's (bucketed) length
+  const uint64_t kv_rows = paged ? (uint64_t)a.n_pages * 128 : (uint64_t)a.kv_cap;
   const uint64_t kv_z = paged ? (uint64_t)a.H : bh;
   CUtensorMap mk, mv;
   if (!encode_tmap_3d(&mk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, t.k, D, kv_rows, kv_z, 64, 128,

@@ -111,6 +111,7 @@ struct AttnArgs {
   const int4* row_segs;  // [Bm][2][seg_len]: see fa_block_mask
   int64_t seg_len;
   int32_t kv_block;  // forward: key positions per listed key tile (128, or 64 below block 128)
+  int32_t kv_cap;    // short-query forward: rows per (b, h) of k / v (>= kv_len: a bucketed cache)
 };
 
 struct FwdTensors {

@@ -321,9 +321,17 @@ fa_status fa_forward_decode_workspace_bytes(int32_t B, int32_t H, int64_t q_len,
                                             size_t* bytes);
 
 /* The short-query forward: out and LSE exactly as fa_forward (page_table =
- * NULL, k / v [B][H][kv_len][D]) or fa_forward_paged (page_table != NULL,
- * k / v pools [H][n_pages * 128][D]) define them, for q_len <= FA_DECODE_MAX_Q
- * (bm built for this q_len, so nq = 1).  Keys past kv_len are never read.
+ * NULL) or fa_forward_paged (page_table != NULL, k / v pools
+ * [H][n_pages * 128][D]) define them, for q_len <= FA_DECODE_MAX_Q (bm built
+ * for this q_len, so nq = 1), over the keys [0, kv_len).  Keys past kv_len are
+ * never read.
+ * Bucketed caches (tutorial "Decoding and paged KV caches": keep the cache
+ * length bucketed, e.g. to multiples of 1024, and reuse the block mask): bm
+ * may be built for a longer key length C = bm->kv_len >= kv_len, once per
+ * bucket; key tiles it lists past kv_len are skipped, and the visible set is
+ * the mask's restricted to j < kv_len.  Without a page table k / v are
+ * [B][H][C][D] (rows past kv_len unused); with one, page_table is [B][bm->nkv]
+ * and only the entries of tiles below kv_len are read.
  * workspace: device memory of fa_forward_decode_workspace_bytes() bytes,
  * 16-byte aligned, caller-owned (FA_ERR_WORKSPACE when smaller).  Queues two
  * kernels on `stream`; errors as fa_forward / fa_forward_paged. */

@@ -145,3 +145,44 @@ def test_decode_empty_selection():
     torch.cuda.synchronize()
     assert fa.fa_get_status(bm) == 0
     assert torch.all(out == 0) and torch.all(torch.isneginf(lse))
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("paged", [False, True])
+def test_decode_bucketed_cache(D, paged):
+    """A block mask built once for a cache bucket of 4,096 keys (tutorial
+    "Decoding and paged KV caches": bucket the cache length), reused while the
+    cache grows: at each kv_len the result is the oracle's over the first
+    kv_len keys with the same program.  The cache tensors have the bucket's
+    rows; rows past kv_len hold NaN, and (paged) the table entries of tiles past
+    kv_len name pages outside the pool: neither may be read."""
+    B, H, q_len, cap = 2, 2, 2, 4096
+    nkv = cap // 128
+    docs = make_doc_ids(("geometric", 700.0), cap, 17, batch=B)
+    mask = P(("same_doc",), ("sink", 16), ("or",), ("window", 100000), ("and",))
+    q, k, v = make_qkv(B, H, q_len, D, 90 + D, with_dout=False, kv_len=cap)
+    bm = fa.fa_create_block_mask(device_nodes(mask, docs), B, 1, q_len, cap, 128)
+    for kv_len in (1, 129, 1000, 2500, 4095, 4096):
+        kd, vd = k.clone(), v.clone()
+        kd[:, :, kv_len:] = float("nan")
+        vd[:, :, kv_len:] = float("nan")
+        if paged:
+            n_pages = B * nkv
+            perm = np.random.default_rng(kv_len).permutation(n_pages)
+            table = torch.full((B, nkv), 10 ** 6, dtype=torch.int32)          # out of range past kv_len
+            kpool = torch.full((H, n_pages * 128, D), float("nan"), dtype=torch.bfloat16)
+            vpool = kpool.clone()
+            for b in range(B):
+                for J in range(-(-kv_len // 128)):
+                    pg = int(perm[b * nkv + J])
+                    table[b, J] = pg
+                    kpool[:, pg * 128:(pg + 1) * 128] = kd[b, :, J * 128:(J + 1) * 128]
+                    vpool[:, pg * 128:(pg + 1) * 128] = vd[b, :, J * 128:(J + 1) * 128]
+            out, lse = fa.fa_forward_decode(q.cuda(), kpool.cuda(), vpool.cuda(), bm, page_table=table.cuda(),
+                                            kv_len=kv_len)
+        else:
+            out, lse = fa.fa_forward_decode(q.cuda(), kd.cuda(), vd.cuda(), bm, kv_len=kv_len)
+        torch.cuda.synchronize()
+        assert fa.fa_get_status(bm) == 0
+        check_all(out, lse, q, k[:, :, :kv_len], v[:, :, :kv_len], lambda b: oracle.Program(mask, doc_row=docs[b]),
+                  ("none",), f"D{D} paged {paged} kv_len {kv_len}")
