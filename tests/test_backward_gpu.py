@@ -264,3 +264,32 @@ def test_alibi_slope_gradient(D):
     assert np.abs(ref).max() > 0
     check_grad(got, ref, f"dslope D{D}")
     np.testing.assert_allclose(dslope2.cpu().numpy(), got, rtol=1e-5, atol=1e-6 * np.abs(ref).max())
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("cap", [5.0, 30.0])
+def test_softcap_polynomial_and_exact_paths(D, cap):
+    """Soft-cap rows of both kinds: the kernels evaluate tanh by a polynomial
+    when every logit of a row (forward) or 32-column chunk (backward) has
+    |s / c| <= 0.5, else exactly; query rows scaled by 1 and by 10 give rows of
+    each kind in the same tiles.  Forward and gradients against the oracle,
+    every element."""
+    S, H = 640, 2
+    q, k, v, do = make_qkv(1, H, S, D, 3100 + D, kv_len=S)
+    rows = torch.arange(S)
+    q = (q.float() * torch.where((rows // 48) % 2 == 0, 1.0, 10.0)[None, None, :, None]).to(torch.bfloat16)
+    inp = {"q": q, "k": k, "v": v, "do": do, "docs": None}
+    mask = P(("causal",), ("window", 400), ("and",))
+    qd, kd, vd, dod = (t.cuda() for t in (q, k, v, do))
+    bm = fa.fa_create_block_mask(device_nodes(mask), 1, 1, S, S, 128)
+    out, lse = fa.fa_forward(qd, kd, vd, bm, score=("softcap", [cap]))
+    grads = fa.fa_backward(qd, kd, vd, out, lse, dod, bm, score=("softcap", [cap]))
+    torch.cuda.synchronize()
+    assert fa.fa_get_status(bm) == 0
+    prog = oracle.Program(mask)
+    for h in range(H):
+        ref_out, ref_lse = oracle.forward_head(head64(q, 0, h), head64(k, 0, h), head64(v, 0, h), prog,
+                                               ("softcap", cap), h, 1.0 / np.sqrt(D))
+        check_forward(out[0, h].float().cpu().numpy(), lse[0, h].cpu().numpy(), ref_out, ref_lse, f"cap {cap} h{h}")
+        ref = oracle_grads(inp, mask, 0, h, ("softcap", cap))
+        check_all([g[0, h].float().cpu().numpy() for g in grads], ref, f"cap {cap} D{D} h{h}")
