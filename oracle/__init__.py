@@ -49,7 +49,7 @@ def build(force: bool = False) -> str:
 class _Program(ctypes.Structure):
     _fields_ = [("n", ctypes.c_int32), ("op", ctypes.c_int32 * 16), ("arg", ctypes.c_int64 * 16),
                 ("doc", ctypes.POINTER(ctypes.c_int32)), ("sel", ctypes.POINTER(ctypes.c_int8)),
-                ("sel_block", ctypes.c_int64), ("sel_nkv", ctypes.c_int64)]
+                ("sel_block", ctypes.c_int64), ("sel_nkv", ctypes.c_int64), ("q_off", ctypes.c_int64)]
 
 
 def _load():
@@ -85,11 +85,13 @@ class Program:
     ``selection`` (optional, int8 [nq, nkv], see ``selection_from_lists``)
     restricts it to caller-chosen tiles of ``block`` x ``block``: a pair is
     visible when its tile is selected as full (2), or selected as partial (1)
-    and the program holds there.
+    and the program holds there.  ``q_offset``: query row i sits at position
+    i + q_offset of the sequence (CAUSAL, WINDOW, SAME_DOC and ALiBi see that
+    position), e.g. new tokens decoded at the end of a cache.
     """
 
     def __init__(self, mask, doc_row: Optional[np.ndarray] = None, prefix_len: Optional[int] = None,
-                 selection: Optional[np.ndarray] = None, block: int = 128):
+                 selection: Optional[np.ndarray] = None, block: int = 128, q_offset: int = 0):
         nodes = mask.nodes if hasattr(mask, "nodes") else tuple(mask)
         if len(nodes) > 16:
             raise ValueError("at most 16 nodes")
@@ -100,6 +102,7 @@ class Program:
             self._doc = np.ascontiguousarray(doc_row, dtype=np.int32)
         s = _Program()
         s.n = len(nodes)
+        s.q_off = int(q_offset)
         for t, node in enumerate(nodes):
             s.op[t] = _OP[node[0]]
             if node[0] in ("window", "sink"):
@@ -321,9 +324,10 @@ def head_score(score_kind: tuple, slopes=None, softcap=None) -> tuple:
 # numpy twin (tiny sizes only): dense explicit mask, dense softmax.
 # ---------------------------------------------------------------------------
 
-def np_mask(mask, q_len: int, kv_len: int, doc_row=None, prefix_len=None) -> np.ndarray:
-    """Explicit [q_len, kv_len] boolean mask by broadcasting index grids."""
-    i = np.arange(q_len, dtype=np.int64)[:, None]
+def np_mask(mask, q_len: int, kv_len: int, doc_row=None, prefix_len=None, q_offset: int = 0) -> np.ndarray:
+    """Explicit [q_len, kv_len] boolean mask by broadcasting index grids; query
+    row i sits at position i + q_offset."""
+    i = np.arange(q_offset, q_offset + q_len, dtype=np.int64)[:, None]
     j = np.arange(kv_len, dtype=np.int64)[None, :]
     stack = []
     for node in (mask.nodes if hasattr(mask, "nodes") else mask):
@@ -334,7 +338,7 @@ def np_mask(mask, q_len: int, kv_len: int, doc_row=None, prefix_len=None) -> np.
             stack.append(np.broadcast_to(i >= j, (q_len, kv_len)))
         elif kind == "same_doc":
             d = np.asarray(doc_row, dtype=np.int64)
-            stack.append(d[:q_len][:, None] == d[:kv_len][None, :])
+            stack.append(d[q_offset:q_offset + q_len][:, None] == d[:kv_len][None, :])
         elif kind == "window":
             stack.append(np.broadcast_to((i - j) < node[1], (q_len, kv_len)))
         elif kind == "sink":
@@ -375,9 +379,9 @@ def np_classify(M: np.ndarray, block: int, block_kv: Optional[int] = None) -> np
     return cls
 
 
-def _np_scores(q, k, score, slope, scale, q_len, kv_len):
+def _np_scores(q, k, score, slope, scale, q_len, kv_len, q_offset=0):
     x = scale * (q @ k.T)
-    i = np.arange(q_len)[:, None]
+    i = np.arange(q_offset, q_offset + q_len)[:, None]
     j = np.arange(kv_len)[None, :]
     if score[0] == "softcap":
         c = float(score[1])
@@ -388,11 +392,11 @@ def _np_scores(q, k, score, slope, scale, q_len, kv_len):
     return x, np.ones_like(x)
 
 
-def np_forward(q, k, v, M, score=("none",), slope=0.0, scale=None):
+def np_forward(q, k, v, M, score=("none",), slope=0.0, scale=None, q_offset=0):
     q_len, D = q.shape
     kv_len = k.shape[0]
     scale = 1.0 / np.sqrt(D) if scale is None else scale
-    s, _ = _np_scores(q, k, score, slope, scale, q_len, kv_len)
+    s, _ = _np_scores(q, k, score, slope, scale, q_len, kv_len, q_offset)
     s = np.where(M, s, -np.inf)
     m = s.max(axis=1, keepdims=True)
     m_safe = np.where(np.isfinite(m), m, 0.0)
@@ -404,12 +408,12 @@ def np_forward(q, k, v, M, score=("none",), slope=0.0, scale=None):
     return P @ v, lse, P
 
 
-def np_backward(q, k, v, do, M, score=("none",), slope=0.0, scale=None):
+def np_backward(q, k, v, do, M, score=("none",), slope=0.0, scale=None, q_offset=0):
     q_len, D = q.shape
     kv_len = k.shape[0]
     scale = 1.0 / np.sqrt(D) if scale is None else scale
-    out, lse, P = np_forward(q, k, v, M, score, slope, scale)
-    _, dsdx = _np_scores(q, k, score, slope, scale, q_len, kv_len)
+    out, lse, P = np_forward(q, k, v, M, score, slope, scale, q_offset)
+    _, dsdx = _np_scores(q, k, score, slope, scale, q_len, kv_len, q_offset)
     dP = do @ v.T
     dS = P * (dP - (P * dP).sum(axis=1, keepdims=True)) * dsdx
     dq = scale * dS @ k

@@ -80,11 +80,16 @@ typedef struct {
      * sel_block tiles: 0 not listed, 1 listed partial, 2 listed full. */
     const int8_t *sel;
     int64_t sel_block, sel_nkv;
+    /* Position of query row 0 in the sequence the program describes: row i is
+     * position i + q_off for CAUSAL, WINDOW, SAME_DOC and ALiBi (decoding new
+     * tokens at the end of a cache). */
+    int64_t q_off;
 } or_program;
 
 /* The program's value at (i, j), evaluated with an explicit stack. */
-static int program_at(const or_program *p, int64_t i, int64_t j)
+static int program_at(const or_program *p, int64_t row, int64_t j)
 {
+    const int64_t i = row + p->q_off;  /* the query's position */
     int st[16];
     int sp = 0;
     for (int n = 0; n < p->n; ++n) {
@@ -209,7 +214,7 @@ void oracle_forward_head(const double *q, const double *k, const double *v,
                 vis[j] = (uint8_t)mask_at(p, i, j);
                 if (!vis[j]) continue;
                 const double x = scale * dot(qi, k + j * D, D);
-                s[j] = score_mod(score_op, score_param, x, i, j, NULL);
+                s[j] = score_mod(score_op, score_param, x, i + p->q_off, j, NULL);
                 if (s[j] > m) m = s[j];
                 ++nvis;
             }
@@ -265,7 +270,7 @@ void oracle_backward_head(const double *q, const double *k, const double *v, con
                 vis[j] = (uint8_t)mask_at(p, i, j);
                 if (!vis[j]) continue;
                 const double x = scale * dot(q + i * D, k + j * D, D);
-                s[j] = score_mod(score_op, score_param, x, i, j, NULL);
+                s[j] = score_mod(score_op, score_param, x, i + p->q_off, j, NULL);
                 if (s[j] > m) m = s[j];
                 ++nvis;
             }
@@ -301,7 +306,7 @@ void oracle_backward_head(const double *q, const double *k, const double *v, con
             if (!mask_at(p, i, j)) continue;
             double dsdx;
             const double x = scale * dot(q + i * D, k + j * D, D);
-            const double sij = score_mod(score_op, score_param, x, i, j, &dsdx);
+            const double sij = score_mod(score_op, score_param, x, i + p->q_off, j, &dsdx);
             const double P = exp(sij - lse[i]);
             const double dP = dot(dout + i * D, v + j * D, D);
             const double dS = P * (dP - delta[i]) * dsdx;
@@ -320,7 +325,7 @@ void oracle_backward_head(const double *q, const double *k, const double *v, con
             if (!mask_at(p, i, j)) continue;
             double dsdx;
             const double x = scale * dot(q + i * D, k + j * D, D);
-            const double sij = score_mod(score_op, score_param, x, i, j, &dsdx);
+            const double sij = score_mod(score_op, score_param, x, i + p->q_off, j, &dsdx);
             const double P = exp(sij - lse[i]);
             const double dP = dot(dout + i * D, v + j * D, D);
             const double dS = P * (dP - delta[i]) * dsdx;
@@ -361,7 +366,7 @@ double oracle_score_param_grad_head(const double *q, const double *k, const doub
                 vis[j] = (uint8_t)mask_at(p, i, j);
                 if (!vis[j]) continue;
                 x[j] = scale * dot(q + i * D, k + j * D, D);
-                s[j] = score_mod(score_op, score_param, x[j], i, j, NULL);
+                s[j] = score_mod(score_op, score_param, x[j], i + p->q_off, j, NULL);
                 dp[j] = dot(dout + i * D, v + j * D, D);
                 if (s[j] > m) m = s[j];
                 ++nvis;
@@ -377,7 +382,7 @@ double oracle_score_param_grad_head(const double *q, const double *k, const doub
             for (int64_t j = 0; j < kv_len; ++j) {
                 if (!vis[j]) continue;
                 const double P = exp(s[j] - lse);
-                total += P * (dp[j] - delta) * score_mod_dparam(score_op, score_param, x[j], i, j);
+                total += P * (dp[j] - delta) * score_mod_dparam(score_op, score_param, x[j], i + p->q_off, j);
             }
         }
         free(s);

@@ -681,3 +681,60 @@ def test_paged_gather_identity_table_and_invalid_pages():
             oracle.paged_gather(pool, t, 22, 4)
     with pytest.raises(ValueError):
         oracle.paged_gather(pool, ident[:, :5], 22, 4)                       # table too short
+
+
+# ---------------------------------------------------------------- query offset
+
+@pytest.mark.parametrize("seed", range(6))
+def test_q_offset_mask_matches_numpy_twin(seed):
+    """A query offset in the C element-wise evaluation and in the numpy twin's
+    broadcasting, on random programs, ragged lengths and small blocks."""
+    rng = np.random.default_rng(50 + seed)
+    nodes = _random_program(rng)
+    if len(nodes) > 16:
+        nodes = nodes[:1]
+    prog = MaskProgram(tuple(nodes))
+    kv_len = int(rng.integers(60, 300))
+    q_len = int(rng.integers(1, kv_len))
+    off = int(rng.integers(0, kv_len - q_len + 1))
+    docs = make_doc_ids(("geometric", 30.0), kv_len, seed)[0]
+    prefix = int(rng.integers(0, 150))
+    cp = oracle.Program(prog, doc_row=docs, prefix_len=prefix, q_offset=off)
+    M = oracle.mask_dense(cp, q_len, kv_len)
+    np.testing.assert_array_equal(M, oracle.np_mask(prog, q_len, kv_len, doc_row=docs, prefix_len=prefix,
+                                                    q_offset=off))
+    for block in (16, 64):
+        np.testing.assert_array_equal(oracle.classify_tiles(cp, q_len, kv_len, block), oracle.np_classify(M, block))
+
+
+@pytest.mark.parametrize("score", ["none", "alibi", "softcap"])
+def test_q_offset_rows_are_rows_of_the_whole_sequence(score):
+    """Query rows at an offset (decoding new tokens at the end of a cache) give
+    exactly the corresponding rows of the same sequence computed whole; their
+    gradients are the whole sequence's with dO zero on every other row."""
+    kv_len, q_len, off, D = 300, 7, 290, 16
+    docs = make_doc_ids(("geometric", 60.0), kv_len, 3)[0]
+    mask = P(("causal",), ("same_doc",), ("window", 100), ("sink", 8), ("or",), ("and",), ("and",))
+    sc = {"none": ("none",), "alibi": ("alibi", np.array([0.3], np.float32)), "softcap": ("softcap", 5.0)}[score]
+    g = torch.Generator().manual_seed(11)
+    qf, k, v, dof = (torch.randn(n, D, generator=g, dtype=torch.float64).numpy() for n in (kv_len, kv_len, kv_len, kv_len))
+    dof[:off] = 0.0
+    dof[off + q_len:] = 0.0
+    q, do = qf[off:off + q_len], dof[off:off + q_len]
+    whole = oracle.Program(mask, doc_row=docs)
+    part = oracle.Program(mask, doc_row=docs, q_offset=off)
+    scale = 1.0 / np.sqrt(D)
+    out_w, lse_w = oracle.forward_head(qf, k, v, whole, sc, 0, scale)
+    out_p, lse_p = oracle.forward_head(q, k, v, part, sc, 0, scale)
+    np.testing.assert_allclose(out_p, out_w[off:off + q_len], rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(lse_p, lse_w[off:off + q_len], rtol=1e-12, atol=1e-12)
+    dq_w, dk_w, dv_w, _, _ = oracle.backward_head(qf, k, v, dof, whole, sc, 0, scale)
+    dq_p, dk_p, dv_p, _, _ = oracle.backward_head(q, k, v, do, part, sc, 0, scale)
+    np.testing.assert_allclose(dq_p, dq_w[off:off + q_len], rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(dk_p, dk_w, rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(dv_p, dv_w, rtol=1e-10, atol=1e-12)
+    # and the numpy twin, in matrix form, agrees
+    M = oracle.np_mask(mask, q_len, kv_len, doc_row=docs, q_offset=off)
+    slope = float(np.float32(0.3)) if score == "alibi" else 0.0  # the oracle takes slopes as fp32 values
+    o2, l2, _ = oracle.np_forward(q, k, v, M, sc if score != "alibi" else ("alibi",), slope, scale, q_offset=off)
+    np.testing.assert_allclose(o2, out_p, rtol=1e-10, atol=1e-12)
