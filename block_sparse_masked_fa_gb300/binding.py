@@ -46,7 +46,8 @@ class MaskNode(ctypes.Structure):
 
 
 class MaskSpec(ctypes.Structure):
-    _fields_ = [("n", ctypes.c_int32), ("doc_len", ctypes.c_int64), ("node", MaskNode * MAX_NODES)]
+    _fields_ = [("n", ctypes.c_int32), ("doc_len", ctypes.c_int64), ("node", MaskNode * MAX_NODES),
+                ("q_offset", ctypes.c_int64)]
 
 
 class ScoreSpec(ctypes.Structure):
@@ -150,13 +151,15 @@ def _dev_int32(x, device) -> torch.Tensor:
     return torch.as_tensor(x, dtype=torch.int32, device=device).reshape(-1)
 
 
-def make_mask_spec(nodes: Sequence[tuple], device=None):
+def make_mask_spec(nodes: Sequence[tuple], device=None, q_offset: int = 0):
     """Device-side mask spec from a postfix node list.
 
     Nodes: ("causal",), ("true",), ("same_doc", doc_ids [Bm, doc_len] int32),
     ("window", W), ("sink", n), ("prefix", prefix_len [Bm]), ("and",), ("or",).
     Scalars given as Python ints are copied into fresh device int32 tensors;
     pass an int32 CUDA tensor to change a parameter later without a new spec.
+    q_offset: position of query row 0 (e.g. kv_len - q_len when decoding the
+    newest tokens of a cache; see fa_mask_spec in fa.h).
     Returns (MaskSpec, keepalive list of tensors).
     """
     device = device or torch.device("cuda", torch.cuda.current_device())
@@ -177,6 +180,7 @@ def make_mask_spec(nodes: Sequence[tuple], device=None):
             if kind == "same_doc":
                 doc_len = int(t.shape[-1])
     spec.doc_len = doc_len
+    spec.q_offset = int(q_offset)
     return spec, keep
 
 
@@ -305,9 +309,11 @@ def _check_buffer(buffer: torch.Tensor):
 
 
 def fa_create_block_mask(nodes: Sequence[tuple], Bm: int, Hm: int, q_len: int, kv_len: int, block: int = 128,
-                         buffer: Optional[torch.Tensor] = None, stream=None) -> BlockMask:
-    """Builds the block mask of a postfix mask program (see make_mask_spec)."""
-    spec, keep = nodes if isinstance(nodes, tuple) and isinstance(nodes[0], MaskSpec) else make_mask_spec(nodes)
+                         buffer: Optional[torch.Tensor] = None, stream=None, q_offset: int = 0) -> BlockMask:
+    """Builds the block mask of a postfix mask program (see make_mask_spec;
+    q_offset applies to a node list, a prebuilt spec carries its own)."""
+    spec, keep = (nodes if isinstance(nodes, tuple) and isinstance(nodes[0], MaskSpec)
+                  else make_mask_spec(nodes, q_offset=q_offset))
     nbytes = fa_block_mask_bytes(Bm, Hm, q_len, kv_len, block)
     if buffer is None:
         buffer = torch.empty(nbytes, dtype=torch.uint8, device="cuda")

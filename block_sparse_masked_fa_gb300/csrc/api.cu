@@ -119,6 +119,11 @@ fa_status check_mask(const fa_mask_spec* spec, int64_t q_len, int64_t kv_len, De
     dm->param[k] = prm;
   }
   if (depth != 1) return FA_ERR_INVALID_ARG;
+  // every query row's position lies below max(q_len, kv_len), where the
+  // document ids and their run table are defined
+  const int64_t span = q_len > kv_len ? q_len : kv_len;
+  if (spec->q_offset < 0 || spec->q_offset > span - q_len) return FA_ERR_INVALID_ARG;
+  dm->q_off = spec->q_offset;
   if (doc != nullptr) {
     const int64_t need = q_len > kv_len ? q_len : kv_len;
     if (spec->doc_len < need) return FA_ERR_SHAPE;

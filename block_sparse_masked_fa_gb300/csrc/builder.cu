@@ -110,8 +110,9 @@ __global__ void tile_summary_kernel(const __grid_constant__ BuildArgs a) {
   const int ntiles = which ? a.nkv : a.nq;
   if (t >= ntiles) return;
   const int32_t* doc = a.mask.doc + (int64_t)bm * a.mask.doc_len;
-  const int64_t i0 = (int64_t)t * a.block;
-  const int64_t i1 = min(i0 + a.block, len);
+  const int64_t off = which ? 0 : a.mask.q_off;  // query rows sit at positions row + q_off
+  const int64_t i0 = (int64_t)t * a.block + off;
+  const int64_t i1 = min((int64_t)t * a.block + a.block, len) + off;
   int mn = INT_MAX, mx = INT_MIN;
   bool run = true;
   for (int64_t i = i0 + lane; i < i1; i += 32) {
@@ -181,8 +182,8 @@ struct RowSegs {
 
 // The program's value at one pair (x, y).
 __device__ __forceinline__ bool mask_bit(int nn, uint64_t ops, const int32_t* arg, bool transposed, int64_t x,
-                                         int64_t y, int run_lo, int run_hi) {
-  const int64_t i = transposed ? y : x, j = transposed ? x : y;
+                                         int64_t y, int run_lo, int run_hi, int64_t off) {
+  const int64_t i = (transposed ? y : x) + off, j = transposed ? x : y;  // i: the query's position
   uint32_t st = 0;  // bit stack, top at bit 0
 #pragma unroll 1
   for (int k = 0; k < nn; ++k, ops >>= 4) {
@@ -203,7 +204,10 @@ __device__ __forceinline__ bool mask_bit(int nn, uint64_t ops, const int32_t* ar
 }
 
 //  len            extent of y (kv_len, or q_len when transposed)
-//  have_run       the ids never decrease and [run_lo, run_hi) is x's run
+//  have_run       the ids never decrease and [run_lo, run_hi) is the run of x's
+//                 position (x + off for a query row)
+//  off            position of query row 0: a query row x is position x + off,
+//                 and the intervals of a key column are over query rows
 // Everything stays in registers (constant indices only): at most kRowBreaks
 // interval ends besides 0, else the row is left to the per-word evaluation.
 constexpr int kRowBreaks = 8;
@@ -215,8 +219,13 @@ __device__ __forceinline__ void cswap(int64_t& a, int64_t& b) {
 }
 
 __device__ RowSegs row_segments(int nn, uint64_t ops, const int32_t* arg, bool transposed,
-                                                    int64_t x, bool have_run, int run_lo, int run_hi, int64_t len) {
+                                                    int64_t x, bool have_run, int run_lo, int run_hi, int64_t len,
+                                                    int64_t off) {
   RowSegs seg{-1, 0, 0, 0, 0};
+  if (transposed) {  // the run, in query rows
+    run_lo -= (int)off;
+    run_hi -= (int)off;
+  }
   int64_t bp[kRowBreaks];
 #pragma unroll
   for (int t = 0; t < kRowBreaks; ++t) bp[t] = len;
@@ -234,10 +243,10 @@ __device__ RowSegs row_segments(int nn, uint64_t ops, const int32_t* arg, bool t
       v1 = run_hi;
       add = 2;
     } else if (op == FA_M_CAUSAL) {
-      v0 = transposed ? x : x + 1;
+      v0 = transposed ? x - off : x + off + 1;
       add = 1;
     } else if (op == FA_M_WINDOW) {
-      v0 = transposed ? x + (int64_t)arg[k] : x - (int64_t)arg[k] + 1;
+      v0 = transposed ? x + (int64_t)arg[k] - off : x + off - (int64_t)arg[k] + 1;
       add = 1;
     } else if (!transposed && (op == FA_M_SINK || op == FA_M_PREFIX)) {
       v0 = arg[k];
@@ -265,7 +274,7 @@ __device__ RowSegs row_segments(int nn, uint64_t ops, const int32_t* arg, bool t
 #pragma unroll
   for (int t = 0; t + 1 < kRowBreaks; ++t) {
     const int64_t y0 = bp[t], y1 = bp[t + 1];
-    if (y0 < y1 && mask_bit(nn, ops, arg, transposed, x, y0, run_lo, run_hi)) {
+    if (y0 < y1 && mask_bit(nn, ops, arg, transposed, x, y0, run_lo, run_hi, off)) {
       if (n == 1 && hi0 == (int)y0) {
         hi0 = (int)y1;
       } else if (n == 2 && hi1 == (int)y0) {
@@ -302,12 +311,17 @@ __global__ void __launch_bounds__(256) row_segs_kernel(const __grid_constant__ B
   const int64_t x = gid % L;
   const int which = (int)((gid / L) % 2);
   const int bm = (int)(gid / (2 * L));
+  const int64_t off = a.mask.q_off;
+  if (which == 0 && x + off >= L) {  // past the last query row's position: no row
+    reinterpret_cast<int4*>(a.row_segs)[gid] = make_int4(-1, -1, 0, 0);
+    return;
+  }
   int32_t arg[FA_MAX_MASK_NODES];
   for (int k = 0; k < a.mask.n; ++k) arg[k] = node_arg(a.mask, k, bm);
   int lo = 0, hi = 0;
-  const bool have_run = a.mask.has_doc && doc_run(a.mask, bm, x, lo, hi);
+  const bool have_run = a.mask.has_doc && doc_run(a.mask, bm, which == 0 ? x + off : x, lo, hi);
   const RowSegs s = row_segments(a.mask.n, pack_ops(a.mask), arg, which == 1, x, have_run, lo, hi,
-                                 which ? a.q_len : a.kv_len);
+                                 which ? a.q_len : a.kv_len, off);
   reinterpret_cast<int4*>(a.row_segs)[gid] = (s.n < 0) ? make_int4(-1, -1, 0, 0) : make_int4(s.lo0, s.hi0, s.lo1, s.hi1);
 }
 
@@ -357,7 +371,8 @@ __global__ void __launch_bounds__(kBuildWarps * 32) classify_kernel(const __grid
       k_mx = sm[1];
       k_run = sm[2];
     }
-    k3 = program_interval(a.mask, arg, i0, i1, j0, j1, q_mn, q_mx, q_run, k_mn, k_mx, k_run);
+    k3 = program_interval(a.mask, arg, i0 + a.mask.q_off, i1 + a.mask.q_off, j0, j1, q_mn, q_mx, q_run, k_mn, k_mx,
+                          k_run);
     cls = (k3 == K_ALL) ? 2 : (k3 == K_PART ? 1 : 0);
   }
   uint32_t undecided = __ballot_sync(0xffffffffu, valid && k3 == K_SOME);
@@ -379,9 +394,10 @@ __global__ void __launch_bounds__(kBuildWarps * 32) classify_kernel(const __grid
                      max((int64_t)0, min((int64_t)sg.w, j1 + 1) - max((int64_t)sg.z, j0)));
         continue;
       }
-      const int32_t doc_i = doc ? __ldg(doc + i) : 0;
+      const int64_t ip = i + a.mask.q_off;  // the query's position
+      const int32_t doc_i = doc ? __ldg(doc + ip) : 0;
       int run_lo = 0, run_hi = 0;
-      const bool use_run = doc != nullptr && doc_run(a.mask, bm, i, run_lo, run_hi);
+      const bool use_run = doc != nullptr && doc_run(a.mask, bm, ip, run_lo, run_hi);
       for (int64_t jc = j0; jc <= j1; jc += 32) {
         auto eq = [&]() {
           if (use_run) return range_bits(run_lo, run_hi, (int)jc);
@@ -400,7 +416,7 @@ __global__ void __launch_bounds__(kBuildWarps * 32) classify_kernel(const __grid
           }
           return w;
         };
-        cnt += __popc(mask_word_rolled(a.mask.n, ops, arg, i, jc, eq) & low_bits(j1 + 1 - jc));
+        cnt += __popc(mask_word_rolled(a.mask.n, ops, arg, ip, jc, eq) & low_bits(j1 + 1 - jc));
       }
     }
     const int total = (int)__reduce_add_sync(0xffffffffu, (unsigned)cnt);

@@ -668,6 +668,7 @@ __global__ void __launch_bounds__(512, 1)
     const uint32_t lane_off = (uint32_t)((warp % 4) * 32) << 16;
     const uint32_t tS = tmem + lane_off + C::T_S, tP = tmem + lane_off + C::T_DP;
     const uint64_t mask_ops = pack_ops(p.mask);
+    const int qoff = (int)p.mask.q_off;  // query row i is position i + qoff (below 2^31: checked on the host)
     const float sc_l2 = p.scale * kLog2e;
     float cap_l2 = 0.f, sc_over_cap = 0.f;
     if constexpr (SCORE == FA_S_SOFTCAP) {
@@ -748,11 +749,12 @@ __global__ void __launch_bounds__(512, 1)
 #pragma unroll 1
           for (int c2 = 0; c2 < 2; ++c2) {
             const int i0 = I * 128 + 32 * (2 * half + c2);
+            const int ip0 = i0 + qoff;  // the rows' positions (query row i is position i + q_off)
             auto eq = [&]() {
-              if (use_run) return range_bits(run_lo, run_hi, i0);
+              if (use_run) return range_bits(run_lo, run_hi, ip0);
               uint32_t bits = 0;
-              if (i0 + 32 <= p.q_len && p.mask.doc_vec_ok) {
-                const int4* dv = reinterpret_cast<const int4*>(doc_row + i0);
+              if (i0 + 32 <= p.q_len && p.mask.doc_vec_ok && (qoff & 3) == 0) {  // 16-byte aligned rows
+                const int4* dv = reinterpret_cast<const int4*>(doc_row + ip0);
 #pragma unroll
                 for (int q4 = 0; q4 < 8; ++q4) {
                   const int4 d = __ldg(dv + q4);
@@ -761,11 +763,12 @@ __global__ void __launch_bounds__(512, 1)
                 }
               } else {
                 const int in = min(i0 + 32, p.q_len);
-                for (int i = i0; i < in; ++i) bits |= (uint32_t)(__ldg(doc_row + i) == doc_j) << (uint32_t)(i - i0);
+                for (int i = i0; i < in; ++i)
+                  bits |= (uint32_t)(__ldg(doc_row + i + qoff) == doc_j) << (uint32_t)(i - i0);
               }
               return bits;
             };
-            const uint32_t w = mask_word_t_rolled(p.mask.n, mask_ops, arg_s, j, i0, eq);
+            const uint32_t w = mask_word_t_rolled(p.mask.n, mask_ops, arg_s, j, ip0, eq);
             wm0 = (c2 == 0) ? w : wm0;
             wm1 = (c2 == 1) ? w : wm1;
           }
@@ -798,8 +801,8 @@ __global__ void __launch_bounds__(512, 1)
               gd = fma2(make_float2(-t0, -t1), make_float2(t0, t1), make_float2(1.0f, 1.0f));
             } else if constexpr (SCORE == FA_S_ALIBI) {
               a = fma2(make_float2(sv[e], sv[e + 1]), make_float2(sc_l2, sc_l2),
-                       make_float2(fmaf(-slope_l2, (float)(i0 + e - j), nl.x),
-                                   fmaf(-slope_l2, (float)(i0 + e + 1 - j), nl.y)));
+                       make_float2(fmaf(-slope_l2, (float)(i0 + qoff + e - j), nl.x),
+                                   fmaf(-slope_l2, (float)(i0 + qoff + e + 1 - j), nl.y)));
             } else {
               a = fma2(make_float2(sv[e], sv[e + 1]), make_float2(sc_l2, sc_l2), nl);
             }
@@ -847,7 +850,7 @@ __global__ void __launch_bounds__(512, 1)
         if constexpr (PGRAD) {
           // dL/dslope += dS * ds/dslope, ds/dslope = -(i - j) = j - i, once dS is
           // handed over (the dQ MMA does not wait for it)
-          const float jb = (float)(j - (I * 128 + 64 * half));  // j - i of this half's first column (exact)
+          const float jb = (float)(j - (I * 128 + 64 * half + qoff));  // j - i of this half's first column (exact)
 #pragma unroll
           for (int e = 0; e < 64; e += 2)
             pacc = fma2(make_float2(pg[e], pg[e + 1]), make_float2(jb - (float)e, jb - (float)(e + 1)), pacc);

@@ -31,6 +31,7 @@ struct DevMask {
   const int32_t* runs;
   const int32_t* sorted;
   int64_t run_len;
+  int64_t q_off;  // position of query row 0 (fa_mask_spec::q_offset)
   int32_t op[FA_MAX_MASK_NODES];
   const int32_t* param[FA_MAX_MASK_NODES];
 };

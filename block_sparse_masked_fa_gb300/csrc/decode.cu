@@ -175,6 +175,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     // ------------------------------------------------------------ compute warps
     const uint64_t mask_ops = pack_ops(p.mask);
     const int32_t* doc_row = p.mask.has_doc ? p.mask.doc + (int64_t)bm * p.mask.doc_len : nullptr;
+    const int qoff = (int)p.mask.q_off;
     float slope_l2 = 0.f, cap = 1.f;
     if constexpr (SCORE == FA_S_ALIBI) slope_l2 = __ldg(p.score_param + h) * kLog2e;
     if constexpr (SCORE == FA_S_SOFTCAP) cap = __ldg(p.score_param);
@@ -258,13 +259,14 @@ __global__ void __launch_bounds__(kDecThreads, 1)
             int run_lo = 0, run_hi = 0;
             const bool use_run = doc_row != nullptr && doc_run(p.mask, bm, j, run_lo, run_hi);
             const int32_t doc_j = doc_row != nullptr ? __ldg(doc_row + j) : 0;
+            // query row i is position i + q_off of the sequence
             auto eq = [&]() {
-              if (use_run) return range_bits(run_lo, run_hi, 0);
+              if (use_run) return range_bits(run_lo, run_hi, qoff);
               uint32_t bits = 0;
-              for (int i = 0; i < ql; ++i) bits |= (uint32_t)(__ldg(doc_row + i) == doc_j) << i;
+              for (int i = 0; i < ql; ++i) bits |= (uint32_t)(__ldg(doc_row + i + qoff) == doc_j) << i;
               return bits;
             };
-            w = mask_word_t_rolled(p.mask.n, mask_ops, s_arg, j, 0, eq);
+            w = mask_word_t_rolled(p.mask.n, mask_ops, s_arg, j, qoff, eq);
           }
         }
       }
@@ -279,7 +281,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
             if constexpr (SCORE == FA_S_SOFTCAP) {
               sc = cap * tanh_fast(x / cap) * kLog2e;
             } else if constexpr (SCORE == FA_S_ALIBI) {
-              sc = fmaf(x, kLog2e, -slope_l2 * (float)(i - j));
+              sc = fmaf(x, kLog2e, -slope_l2 * (float)(i + qoff - j));
             } else {
               sc = x * kLog2e;
             }

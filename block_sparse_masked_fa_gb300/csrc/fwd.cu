@@ -430,6 +430,10 @@ __global__ void __launch_bounds__(192, 2)
       const FwdItem cur = ctl->desc[dsl];
       const int n = cur.n, n_full = cur.n_full, I = cur.I, bh = cur.bh, bm = cur.bm;
       const int i = I * 128 + r;
+      // the row's position in the sequence the program describes (rows past
+      // q_len, which store nothing, take the last row's)
+      const int64_t ipos = (int64_t)i + p.mask.q_off;
+      const int64_t ipos_c = (int64_t)min(i, p.q_len - 1) + p.mask.q_off;
       if (p.Bm > 1) {  // this item's mask arguments, once every thread is done with the last item's
         named_bar_sync(1, 128);
         if (r < p.mask.n) ctl->arg[r] = node_arg(p.mask, r, bm);
@@ -457,8 +461,8 @@ __global__ void __launch_bounds__(192, 2)
       int run_lo = 0, run_hi = 0;  // with sorted ids: doc[j] == doc[i] exactly for j in [run_lo, run_hi)
       bool use_run = false;
       if (seg0.x < 0 && doc_row != nullptr) {
-        doc_i = __ldg(doc_row + min(i, p.q_len - 1));
-        use_run = doc_run(p.mask, bm, min(i, p.q_len - 1), run_lo, run_hi);
+        doc_i = __ldg(doc_row + ipos_c);
+        use_run = doc_run(p.mask, bm, ipos_c, run_lo, run_hi);
       }
       float slope_l2 = 0.f;
       if constexpr (SCORE == FA_S_ALIBI) slope_l2 = __ldg(p.score_param + cur.h) * kLog2e;
@@ -505,7 +509,7 @@ __global__ void __launch_bounds__(192, 2)
                 }
                 return bits;
               };
-              w &= mask_word_rolled(p.mask.n, mask_ops, ctl->arg, i, jc, eq);
+              w &= mask_word_rolled(p.mask.n, mask_ops, ctl->arg, ipos, jc, eq);
             }
             // select by c without dynamic indexing
   #pragma unroll
@@ -533,7 +537,7 @@ __global__ void __launch_bounds__(192, 2)
           for (int e = 0; e < BK; ++e) s[e] = ((wd[e >> 5] >> (e & 31)) & 1u) ? s[e] : -INFINITY;
         }
 
-        const float base = slope_l2 * (float)(i - (int)j0);  // ALiBi: -slope (i - j) = -base + slope * e
+        const float base = slope_l2 * (float)(ipos - j0);  // ALiBi: -slope (i - j) = -base + slope * e
         // -- row maximum in log2 units (4 independent chains)
         float mx;
         {

@@ -101,6 +101,13 @@ typedef struct {
   int64_t doc_len;   /* row length (elements) of the SAME_DOC array; must be
                         >= max(q_len, kv_len) when SAME_DOC is used, else 0     */
   fa_mask_node node[FA_MAX_MASK_NODES];
+  /* Position of query row 0 in the sequence the program describes: query row i
+   * is position i + q_offset for CAUSAL, WINDOW and SAME_DOC (and for ALiBi's
+   * i - j), key j is position j.  0 for training shapes; kv_len - q_len when
+   * the queries are the newest tokens of a cache (tutorial "Decoding and paged
+   * KV caches": a mask built for training shapes is wrong during generation).
+   * Must lie in [0, max(q_len, kv_len) - q_len] (FA_ERR_INVALID_ARG). */
+  int64_t q_offset;
 } fa_mask_spec;
 
 /* ------------------------------------------------------------------------
