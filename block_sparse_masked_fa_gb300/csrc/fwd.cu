@@ -27,7 +27,11 @@
 // smaller (tutorial, sharp edge 4): then S is 128 x 64, the P V of a step is
 // one group of four MMAs, and the output has a staging buffer of its own.
 // The running maximum is only moved (and O rescaled) when a new row maximum
-// exceeds it by more than 2^8, so most tiles need no O round trip.
+// exceeds it by more than 2^8, so most tiles need no O round trip.  With ALiBi
+// a row's key tiles are visited nearest first (PARTIAL tiles, then FULL tiles,
+// each list from its last entry), so that the largest bias of the row is met in
+// the first step and the maximum then rarely moves; otherwise FULL tiles come
+// first, so that an item's first step has no mask words to compute.
 #include <algorithm>
 #include <cfloat>
 #include <cmath>
@@ -60,7 +64,8 @@ struct FwdCfg {
 };
 
 // One work item: the query tile I of head (b, h), with the key tiles of its
-// row lists (FULL first, then PARTIAL).
+// row lists: FULL then PARTIAL, or with ALiBi PARTIAL then FULL, each read
+// backwards (highest key tile first).
 struct FwdItem {
   int I, bh, bm, h, n_full, n;
   int J0;        // the first key tile (when n > 0)
@@ -151,8 +156,19 @@ __device__ __forceinline__ FwdItem fwd_item(const AttnArgs& p, int k) {
   return it;
 }
 
+// Whether step jj of an item is a PARTIAL tile, and its key tile.
+template <bool NEAR_FIRST>
+__device__ __forceinline__ bool step_partial(const FwdItem& it, int jj) {
+  return NEAR_FIRST ? jj < it.n - it.n_full : jj >= it.n_full;
+}
+template <bool NEAR_FIRST>
 __device__ __forceinline__ int tile_of(const AttnArgs& p, const FwdItem& it, int jj) {
-  return jj < it.n_full ? __ldg(p.full_idx + it.list + jj) : __ldg(p.kv_idx + it.list + jj - it.n_full);
+  if constexpr (NEAR_FIRST) {
+    const int n_part = it.n - it.n_full;
+    return jj < n_part ? __ldg(p.kv_idx + it.list + (n_part - 1 - jj)) : __ldg(p.full_idx + it.list + (it.n - 1 - jj));
+  } else {
+    return jj < it.n_full ? __ldg(p.full_idx + it.list + jj) : __ldg(p.kv_idx + it.list + jj - it.n_full);
+  }
 }
 
 // This CTA's first item at or after k (its items are k, k + gridDim.x, ...)
@@ -172,6 +188,7 @@ __global__ void __launch_bounds__(192, 2)
                const __grid_constant__ AttnArgs p, float* __restrict__ lse_out,
                __nv_bfloat16* __restrict__ out_g) {
   using C = FwdCfg<D, BK>;
+  constexpr bool NF = (SCORE == FA_S_ALIBI);  // nearest key tiles first
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = smem;
@@ -246,7 +263,7 @@ __global__ void __launch_bounds__(192, 2)
     bool ok = true;
     for (int k = first; ok && k < items; k += (int)gridDim.x, ++v) {
       FwdItem cur = fwd_item(p, k);
-      if (cur.n > 0) cur.J0 = tile_of(p, cur, 0);
+      if (cur.n > 0) cur.J0 = tile_of<NF>(p, cur, 0);
       // hand the item to the softmax warps (every item, with or without visible tiles)
       const int dsl = v & 1;
       const uint32_t dfull = smem_u32(&ctl->desc_full[dsl]);
@@ -277,7 +294,7 @@ __global__ void __launch_bounds__(192, 2)
       }
       q_issued = u + 1;
       for (int jj = 0; ok && jj < cur.n; ++jj, ++t) {
-        const int J = jj == 0 ? cur.J0 : tile_of(p, cur, jj);
+        const int J = jj == 0 ? cur.J0 : tile_of<NF>(p, cur, jj);
         // rows of key tile J: in the caller's [B*H][kv_len] tensors, or (paged,
         // BK = 128 only) in the page the table names, of this head's
         // [n_pages * 128] pool rows
@@ -464,17 +481,21 @@ __global__ void __launch_bounds__(192, 2)
         doc_i = __ldg(doc_row + ipos_c);
         use_run = doc_run(p.mask, bm, ipos_c, run_lo, run_hi);
       }
-      float slope_l2 = 0.f;
-      if constexpr (SCORE == FA_S_ALIBI) slope_l2 = __ldg(p.score_param + cur.h) * kLog2e;
+      float slope_l2 = 0.f, slope_sc = 0.f;
+      if constexpr (SCORE == FA_S_ALIBI) {
+        const float slope = __ldg(p.score_param + cur.h);
+        slope_l2 = slope * kLog2e;
+        slope_sc = slope / p.scale;
+      }
 
       float m = -INFINITY;  // reference maximum, log2 units
       float l = 0.f;
       // the list entry of the next step is fetched one step ahead, off the path
       // from the S wait to the mask words
       for (int jj = 0; jj < n; ++jj, ++t) {
-        const bool partial = jj >= n_full;
+        const bool partial = step_partial<NF>(cur, jj);
         const int J = J_next;
-        if (jj + 1 < n) J_next = tile_of(p, cur, jj + 1);
+        if (jj + 1 < n) J_next = tile_of<NF>(p, cur, jj + 1);
         const int64_t j0 = (int64_t)J * BK;
         const bool ragged = j0 + BK > p.kv_len;
         const bool msk = partial || ragged;
@@ -537,40 +558,32 @@ __global__ void __launch_bounds__(192, 2)
           for (int e = 0; e < BK; ++e) s[e] = ((wd[e >> 5] >> (e & 31)) & 1u) ? s[e] : -INFINITY;
         }
 
-        const float base = slope_l2 * (float)(ipos - j0);  // ALiBi: -slope (i - j) = -base + slope * e
+        // ALiBi: -slope (i - j) = slope e - slope (i - j0) for column e of the tile.
+        // The e term joins S in place, in units of the scaled logit
+        // (s_e + e slope / scale), so that the maximum and the exponent
+        // arguments below are those of the plain score; the j0 term is `base`.
+        const float base = slope_l2 * (float)(ipos - j0);
+        if constexpr (SCORE == FA_S_ALIBI) {
+  #pragma unroll
+          for (int e = 0; e < BK; ++e) s[e] = fmaf(slope_sc, (float)e, s[e]);
+        }
         // -- row maximum in log2 units (4 independent chains)
         float mx;
         {
           float a0 = -INFINITY, a1 = -INFINITY, a2 = -INFINITY, a3 = -INFINITY;
   #pragma unroll
           for (int e = 0; e < BK; e += 8) {
-            if constexpr (SCORE == FA_S_ALIBI) {
-              float t[8];
-  #pragma unroll
-              for (int u = 0; u < 8; u += 2) {
-                const float2 v = fma2(make_float2(s[e + u], s[e + u + 1]), make_float2(sc_l2, sc_l2),
-                                      make_float2(slope_l2 * (float)(e + u), slope_l2 * (float)(e + u + 1)));
-                t[u] = v.x;
-                t[u + 1] = v.y;
-              }
-              a0 = max3f(a0, t[0], t[1]);
-              a1 = max3f(a1, t[2], t[3]);
-              a2 = max3f(a2, t[4], t[5]);
-              a3 = max3f(a3, t[6], t[7]);
-            } else {
-              a0 = max3f(a0, s[e], s[e + 1]);
-              a1 = max3f(a1, s[e + 2], s[e + 3]);
-              a2 = max3f(a2, s[e + 4], s[e + 5]);
-              a3 = max3f(a3, s[e + 6], s[e + 7]);
-            }
+            a0 = max3f(a0, s[e], s[e + 1]);
+            a1 = max3f(a1, s[e + 2], s[e + 3]);
+            a2 = max3f(a2, s[e + 4], s[e + 5]);
+            a3 = max3f(a3, s[e + 6], s[e + 7]);
           }
           mx = fmaxf(fmaxf(a0, a1), fmaxf(a2, a3));
-          if constexpr (SCORE == FA_S_NONE) {
-            mx *= sc_l2;  // scale > 0 keeps the order
-          } else if constexpr (SCORE == FA_S_SOFTCAP) {
+          if constexpr (SCORE == FA_S_SOFTCAP) {
             mx = (mx == -INFINITY) ? -INFINITY : cap_l2 * tanh_fast(mx * sc_over_cap);  // soft-cap is increasing
           } else {
-            mx -= base;
+            mx *= sc_l2;  // scale > 0 keeps the order
+            if constexpr (SCORE == FA_S_ALIBI) mx -= base;
           }
         }
 
@@ -606,8 +619,7 @@ __global__ void __launch_bounds__(192, 2)
               }
               return x;
             } else {
-              return fma2(make_float2(s[e], s[e + 1]), make_float2(sc_l2, sc_l2),
-                          make_float2(fmaf(slope_l2, (float)e, off), fmaf(slope_l2, (float)(e + 1), off)));
+              return fma2(make_float2(s[e], s[e + 1]), make_float2(sc_l2, sc_l2), make_float2(off, off));
             }
           };
   #pragma unroll
