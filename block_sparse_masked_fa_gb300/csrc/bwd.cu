@@ -781,10 +781,12 @@ __global__ void __launch_bounds__(512, 1)
         lok = warp_wait(b_s, g & 1, &ctl->abort);
         tc_fence_after();
         float pg[64];
+        // ALiBi, log2 units: -slope (i + qoff - j) = -slope (i - 128 I) + slope (j - 128 I - qoff)
+        float bj = 0.f;
+        if constexpr (SCORE == FA_S_ALIBI) bj = slope_l2 * (float)(j - (I * 128 + qoff));
 #pragma unroll
         for (int c2 = 0; c2 < 2; ++c2) {
           const int c = 2 * half + c2;  // 32-column chunk of the 128 query columns
-          const int i0 = I * 128 + 32 * c;
           const uint32_t w = (c2 == 0) ? wm0 : wm1;
           float sv[32];
           tmem_ld32f(tS + 32 * c, sv);
@@ -800,9 +802,8 @@ __global__ void __launch_bounds__(512, 1)
               a = fma2(make_float2(cap_l2, cap_l2), make_float2(t0, t1), nl);
               gd = fma2(make_float2(-t0, -t1), make_float2(t0, t1), make_float2(1.0f, 1.0f));
             } else if constexpr (SCORE == FA_S_ALIBI) {
-              a = fma2(make_float2(sv[e], sv[e + 1]), make_float2(sc_l2, sc_l2),
-                       make_float2(fmaf(-slope_l2, (float)(i0 + qoff + e - j), nl.x),
-                                   fmaf(-slope_l2, (float)(i0 + qoff + e + 1 - j), nl.y)));
+              // the stats carry -slope (i - 128 I) of each query row; the key's part is bj
+              a = fma2(make_float2(sv[e], sv[e + 1]), make_float2(sc_l2, sc_l2), add2(nl, make_float2(bj, bj)));
             } else {
               a = fma2(make_float2(sv[e], sv[e + 1]), make_float2(sc_l2, sc_l2), nl);
             }
@@ -883,7 +884,9 @@ __global__ void __launch_bounds__(512, 1)
 }
 
 // Per query row: -LSE * log2(e) and -Delta (Delta_i = dO_i . out_i, fp32)
-// into the per-tile stats array [B*H][nq][2][128], zero for the rows past
+// into the per-tile stats array [B*H][nq][2][128] -- with ALiBi the first also
+// carries the query row's part of the bias within its tile, -slope_h (i - 128 I)
+// log2(e), so that the main kernel adds only the key's part -- zero for the rows past
 // q_len in the last tile; the fp32 dq accumulator rows, the score parameter's
 // gradient (if requested) and the main kernel's item counter set to zero.
 // 16 threads per row, 16 rows per 256-thread block; the blocks after the rows'
@@ -942,7 +945,9 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __grid_constant__ At
     const int64_t bh = row / q_len;
     const int i = (int)(row % q_len);
     float* st = stats + (bh * nq + i / 128) * 256;
-    st[i % 128] = -__ldg(lse + row) * kLog2e;
+    float nl = -__ldg(lse + row) * kLog2e;
+    if (p.score_op == FA_S_ALIBI) nl -= (__ldg(p.score_param + (int)(bh % p.H)) * kLog2e) * (float)(i % 128);
+    st[i % 128] = nl;
     st[128 + i % 128] = -acc;
     if (i == q_len - 1)  // rows past q_len in the last tile
       for (int k = i % 128 + 1; k < 128; ++k) st[k] = st[128 + k] = 0.f;
