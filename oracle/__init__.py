@@ -34,7 +34,7 @@ _lib = None
 
 # Node numbering of oracle.c (independent of the product library's numbering).
 _OP = {"true": 0, "causal": 1, "same_doc": 2, "window": 3, "sink": 4, "prefix": 5, "and": 6, "or": 7}
-_SCORE = {"none": 0, "softcap": 1, "alibi": 2}
+_SCORE = {"none": 0, "softcap": 1, "alibi": 2, "relbias": 3}
 
 
 def build(force: bool = False) -> str:
@@ -63,17 +63,21 @@ def _load():
         lib.oracle_mask_dense.argtypes = [P(_Program), ctypes.c_int64, ctypes.c_int64, P(ctypes.c_uint8)]
         lib.oracle_classify_tiles.argtypes = [P(_Program), ctypes.c_int64, ctypes.c_int64, ctypes.c_int32,
                                               P(ctypes.c_int8)]
+        bias = [d, ctypes.c_int64, ctypes.c_int64]  # the head's bias table, its first distance, its length
         lib.oracle_forward_head.argtypes = [d, d, d, ctypes.c_int64, ctypes.c_int64, ctypes.c_int32, P(_Program),
                                             ctypes.c_int32, ctypes.c_double, ctypes.c_double, i64p,
-                                            ctypes.c_int64, d, d]
+                                            ctypes.c_int64, d, d] + bias
         lib.oracle_backward_head.argtypes = [d, d, d, d, ctypes.c_int64, ctypes.c_int64, ctypes.c_int32,
                                              P(_Program), ctypes.c_int32, ctypes.c_double, ctypes.c_double,
-                                             i64p, ctypes.c_int64, i64p, ctypes.c_int64, d, d, d, d, d]
+                                             i64p, ctypes.c_int64, i64p, ctypes.c_int64, d, d, d, d, d] + bias
         lib.oracle_score_param_grad_head.argtypes = [d, d, d, d, ctypes.c_int64, ctypes.c_int64, ctypes.c_int32,
-                                                     P(_Program), ctypes.c_int32, ctypes.c_double, ctypes.c_double]
+                                                     P(_Program), ctypes.c_int32, ctypes.c_double,
+                                                     ctypes.c_double] + bias
         lib.oracle_score_param_grad_head.restype = ctypes.c_double
+        lib.oracle_bias_grad_head.argtypes = [d, d, d, d, ctypes.c_int64, ctypes.c_int64, ctypes.c_int32,
+                                              P(_Program), d, ctypes.c_int64, ctypes.c_int64, ctypes.c_double, d]
         for f in (lib.oracle_mask_dense, lib.oracle_classify_tiles, lib.oracle_forward_head,
-                  lib.oracle_backward_head):
+                  lib.oracle_backward_head, lib.oracle_bias_grad_head):
             f.restype = None
         _lib = lib
     return _lib
@@ -226,14 +230,27 @@ def tile_lists(cls: np.ndarray) -> dict:
 
 
 def _score_args(score: tuple, h: int):
+    """(op, scalar parameter, bias table of head h or None, its first distance d0).
+    Score tuples: ("none",), ("softcap", c), ("alibi", slopes[H]),
+    ("relbias", table[H, L], d0) -- the learned relative-position bias
+    s = x + table[h, clamp(q_pos - kv_idx - d0, 0, L - 1)]."""
     kind = score[0]
     if kind == "none":
-        return _SCORE["none"], 0.0
+        return _SCORE["none"], 0.0, None, 0
     if kind == "softcap":
-        return _SCORE["softcap"], float(score[1])
+        return _SCORE["softcap"], float(score[1]), None, 0
     if kind == "alibi":
-        return _SCORE["alibi"], float(np.float32(score[1][h]))
+        return _SCORE["alibi"], float(np.float32(score[1][h])), None, 0
+    if kind == "relbias":
+        table = np.ascontiguousarray(np.asarray(score[1], dtype=np.float32)[h], dtype=np.float64)
+        return _SCORE["relbias"], 0.0, table, int(score[2])
     raise ValueError(score)
+
+
+def _bias_args(table: Optional[np.ndarray], d0: int):
+    if table is None:
+        return [None, 0, 0]
+    return [_dptr(table), int(d0), int(table.shape[0])]
 
 
 def forward_head(q: np.ndarray, k: np.ndarray, v: np.ndarray, prog: Program, score: tuple, h: int,
@@ -247,10 +264,10 @@ def forward_head(q: np.ndarray, k: np.ndarray, v: np.ndarray, prog: Program, sco
     n = q.shape[0] if r is None else len(r)
     out = np.zeros((n, D), dtype=np.float64)
     lse = np.zeros(n, dtype=np.float64)
-    op, param = _score_args(score, h)
+    op, param, table, d0 = _score_args(score, h)
     _load().oracle_forward_head(_dptr(q), _dptr(k), _dptr(v), q.shape[0], k.shape[0], D,
                                 ctypes.byref(prog.struct), op, param, float(scale), _i64ptr(r),
-                                n, _dptr(out), _dptr(lse))
+                                n, _dptr(out), _dptr(lse), *_bias_args(table, d0))
     return out, lse
 
 
@@ -271,10 +288,11 @@ def backward_head(q, k, v, do, prog: Program, score: tuple, h: int, scale: float
     dv = np.zeros((nc, D))
     lse = np.zeros(q.shape[0])
     delta = np.zeros(q.shape[0])
-    op, param = _score_args(score, h)
+    op, param, table, d0 = _score_args(score, h)
     _load().oracle_backward_head(_dptr(q), _dptr(k), _dptr(v), _dptr(do), q.shape[0], k.shape[0], D,
                                  ctypes.byref(prog.struct), op, param, float(scale), _i64ptr(r), nr,
-                                 _i64ptr(c), nc, _dptr(dq), _dptr(dk), _dptr(dv), _dptr(lse), _dptr(delta))
+                                 _i64ptr(c), nc, _dptr(dq), _dptr(dk), _dptr(dv), _dptr(lse), _dptr(delta),
+                                 *_bias_args(table, d0))
     return dq, dk, dv, lse, delta
 
 
@@ -305,10 +323,26 @@ def score_param_grad_head(q, k, v, do, prog: Program, score: tuple, h: int, scal
     """dL/dparam of L = sum(out * dO) for one head: the soft-cap c, or the ALiBi
     slope of head h (0.0 for a score mod without a parameter)."""
     arrs = [np.ascontiguousarray(a, dtype=np.float64) for a in (q, k, v, do)]
-    op, param = _score_args(score, h)
+    op, param, table, d0 = _score_args(score, h)
     return float(_load().oracle_score_param_grad_head(*(_dptr(a) for a in arrs), arrs[0].shape[0],
                                                       arrs[1].shape[0], arrs[0].shape[1],
-                                                      ctypes.byref(prog.struct), op, param, float(scale)))
+                                                      ctypes.byref(prog.struct), op, param, float(scale),
+                                                      *_bias_args(table, d0)))
+
+
+def bias_grad_head(q, k, v, do, prog: Program, score: tuple, h: int, scale: float) -> np.ndarray:
+    """dL/dtable[h, :] of L = sum(out * dO) for one (b, h) under ("relbias",
+    table, d0): every visible pair's P (dP - Delta) added to the entry of its
+    distance (tutorial Pattern 3: a learned relative-position bias trains)."""
+    if score[0] != "relbias":
+        raise ValueError(score)
+    arrs = [np.ascontiguousarray(a, dtype=np.float64) for a in (q, k, v, do)]
+    _, _, table, d0 = _score_args(score, h)
+    grad = np.zeros(table.shape[0], dtype=np.float64)
+    _load().oracle_bias_grad_head(*(_dptr(a) for a in arrs), arrs[0].shape[0], arrs[1].shape[0],
+                                  arrs[0].shape[1], ctypes.byref(prog.struct), _dptr(table), int(d0),
+                                  table.shape[0], float(scale), _dptr(grad))
+    return grad
 
 
 def head_score(score_kind: tuple, slopes=None, softcap=None) -> tuple:
@@ -379,10 +413,22 @@ def np_classify(M: np.ndarray, block: int, block_kv: Optional[int] = None) -> np
     return cls
 
 
+def _np_bias_entry(d0, L, q_len, kv_len, q_offset=0):
+    """[q_len, kv_len] table entry of every pair: clip(q_pos - kv_idx - d0, 0, L - 1)."""
+    i = np.arange(q_offset, q_offset + q_len)[:, None]
+    j = np.arange(kv_len)[None, :]
+    return np.clip(i - j - d0, 0, L - 1)
+
+
 def _np_scores(q, k, score, slope, scale, q_len, kv_len, q_offset=0):
+    """Scores and ds/dx.  score: ("none",), ("softcap", c), ("alibi",) with the
+    head's slope in `slope`, or ("relbias", table_h [L], d0)."""
     x = scale * (q @ k.T)
     i = np.arange(q_offset, q_offset + q_len)[:, None]
     j = np.arange(kv_len)[None, :]
+    if score[0] == "relbias":
+        table = np.asarray(score[1], dtype=np.float64)
+        return x + table[_np_bias_entry(int(score[2]), len(table), q_len, kv_len, q_offset)], np.ones_like(x)
     if score[0] == "softcap":
         c = float(score[1])
         t = np.tanh(x / c)
@@ -440,3 +486,18 @@ def np_score_param_grad(q, k, v, do, M, score=("none",), slope=0.0, scale=None) 
     else:
         dsdp = np.zeros_like(x)
     return float(np.where(M, P * (dP - delta) * dsdp, 0.0).sum())
+
+
+def np_bias_grad(q, k, v, do, M, table_h, d0, scale=None, q_offset=0) -> np.ndarray:
+    """dL/dtable_h in matrix form: dS = P (dP - Delta) over the mask, summed into
+    the entry of each pair's distance."""
+    q_len, D = q.shape
+    kv_len = k.shape[0]
+    scale = 1.0 / np.sqrt(D) if scale is None else scale
+    score = ("relbias", table_h, d0)
+    _, _, P = np_forward(q, k, v, M, score, 0.0, scale, q_offset)
+    dP = do @ v.T
+    dS = np.where(M, P * (dP - (P * dP).sum(axis=1, keepdims=True)), 0.0)
+    grad = np.zeros(len(table_h))
+    np.add.at(grad, _np_bias_entry(int(d0), len(table_h), q_len, kv_len, q_offset), dS)
+    return grad

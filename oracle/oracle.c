@@ -40,13 +40,17 @@
  *      dv_j   = sum_i P_ij dO_i
  *
  * Score mods: none (s = x); soft-cap s = c tanh(x / c), ds/dx = 1 - tanh^2(x / c);
- * ALiBi s = x - slope_h (i - j), ds/dx = 1.
+ * ALiBi s = x - slope_h (i - j), ds/dx = 1; a learned relative-position bias
+ * s = x + bias_h[clamp(i - j - d0, 0, L - 1)], ds/dx = 1: one table entry per
+ * query-minus-key distance from d0 to d0 + L - 1, distances outside that range
+ * taking the nearest end entry.
  *
  *  - the gradient of L with respect to the score mod's parameter (tutorial
  *    Pattern 3: a learned relative-position bias trains through the fused
  *    backward):  dL/dparam = sum_{i, j in V_i} P_ij (dP_ij - Delta_i) ds_ij/dparam
  *    with ds/dslope_h = -(i - j) for ALiBi and ds/dc = tanh(x/c) - (x/c)(1 - tanh^2(x/c))
- *    for the soft-cap.
+ *    for the soft-cap; for the bias table, dL/dbias_h[t] is that sum over the
+ *    pairs whose distance maps to entry t (ds/dbias_h[t] = 1 there, 0 elsewhere).
  *
  * All arithmetic is double precision on the bf16-rounded inputs that the
  * caller widens to double.  Loops are parallel over independent rows or
@@ -69,7 +73,25 @@ enum {
     OR_OR = 7
 };
 
-enum { OR_SCORE_NONE = 0, OR_SCORE_SOFTCAP = 1, OR_SCORE_ALIBI = 2 };
+enum { OR_SCORE_NONE = 0, OR_SCORE_SOFTCAP = 1, OR_SCORE_ALIBI = 2, OR_SCORE_RELBIAS = 3 };
+
+/* A score mod for one head: the soft-cap c or ALiBi slope in `param`; the
+ * bias table of this head (len entries, entry 0 at distance d0) for RELBIAS. */
+typedef struct {
+    int32_t op;
+    double param;
+    const double *bias;
+    int64_t d0, len;
+} or_score;
+
+/* The bias table entry of the pair at query position i and key j. */
+static int64_t bias_entry(const or_score *sc, int64_t i, int64_t j)
+{
+    int64_t t = i - j - sc->d0;
+    if (t < 0) t = 0;
+    if (t > sc->len - 1) t = sc->len - 1;
+    return t;
+}
 
 typedef struct {
     int32_t n;             /* number of nodes (postfix order)            */
@@ -160,45 +182,60 @@ static double dot(const double *a, const double *b, int D)
     return s;
 }
 
-/* s = score_mod(x) and ds/dx for one pair. */
-static double score_mod(int op, double param, double x, int64_t i, int64_t j, double *dsdx)
+/* s = score_mod(x) and ds/dx for one pair (i the query's position). */
+static double score_mod(const or_score *sc, double x, int64_t i, int64_t j, double *dsdx)
 {
-    if (op == OR_SCORE_SOFTCAP) {
-        const double t = tanh(x / param);
+    if (sc->op == OR_SCORE_SOFTCAP) {
+        const double t = tanh(x / sc->param);
         if (dsdx) *dsdx = 1.0 - t * t;
-        return param * t;
-    }
-    if (op == OR_SCORE_ALIBI) {
-        if (dsdx) *dsdx = 1.0;
-        return x - param * (double)(i - j);
+        return sc->param * t;
     }
     if (dsdx) *dsdx = 1.0;
+    if (sc->op == OR_SCORE_ALIBI)
+        return x - sc->param * (double)(i - j);
+    if (sc->op == OR_SCORE_RELBIAS)
+        return x + sc->bias[bias_entry(sc, i, j)];
     return x;
 }
 
-/* ds/dparam for one pair: the soft-cap c or the ALiBi slope (0 without a parameter). */
-static double score_mod_dparam(int op, double param, double x, int64_t i, int64_t j)
+/* ds/dparam for one pair: the soft-cap c or the ALiBi slope (0 without a
+ * scalar parameter; the bias table has its own gradient below). */
+static double score_mod_dparam(const or_score *sc, double x, int64_t i, int64_t j)
 {
-    if (op == OR_SCORE_SOFTCAP) {
-        const double t = tanh(x / param);
-        return t - (x / param) * (1.0 - t * t);
+    if (sc->op == OR_SCORE_SOFTCAP) {
+        const double t = tanh(x / sc->param);
+        return t - (x / sc->param) * (1.0 - t * t);
     }
-    if (op == OR_SCORE_ALIBI)
+    if (sc->op == OR_SCORE_ALIBI)
         return -(double)(i - j);
     return 0.0;
+}
+
+static or_score make_score(int32_t op, double param, const double *bias, int64_t d0, int64_t len)
+{
+    or_score sc;
+    sc.op = op;
+    sc.param = param;
+    sc.bias = bias;
+    sc.d0 = d0;
+    sc.len = len;
+    return sc;
 }
 
 /*
  * Forward for one (b, h): q [q_len][D], k, v [kv_len][D] (row-major doubles).
  * rows: the query rows to compute (NULL = all q_len rows, in order); out is
  * [n_rows][D] and lse [n_rows].  score_param is the soft-cap c or the ALiBi
- * slope of this head.
+ * slope of this head; bias / bias_d0 / bias_len this head's bias table (RELBIAS).
  */
 void oracle_forward_head(const double *q, const double *k, const double *v,
                          int64_t q_len, int64_t kv_len, int32_t D,
                          const or_program *p, int32_t score_op, double score_param, double scale,
-                         const int64_t *rows, int64_t n_rows, double *out, double *lse)
+                         const int64_t *rows, int64_t n_rows, double *out, double *lse,
+                         const double *bias, int64_t bias_d0, int64_t bias_len)
 {
+    const or_score sc_ = make_score(score_op, score_param, bias, bias_d0, bias_len);
+    const or_score *sc = &sc_;
     if (rows == NULL) n_rows = q_len;
     #pragma omp parallel
     {
@@ -214,7 +251,7 @@ void oracle_forward_head(const double *q, const double *k, const double *v,
                 vis[j] = (uint8_t)mask_at(p, i, j);
                 if (!vis[j]) continue;
                 const double x = scale * dot(qi, k + j * D, D);
-                s[j] = score_mod(score_op, score_param, x, i + p->q_off, j, NULL);
+                s[j] = score_mod(sc, x, i + p->q_off, j, NULL);
                 if (s[j] > m) m = s[j];
                 ++nvis;
             }
@@ -250,8 +287,11 @@ void oracle_backward_head(const double *q, const double *k, const double *v, con
                           int64_t q_len, int64_t kv_len, int32_t D,
                           const or_program *p, int32_t score_op, double score_param, double scale,
                           const int64_t *rows, int64_t n_rows, const int64_t *cols, int64_t n_cols,
-                          double *dq, double *dk, double *dv, double *lse_all, double *delta_all)
+                          double *dq, double *dk, double *dv, double *lse_all, double *delta_all,
+                          const double *bias, int64_t bias_d0, int64_t bias_len)
 {
+    const or_score sc_ = make_score(score_op, score_param, bias, bias_d0, bias_len);
+    const or_score *sc = &sc_;
     double *lse = (double *)malloc(sizeof(double) * (size_t)(q_len > 0 ? q_len : 1));
     double *delta = (double *)malloc(sizeof(double) * (size_t)(q_len > 0 ? q_len : 1));
     if (rows == NULL) n_rows = q_len;
@@ -270,7 +310,7 @@ void oracle_backward_head(const double *q, const double *k, const double *v, con
                 vis[j] = (uint8_t)mask_at(p, i, j);
                 if (!vis[j]) continue;
                 const double x = scale * dot(q + i * D, k + j * D, D);
-                s[j] = score_mod(score_op, score_param, x, i + p->q_off, j, NULL);
+                s[j] = score_mod(sc, x, i + p->q_off, j, NULL);
                 if (s[j] > m) m = s[j];
                 ++nvis;
             }
@@ -306,7 +346,7 @@ void oracle_backward_head(const double *q, const double *k, const double *v, con
             if (!mask_at(p, i, j)) continue;
             double dsdx;
             const double x = scale * dot(q + i * D, k + j * D, D);
-            const double sij = score_mod(score_op, score_param, x, i + p->q_off, j, &dsdx);
+            const double sij = score_mod(sc, x, i + p->q_off, j, &dsdx);
             const double P = exp(sij - lse[i]);
             const double dP = dot(dout + i * D, v + j * D, D);
             const double dS = P * (dP - delta[i]) * dsdx;
@@ -325,7 +365,7 @@ void oracle_backward_head(const double *q, const double *k, const double *v, con
             if (!mask_at(p, i, j)) continue;
             double dsdx;
             const double x = scale * dot(q + i * D, k + j * D, D);
-            const double sij = score_mod(score_op, score_param, x, i + p->q_off, j, &dsdx);
+            const double sij = score_mod(sc, x, i + p->q_off, j, &dsdx);
             const double P = exp(sij - lse[i]);
             const double dP = dot(dout + i * D, v + j * D, D);
             const double dS = P * (dP - delta[i]) * dsdx;
@@ -349,8 +389,11 @@ void oracle_backward_head(const double *q, const double *k, const double *v, con
  */
 double oracle_score_param_grad_head(const double *q, const double *k, const double *v, const double *dout,
                                     int64_t q_len, int64_t kv_len, int32_t D,
-                                    const or_program *p, int32_t score_op, double score_param, double scale)
+                                    const or_program *p, int32_t score_op, double score_param, double scale,
+                                    const double *bias, int64_t bias_d0, int64_t bias_len)
 {
+    const or_score sc_ = make_score(score_op, score_param, bias, bias_d0, bias_len);
+    const or_score *sc = &sc_;
     double total = 0.0;
     #pragma omp parallel reduction(+ : total)
     {
@@ -366,7 +409,7 @@ double oracle_score_param_grad_head(const double *q, const double *k, const doub
                 vis[j] = (uint8_t)mask_at(p, i, j);
                 if (!vis[j]) continue;
                 x[j] = scale * dot(q + i * D, k + j * D, D);
-                s[j] = score_mod(score_op, score_param, x[j], i + p->q_off, j, NULL);
+                s[j] = score_mod(sc, x[j], i + p->q_off, j, NULL);
                 dp[j] = dot(dout + i * D, v + j * D, D);
                 if (s[j] > m) m = s[j];
                 ++nvis;
@@ -382,7 +425,7 @@ double oracle_score_param_grad_head(const double *q, const double *k, const doub
             for (int64_t j = 0; j < kv_len; ++j) {
                 if (!vis[j]) continue;
                 const double P = exp(s[j] - lse);
-                total += P * (dp[j] - delta) * score_mod_dparam(score_op, score_param, x[j], i + p->q_off, j);
+                total += P * (dp[j] - delta) * score_mod_dparam(sc, x[j], i + p->q_off, j);
             }
         }
         free(s);
@@ -391,4 +434,49 @@ double oracle_score_param_grad_head(const double *q, const double *k, const doub
         free(vis);
     }
     return total;
+}
+
+/*
+ * dL/dbias_h[t] for one (b, h) under the RELBIAS score mod, ADDED into
+ * grad[bias_len]: for every visible pair, P_ij (dP_ij - Delta_i) goes to the
+ * entry its distance maps to.  Rows are taken one at a time (no threads, so
+ * that the sums need no reduction across threads).
+ */
+void oracle_bias_grad_head(const double *q, const double *k, const double *v, const double *dout,
+                           int64_t q_len, int64_t kv_len, int32_t D, const or_program *p,
+                           const double *bias, int64_t bias_d0, int64_t bias_len, double scale, double *grad)
+{
+    const or_score sc_ = make_score(OR_SCORE_RELBIAS, 0.0, bias, bias_d0, bias_len);
+    const or_score *sc = &sc_;
+    double *s = (double *)malloc(sizeof(double) * (size_t)(kv_len > 0 ? kv_len : 1));
+    double *dp = (double *)malloc(sizeof(double) * (size_t)(kv_len > 0 ? kv_len : 1));
+    uint8_t *vis = (uint8_t *)malloc((size_t)(kv_len > 0 ? kv_len : 1));
+    for (int64_t i = 0; i < q_len; ++i) {
+        double m = -INFINITY;
+        int64_t nvis = 0;
+        for (int64_t j = 0; j < kv_len; ++j) {
+            vis[j] = (uint8_t)mask_at(p, i, j);
+            if (!vis[j]) continue;
+            const double x = scale * dot(q + i * D, k + j * D, D);
+            s[j] = score_mod(sc, x, i + p->q_off, j, NULL);
+            dp[j] = dot(dout + i * D, v + j * D, D);
+            if (s[j] > m) m = s[j];
+            ++nvis;
+        }
+        if (nvis == 0) continue;
+        double l = 0.0;
+        for (int64_t j = 0; j < kv_len; ++j)
+            if (vis[j]) l += exp(s[j] - m);
+        const double lse = m + log(l);
+        double delta = 0.0;
+        for (int64_t j = 0; j < kv_len; ++j)
+            if (vis[j]) delta += exp(s[j] - lse) * dp[j];
+        for (int64_t j = 0; j < kv_len; ++j) {
+            if (!vis[j]) continue;
+            grad[bias_entry(sc, i + p->q_off, j)] += exp(s[j] - lse) * (dp[j] - delta);
+        }
+    }
+    free(s);
+    free(dp);
+    free(vis);
 }

@@ -650,6 +650,113 @@ def test_score_param_grad_vanishes_where_out_cannot_move():
     assert oracle.score_param_grad_head(q, k, v, do, diag, ("alibi", [0.2]), 0, 0.2) == 0.0
 
 
+# ------------------------------------------------- learned relative-position bias
+
+def _alibi_table(slope, d0, L):
+    """The bias table that reproduces ALiBi: entry t (distance d0 + t) = -slope (d0 + t)."""
+    return np.array([[-slope * (d0 + t) for t in range(L)]], dtype=np.float32)
+
+
+@pytest.mark.parametrize("d0,L,off", [(0, 64, 0), (-5, 80, 0), (-2, 70, 37)])
+def test_relbias_with_alibi_distances_is_alibi(d0, L, off):
+    """A table holding -slope * distance over every visible distance is ALiBi
+    (tutorial Pattern 3): forward and backward of the two score mods agree, with
+    query rows at an offset too.  A sign slip (j - i), a shifted first distance or
+    a missing q_offset in the bias fails this."""
+    S, kv_len, D = 50, 90, 16
+    q, k, v, do = _qkv(S, D, 60, kv_len=kv_len)
+    prog = oracle.Program(P(("causal",), ("window", 60), ("and",)), q_offset=off)
+    slope, scale = 0.3125, 0.4
+    rb, al = ("relbias", _alibi_table(slope, d0, L), d0), ("alibi", [slope])
+    o1, l1 = oracle.forward_head(q, k, v, prog, rb, 0, scale)
+    o2, l2 = oracle.forward_head(q, k, v, prog, al, 0, scale)
+    np.testing.assert_allclose(o1, o2, atol=1e-12)
+    np.testing.assert_allclose(l1, l2, atol=1e-12)
+    for a, b in zip(oracle.backward_head(q, k, v, do, prog, rb, 0, scale)[:3],
+                    oracle.backward_head(q, k, v, do, prog, al, 0, scale)[:3]):
+        np.testing.assert_allclose(a, b, atol=1e-12)
+
+
+def test_relbias_gradient_contracts_to_the_alibi_slope_gradient():
+    """With table[t] = -slope (d0 + t), dL/dslope = sum_t dL/dtable[t] * (-(d0 + t)):
+    the table gradient and the independently written slope gradient agree."""
+    S, D, d0, L = 70, 16, -3, 90
+    q, k, v, do = _qkv(S, D, 61)
+    docs = make_doc_ids(("geometric", 20.0), S, 62)[0]
+    prog = oracle.Program(P(("causal",), ("same_doc",), ("and",), ("sink", 4), ("or",)), doc_row=docs)
+    slope, scale = 0.25, 0.5
+    g = oracle.bias_grad_head(q, k, v, do, prog, ("relbias", _alibi_table(slope, d0, L), d0), 0, scale)
+    gs = oracle.score_param_grad_head(q, k, v, do, prog, ("alibi", [slope]), 0, scale)
+    contracted = float((g * -(d0 + np.arange(L))).sum())
+    assert abs(gs) > 1e-3
+    assert abs(contracted - gs) < 1e-10 * max(1.0, abs(gs)), (contracted, gs)
+
+
+def test_relbias_constant_table_shifts_lse_only():
+    """A constant bias c leaves the softmax (out) unchanged and adds c to LSE; the
+    table gradient of any table sums to zero (softmax is shift invariant: the
+    row sums of P (dP - Delta) vanish)."""
+    S, D, c = 80, 16, 1.75
+    q, k, v, do = _qkv(S, D, 63)
+    prog = oracle.Program(P(("causal",), ("window", 30), ("and",)))
+    o0, l0 = oracle.forward_head(q, k, v, prog, ("none",), 0, 0.3)
+    o1, l1 = oracle.forward_head(q, k, v, prog, ("relbias", np.full((1, 12), c, np.float32), 4), 0, 0.3)
+    np.testing.assert_allclose(o1, o0, atol=1e-12)
+    np.testing.assert_allclose(l1, l0 + c, atol=1e-12)
+    table = np.random.default_rng(64).normal(size=(1, 25)).astype(np.float32)
+    g = oracle.bias_grad_head(q, k, v, do, prog, ("relbias", table, 2), 0, 0.3)
+    assert np.abs(g).max() > 1e-3
+    assert abs(g.sum()) < 1e-10
+
+
+def test_relbias_gradient_finite_differences():
+    """dL/dtable against central differences of L = sum(out * dO) through the
+    oracle forward, at an interior entry and at both end entries (which collect
+    every distance outside the table)."""
+    S, D, d0, L = 60, 16, 3, 20
+    q, k, v, do = _qkv(S, D, 65)
+    prog = oracle.Program(P(("window", 40), ("sink", 5), ("or",)))  # distances below d0 and past the end
+    table = np.random.default_rng(66).normal(scale=0.5, size=(1, L)).astype(np.float32)
+    scale = 0.45
+    g = oracle.bias_grad_head(q, k, v, do, prog, ("relbias", table, d0), 0, scale)
+    eps = 2.0 ** -12  # table entries are fp32: +- eps stays exact for these magnitudes
+    for t in (0, 7, L - 1):
+        def loss(delta):
+            tb = table.copy()
+            tb[0, t] += delta
+            o, _ = oracle.forward_head(q, k, v, prog, ("relbias", tb, d0), 0, scale)
+            return float((o * do).sum())
+        num = (loss(eps) - loss(-eps)) / (2 * eps)
+        assert abs(g[t]) > 1e-4
+        assert abs(num - g[t]) < 1e-6 * max(1.0, abs(num)), (t, num, g[t])
+
+
+@pytest.mark.parametrize("off", [0, 25])
+def test_relbias_matches_numpy_twin(off):
+    """The C loops against the numpy twin (explicit mask, dense matrices, the
+    table gathered with np.clip): out, LSE, dq, dk, dv and the table gradient,
+    on a mask with distances on both sides of a short table."""
+    S, kv_len, D, d0, L = 40, 90, 16, -4, 30
+    q, k, v, do = _qkv(S, D, 67, kv_len=kv_len)
+    docs = make_doc_ids(("geometric", 25.0), kv_len, 68)[0]
+    mask = P(("same_doc",), ("window", 45), ("and",))  # no causal: negative distances too
+    prog = oracle.Program(mask, doc_row=docs, q_offset=off)
+    table = np.random.default_rng(69).normal(scale=0.7, size=(1, L)).astype(np.float32)
+    sc = ("relbias", table, d0)
+    th = table[0].astype(np.float64)
+    M = oracle.np_mask(mask, S, kv_len, doc_row=docs, q_offset=off)
+    out, lse = oracle.forward_head(q, k, v, prog, sc, 0, 0.35)
+    ro, rl, _ = oracle.np_forward(q, k, v, M, ("relbias", th, d0), 0.0, 0.35, q_offset=off)
+    np.testing.assert_allclose(out, ro, atol=1e-12)
+    np.testing.assert_allclose(lse, rl, atol=1e-12)
+    for a, b in zip(oracle.backward_head(q, k, v, do, prog, sc, 0, 0.35)[:3],
+                    oracle.np_backward(q, k, v, do, M, ("relbias", th, d0), 0.0, 0.35, q_offset=off)):
+        np.testing.assert_allclose(a, b, atol=1e-12)
+    g = oracle.bias_grad_head(q, k, v, do, prog, sc, 0, 0.35)
+    np.testing.assert_allclose(g, oracle.np_bias_grad(q, k, v, do, M, th, d0, 0.35, q_offset=off), atol=1e-12)
+    assert (g != 0).sum() > L // 2
+
+
 # ------------------------------------------------- paged key / value cache
 
 def test_paged_gather_inverts_the_scatter_into_pages():
