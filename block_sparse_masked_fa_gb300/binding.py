@@ -29,7 +29,7 @@ _lib = ctypes.CDLL(LIB_PATH)
 
 MAX_NODES = 16
 MASK_OPS = {"true": 0, "causal": 1, "same_doc": 2, "window": 3, "sink": 4, "prefix": 5, "and": 6, "or": 7}
-SCORE_OPS = {"none": 0, "softcap": 1, "alibi": 2}
+SCORE_OPS = {"none": 0, "softcap": 1, "alibi": 2, "relbias": 3}
 STATUS = {0: "FA_OK", 1: "FA_ERR_INVALID_ARG", 2: "FA_ERR_UNSUPPORTED", 3: "FA_ERR_SHAPE",
           4: "FA_ERR_ALIGNMENT", 5: "FA_ERR_CUDA", 6: "FA_ERR_TIMEOUT", 7: "FA_ERR_DEVICE_CHECK",
           8: "FA_ERR_WORKSPACE"}
@@ -51,7 +51,8 @@ class MaskSpec(ctypes.Structure):
 
 
 class ScoreSpec(ctypes.Structure):
-    _fields_ = [("op", ctypes.c_int32), ("param", ctypes.c_void_p), ("param_grad", ctypes.c_void_p)]
+    _fields_ = [("op", ctypes.c_int32), ("param", ctypes.c_void_p), ("param_grad", ctypes.c_void_p),
+                ("bias_len", ctypes.c_int32), ("bias_d0", ctypes.c_int32)]
 
 
 class BlockMaskStruct(ctypes.Structure):
@@ -184,8 +185,10 @@ def make_mask_spec(nodes: Sequence[tuple], device=None, q_offset: int = 0):
     return spec, keep
 
 
-def make_score_spec(kind: str = "none", param=None, device=None):
-    """("none"), ("softcap", c), ("alibi", slopes[H]); param becomes a device fp32 tensor."""
+def make_score_spec(kind: str = "none", param=None, device=None, d0: int = 0):
+    """("none"), ("softcap", c), ("alibi", slopes[H]), ("relbias", table[H, L], d0) -- the
+    learned relative-position bias s = x + table[h, clamp(q_pos - kv_idx - d0, 0, L - 1)];
+    param becomes a device fp32 tensor."""
     device = device or torch.device("cuda", torch.cuda.current_device())
     s = ScoreSpec()
     s.op = SCORE_OPS[kind]
@@ -193,6 +196,10 @@ def make_score_spec(kind: str = "none", param=None, device=None):
     keep = []
     if kind != "none":
         t = param if isinstance(param, torch.Tensor) else torch.as_tensor(param, dtype=torch.float32)
+        if kind == "relbias":
+            if t.dim() != 2:
+                raise ValueError("the relbias table must be [H, L]")
+            s.bias_len, s.bias_d0 = int(t.shape[1]), int(d0)
         t = t.to(device=device, dtype=torch.float32).reshape(-1).contiguous()
         keep.append(t)
         s.param = t.data_ptr()
@@ -415,14 +422,21 @@ def _check_storage(q, tensors):
             raise ValueError(f"{name} is on {t.device}, q on {q.device}")
 
 
-def _score(score):
+def _score(score, H: int):
+    """The score spec of a score tuple, with its parameter's size checked against
+    the H heads the kernels index it by (a prebuilt (ScoreSpec, keep) pair is
+    taken as it is)."""
     if score is None:
         return make_score_spec("none")
     if isinstance(score, tuple) and isinstance(score[0], ScoreSpec):
         return score
     if isinstance(score, str):
         return make_score_spec(score)
-    return make_score_spec(score[0], score[1] if len(score) > 1 else None)
+    spec, keep = make_score_spec(score[0], score[1] if len(score) > 1 else None, d0=score[2] if len(score) > 2 else 0)
+    need = {"softcap": 1, "alibi": H, "relbias": H * spec.bias_len}.get(score[0], 0)
+    if keep and keep[0].numel() != need:
+        raise ValueError(f"{score[0]} parameter has {keep[0].numel()} values, {need} needed for {H} heads")
+    return spec, keep
 
 
 def fa_forward(q, k, v, block_mask: BlockMask, score=None, scale: float = 0.0, out=None, lse=None, stream=None):
@@ -435,7 +449,7 @@ def fa_forward(q, k, v, block_mask: BlockMask, score=None, scale: float = 0.0, o
     if lse is None:
         lse = torch.empty(B, H, q_len, dtype=torch.float32, device=q.device)
     _check_storage(q, (("k", k, _BF16), ("v", v, _BF16), ("out", out, _BF16), ("lse", lse, _F32)))
-    sspec, keep = _score(score)
+    sspec, keep = _score(score, H)
     _check(_lib.fa_forward(_ptr(q), _ptr(k), _ptr(v), B, H, q_len, kv_len, D, ctypes.byref(block_mask.struct),
                            ctypes.byref(sspec), float(scale), _ptr(out), _ptr(lse), _stream(stream)), "fa_forward")
     return out, lse
@@ -443,14 +457,17 @@ def fa_forward(q, k, v, block_mask: BlockMask, score=None, scale: float = 0.0, o
 
 def _backward_score(score, score_param_grad, H: int):
     """Score spec for the backward: a copy of the caller's, with the device
-    pointer of ``score_param_grad`` (fp32 [H], receives dL/dslope for ALiBi)."""
-    sspec, keep = _score(score)
+    pointer of ``score_param_grad`` (fp32, receives dL/dslope [H] for ALiBi or
+    dL/dtable [H, L] for the learned relative-position bias)."""
+    sspec, keep = _score(score, H)
     spec = ScoreSpec()
     spec.op, spec.param, spec.param_grad = sspec.op, sspec.param, None
+    spec.bias_len, spec.bias_d0 = sspec.bias_len, sspec.bias_d0
     if score_param_grad is not None:
         g = score_param_grad
-        if g.dtype != torch.float32 or not g.is_cuda or not g.is_contiguous() or g.numel() != H:
-            raise ValueError("score_param_grad must be a contiguous fp32 CUDA tensor of H elements")
+        n = H * sspec.bias_len if sspec.op == SCORE_OPS["relbias"] else H
+        if g.dtype != torch.float32 or not g.is_cuda or not g.is_contiguous() or g.numel() != n:
+            raise ValueError(f"score_param_grad must be a contiguous fp32 CUDA tensor of {n} elements")
         spec.param_grad = g.data_ptr()
     return spec, keep + [sspec]
 
@@ -475,7 +492,7 @@ def fa_forward_paged(q, k_pool, v_pool, page_table, block_mask: BlockMask, score
         lse = torch.empty(B, H, q_len, dtype=torch.float32, device=q.device)
     _check_storage(q, (("k_pool", k_pool, _BF16), ("v_pool", v_pool, _BF16), ("page_table", page_table, _I32),
                        ("out", out, _BF16), ("lse", lse, _F32)))
-    sspec, keep = _score(score)
+    sspec, keep = _score(score, H)
     _check(_lib.fa_forward_paged(_ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(page_table), k_pool.shape[1] // 128, B, H,
                                  q_len, kv_len, D, ctypes.byref(block_mask.struct), ctypes.byref(sspec), float(scale),
                                  _ptr(out), _ptr(lse), _stream(stream)), "fa_forward_paged")
@@ -528,7 +545,7 @@ def fa_forward_decode(q, k, v, block_mask: BlockMask, score=None, scale: float =
                                 device=q.device)
     _check_storage(q, (("k", k, _BF16), ("v", v, _BF16), ("page_table", page_table, _I32), ("out", out, _BF16),
                        ("lse", lse, _F32), ("workspace", workspace, _U8)))
-    sspec, keep = _score(score)
+    sspec, keep = _score(score, H)
     _check(_lib.fa_forward_decode(_ptr(q), _ptr(k), _ptr(v), _ptr(page_table), n_pages, B, H, q_len, kv_len, D,
                                   ctypes.byref(block_mask.struct), ctypes.byref(sspec), float(scale), _ptr(out),
                                   _ptr(lse), _ptr(workspace), workspace.numel(), _stream(stream)),
@@ -550,7 +567,8 @@ def _backward_tensors(k, v, out, lse, dout, dq, dk, dv):
 def fa_backward(q, k, v, out, lse, dout, block_mask: BlockMask, score=None, scale: float = 0.0,
                 dq=None, dk=None, dv=None, workspace=None, stream=None, score_param_grad=None):
     """dq, dk, dv (bf16, shaped like q, k, v); with ALiBi, ``score_param_grad``
-    (fp32 [H] CUDA tensor) receives dL/dslope of every head."""
+    (fp32 [H] CUDA tensor) receives dL/dslope of every head, and with the
+    learned relative-position bias (fp32 [H, L]) dL/dtable."""
     _check_shapes(q, kv=(("k", k), ("v", v), ("dk", dk), ("dv", dv)),
                   like_q=(("out", out), ("dout", dout), ("dq", dq)), lse=lse)
     B, H, q_len, D = q.shape

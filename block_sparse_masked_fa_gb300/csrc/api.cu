@@ -173,10 +173,13 @@ fa_status check_attn(int32_t B, int32_t H, int64_t q_len, int64_t kv_len, int32_
   if ((int64_t)B * H * ((kv_len + 127) / 128) > (int64_t)INT32_MAX) return FA_ERR_SHAPE;
   if (bm->status == nullptr || bm->row_order == nullptr) return FA_ERR_INVALID_ARG;
   if (score != nullptr) {
-    if (score->op < FA_S_NONE || score->op > FA_S_ALIBI) return FA_ERR_INVALID_ARG;
+    if (score->op < FA_S_NONE || score->op > FA_S_RELBIAS) return FA_ERR_INVALID_ARG;
     if (score->op != FA_S_NONE && (score->param == nullptr || !aligned4(score->param))) return FA_ERR_INVALID_ARG;
+    if (score->op == FA_S_RELBIAS && (score->bias_len < 1 || score->bias_len > (1 << 24) ||
+                                      score->bias_d0 < -(1 << 30) || score->bias_d0 > (1 << 30)))
+      return FA_ERR_INVALID_ARG;
     if (backward && score->param_grad != nullptr) {
-      if (score->op != FA_S_ALIBI) return FA_ERR_UNSUPPORTED;
+      if (score->op != FA_S_ALIBI && score->op != FA_S_RELBIAS) return FA_ERR_UNSUPPORTED;
       if (!aligned4(score->param_grad)) return FA_ERR_ALIGNMENT;
     }
   }
@@ -212,6 +215,10 @@ AttnArgs attn_args(int32_t B, int32_t H, int64_t q_len, int64_t kv_len, int32_t 
   a.score_op = score ? score->op : FA_S_NONE;
   a.score_param = score ? score->param : nullptr;
   a.param_grad = (backward && score) ? score->param_grad : nullptr;
+  if (score != nullptr && score->op == FA_S_RELBIAS) {
+    a.bias_len = score->bias_len;
+    a.bias_d0 = score->bias_d0;
+  }
   a.status = bm->status;
   a.mask = dm;
   a.kv_block = 128;

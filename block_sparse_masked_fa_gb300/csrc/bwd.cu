@@ -721,6 +721,8 @@ __global__ void __launch_bounds__(512, 1)
       }
       float slope_l2 = 0.f;
       if constexpr (SCORE == FA_S_ALIBI) slope_l2 = __ldg(p.score_param + cur.h) * kLog2e;
+      const float* bias_h = nullptr;  // RELBIAS: this head's table
+      if constexpr (SCORE == FA_S_RELBIAS) bias_h = p.score_param + (int64_t)cur.h * p.bias_len;
       const bool row_ok = j < p.kv_len;
       float2 pacc = make_float2(0.f, 0.f);  // PGRAD: this thread's share of dL/dslope[h] in this item
       for (int s = 0; s < n; ++s, ++g) {
@@ -784,6 +786,11 @@ __global__ void __launch_bounds__(512, 1)
         // ALiBi, log2 units: -slope (i + qoff - j) = -slope (i - 128 I) + slope (j - 128 I - qoff)
         float bj = 0.f;
         if constexpr (SCORE == FA_S_ALIBI) bj = slope_l2 * (float)(j - (I * 128 + qoff));
+        // learned bias: query column x of the tile (0..127) takes entry clamp(bq + x, 0, L - 1),
+        // bq = 128 I + q_offset - j - d0 held within [-128, L] (which changes no entry)
+        int bq = 0;
+        if constexpr (SCORE == FA_S_RELBIAS)
+          bq = (int)max((int64_t)-128, min((int64_t)I * 128 + qoff - j - p.bias_d0, (int64_t)p.bias_len));
 #pragma unroll
         for (int c2 = 0; c2 < 2; ++c2) {
           const int c = 2 * half + c2;  // 32-column chunk of the 128 query columns
@@ -804,6 +811,12 @@ __global__ void __launch_bounds__(512, 1)
             } else if constexpr (SCORE == FA_S_ALIBI) {
               // the stats carry -slope (i - 128 I) of each query row; the key's part is bj
               a = fma2(make_float2(sv[e], sv[e + 1]), make_float2(sc_l2, sc_l2), add2(nl, make_float2(bj, bj)));
+            } else if constexpr (SCORE == FA_S_RELBIAS) {
+              const int x = 32 * c + e;
+              const float2 bv = make_float2(__ldg(bias_h + min(max(bq + x, 0), p.bias_len - 1)),
+                                            __ldg(bias_h + min(max(bq + x + 1, 0), p.bias_len - 1)));
+              a = fma2(make_float2(sv[e], sv[e + 1]), make_float2(sc_l2, sc_l2),
+                       fma2(bv, make_float2(kLog2e, kLog2e), nl));
             } else {
               a = fma2(make_float2(sv[e], sv[e + 1]), make_float2(sc_l2, sc_l2), nl);
             }
@@ -838,7 +851,7 @@ __global__ void __launch_bounds__(512, 1)
             const float2 dsv = mul2(make_float2(pg[32 * c2 + e], pg[32 * c2 + e + 1]),
                                     add2(make_float2(dp[e], dp[e + 1]), nd));
             dk[e / 2] = pack_bf16x2(dsv.x, dsv.y);
-            if constexpr (PGRAD) {  // kept for the slope gradient below
+            if constexpr (PGRAD) {  // kept for the parameter gradient below
               pg[32 * c2 + e] = dsv.x;
               pg[32 * c2 + e + 1] = dsv.y;
             }
@@ -848,7 +861,15 @@ __global__ void __launch_bounds__(512, 1)
         fence_proxy_async_smem();
         tc_fence_before();
         mbar_arrive(b_pb);
-        if constexpr (PGRAD) {
+        if constexpr (PGRAD && SCORE == FA_S_RELBIAS) {
+          // dL/dbias[h][t] += dS of every pair mapped to entry t (ds/dbias = 1), once
+          // dS is handed over; for one column the 32 lanes' entries are consecutive
+          float* gh = p.param_grad + (int64_t)cur.h * p.bias_len;
+#pragma unroll
+          for (int e = 0; e < 64; ++e)
+            if (pg[e] != 0.f) atomicAdd(gh + min(max(bq + 64 * half + e, 0), p.bias_len - 1), pg[e]);
+        }
+        if constexpr (PGRAD && SCORE == FA_S_ALIBI) {
           // dL/dslope += dS * ds/dslope, ds/dslope = -(i - j) = j - i, once dS is
           // handed over (the dQ MMA does not wait for it)
           const float jb = (float)(j - (I * 128 + 64 * half + qoff));  // j - i of this half's first column (exact)
@@ -862,7 +883,7 @@ __global__ void __launch_bounds__(512, 1)
         if (s + 1 < n || kn < items) reinterpret_cast<float*>(&ctl->stats)[st_idx] = st_next;
         if (s + 1 == n && kn < items && r < p.mask.n) arg_s[r] = node_arg(p.mask, r, nxt_bm);
       }
-      if constexpr (PGRAD) {
+      if constexpr (PGRAD && SCORE == FA_S_ALIBI) {
         // the item's part of dL/dslope[h]: one atomic per warp (ok is uniform per half)
         if (ok) {
           float sum = pacc.x + pacc.y;
@@ -898,14 +919,14 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __grid_constant__ At
                                                       const __nv_bfloat16* __restrict__ dout,
                                                       const float* __restrict__ lse, float* __restrict__ stats,
                                                       float* __restrict__ dq_acc, int64_t rows, int64_t row_blocks,
-                                                      float* __restrict__ param_grad, int n_param_grad,
+                                                      float* __restrict__ param_grad, int64_t n_param_grad,
                                                       uint32_t* __restrict__ sched, __nv_bfloat16* __restrict__ dk,
                                                       __nv_bfloat16* __restrict__ dv) {
   const int q_len = p.q_len, nq = p.nq;
-  if (blockIdx.x == 0) {  // the main kernel adds into them
-    for (int k = threadIdx.x; k < n_param_grad; k += blockDim.x) param_grad[k] = 0.f;
-    if (threadIdx.x == 0) *sched = 0u;
-  }
+  // the main kernel adds into them
+  for (int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; k < n_param_grad; k += (int64_t)gridDim.x * blockDim.x)
+    param_grad[k] = 0.f;
+  if (blockIdx.x == 0 && threadIdx.x == 0) *sched = 0u;
   if ((int64_t)blockIdx.x >= row_blocks) {
     const int64_t t = (int64_t)blockIdx.x - row_blocks;  // (b * H + h) * nkv + J
     const int J = (int)(t % p.nkv);
@@ -977,7 +998,9 @@ cudaError_t launch_bwd_t(const AttnArgs& a, const BwdTensors& t, cudaStream_t st
   const int64_t row_blocks = (rows + 15) / 16;
   bwd_pre_kernel<D><<<(unsigned)(row_blocks + (int64_t)bh * a.nkv), 256, 0, stream>>>(
       a, static_cast<const __nv_bfloat16*>(t.out), static_cast<const __nv_bfloat16*>(t.dout), t.lse, t.stats,
-      t.dq_acc, rows, row_blocks, a.param_grad, PGRAD ? a.H : 0, t.sched, static_cast<__nv_bfloat16*>(t.dk),
+      t.dq_acc, rows, row_blocks, a.param_grad,
+      PGRAD ? (SCORE == FA_S_RELBIAS ? (int64_t)a.H * a.bias_len : (int64_t)a.H) : (int64_t)0, t.sched,
+      static_cast<__nv_bfloat16*>(t.dk),
       static_cast<__nv_bfloat16*>(t.dv));
 
   CUtensorMap mq, mk, mv, mdo, mdk, mdv;
@@ -1056,16 +1079,24 @@ cudaError_t test_hook_backward(int on) {
 
 cudaError_t launch_backward(const AttnArgs& a, const BwdTensors& t, cudaStream_t stream, bool* enc_failed) {
   *enc_failed = false;
-  const bool pgrad = a.score_op == FA_S_ALIBI && a.param_grad != nullptr;  // learned ALiBi slopes
+  const bool pgrad = a.param_grad != nullptr;  // learned ALiBi slopes or bias table (checked on the host)
   if (a.D == 64) {
     if (a.score_op == FA_S_SOFTCAP) return launch_bwd_t<64, FA_S_SOFTCAP, false>(a, t, stream, enc_failed);
-    if (pgrad) return launch_bwd_t<64, FA_S_ALIBI, true>(a, t, stream, enc_failed);
-    if (a.score_op == FA_S_ALIBI) return launch_bwd_t<64, FA_S_ALIBI, false>(a, t, stream, enc_failed);
+    if (a.score_op == FA_S_ALIBI)
+      return pgrad ? launch_bwd_t<64, FA_S_ALIBI, true>(a, t, stream, enc_failed)
+                   : launch_bwd_t<64, FA_S_ALIBI, false>(a, t, stream, enc_failed);
+    if (a.score_op == FA_S_RELBIAS)
+      return pgrad ? launch_bwd_t<64, FA_S_RELBIAS, true>(a, t, stream, enc_failed)
+                   : launch_bwd_t<64, FA_S_RELBIAS, false>(a, t, stream, enc_failed);
     return launch_bwd_t<64, FA_S_NONE, false>(a, t, stream, enc_failed);
   }
   if (a.score_op == FA_S_SOFTCAP) return launch_bwd_t<128, FA_S_SOFTCAP, false>(a, t, stream, enc_failed);
-  if (pgrad) return launch_bwd_t<128, FA_S_ALIBI, true>(a, t, stream, enc_failed);
-  if (a.score_op == FA_S_ALIBI) return launch_bwd_t<128, FA_S_ALIBI, false>(a, t, stream, enc_failed);
+  if (a.score_op == FA_S_ALIBI)
+    return pgrad ? launch_bwd_t<128, FA_S_ALIBI, true>(a, t, stream, enc_failed)
+                 : launch_bwd_t<128, FA_S_ALIBI, false>(a, t, stream, enc_failed);
+  if (a.score_op == FA_S_RELBIAS)
+    return pgrad ? launch_bwd_t<128, FA_S_RELBIAS, true>(a, t, stream, enc_failed)
+                 : launch_bwd_t<128, FA_S_RELBIAS, false>(a, t, stream, enc_failed);
   return launch_bwd_t<128, FA_S_NONE, false>(a, t, stream, enc_failed);
 }
 

@@ -178,6 +178,8 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     const int qoff = (int)p.mask.q_off;
     float slope_l2 = 0.f, cap = 1.f;
     if constexpr (SCORE == FA_S_ALIBI) slope_l2 = __ldg(p.score_param + h) * kLog2e;
+    const float* bias_h = nullptr;  // RELBIAS: this head's table
+    if constexpr (SCORE == FA_S_RELBIAS) bias_h = p.score_param + (int64_t)h * p.bias_len;
     if constexpr (SCORE == FA_S_SOFTCAP) cap = __ldg(p.score_param);
 #pragma unroll
     for (int i = 0; i < QB; ++i) {
@@ -282,6 +284,10 @@ __global__ void __launch_bounds__(kDecThreads, 1)
               sc = cap * tanh_fast(x / cap) * kLog2e;
             } else if constexpr (SCORE == FA_S_ALIBI) {
               sc = fmaf(x, kLog2e, -slope_l2 * (float)(i + qoff - j));
+            } else if constexpr (SCORE == FA_S_RELBIAS) {  // entry clamp(q_pos - j - d0, 0, L - 1)
+              const int64_t d = (int64_t)(i + qoff) - j - p.bias_d0;
+              const int te = (int)max((int64_t)0, min(d, (int64_t)p.bias_len - 1));
+              sc = (x + __ldg(bias_h + te)) * kLog2e;
             } else {
               sc = x * kLog2e;
             }
@@ -490,10 +496,12 @@ cudaError_t launch_decode(const AttnArgs& a, const FwdTensors& t, void* workspac
   if (a.D == 64) {
     if (a.score_op == FA_S_SOFTCAP) return launch_decode_q<64, FA_S_SOFTCAP>(a, t, ws, splits, stream, enc_failed);
     if (a.score_op == FA_S_ALIBI) return launch_decode_q<64, FA_S_ALIBI>(a, t, ws, splits, stream, enc_failed);
+    if (a.score_op == FA_S_RELBIAS) return launch_decode_q<64, FA_S_RELBIAS>(a, t, ws, splits, stream, enc_failed);
     return launch_decode_q<64, FA_S_NONE>(a, t, ws, splits, stream, enc_failed);
   }
   if (a.score_op == FA_S_SOFTCAP) return launch_decode_q<128, FA_S_SOFTCAP>(a, t, ws, splits, stream, enc_failed);
   if (a.score_op == FA_S_ALIBI) return launch_decode_q<128, FA_S_ALIBI>(a, t, ws, splits, stream, enc_failed);
+  if (a.score_op == FA_S_RELBIAS) return launch_decode_q<128, FA_S_RELBIAS>(a, t, ws, splits, stream, enc_failed);
   return launch_decode_q<128, FA_S_NONE>(a, t, ws, splits, stream, enc_failed);
 }
 

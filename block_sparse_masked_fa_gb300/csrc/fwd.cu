@@ -445,7 +445,7 @@ __global__ void __launch_bounds__(192, 2)
       ok = named_bar_and(1, 128, ok && warp_wait(smem_u32(&ctl->desc_full[dsl]), (v >> 1) & 1, &ctl->abort));
       if (!ok) break;
       const FwdItem cur = ctl->desc[dsl];
-      const int n = cur.n, n_full = cur.n_full, I = cur.I, bh = cur.bh, bm = cur.bm;
+      const int n = cur.n, I = cur.I, bh = cur.bh, bm = cur.bm;
       const int i = I * 128 + r;
       // the row's position in the sequence the program describes (rows past
       // q_len, which store nothing, take the last row's)
@@ -487,6 +487,8 @@ __global__ void __launch_bounds__(192, 2)
         slope_l2 = slope * kLog2e;
         slope_sc = slope / p.scale;
       }
+      const float* bias_h = nullptr;  // RELBIAS: this head's table
+      if constexpr (SCORE == FA_S_RELBIAS) bias_h = p.score_param + (int64_t)cur.h * p.bias_len;
 
       float m = -INFINITY;  // reference maximum, log2 units
       float l = 0.f;
@@ -566,6 +568,17 @@ __global__ void __launch_bounds__(192, 2)
         if constexpr (SCORE == FA_S_ALIBI) {
   #pragma unroll
           for (int e = 0; e < BK; ++e) s[e] = fmaf(slope_sc, (float)e, s[e]);
+        }
+        // Learned bias: column e's entry is clamp(b - e, 0, L - 1) with b the
+        // distance q_pos - j0 - d0 (held within [-BK, L + BK], which changes no
+        // entry, so that the per-column arithmetic stays in 32 bits); it joins S
+        // in place in units of the scaled logit, like ALiBi's column term.
+        if constexpr (SCORE == FA_S_RELBIAS) {
+          const int64_t bb = ipos - j0 - p.bias_d0;
+          const int b = (int)max((int64_t)-BK, min(bb, (int64_t)p.bias_len + BK));
+          const float inv_scale = 1.0f / p.scale;
+  #pragma unroll
+          for (int e = 0; e < BK; ++e) s[e] = fmaf(__ldg(bias_h + min(max(b - e, 0), p.bias_len - 1)), inv_scale, s[e]);
         }
         // -- row maximum in log2 units (4 independent chains)
         float mx;
@@ -773,10 +786,12 @@ cudaError_t launch_forward_bk(const AttnArgs& a, const FwdTensors& t, cudaStream
   if (a.D == 64) {
     if (a.score_op == FA_S_SOFTCAP) return launch_fwd_t<64, FA_S_SOFTCAP, BK>(a, t, stream, enc_failed);
     if (a.score_op == FA_S_ALIBI) return launch_fwd_t<64, FA_S_ALIBI, BK>(a, t, stream, enc_failed);
+    if (a.score_op == FA_S_RELBIAS) return launch_fwd_t<64, FA_S_RELBIAS, BK>(a, t, stream, enc_failed);
     return launch_fwd_t<64, FA_S_NONE, BK>(a, t, stream, enc_failed);
   }
   if (a.score_op == FA_S_SOFTCAP) return launch_fwd_t<128, FA_S_SOFTCAP, BK>(a, t, stream, enc_failed);
   if (a.score_op == FA_S_ALIBI) return launch_fwd_t<128, FA_S_ALIBI, BK>(a, t, stream, enc_failed);
+  if (a.score_op == FA_S_RELBIAS) return launch_fwd_t<128, FA_S_RELBIAS, BK>(a, t, stream, enc_failed);
   return launch_fwd_t<128, FA_S_NONE, BK>(a, t, stream, enc_failed);
 }
 

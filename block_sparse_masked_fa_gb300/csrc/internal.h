@@ -101,7 +101,8 @@ struct AttnArgs {
   float scale;
   int32_t score_op;
   const float* score_param;
-  float* param_grad;  // backward only: dL/dslope[H] (ALiBi), or null
+  float* param_grad;  // backward only: dL/dslope[H] (ALiBi), dL/dbias[H][bias_len] (RELBIAS), or null
+  int32_t bias_len, bias_d0;  // RELBIAS: table length per head, distance of entry 0
   // forward only: paged keys / values -- page of logical key tile J of batch b
   // at page_table[b * nkv + J], pages of 128 rows in [H][n_pages * 128][D] pools; or null
   const int32_t* page_table;

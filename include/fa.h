@@ -116,19 +116,33 @@ typedef struct {
  *   FA_S_NONE     s = x                                 param: NULL
  *   FA_S_SOFTCAP  s = c * tanh(x / c)                   param: device fp32 c (1 value), c > 0
  *   FA_S_ALIBI    s = x - slope[h] * (q_idx - kv_idx)   param: device fp32 slopes [H]
+ *   FA_S_RELBIAS  s = x + bias[h][t],                   param: device fp32 table [H][bias_len]
+ *                 t = clamp(q_idx - kv_idx - bias_d0, 0, bias_len - 1)
+ * FA_S_RELBIAS is a learned relative-position bias (Pattern 3: "a learned
+ * relative-position bias trains"): one entry per query-minus-key distance from
+ * bias_d0 to bias_d0 + bias_len - 1, distances outside that range taking the
+ * nearest end entry.  q_idx is the query's position (row + the mask program's
+ * q_offset), as for ALiBi and the mask atoms.
  * ---------------------------------------------------------------------- */
-typedef enum { FA_S_NONE = 0, FA_S_SOFTCAP = 1, FA_S_ALIBI = 2 } fa_score_op;
+typedef enum { FA_S_NONE = 0, FA_S_SOFTCAP = 1, FA_S_ALIBI = 2, FA_S_RELBIAS = 3 } fa_score_op;
 
 typedef struct {
   int32_t op;          /* fa_score_op */
   const float* param;  /* device pointer, see the table */
-  /* fa_backward / fa_backward_noalloc only (fa_forward ignores it): device fp32
-   * [H] receiving dL/dslope[h] of L = sum(out * dO) for FA_S_ALIBI -- learned
-   * slopes (tutorial Pattern 3: a learned relative-position bias trains
-   * through the fused backward) -- overwritten, not accumulated; or NULL for
-   * no parameter gradient.  Non-NULL with another op: FA_ERR_UNSUPPORTED (the
-   * soft-cap constant is not a learned parameter on the pages). */
+  /* fa_backward / fa_backward_noalloc only (fa_forward ignores it): the
+   * gradient of L = sum(out * dO) with respect to the score mod's learned
+   * parameter (tutorial Pattern 3: a learned relative-position bias trains
+   * through the fused backward), overwritten, not accumulated -- device fp32
+   * [H] receiving dL/dslope[h] for FA_S_ALIBI, or [H][bias_len] receiving
+   * dL/dbias[h][t] for FA_S_RELBIAS; or NULL for no parameter gradient.
+   * Non-NULL with another op: FA_ERR_UNSUPPORTED (the soft-cap constant is not
+   * a learned parameter on the pages). */
   float* param_grad;
+  /* FA_S_RELBIAS only: the table's length per head, in [1, 2^24]
+   * (FA_ERR_INVALID_ARG otherwise), and the distance of its entry 0, in
+   * [-2^30, 2^30]. */
+  int32_t bias_len;
+  int32_t bias_d0;
 } fa_score_spec;
 
 /* ------------------------------------------------------------------------

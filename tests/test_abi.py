@@ -253,8 +253,8 @@ def test_forward_decode_rejects():
 
 
 def test_score_param_grad_rejects():
-    """A gradient buffer for the score parameter: ALiBi only, 4-byte aligned;
-    the forward ignores it."""
+    """A gradient buffer for the score parameter: ALiBi slopes (and the learned
+    bias table) only, 4-byte aligned; the forward ignores it."""
     bm = _bm()
     base = [FAKE] * 6 + [1, 1, 1024, 1024, 64, ctypes.byref(bm)]
     for op, grad, want in ((0, FAKE, UNSUPPORTED), (1, FAKE, UNSUPPORTED), (2, FAKE + 2, ALIGN)):
@@ -269,6 +269,24 @@ def test_score_param_grad_rejects():
     sc.param_grad = FAKE
     assert B._lib.fa_backward(*(base + [ctypes.byref(sc), -1.0] + [FAKE] * 4), 1 << 30, None) == UNSUPPORTED
     assert _fwd(score=sc, scale=-1.0) == INVALID
+
+
+def test_relbias_table_arguments_checked():
+    """The learned bias: a table pointer, a length in [1, 2^24] and a first
+    distance in [-2^30, 2^30]; its gradient buffer 4-byte aligned."""
+    for length, d0, want in ((0, 0, INVALID), ((1 << 24) + 1, 0, INVALID), (10, (1 << 30) + 1, INVALID),
+                             (10, -(1 << 30) - 1, INVALID)):
+        sc = B.ScoreSpec()
+        sc.op, sc.param, sc.bias_len, sc.bias_d0 = 3, FAKE, length, d0
+        assert _fwd(score=sc) == want
+    sc = B.ScoreSpec()
+    sc.op, sc.param, sc.bias_len = 3, None, 10
+    assert _fwd(score=sc) == INVALID
+    bm = _bm()
+    base = [FAKE] * 6 + [1, 1, 1024, 1024, 64, ctypes.byref(bm)]
+    sc = B.ScoreSpec()
+    sc.op, sc.param, sc.param_grad, sc.bias_len = 3, FAKE, FAKE + 2, 10
+    assert B._lib.fa_backward(*(base + [ctypes.byref(sc), 0.0] + [FAKE] * 4), 1 << 30, None) == ALIGN
 
 
 def test_status_calls_reject_null():
