@@ -554,14 +554,18 @@ __global__ void __launch_bounds__(256) coarsen_kernel(const uint8_t* __restrict_
 }
 
 // Work order: block 0 orders the rows (forward), block 1 the columns
-// (backward), longest first so that long lists do not end the grid.  The
-// forward's rows are sorted by exact count.  For the backward, exact count
-// order scatters neighbouring tiles when counts are noisy (document masks)
-// and loses the L2 reuse of Q / dO and of the dq accumulator, so its key is
-// the count quantized to q = ceil(cmax / 16) (cmax: the largest count), with
-// everything in one bucket (index order) when cmax <= 16.  A stable counting
-// sort keeps index order inside each bucket.  The histogram has kOrderBuckets
-// entries; coarser buckets are used if the counts would need more.
+// (backward), longest first so that long lists do not end the grid.  Rows /
+// columns go in chunks of 32 neighbours (one warp), the chunks ordered by
+// their longest count and, inside a chunk, the entries longest first (index
+// order among equals), so that neighbouring tiles, which share most of their
+// key (query) tiles under a window, run in the same few waves of CTAs and
+// share those tiles in L2; sorting every entry by its own count scatters them
+// when counts are noisy (document masks).  Counts are exact for the forward
+// and quantized to q = ceil(cmax / 16) for the backward (cmax: the largest
+// count), with everything in one bucket when cmax <= 16.  A stable counting
+// sort over the chunk keys keeps chunks in index order inside each bucket.
+// The histogram has kOrderBuckets entries; coarser buckets are used if the
+// counts would need more.
 constexpr int kOrderBuckets = 4096;
 
 __global__ void __launch_bounds__(1024) order_kernel(const __grid_constant__ ListJob j) {
@@ -589,8 +593,16 @@ __global__ void __launch_bounds__(1024) order_kernel(const __grid_constant__ Lis
   const int nb = top + 1;
   for (int k = threadIdx.x; k < nb; k += blockDim.x) hist[k] = 0;
   __syncthreads();
-  for (int r = threadIdx.x; r < n; r += blockDim.x)
-    atomicAdd(&hist[top - min((num[r] + full_num[r]) / qz, top)], 1);
+  // the bucket of entry r: its chunk's (this warp's 32 entries') longest count
+  auto chunk_bucket = [&](int r) {
+    const int key = __reduce_max_sync(0xffffffffu, r < n ? num[r] + full_num[r] : 0);
+    return top - min(key / qz, top);
+  };
+  for (int round = 0; round < n; round += blockDim.x) {
+    const int r = round + threadIdx.x;
+    const int bucket = chunk_bucket(r);
+    if (r < n) atomicAdd(&hist[bucket], 1);
+  }
   __syncthreads();
   // exclusive scan, one warp
   if (warp == 0) {
@@ -610,12 +622,19 @@ __global__ void __launch_bounds__(1024) order_kernel(const __grid_constant__ Lis
   }
   __syncthreads();
   // scatter in index order: warps take their turn inside each round of blockDim items
-  const uint32_t lt = (1u << lane) - 1u;
   for (int round = 0; round < n; round += blockDim.x) {
     const int r = round + threadIdx.x;
     const bool valid = r < n;
-    const int bucket = valid ? top - min((num[r] + full_num[r]) / qz, top) : -1;
+    const int cb = chunk_bucket(r);
+    const int bucket = valid ? cb : -1;
     const uint32_t peers = __match_any_sync(0xffffffffu, bucket);
+    // rank inside the chunk: longer first, index order among equals
+    const int mine = valid ? (num[r] + full_num[r]) / qz : -1;
+    int rank = 0;
+    for (int l = 0; l < 32; ++l) {
+      const int other = __shfl_sync(0xffffffffu, mine, l);
+      rank += (((peers >> l) & 1u) && (other > mine || (other == mine && l < lane))) ? 1 : 0;
+    }
     const int leader = __ffs(peers) - 1;
     int off = 0;
     for (int w = 0; w < (int)(blockDim.x / 32); ++w) {
@@ -626,7 +645,7 @@ __global__ void __launch_bounds__(1024) order_kernel(const __grid_constant__ Lis
       __syncthreads();
     }
     off = __shfl_sync(0xffffffffu, off, leader);
-    if (valid) order[off + __popc(peers & lt)] = r;
+    if (valid) order[off + rank] = r;
   }
 }
 

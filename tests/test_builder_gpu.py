@@ -33,8 +33,10 @@ def compare(bm, cls, lists):
     np.testing.assert_array_equal(bm.tile_class().cpu().numpy(), cls.astype(np.uint8))
     for n in LIST_NAMES:
         np.testing.assert_array_equal(got[n], lists[n], err_msg=n)
-    # work orders: rows by exact count, columns by count quantized to ceil(cmax / 16)
-    # (one bucket when cmax <= 16); longest bucket first, index order inside a bucket
+    # work orders in chunks of 32 neighbours: chunks by their longest count (longest
+    # bucket first, index order inside a bucket), entries inside a chunk longest first
+    # (index order among equals); counts exact for rows, quantized to ceil(cmax / 16)
+    # for columns (one bucket when cmax <= 16)
     for field, n_key, f_key, quantized in (("row_order", "kv_num_blocks", "full_kv_num_blocks", False),
                                            ("col_order", "q_num_blocks", "full_q_num_blocks", True)):
         work = (got[n_key] + got[f_key]).reshape(-1)
@@ -42,7 +44,8 @@ def compare(bm, cls, lists):
         order = bm.buffer[off:off + 4 * work.size].view(torch.int32).cpu().numpy()
         cmax = int(work.max())
         qz = (cmax + 1 if cmax <= 16 else -(-cmax // 16)) if quantized else 1
-        expect = sorted(range(work.size), key=lambda r: (-(work[r] // qz), r))
+        chunk = np.array([work[(r // 32) * 32:(r // 32) * 32 + 32].max() for r in range(work.size)])
+        expect = sorted(range(work.size), key=lambda r: (-(chunk[r] // qz), r // 32, -(work[r] // qz), r))
         np.testing.assert_array_equal(order, np.array(expect), err_msg=field)
     assert fa.fa_get_status(bm) == 0
 
