@@ -139,11 +139,10 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const v
   return __all_sync(0xffffffffu, r);
 }
 
-__device__ __forceinline__ float tanh_fast(float t) {
-  const float e = ex2_approx(t * (2.0f * kLog2e));
+__device__ __forceinline__ float rcp_approx(float x) {
   float r;
-  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(1.0f + e));
-  return fmaf(-2.0f, r, 1.0f);
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
 }
 
 // Writes 32 bf16 values (16 packed words) of row r into a 128-byte-swizzled
@@ -670,11 +669,11 @@ __global__ void __launch_bounds__(512, 1)
     const uint64_t mask_ops = pack_ops(p.mask);
     const int qoff = (int)p.mask.q_off;  // query row i is position i + qoff (below 2^31: checked on the host)
     const float sc_l2 = p.scale * kLog2e;
-    float cap_l2 = 0.f, sc_over_cap = 0.f;
+    float cap_l2 = 0.f, sc_cap2 = 0.f;
     if constexpr (SCORE == FA_S_SOFTCAP) {
       const float cap = __ldg(p.score_param);
       cap_l2 = cap * kLog2e;
-      sc_over_cap = p.scale / cap;
+      sc_cap2 = (p.scale / cap) * (2.0f * kLog2e);  // S -> the exponent of e^{2 x / c}, base 2
     }
     // -LSE (log2 units) and -Delta of the query columns this half handles: one
     // value per thread of the half, copied into shared memory once per step;
@@ -805,9 +804,14 @@ __global__ void __launch_bounds__(512, 1)
             const float2 nl = (e % 4 == 0) ? make_float2(nlq.x, nlq.y) : make_float2(nlq.z, nlq.w);
             float2 a, gd = make_float2(1.0f, 1.0f);
             if constexpr (SCORE == FA_S_SOFTCAP) {
-              const float t0 = tanh_fast(sv[e] * sc_over_cap), t1 = tanh_fast(sv[e + 1] * sc_over_cap);
-              a = fma2(make_float2(cap_l2, cap_l2), make_float2(t0, t1), nl);
-              gd = fma2(make_float2(-t0, -t1), make_float2(t0, t1), make_float2(1.0f, 1.0f));
+              // tanh(t) = 1 - 2 r with r = 1 / (1 + e^{2t}): the score c tanh(x / c) log2(e)
+              // = c log2(e) - 2 c log2(e) r (the stats carry the c log2(e)), and
+              // 1 - tanh^2 = 4 r (1 - r); packed in pairs
+              const float2 u = mul2(make_float2(sv[e], sv[e + 1]), make_float2(sc_cap2, sc_cap2));
+              const float2 d = add2(make_float2(ex2_approx(u.x), ex2_approx(u.y)), make_float2(1.0f, 1.0f));
+              const float2 rr = make_float2(rcp_approx(d.x), rcp_approx(d.y));
+              a = fma2(rr, make_float2(-2.0f * cap_l2, -2.0f * cap_l2), nl);
+              gd = mul2(fma2(make_float2(-rr.x, -rr.y), rr, rr), make_float2(4.0f, 4.0f));
             } else if constexpr (SCORE == FA_S_ALIBI) {
               // the stats carry -slope (i - 128 I) of each query row; the key's part is bj
               a = fma2(make_float2(sv[e], sv[e + 1]), make_float2(sc_l2, sc_l2), add2(nl, make_float2(bj, bj)));
@@ -907,7 +911,8 @@ __global__ void __launch_bounds__(512, 1)
 // Per query row: -LSE * log2(e) and -Delta (Delta_i = dO_i . out_i, fp32)
 // into the per-tile stats array [B*H][nq][2][128] -- with ALiBi the first also
 // carries the query row's part of the bias within its tile, -slope_h (i - 128 I)
-// log2(e), so that the main kernel adds only the key's part -- zero for the rows past
+// log2(e), so that the main kernel adds only the key's part, and with the
+// soft-cap the constant term c log2(e) of c tanh(x / c) log2(e) -- zero for the rows past
 // q_len in the last tile; the fp32 dq accumulator rows, the score parameter's
 // gradient (if requested) and the main kernel's item counter set to zero.
 // 16 threads per row, 16 rows per 256-thread block; the blocks after the rows'
@@ -968,6 +973,7 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __grid_constant__ At
     float* st = stats + (bh * nq + i / 128) * 256;
     float nl = -__ldg(lse + row) * kLog2e;
     if (p.score_op == FA_S_ALIBI) nl -= (__ldg(p.score_param + (int)(bh % p.H)) * kLog2e) * (float)(i % 128);
+    if (p.score_op == FA_S_SOFTCAP) nl += __ldg(p.score_param) * kLog2e;  // the soft-cap's constant term
     st[i % 128] = nl;
     st[128 + i % 128] = -acc;
     if (i == q_len - 1)  // rows past q_len in the last tile

@@ -137,6 +137,11 @@ __device__ __forceinline__ float tanh_fast(float t) {
   asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(1.0f + e));
   return fmaf(-2.0f, r, 1.0f);
 }
+__device__ __forceinline__ float rcp_approx(float x) {
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
 
 __device__ __forceinline__ FwdItem fwd_item(const AttnArgs& p, int k) {
   const int rep = (p.B / p.Bm) * (p.H / p.Hm);
@@ -429,11 +434,12 @@ __global__ void __launch_bounds__(192, 2)
     const uint32_t tO = tmem + lane_off + 128;
     const uint64_t mask_ops = pack_ops(p.mask);
     const float sc_l2 = p.scale * kLog2e;  // logit -> log2 units
-    float cap_l2 = 0.f, sc_over_cap = 0.f;
+    float cap_l2 = 0.f, sc_over_cap = 0.f, sc_cap2 = 0.f;
     if constexpr (SCORE == FA_S_SOFTCAP) {
       const float cap = __ldg(p.score_param);
       cap_l2 = cap * kLog2e;
       sc_over_cap = p.scale / cap;
+      sc_cap2 = sc_over_cap * (2.0f * kLog2e);  // S -> the exponent of e^{2 x / c}, base 2
     }
     int t = 0, u = 0, v = 0;
     bool ok = true;
@@ -623,9 +629,12 @@ __global__ void __launch_bounds__(192, 2)
             if constexpr (SCORE == FA_S_NONE) {
               return fma2(make_float2(s[e], s[e + 1]), make_float2(sc_l2, sc_l2), make_float2(-m_use, -m_use));
             } else if constexpr (SCORE == FA_S_SOFTCAP) {
-              float2 x = fma2(make_float2(cap_l2, cap_l2),
-                              make_float2(tanh_fast(s[e] * sc_over_cap), tanh_fast(s[e + 1] * sc_over_cap)),
-                              make_float2(-m_use, -m_use));
+              // c tanh(x / c) log2(e) - m with tanh(t) = 1 - 2 / (1 + e^{2t}):
+              // (c log2(e) - m) - 2 c log2(e) / (1 + 2^{S sc_cap2}), packed in pairs
+              const float2 u = mul2(make_float2(s[e], s[e + 1]), make_float2(sc_cap2, sc_cap2));
+              const float2 d = add2(make_float2(ex2_approx(u.x), ex2_approx(u.y)), make_float2(1.0f, 1.0f));
+              float2 x = fma2(make_float2(rcp_approx(d.x), rcp_approx(d.y)), make_float2(-2.0f * cap_l2, -2.0f * cap_l2),
+                              make_float2(cap_l2 - m_use, cap_l2 - m_use));
               if (msk) {
                 x.x = (s[e] == -INFINITY) ? -INFINITY : x.x;
                 x.y = (s[e + 1] == -INFINITY) ? -INFINITY : x.y;
