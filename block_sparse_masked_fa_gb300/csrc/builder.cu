@@ -327,18 +327,20 @@ __global__ void __launch_bounds__(256) row_segs_kernel(const __grid_constant__ B
 
 constexpr int kBuildWarps = 8;
 
-// One warp per (query-tile row, chunk of 32 key tiles): each lane classifies
-// one tile; undecided tiles are settled exactly by the whole warp.  Writes
-// the class bytes only; compaction into lists is a separate pass.
+// One warp per query-tile row.  The row's key tiles go in chunks of 32, one
+// chunk per lane first: the interval test of the program over the chunk's whole
+// key range (its document ids bounded by its tiles' summaries) proves most
+// chunks of a windowed or document mask EMPTY, and those are written as zeros.
+// The warp then classifies the other chunks one at a time, a tile per lane;
+// undecided tiles are settled exactly by the whole warp.  Writes the class
+// bytes only; compaction into lists is a separate pass.
 __global__ void __launch_bounds__(kBuildWarps * 32) classify_kernel(const __grid_constant__ BuildArgs a) {
   pdl_wait_then_release();
   __shared__ int32_t s_arg[kBuildWarps][FA_MAX_MASK_NODES];
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int nchunk = (a.nkv + 31) / 32;
-  const int64_t wid = (int64_t)blockIdx.x * kBuildWarps + warp;
-  if (wid >= (int64_t)a.Bm * a.Hm * a.nq * nchunk) return;
-  const int64_t row = wid / nchunk;  // (bm, hm, I)
-  const int c0 = (int)(wid % nchunk) * 32;
+  const int64_t row = (int64_t)blockIdx.x * kBuildWarps + warp;  // (bm, hm, I)
+  if (row >= (int64_t)a.Bm * a.Hm * a.nq) return;
   const int I = (int)(row % a.nq);
   const int bm = (int)(row / ((int64_t)a.Hm * a.nq));
   if (lane < a.mask.n) s_arg[warp][lane] = node_arg(a.mask, lane, bm);
@@ -358,72 +360,113 @@ __global__ void __launch_bounds__(kBuildWarps * 32) classify_kernel(const __grid
     q_mx = sm[1];
     q_run = sm[2];
   }
-  const int J = c0 + lane;
-  const bool valid = J < a.nkv;
-  int cls = 0, k3 = K_NONE;
-  if (valid) {
-    const int64_t j0 = (int64_t)J * a.block;
-    const int64_t j1 = min(j0 + a.block, a.kv_len) - 1;
-    int k_mn = 0, k_mx = 0, k_run = 0;
-    if (doc) {
-      const int32_t* sm = a.summary + (((int64_t)bm * 2 + 1) * tmax + J) * 4;
-      k_mn = sm[0];
-      k_mx = sm[1];
-      k_run = sm[2];
-    }
-    k3 = program_interval(a.mask, arg, i0 + a.mask.q_off, i1 + a.mask.q_off, j0, j1, q_mn, q_mx, q_run, k_mn, k_mx,
-                          k_run);
-    cls = (k3 == K_ALL) ? 2 : (k3 == K_PART ? 1 : 0);
-  }
-  uint32_t undecided = __ballot_sync(0xffffffffu, valid && k3 == K_SOME);
-  while (undecided) {
-    const int t = __ffs(undecided) - 1;
-    undecided &= undecided - 1;
-    const int64_t j0 = (int64_t)(c0 + t) * a.block;
-    const int64_t j1 = min(j0 + a.block, a.kv_len) - 1;
-    const int64_t rows = i1 - i0 + 1, cols = j1 - j0 + 1;
-    int cnt = 0;
-    const int64_t L = max(a.q_len, a.kv_len);
-    for (int64_t r = lane; r < rows; r += 32) {
-      const int64_t i = i0 + r;
-      // the row's visible columns as two intervals (row_segs_kernel ran first):
-      // its count inside the tile is two overlaps
-      const int4 sg = reinterpret_cast<const int4*>(a.row_segs)[((int64_t)bm * 2) * L + i];
-      if (sg.x >= 0) {
-        cnt += (int)(max((int64_t)0, min((int64_t)sg.y, j1 + 1) - max((int64_t)sg.x, j0)) +
-                     max((int64_t)0, min((int64_t)sg.w, j1 + 1) - max((int64_t)sg.z, j0)));
-        continue;
-      }
-      const int64_t ip = i + a.mask.q_off;  // the query's position
-      const int32_t doc_i = doc ? __ldg(doc + ip) : 0;
-      int run_lo = 0, run_hi = 0;
-      const bool use_run = doc != nullptr && doc_run(a.mask, bm, ip, run_lo, run_hi);
-      for (int64_t jc = j0; jc <= j1; jc += 32) {
-        auto eq = [&]() {
-          if (use_run) return range_bits(run_lo, run_hi, (int)jc);
-          uint32_t w = 0;
-          if (doc_vec && jc + 32 <= j1 + 1) {
-            const int4* dv = reinterpret_cast<const int4*>(doc + jc);  // same addresses in every lane
+  uint8_t* out = a.tile_class + row * a.nkv;
+  // chunk c: tiles [32 c, min(32 c + 32, nkv)); EMPTY as a whole when the test over its range says so
+  for (int cb = 0; cb < nchunk; cb += 32) {
+    const int c = cb + lane;
+    bool live = false;
+    if (c < nchunk) {
+      const int t0 = 32 * c, t1 = min(t0 + 32, a.nkv);
+      const int64_t j0 = (int64_t)t0 * a.block;
+      const int64_t j1 = min((int64_t)t1 * a.block, (int64_t)a.kv_len) - 1;
+      int k_mn = 0, k_mx = 0;
+      if (doc) {
+        k_mn = INT_MAX;
+        k_mx = INT_MIN;
+        const int32_t* ks = a.summary + (((int64_t)bm * 2 + 1) * tmax + t0) * 4;
 #pragma unroll
-            for (int q4 = 0; q4 < 8; ++q4) {
-              const int4 d = __ldg(dv + q4);
-              w |= (uint32_t)(d.x == doc_i) << (4 * q4) | (uint32_t)(d.y == doc_i) << (4 * q4 + 1) |
-                   (uint32_t)(d.z == doc_i) << (4 * q4 + 2) | (uint32_t)(d.w == doc_i) << (4 * q4 + 3);
-            }
-          } else {
-            const int64_t jn = min(jc + 32, j1 + 1);
-            for (int64_t j = jc; j < jn; ++j) w |= (uint32_t)(__ldg(doc + j) == doc_i) << (uint32_t)(j - jc);
+        for (int t = 0; t < 32; ++t) {  // all 32 loads in flight at once
+          if (t0 + t < t1) {
+            const int2 sm = __ldg(reinterpret_cast<const int2*>(ks + 4 * t));
+            k_mn = min(k_mn, sm.x);
+            k_mx = max(k_mx, sm.y);
           }
-          return w;
-        };
-        cnt += __popc(mask_word_rolled(a.mask.n, ops, arg, ip, jc, eq) & low_bits(j1 + 1 - jc));
+        }
+      }
+      // (no "every id occurs" claim for the chunk: SAME_DOC then decides only disjoint ranges)
+      live = program_interval(a.mask, arg, i0 + a.mask.q_off, i1 + a.mask.q_off, j0, j1, q_mn, q_mx, q_run, k_mn,
+                              k_mx, 0) != K_NONE;
+      if (!live) {
+        if (t1 - t0 == 32 && (reinterpret_cast<uintptr_t>(out + t0) & 15) == 0) {
+          reinterpret_cast<uint4*>(out + t0)[0] = make_uint4(0u, 0u, 0u, 0u);
+          reinterpret_cast<uint4*>(out + t0)[1] = make_uint4(0u, 0u, 0u, 0u);
+        } else {
+          for (int t = t0; t < t1; ++t) out[t] = 0;
+        }
       }
     }
-    const int total = (int)__reduce_add_sync(0xffffffffu, (unsigned)cnt);
-    const int c = (total == 0) ? 0 : ((int64_t)total == rows * cols ? 2 : 1);
-    if (lane == t) cls = c;
+    uint32_t live_mask = __ballot_sync(0xffffffffu, live);
+    while (live_mask) {
+      const int c0 = 32 * (cb + __ffs(live_mask) - 1);
+      live_mask &= live_mask - 1;
+      const int J = c0 + lane;
+      const bool valid = J < a.nkv;
+      int cls = 0, k3 = K_NONE;
+      if (valid) {
+        const int64_t j0 = (int64_t)J * a.block;
+        const int64_t j1 = min(j0 + a.block, a.kv_len) - 1;
+        int k_mn = 0, k_mx = 0, k_run = 0;
+        if (doc) {
+          const int32_t* sm = a.summary + (((int64_t)bm * 2 + 1) * tmax + J) * 4;
+          k_mn = sm[0];
+          k_mx = sm[1];
+          k_run = sm[2];
+        }
+        k3 = program_interval(a.mask, arg, i0 + a.mask.q_off, i1 + a.mask.q_off, j0, j1, q_mn, q_mx, q_run, k_mn, k_mx,
+                              k_run);
+        cls = (k3 == K_ALL) ? 2 : (k3 == K_PART ? 1 : 0);
+      }
+      uint32_t undecided = __ballot_sync(0xffffffffu, valid && k3 == K_SOME);
+      while (undecided) {
+        const int t = __ffs(undecided) - 1;
+        undecided &= undecided - 1;
+        const int64_t j0 = (int64_t)(c0 + t) * a.block;
+        const int64_t j1 = min(j0 + a.block, a.kv_len) - 1;
+        const int64_t rows = i1 - i0 + 1, cols = j1 - j0 + 1;
+        int cnt = 0;
+        const int64_t L = max(a.q_len, a.kv_len);
+        for (int64_t r = lane; r < rows; r += 32) {
+          const int64_t i = i0 + r;
+          // the row's visible columns as two intervals (row_segs_kernel ran first):
+          // its count inside the tile is two overlaps
+          const int4 sg = reinterpret_cast<const int4*>(a.row_segs)[((int64_t)bm * 2) * L + i];
+          if (sg.x >= 0) {
+            cnt += (int)(max((int64_t)0, min((int64_t)sg.y, j1 + 1) - max((int64_t)sg.x, j0)) +
+                         max((int64_t)0, min((int64_t)sg.w, j1 + 1) - max((int64_t)sg.z, j0)));
+            continue;
+          }
+          const int64_t ip = i + a.mask.q_off;  // the query's position
+          const int32_t doc_i = doc ? __ldg(doc + ip) : 0;
+          int run_lo = 0, run_hi = 0;
+          const bool use_run = doc != nullptr && doc_run(a.mask, bm, ip, run_lo, run_hi);
+          for (int64_t jc = j0; jc <= j1; jc += 32) {
+            auto eq = [&]() {
+              if (use_run) return range_bits(run_lo, run_hi, (int)jc);
+              uint32_t w = 0;
+              if (doc_vec && jc + 32 <= j1 + 1) {
+                const int4* dv = reinterpret_cast<const int4*>(doc + jc);  // same addresses in every lane
+#pragma unroll
+                for (int q4 = 0; q4 < 8; ++q4) {
+                  const int4 d = __ldg(dv + q4);
+                  w |= (uint32_t)(d.x == doc_i) << (4 * q4) | (uint32_t)(d.y == doc_i) << (4 * q4 + 1) |
+                       (uint32_t)(d.z == doc_i) << (4 * q4 + 2) | (uint32_t)(d.w == doc_i) << (4 * q4 + 3);
+                }
+              } else {
+                const int64_t jn = min(jc + 32, j1 + 1);
+                for (int64_t j = jc; j < jn; ++j) w |= (uint32_t)(__ldg(doc + j) == doc_i) << (uint32_t)(j - jc);
+              }
+              return w;
+            };
+            cnt += __popc(mask_word_rolled(a.mask.n, ops, arg, ip, jc, eq) & low_bits(j1 + 1 - jc));
+          }
+        }
+        const int total = (int)__reduce_add_sync(0xffffffffu, (unsigned)cnt);
+        const int c = (total == 0) ? 0 : ((int64_t)total == rows * cols ? 2 : 1);
+        if (lane == t) cls = c;
+      }
+      if (valid) out[J] = (uint8_t)cls;
+    }
   }
-  if (valid) a.tile_class[row * a.nkv + J] = (uint8_t)cls;
 }
 
 // Caller-chosen tiles (tutorial "FlexAttention in PyTorch": block-selection
@@ -475,16 +518,90 @@ __global__ void __launch_bounds__(kBuildWarps * 32) select_kernel(const __grid_c
   }
 }
 
-// Compaction of one class grid [Bm * Hm][n_r][n_c] into lists: warps [0, rows)
-// build the per-row lists, the next [0, cols) warps the per-column lists, both
-// with ballots over the class bytes (rows or columns without list pointers are
-// skipped).
+// Compaction of one class grid [planes][n_r][n_c] into lists, ascending, with
+// zero tails.  Warps [0, rows) build the per-row lists, the next [0, cols) warps
+// the per-column lists (rows or columns without list pointers are skipped).  A
+// row's class bytes are read 16 at a time by every lane when the grid's rows
+// are 16-byte aligned (n_c a multiple of 16), and its entries placed by a
+// prefix count over the lanes; otherwise, and for the columns, one byte a lane
+// with ballots.  The tails are written in 16-byte stores where the list allows.
+constexpr int kColGroup = 16;
+
+__device__ __forceinline__ bool compact_vec(const ListJob& j) {
+  return j.n_c % kColGroup == 0 && (reinterpret_cast<uintptr_t>(j.cls) & 15) == 0;
+}
+
+// byte k (0..15) of a 16-byte load
+__device__ __forceinline__ int byte_of(const uint4& v, int k) {
+  const uint32_t w = (k < 4) ? v.x : (k < 8) ? v.y : (k < 12) ? v.z : v.w;
+  return (int)((w >> (8 * (k & 3))) & 0xffu);
+}
+
+// list[from, n) = 0 by the 32 lanes, in 16-byte stores where the list allows
+__device__ __forceinline__ void zero_tail(int32_t* list, int from, int n, int lane) {
+  const int v0 = (from + 3) / 4, v1 = n / 4;  // the int4 groups [v0, v1) lie inside [from, n)
+  if ((reinterpret_cast<uintptr_t>(list) & 15) != 0 || v0 >= v1) {
+    for (int x = from + lane; x < n; x += 32) list[x] = 0;
+    return;
+  }
+  if (lane < 4 * v0 - from) list[from + lane] = 0;
+  for (int q = v0 + lane; q < v1; q += 32) reinterpret_cast<int4*>(list)[q] = make_int4(0, 0, 0, 0);
+  if (lane < n - 4 * v1) list[4 * v1 + lane] = 0;
+}
+
 __global__ void __launch_bounds__(kBuildWarps * 32) compact_kernel(const __grid_constant__ ListJob j) {
   pdl_wait_then_release();
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int64_t wid = (int64_t)blockIdx.x * kBuildWarps + warp;
   const int64_t rows = j.row_num ? (int64_t)j.planes * j.n_r : 0, cols = j.col_num ? (int64_t)j.planes * j.n_c : 0;
   if (wid >= rows + cols) return;
+  const uint32_t lt = (1u << lane) - 1u;
+  if (wid < rows && compact_vec(j)) {
+    // ---- row id: 512 tiles a round, 16 per lane
+    const int64_t id = wid;
+    const int n = j.n_c;
+    const uint8_t* rb = j.cls + id * n;
+    int32_t* part_idx = j.row_idx + id * n;
+    int32_t* full_idx = j.row_full_idx + id * n;
+    int n_part = 0, n_full = 0;
+    for (int s0 = 0; s0 < n; s0 += 32 * kColGroup) {
+      const int x0 = s0 + kColGroup * lane;
+      const uint4 v = (x0 < n) ? __ldg(reinterpret_cast<const uint4*>(rb + x0)) : make_uint4(0u, 0u, 0u, 0u);
+      int np = 0, nf = 0;
+#pragma unroll
+      for (int k = 0; k < kColGroup; ++k) {
+        const int b = byte_of(v, k);
+        np += (b == 1);
+        nf += (b == 2);
+      }
+      int ip = np, iF = nf;  // inclusive prefix counts over the lanes
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const int yp = __shfl_up_sync(0xffffffffu, ip, d), yf = __shfl_up_sync(0xffffffffu, iF, d);
+        if (lane >= d) {
+          ip += yp;
+          iF += yf;
+        }
+      }
+      int op = n_part + ip - np, of = n_full + iF - nf;
+#pragma unroll
+      for (int k = 0; k < kColGroup; ++k) {
+        const int b = byte_of(v, k);
+        if (b == 1) part_idx[op++] = x0 + k;
+        if (b == 2) full_idx[of++] = x0 + k;
+      }
+      n_part += __shfl_sync(0xffffffffu, ip, 31);
+      n_full += __shfl_sync(0xffffffffu, iF, 31);
+    }
+    zero_tail(part_idx, n_part, n, lane);
+    zero_tail(full_idx, n_full, n, lane);
+    if (lane == 0) {
+      j.row_num[id] = n_part;
+      j.row_full_num[id] = n_full;
+    }
+    return;
+  }
+  // ---- one byte at a time: a row (grid rows not 16-byte aligned) or a column per warp
   const bool by_row = wid < rows;
   const int64_t id = by_row ? wid : wid - rows;
   const int n = by_row ? j.n_c : j.n_r;                   // list length
@@ -497,9 +614,7 @@ __global__ void __launch_bounds__(kBuildWarps * 32) compact_kernel(const __grid_
   // class bytes of eight 32-tile chunks are loaded before any list entry is
   // stored: the stores (int32) could alias the bytes for the compiler, which
   // would otherwise keep each load behind the stores of the chunk before it
-  // (for a column, 32 cache lines a load)
   constexpr int kBatch = 8;
-  const uint32_t lt = (1u << lane) - 1u;
   for (int c0 = 0; c0 < n; c0 += 32 * kBatch) {
     int cls[kBatch];
 #pragma unroll
@@ -518,8 +633,8 @@ __global__ void __launch_bounds__(kBuildWarps * 32) compact_kernel(const __grid_
       n_full += __popc(fb);
     }
   }
-  for (int k = n_part + lane; k < n; k += 32) part_idx[k] = 0;
-  for (int k = n_full + lane; k < n; k += 32) full_idx[k] = 0;
+  zero_tail(part_idx, n_part, n, lane);
+  zero_tail(full_idx, n_full, n, lane);
   if (lane == 0) {
     (by_row ? j.row_num : j.col_num)[id] = n_part;
     (by_row ? j.row_full_num : j.col_full_num)[id] = n_full;
@@ -678,12 +793,11 @@ cudaError_t launch_build(const BuildArgs& a, cudaStream_t stream) {
   }
   const int64_t rows = (int64_t)a.Bm * a.Hm * a.nq;
   const int64_t cols = (int64_t)a.Bm * a.Hm * a.nkv;
-  const int64_t cwarps = rows * ((a.nkv + 31) / 32);
   if (a.sel_num != nullptr)
     e = launch_k(select_kernel, dim3((unsigned)((rows + kBuildWarps - 1) / kBuildWarps)), dim3(kBuildWarps * 32), 0,
                  stream, a);
   else
-    e = launch_k(classify_kernel, dim3((unsigned)((cwarps + kBuildWarps - 1) / kBuildWarps)),
+    e = launch_k(classify_kernel, dim3((unsigned)((rows + kBuildWarps - 1) / kBuildWarps)),
                  dim3(kBuildWarps * 32), 0, stream, a);
   if (e != cudaSuccess) return e;
   ListJob fine;
