@@ -212,8 +212,8 @@ __device__ __forceinline__ bool mask_bit(int nn, uint64_t ops, const int32_t* ar
 // interval ends besides 0, else the row is left to the per-word evaluation.
 constexpr int kRowBreaks = 8;
 
-__device__ __forceinline__ void cswap(int64_t& a, int64_t& b) {
-  const int64_t lo = a < b ? a : b, hi = a < b ? b : a;
+__device__ __forceinline__ void cswap(int& a, int& b) {
+  const int lo = min(a, b), hi = max(a, b);
   a = lo;
   b = hi;
 }
@@ -260,20 +260,22 @@ __device__ RowSegs row_segments(int nn, uint64_t ops, const int32_t* arg, bool t
     }
     nb += add;
   }
+  // clamped to [0, len] (len < 2^31), so the sort and the segments run in 32 bits
+  int b32[kRowBreaks];
 #pragma unroll
-  for (int t = 0; t < kRowBreaks; ++t) bp[t] = bp[t] < 0 ? 0 : (bp[t] > len ? len : bp[t]);
+  for (int t = 0; t < kRowBreaks; ++t) b32[t] = (int)(bp[t] < 0 ? 0 : (bp[t] > len ? len : bp[t]));
   // sorting network for 8 values (19 compare-exchanges)
-  cswap(bp[0], bp[2]); cswap(bp[1], bp[3]); cswap(bp[4], bp[6]); cswap(bp[5], bp[7]);
-  cswap(bp[0], bp[4]); cswap(bp[1], bp[5]); cswap(bp[2], bp[6]); cswap(bp[3], bp[7]);
-  cswap(bp[0], bp[1]); cswap(bp[2], bp[3]); cswap(bp[4], bp[5]); cswap(bp[6], bp[7]);
-  cswap(bp[2], bp[4]); cswap(bp[3], bp[5]);
-  cswap(bp[1], bp[4]); cswap(bp[3], bp[6]);
-  cswap(bp[1], bp[2]); cswap(bp[3], bp[4]); cswap(bp[5], bp[6]);
+  cswap(b32[0], b32[2]); cswap(b32[1], b32[3]); cswap(b32[4], b32[6]); cswap(b32[5], b32[7]);
+  cswap(b32[0], b32[4]); cswap(b32[1], b32[5]); cswap(b32[2], b32[6]); cswap(b32[3], b32[7]);
+  cswap(b32[0], b32[1]); cswap(b32[2], b32[3]); cswap(b32[4], b32[5]); cswap(b32[6], b32[7]);
+  cswap(b32[2], b32[4]); cswap(b32[3], b32[5]);
+  cswap(b32[1], b32[4]); cswap(b32[3], b32[6]);
+  cswap(b32[1], b32[2]); cswap(b32[3], b32[4]); cswap(b32[5], b32[6]);
   int n = 0;
   int lo0 = 0, hi0 = 0, lo1 = 0, hi1 = 0;
 #pragma unroll
   for (int t = 0; t + 1 < kRowBreaks; ++t) {
-    const int64_t y0 = bp[t], y1 = bp[t + 1];
+    const int y0 = b32[t], y1 = b32[t + 1];
     if (y0 < y1 && mask_bit(nn, ops, arg, transposed, x, y0, run_lo, run_hi, off)) {
       if (n == 1 && hi0 == (int)y0) {
         hi0 = (int)y1;
