@@ -61,12 +61,12 @@ constexpr size_t dec_smem_bytes() {
          + 2 * kDecStages * 8 + 16;                       // mbarriers, abort flag
 }
 
-// tanh(t) = 1 - 2 / (1 + e^{2t}); exact at both saturations, absolute error a few ulp of 1.
-__device__ __forceinline__ float tanh_fast(float t) {
-  const float e = ex2_approx(t * (2.0f * kLog2e));
+// 1 / x by the special-function unit (the soft-cap's tanh(t) = 1 - 2 / (1 + e^{2t}),
+// exact at both saturations, absolute error a few ulp of 1)
+__device__ __forceinline__ float rcp_approx(float x) {
   float r;
-  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(1.0f + e));
-  return fmaf(-2.0f, r, 1.0f);
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
 }
 
 // Warp roles: warps 0..7 compute, each on keys [16 w, 16 w + 16) of every tile
@@ -180,7 +180,12 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     if constexpr (SCORE == FA_S_ALIBI) slope_l2 = __ldg(p.score_param + h) * kLog2e;
     const float* bias_h = nullptr;  // RELBIAS: this head's table
     if constexpr (SCORE == FA_S_RELBIAS) bias_h = p.score_param + (int64_t)h * p.bias_len;
-    if constexpr (SCORE == FA_S_SOFTCAP) cap = __ldg(p.score_param);
+    float cap_l2 = 0.f, sc_cap2 = 0.f;  // soft-cap: c log2(e), and S -> the exponent of e^{2 x / c} in base 2
+    if constexpr (SCORE == FA_S_SOFTCAP) {
+      cap = __ldg(p.score_param);
+      cap_l2 = cap * kLog2e;
+      sc_cap2 = (p.scale / cap) * (2.0f * kLog2e);
+    }
 #pragma unroll
     for (int i = 0; i < QB; ++i) {
       m_run[i] = -INFINITY;
@@ -281,7 +286,8 @@ __global__ void __launch_bounds__(kDecThreads, 1)
           if ((w >> i) & 1u) {
             const float x = a[i] * p.scale;
             if constexpr (SCORE == FA_S_SOFTCAP) {
-              sc = cap * tanh_fast(x / cap) * kLog2e;
+              // c tanh(x / c) log2(e) with tanh(t) = 1 - 2 / (1 + e^{2t})
+              sc = fmaf(-2.0f * cap_l2, rcp_approx(1.0f + ex2_approx(a[i] * sc_cap2)), cap_l2);
             } else if constexpr (SCORE == FA_S_ALIBI) {
               sc = fmaf(x, kLog2e, -slope_l2 * (float)(i + qoff - j));
             } else if constexpr (SCORE == FA_S_RELBIAS) {  // entry clamp(q_pos - j - d0, 0, L - 1)
