@@ -151,8 +151,12 @@ def _run_and_check(q_len, kv_len, D, B, H, sel, mask, docs, score, seed, what):
     nodes = None if mask is None else device_nodes(mask, docs)
     bm = fa.fa_block_mask_from_kv_blocks(*cuda32(num, idx), q_len, kv_len, *cuda32(fnum, fidx), nodes=nodes)
     slopes = make_alibi_slopes(H)
-    dev_score = {"none": None, "softcap": ("softcap", [20.0]), "alibi": ("alibi", torch.as_tensor(slopes))}[score]
-    ref_score = {"none": ("none",), "softcap": ("softcap", 20.0), "alibi": ("alibi", slopes)}[score]
+    # the learned bias: distances -200 .. 999 in the table, both ends clamped for these lengths
+    table = np.random.default_rng(seed + 1).normal(scale=0.6, size=(H, 1200)).astype(np.float32)
+    dev_score = {"none": None, "softcap": ("softcap", [20.0]), "alibi": ("alibi", torch.as_tensor(slopes)),
+                 "relbias": ("relbias", torch.as_tensor(table), -200)}[score]
+    ref_score = {"none": ("none",), "softcap": ("softcap", 20.0), "alibi": ("alibi", slopes),
+                 "relbias": ("relbias", table, -200)}[score]
     qd, kd, vd, dod = (t.cuda() for t in (q, k, v, do))
     out, lse = fa.fa_forward(qd, kd, vd, bm, score=dev_score)
     dq, dk, dv = fa.fa_backward(qd, kd, vd, out, lse, dod, bm, score=dev_score)
@@ -179,7 +183,7 @@ def _run_and_check(q_len, kv_len, D, B, H, sel, mask, docs, score, seed, what):
 
 
 @pytest.mark.parametrize("D", [64, 128])
-@pytest.mark.parametrize("score", ["none", "softcap", "alibi"])
+@pytest.mark.parametrize("score", ["none", "softcap", "alibi", "relbias"])
 def test_forward_backward_per_head_lists(D, score):
     """Per-(batch, head) random selections (Bm = B, Hm = H), no program: every
     pair of a listed tile is visible; ragged lengths."""

@@ -31,7 +31,7 @@ def gather(pool, table, kv_len):
 
 
 @pytest.mark.parametrize("D", [64, 128])
-@pytest.mark.parametrize("score", ["none", "alibi"])
+@pytest.mark.parametrize("score", ["none", "alibi", "relbias"])
 def test_paged_forward_equals_gathered(D, score):
     B, H, q_len, kv_len = 3, 2, 700, 900
     nkv = -(-kv_len // 128)
@@ -43,7 +43,9 @@ def test_paged_forward_equals_gathered(D, score):
     docs = make_doc_ids(("geometric", 200.0), max(q_len, kv_len), 4, batch=B)
     mask = P(("causal",), ("same_doc",), ("and",), ("window", 500), ("and",))
     slopes = make_alibi_slopes(H)
-    dev_score = ("alibi", torch.as_tensor(slopes)) if score == "alibi" else None
+    btab = np.random.default_rng(5).normal(scale=0.6, size=(H, 300)).astype(np.float32)  # distances 2 .. 301
+    dev_score = {"none": None, "alibi": ("alibi", torch.as_tensor(slopes)),
+                 "relbias": ("relbias", torch.as_tensor(btab), 2)}[score]
     qd, kpd, vpd, td = q.cuda(), kp.cuda(), vp.cuda(), table.cuda()
     bm = fa.fa_create_block_mask(device_nodes(mask, docs), B, 1, q_len, kv_len, 128)
     out_p, lse_p = fa.fa_forward_paged(qd, kpd, vpd, td, bm, score=dev_score)
@@ -55,7 +57,7 @@ def test_paged_forward_equals_gathered(D, score):
     # the oracle on its own gather of the same pools
     kg = oracle.paged_gather(kp.double().numpy(), table.numpy(), kv_len)
     vg = oracle.paged_gather(vp.double().numpy(), table.numpy(), kv_len)
-    ref_score = ("alibi", slopes) if score == "alibi" else ("none",)
+    ref_score = {"none": ("none",), "alibi": ("alibi", slopes), "relbias": ("relbias", btab, 2)}[score]
     for b, h in ((0, 0), (2, 1)):
         prog = oracle.Program(mask, doc_row=docs[b])
         ref_out, ref_lse = oracle.forward_head(q[b, h].double().numpy(), kg[b, h], vg[b, h], prog, ref_score, h,
