@@ -61,6 +61,11 @@ struct FwdCfg {
   static constexpr bool STAGE_IN_RING = (NS == 2 && BK == 128);  // output staged in the last V slot
   static constexpr int NW = BK / 32;                     // 32-column mask words per row and step
   static constexpr uint32_t TMEM_COLS = 256;
+  // P in TMEM columns of its own when S (BK columns), O ([128, 128 + D)) and P
+  // (BK / 2 columns) fit in the 256: then the next step's S is computed while
+  // the softmax warps work on this one's; else P overwrites S's first columns
+  static constexpr bool SP = (BK == 64) || (D == 64);
+  static constexpr uint32_t T_P = !SP ? 0u : (BK == 64 ? 64u : 128u + D);
 };
 
 // One work item: the query tile I of head (b, h), with the key tiles of its
@@ -82,6 +87,7 @@ struct FwdCtl {
   uint64_t p_half, p_full;  // P of the first 64 keys, of all 128 keys
   uint64_t o_full, o_free;
   uint64_t stg_free;
+  uint64_t s_free, p_free;  // separate P: S read by the softmax warps; P consumed by its P V
   uint64_t fin;
   uint32_t tmem;
   int abort;
@@ -206,6 +212,9 @@ __global__ void __launch_bounds__(192, 2)
   static_assert(C::NS * C::KV_TILE + (C::STAGE_IN_RING ? 0 : C::TILE) + C::TILE + sizeof(FwdCtl) + 1024 <=
                     fwd_smem_bytes<D, BK>(),
                 "forward shared-memory layout");
+  static_assert(!C::SP || (C::T_P >= (uint32_t)BK && C::T_P + BK / 2 <= 128u) ||
+                    (C::T_P >= 128u + D && C::T_P + BK / 2 <= C::TMEM_COLS),
+                "separate P: its columns clear of S and O");
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int items = p.B * p.H * p.nq;  // below 2^31: checked at launch
@@ -213,7 +222,8 @@ __global__ void __launch_bounds__(192, 2)
   const uint32_t b_q = smem_u32(&ctl->q_full), b_qe = smem_u32(&ctl->q_empty), b_s = smem_u32(&ctl->s_full),
                  b_p = smem_u32(&ctl->p_full), b_ph = smem_u32(&ctl->p_half), b_o = smem_u32(&ctl->o_full),
                  b_of = smem_u32(&ctl->o_free),
-                 b_stg = smem_u32(&ctl->stg_free), b_fin = smem_u32(&ctl->fin);
+                 b_stg = smem_u32(&ctl->stg_free), b_fin = smem_u32(&ctl->fin),
+                 b_sfree = smem_u32(&ctl->s_free), b_pfree = smem_u32(&ctl->p_free);
   if (threadIdx.x == 0) {
     mbar_init(b_q, 1);
     mbar_init(b_qe, 1);
@@ -227,6 +237,8 @@ __global__ void __launch_bounds__(192, 2)
     mbar_init(b_o, 1);
     mbar_init(b_of, 128);
     mbar_init(b_stg, 1);
+    mbar_init(b_sfree, 128);
+    mbar_init(b_pfree, 1);
     mbar_init(b_fin, 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(smem_u32(&ctl->desc_full[s]), 1);
@@ -367,12 +379,10 @@ __global__ void __launch_bounds__(192, 2)
           ok = false;
           break;
         }
-        for (int jj = 0; jj < n; ++jj, ++t) {
-          const int pk = 2 * t, sk = pk % C::NS;
-          if (!mbar_wait(smem_u32(&ctl->kv_full[sk]), (pk / C::NS) & 1, &ctl->abort)) {
-            ok = false;
-            break;
-          }
+        // S of step tt = Q K^T into TMEM [0, BK); `last`: the item's last S
+        auto issue_s = [&](int tt, bool last) -> bool {
+          const int pk = 2 * tt, sk = pk % C::NS;
+          if (!mbar_wait(smem_u32(&ctl->kv_full[sk]), (pk / C::NS) & 1, &ctl->abort)) return false;
           tc_fence_after();
           const uint32_t k_base = smem_u32(sKV + sk * C::KV_TILE);
           const uint64_t a0 = opaque(sdesc_sw128(q_base, 16, 1024)), b0 = opaque(sdesc_sw128(k_base, 16, 1024));
@@ -380,10 +390,28 @@ __global__ void __launch_bounds__(192, 2)
           for (int kk = 0; kk < D / 16; ++kk)
             mma_ss(tmem, kmajor_step(a0, kk), kmajor_step_c<C::KV_CHUNK>(b0, kk), kIdS, kk > 0);
           mma_commit(smem_u32(&ctl->kv_empty[sk]));
-          if (jj == n - 1) mma_commit(b_qe);  // Q read for the last time in this item
+          if (last) mma_commit(b_qe);  // Q read for the last time in this item
           mma_commit(b_s);
+          return true;
+        };
+        for (int jj = 0; jj < n; ++jj, ++t) {
+          const int pk = 2 * t;
+          // S of this step (with P in columns of its own, issued at the step before
+          // except for an item's first)
+          if ((!C::SP || jj == 0) && !issue_s(t, jj == n - 1)) {
+            ok = false;
+            break;
+          }
           // the next item, looked up while the softmax runs
           if (jj == 0) kn = next_live(p, k + (int)gridDim.x, items, nxt);
+          if constexpr (C::SP) {
+            // the softmax warps have read S: the next step's S into the same
+            // columns now, ahead of this step's P V
+            if (!mbar_wait(b_sfree, t & 1, &ctl->abort) || (jj + 1 < n && !issue_s(t + 1, jj + 1 == n - 1))) {
+              ok = false;
+              break;
+            }
+          }
           // P V in two halves: keys [0, 64) as soon as their P is in TMEM, while
           // the softmax warps compute the rest
           if (!mbar_wait(b_ph, t & 1, &ctl->abort)) {
@@ -404,7 +432,8 @@ __global__ void __launch_bounds__(192, 2)
           const uint32_t v_base = smem_u32(sKV + sv * C::KV_TILE);
           const uint64_t v0 = opaque(sdesc_sw128(v_base, C::KV_CHUNK, 1024));
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) mma_ts(tmem + 128, tmem + kk * 8, mnmajor_step(v0, kk), kIdO, (jj > 0 || kk > 0));
+          for (int kk = 0; kk < 4; ++kk)
+            mma_ts(tmem + 128, tmem + C::T_P + kk * 8, mnmajor_step(v0, kk), kIdO, (jj > 0 || kk > 0));
           if constexpr (BK == 128) {  // keys [64, 128) once the rest of P is in
             if (!mbar_wait(b_p, t & 1, &ctl->abort)) {
               ok = false;
@@ -412,9 +441,10 @@ __global__ void __launch_bounds__(192, 2)
             }
             tc_fence_after();
 #pragma unroll
-            for (int kk = 4; kk < 8; ++kk) mma_ts(tmem + 128, tmem + kk * 8, mnmajor_step(v0, kk), kIdO, true);
+            for (int kk = 4; kk < 8; ++kk) mma_ts(tmem + 128, tmem + C::T_P + kk * 8, mnmajor_step(v0, kk), kIdO, true);
           }
           mma_commit(smem_u32(&ctl->kv_empty[sv]));
+          if constexpr (C::SP) mma_commit(b_pfree);  // P of this step consumed, O updated
         }
         if (!ok) break;
         mma_commit(b_o);
@@ -561,6 +591,10 @@ __global__ void __launch_bounds__(192, 2)
           tmem_ld128f(tS, s);
         else
           tmem_ld64f(tS, s);
+        if constexpr (C::SP) {  // S is in registers: the next step's S may overwrite it
+          tc_fence_before();
+          mbar_arrive(b_sfree);
+        }
         if (msk) {
   #pragma unroll
           for (int e = 0; e < BK; ++e) s[e] = ((wd[e >> 5] >> (e & 31)) & 1u) ? s[e] : -INFINITY;
@@ -620,7 +654,17 @@ __global__ void __launch_bounds__(192, 2)
         }
         const bool rescale = __any_sync(0xffffffffu, need);  // O is rescaled below, once S is no longer live
         const float m_use = (m == -INFINITY) ? 0.f : m;
-        // -- P = 2^(x - m) as bf16 into TMEM (over the consumed S columns), row sum (4 chains)
+        // P and O may be written once the last P V is done (with P in columns of its
+        // own that is a wait; else S of this step came after it)
+        if constexpr (C::SP) {
+          if (jj > 0 && !warp_wait(b_pfree, (t - 1) & 1, &ctl->abort)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+        }
+        // -- P = 2^(x - m) as bf16 into TMEM (over the consumed S columns, or its
+        //    own), row sum (4 chains)
         {
           float2 c01 = make_float2(0.f, 0.f), c23 = make_float2(0.f, 0.f);
           const float off = -(base + m_use);
@@ -658,10 +702,10 @@ __global__ void __launch_bounds__(192, 2)
               pk[e2] = pack_bf16x2(p01.x, p01.y);
               pk[e2 + 1] = pack_bf16x2(p23.x, p23.y);
             }
-            tmem_st16(tS + 16 * c, pk);
+            tmem_st16(tS + C::T_P + 16 * c, pk);
             if (c == 1) {
               // P of the first 64 keys is in: P V over them may start, once O has
-              // been rescaled (the last P V is done: S of this step came after it)
+              // been rescaled (the last P V is done: see above)
               if (rescale) {
   #pragma unroll 1
                 for (int c3 = 0; c3 < D / 32; ++c3) {
