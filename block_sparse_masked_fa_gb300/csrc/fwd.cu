@@ -21,8 +21,10 @@
 // S has read the buffer, its first S runs while the epilogue reads O out of
 // TMEM, and the output is staged in shared memory (the last V slot with two
 // slots) and stored by TMA (thread 0) without waiting.
-// TMEM (256 columns): S at [0, BK) -- P (bf16 pairs) overwrites its first BK / 2
-// columns after the softmax has read S -- and O at [128, 128 + D).
+// TMEM (256 columns): S at [0, BK) and O at [128, 128 + D).  P (bf16 pairs, BK / 2
+// columns) overwrites S's first columns after the softmax has read S when D = 128
+// with 128-key tiles; in the other shapes it has columns of its own, and the next
+// step's S is computed while the softmax warps work on this one.
 // Key tiles are BK = 128 positions, or 64 when the block mask's tiles are
 // smaller (tutorial, sharp edge 4): then S is 128 x 64, the P V of a step is
 // one group of four MMAs, and the output has a staging buffer of its own.
