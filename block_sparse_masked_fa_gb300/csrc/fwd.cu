@@ -24,7 +24,8 @@
 // TMEM (256 columns): S at [0, BK) and O at [128, 128 + D).  P (bf16 pairs, BK / 2
 // columns) overwrites S's first columns after the softmax has read S when D = 128
 // with 128-key tiles; in the other shapes it has columns of its own, and the next
-// step's S is computed while the softmax warps work on this one.
+// step's S is computed while the softmax warps work on this one where the K / V
+// ring has loaded the next K in time (D = 64).
 // Key tiles are BK = 128 positions, or 64 when the block mask's tiles are
 // smaller (tutorial, sharp edge 4): then S is 128 x 64, the P V of a step is
 // one group of four MMAs, and the output has a staging buffer of its own.
@@ -68,6 +69,10 @@ struct FwdCfg {
   // the softmax warps work on this one's; else P overwrites S's first columns
   static constexpr bool SP = (BK == 64) || (D == 64);
   static constexpr uint32_t T_P = !SP ? 0u : (BK == 64 ? 64u : 128u + D);
+  // the next S ahead of this step's P V only where the ring has loaded the next K
+  // by then (with two slots it is loaded once this step's S is done, and waiting
+  // for it would hold up the P V)
+  static constexpr bool EARLY_S = SP && NS >= 4;
 };
 
 // One work item: the query tile I of head (b, h), with the key tiles of its
@@ -400,13 +405,13 @@ __global__ void __launch_bounds__(192, 2)
           const int pk = 2 * t;
           // S of this step (with P in columns of its own, issued at the step before
           // except for an item's first)
-          if ((!C::SP || jj == 0) && !issue_s(t, jj == n - 1)) {
+          if ((!C::EARLY_S || jj == 0) && !issue_s(t, jj == n - 1)) {
             ok = false;
             break;
           }
           // the next item, looked up while the softmax runs
           if (jj == 0) kn = next_live(p, k + (int)gridDim.x, items, nxt);
-          if constexpr (C::SP) {
+          if constexpr (C::EARLY_S) {
             // the softmax warps have read S: the next step's S into the same
             // columns now, ahead of this step's P V
             if (!mbar_wait(b_sfree, t & 1, &ctl->abort) || (jj + 1 < n && !issue_s(t + 1, jj + 1 == n - 1))) {
@@ -593,7 +598,7 @@ __global__ void __launch_bounds__(192, 2)
           tmem_ld128f(tS, s);
         else
           tmem_ld64f(tS, s);
-        if constexpr (C::SP) {  // S is in registers: the next step's S may overwrite it
+        if constexpr (C::EARLY_S) {  // S is in registers: the next step's S may overwrite it
           tc_fence_before();
           mbar_arrive(b_sfree);
         }
@@ -657,7 +662,8 @@ __global__ void __launch_bounds__(192, 2)
         const bool rescale = __any_sync(0xffffffffu, need);  // O is rescaled below, once S is no longer live
         const float m_use = (m == -INFINITY) ? 0.f : m;
         // P and O may be written once the last P V is done (with P in columns of its
-        // own that is a wait; else S of this step came after it)
+        // own that is a wait -- met at once unless the next S runs ahead; else S of
+        // this step came after it)
         if constexpr (C::SP) {
           if (jj > 0 && !warp_wait(b_pfree, (t - 1) & 1, &ctl->abort)) {
             ok = false;
