@@ -11,6 +11,7 @@ from .binding import (  # noqa: F401
     FaError,
     fa_backward,
     fa_backward_noalloc,
+    fa_backward_prepared,
     fa_backward_workspace_bytes,
     fa_block_mask_bytes,
     fa_block_mask_from_kv_blocks,
@@ -20,6 +21,7 @@ from .binding import (  # noqa: F401
     fa_forward_decode,
     fa_forward_decode_workspace_bytes,
     fa_forward_paged,
+    fa_forward_prepare_backward,
     fa_get_status,
     fa_status_string,
     fa_version,

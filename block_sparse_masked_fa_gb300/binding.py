@@ -3,8 +3,8 @@
 Names mirror the C entry points: fa_block_mask_bytes, fa_create_block_mask,
 fa_block_mask_from_kv_blocks, fa_forward, fa_forward_paged,
 fa_forward_decode_workspace_bytes, fa_forward_decode,
-fa_backward_workspace_bytes, fa_backward, fa_get_status, fa_block_mask_summary,
-fa_status_string.  Tensors are torch CUDA tensors; the binding passes their
+fa_backward_workspace_bytes, fa_backward, fa_forward_prepare_backward,
+fa_backward_prepared, fa_get_status, fa_block_mask_summary, fa_status_string.  Tensors are torch CUDA tensors; the binding passes their
 device pointers and the current CUDA stream.  Every step
 of the computation runs in the library's kernels; importing this module fails
 loudly when the library has not been built.
@@ -104,6 +104,11 @@ def _bind(lib):
                                                      _c.POINTER(BlockMaskStruct), _c.POINTER(ScoreSpec), _c.c_float,
                                                      _c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_void_p,
                                                      _c.c_size_t, _c.c_void_p]
+    lib.fa_forward_prepare_backward.argtypes = [_c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_int32, _c.c_int32,
+                                                 _c.c_int64, _c.c_int64, _c.c_int32, _c.POINTER(BlockMaskStruct),
+                                                 _c.POINTER(ScoreSpec), _c.c_float, _c.c_void_p, _c.c_void_p,
+                                                 _c.c_void_p, _c.c_size_t, _c.c_void_p]
+    lib.fa_backward_prepared.argtypes = lib.fa_backward.argtypes
     lib.fa_backward_noalloc.argtypes = [_c.c_void_p] * 6 + [_c.c_int32, _c.c_int32, _c.c_int64, _c.c_int64,
                                                              _c.c_int32, _c.POINTER(BlockMaskStruct),
                                                              _c.POINTER(ScoreSpec), _c.c_float, _c.c_void_p,
@@ -114,7 +119,8 @@ def _bind(lib):
     lib.fa_status_string.restype = _c.c_char_p
     for _f in (lib.fa_block_mask_bytes, lib.fa_create_block_mask, lib.fa_block_mask_from_kv_blocks, lib.fa_forward,
                lib.fa_forward_paged, lib.fa_forward_decode_workspace_bytes, lib.fa_forward_decode, lib.fa_backward_workspace_bytes,
-               lib.fa_backward, lib.fa_backward_noalloc, lib.fa_get_status, lib.fa_block_mask_summary):
+               lib.fa_backward, lib.fa_backward_noalloc, lib.fa_forward_prepare_backward, lib.fa_backward_prepared,
+               lib.fa_get_status, lib.fa_block_mask_summary):
         _f.restype = _c.c_int
     lib.fa_version.restype = _c.c_int32
     return lib
@@ -124,8 +130,8 @@ _lib = _bind(_lib)
 
 EXPORTED = ("fa_block_mask_bytes", "fa_create_block_mask", "fa_block_mask_from_kv_blocks", "fa_forward",
             "fa_forward_paged", "fa_forward_decode_workspace_bytes", "fa_forward_decode", "fa_backward_workspace_bytes",
-            "fa_backward", "fa_backward_noalloc", "fa_get_status", "fa_block_mask_summary", "fa_status_string",
-            "fa_version")
+            "fa_backward", "fa_backward_noalloc", "fa_forward_prepare_backward", "fa_backward_prepared",
+            "fa_get_status", "fa_block_mask_summary", "fa_status_string", "fa_version")
 NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
@@ -455,6 +461,28 @@ def fa_forward(q, k, v, block_mask: BlockMask, score=None, scale: float = 0.0, o
     return out, lse
 
 
+def fa_forward_prepare_backward(q, k, v, block_mask: BlockMask, workspace, score=None, scale: float = 0.0,
+                                out=None, lse=None, stream=None):
+    """fa_forward that also sets ``workspace``'s dq accumulator to zero while it
+    runs (uint8 CUDA tensor of at least fa_backward_workspace_bytes(B, H,
+    q_len, D)); pass the same workspace to fa_backward_prepared."""
+    _check_shapes(q, kv=(("k", k), ("v", v)), like_q=(("out", out),), lse=lse)
+    B, H, q_len, D = q.shape
+    kv_len = k.shape[2]
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty(B, H, q_len, dtype=torch.float32, device=q.device)
+    _check_storage(q, (("k", k, _BF16), ("v", v, _BF16), ("out", out, _BF16), ("lse", lse, _F32),
+                       ("workspace", workspace, _U8)))
+    sspec, keep = _score(score, H)
+    _check(_lib.fa_forward_prepare_backward(_ptr(q), _ptr(k), _ptr(v), B, H, q_len, kv_len, D,
+                                            ctypes.byref(block_mask.struct), ctypes.byref(sspec), float(scale),
+                                            _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(),
+                                            _stream(stream)), "fa_forward_prepare_backward")
+    return out, lse
+
+
 def _backward_score(score, score_param_grad, H: int):
     """Score spec for the backward: a copy of the caller's, with the device
     pointer of ``score_param_grad`` (fp32, receives dL/dslope [H] for ALiBi or
@@ -583,6 +611,26 @@ def fa_backward(q, k, v, out, lse, dout, block_mask: BlockMask, score=None, scal
     _check(_lib.fa_backward(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout), B, H, q_len, kv_len, D,
                             ctypes.byref(block_mask.struct), ctypes.byref(sspec), float(scale), _ptr(dq), _ptr(dk),
                             _ptr(dv), _ptr(workspace), workspace.numel(), _stream(stream)), "fa_backward")
+    return dq, dk, dv
+
+
+def fa_backward_prepared(q, k, v, out, lse, dout, block_mask: BlockMask, workspace, score=None, scale: float = 0.0,
+                         dq=None, dk=None, dv=None, stream=None, score_param_grad=None):
+    """fa_backward on a workspace prepared by fa_forward_prepare_backward (its
+    dq accumulator taken as zero)."""
+    _check_shapes(q, kv=(("k", k), ("v", v), ("dk", dk), ("dv", dv)),
+                  like_q=(("out", out), ("dout", dout), ("dq", dq)), lse=lse)
+    B, H, q_len, D = q.shape
+    kv_len = k.shape[2]
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    _check_storage(q, _backward_tensors(k, v, out, lse, dout, dq, dk, dv) + (("workspace", workspace, _U8),))
+    sspec, keep = _backward_score(score, score_param_grad, H)
+    _check(_lib.fa_backward_prepared(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout), B, H, q_len,
+                                     kv_len, D, ctypes.byref(block_mask.struct), ctypes.byref(sspec), float(scale),
+                                     _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace), workspace.numel(),
+                                     _stream(stream)), "fa_backward_prepared")
     return dq, dk, dv
 
 

@@ -551,6 +551,32 @@ fa_status fa_forward_decode(const void* q, const void* k, const void* v, const i
   return cuda_status(e);
 }
 
+fa_status fa_forward_prepare_backward(const void* q, const void* k, const void* v, int32_t B, int32_t H,
+                                      int64_t q_len, int64_t kv_len, int32_t D, const fa_block_mask* bm,
+                                      const fa_score_spec* score, float scale, void* out, float* lse,
+                                      void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  if (!q || !k || !v || !out || !lse || !workspace) return FA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned4(lse) || !aligned16(workspace))
+    return FA_ERR_ALIGNMENT;
+  fa_status st = check_attn(B, H, q_len, kv_len, D, bm, score, &scale, kForward);
+  if (st != FA_OK) return st;
+  size_t need = 0;
+  st = fa_backward_workspace_bytes(B, H, q_len, D, &need);
+  if (st != FA_OK) return st;
+  if (workspace_bytes < need) return FA_ERR_WORKSPACE;
+  DevMask dm;
+  st = check_mask(&bm->spec, q_len, kv_len, &dm);
+  if (st != FA_OK) return st;
+  AttnArgs a = attn_args(B, H, q_len, kv_len, D, bm, score, scale, dm, false);
+  a.zero_dst = static_cast<uint4*>(workspace);  // the dq accumulator: the workspace's first rows * D * 4 bytes
+  a.zero_n16 = (int64_t)B * H * q_len * D * 4 / 16;
+  FwdTensors t{q, k, v, out, lse};
+  bool enc_failed = false;
+  const cudaError_t e = launch_forward(a, t, stream, &enc_failed);
+  if (enc_failed) return FA_ERR_CUDA;
+  return cuda_status(e);
+}
+
 fa_status fa_backward_workspace_bytes(int32_t B, int32_t H, int64_t q_len, int32_t D, size_t* bytes) {
   if (bytes == nullptr) return FA_ERR_INVALID_ARG;
   if (B < 1 || H < 1 || q_len < 1) return FA_ERR_SHAPE;
@@ -561,10 +587,12 @@ fa_status fa_backward_workspace_bytes(int32_t B, int32_t H, int64_t q_len, int32
   return FA_OK;
 }
 
-fa_status fa_backward(const void* q, const void* k, const void* v, const void* out, const float* lse,
+// fa_backward and fa_backward_prepared: acc_zeroed takes the workspace's dq
+// accumulator as already zero
+static fa_status backward_ws(const void* q, const void* k, const void* v, const void* out, const float* lse,
                       const void* dout, int32_t B, int32_t H, int64_t q_len, int64_t kv_len, int32_t D,
                       const fa_block_mask* bm, const fa_score_spec* score, float scale, void* dq, void* dk,
-                      void* dv, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+                      void* dv, void* workspace, size_t workspace_bytes, bool acc_zeroed, cudaStream_t stream) {
   if (!q || !k || !v || !out || !lse || !dout || !dq || !dk || !dv || !workspace) return FA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(dout) || !aligned16(dq) ||
       !aligned16(dk) || !aligned16(dv) || !aligned16(workspace) || !aligned4(lse))
@@ -578,7 +606,8 @@ fa_status fa_backward(const void* q, const void* k, const void* v, const void* o
   DevMask dm;
   st = check_mask(&bm->spec, q_len, kv_len, &dm);
   if (st != FA_OK) return st;
-  const AttnArgs a = attn_args(B, H, q_len, kv_len, D, bm, score, scale, dm, true);
+  AttnArgs a = attn_args(B, H, q_len, kv_len, D, bm, score, scale, dm, true);
+  a.acc_zeroed = acc_zeroed ? 1 : 0;
   const size_t rows = (size_t)B * H * (size_t)q_len;
   BwdTensors t;
   t.q = q;
@@ -598,6 +627,22 @@ fa_status fa_backward(const void* q, const void* k, const void* v, const void* o
   const cudaError_t e = launch_backward(a, t, stream, &enc_failed);
   if (enc_failed) return FA_ERR_CUDA;
   return cuda_status(e);
+}
+
+fa_status fa_backward(const void* q, const void* k, const void* v, const void* out, const float* lse,
+                      const void* dout, int32_t B, int32_t H, int64_t q_len, int64_t kv_len, int32_t D,
+                      const fa_block_mask* bm, const fa_score_spec* score, float scale, void* dq, void* dk,
+                      void* dv, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  return backward_ws(q, k, v, out, lse, dout, B, H, q_len, kv_len, D, bm, score, scale, dq, dk, dv, workspace,
+                     workspace_bytes, false, stream);
+}
+
+fa_status fa_backward_prepared(const void* q, const void* k, const void* v, const void* out, const float* lse,
+                               const void* dout, int32_t B, int32_t H, int64_t q_len, int64_t kv_len, int32_t D,
+                               const fa_block_mask* bm, const fa_score_spec* score, float scale, void* dq, void* dk,
+                               void* dv, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  return backward_ws(q, k, v, out, lse, dout, B, H, q_len, kv_len, D, bm, score, scale, dq, dk, dv, workspace,
+                     workspace_bytes, true, stream);
 }
 
 fa_status fa_backward_noalloc(const void* q, const void* k, const void* v, const void* out, const float* lse,

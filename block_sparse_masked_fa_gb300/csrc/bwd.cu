@@ -961,9 +961,11 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __grid_constant__ At
       const float2 c = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(g + e));
       acc = fmaf(a.x, c.x, fmaf(a.y, c.y, acc));
     }
-    float4* z = reinterpret_cast<float4*>(dq_acc + row * D + t * E);
+    if (!p.acc_zeroed) {  // (else a forward that prepared the workspace cleared it)
+      float4* z = reinterpret_cast<float4*>(dq_acc + row * D + t * E);
 #pragma unroll
-    for (int e = 0; e < E / 4; ++e) z[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int e = 0; e < E / 4; ++e) z[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
   }
 #pragma unroll
   for (int d = 8; d >= 1; d >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, d);

@@ -107,10 +107,15 @@ struct FwdCtl {
   alignas(16) int4 seg[2][128];
 };
 
+// a block of zeros the producer copies over a buffer to be cleared (a backward
+// workspace's dq accumulator), 4 KB a copy
+constexpr uint32_t kZeroBytes = 4096;
+
 template <int D, int BK>
 constexpr size_t fwd_smem_bytes() {
   using C = FwdCfg<D, BK>;
-  return 1024 + (size_t)C::TILE * (1 + (C::STAGE_IN_RING ? 0 : 1)) + (size_t)C::KV_TILE * C::NS + sizeof(FwdCtl);
+  return 1024 + (size_t)C::TILE * (1 + (C::STAGE_IN_RING ? 0 : 1)) + (size_t)C::KV_TILE * C::NS + sizeof(FwdCtl) +
+         128 + kZeroBytes;
 }
 // two CTAs per SM (228 KB of shared memory, 1 KB of it reserved per CTA)
 static_assert(2 * (fwd_smem_bytes<128, 128>() + 1024) <= 228 * 1024, "forward shared memory, D = 128");
@@ -216,7 +221,10 @@ __global__ void __launch_bounds__(192, 2)
   uint8_t* sOut = C::STAGE_IN_RING ? sKV + C::KV_TILE : sKV + C::NS * C::KV_TILE;
   // control block after the ring and the output buffer (when there is one)
   FwdCtl* ctl = reinterpret_cast<FwdCtl*>(sKV + C::NS * C::KV_TILE + (C::STAGE_IN_RING ? 0 : C::TILE));
-  static_assert(C::NS * C::KV_TILE + (C::STAGE_IN_RING ? 0 : C::TILE) + C::TILE + sizeof(FwdCtl) + 1024 <=
+  // the zero block after the control block, 128-byte aligned
+  uint8_t* sZero = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(ctl + 1) + 127) & ~uintptr_t(127));
+  static_assert(C::NS * C::KV_TILE + (C::STAGE_IN_RING ? 0 : C::TILE) + C::TILE + sizeof(FwdCtl) + 128 + kZeroBytes +
+                        1024 <=
                     fwd_smem_bytes<D, BK>(),
                 "forward shared-memory layout");
   static_assert(!C::SP || (C::T_P >= (uint32_t)BK && C::T_P + BK / 2 <= 128u) ||
@@ -284,6 +292,34 @@ __global__ void __launch_bounds__(192, 2)
       prefetch_tmap(&tm_o);
     }
     int t = 0, u = 0, v = 0, issued = 0, q_issued = 0, published = 0;
+    // A buffer to clear while the forward runs (a backward workspace's dq
+    // accumulator): this CTA's share, in copies of the zero block issued after
+    // the K / V loads (so that no load waits behind them) and the rest at the
+    // end; an evict-first L2 policy keeps the stream from pushing out K / V.
+    int64_t z_next = 0, z_end = 0;
+    uint64_t z_pol = 0;
+    const uint32_t s_zero = smem_u32(sZero);
+    if (p.zero_dst != nullptr) {
+      const int64_t per = ((p.zero_n16 + gridDim.x - 1) / gridDim.x + 255) / 256 * 256;  // whole 4 KB copies
+      z_next = min((int64_t)blockIdx.x * per, p.zero_n16);
+      z_end = min(z_next + per, p.zero_n16);
+      for (int q = lane; q < (int)(kZeroBytes / 16); q += 32) reinterpret_cast<uint4*>(sZero)[q] = make_uint4(0u, 0u, 0u, 0u);
+      fence_proxy_async_smem();
+      __syncwarp();
+      z_pol = l2_evict_first_policy();
+    }
+    auto zero_some = [&](int copies) {
+      if (z_next >= z_end) return;
+      if (lane == 0) {
+        for (int c = 0; c < copies && z_next < z_end; ++c) {
+          const int64_t n = min((int64_t)(kZeroBytes / 16), z_end - z_next);
+          bulk_store(p.zero_dst + z_next, s_zero, (uint32_t)(n * 16), z_pol);
+          z_next += n;
+        }
+        bulk_commit();
+      }
+      z_next = __shfl_sync(0xffffffffu, z_next, 0);
+    };
     bool ok = true;
     for (int k = first; ok && k < items; k += (int)gridDim.x, ++v) {
       FwdItem cur = fwd_item(p, k);
@@ -355,10 +391,13 @@ __global__ void __launch_bounds__(192, 2)
               tma_load_3d(smem_u32(sKV + slot * C::KV_TILE + c * C::KV_CHUNK), m, bar, c * 64, kv_row, kv_z);
           }
           issued = pos + 1;
+          zero_some(2);
         }
       }
       ++u;
     }
+    if (ok)
+      while (z_next < z_end) zero_some(64);
     if (!ok && lane == 0) fail(p, ctl);
     // drain: every copy this CTA started lands before it exits (each buffer's
     // earlier loads were waited for before the last one was issued)
@@ -368,6 +407,7 @@ __global__ void __launch_bounds__(192, 2)
         mbar_wait(smem_u32(&ctl->desc_full[w & 1]), (w >> 1) & 1, nullptr);
       for (int pos = max(0, issued - C::NS); pos < issued; ++pos)
         mbar_wait(smem_u32(&ctl->kv_full[pos % C::NS]), (pos / C::NS) & 1, nullptr);
+      if (p.zero_dst != nullptr) bulk_wait0();  // the zero copies have landed
     }
   } else if (warp == 5) {
     // ------------------------------------------------------------ MMA issuer

@@ -107,6 +107,12 @@ struct AttnArgs {
   // at page_table[b * nkv + J], pages of 128 rows in [H][n_pages * 128][D] pools; or null
   const int32_t* page_table;
   int32_t n_pages;
+  // forward: a buffer its producer warps set to zero while it runs (the dq
+  // accumulator of a backward workspace; 16-byte units), or null
+  uint4* zero_dst;
+  int64_t zero_n16;
+  // backward: the dq accumulator is already zero (set so by such a forward)
+  int32_t acc_zeroed;
   uint32_t* status;
   DevMask mask;
   const int4* row_segs;  // [Bm][2][seg_len]: see fa_block_mask

@@ -377,6 +377,30 @@ fa_status fa_backward(const void* q, const void* k, const void* v, const void* o
                       const fa_block_mask* bm, const fa_score_spec* score, float scale, void* dq, void* dk,
                       void* dv, void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
+/* ------------------------------------------------------------------------
+ * A forward that prepares the backward's workspace, and the backward that
+ * takes it prepared.  fa_forward_prepare_backward computes exactly what
+ * fa_forward computes; while it runs, its producer warps also set the
+ * workspace's fp32 dq accumulator (its first B*H*q_len*D*4 bytes) to zero, in
+ * bulk copies beside the K / V loads -- work the backward's preprocessing
+ * kernel otherwise does, at half of its memory traffic.  fa_backward_prepared
+ * is fa_backward for such a workspace: it takes the accumulator as zero.  The
+ * pair must see the same B, H, q_len and D, and nothing else may use the
+ * workspace between them (a second fa_backward_prepared on it would add into a
+ * spent accumulator: call fa_backward, which clears it, instead).
+ * workspace: device, 16-byte aligned, >= fa_backward_workspace_bytes(B, H,
+ * q_len, D) (FA_ERR_WORKSPACE); other arguments and errors as fa_forward /
+ * fa_backward.  Asynchronous on the stream.
+ * ---------------------------------------------------------------------- */
+fa_status fa_forward_prepare_backward(const void* q, const void* k, const void* v, int32_t B, int32_t H,
+                                      int64_t q_len, int64_t kv_len, int32_t D, const fa_block_mask* bm,
+                                      const fa_score_spec* score, float scale, void* out, float* lse,
+                                      void* workspace, size_t workspace_bytes, cudaStream_t stream);
+fa_status fa_backward_prepared(const void* q, const void* k, const void* v, const void* out, const float* lse,
+                               const void* dout, int32_t B, int32_t H, int64_t q_len, int64_t kv_len, int32_t D,
+                               const fa_block_mask* bm, const fa_score_spec* score, float scale, void* dq, void* dk,
+                               void* dv, void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
 /* Backward without a caller-provided workspace.  The pages have no
  * counterpart: this entry point exists for callers that cannot allocate
  * device memory when they call the backward -- for example code running

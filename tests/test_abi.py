@@ -211,6 +211,34 @@ def test_backward_workspace_and_rejects():
     assert B._lib.fa_backward(*bad, 1 << 30, None) == UNSUPPORTED
 
 
+def test_prepared_pair_rejects():
+    """Host-side errors of fa_forward_prepare_backward and fa_backward_prepared,
+    before any GPU work: the workspace's size and alignment, and the ordinary
+    forward / backward checks."""
+    bm = _bm()
+    sc = B.ScoreSpec()
+    need = fa.fa_backward_workspace_bytes(1, 1, 1024, 64)
+    fwd = [FAKE] * 3 + [1, 1, 1024, 1024, 64, ctypes.byref(bm), ctypes.byref(sc), 0.0, FAKE, FAKE, FAKE]
+    assert B._lib.fa_forward_prepare_backward(*fwd, need - 1, None) == WORKSPACE
+    bad = list(fwd)
+    bad[13] = FAKE + 8
+    assert B._lib.fa_forward_prepare_backward(*bad, need, None) == ALIGN
+    bad = list(fwd)
+    bad[13] = None
+    assert B._lib.fa_forward_prepare_backward(*bad, need, None) == INVALID
+    bad = list(fwd)
+    bad[7] = 96
+    assert B._lib.fa_forward_prepare_backward(*bad, need, None) == UNSUPPORTED
+    bad = list(fwd)
+    bad[5] = 2048
+    assert B._lib.fa_forward_prepare_backward(*bad, need, None) == SHAPE
+    bwd = [FAKE] * 6 + [1, 1, 1024, 1024, 64, ctypes.byref(bm), ctypes.byref(sc), 0.0] + [FAKE] * 4
+    assert B._lib.fa_backward_prepared(*bwd, need - 1, None) == WORKSPACE
+    bad = list(bwd)
+    bad[17] = FAKE + 4
+    assert B._lib.fa_backward_prepared(*bad, need, None) == ALIGN
+
+
 def test_forward_paged_rejects():
     """Host-side errors of the paged forward, before any GPU work."""
     bm = _bm()
