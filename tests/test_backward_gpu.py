@@ -291,3 +291,28 @@ def test_softcap_small_and_saturating_logits(D, cap):
         check_forward(out[0, h].float().cpu().numpy(), lse[0, h].cpu().numpy(), ref_out, ref_lse, f"cap {cap} h{h}")
         ref = oracle_grads(inp, mask, 0, h, ("softcap", cap))
         check_all([g[0, h].float().cpu().numpy() for g in grads], ref, f"cap {cap} D{D} h{h}")
+
+
+def test_query_tiles_no_key_tile_sees_get_zero_dq():
+    """Causal & window 100 with 200 keys and 600 queries: query rows from 300
+    on see no key, so query tiles 3 and 4 have no visible key tile and no key
+    tile's work ever reaches them; their dq (NaN beforehand) must come out
+    zero.  The rest against the oracle."""
+    B, H, S, KV, D = 1, 2, 600, 200, 64
+    q, k, v, do = (t.cuda() for t in make_qkv(B, H, S, D, 517, kv_len=KV))
+    mask = P(("causal",), ("window", 100), ("and",))
+    bm = fa.fa_create_block_mask(device_nodes(mask), 1, 1, S, KV, 128)
+    assert fa.fa_block_mask_summary(bm)[0] > 0  # some tiles EMPTY
+    dq = torch.full_like(q, float("nan"))
+    out, lse = fa.fa_forward(q, k, v, bm)
+    dq, dk, dv = fa.fa_backward(q, k, v, out, lse, do, bm, dq=dq)
+    torch.cuda.synchronize()
+    assert fa.fa_get_status(bm) == 0
+    assert bool((dq[:, :, 384:] == 0).all())
+    inp = {n: t.cpu() for n, t in zip(("q", "k", "v", "do"), (q, k, v, do))}
+    prog = oracle_program(mask, None, None, 0, 1)
+    for h in range(H):
+        ref = oracle.backward_head(head64(inp["q"], 0, h), head64(inp["k"], 0, h), head64(inp["v"], 0, h),
+                                   head64(inp["do"], 0, h), prog, ("none",), h, 1.0 / np.sqrt(D))[:3]
+        for name, gt, rf in zip(("dq", "dk", "dv"), (dq, dk, dv), ref):
+            check_grad(gt[0, h].float().cpu().numpy(), rf, f"h{h} {name}")
