@@ -915,8 +915,10 @@ __global__ void __launch_bounds__(512, 1)
 // soft-cap the constant term c log2(e) of c tanh(x / c) log2(e) -- zero for the rows past
 // q_len in the last tile; the fp32 dq accumulator rows, the score parameter's
 // gradient (if requested) and the main kernel's item counter set to zero.
-// 16 threads per row, 16 rows per 256-thread block; the blocks after the rows'
-// take one key tile (b, h, J) each and write zero dK and dV for a key tile
+// D / 16 threads per row, each with two 16-byte loads of out and of dO in
+// flight (256 / (D / 16) rows per 256-thread block: enough bytes in flight
+// per SM for the HBM roof); the blocks after the rows' take one key tile
+// (b, h, J) each and write zero dK and dV for a key tile
 // that no query tile sees (the main kernel hands out only the others).
 template <int D>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const __grid_constant__ AttnArgs p,
@@ -948,17 +950,22 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __grid_constant__ At
     }
     return;
   }
-  constexpr int E = D / 16;  // elements per thread
-  const int64_t row = (int64_t)blockIdx.x * 16 + threadIdx.x / 16;
-  const int t = threadIdx.x % 16;
+  constexpr int E = 16;        // elements per thread: two 16-byte pieces of each tensor
+  constexpr int TPR = D / E;   // threads per row
+  constexpr int RPB = 256 / TPR;
+  const int64_t row = (int64_t)blockIdx.x * RPB + threadIdx.x / TPR;
+  const int t = threadIdx.x % TPR;
   float acc = 0.f;
   if (row < rows) {
-    const __nv_bfloat16* o = out + row * D + t * E;
-    const __nv_bfloat16* g = dout + row * D + t * E;
+    const uint4* o = reinterpret_cast<const uint4*>(out + row * D + t * E);
+    const uint4* g = reinterpret_cast<const uint4*>(dout + row * D + t * E);
+    const uint4 o0 = __ldg(o), o1 = __ldg(o + 1), g0 = __ldg(g), g1 = __ldg(g + 1);
+    const uint32_t ow[8] = {o0.x, o0.y, o0.z, o0.w, o1.x, o1.y, o1.z, o1.w};
+    const uint32_t gw[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
 #pragma unroll
-    for (int e = 0; e < E; e += 2) {
-      const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(o + e));
-      const float2 c = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(g + e));
+    for (int e = 0; e < 8; ++e) {
+      const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ow[e]));
+      const float2 c = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&gw[e]));
       acc = fmaf(a.x, c.x, fmaf(a.y, c.y, acc));
     }
     if (!p.acc_zeroed) {  // (else a forward that prepared the workspace cleared it)
@@ -968,7 +975,7 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __grid_constant__ At
     }
   }
 #pragma unroll
-  for (int d = 8; d >= 1; d >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, d);
+  for (int d = TPR / 2; d >= 1; d >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, d);
   if (row < rows && t == 0) {
     const int64_t bh = row / q_len;
     const int i = (int)(row % q_len);
@@ -1003,7 +1010,7 @@ template <int D, int SCORE, bool PGRAD>
 cudaError_t launch_bwd_t(const AttnArgs& a, const BwdTensors& t, cudaStream_t stream, bool* enc_failed) {
   const uint64_t bh = (uint64_t)a.B * a.H;
   const int64_t rows = (int64_t)bh * a.q_len;
-  const int64_t row_blocks = (rows + 15) / 16;
+  const int64_t row_blocks = (rows + 256 / (D / 16) - 1) / (256 / (D / 16));  // rows per block of bwd_pre
   bwd_pre_kernel<D><<<(unsigned)(row_blocks + (int64_t)bh * a.nkv), 256, 0, stream>>>(
       a, static_cast<const __nv_bfloat16*>(t.out), static_cast<const __nv_bfloat16*>(t.dout), t.lse, t.stats,
       t.dq_acc, rows, row_blocks, a.param_grad,
