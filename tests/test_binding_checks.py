@@ -179,3 +179,31 @@ def test_block_mask_buffer_checked():
         B._check_buffer(torch.zeros(64, dtype=torch.uint8))                  # host memory
     with pytest.raises(ValueError, match="buffer"):
         B._check_buffer(torch.zeros(64, dtype=torch.int32))
+
+
+@pytest.mark.parametrize("bad", ["workspace_float32", "workspace_view", "out_float32", "dq_expand"])
+def test_prepared_pair_refuses_views_and_wrong_dtypes(bad):
+    """fa_forward_prepare_backward and fa_backward_prepared take the caller's
+    workspace: it is checked like every other tensor (contiguous uint8 on q's
+    device), and so are the outputs."""
+    q, k, v = _fwd_args()
+    out, dout = q.clone(), q.clone()
+    lse = torch.zeros(1, 4, 128)
+    ws = torch.zeros(1 << 16, dtype=torch.uint8)
+    kw_f, kw_b = {}, {}
+    match = "contiguous"
+    if bad == "workspace_float32":
+        ws, match = torch.zeros(1 << 14, dtype=torch.float32), "workspace must be torch.uint8"
+    elif bad == "workspace_view":
+        ws = torch.zeros(2, 1 << 16, dtype=torch.uint8)[:, ::2].reshape(-1)[::2]
+    elif bad == "out_float32":
+        kw_f["out"], match = torch.zeros(1, 4, 128, 64), "out must be torch.bfloat16"
+    else:
+        kw_b["dq"] = torch.zeros(1, 1, 128, 64, dtype=torch.bfloat16).expand(1, 4, 128, 64)
+    mask = _Mask(q_len=128, kv_len=128)
+    if bad != "dq_expand":
+        with pytest.raises(ValueError, match=match):
+            B.fa_forward_prepare_backward(q, k, v, mask, ws, **kw_f)
+    if bad != "out_float32":
+        with pytest.raises(ValueError, match=match):
+            B.fa_backward_prepared(q, k, v, out, lse, dout, mask, ws, **kw_b)
