@@ -91,3 +91,60 @@ def test_prepared_pair_twice_in_a_row():
         assert torch.equal(ref[1], got[1]) and torch.equal(ref[2], got[2])
         r, g = ref[0].float(), got[0].float()
         assert (r - g).abs().max() <= 1e-2 * r.abs().max()
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_prepared_pair_block64_forward_tiles(D):
+    """A block-64 mask: the forward walks 128 x 64 key tiles (its BK = 64
+    kernels, which carry the same clearing stream) and the backward 128 x 128.
+    Accumulator cleared, outputs equal to fa_forward's, gradients equal to
+    fa_backward's."""
+    B, H, S = 1, 3, 1000
+    docs = make_doc_ids(("geometric", 60.0), S, 41 + D)
+    q, k, v, do = (t.cuda() for t in make_qkv(B, H, S, D, 42 + D))
+    bm = fa.fa_create_block_mask(device_nodes(MaskProgram((("causal",), ("same_doc",), ("and",))), docs), 1, 1,
+                                 S, S, 64)
+    ws = torch.full((fa.fa_backward_workspace_bytes(B, H, S, D),), 0xFF, dtype=torch.uint8, device="cuda")
+    out_p, lse_p = fa.fa_forward_prepare_backward(q, k, v, bm, ws)
+    torch.cuda.synchronize()
+    assert int(torch.count_nonzero(ws[: B * H * S * D * 4])) == 0
+    out, lse = fa.fa_forward(q, k, v, bm)
+    assert torch.equal(out, out_p) and torch.equal(lse, lse_p)
+    g_ref = fa.fa_backward(q, k, v, out, lse, do, bm)
+    g_pre = fa.fa_backward_prepared(q, k, v, out, lse, do, bm, ws)
+    torch.cuda.synchronize()
+    assert fa.fa_get_status(bm) == 0
+    assert torch.equal(g_ref[1], g_pre[1]) and torch.equal(g_ref[2], g_pre[2])
+    r, g = g_ref[0].float(), g_pre[0].float()
+    assert r.abs().max() > 0 and (r - g).abs().max() <= 1e-2 * r.abs().max()
+
+
+@pytest.mark.parametrize("kind", ["alibi", "relbias"])
+def test_prepared_pair_with_score_parameter_gradient(kind):
+    """The learned ALiBi slopes' and bias table's gradients through
+    fa_backward_prepared (its preprocessing kernel still zeroes the gradient
+    buffer, NaN beforehand) match fa_backward's."""
+    B, H, S, D = 2, 2, 900, 128
+    docs = make_doc_ids(("geometric", 200.0), S, 61, batch=B)
+    q, k, v, do = (t.cuda() for t in make_qkv(B, H, S, D, 62))
+    mask = MaskProgram((("causal",), ("same_doc",), ("and",), ("window", 400), ("and",)))
+    bm = fa.fa_create_block_mask(device_nodes(mask, docs), B, 1, S, S, 128)
+    if kind == "alibi":
+        score = ("alibi", torch.as_tensor(make_alibi_slopes(H)))
+        shape = (H,)
+    else:
+        rng = np.random.default_rng(63)
+        score = ("relbias", torch.as_tensor(rng.normal(scale=0.5, size=(H, 250)).astype(np.float32)), 3)
+        shape = (H, 250)
+    ws = torch.empty(fa.fa_backward_workspace_bytes(B, H, S, D), dtype=torch.uint8, device="cuda")
+    out, lse = fa.fa_forward_prepare_backward(q, k, v, bm, ws, score=score)
+    g_pre = torch.full(shape, float("nan"), device="cuda")
+    grads = fa.fa_backward_prepared(q, k, v, out, lse, do, bm, ws, score=score, score_param_grad=g_pre)
+    g_ref = torch.full(shape, float("nan"), device="cuda")
+    ref = fa.fa_backward(q, k, v, out, lse, do, bm, score=score, score_param_grad=g_ref)
+    torch.cuda.synchronize()
+    assert fa.fa_get_status(bm) == 0
+    assert torch.equal(grads[1], ref[1]) and torch.equal(grads[2], ref[2])
+    a, b = g_pre.double(), g_ref.double()
+    assert torch.isfinite(a).all() and b.abs().max() > 0
+    assert (a - b).abs().max() <= 1e-3 * b.abs().max()
